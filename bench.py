@@ -1,0 +1,465 @@
+"""Benchmark of the Compressed PagedAttention hot path on one or more GPUs.
+
+Workload (default): one Qwen3-8B-shaped attention layer -- 32 query heads, 8
+kv heads, head_dim 128, bf16, block size 16, budget 8 blocks (128 tokens, 112
+kept) -- with 64 sequences whose contexts are uniform in [1024, 4096] tokens,
+K/V/Q ~ N(0, 1), physical blocks scattered by a seeded permutation.
+
+One step = the whole hot path over that batch:
+  1. zp_append_kv          the new token's key/value of every sequence;
+  2. zp_paged_decode_attn  decode attention of all 64 sequences fused with the
+                           window-score accumulation (w = b = 16, so every
+                           decode step is an observation-window step);
+  3. compression of the sequences whose trigger holds at their length
+     (L % b == 0, L >= N_max * b): host planner, zp_score_tokens (global
+     score, first-compression pooling, lightning redundancy, eq. 4, window),
+     zp_select_topk, zp_compact_pages into the planned target blocks.
+The batch is stationary: lengths and tables are not advanced between steps,
+so every timed step does identical work (the compaction rewrites the same
+target slots each time).
+
+The JSON line reports seq-steps/s for the whole job (sequences x steps / max
+over ranks of the timed region), the roofline of the dominant call (the fused
+decode attention), the oracle's CPU throughput on a bounded sample, and an
+end-to-end figure measured with pinned host buffers and the host<->device
+copies inside the timed region.  Inputs (~1.4 GB of K/V per layer) are larger
+than the 129 MB L2, so no flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import zp_inputs  # noqa: E402
+
+METRIC = "decode seq-steps/s and achieved HBM GB/s (fraction of ~8 TB/s) incl. compression"
+
+WORKLOADS = {
+    # name: (B, h_q, h_kv, d, b, N_max, (lo, hi), dtype, seed)
+    "qwen3_8b_layer_64seq_ctx1k-4k": (64, 32, 8, 128, 16, 8, (1024, 4096), "bf16", 1002),
+    # small case of the same kernels, for ncu captures (a few hundred MB)
+    "qwen3_8b_layer_16seq_ctx1k-4k": (16, 32, 8, 128, 16, 8, (1024, 4096), "bf16", 1012),
+}
+DEFAULT_WORKLOAD = "qwen3_8b_layer_64seq_ctx1k-4k"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+class Workload:
+    """Device buffers and the step of the decode + compression hot path."""
+
+    def __init__(self, name: str, seed_offset: int, dev: torch.device):
+        import compressed_paged_kv_zp_gb300 as zp
+        self.zp = zp
+        B, h_q, h_kv, d, b, N_max, lr, dtype, seed = WORKLOADS[name]
+        self.name, self.B, self.h_q, self.h_kv, self.d, self.b, self.N_max = name, B, h_q, h_kv, d, b, N_max
+        self.dtype = dtype
+        self.w = b
+        self.k = (N_max - 1) * b
+        c = zp_inputs.make_paged_case(seed + seed_offset, B, h_q, h_kv, d, b, len_range=lr, dtype=dtype,
+                                      spare_blocks=B * N_max)
+        self.case = c
+        tdt = zp_inputs.DTYPES[dtype]
+        self.desc = zp.cache_desc(h_q, h_kv, d, b, c.n_total, tdt)
+        self.K = c.k_cache[0].contiguous().to(dev)
+        self.V = c.v_cache[0].contiguous().to(dev)
+        self.q = c.q.to(dev)
+        self.table = c.block_table.to(dev)
+        self.lens = c.seq_lens.to(dev)
+        self.out = torch.empty_like(self.q)
+        self.S = torch.zeros(c.n_total, b, h_kv, dtype=torch.float32, device=dev)
+        self.F = torch.zeros_like(self.S)
+        g = torch.Generator().manual_seed(seed + seed_offset + 7)
+        self.k_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
+        self.v_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
+        self.ws = torch.empty(zp.zp_decode_workspace_size(self.desc, B, c.table_stride),
+                              dtype=torch.uint8, device=dev)
+        # compression set: sequences whose trigger holds at their length
+        lens = c.seq_lens.tolist()
+        self.comp = [s for s in range(B) if zp.zp_needs_compression(lens[s], b, N_max)]
+        self.pool = zp.Pool(c.n_total)
+        self.pool.alloc(c.n_total)
+        held = set(int(x) for x in c.block_table.flatten().tolist() if x >= 0)
+        self.pool.release([i for i in range(c.n_total) if i not in held])
+        n = len(self.comp)
+        self.n_comp = n
+        if n:
+            idx = torch.tensor(self.comp, dtype=torch.long)
+            self.c_table = c.block_table[idx].contiguous().to(dev)
+            self.c_lens = c.seq_lens[idx].contiguous().to(dev)
+            self.c_Lmax = int(c.seq_lens[idx].max())
+            self.c_first = torch.ones(n, dtype=torch.uint8, device=dev)
+            self.c_scores = torch.empty(n, h_kv, self.c_Lmax, dtype=torch.float32, device=dev)
+            self.c_keep = torch.empty(n, h_kv, self.k, dtype=torch.int32, device=dev)
+            self.c_ws = torch.empty(max(zp.zp_score_workspace_size(self.desc, n, self.c_Lmax), 1),
+                                    dtype=torch.uint8, device=dev)
+            self.params = zp.score_params(window=self.w)
+            self.c_targets = torch.tensor([self._plan(s)["targets"] for s in self.comp], dtype=torch.int32,
+                                          device=dev)
+        # pinned host copies for the end-to-end figure
+        self.host_q = self.q.cpu().pin_memory()
+        self.h_k_new = self.k_new.cpu().pin_memory()
+        self.h_v_new = self.v_new.cpu().pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h_keep = (torch.empty(self.c_keep.shape, dtype=torch.int32).pin_memory() if n else None)
+
+    def _plan(self, s):
+        b, N_max = self.b, self.N_max
+        L = int(self.case.seq_lens[s])
+        return self.pool.plan_compaction(self.case.block_table[s, :L // b].tolist(), N_max)
+
+    # ---- algorithmic bytes (per the roofline definition in the design doc)
+    def decode_bytes(self) -> int:
+        es = 2 if self.dtype == "bf16" else 4
+        tot = 0
+        for L in self.case.seq_lens.tolist():
+            tot += 2 * L * self.h_kv * self.d * es + 2 * self.h_q * self.d * es
+            r = (L - 1) % self.b
+            if r >= self.b - self.w:
+                tot += (4 if r == self.b - self.w else 8) * L * self.h_kv
+        return tot
+
+    def compress_bytes(self) -> int:
+        es = 2 if self.dtype == "bf16" else 4
+        tot = 0
+        for s in self.comp:
+            L = int(self.case.seq_lens[s])
+            tot += 4 * L * self.h_kv + 8 * L * self.h_kv + L * self.h_kv * self.d * es  # S, F r/w, K
+            tot += 4 * L * self.h_kv + 4 * self.k * self.h_kv                        # top-k
+            tot += 2 * 2 * self.k * self.h_kv * self.d * es + 8 * self.k * self.h_kv  # move K, V, F
+        return tot
+
+    def launches_per_step(self) -> int:
+        return 1 + 2 + (5 if self.n_comp else 0)  # append; decode main + score; score x3, top-k, compact
+
+    # ---- the step
+    def decode(self, stream=None):
+        zp = self.zp
+        zp.zp_append_kv(self.desc, self.k_new, self.v_new, self.K, self.V, self.table, self.lens, stream)
+        zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens, self.out,
+                                score_accum=self.S, window=self.w, workspace=self.ws, stream=stream)
+
+    def compress(self, stream=None):
+        if not self.n_comp:
+            return
+        zp = self.zp
+        for s in self.comp:  # host planning (a11); identical plans each step
+            self._plan(s)
+        zp.zp_score_tokens(self.desc, self.params, self.K, self.c_table, self.c_lens, self.c_first, self.S,
+                           self.F, self.c_scores, workspace=self.c_ws, stream=stream)
+        zp.zp_select_topk(self.c_scores, self.c_lens, self.k, self.c_keep, stream=stream)
+        zp.zp_compact_pages(self.desc, self.K, self.V, 0, 1, self.F, 0, self.c_table, self.c_targets,
+                            self.c_lens, self.c_keep, self.k, stream=stream)
+
+    def step(self):
+        self.decode()
+        self.compress()
+
+    def step_e2e(self):
+        """Same step through the public calls with host buffers: H2D of q and
+        the new k/v from pinned memory, D2H of the outputs and keep sets."""
+        self.q.copy_(self.host_q, non_blocking=True)
+        self.k_new.copy_(self.h_k_new, non_blocking=True)
+        self.v_new.copy_(self.h_v_new, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+        if self.n_comp:
+            self.h_keep.copy_(self.c_keep, non_blocking=True)
+
+    def e2e_bytes(self):
+        bi = sum(t.numel() * t.element_size() for t in (self.host_q, self.h_k_new, self.h_v_new))
+        bo = self.h_out.numel() * self.h_out.element_size()
+        if self.n_comp:
+            bo += self.h_keep.numel() * 4
+        return bi, bo
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _max_over_ranks(dist, x: float, dev) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of one step of the workload: decode
+    (with the window-score accumulation) of n_seqs sequences and the
+    compression (scores, top-k, Alg. 4 moves) of n_comp triggered sequences --
+    about the workload's ratio of 7 compressions per 64 decodes."""
+
+    def __init__(self, wl_name: str, n_seqs: int = 16, n_comp: int = 2, seed_offset: int = 0):
+        import oracle
+        from oracle import pipeline
+        self.oracle, self.pipeline = oracle, pipeline
+        B, h_q, h_kv, d, b, N_max, lr, dtype, seed = WORKLOADS[wl_name]
+        self.geom = (h_kv, d, b, N_max)
+        c = zp_inputs.make_paged_case(seed + seed_offset, B, h_q, h_kv, d, b, len_range=lr, dtype=dtype)
+        self.c = c
+        self.K = c.k_cache[0].float().numpy()
+        self.V = c.v_cache[0].float().numpy()
+        self.Kraw = c.k_cache.view(torch.int16).numpy()  # shares memory: moved in place
+        self.Vraw = c.v_cache.view(torch.int16).numpy()
+        self.q = c.q.float().numpy()
+        self.lens = c.seq_lens.numpy()
+        self.table = c.block_table.numpy()
+        trig = [s for s in range(B) if oracle.needs_compression(int(self.lens[s]), b, N_max)][:n_comp]
+        rest = [s for s in range(B) if s not in trig]
+        self.trig = trig
+        self.seqs = trig + rest[: max(n_seqs - len(trig), 0)]
+
+    def step(self) -> float:
+        oracle, pipeline = self.oracle, self.pipeline
+        h_kv, d, b, N_max = self.geom
+        seqs, lens, table = self.seqs, self.lens, self.table
+        S = np.zeros((self.c.n_total, b, h_kv))
+        t0 = time.perf_counter()
+        out, probs = oracle.decode_attention(self.q[seqs], self.K, self.V, table[seqs], lens[seqs],
+                                             want_probs=True)
+        oracle.accumulate_window_score(probs, table[seqs], lens[seqs], h_kv, b, b, S)
+        prm = pipeline.ScoreParams(window=b)
+        F = np.zeros((self.c.n_total, b, h_kv))
+        for s in self.trig:
+            L = int(lens[s])
+            sc = pipeline.final_scores(pipeline.gather_slots(S, table[s], L, b), self.K, F, table[s], L, b,
+                                       True, prm)
+            keep = pipeline.keep_sets(sc, (N_max - 1) * b)
+            pipeline.compact_sequence([self.Kraw, self.Vraw], [d * 2, d * 2], b, h_kv, table[s], L // b,
+                                      table[s][:N_max - 1], keep[None], L)
+        return time.perf_counter() - t0
+
+
+def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the host cores."""
+    dist, rank, world = _dist()
+    if rank != 0:
+        return 0
+    wl = args.workload
+    sample = OracleSample(wl)
+    n_sample = len(sample.seqs)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = sample.step()
+        if i >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = n_sample * len(times) / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "seq-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl, "sample": "%d of %d sequences per step" % (
+            n_sample, WORKLOADS[wl][0])},
+        "cpu_baseline": {"value": value, "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                         "sample": "decode + window score of %d sequences and the compression of two "
+                                   "triggered sequences, per step" % n_sample},
+        "e2e": {"value": value, "unit": "seq-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="zp", choices=["zp", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "zp":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = Workload(args.workload, seed_offset=rank, dev=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    zp = wl.zp
+    code, _ = zp.zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d after warm-up" % code)
+
+    # ---- timed region: K steps, events around the fused decode call
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    _barrier(dist)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        zp.zp_append_kv(wl.desc, wl.k_new, wl.v_new, wl.K, wl.V, wl.table, wl.lens)
+        ev_dec[i][0].record(stream)
+        zp.zp_paged_decode_attn(wl.desc, wl.q, wl.K, wl.V, wl.table, wl.lens, wl.out, score_accum=wl.S,
+                                window=wl.w, workspace=wl.ws)
+        ev_dec[i][1].record(stream)
+        wl.compress()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    code, _ = zp.zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d in the timed region" % code)
+    elapsed_ms = _max_over_ranks(dist, elapsed_ms, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = wl.B * args.steps * world / (elapsed_ms / 1e3)
+
+    # compression of all 64 sequences (lengths rounded down to a block), once, timed alone
+    # ---- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            wl.step_e2e()
+        torch.cuda.synchronize()
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(dist)
+        s2.record(stream)
+        for _ in range(args.steps):
+            wl.step_e2e()
+        t2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = _max_over_ranks(dist, s2.elapsed_time(t2), dev)
+        bi, bo = wl.e2e_bytes()
+        e2e = {"value": wl.B * args.steps * world / (e2e_ms / 1e3), "unit": "seq-steps/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    peak, peak_kind = _peaks()
+    dbytes = wl.decode_bytes()
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    achieved = dbytes / (dec_avg / 1e3) / 1e9
+    step_bytes = dbytes + wl.compress_bytes()
+    line = {
+        "metric": METRIC, "value": value, "unit": "seq-steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "seqs": wl.B, "heads": "32q/8kv", "head_dim": wl.d,
+                   "block": wl.b, "max_blocks_per_seq": wl.N_max, "kept_tokens": wl.k, "window": wl.w,
+                   "ctx": "uniform 1024-4096", "compressed_per_step": wl.n_comp,
+                   "l2": "inputs larger than L2 (K+V %.0f MB)" % (2 * wl.K.numel() * wl.K.element_size() / 1e6),
+                   "peak_kind": peak_kind},
+        "roofline": {"kernel": "zp_paged_decode_attn (decode_main + score epilogue)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_8tbs": achieved / 8000.0, "traffic": None,
+                     "algorithmic_bytes": dbytes, "avg_ms": dec_avg},
+        "step_hbm_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
+        "decode_ms_per_step": dec_avg,
+        "clocks": clk,
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(args.workload)
+        n = len(sample.seqs)
+        dt = sample.step()
+        line["cpu_baseline"] = {"value": n / dt, "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                                "sample": "decode + window score of %d of %d sequences and the "
+                                          "compression of two triggered sequences (one step)" % (n, wl.B)}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

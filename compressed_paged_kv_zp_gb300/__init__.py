@@ -1,0 +1,265 @@
+"""Python binding of libzp, the Compressed PagedAttention hot path for GB300.
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers and sizes to the C ABI declared in ``include/zp.h`` and raises
+``ZPError`` on a non-OK status.  All arithmetic runs in the CUDA kernels of
+libzp.so; there is no CPU fallback.  The library must have been built (see
+``compressed_paged_kv_zp_gb300/_build.py`` or ``__graft_entry__.build()``):
+importing this package without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzp.so")
+
+ZP_BF16 = 0
+ZP_F32 = 1
+_DTYPES = {torch.bfloat16: ZP_BF16, torch.float32: ZP_F32}
+
+STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTYPE",
+          4: "ZP_ERR_CAPACITY", 5: "ZP_ERR_CUDA", 6: "ZP_ERR_TIMEOUT", 7: "ZP_ERR_DEVICE"}
+
+# every symbol include/zp.h declares
+EXPORTS = [
+    "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
+    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_append_kv", "zp_needs_compression",
+    "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
+    "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
+    "zp_pool_incref", "zp_pool_release", "zp_plan_compaction",
+]
+
+
+class ZPError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), msg))
+        self.status = status
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("n_total_blocks", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class ScoreParams(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("use_global", ctypes.c_int32), ("alpha", ctypes.c_float),
+                ("pool_kernel", ctypes.c_int32), ("pool_policy", ctypes.c_int32),
+                ("use_similarity", ctypes.c_int32), ("lightning", ctypes.c_int32),
+                ("threshold", ctypes.c_float), ("lambda_", ctypes.c_float), ("tau", ctypes.c_float)]
+
+
+def score_params(window=16, use_global=True, alpha=0.8, pool_kernel=7, pool_policy=1,
+                 use_similarity=True, lightning=True, threshold=0.9, lam=0.2, tau=0.4) -> ScoreParams:
+    return ScoreParams(int(window), int(bool(use_global)), float(alpha), int(pool_kernel),
+                       int(pool_policy), int(bool(use_similarity)), int(bool(lightning)),
+                       float(threshold), float(lam), float(tau))
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libzp.so is not built (expected at %s); run "
+                          "compressed_paged_kv_zp_gb300._build.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(CacheDesc)
+    lib.zp_last_error.restype = ctypes.c_char_p
+    lib.zp_status_string.restype = ctypes.c_char_p
+    lib.zp_status_string.argtypes = [ctypes.c_int]
+    lib.zp_device_status.argtypes = [P, P, I32]
+    lib.zp_decode_workspace_size.restype = SZ
+    lib.zp_decode_workspace_size.argtypes = [D, I32, I32]
+    lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, I32, P, SZ, P]
+    lib.zp_append_kv.argtypes = [D, P, P, P, P, P, I32, P, I32, P]
+    lib.zp_needs_compression.argtypes = [I32, I32, I32]
+    lib.zp_score_workspace_size.restype = SZ
+    lib.zp_score_workspace_size.argtypes = [D, I32, I32]
+    lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P,
+                                    I32, P, SZ, P]
+    lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
+    lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, I32, P, I32, P, P, I32, I32, P]
+    lib.zp_pool_create.restype = P
+    lib.zp_pool_create.argtypes = [I32]
+    lib.zp_pool_destroy.argtypes = [P]
+    lib.zp_pool_num_free.argtypes = [P]
+    lib.zp_pool_refcount.argtypes = [P, I32]
+    lib.zp_pool_alloc.argtypes = [P, I32, P]
+    lib.zp_pool_incref.argtypes = [P, I32, P]
+    lib.zp_pool_release.argtypes = [P, I32, P]
+    lib.zp_plan_compaction.argtypes = [P, P, I32, I32, P, P, P, P, P]
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise ZPError(status, lib.zp_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libzp must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: Optional[torch.Tensor], name: str):
+    if t is not None and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return _ptr(t)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def cache_desc(h_q, h_kv, head_dim, block_size, n_total_blocks, dtype) -> CacheDesc:
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return CacheDesc(int(h_q), int(h_kv), int(head_dim), int(block_size), int(n_total_blocks), code)
+
+
+# ----------------------------------------------------------------------------- decode
+def zp_decode_workspace_size(desc: CacheDesc, B: int, table_stride: int) -> int:
+    n = lib.zp_decode_workspace_size(ctypes.byref(desc), int(B), int(table_stride))
+    if n == 0 and B > 0:
+        raise ZPError(2, lib.zp_last_error().decode() or "unsupported decode shape")
+    return int(n)
+
+
+def zp_paged_decode_attn(desc, q, k_cache, v_cache, block_table, seq_lens, out, score_accum=None,
+                         window=0, workspace=None, stream=None) -> None:
+    B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    if workspace is None:
+        workspace = torch.empty(zp_decode_workspace_size(desc, B, table_stride), dtype=torch.uint8,
+                                device=q.device)
+    _check(lib.zp_paged_decode_attn(ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"),
+                                    _dev(v_cache, "v_cache"), _dev(block_table, "block_table"),
+                                    table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
+                                    _dev(score_accum, "score_accum"), int(window),
+                                    _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def zp_append_kv(desc, k_new, v_new, k_cache, v_cache, block_table, seq_lens, stream=None) -> None:
+    B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    _check(lib.zp_append_kv(ctypes.byref(desc), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                            _dev(block_table, "block_table"), table_stride, _dev(seq_lens, "seq_lens"),
+                            B, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- compression
+def zp_needs_compression(seq_len: int, block_size: int, max_blocks: int) -> bool:
+    return bool(lib.zp_needs_compression(int(seq_len), int(block_size), int(max_blocks)))
+
+
+def zp_score_workspace_size(desc: CacheDesc, n: int, Lmax: int) -> int:
+    return int(lib.zp_score_workspace_size(ctypes.byref(desc), int(n), int(Lmax)))
+
+
+def zp_score_tokens(desc, params: ScoreParams, k_cache, block_table, seq_lens, first_compression,
+                    score_accum, global_F, scores_out, workspace=None, stream=None) -> None:
+    n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    Lmax = int(scores_out.shape[-1])
+    if workspace is None:
+        workspace = torch.empty(max(zp_score_workspace_size(desc, n, Lmax), 1), dtype=torch.uint8,
+                                device=scores_out.device)
+    _check(lib.zp_score_tokens(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
+                               _dev(block_table, "block_table"), table_stride,
+                               _dev(seq_lens, "seq_lens"), _dev(first_compression, "first_compression"),
+                               n, _dev(score_accum, "score_accum"), _dev(global_F, "global_F"),
+                               _dev(scores_out, "scores_out"), Lmax, _dev(workspace, "workspace"),
+                               workspace.numel(), _stream(stream)))
+
+
+def zp_select_topk(scores, seq_lens, k, keep_idx, tie_count=None, stream=None) -> None:
+    n, h_kv, Lmax = (int(x) for x in scores.shape)
+    _check(lib.zp_select_topk(_dev(scores, "scores"), h_kv, Lmax, _dev(seq_lens, "seq_lens"), n,
+                              int(k), _dev(keep_idx, "keep_idx"), _dev(tie_count, "tie_count"),
+                              _stream(stream)))
+
+
+def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, F_layer_stride,
+                     src_table, dst_targets, seq_lens, keep_idx, k, stream=None) -> None:
+    n, table_stride = int(src_table.shape[0]), int(src_table.shape[1])
+    _check(lib.zp_compact_pages(ctypes.byref(desc), _dev(k_base, "k_base"), _dev(v_base, "v_base"),
+                                int(layer_stride), int(layer_count), _dev(global_F, "global_F"),
+                                int(F_layer_stride), _dev(src_table, "src_table"), table_stride,
+                                _dev(dst_targets, "dst_targets"), int(dst_targets.shape[1]),
+                                _dev(seq_lens, "seq_lens"), _dev(keep_idx, "keep_idx"), int(k), n,
+                                _stream(stream)))
+
+
+def zp_device_status(clear: bool = True):
+    code, detail = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.zp_device_status(ctypes.byref(code), ctypes.byref(detail), int(bool(clear))))
+    return code.value, detail.value
+
+
+# ----------------------------------------------------------------------------- host pool
+def _i32buf(n):
+    return (ctypes.c_int32 * max(int(n), 1))()
+
+
+class Pool:
+    """Host block pool (zp_pool_*): reference counts and the free list."""
+
+    def __init__(self, n_total: int):
+        self._p = lib.zp_pool_create(int(n_total))
+        if not self._p:
+            raise ZPError(1, lib.zp_last_error().decode())
+        self.n_total = int(n_total)
+
+    def __del__(self):
+        p = getattr(self, "_p", None)
+        if p:
+            lib.zp_pool_destroy(p)
+            self._p = None
+
+    @property
+    def num_free(self) -> int:
+        return int(lib.zp_pool_num_free(self._p))
+
+    def refcount(self, block: int) -> int:
+        return int(lib.zp_pool_refcount(self._p, int(block)))
+
+    def alloc(self, n: int):
+        buf = _i32buf(n)
+        _check(lib.zp_pool_alloc(self._p, int(n), buf))
+        return list(buf)[: int(n)]
+
+    def incref(self, ids):
+        ids = list(ids)
+        buf = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(lib.zp_pool_incref(self._p, len(ids), buf))
+
+    def release(self, ids):
+        ids = list(ids)
+        buf = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(lib.zp_pool_release(self._p, len(ids), buf))
+
+    def plan_compaction(self, table, max_blocks: int):
+        table = [int(x) for x in table]
+        tb = (ctypes.c_int32 * max(len(table), 1))(*table)
+        targets, new_table = _i32buf(max_blocks - 1), _i32buf(max_blocks)
+        dropped = _i32buf(len(table))
+        nd, nf = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(lib.zp_plan_compaction(self._p, tb, len(table), int(max_blocks), targets, new_table,
+                                      dropped, ctypes.byref(nd), ctypes.byref(nf)))
+        return {"targets": list(targets)[: max_blocks - 1], "new_table": list(new_table)[:max_blocks],
+                "dropped": list(dropped)[: nd.value], "n_fresh": nf.value}
+
+
+__all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "score_params",
+           "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_append_kv",
+           "zp_needs_compression", "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
+           "zp_compact_pages", "zp_device_status", "Pool", "ZP_BF16", "ZP_F32"]

@@ -1,0 +1,171 @@
+// compact.cu -- gather-compaction of the kept rows into the target blocks.
+//
+// Zipage paper App. C.6, Alg. 4: the kept entries of a sequence are packed, in
+// their original order, into the first N_max - 1 blocks (or the target blocks
+// of §4.4 when prefix blocks are shared); the global score cache F moves the
+// same way ("compress score").  Rank r of the keep list goes to slot r % b of
+// target block r / b.
+//
+// One CTA per (kv head, sequence, layer).  Alg. 4 walks one slot at a time;
+// here a CTA moves a chunk of kChunk ranks at once: every thread first loads
+// its share of the chunk's source rows (16-byte vectors) into registers, the
+// CTA synchronises, then the rows are stored.  Rank r's source position is
+// >= r, so a chunk's stores (positions < chunk end) never overwrite a source
+// of a later chunk, and the barrier orders the loads of the chunk before its
+// own stores: the move is correct in place as well as into fresh blocks.
+#include "zp_common.cuh"
+
+namespace zp {
+namespace {
+
+constexpr int kChunk = 32;
+constexpr int kThreads = 256;
+constexpr int kMaxVecPerThread = 8;  // kChunk * row_vec * 2 / kThreads
+
+struct CompactArgs {
+    uint4 *K;
+    uint4 *V;
+    long long layer_stride_vec;  // in 16-byte vectors
+    float *F;
+    long long F_layer_stride;
+    const int32_t *src_table;
+    int table_stride;
+    const int32_t *dst;
+    int target_stride;
+    const int32_t *seq_lens;
+    const int32_t *keep;
+    int k, n, h_kv, b, n_total;
+    int row_vec;  // vectors per (token, kv head) row = d * elem / 16
+    unsigned *err;
+};
+
+__global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) {
+    const int kvh = blockIdx.x;
+    const int s = blockIdx.y;
+    const int layer = blockIdx.z;
+    int L = a.seq_lens[s];
+    if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    const int kk = min(a.k, L);
+    const int32_t *kp = a.keep + (((size_t)layer * a.n + s) * a.h_kv + kvh) * a.k;
+    uint4 *K = a.K + layer * a.layer_stride_vec;
+    uint4 *V = a.V + layer * a.layer_stride_vec;
+    float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
+    const int per_rank = 2 * a.row_vec;  // K then V vectors
+    for (int r0 = 0; r0 < kk; r0 += kChunk) {
+        const int nr = min(kChunk, kk - r0);
+        const int items = nr * per_rank;
+        uint4 buf[kMaxVecPerThread];
+        float fbuf = 0.f;
+        // ---- load phase
+#pragma unroll
+        for (int i = 0; i < kMaxVecPerThread; ++i) {
+            const int it = threadIdx.x + i * kThreads;
+            if (it < items) {
+                const int r = r0 + it / per_rank;
+                const int v = it % per_rank;
+                const int pos = kp[r];
+                int blk = -1;
+                if (pos >= 0 && pos < L) blk = a.src_table[(size_t)s * a.table_stride + pos / a.b];
+                if (blk < 0 || blk >= a.n_total) {
+                    record_error(a.err, ZP_ERR_DEVICE, 0x400);
+                    buf[i] = make_uint4(0, 0, 0, 0);
+                } else {
+                    const size_t row = ((size_t)blk * a.b + pos % a.b) * a.h_kv + kvh;
+                    const uint4 *base = v < a.row_vec ? K : V;
+                    buf[i] = base[row * a.row_vec + (v % a.row_vec)];
+                }
+            }
+        }
+        if (F && threadIdx.x < nr) {
+            const int pos = kp[r0 + threadIdx.x];
+            if (pos >= 0 && pos < L) {
+                const int blk = a.src_table[(size_t)s * a.table_stride + pos / a.b];
+                if (blk >= 0 && blk < a.n_total) fbuf = F[((size_t)blk * a.b + pos % a.b) * a.h_kv + kvh];
+            }
+        }
+        __syncthreads();
+        // ---- store phase
+#pragma unroll
+        for (int i = 0; i < kMaxVecPerThread; ++i) {
+            const int it = threadIdx.x + i * kThreads;
+            if (it < items) {
+                const int r = r0 + it / per_rank;
+                const int v = it % per_rank;
+                const int blk = a.dst[(size_t)s * a.target_stride + r / a.b];
+                if (blk < 0 || blk >= a.n_total) {
+                    record_error(a.err, ZP_ERR_DEVICE, 0x401);
+                } else {
+                    const size_t row = ((size_t)blk * a.b + r % a.b) * a.h_kv + kvh;
+                    uint4 *base = v < a.row_vec ? K : V;
+                    base[row * a.row_vec + (v % a.row_vec)] = buf[i];
+                }
+            }
+        }
+        if (F && threadIdx.x < nr) {
+            const int r = r0 + threadIdx.x;
+            const int blk = a.dst[(size_t)s * a.target_stride + r / a.b];
+            if (blk >= 0 && blk < a.n_total) F[((size_t)blk * a.b + r % a.b) * a.h_kv + kvh] = fbuf;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+}  // namespace zp
+
+using namespace zp;
+
+extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
+                                      int64_t layer_stride, int32_t layer_count, float *global_F,
+                                      int64_t F_layer_stride, const int32_t *src_table,
+                                      int32_t table_stride, const int32_t *dst_targets,
+                                      int32_t target_stride, const int32_t *seq_lens,
+                                      const int32_t *keep_idx, int32_t k, int32_t n, void *stream) {
+    zp_status rc = check_desc(D);
+    if (rc != ZP_OK) return rc;
+    if (n < 0 || k < 0 || layer_count < 0 || table_stride < 1 || target_stride < 1)
+        return fail(ZP_ERR_INVALID_ARG, "compact: bad sizes");
+    if (n == 0 || k == 0 || layer_count == 0) return ok();
+    if (!k_base || !v_base || !src_table || !dst_targets || !seq_lens || !keep_idx)
+        return fail(ZP_ERR_INVALID_ARG, "compact: NULL buffer");
+    if ((long long)target_stride * D->block_size < k)
+        return fail(ZP_ERR_CAPACITY, "compact: %d target blocks hold fewer than k=%d rows", target_stride, k);
+    const int es = elem_bytes(D->dtype);
+    const size_t row_bytes = (size_t)D->head_dim * es;
+    if (row_bytes % 16) return fail(ZP_ERR_SHAPE, "compact: row of %zu bytes", row_bytes);
+    const long long elems_per_layer = (long long)D->n_total_blocks * D->block_size * D->h_kv * D->head_dim;
+    if (layer_count > 1 && layer_stride < elems_per_layer)
+        return fail(ZP_ERR_INVALID_ARG, "compact: layer_stride %lld < one layer", (long long)layer_stride);
+    if ((layer_stride * es) % 16) return fail(ZP_ERR_INVALID_ARG, "compact: layer_stride not 16-byte aligned");
+    if (((uintptr_t)k_base | (uintptr_t)v_base) % 16) return fail(ZP_ERR_INVALID_ARG, "compact: unaligned cache");
+    const int row_vec = (int)(row_bytes / 16);
+    if (kChunk * 2 * row_vec > kThreads * kMaxVecPerThread)
+        return fail(ZP_ERR_SHAPE, "compact: head_dim %d too large", D->head_dim);
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != ZP_OK) return rc;
+    CompactArgs a;
+    a.K = static_cast<uint4 *>(k_base);
+    a.V = static_cast<uint4 *>(v_base);
+    a.layer_stride_vec = layer_stride * es / 16;
+    a.F = global_F;
+    a.F_layer_stride = F_layer_stride;
+    a.src_table = src_table;
+    a.table_stride = table_stride;
+    a.dst = dst_targets;
+    a.target_stride = target_stride;
+    a.seq_lens = seq_lens;
+    a.keep = keep_idx;
+    a.k = k;
+    a.n = n;
+    a.h_kv = D->h_kv;
+    a.b = D->block_size;
+    a.n_total = D->n_total_blocks;
+    a.row_vec = row_vec;
+    a.err = dev.error_word;
+    dim3 grid(D->h_kv, n, layer_count);
+    compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "compact: launch");
+    return ok();
+}

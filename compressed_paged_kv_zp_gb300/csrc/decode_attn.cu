@@ -1,0 +1,856 @@
+// decode_attn.cu -- paged GQA decode attention fused with the window score.
+//
+// Computes, for every sequence s and query head h (Zipage paper §3 paged
+// cache, §6 decode attention on it):
+//     out[s][h] = sum_{t<L_s} softmax_t(q[s][h] . k_t / sqrt(d)) v_t
+// and, on observation-window steps, the per-token window score of App. C.2
+// accumulated one decode step at a time (see zp_paged_decode_attn in zp.h).
+//
+// Design (HBM bound: ~4 flop per byte of K/V at a group of 4):
+//   * Work unit = up to T tokens of one block of one sequence, all kv heads:
+//     in the [N_total][b][h_kv][d] layout these are T*h_kv*d contiguous
+//     elements, fetched with ONE 1-D bulk copy (TMA engine) per tensor into a
+//     shared-memory ring of S stages guarded by mbarriers.  K/V loads carry
+//     an L2 evict-first hint so the small scratch arrays stay resident.
+//   * Stream-K split: the units of all sequences are concatenated and every
+//     CTA (one per SM, persistent) takes an equal contiguous range, so ragged
+//     lengths cannot unbalance the grid.  A sequence cut between CTAs leaves
+//     per-CTA partial (max, sum, accumulator) records; the CTA that finishes
+//     the sequence's last partial merges them (atomic arrival count, no wait).
+//   * Warp specialisation: one producer warp issues the copies; consumer warp
+//     w handles kv head w / WPH, so the GQA group of a kv head shares each
+//     K/V row read from shared memory.  In a warp, a half-warp covers one
+//     token row (16 lanes x d/16 dims, one 16-byte smem load for bf16 d=128)
+//     and the two halves take different tokens.  Dot products use the packed
+//     fp32x2 FMA; the 16-lane reduction is a butterfly reduce-scatter so each
+//     lane ends with one (token, head) logit.  Online softmax in base 2.
+//   * Score: on window steps the logits (already in log2 units) go to a
+//     scratch array; once every sequence's final max and sum are known, a
+//     second, fully parallel kernel turns them into probabilities, takes the
+//     max over the GQA group and adds 1/w of it to the paged score.
+#include <math.h>
+
+#include "zp_common.cuh"
+
+namespace zp {
+namespace {
+
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kStageBytesCap = 32768;  // per tensor and stage
+constexpr int kMaxB = 4096;
+
+struct DecodeArgs {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *out;
+    const int32_t *table;
+    int table_stride;
+    const int32_t *seq_lens;
+    int B;
+    int h_q, h_kv, b, n_total;
+    int T;     // tokens per unit
+    int upb;   // units per block = b / T
+    int wph;   // consumer warps per kv head
+    int ncw;   // consumer warps
+    int stages;
+    float qscale;  // log2(e) / sqrt(d)
+    int want_score;
+    int window;
+    float *score;
+    float *logits;     // [units * T][h_q]
+    float2 *stats;     // [B][h_q] final (max, sum), log2 units
+    float *part_acc;   // [2*grid][h_q][D]
+    float2 *part_ml;   // [2*grid][h_q]
+    int *seq_count;    // [B], zero on entry
+    int *unit_prefix;  // [B+1]
+    long long logits_units;  // capacity of `logits` in units
+    unsigned *err;
+};
+
+// Reduce-scatter of V per-lane values over the 16 lanes of a half-warp (lane
+// bits 3..0, high bit first).  Afterwards lane l holds in v[0..max(V/16,1))
+// the full sums of indices l*(V/16)+i (V >= 16) or l/(16/V) (V < 16).
+template <int N, int BIT>
+struct ReduceScatter16 {
+    template <int V>
+    static __device__ __forceinline__ void run(float (&v)[V], int lane) {
+        if constexpr (BIT >= 0) {
+            if constexpr (N > 1) {
+                constexpr int H = N / 2;
+                const bool up = (lane >> BIT) & 1;
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const float send = up ? v[i] : v[i + H];
+                    const float keep = up ? v[i + H] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1 << BIT);
+                }
+                ReduceScatter16<H, BIT - 1>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1 << BIT);
+                ReduceScatter16<1, BIT - 1>::run(v, lane);
+            }
+        }
+    }
+};
+
+// DPL elements of a row (this lane's dims) as DPL/2 float pairs.
+template <typename T, int DPL>
+__device__ __forceinline__ void load_row(const T *p, float2 (&o)[DPL / 2]) {
+    if constexpr (sizeof(T) == 2) {
+        if constexpr (DPL == 8) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(p);
+            o[0] = bf2_to_f2(w.x);
+            o[1] = bf2_to_f2(w.y);
+            o[2] = bf2_to_f2(w.z);
+            o[3] = bf2_to_f2(w.w);
+        } else {
+            static_assert(DPL == 4, "bf16 rows: d in {64, 128}");
+            const uint2 w = *reinterpret_cast<const uint2 *>(p);
+            o[0] = bf2_to_f2(w.x);
+            o[1] = bf2_to_f2(w.y);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < DPL / 4; ++i) {
+            const float4 w = reinterpret_cast<const float4 *>(p)[i];
+            o[2 * i] = make_float2(w.x, w.y);
+            o[2 * i + 1] = make_float2(w.z, w.w);
+        }
+    }
+}
+
+template <typename T, int DPL>
+__device__ __forceinline__ void store_row(T *p, const float2 (&o)[DPL / 2], float scale) {
+    if constexpr (sizeof(T) == 2) {
+        uint32_t w[DPL / 2];
+#pragma unroll
+        for (int i = 0; i < DPL / 2; ++i) w[i] = f2_to_bf2(o[i].x * scale, o[i].y * scale);
+        if constexpr (DPL == 8) {
+            *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < DPL / 4; ++i)
+            reinterpret_cast<float4 *>(p)[i] = make_float4(o[2 * i].x * scale, o[2 * i].y * scale,
+                                                           o[2 * i + 1].x * scale,
+                                                           o[2 * i + 1].y * scale);
+    }
+}
+
+__device__ __forceinline__ long long cta_start(int c, long long U, int G) {
+    return (long long)c * U / G;
+}
+
+// CTA whose range [start(c), start(c+1)) holds unit u.
+__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
+    int c = (int)((u * G) / U);
+    if (c >= G) c = G - 1;
+    while (c + 1 < G && cta_start(c + 1, U, G) <= u) ++c;
+    while (c > 0 && cta_start(c, U, G) > u) --c;
+    return c;
+}
+
+// Shared-memory layout (dynamic).
+struct SmemLayout {
+    int bar_off;      // 2*stages mbarriers
+    int ctl_off;      // small ints: abort flag, last-arriver flag
+    int stage_off;    // stages * 2 * stage_bytes
+    int warp_off;     // per consumer warp: p[8][G], m_new[G], alpha[G], l[G]
+    int merge_off;    // (ncw - h_kv) * (G*D + 2G) floats
+    int prefix_off;   // B+1 ints
+    int lens_off;     // B ints
+    int total;
+};
+
+__host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, int ncw, int h_kv,
+                                                  int G, int D, int B) {
+    SmemLayout L;
+    int off = 0;
+    L.bar_off = off;
+    off += 2 * stages * 8;
+    L.ctl_off = off;
+    off += 16;
+    off = (off + 127) / 128 * 128;
+    L.stage_off = off;
+    off += stages * 2 * stage_bytes;
+    L.warp_off = off;
+    off += ncw * (8 * G + 3 * G) * 4;
+    off = (off + 15) / 16 * 16;
+    L.merge_off = off;
+    off += (ncw - h_kv) * (G * D + 2 * G) * 4;
+    off = (off + 15) / 16 * 16;
+    L.prefix_off = off;
+    off += (B + 1) * 4;
+    L.lens_off = off;
+    off += B * 4;
+    L.total = (off + 127) / 128 * 128;
+    return L;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
+    decode_main_kernel(const DecodeArgs a) {
+    constexpr int DPL = D / 16;  // dims per lane (16 lanes per token row)
+    constexpr int V = 4 * G;     // (token, head) partial sums per lane per half-warp step
+    constexpr int NV = V >= 16 ? V / 16 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int B = a.B;
+    const int TU = a.T;
+    const int stage_bytes = TU * a.h_kv * D * (int)sizeof(T);
+    const SmemLayout lay = make_layout(a.stages, stage_bytes, a.ncw, a.h_kv, G, D, B);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+    uint64_t *empty = full + a.stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.ctl_off);
+    volatile int *last_flag = abort_flag + 1;
+    int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
+    int *lens = reinterpret_cast<int *>(smem + lay.lens_off);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- unit prefix over sequences: n_units(s) = ceil(L_s / T)
+    for (int s = tid; s < B; s += blockDim.x) {
+        int L = a.seq_lens[s];
+        if (L < 0) {
+            record_error(a.err, ZP_ERR_DEVICE, 1);
+            L = 0;
+        }
+        const int maxL = a.table_stride * a.b;
+        if (L > maxL) {
+            record_error(a.err, ZP_ERR_DEVICE, 2);
+            L = maxL;
+        }
+        lens[s] = L;
+    }
+    if (tid == 0) {
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], a.ncw);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // block-wide exclusive scan of unit counts (B <= 4096, serial chunks per warp 0)
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int s = base + lane;
+            const int n = s < B ? (lens[s] + TU - 1) / TU : 0;
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (s < B) prefix[s] = carry + x - n;
+            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+        if (lane == 0) prefix[B] = carry;
+    }
+    __syncthreads();
+    const long long U = prefix[B];
+    if (blockIdx.x == 0) {
+        for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
+    }
+    if (a.want_score && U > a.logits_units) {
+        if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 3);
+        return;
+    }
+    const int Gd = gridDim.x;
+    const long long u0 = cta_start(blockIdx.x, U, Gd);
+    const long long u1 = cta_start(blockIdx.x + 1, U, Gd);
+    if (u0 >= u1) return;
+
+    // first sequence of the range: largest s with prefix[s] <= u0
+    int s_first = 0;
+    {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= u0) lo = mid;
+            else hi = mid - 1;
+        }
+        s_first = lo;
+    }
+
+    unsigned char *stage_base = smem + lay.stage_off;
+    const int row_elems = a.h_kv * D;
+
+    // =====================================================================
+    // Copies are issued by lane 0 of warp 0 (no dedicated producer warp: a
+    // 17th warp would cap every thread at 96 registers).  Unit i of the range
+    // goes to stage i % stages; the stage is refilled once all consumer warps
+    // have released it (empty barrier), so up to stages-1 units are in flight
+    // ahead of the slowest warp.
+    const uint64_t pol = l2_evict_first_policy();
+    int ps = s_first;  // sequence of the next unit to issue (lane 0 of warp 0 only)
+    auto issue = [&](long long i) {
+        const long long u = u0 + i;
+        while (u >= prefix[ps + 1]) ++ps;
+        const int st = (int)(i % a.stages);
+        const int j = (int)(u - prefix[ps]);
+        const int tok0 = j * TU;
+        int valid = lens[ps] - tok0;
+        if (valid > TU) valid = TU;
+        const int blk = __ldg(&a.table[(size_t)ps * a.table_stride + tok0 / a.b]);
+        unsigned char *ks = stage_base + (size_t)st * 2 * stage_bytes;
+        unsigned char *vs = ks + stage_bytes;
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 4);
+            mbar_arrive_expect_tx(&full[st], 0);
+        } else {
+            const unsigned bytes = (unsigned)(valid * row_elems * (int)sizeof(T));
+            const size_t off = ((size_t)blk * a.b + (tok0 % a.b)) * row_elems;
+            mbar_arrive_expect_tx(&full[st], 2 * bytes);
+            bulk_g2s(ks, static_cast<const T *>(a.k) + off, bytes, &full[st], pol);
+            bulk_g2s(vs, static_cast<const T *>(a.v) + off, bytes, &full[st], pol);
+        }
+    };
+    const long long n_units = u1 - u0;
+    if (tid == 0) {
+        for (long long i = 0; i < n_units && i < a.stages; ++i) issue(i);
+    }
+
+    // =====================================================================
+    // consumer warps
+    const int ncw_threads = a.ncw * 32;
+    const int kvh = warp / a.wph;
+    const int wih = warp % a.wph;
+    const int lane16 = lane & 15;
+    const int half = lane >> 4;
+    const int TPW = TU / a.wph;
+    float *wsm = reinterpret_cast<float *>(smem + lay.warp_off) + warp * (11 * G);
+    float *sp = wsm;               // p[8][G]
+    float *ctl_m = wsm + 8 * G;    // m_new[G]
+    float *ctl_a = ctl_m + G;      // alpha[G]
+    float *ctl_l = ctl_a + G;      // l[G]
+    float *merge = reinterpret_cast<float *>(smem + lay.merge_off);
+    const int h0 = kvh * G;
+
+    // value i of this lane: head index and "writer / owner" roles
+    int jv[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int idx = V >= 16 ? lane16 * NV + i : lane16 / (16 / V);
+        jv[i] = idx % G;
+    }
+    const bool writer = V >= 16 ? true : (lane16 % (16 / V)) == 0;
+    const bool owner = writer && ((lane & 0x1C) == 0);
+    const int tok_in_step = half * 4 + (lane16 >> 2);
+
+    float2 qv[G][DPL / 2];
+    float2 acc[G][DPL / 2];
+    float m[G];
+    float l_own[NV];
+
+    auto reset_state = [&]() {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            m[j] = -INFINITY;
+#pragma unroll
+            for (int p = 0; p < DPL / 2; ++p) acc[j][p] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) l_own[i] = 0.f;
+    };
+    auto load_q = [&](int s) {
+        const T *qg = static_cast<const T *>(a.q) + ((size_t)s * a.h_q + h0) * D + lane16 * DPL;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            float2 t2[DPL / 2];
+            load_row<T, DPL>(qg + (size_t)j * D, t2);
+#pragma unroll
+            for (int p = 0; p < DPL / 2; ++p)
+                qv[j][p] = make_float2(t2[p].x * a.qscale, t2[p].y * a.qscale);
+        }
+    };
+
+    int s = s_first;
+    long long seg_begin = u0;
+    reset_state();
+    load_q(s);
+    bool window_step = false;
+    auto compute_window = [&](int seq) {
+        const int P = lens[seq] - 1;
+        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window;
+    };
+    window_step = compute_window(s);
+
+    for (long long u = u0, i = 0; u < u1; ++u, ++i) {
+        const int st = (int)(i % a.stages);
+        const bool got = mbar_wait_bounded(&full[st], (unsigned)((i / a.stages) & 1), a.err,
+                                           abort_flag, 20);
+        const int j_unit = (int)(u - prefix[s]);
+        int valid = lens[s] - j_unit * TU;
+        if (valid > TU) valid = TU;
+        if (!got) valid = 0;
+        const T *ks = reinterpret_cast<const T *>(stage_base + (size_t)st * 2 * stage_bytes);
+        const T *vs = reinterpret_cast<const T *>(stage_base + (size_t)st * 2 * stage_bytes +
+                                                  stage_bytes);
+
+        for (int step = 0; step < TPW / 8; ++step) {
+            const int tok_base = wih * TPW + step * 8;  // token index within the unit
+            if (tok_base >= valid) break;  // warp-uniform
+            // ---- logits for 4 tokens of this half-warp
+            float v[V];
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const int tok = tok_base + half * 4 + i4;
+                float2 kk[DPL / 2];
+                load_row<T, DPL>(ks + ((size_t)tok * a.h_kv + kvh) * D + lane16 * DPL, kk);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int p = 0; p < DPL / 2; ++p) acc2 = ffma2(qv[j][p], kk[p], acc2);
+                    v[i4 * G + j] = acc2.x + acc2.y;
+                }
+            }
+            ReduceScatter16<V, 3>::run(v, lane16);
+            const int tok = tok_base + tok_in_step;
+            const bool tvalid = tok < valid;
+            float sc[NV], mx[NV];
+#pragma unroll
+            for (int i2 = 0; i2 < NV; ++i2) {
+                sc[i2] = tvalid ? v[i2] : -INFINITY;
+                mx[i2] = sc[i2];
+                mx[i2] = warp_max_xor(mx[i2], 4);
+                mx[i2] = warp_max_xor(mx[i2], 8);
+                mx[i2] = warp_max_xor(mx[i2], 16);
+            }
+            if (window_step && writer && tvalid) {
+                float *lg = a.logits + ((size_t)u * TU + tok) * a.h_q + h0;
+#pragma unroll
+                for (int i2 = 0; i2 < NV; ++i2) lg[jv[i2]] = sc[i2];
+            }
+            if (owner) {
+#pragma unroll
+                for (int i2 = 0; i2 < NV; ++i2) {
+                    const int j = jv[i2];
+                    const float mo = m[j];
+                    const float mn = fmaxf(mo, mx[i2]);
+                    ctl_m[j] = mn;
+                    ctl_a[j] = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+                }
+            }
+            __syncwarp();
+            float alpha[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                m[j] = ctl_m[j];
+                alpha[j] = ctl_a[j];
+            }
+            float pr[NV], ps[NV];
+#pragma unroll
+            for (int i2 = 0; i2 < NV; ++i2) {
+                pr[i2] = (sc[i2] == -INFINITY) ? 0.f : exp2f(sc[i2] - m[jv[i2]]);
+                ps[i2] = pr[i2];
+                ps[i2] += __shfl_xor_sync(0xFFFFFFFFu, ps[i2], 4);
+                ps[i2] += __shfl_xor_sync(0xFFFFFFFFu, ps[i2], 8);
+                ps[i2] += __shfl_xor_sync(0xFFFFFFFFu, ps[i2], 16);
+                if (owner) l_own[i2] = l_own[i2] * alpha[jv[i2]] + ps[i2];
+                if (writer) sp[tok_in_step * G + jv[i2]] = pr[i2];
+            }
+            __syncwarp();
+            // ---- P V
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float2 a2 = make_float2(alpha[j], alpha[j]);
+#pragma unroll
+                for (int p = 0; p < DPL / 2; ++p) acc[j][p] = fmul2(acc[j][p], a2);
+            }
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const int tl = half * 4 + i4;
+                if (tok_base + tl < valid) {
+                    float2 vv[DPL / 2];
+                    load_row<T, DPL>(vs + ((size_t)(tok_base + tl) * a.h_kv + kvh) * D + lane16 * DPL,
+                                     vv);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const float pj = sp[tl * G + j];
+                        const float2 p2 = make_float2(pj, pj);
+#pragma unroll
+                        for (int p = 0; p < DPL / 2; ++p) acc[j][p] = ffma2(vv[p], p2, acc[j][p]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (tid == 0 && i + a.stages < n_units) {
+            if (mbar_wait_bounded(&empty[st], (unsigned)((i / a.stages) & 1), a.err, abort_flag, 10))
+                issue(i + a.stages);
+        }
+
+        // ---- end of a segment: this sequence ends here, or the CTA range ends
+        const bool seq_ends = (u + 1 == prefix[s + 1]);
+        if (seq_ends || u + 1 == u1) {
+            // halves -> lanes 0..15
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int p = 0; p < DPL / 2; ++p) {
+                    acc[j][p].x += __shfl_xor_sync(0xFFFFFFFFu, acc[j][p].x, 16);
+                    acc[j][p].y += __shfl_xor_sync(0xFFFFFFFFu, acc[j][p].y, 16);
+                }
+            if (owner) {
+#pragma unroll
+                for (int i2 = 0; i2 < NV; ++i2) ctl_l[jv[i2]] = l_own[i2];
+            }
+            __syncwarp();
+            float l[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) l[j] = ctl_l[j];
+
+            // merge the WPH warps of a kv head into its leader (wih == 0)
+            if (a.wph > 1) {
+                if (wih > 0) {
+                    float *mw = merge + (size_t)(kvh * (a.wph - 1) + (wih - 1)) * (G * D + 2 * G);
+                    if (lane < 16) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j)
+#pragma unroll
+                            for (int p = 0; p < DPL / 2; ++p)
+                                reinterpret_cast<float2 *>(mw + j * D + lane16 * DPL)[p] = acc[j][p];
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            mw[G * D + j] = m[j];
+                            mw[G * D + G + j] = l[j];
+                        }
+                    }
+                }
+                named_bar_sync(1, ncw_threads);
+                if (wih == 0) {
+                    for (int w2 = 1; w2 < a.wph; ++w2) {
+                        const float *mw = merge + (size_t)(kvh * (a.wph - 1) + (w2 - 1)) * (G * D + 2 * G);
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const float mo = mw[G * D + j];
+                            const float lo = mw[G * D + G + j];
+                            const float mn = fmaxf(m[j], mo);
+                            const float f_self = (mn == -INFINITY) ? 0.f : exp2f(m[j] - mn);
+                            const float f_oth = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+                            l[j] = l[j] * f_self + lo * f_oth;
+                            m[j] = mn;
+                            const float2 fs = make_float2(f_self, f_self);
+                            const float2 fo = make_float2(f_oth, f_oth);
+#pragma unroll
+                            for (int p = 0; p < DPL / 2; ++p) {
+                                const float2 ov =
+                                    reinterpret_cast<const float2 *>(mw + j * D + lane16 * DPL)[p];
+                                acc[j][p] = ffma2(ov, fo, fmul2(acc[j][p], fs));
+                            }
+                        }
+                    }
+                }
+                named_bar_sync(1, ncw_threads);
+            }
+
+            const bool whole = (prefix[s] >= seg_begin) && seq_ends;
+            if (whole) {
+                if (wih == 0 && lane < 16) {
+                    T *og = static_cast<T *>(a.out) + ((size_t)s * a.h_q + h0) * D + lane16 * DPL;
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
+                        store_row<T, DPL>(og + (size_t)j * D, acc[j], inv);
+                    }
+                    if (a.want_score && lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) a.stats[(size_t)s * a.h_q + h0 + j] = make_float2(m[j], l[j]);
+                    }
+                }
+            } else {
+                // partial record of this CTA for sequence s
+                const int slot = 2 * blockIdx.x + ((prefix[s] <= u0) ? 0 : 1);
+                if (wih == 0 && lane < 16) {
+                    float *pa = a.part_acc + ((size_t)slot * a.h_q + h0) * D + lane16 * DPL;
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+#pragma unroll
+                        for (int p = 0; p < DPL / 2; ++p)
+                            reinterpret_cast<float2 *>(pa + (size_t)j * D)[p] = acc[j][p];
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j)
+                            a.part_ml[(size_t)slot * a.h_q + h0 + j] = make_float2(m[j], l[j]);
+                    }
+                }
+                __threadfence();
+                named_bar_sync(1, ncw_threads);
+                if (tid == 0) {
+                    const int nseg = (int)(u + 1 - seg_begin);
+                    const int ntot = prefix[s + 1] - prefix[s];
+                    const int before = atomicAdd(&a.seq_count[s], nseg);
+                    *last_flag = (before + nseg == ntot) ? 1 : 0;
+                }
+                named_bar_sync(1, ncw_threads);
+                if (*last_flag) {
+                    __threadfence();
+                    const int c_lo = cta_of(prefix[s], U, Gd);
+                    const int c_hi = cta_of(prefix[s + 1] - 1, U, Gd);
+                    // every consumer thread merges some (head, dim) elements
+                    for (int e = tid; e < a.h_q * D; e += ncw_threads) {
+                        const int h = e / D;
+                        const int dd = e % D;
+                        float M = -INFINITY;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const long long cs = cta_start(c, U, Gd);
+                            if (cs == cta_start(c + 1, U, Gd)) continue;  // empty range: no record
+                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
+                            M = fmaxf(M, __ldcg(&a.part_ml[(size_t)sl * a.h_q + h].x));
+                        }
+                        float Ls = 0.f, A = 0.f;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const long long cs = cta_start(c, U, Gd);
+                            if (cs == cta_start(c + 1, U, Gd)) continue;
+                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
+                            const float2 ml = __ldcg(&a.part_ml[(size_t)sl * a.h_q + h]);
+                            const float f = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                            Ls += ml.y * f;
+                            A += __ldcg(&a.part_acc[((size_t)sl * a.h_q + h) * D + dd]) * f;
+                        }
+                        const float o = Ls > 0.f ? A / Ls : 0.f;
+                        T *og = static_cast<T *>(a.out) + ((size_t)s * a.h_q + h) * D + dd;
+                        if constexpr (sizeof(T) == 2) *og = __float2bfloat16_rn(o);
+                        else *og = o;
+                        if (a.want_score && dd == 0) a.stats[(size_t)s * a.h_q + h] = make_float2(M, Ls);
+                    }
+                }
+            }
+            // next sequence
+            if (u + 1 < u1) {
+                ++s;
+                seg_begin = u + 1;
+                reset_state();
+                load_q(s);
+                window_step = compute_window(s);
+            }
+        }
+    }
+}
+
+// Window-score epilogue: one thread per (token, kv head) of window-step
+// sequences.  p_h(t) = 2^(logit - m_h) / l_h; S += (1/w) max_h p_h(t).
+template <int G>
+__global__ void decode_score_kernel(const DecodeArgs a) {
+    extern __shared__ int pre[];  // unit prefix [B+1]
+    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) pre[i] = a.unit_prefix[i];
+    __syncthreads();
+    const int U = pre[a.B];
+    const int items = a.T * a.h_kv;
+    const float inv_w = 1.f / (float)a.window;
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        const int s = lo;
+        int L = a.seq_lens[s];
+        if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+        const int P = L - 1;
+        if (P < 0) continue;
+        const int r = P % a.b;
+        if (r < a.b - a.window) continue;  // block-uniform
+        const bool first_row = (r == a.b - a.window);
+        for (int it = threadIdx.x; it < items; it += blockDim.x) {
+            const int tl = it / a.h_kv;
+            const int kvh = it % a.h_kv;
+            const int tok = (u - pre[s]) * a.T + tl;
+            if (tok >= L) continue;
+            const float *lg = a.logits + ((size_t)u * a.T + tl) * a.h_q + kvh * G;
+            const float2 *st = a.stats + (size_t)s * a.h_q + kvh * G;
+            float best = 0.f;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float2 ml = st[j];
+                const float p = exp2f(lg[j] - ml.x) / ml.y;
+                best = fmaxf(best, p);
+            }
+            const float c = best * inv_w;
+            const int blk = a.table[(size_t)s * a.table_stride + tok / a.b];
+            if (blk < 0 || blk >= a.n_total) {
+                record_error(a.err, ZP_ERR_DEVICE, 5);
+                continue;
+            }
+            float *dst = a.score + ((size_t)blk * a.b + tok % a.b) * a.h_kv + kvh;
+            *dst = (first_row || tok == P) ? c : (*dst + c);
+        }
+    }
+}
+
+struct Plan {
+    int T, wph, ncw, stages, smem, grid;
+    size_t off_count, off_prefix, off_stats, off_pml, off_pacc, off_logits, total;
+    long long logits_units;
+};
+
+zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const DeviceInfo &dev,
+                    Plan *p) {
+    const int es = elem_bytes(D->dtype);
+    const int d = D->head_dim, b = D->block_size, h_kv = D->h_kv;
+    const int G = D->h_q / D->h_kv;
+    if (!(d == 64 || d == 128)) return fail(ZP_ERR_SHAPE, "decode: head_dim %d not in {64,128}", d);
+    if (!(G == 4 || G == 8)) return fail(ZP_ERR_SHAPE, "decode: group size %d not in {4,8}", G);
+    if (!(h_kv == 2 || h_kv == 4 || h_kv == 8 || h_kv == 16))
+        return fail(ZP_ERR_SHAPE, "decode: h_kv %d not in {2,4,8,16}", h_kv);
+    if (b < 16 || (b & (b - 1))) return fail(ZP_ERR_SHAPE, "decode: block size %d", b);
+    if (B > kMaxB) return fail(ZP_ERR_SHAPE, "decode: B %d > %d", B, kMaxB);
+    const int row = h_kv * d * es;
+    int T = b;
+    while (T > 8 && T * row > kStageBytesCap) T >>= 1;
+    if (T * row > kStageBytesCap) return fail(ZP_ERR_SHAPE, "decode: row of %d bytes too large", row);
+    int wph = T / 8;
+    if (wph > kMaxConsumerWarps / h_kv) wph = kMaxConsumerWarps / h_kv;
+    if (wph < 1) wph = 1;
+    p->T = T;
+    p->wph = wph;
+    p->ncw = h_kv * wph;
+    p->grid = dev.sm_count;
+    const int stage_bytes = T * row;
+    int stages = 4;
+    while (stages > 2 &&
+           make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total > dev.smem_optin)
+        --stages;
+    p->stages = stages;
+    p->smem = make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total;
+    if (p->smem > dev.smem_optin) return fail(ZP_ERR_SHAPE, "decode: needs %d B of shared memory", p->smem);
+    const long long units_cap = (long long)B * table_stride * (b / T);
+    p->logits_units = units_cap;
+    size_t off = 0;
+    p->off_count = off;
+    off = align_up(off + (size_t)B * 4, 256);
+    p->off_prefix = off;
+    off = align_up(off + (size_t)(B + 1) * 4, 256);
+    p->off_stats = off;
+    off = align_up(off + (size_t)B * D->h_q * 8, 256);
+    p->off_pml = off;
+    off = align_up(off + (size_t)2 * p->grid * D->h_q * 8, 256);
+    p->off_pacc = off;
+    off = align_up(off + (size_t)2 * p->grid * D->h_q * d * 4, 256);
+    p->off_logits = off;
+    off = align_up(off + (size_t)units_cap * T * D->h_q * 4, 256);
+    p->total = off;
+    return ZP_OK;
+}
+
+template <typename T, int Dd, int G>
+zp_status launch_t(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cudaStream_t st) {
+    static int configured_smem[64] = {0};
+    auto kmain = decode_main_kernel<T, Dd, G>;
+    const int dv = dev.device < 64 ? dev.device : 63;
+    if (configured_smem[dv] < p.smem) {
+        cudaError_t e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+        if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
+        configured_smem[dv] = p.smem;
+    }
+    kmain<<<p.grid, p.ncw * 32, p.smem, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode: main kernel launch");
+    if (a.want_score) {
+        const int threads = 128;
+        decode_score_kernel<G><<<p.grid * 8, threads, (a.B + 1) * 4, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
+    }
+    return ZP_OK;
+}
+
+}  // namespace
+}  // namespace zp
+
+using namespace zp;
+
+extern "C" size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table_stride) {
+    if (check_desc(D) != ZP_OK || B < 0 || table_stride < 0) return 0;
+    DeviceInfo dev;
+    if (device_info(&dev) != ZP_OK) return 0;
+    Plan p;
+    if (make_plan(D, B, table_stride, dev, &p) != ZP_OK) return 0;
+    return p.total;
+}
+
+extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_table,
+                                          int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                                          void *out, float *score_accum, int32_t window,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+    zp_status rc = check_desc(D);
+    if (rc != ZP_OK) return rc;
+    if (B < 0 || table_stride < 0) return fail(ZP_ERR_INVALID_ARG, "decode: B or table_stride negative");
+    if (B == 0) return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
+        return fail(ZP_ERR_INVALID_ARG, "decode: NULL buffer");
+    if (table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "decode: table_stride < 1");
+    if (score_accum && (window < 1 || window > D->block_size))
+        return fail(ZP_ERR_INVALID_ARG, "decode: window %d outside [1, b=%d]", window, D->block_size);
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != ZP_OK) return rc;
+    Plan p;
+    rc = make_plan(D, B, table_stride, dev, &p);
+    if (rc != ZP_OK) return rc;
+    if (workspace_bytes < p.total)
+        return fail(ZP_ERR_CAPACITY, "decode: workspace %zu < %zu bytes", workspace_bytes, p.total);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    DecodeArgs a;
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.out = out;
+    a.table = block_table;
+    a.table_stride = table_stride;
+    a.seq_lens = seq_lens;
+    a.B = B;
+    a.h_q = D->h_q;
+    a.h_kv = D->h_kv;
+    a.b = D->block_size;
+    a.n_total = D->n_total_blocks;
+    a.T = p.T;
+    a.upb = D->block_size / p.T;
+    a.wph = p.wph;
+    a.ncw = p.ncw;
+    a.stages = p.stages;
+    a.qscale = (float)(1.4426950408889634 / sqrt((double)D->head_dim));
+    a.want_score = score_accum != nullptr;
+    a.window = window;
+    a.score = score_accum;
+    a.logits = reinterpret_cast<float *>(ws + p.off_logits);
+    a.stats = reinterpret_cast<float2 *>(ws + p.off_stats);
+    a.part_acc = reinterpret_cast<float *>(ws + p.off_pacc);
+    a.part_ml = reinterpret_cast<float2 *>(ws + p.off_pml);
+    a.seq_count = reinterpret_cast<int *>(ws + p.off_count);
+    a.unit_prefix = reinterpret_cast<int *>(ws + p.off_prefix);
+    a.logits_units = p.logits_units;
+    a.err = dev.error_word;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(a.seq_count, 0, (size_t)B * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode: memset of arrival counters");
+    const int G = D->h_q / D->h_kv;
+    const int d = D->head_dim;
+    if (D->dtype == ZP_BF16) {
+        if (d == 128 && G == 4) return launch_t<__nv_bfloat16, 128, 4>(a, p, dev, st);
+        if (d == 128 && G == 8) return launch_t<__nv_bfloat16, 128, 8>(a, p, dev, st);
+        if (d == 64 && G == 4) return launch_t<__nv_bfloat16, 64, 4>(a, p, dev, st);
+        if (d == 64 && G == 8) return launch_t<__nv_bfloat16, 64, 8>(a, p, dev, st);
+    } else {
+        if (d == 128 && G == 4) return launch_t<float, 128, 4>(a, p, dev, st);
+        if (d == 128 && G == 8) return launch_t<float, 128, 8>(a, p, dev, st);
+        if (d == 64 && G == 4) return launch_t<float, 64, 4>(a, p, dev, st);
+        if (d == 64 && G == 8) return launch_t<float, 64, 8>(a, p, dev, st);
+    }
+    return fail(ZP_ERR_SHAPE, "decode: no kernel for d=%d, group=%d", d, G);
+}

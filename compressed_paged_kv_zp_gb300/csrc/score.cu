@@ -1,0 +1,347 @@
+// score.cu -- per-token eviction scores of the sequences being compressed.
+//
+// Zipage paper App. C.2-C.8 and §4.2, in the order of the paper's per-op
+// timing figure (Figs. 13/14): attention score -> global score -> pooling ->
+// redundancy score -> window mask.  Three launches:
+//   1. gather_global: the accumulated window score S (paged, written by the
+//      decode kernel) is gathered per (sequence, kv head) and, if enabled, run
+//      through Alg. 2 against the paged global score cache F (updated in
+//      place).  Result X [n][h_kv][Lmax].
+//   2. lightning: one CTA per (sequence, block): the block's keys of every kv
+//      head are staged in shared memory, each warp forms the b x b cosine
+//      matrix of one kv head, zeroes the diagonal and, per column, the newest
+//      entry above the threshold p (C.5, restricted to the block as in C.7),
+//      and writes the row sums rho [n][h_kv][Lmax].
+//   3. finalize: one CTA per (sequence, kv head): max-pool X (C.4) when the
+//      policy says so, R = softmax(rho / (L * tau)) (C.5, C.8), out = Xp -
+//      lambda * R (eq. 4), last w tokens -> +inf (§4.2, App. C.6).
+#include <math.h>
+
+#include "zp_common.cuh"
+
+namespace zp {
+namespace {
+
+constexpr int kTile = 64;  // tokens per gather tile
+
+struct ScoreArgs {
+    const int32_t *table;
+    int table_stride;
+    const int32_t *seq_lens;
+    const uint8_t *first;
+    int n, h_kv, b, n_total, Lmax, d;
+    const float *S;   // paged [N_total][b][h_kv]
+    float *F;         // paged, nullable
+    float *X;         // [n][h_kv][Lmax]
+    float *rho;       // [n][h_kv][Lmax]
+    float *out;       // [n][h_kv][Lmax]
+    const void *k;    // paged keys of this layer
+    int use_global;
+    float alpha;
+    int pool_kernel, pool_policy;
+    int use_sim;
+    float p, lambda, tau;
+    int window;
+    unsigned *err;
+};
+
+__device__ __forceinline__ int clamp_len(const ScoreArgs &a, int s) {
+    int L = a.seq_lens[s];
+    if (L < 0) L = 0;
+    if (L > a.Lmax) L = a.Lmax;
+    if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    return L;
+}
+
+// grid (ceil(Lmax / kTile), n), 256 threads
+__global__ void gather_global_kernel(const ScoreArgs a) {
+    __shared__ float tile[16][kTile + 1];  // h_kv <= 16
+    const int s = blockIdx.y;
+    const int t0 = blockIdx.x * kTile;
+    const int L = clamp_len(a, s);
+    if (t0 >= L) return;
+    const int N = (L + a.b - 1) / a.b;
+    const bool first = a.first ? a.first[s] != 0 : true;
+    const int items = kTile * a.h_kv;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int tl = it / a.h_kv;
+        const int kvh = it % a.h_kv;
+        const int t = t0 + tl;
+        float v = 0.f;
+        if (t < L) {
+            const int bi = t / a.b;
+            const int blk = a.table[(size_t)s * a.table_stride + bi];
+            if (blk < 0 || blk >= a.n_total) {
+                record_error(a.err, ZP_ERR_DEVICE, 0x200);
+            } else {
+                const size_t at = ((size_t)blk * a.b + t % a.b) * a.h_kv + kvh;
+                v = a.S[at];
+                if (a.use_global) {
+                    if (first) {
+                        a.F[at] = v;
+                    } else {
+                        if (bi != N - 1) v = fmaxf(a.alpha * a.F[at], v);
+                        a.F[at] = v;
+                    }
+                }
+            }
+        }
+        tile[kvh][tl] = v;
+    }
+    __syncthreads();
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int kvh = it / kTile;
+        const int tl = it % kTile;
+        const int t = t0 + tl;
+        if (t < L) a.X[((size_t)s * a.h_kv + kvh) * a.Lmax + t] = tile[kvh][tl];
+    }
+}
+
+// grid (ceil(Lmax / b), n), h_kv warps; dynamic smem: h_kv * b * (d + 1) floats
+// + b * h_kv norms.  Keys are converted to fp32 once; the padded row stride
+// (d + 1) keeps the 16 lanes that read 16 different rows on 16 banks.
+template <typename T>
+__global__ void lightning_kernel(const ScoreArgs a) {
+    extern __shared__ float kf[];
+    const int s = blockIdx.y;
+    const int bi = blockIdx.x;
+    const int L = clamp_len(a, s);
+    const int tb0 = bi * a.b;
+    if (tb0 >= L) return;
+    const int nvalid = min(a.b, L - tb0);
+    const int blk = a.table[(size_t)s * a.table_stride + bi];
+    if (blk < 0 || blk >= a.n_total) {
+        if (threadIdx.x == 0) record_error(a.err, ZP_ERR_DEVICE, 0x201);
+        return;
+    }
+    const int d = a.d;
+    const int ld = d + 1;
+    const T *src = static_cast<const T *>(a.k) + (size_t)blk * a.b * a.h_kv * d;
+    const int total = nvalid * a.h_kv * d;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int r = i / (a.h_kv * d);
+        const int rem = i % (a.h_kv * d);
+        const int kvh = rem / d;
+        const int dd = rem % d;
+        float x;
+        if constexpr (sizeof(T) == 2) x = __bfloat162float(src[i]);
+        else x = src[i];
+        kf[((size_t)kvh * a.b + r) * ld + dd] = x;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kvh = warp;
+    if (kvh >= a.h_kv) return;
+    const float *kh = kf + (size_t)kvh * a.b * ld;
+    // one warp per kv head; b <= 32 rows; lane = (row r, column half)
+    // Rows/columns beyond nvalid are outside the sequence and excluded.
+    const int b = a.b;
+    for (int rbase = 0; rbase < b; rbase += 16) {
+        const int r = rbase + (lane & 15);
+        const int chalf = lane >> 4;
+        // columns c = cb*16 + chalf*8 + j, processed 8 at a time
+        float rowsum = 0.f;
+        const float nr2 = [&] {
+            float acc = 0.f;
+            if (r < nvalid)
+                for (int dd = 0; dd < d; ++dd) acc = fmaf(kh[r * ld + dd], kh[r * ld + dd], acc);
+            return acc;
+        }();
+        const float nr = sqrtf(nr2);
+        for (int cb = 0; cb < b; cb += 16) {
+            float dot[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dot[j] = 0.f;
+            const int c0 = cb + chalf * 8;
+            if (r < nvalid) {
+                for (int dd = 0; dd < d; ++dd) {
+                    const float x = kh[r * ld + dd];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int c = c0 + j;
+                        if (c < nvalid) dot[j] = fmaf(x, kh[c * ld + dd], dot[j]);
+                    }
+                }
+            }
+            // cosine, diagonal, threshold: for column c the newest row r* with
+            // cos > p is zeroed.  Rows of this column live in lanes with the
+            // same chalf across the 16-row groups; with b <= 16 one group.
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = c0 + j;
+                float cosv = 0.f;
+                if (r < nvalid && c < nvalid && r != c) {
+                    float nc2 = 0.f;
+                    for (int dd = 0; dd < d; ++dd) nc2 = fmaf(kh[c * ld + dd], kh[c * ld + dd], nc2);
+                    const float nc = sqrtf(nc2);
+                    if (nr > 0.f && nc > 0.f) cosv = dot[j] / (nr * nc);
+                }
+                const unsigned above = __ballot_sync(0xFFFFFFFFu, cosv > a.p);
+                const unsigned mine = (above >> (chalf * 16)) & 0xFFFFu;
+                const int rstar = mine ? (31 - __clz(mine)) : -1;
+                if ((lane & 15) == rstar) cosv = 0.f;
+                rowsum += cosv;
+            }
+        }
+        rowsum += __shfl_xor_sync(0xFFFFFFFFu, rowsum, 16);
+        if (chalf == 0 && r < nvalid)
+            a.rho[((size_t)s * a.h_kv + kvh) * a.Lmax + tb0 + r] = rowsum;
+    }
+}
+
+// grid (h_kv, n), 1024 threads
+__global__ void finalize_kernel(const ScoreArgs a) {
+    __shared__ float red[32];
+    const int kvh = blockIdx.x;
+    const int s = blockIdx.y;
+    const int L = clamp_len(a, s);
+    if (L <= 0) return;
+    const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
+    const float *X = a.X + row;
+    const float *rho = a.rho + row;
+    float *out = a.out + row;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const bool first = a.first ? a.first[s] != 0 : true;
+    const bool pool = a.pool_kernel > 1 && (a.pool_policy == 2 || (a.pool_policy == 1 && first));
+    const int r = a.pool_kernel / 2;
+    float rmax = -INFINITY, rsum = 0.f;
+    const float inv = 1.f / ((float)L * a.tau);
+    if (a.use_sim) {
+        float m = -INFINITY;
+        for (int t = tid; t < L; t += blockDim.x) m = fmaxf(m, rho[t] * inv);
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        if (warp == 0) {
+            float x = lane < nw ? red[lane] : -INFINITY;
+            for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+            if (lane == 0) red[0] = x;
+        }
+        __syncthreads();
+        rmax = red[0];
+        __syncthreads();
+        float sum = 0.f;
+        for (int t = tid; t < L; t += blockDim.x) sum += expf(rho[t] * inv - rmax);
+        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane == 0) red[warp] = sum;
+        __syncthreads();
+        if (warp == 0) {
+            float x = lane < nw ? red[lane] : 0.f;
+            for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+            if (lane == 0) red[0] = x;
+        }
+        __syncthreads();
+        rsum = red[0];
+    }
+    for (int t = tid; t < L; t += blockDim.x) {
+        float v;
+        if (pool) {
+            const int lo = max(0, t - r), hi = min(L - 1, t + r);
+            v = X[lo];
+            for (int j = lo + 1; j <= hi; ++j) v = fmaxf(v, X[j]);
+        } else {
+            v = X[t];
+        }
+        if (a.use_sim) v -= a.lambda * (expf(rho[t] * inv - rmax) / rsum);
+        if (t >= L - a.window) v = INFINITY;
+        out[t] = v;
+    }
+}
+
+}  // namespace
+}  // namespace zp
+
+using namespace zp;
+
+extern "C" size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax) {
+    if (!D || n < 0 || Lmax < 0) return 0;
+    return 2 * align_up((size_t)n * D->h_kv * Lmax * 4, 256);
+}
+
+extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
+                                     const void *k_cache, const int32_t *block_table,
+                                     int32_t table_stride, const int32_t *seq_lens,
+                                     const uint8_t *first_compression, int32_t n,
+                                     const float *score_accum, float *global_F, float *scores_out,
+                                     int32_t Lmax, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+    zp_status rc = check_desc(D);
+    if (rc != ZP_OK) return rc;
+    if (!P) return fail(ZP_ERR_INVALID_ARG, "score: NULL params");
+    if (n < 0 || Lmax < 0 || table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: bad sizes");
+    if (n == 0 || Lmax == 0) return ok();
+    if (!block_table || !seq_lens || !score_accum || !scores_out || !workspace)
+        return fail(ZP_ERR_INVALID_ARG, "score: NULL buffer");
+    if (P->use_global && !global_F) return fail(ZP_ERR_INVALID_ARG, "score: use_global needs global_F");
+    if (P->use_similarity && !k_cache) return fail(ZP_ERR_INVALID_ARG, "score: similarity needs k_cache");
+    if (P->window < 0) return fail(ZP_ERR_INVALID_ARG, "score: window %d", P->window);
+    if (P->pool_kernel > 1 && P->pool_kernel % 2 == 0)
+        return fail(ZP_ERR_INVALID_ARG, "score: pool kernel %d must be odd", P->pool_kernel);
+    if (P->pool_policy < 0 || P->pool_policy > 2) return fail(ZP_ERR_INVALID_ARG, "score: pool policy");
+    if (P->use_similarity && !(P->tau > 0.f)) return fail(ZP_ERR_INVALID_ARG, "score: tau must be > 0");
+    if (D->h_kv > 16) return fail(ZP_ERR_SHAPE, "score: h_kv %d > 16", D->h_kv);
+    if (P->use_similarity && !P->lightning)
+        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy score is not built; use lightning");
+    if (P->use_similarity && D->block_size > 16)
+        return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
+    const size_t need = zp_score_workspace_size(D, n, Lmax);
+    if (workspace_bytes < need) return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != ZP_OK) return rc;
+    ScoreArgs a;
+    a.table = block_table;
+    a.table_stride = table_stride;
+    a.seq_lens = seq_lens;
+    a.first = first_compression;
+    a.n = n;
+    a.h_kv = D->h_kv;
+    a.b = D->block_size;
+    a.n_total = D->n_total_blocks;
+    a.Lmax = Lmax;
+    a.d = D->head_dim;
+    a.S = score_accum;
+    a.F = global_F;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.X = reinterpret_cast<float *>(ws);
+    a.rho = reinterpret_cast<float *>(ws + align_up((size_t)n * D->h_kv * Lmax * 4, 256));
+    a.out = scores_out;
+    a.k = k_cache;
+    a.use_global = P->use_global;
+    a.alpha = P->alpha;
+    a.pool_kernel = P->pool_kernel;
+    a.pool_policy = P->pool_policy;
+    a.use_sim = P->use_similarity;
+    a.p = P->threshold;
+    a.lambda = P->lambda;
+    a.tau = P->tau;
+    a.window = P->window;
+    a.err = dev.error_word;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    dim3 g1((Lmax + kTile - 1) / kTile, n);
+    gather_global_kernel<<<g1, 256, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "score: gather launch");
+    if (a.use_sim) {
+        dim3 g2((Lmax + a.b - 1) / a.b, n);
+        const size_t smem = (size_t)a.h_kv * a.b * (a.d + 1) * 4;
+        if (smem > (size_t)dev.smem_optin) return fail(ZP_ERR_SHAPE, "score: block of keys too large");
+        if (D->dtype == ZP_BF16) {
+            cudaFuncSetAttribute(lightning_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            lightning_kernel<__nv_bfloat16><<<g2, a.h_kv * 32, smem, st>>>(a);
+        } else {
+            cudaFuncSetAttribute(lightning_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            lightning_kernel<float><<<g2, a.h_kv * 32, smem, st>>>(a);
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "score: lightning launch");
+    }
+    dim3 g3(a.h_kv, n);
+    finalize_kernel<<<g3, 1024, 0, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "score: finalize launch");
+    return ok();
+}

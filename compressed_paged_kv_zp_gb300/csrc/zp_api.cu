@@ -1,0 +1,122 @@
+// zp_api.cu -- host-side plumbing of libzp: error messages, per-device
+// properties, the device status word and small entry points.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "zp_common.cuh"
+
+namespace zp {
+
+// Device status word of this module (one per device context).  Kernels get
+// its device address from device_info(); host code never dereferences it.
+__device__ unsigned g_zp_status_word;
+
+namespace {
+thread_local std::string t_last_error;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+bool g_dev_ready[64] = {false};
+}  // namespace
+
+zp_status fail(zp_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+zp_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(ZP_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+zp_status ok() {
+    t_last_error.clear();
+    return ZP_OK;
+}
+
+zp_status device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(ZP_ERR_CUDA, "device id %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem opt-in)");
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_zp_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        d.error_word = static_cast<unsigned *>(p);
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return ZP_OK;
+}
+
+zp_status check_desc(const zp_cache_desc *D) {
+    if (!D) return fail(ZP_ERR_INVALID_ARG, "NULL cache descriptor");
+    if (D->dtype != ZP_BF16 && D->dtype != ZP_F32) return fail(ZP_ERR_DTYPE, "unknown dtype %d", D->dtype);
+    if (D->h_q <= 0 || D->h_kv <= 0 || D->h_q % D->h_kv != 0)
+        return fail(ZP_ERR_SHAPE, "heads h_q=%d h_kv=%d", D->h_q, D->h_kv);
+    if (D->head_dim <= 0 || D->head_dim % 16 != 0) return fail(ZP_ERR_SHAPE, "head_dim %d", D->head_dim);
+    if (D->block_size <= 0) return fail(ZP_ERR_SHAPE, "block_size %d", D->block_size);
+    if (D->n_total_blocks <= 0) return fail(ZP_ERR_SHAPE, "n_total_blocks %d", D->n_total_blocks);
+    return ZP_OK;
+}
+
+}  // namespace zp
+
+using namespace zp;
+
+extern "C" const char *zp_last_error(void) { return t_last_error.c_str(); }
+
+extern "C" const char *zp_status_string(zp_status s) {
+    switch (s) {
+        case ZP_OK: return "ZP_OK";
+        case ZP_ERR_INVALID_ARG: return "ZP_ERR_INVALID_ARG";
+        case ZP_ERR_SHAPE: return "ZP_ERR_SHAPE";
+        case ZP_ERR_DTYPE: return "ZP_ERR_DTYPE";
+        case ZP_ERR_CAPACITY: return "ZP_ERR_CAPACITY";
+        case ZP_ERR_CUDA: return "ZP_ERR_CUDA";
+        case ZP_ERR_TIMEOUT: return "ZP_ERR_TIMEOUT";
+        case ZP_ERR_DEVICE: return "ZP_ERR_DEVICE";
+    }
+    return "ZP_ERR_UNKNOWN";
+}
+
+extern "C" int32_t zp_version(void) { return 1; }
+
+extern "C" zp_status zp_device_status(int32_t *code, int32_t *detail, int32_t clear) {
+    DeviceInfo dev;
+    zp_status rc = device_info(&dev);
+    if (rc != ZP_OK) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "zp_device_status: synchronize");
+    unsigned w = 0;
+    e = cudaMemcpy(&w, dev.error_word, sizeof w, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "zp_device_status: read");
+    if (code) *code = (int32_t)(w >> 24);
+    if (detail) *detail = (int32_t)(w & 0xFFFFFFu);
+    if (clear) {
+        e = cudaMemset(dev.error_word, 0, sizeof w);
+        if (e != cudaSuccess) return cuda_fail(e, "zp_device_status: clear");
+    }
+    return ok();
+}
+
+extern "C" int32_t zp_needs_compression(int32_t seq_len, int32_t block_size, int32_t max_blocks) {
+    if (seq_len <= 0 || block_size <= 0) return 0;
+    const int32_t n = (seq_len + block_size - 1) / block_size;
+    return (n >= max_blocks && seq_len % block_size == 0) ? 1 : 0;
+}

@@ -1,0 +1,159 @@
+// zp_common.cuh -- device helpers shared by the kernels of libzp (sm_103a).
+//
+// Inline PTX for the Blackwell pieces used here: mbarrier waits with an
+// iteration bound, 1-D bulk copies (cp.async.bulk, TMA engine) with an L2
+// eviction hint, and the packed fp32x2 FMA.  Nothing here traps: failures are
+// recorded in the library's device status word and the kernel carries on.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zp_internal.h"
+
+namespace zp {
+
+// ---------------------------------------------------------------- status word
+// The first error wins; the word holds (code << 24) | detail.
+__device__ __forceinline__ void record_error(unsigned *err, unsigned code, unsigned detail) {
+    if (err) atomicCAS(err, 0u, (code << 24) | (detail & 0xFFFFFFu));
+}
+
+// ---------------------------------------------------------------- element IO
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kBytes = 4;
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+};
+
+// bf16x2 word -> (low element, high element) as floats: the bf16 bits are the
+// high half of the fp32 bits.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    float2 r;
+    r.x = __uint_as_float(w << 16);
+    r.y = __uint_as_float(w & 0xFFFF0000u);
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- fp32x2 FMA
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long Bv = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long C = *reinterpret_cast<unsigned long long *>(&c);
+    unsigned long long Dv;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(Dv) : "l"(A), "l"(Bv), "l"(C));
+    return *reinterpret_cast<float2 *>(&Dv);
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long A = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long Bv = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long Dv;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(Dv) : "l"(A), "l"(Bv));
+    return *reinterpret_cast<float2 *>(&Dv);
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up after
+// about kWaitLimitNs of wall time, records ZP_ERR_TIMEOUT and returns false;
+// *abort is then set so that the other waits of the CTA return at once.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity, unsigned *err,
+                                                  volatile int *abort, unsigned where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (*abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            record_error(err, ZP_ERR_TIMEOUT, where);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- bulk copy
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global -> shared 1-D bulk copy completing on `bar` (bytes and both addresses
+// multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, unsigned bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- misc
+__device__ __forceinline__ float warp_max_xor(float v, int mask) {
+    return fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, mask));
+}
+
+__device__ __forceinline__ float ld_cg(const float *p) { return __ldcg(p); }
+
+}  // namespace zp

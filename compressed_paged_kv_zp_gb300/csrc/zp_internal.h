@@ -1,0 +1,32 @@
+// zp_internal.h -- declarations shared by the translation units of libzp.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "zp.h"
+
+namespace zp {
+
+// Host: record a message for zp_last_error() and return the status.
+zp_status fail(zp_status s, const char *fmt, ...);
+zp_status cuda_fail(cudaError_t e, const char *where);
+zp_status ok();
+
+// Host: properties of the current device (cached per device).
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int smem_optin;  // max dynamic shared memory per block
+    unsigned *error_word;  // device address of the status word
+};
+zp_status device_info(DeviceInfo *out);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int elem_bytes(int dtype) { return dtype == ZP_BF16 ? 2 : (dtype == ZP_F32 ? 4 : 0); }
+
+zp_status check_desc(const zp_cache_desc *D);
+
+}  // namespace zp

@@ -1,0 +1,213 @@
+/*
+ * zp.h -- C ABI of the Compressed PagedAttention hot path for one GB300 GPU.
+ *
+ * The operations follow the paper "Zipage: Maintain High Request Concurrency
+ * for LLM Reasoning through Compressed PagedAttention" (Liao et al., arXiv
+ * 2603.08743), cited below as [Zipage <section>].
+ *
+ * Conventions (apply to every call):
+ *   Ownership   Every device buffer is owned by the caller.  The library never
+ *               allocates device memory: scratch comes from a caller-supplied
+ *               workspace whose size the matching *_workspace_size() returns.
+ *               The host block pool (zp_pool_*) is owned by the library.
+ *   Streams     `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *               default stream).  Device calls only enqueue work on it and
+ *               never synchronise the device.
+ *   Errors      Every call returns zp_status.  ZP_OK means the arguments were
+ *               valid and the work was enqueued; a launch failure returns
+ *               ZP_ERR_CUDA.  zp_last_error() gives a message for the calling
+ *               thread.  Kernels never trap: a block id outside [0, N_total) or
+ *               a failed bounded wait is skipped and recorded in a device status
+ *               word that zp_device_status() reads.
+ *   Layouts     One layer of the K or V cache is [N_total][b][h_kv][d] ([Zipage
+ *               §3]); element (blk, slot, kvh, i) is at ((blk*b+slot)*h_kv+kvh)*d+i.
+ *               Several layers sit one after another, `layer_stride` elements
+ *               apart.  Per-slot float arrays (the window score S and the global
+ *               score cache F of [Zipage App. C.3]) are [N_total][b][h_kv].
+ *               Block tables are int32 [B][table_stride]: token t of sequence s
+ *               is in block table[s*table_stride + t/b], slot t%b.  Query head h
+ *               reads key/value head h/(h_q/h_kv).
+ *   Types       ZP_BF16 or ZP_F32 for q, K, V and the attention output; scores
+ *               are float32; ids and lengths int32.
+ */
+#ifndef ZP_H
+#define ZP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZP_OK = 0,
+    ZP_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad flag */
+    ZP_ERR_SHAPE = 2,       /* head / block geometry this build does not support */
+    ZP_ERR_DTYPE = 3,       /* unknown element type */
+    ZP_ERR_CAPACITY = 4,    /* workspace too small, pool exhausted, budget < window */
+    ZP_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    ZP_ERR_TIMEOUT = 6,     /* a bounded device wait gave up (device status) */
+    ZP_ERR_DEVICE = 7       /* kernels recorded a bad index (device status) */
+} zp_status;
+
+typedef enum { ZP_BF16 = 0, ZP_F32 = 1 } zp_dtype;
+
+/* Geometry of one layer of the paged cache [Zipage §3]. */
+typedef struct {
+    int32_t h_q;            /* query heads */
+    int32_t h_kv;           /* key/value heads; h_q % h_kv == 0 */
+    int32_t head_dim;       /* d */
+    int32_t block_size;     /* b, tokens per block */
+    int32_t n_total_blocks; /* N_total, blocks in the pool */
+    int32_t dtype;          /* zp_dtype of q, K, V, out */
+} zp_cache_desc;
+
+/* Scoring switches [Zipage App. C.2-C.8].  Recommended values (App. C.8):
+ * alpha 0.8, lambda 0.2, tau 0.4, pooling at the first compression only.  The
+ * paper gives neither the pooling kernel size nor the similarity threshold p. */
+typedef struct {
+    int32_t window;         /* w, observation window (1 <= w <= b) */
+    int32_t use_global;     /* global score, Alg. 2 */
+    float alpha;            /* decay of the global score */
+    int32_t pool_kernel;    /* odd max-pool kernel size; <= 1 disables pooling */
+    int32_t pool_policy;    /* 0 never, 1 first compression only, 2 every compression */
+    int32_t use_similarity; /* redundancy score (eq. 4) */
+    int32_t lightning;      /* 1: same-block pairs only (C.7); 0: all pairs (C.5) */
+    float threshold;        /* p: similarity above which the newest pair is zeroed */
+    float lambda;           /* weight of the redundancy score in eq. (4) */
+    float tau;              /* softmax temperature of the redundancy score (C.8) */
+} zp_score_params;
+
+/* ---- status ------------------------------------------------------------- */
+const char *zp_last_error(void);
+const char *zp_status_string(zp_status s);
+int32_t zp_version(void);
+/* Reads (and, if clear != 0, resets) the device status word of the current
+ * device: 0 = clean, else ZP_ERR_DEVICE / ZP_ERR_TIMEOUT with details in
+ * *detail (nullable).  Synchronises the current device. */
+zp_status zp_device_status(int32_t *code, int32_t *detail, int32_t clear);
+
+/* ---- decode ------------------------------------------------------------- */
+
+/* Bytes of workspace zp_paged_decode_attn needs for B sequences whose tables
+ * have table_stride entries.  The workspace is scratch: any content is fine
+ * on entry and it need not be kept between calls. */
+size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table_stride);
+
+/* Paged GQA decode attention fused with window-score accumulation
+ * [Zipage §3, §6; App. C.2 for the score].
+ *
+ * For every sequence s (L = seq_lens[s] >= 1 cached tokens, the newest one
+ * included) and query head h:
+ *     out[s][h] = sum_{t<L} softmax_t(q[s][h] . k_t / sqrt(d)) v_t
+ * q, out: [B][h_q][d] (dtype); k_cache, v_cache: one layer, paged.
+ *
+ * score_accum (nullable, float [N_total][b][h_kv]): when set, sequences whose
+ * query position P = L-1 lies in the observation window of its block
+ * (P mod b >= b - window) add (1/window) * max over the q heads of each kv
+ * head of the attention probability of every token t <= P; at the first
+ * window row (P mod b == b - window) and for t == P the value is written
+ * instead of added.  After the window steps that fill a block, S equals the
+ * observation-window score of App. C.2 computed from those queries.
+ *
+ * Limits: B <= 4096, h_kv in {2,4,8,16}, h_q/h_kv in {4,8}, d in {64,128},
+ * b a power of two >= 16.  Errors: ZP_ERR_INVALID_ARG (NULL buffer, B < 0,
+ * window outside [1, b] with score_accum set), ZP_ERR_SHAPE, ZP_ERR_DTYPE,
+ * ZP_ERR_CAPACITY (workspace_bytes too small), ZP_ERR_CUDA. */
+zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
+                               const void *v_cache, const int32_t *block_table,
+                               int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                               void *out, float *score_accum, int32_t window,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Writes the new token's key and value of each sequence into its slot
+ * [Zipage §3: the cache of a block is written into the block's slots]:
+ * k_new, v_new [B][h_kv][d] go to slot (L-1) % b of block table[(L-1)/b],
+ * where L = seq_lens[s] already counts the new token. */
+zp_status zp_append_kv(const zp_cache_desc *D, const void *k_new, const void *v_new,
+                       void *k_cache, void *v_cache, const int32_t *block_table,
+                       int32_t table_stride, const int32_t *seq_lens, int32_t B, void *stream);
+
+/* ---- compression -------------------------------------------------------- */
+
+/* Compression trigger [Zipage §4.1]: 1 iff ceil(L/b) >= max_blocks and L%b == 0. */
+int32_t zp_needs_compression(int32_t seq_len, int32_t block_size, int32_t max_blocks);
+
+size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
+
+/* Final per-token scores of n sequences of one layer, ready for the top-k
+ * [Zipage App. C.2-C.8, §4.2], in the paper's order:
+ *   S  <- score_accum gathered through the block table  (attention score)
+ *   S  <- Alg. 2 with global_F when use_global          (global score)
+ *   Sp <- MaxPool1D(S) when pooling applies              (C.4, eq. 3)
+ *   R  <- softmax_t(rho_t / (L*tau)) of the key redundancy (C.5 / C.7)
+ *   out = Sp - lambda*R, then +inf on the last `window` tokens.
+ * first_compression[n] (uint8) says whether each sequence was ever compressed
+ * (Alg. 2 branch, pooling policy).  global_F (float [N_total][b][h_kv]) is
+ * updated in place.  scores_out: float [n][h_kv][Lmax]; entries t >= L are
+ * left untouched.  Requires L <= Lmax and L >= window for every sequence. */
+zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
+                          const void *k_cache, const int32_t *block_table, int32_t table_stride,
+                          const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
+                          const float *score_accum, float *global_F, float *scores_out,
+                          int32_t Lmax, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Top-k keep set [Zipage §4.2, App. C.6]: for every (sequence, kv head) the k
+ * highest scores among t < L, equal scores ranked newer (larger t) first; the
+ * kept positions are written ascending to keep_idx [n][h_kv][k].  If L <= k all
+ * L positions are kept and keep_idx[L..k-1] = -1.  tie_count (nullable, int32
+ * [n][h_kv]) receives how many tokens share the score of the k-th kept token
+ * when that score was split between kept and dropped tokens, else 0. */
+zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const int32_t *seq_lens,
+                         int32_t n, int32_t k, int32_t *keep_idx, int32_t *tie_count,
+                         void *stream);
+
+/* KV compaction [Zipage App. C.6, Alg. 4; §4.4 target blocks]: for layers
+ * [0, layer_count) (K, V and global_F of layer l at base + l*layer_stride
+ * elements), every sequence i and kv head h, rank r < min(k, L_i) moves the row
+ * at position keep_idx[l][i][h][r] (block src_table[i][pos/b]) to slot r%b of
+ * block dst_targets[i][r/b].  The move is order preserving and safe when a
+ * target block is the source block of the same index (in place).  global_F
+ * (nullable) moves with the rows; src_table [n][table_stride],
+ * dst_targets [n][target_stride] (at least ceil(k/b) entries), keep_idx
+ * [layer_count][n][h_kv][k], seq_lens [n]. */
+zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
+                           int64_t layer_stride, int32_t layer_count, float *global_F,
+                           int64_t F_layer_stride, const int32_t *src_table, int32_t table_stride,
+                           const int32_t *dst_targets, int32_t target_stride,
+                           const int32_t *seq_lens, const int32_t *keep_idx, int32_t k,
+                           int32_t n, void *stream);
+
+/* ---- host block pool and planner (no device work) ------------------------ */
+typedef struct zp_pool zp_pool;
+
+/* Pool of n_total blocks, all free, reference count 0 [Zipage §3, §4.4]. */
+zp_pool *zp_pool_create(int32_t n_total);
+void zp_pool_destroy(zp_pool *pool);
+int32_t zp_pool_num_free(const zp_pool *pool);
+int32_t zp_pool_refcount(const zp_pool *pool, int32_t block);
+/* Takes n free blocks (reference count 1), lowest free id first.
+ * ZP_ERR_CAPACITY if fewer than n are free (nothing is taken). */
+zp_status zp_pool_alloc(zp_pool *pool, int32_t n, int32_t *ids);
+/* Adds one reference to each block (prefix sharing). */
+zp_status zp_pool_incref(zp_pool *pool, int32_t n, const int32_t *ids);
+/* Drops one reference from each block; a block reaching 0 becomes free. */
+zp_status zp_pool_release(zp_pool *pool, int32_t n, const int32_t *ids);
+
+/* Target blocks of one compression [Zipage §4.1, §4.4]: target t is a new
+ * block when table[t] is shared (reference count > 1), else table[t]; the
+ * reserved block is table[max_blocks-1] when not shared, else new.  New blocks
+ * are taken from the pool.  Outputs: targets[max_blocks-1], new_table
+ * [max_blocks] (targets + reserved), dropped[n_dropped] = the blocks of the old
+ * table that the new one no longer holds (own and shared); the caller releases
+ * them with zp_pool_release once the compaction that reads them has finished.
+ * *n_fresh = new blocks taken.  Requires n_blocks >= max_blocks >= 2. */
+zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int32_t n_blocks,
+                             int32_t max_blocks, int32_t *targets, int32_t *new_table,
+                             int32_t *dropped, int32_t *n_dropped, int32_t *n_fresh);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZP_H */

@@ -12,6 +12,14 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA path)")
 
 
+def pytest_sessionstart(session):
+    # build (or bring up to date) libzp.so and the oracle before any import
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+    import oracle
+    oracle.build()
+
+
 @pytest.fixture(scope="session")
 def orc():
     import oracle

@@ -1,0 +1,113 @@
+"""C ABI checks and host logic that need no GPU.
+
+* libzp.so loads and exports every function include/zp.h declares;
+* the trigger and the host block pool / planner agree with the oracle's
+  reading of [Zipage §4.1, §4.4] on random tables with shared prefixes;
+* calls with invalid arguments fail with the documented status before any
+  device work.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def zp():
+    import compressed_paged_kv_zp_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "zp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(zp_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports(zp):
+    assert sorted(zp.EXPORTS) == _declared()
+
+
+def test_every_declared_symbol_is_exported(zp):
+    for name in _declared():
+        assert hasattr(zp.lib, name), name
+        assert ctypes.cast(getattr(zp.lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(zp):
+    for code, name in zp.STATUS.items():
+        assert zp.lib.zp_status_string(code).decode() == name
+    assert zp.lib.zp_version() >= 1
+
+
+def test_trigger_matches_oracle(zp, orc):
+    for b in (4, 16):
+        for N_max in (2, 4, 8):
+            for L in range(0, 12 * b):
+                assert zp.zp_needs_compression(L, b, N_max) == orc.needs_compression(L, b, N_max)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_planner_matches_oracle(zp, orc, seed):
+    rng = np.random.default_rng(seed)
+    n_total = 64
+    pool = zp.Pool(n_total)
+    N_max = int(rng.integers(2, 7))
+    N = int(rng.integers(N_max, N_max + 5))
+    n_prefix = int(rng.integers(0, N + 1))
+    prefix = pool.alloc(n_prefix)
+    sharers = int(rng.integers(1, 4))
+    for _ in range(sharers - 1):
+        pool.incref(prefix)
+    own = pool.alloc(N - n_prefix)
+    table = prefix + own
+    ref = np.array([pool.refcount(i) for i in range(n_total)], dtype=np.int32)
+    free_before = pool.num_free
+    # the oracle takes fresh blocks in the order the pool hands them out
+    fresh = sorted(set(range(n_total)) - {i for i in range(n_total) if ref[i] > 0})
+    plan_o = orc.plan_targets(np.array(table, dtype=np.int32), N_max, ref,
+                              np.array(fresh, dtype=np.int32))
+    plan = pool.plan_compaction(table, N_max)
+    assert plan["targets"] == list(plan_o["targets"])
+    assert plan["new_table"] == list(plan_o["new_table"])
+    assert sorted(plan["dropped"]) == sorted(list(plan_o["released"]) + list(plan_o["dropped_shared"]))
+    assert plan["n_fresh"] == plan_o["fresh_used"] == pool.n_total - pool.num_free - (n_total - free_before)
+    # release what the sequence no longer holds: own blocks return to the pool,
+    # shared ones lose one reference
+    pool.release(plan["dropped"])
+    for blk in plan_o["released"]:
+        assert pool.refcount(int(blk)) == 0
+    for blk in plan_o["dropped_shared"]:
+        assert pool.refcount(int(blk)) == ref[blk] - 1
+    held = sum(1 for i in range(n_total) if pool.refcount(i) > 0)
+    assert held + pool.num_free == n_total  # conservation
+
+
+def test_pool_errors(zp):
+    pool = zp.Pool(4)
+    with pytest.raises(zp.ZPError) as e:
+        pool.alloc(5)
+    assert e.value.status == 4
+    ids = pool.alloc(2)
+    with pytest.raises(zp.ZPError):
+        pool.release([ids[0], ids[0]])  # over-release
+    pool.release(ids)
+    assert pool.num_free == 4
+    with pytest.raises(zp.ZPError):
+        pool.plan_compaction([0, 1], 3)  # fewer blocks than the budget
+
+
+def test_invalid_arguments_rejected_without_device(zp):
+    desc = zp.cache_desc(8, 3, 64, 16, 10, 0)  # h_q % h_kv != 0
+    rc = zp.lib.zp_append_kv(ctypes.byref(desc), None, None, None, None, None, 1, None, 1, None)
+    assert rc == 2
+    desc = zp.cache_desc(8, 2, 64, 16, 10, 9)  # bad dtype
+    rc = zp.lib.zp_select_topk(None, 2, 4, None, 1, 2, None, None, None)
+    assert rc == 1
+    rc = zp.lib.zp_compact_pages(ctypes.byref(desc), None, None, 0, 1, None, 0, None, 1, None, 1,
+                                 None, None, 4, 1, None)
+    assert rc == 3

@@ -1,0 +1,243 @@
+"""GPU parity of the compression step: scores, top-k keep sets, compaction.
+
+* zp_score_tokens vs the oracle pipeline (gather + Alg. 2 + pooling +
+  lightning redundancy + eq. 4 + window), first and later compressions,
+  duplicate-planted keys so the similarity threshold fires;
+* zp_select_topk vs the oracle on identical float scores: bit-exact, ties
+  (pooling plateaus) included, L <= k and L = k + 1;
+* zp_compact_pages vs Alg. 4 of the oracle: bit-exact bytes, in place and
+  into fresh target blocks, several layers, F moved with the rows;
+* end to end on the tiny and Qwen-shaped workloads: keep sets equal except for
+  reported swaps among near-tied scores; retained count == (N_max - 1) * b.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zp_inputs
+from oracle import pipeline
+from tests.gpu_util import TOL_SCORE, DeviceCase, gather_slots, keep_sets_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zp():
+    import compressed_paged_kv_zp_gb300 as m
+    return m
+
+
+def _desc(zp, c):
+    return zp.cache_desc(c.h_q, c.h_kv, c.d, c.b, c.n_total,
+                         torch.bfloat16 if c.dtype == "bf16" else torch.float32)
+
+
+def _block_aligned_case(seed, B, h_q, h_kv, d, b, lo, hi, dtype, dup=False, spare=0):
+    g = torch.Generator().manual_seed(seed)
+    lens = (torch.randint(lo, hi + 1, (B,), generator=g) // b * b).clamp(min=b).tolist()
+    c = zp_inputs.make_paged_case(seed, B, h_q, h_kv, d, b, lens=lens, dtype=dtype, spare_blocks=spare)
+    if dup:
+        zp_inputs.plant_duplicates(c, seed + 1)
+    return c
+
+
+SCORE_CASES = [
+    # name, B, h_q, h_kv, d, b, lo, hi, dtype, dup, first, prm
+    ("tiny_first", 4, 8, 2, 64, 16, 80, 150, "f32", False, True, {}),
+    ("tiny_dup_later", 4, 8, 2, 64, 16, 80, 150, "f32", True, False, {}),
+    ("tiny_nosim_everypool", 3, 8, 2, 64, 16, 60, 100, "f32", False, False,
+     dict(use_similarity=False, pool_policy=2)),
+    ("tiny_noglobal", 3, 8, 2, 64, 16, 60, 100, "f32", True, True, dict(use_global=False, pool_kernel=3)),
+    ("qwen_dup_first", 6, 32, 8, 128, 16, 200, 900, "bf16", True, True, {}),
+    ("qwen_later_w8", 5, 32, 8, 128, 16, 200, 600, "bf16", True, False, dict(window=8)),
+]
+
+
+@pytest.mark.parametrize("name,B,h_q,h_kv,d,b,lo,hi,dtype,dup,first,prm", SCORE_CASES)
+def test_score_tokens_matches_oracle(zp, name, B, h_q, h_kv, d, b, lo, hi, dtype, dup, first, prm):
+    seed = 300 + [x[0] for x in SCORE_CASES].index(name)
+    c = _block_aligned_case(seed, B, h_q, h_kv, d, b, lo, hi, dtype, dup)
+    dc = DeviceCase(c)
+    P = pipeline.ScoreParams(**prm)
+    params = zp.score_params(window=P.window, use_global=P.use_global, alpha=P.alpha,
+                             pool_kernel=P.pool_kernel, pool_policy=P.pool_policy,
+                             use_similarity=P.use_similarity, lightning=P.lightning, threshold=P.p,
+                             lam=P.lam, tau=P.tau)
+    rng = np.random.default_rng(seed)
+    S = torch.from_numpy((rng.random((c.n_total, b, h_kv)) / 50).astype(np.float32)).cuda()
+    F0 = (rng.random((c.n_total, b, h_kv)) / 40).astype(np.float32)
+    F = torch.from_numpy(F0).cuda()
+    Lmax = int(c.seq_lens.max()) + 5
+    out = torch.full((B, h_kv, Lmax), -7.0, device="cuda")
+    first_t = torch.full((B,), 1 if first else 0, dtype=torch.uint8, device="cuda")
+    zp.zp_score_tokens(_desc(zp, c), params, dc.K[0], dc.table, dc.lens, first_t, S, F, out)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    got = out.cpu().numpy()
+    Sg = S.cpu().numpy().astype(np.float64)
+    F_ref = F0.astype(np.float64)
+    K = dc.np_k()
+    for s in range(B):
+        L = int(c.seq_lens[s])
+        S_seq = gather_slots(Sg, c.block_table[s].numpy(), L, b)
+        ref = pipeline.final_scores(S_seq, K, F_ref, c.block_table[s].numpy(), L, b, first, P)
+        fin = np.isfinite(ref)
+        assert np.array_equal(np.isinf(got[s, :, :L]), ~fin)
+        np.testing.assert_allclose(got[s, :, :L][fin], ref[fin], **TOL_SCORE["f32"])
+        assert np.all(got[s, :, L:] == -7.0)  # untouched beyond L
+    if P.use_global:
+        np.testing.assert_allclose(F.cpu().numpy(), F_ref, rtol=1e-6, atol=0)
+
+
+TOPK_CASES = [(L, k) for L in (1, 47, 48, 49, 160, 1000, 4099) for k in (48, 112)] + [(32768, 2032)]
+
+
+@pytest.mark.parametrize("L,k", TOPK_CASES)
+def test_topk_bit_exact(zp, L, k):
+    rng = np.random.default_rng(L * 7 + k)
+    n, h_kv = 3, 2
+    Lmax = L + 3
+    sc = rng.random((n, h_kv, Lmax)).astype(np.float32)
+    sc[0, 0, : L // 2] = 0.25  # a plateau (ties) crossing the threshold
+    sc[1, 1] = np.round(sc[1, 1] * 8) / 8  # few distinct values
+    sc[2, 0, L - 16:L] = np.inf  # window
+    sc[2, 1, :L] = -sc[2, 1, :L]  # negative scores
+    lens = np.array([L, max(L - 1, 1), L], dtype=np.int32)
+    keep = torch.full((n, h_kv, k), -9, dtype=torch.int32, device="cuda")
+    ties = torch.full((n, h_kv), -1, dtype=torch.int32, device="cuda")
+    zp.zp_select_topk(torch.from_numpy(sc).cuda(), torch.from_numpy(lens).cuda(), k, keep, ties)
+    torch.cuda.synchronize()
+    got = keep.cpu().numpy()
+    for s in range(n):
+        for h in range(h_kv):
+            ref, _, cnt = oracle.topk_keep(sc[s, h, : lens[s]].astype(np.float64), k)
+            assert np.array_equal(got[s, h], ref), (s, h)
+            assert cnt == min(k, lens[s])
+    t = ties.cpu().numpy()
+    if lens[1] > k:
+        assert t[1, 1] > 1  # the quantised row has a split tie at the threshold
+    if lens[1] <= k:
+        assert t[1, 1] == 0
+
+
+def _compaction_setup(zp, seed, layers, fresh_targets):
+    b, h_kv, d, h_q = 16, 8, 128, 32
+    N_max = 4
+    k = (N_max - 1) * b
+    lens = [4 * b, 7 * b, 5 * b]
+    c = zp_inputs.make_paged_case(seed, 3, h_q, h_kv, d, b, lens=lens, dtype="bf16", layers=layers,
+                                  spare_blocks=16)
+    dc = DeviceCase(c)
+    rng = np.random.default_rng(seed)
+    keep = np.full((layers, 3, h_kv, k), -1, dtype=np.int32)
+    for l in range(layers):
+        for s, L in enumerate(lens):
+            for h in range(h_kv):
+                keep[l, s, h] = np.sort(rng.choice(L, k, replace=False))
+    free = c.free_blocks.numpy()
+    if fresh_targets:
+        tgt = free[: 3 * (N_max - 1)].reshape(3, N_max - 1)
+    else:
+        tgt = c.block_table.numpy()[:, : N_max - 1].copy()
+    F = torch.from_numpy(rng.random((layers, c.n_total, b, h_kv)).astype(np.float32)).cuda()
+    return c, dc, keep, tgt, F, k
+
+
+@pytest.mark.parametrize("layers,fresh", [(1, False), (3, False), (2, True)])
+def test_compaction_bit_exact_vs_alg4(zp, layers, fresh):
+    c, dc, keep, tgt, F, k = _compaction_setup(zp, 500 + layers, layers, fresh)
+    Kraw = dc.K.view(torch.int16).cpu().numpy().copy()
+    Vraw = dc.V.view(torch.int16).cpu().numpy().copy()
+    Fref = F.cpu().numpy().copy()
+    desc = _desc(zp, c)
+    layer_stride = c.n_total * c.b * c.h_kv * c.d
+    zp.zp_compact_pages(desc, dc.K, dc.V, layer_stride, layers, F, c.n_total * c.b * c.h_kv,
+                        dc.table, torch.from_numpy(tgt).cuda(), dc.lens, torch.from_numpy(keep).cuda(), k)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    row = c.d * 2
+    for s, L in enumerate(c.seq_lens.tolist()):
+        N = (L + c.b - 1) // c.b
+        pipeline.compact_sequence([Kraw, Vraw, Fref], [row, row, 4], c.b, c.h_kv,
+                                  c.block_table[s].numpy(), N, tgt[s], keep[:, s], L)
+    assert np.array_equal(dc.K.view(torch.int16).cpu().numpy(), Kraw)
+    assert np.array_equal(dc.V.view(torch.int16).cpu().numpy(), Vraw)
+    assert np.array_equal(F.cpu().numpy(), Fref)
+
+
+@pytest.mark.parametrize("shape", ["tiny", "qwen"])
+def test_end_to_end_compression(zp, shape):
+    """decode window -> scores -> top-k -> plan -> compaction, against the oracle."""
+    if shape == "tiny":
+        B, h_q, h_kv, d, b, N_max, dtype, lo, hi = 4, 8, 2, 64, 16, 4, "f32", 80, 150
+    else:
+        B, h_q, h_kv, d, b, N_max, dtype, lo, hi = 8, 32, 8, 128, 16, 8, "bf16", 200, 700
+    w = 16
+    c = _block_aligned_case(900 + len(shape), B, h_q, h_kv, d, b, lo, hi, dtype, dup=True, spare=B * N_max)
+    dc = DeviceCase(c)
+    desc = _desc(zp, c)
+    S = torch.zeros(c.n_total, b, h_kv, device="cuda")
+    # the last w steps of each sequence, queries from the seeded generator
+    final = c.seq_lens.tolist()
+    qw = zp_inputs.normal((B, w, h_q, d), 901, dtype)
+    for u in range(w):
+        lens_d = torch.tensor([L - w + u + 1 for L in final], dtype=torch.int32, device="cuda")
+        q = qw[:, u].contiguous().cuda()
+        zp.zp_paged_decode_attn(desc, q, dc.K[0], dc.V[0], dc.table, lens_d, torch.empty_like(q),
+                                score_accum=S, window=w)
+    F = torch.zeros_like(S)
+    Lmax = max(final)
+    scores = torch.empty(B, h_kv, Lmax, device="cuda")
+    first = torch.ones(B, dtype=torch.uint8, device="cuda")
+    params = zp.score_params(window=w)
+    zp.zp_score_tokens(desc, params, dc.K[0], dc.table, dc.lens, first, S, F, scores)
+    k = (N_max - 1) * b
+    keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
+    zp.zp_select_topk(scores, dc.lens, k, keep)
+    # host planner (no sharing): targets are the first N_max-1 blocks
+    pool = zp.Pool(c.n_total)
+    pool.alloc(c.n_total)  # everything in use; release what the table does not hold
+    held = set(int(x) for x in c.block_table.flatten().tolist() if x >= 0)
+    pool.release([i for i in range(c.n_total) if i not in held])
+    tg = np.zeros((B, N_max - 1), dtype=np.int32)
+    new_tables = []
+    for s in range(B):
+        N = final[s] // b
+        plan = pool.plan_compaction(c.block_table[s, :N].tolist(), N_max)
+        tg[s] = plan["targets"]
+        new_tables.append(plan["new_table"])
+        pool.release(plan["dropped"])
+    zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, torch.from_numpy(tg).cuda(), dc.lens,
+                        keep, k)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    # ---- oracle, same steps
+    K0 = c.k_cache[0].float().numpy()
+    V0 = c.v_cache[0].float().numpy()
+    P = pipeline.ScoreParams(window=w)
+    swaps = 0
+    Kg = dc.K[0].float().cpu().numpy()
+    Vg = dc.V[0].float().cpu().numpy()
+    kept_all = keep.cpu().numpy()
+    for s in range(B):
+        L = final[s]
+        Sref = oracle.window_score(qw[s].float().numpy(), K0, c.block_table[s].numpy(), L, w)
+        Fref = np.zeros((c.n_total, b, h_kv))
+        sref = pipeline.final_scores(Sref, K0, Fref, c.block_table[s].numpy(), L, b, True, P)
+        for h in range(h_kv):
+            kref = oracle.topk_keep(sref[h], k)[0]
+            swaps += keep_sets_match(kept_all[s, h], kref, sref[h], k, L)
+            # retained rows: GPU-moved rows equal the source rows of the GPU keep set
+            assert (kept_all[s, h] >= 0).sum() == k
+            assert set(range(L - w, L)) <= set(kept_all[s, h].tolist())  # window kept
+            src = kept_all[s, h]
+            for r in range(0, k, 7):
+                pos = src[r]
+                sb, ss = c.block_table[s, pos // b], pos % b
+                db, ds = tg[s, r // b], r % b
+                assert np.array_equal(Kg[db, ds, h], K0[sb, ss, h])
+                assert np.array_equal(Vg[db, ds, h], V0[sb, ss, h])
+        assert len(new_tables[s]) == N_max
+    print("reported tie swaps:", swaps)
+    assert pool.num_free == c.n_total - B * N_max
