@@ -28,7 +28,7 @@ STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTY
 # every symbol include/zp.h declares
 EXPORTS = [
     "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
-    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_append_kv", "zp_needs_compression",
+    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction",
@@ -75,6 +75,7 @@ def _load() -> ctypes.CDLL:
     lib.zp_decode_workspace_size.restype = SZ
     lib.zp_decode_workspace_size.argtypes = [D, I32, I32]
     lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, I32, P, SZ, P]
+    lib.zp_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, I32, P, I32, P, P, I32, P]
     lib.zp_append_kv.argtypes = [D, P, P, P, P, P, I32, P, I32, P]
     lib.zp_needs_compression.argtypes = [I32, I32, I32]
     lib.zp_score_workspace_size.restype = SZ
@@ -147,6 +148,17 @@ def zp_paged_decode_attn(desc, q, k_cache, v_cache, block_table, seq_lens, out, 
                                     table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
                                     _dev(score_accum, "score_accum"), int(window),
                                     _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def zp_paged_decode_attn_noalloc(desc, q, k_cache, v_cache, block_table, seq_lens, out,
+                                 score_accum=None, window=0, stream=None) -> None:
+    """zp_paged_decode_attn with the library's built-in scratch (no workspace)."""
+    B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    _check(lib.zp_paged_decode_attn_noalloc(ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"),
+                                            _dev(v_cache, "v_cache"), _dev(block_table, "block_table"),
+                                            table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
+                                            _dev(score_accum, "score_accum"), int(window),
+                                            _stream(stream)))
 
 
 def zp_append_kv(desc, k_new, v_new, k_cache, v_cache, block_table, seq_lens, stream=None) -> None:
@@ -260,6 +272,7 @@ class Pool:
 
 
 __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "score_params",
-           "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_append_kv",
+           "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn",
+           "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
            "zp_compact_pages", "zp_device_status", "Pool", "ZP_BF16", "ZP_F32"]

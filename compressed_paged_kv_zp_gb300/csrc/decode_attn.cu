@@ -30,6 +30,8 @@
 //     max over the GQA group and adds 1/w of it to the paged score.
 #include <math.h>
 
+#include <mutex>
+
 #include "zp_common.cuh"
 
 namespace zp {
@@ -853,4 +855,62 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
         if (d == 64 && G == 8) return launch_t<float, 64, 8>(a, p, dev, st);
     }
     return fail(ZP_ERR_SHAPE, "decode: no kernel for d=%d, group=%d", d, G);
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention without any allocation.
+//
+// For callers that cannot allocate device memory at the point where they
+// decode: for example a serving loop whose device memory is all reserved up
+// front and which may not call cudaMalloc between steps, or a plain C client
+// of this library that owns no device allocator at all.  The scratch that zp_paged_decode_attn takes from the
+// caller's workspace comes instead from one fixed array compiled into this
+// library.  Every GPU that loads the library holds that array until the
+// process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[64] = {nullptr};
+}  // namespace
+
+extern "C" zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q,
+                                                  const void *k_cache, const void *v_cache,
+                                                  const int32_t *block_table, int32_t table_stride,
+                                                  const int32_t *seq_lens, int32_t B, void *out,
+                                                  float *score_accum, int32_t window, void *stream) {
+    zp_status rc = check_desc(D);
+    if (rc != ZP_OK) return rc;
+    if (B < 0 || table_stride < 0) return fail(ZP_ERR_INVALID_ARG, "decode_noalloc: B or table_stride negative");
+    if (B == 0) return ok();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(ZP_ERR_CUDA, "decode_noalloc: device id %d out of range", dev);
+    void *scratch = nullptr;
+    {
+        // First call on a device: look up the device address of the array
+        // with that device current.  The host-side name of the array is not
+        // a device address and must never be passed to a kernel.
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_ptr[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "decode_noalloc: cudaGetSymbolAddress");
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    const size_t need = zp_decode_workspace_size(D, B, table_stride);
+    if (need == 0) return fail(ZP_ERR_SHAPE, "decode_noalloc: %s", zp_last_error());
+    if (need > kNoAllocScratchBytes)
+        return fail(ZP_ERR_CAPACITY,
+                    "decode_noalloc: this call needs %zu bytes of scratch; the built-in buffer holds "
+                    "%zu (reduce B or table_stride, or use zp_paged_decode_attn with a workspace)",
+                    need, kNoAllocScratchBytes);
+    // The arrival counters, the only part that must start at zero, are
+    // cleared on the stream by zp_paged_decode_attn itself.
+    return zp_paged_decode_attn(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out,
+                                score_accum, window, scratch, kNoAllocScratchBytes, stream);
 }

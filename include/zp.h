@@ -121,6 +121,28 @@ zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void
                                void *out, float *score_accum, int32_t window,
                                void *workspace, size_t workspace_bytes, void *stream);
 
+/* Same computation and arguments as zp_paged_decode_attn, without the
+ * workspace: for callers that cannot allocate device memory when they decode
+ * (a serving loop whose device memory is all reserved up front and which may
+ * not call cudaMalloc between steps, or a host program, such as a plain C
+ * client of this library, that has no device allocator of its own).  The paper has no
+ * counterpart; this is an interface convenience.
+ *
+ * Scratch comes from one 64 MiB array built into the library; every GPU that
+ * loads the library holds it until the process exits.  A call whose scratch
+ * need (zp_decode_workspace_size) exceeds 64 MiB fails with ZP_ERR_CAPACITY
+ * and does nothing.  No device memory is allocated by this call.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.
+ * All calls share the array and it keeps the previous call's contents (the
+ * part that must start at zero is cleared on the stream by each call), so
+ * calls that may overlap on the GPU -- on different streams, or from
+ * different threads -- race and must be ordered by the caller. */
+zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q, const void *k_cache,
+                                       const void *v_cache, const int32_t *block_table,
+                                       int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                                       void *out, float *score_accum, int32_t window, void *stream);
+
 /* Writes the new token's key and value of each sequence into its slot
  * [Zipage §3: the cache of a block is written into the block's slots]:
  * k_new, v_new [B][h_kv][d] go to slot (L-1) % b of block table[(L-1)/b],
