@@ -28,6 +28,8 @@
 //     scratch array; once every sequence's final max and sum are known, a
 //     second, fully parallel kernel turns them into probabilities, takes the
 //     max over the GQA group and adds 1/w of it to the paged score.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
@@ -631,9 +633,9 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
                     }
                 }
             }
-            // next sequence
+            // next sequence (skipping empty ones)
             if (u + 1 < u1) {
-                ++s;
+                while (u + 1 >= prefix[s + 1]) ++s;
                 seg_begin = u + 1;
                 reset_state();
                 load_q(s);
@@ -694,8 +696,397 @@ __global__ void decode_score_kernel(const DecodeArgs a) {
     }
 }
 
+// ===========================================================================
+// Tensor-core decode for bf16 caches.
+//
+// Same stream-K unit distribution, merge and score epilogue as the kernel
+// above, with both products on the tensor cores (mma.sync m16n8k16, bf16 in,
+// fp32 accumulate):
+//   S  = Q_g K^T : A = the group's queries (rows = q heads, padded to 16),
+//                  B = 16 tokens of K (from shared memory by ldmatrix);
+//   O^T += V^T P^T: A = V^T (ldmatrix.trans), B = P^T, which is exactly the
+//                  fragment the first product leaves in each lane, so P never
+//                  leaves the registers.
+// Operands come from shared memory filled by 3-D TMA tensor copies, one box
+// of 16 tokens x 64 dims per (kv head, half of d), swizzled by 128 bytes so
+// that the eight rows an ldmatrix reads sit on eight different bank groups
+// (a 1-D copy would leave the rows of one kv head 2 KB apart, all on the same
+// banks).  One consumer warp per kv head, one producer warp for the copies.
+// P is rounded to bf16 for the second product; the scores and the softmax
+// statistics stay in fp32.
+constexpr int kTcTokens = 16;     // tokens per unit (one TMA box)
+constexpr int kTcTile = 16 * 128; // bytes of one (head, half) tile: 16 rows x 128 B
+
+__host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int halves, int B) {
+    SmemLayout L;
+    int off = 0;
+    L.bar_off = off;
+    off += 2 * stages * 8;
+    L.ctl_off = off;
+    off += 16;
+    off = (off + 1023) / 1024 * 1024;  // 128-byte swizzle atoms need 1024-byte alignment
+    L.stage_off = off;
+    off += stages * 2 * h_kv * halves * kTcTile;
+    L.warp_off = off;
+    L.merge_off = off;
+    L.prefix_off = off;
+    off += (B + 1) * 4;
+    L.lens_off = off;
+    off += B * 4;
+    L.total = (off + 127) / 128 * 128 + 1024;  // + slack to align the base at run time
+    return L;
+}
+
+// Address of 16-byte chunk `chunk` (0..7) of row `row` (0..15) in a swizzled tile.
+__device__ __forceinline__ uint32_t sw128(uint32_t tile, int row, int chunk) {
+    return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(9 * 32, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const DecodeArgs a) {
+    constexpr int HALVES = D / 64;
+    constexpr int KS = D / 16;  // k-steps of Q K^T = m-tiles of V^T P^T
+    static_assert(G >= 1 && G <= 8, "group of at most 8 q heads");
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the swizzled tiles need 1024-byte aligned shared addresses
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int B = a.B;
+    const int h_kv = a.h_kv;
+    const SmemLayout lay = make_tc_layout(a.stages, h_kv, HALVES, B);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
+    uint64_t *empty = full + a.stages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.ctl_off);
+    volatile int *last_flag = abort_flag + 1;
+    int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
+    int *lens = reinterpret_cast<int *>(smem + lay.lens_off);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int stage_bytes = 2 * h_kv * HALVES * kTcTile;  // K then V
+
+    for (int s = tid; s < B; s += blockDim.x) {
+        int L = a.seq_lens[s];
+        if (L < 0) {
+            record_error(a.err, ZP_ERR_DEVICE, 1);
+            L = 0;
+        }
+        const int maxL = a.table_stride * a.b;
+        if (L > maxL) {
+            record_error(a.err, ZP_ERR_DEVICE, 2);
+            L = maxL;
+        }
+        lens[s] = L;
+    }
+    if (tid == 0) {
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], h_kv);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < B; base += 32) {
+            const int s = base + lane;
+            const int n = s < B ? (lens[s] + kTcTokens - 1) / kTcTokens : 0;
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (s < B) prefix[s] = carry + x - n;
+            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
+        if (lane == 0) prefix[B] = carry;
+    }
+    __syncthreads();
+    const long long U = prefix[B];
+    if (blockIdx.x == 0)
+        for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
+    if (a.want_score && U > a.logits_units) {
+        if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 3);
+        return;
+    }
+    const int Gd = gridDim.x;
+    const long long u0 = cta_start(blockIdx.x, U, Gd);
+    const long long u1 = cta_start(blockIdx.x + 1, U, Gd);
+    if (u0 >= u1) return;
+    int s_first = 0;
+    {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= u0) lo = mid;
+            else hi = mid - 1;
+        }
+        s_first = lo;
+    }
+    unsigned char *stage_base = smem + lay.stage_off;
+
+    // =====================================================================
+    // producer warp: TMA copies of K and V for every unit of the range
+    if (warp == h_kv) {
+        if (lane == 0) {
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+            const uint64_t pol = l2_evict_first_policy();
+            const unsigned bytes = (unsigned)stage_bytes;
+            int s = s_first;
+            for (long long u = u0, i = 0; u < u1; ++u, ++i) {
+                while (u >= prefix[s + 1]) ++s;
+                const int st = (int)(i % a.stages);
+                if (i >= a.stages &&
+                    !mbar_wait_bounded(&empty[st], (unsigned)(((i / a.stages) - 1) & 1), a.err, abort_flag,
+                                       30))
+                    break;
+                const int tok0 = (int)(u - prefix[s]) * kTcTokens;
+                const int blk = __ldg(&a.table[(size_t)s * a.table_stride + tok0 / a.b]);
+                if (blk < 0 || blk >= a.n_total) {
+                    record_error(a.err, ZP_ERR_DEVICE, 4);
+                    mbar_arrive_expect_tx(&full[st], 0);
+                    continue;
+                }
+                const int row = blk * a.b + (tok0 % a.b);
+                unsigned char *ks = stage_base + (size_t)st * stage_bytes;
+                unsigned char *vs = ks + stage_bytes / 2;
+                mbar_arrive_expect_tx(&full[st], bytes);
+                for (int h = 0; h < h_kv; ++h)
+#pragma unroll
+                    for (int hf = 0; hf < HALVES; ++hf) {
+                        const int t = h * HALVES + hf;
+                        tma_load_3d(ks + t * kTcTile, &tmk, hf * 64, h, row, &full[st], pol);
+                        tma_load_3d(vs + t * kTcTile, &tmv, hf * 64, h, row, &full[st], pol);
+                    }
+            }
+        }
+        return;
+    }
+
+    // =====================================================================
+    // consumer warp `warp` = kv head
+    const int kvh = warp;
+    const int g = lane >> 2;    // fragment row group
+    const int tig = lane & 3;   // thread in group
+    const int h0 = kvh * G;
+    const int ncw_threads = h_kv * 32;
+    // ldmatrix row/chunk of this lane: matrix m = lane/8 -> tokens (m/2)*8.., chunk +(m&1)
+    const int lm = lane >> 3;
+    const int lrow = (lm >> 1) * 8 + (lane & 7);
+    const int lchunk = lm & 1;
+
+    uint32_t qa[KS][2];
+    float acc[KS][4];
+    float m_run, l_run;
+    auto reset_state = [&]() {
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int t = 0; t < KS; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
+    };
+    auto load_q = [&](int s) {
+        const uint32_t *qg = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(a.q) +
+                                                              ((size_t)s * a.h_q + h0 + g) * D);
+#pragma unroll
+        for (int t = 0; t < KS; ++t) {
+            qa[t][0] = g < G ? qg[(16 * t + 2 * tig) / 2] : 0u;
+            qa[t][1] = g < G ? qg[(16 * t + 8 + 2 * tig) / 2] : 0u;
+        }
+    };
+    auto compute_window = [&](int seq) {
+        const int P = lens[seq] - 1;
+        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window;
+    };
+
+    int s = s_first;
+    long long seg_begin = u0;
+    reset_state();
+    load_q(s);
+    bool window_step = compute_window(s);
+
+    for (long long u = u0, i = 0; u < u1; ++u, ++i) {
+        const int st = (int)(i % a.stages);
+        const bool got = mbar_wait_bounded(&full[st], (unsigned)((i / a.stages) & 1), a.err, abort_flag, 40);
+        int valid = lens[s] - (int)(u - prefix[s]) * kTcTokens;
+        if (valid > kTcTokens) valid = kTcTokens;
+        if (!got) valid = 0;
+        unsigned char *ks = stage_base + (size_t)st * stage_bytes + kvh * HALVES * kTcTile;
+        unsigned char *vs = ks + stage_bytes / 2;
+        if (valid > 0) {
+            if (valid < kTcTokens) {
+                // rows past the sequence end hold whatever the block had: zero
+                // them in V so that 0 * garbage cannot produce a NaN
+                for (int c = lane; c < (kTcTokens - valid) * 8 * HALVES; c += 32) {
+                    const int hf = c / ((kTcTokens - valid) * 8);
+                    const int rem = c % ((kTcTokens - valid) * 8);
+                    const int row = valid + rem / 8;
+                    reinterpret_cast<uint4 *>(vs + hf * kTcTile + row * 128)[rem % 8] = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            const uint32_t kt = smem_u32(ks);
+            const uint32_t vt = smem_u32(vs);
+            // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
+            float sc0[4] = {0.f, 0.f, 0.f, 0.f}, sc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(sw128(kt + (t >> 2) * kTcTile, lrow, (t & 3) * 2 + lchunk), b0, b1, b2, b3);
+                mma_16816(sc0, qa[t][0], 0u, qa[t][1], 0u, b0, b1);
+                mma_16816(sc1, qa[t][0], 0u, qa[t][1], 0u, b2, b3);
+            }
+            // lane holds S[head g][tokens 2tig, 2tig+1] (sc0) and [8+2tig, 9+2tig] (sc1)
+            float x[4];
+            x[0] = sc0[0] * a.qscale;
+            x[1] = sc0[1] * a.qscale;
+            x[2] = sc1[0] * a.qscale;
+            x[3] = sc1[1] * a.qscale;
+            const int tk[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (g >= G || tk[e] >= valid) x[e] = -INFINITY;
+            if (window_step && g < G) {
+                float *lg = a.logits + ((size_t)u * kTcTokens) * a.h_q + h0 + g;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (tk[e] < valid) lg[(size_t)tk[e] * a.h_q] = x[e];
+            }
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            float p[4], rs = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p[e] = (x[e] == -INFINITY) ? 0.f : exp2f(x[e] - m_new);
+                rs += p[e];
+            }
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 1);
+            rs += __shfl_xor_sync(0xFFFFFFFFu, rs, 2);
+            l_run = l_run * alpha + rs;
+            m_run = m_new;
+            const uint32_t pb0 = f2_to_bf2(p[0], p[1]);
+            const uint32_t pb1 = f2_to_bf2(p[2], p[3]);
+            // accumulator columns are heads 2tig, 2tig+1: their rescale factors
+            const float a_lo = __shfl_sync(0xFFFFFFFFu, alpha, (2 * tig) * 4);
+            const float a_hi = __shfl_sync(0xFFFFFFFFu, alpha, (2 * tig + 1) * 4);
+            // ---- O^T += V^T P^T, one m-tile of 16 dims at a time
+#pragma unroll
+            for (int t = 0; t < KS; ++t) {
+                acc[t][0] *= a_lo;
+                acc[t][1] *= a_hi;
+                acc[t][2] *= a_lo;
+                acc[t][3] *= a_hi;
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(sw128(vt + (t >> 2) * kTcTile, lrow, (t & 3) * 2 + lchunk), v0, v1, v2, v3);
+                mma_16816(acc[t], v0, v1, v2, v3, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        const bool seq_ends = (u + 1 == prefix[s + 1]);
+        if (seq_ends || u + 1 == u1) {
+            // l and m of the heads 2tig, 2tig+1 owned by this lane's columns
+            const float l_lo = __shfl_sync(0xFFFFFFFFu, l_run, (2 * tig) * 4);
+            const float l_hi = __shfl_sync(0xFFFFFFFFu, l_run, (2 * tig + 1) * 4);
+            const int hc0 = 2 * tig, hc1 = 2 * tig + 1;  // column heads
+            const bool whole = (prefix[s] >= seg_begin) && seq_ends;
+            if (whole) {
+                __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)s * a.h_q + h0) * D;
+                const float i0 = l_lo > 0.f ? 1.f / l_lo : 0.f;
+                const float i1 = l_hi > 0.f ? 1.f / l_hi : 0.f;
+#pragma unroll
+                for (int t = 0; t < KS; ++t) {
+                    const int d0 = 16 * t + g;
+                    if (hc0 < G) {
+                        og[(size_t)hc0 * D + d0] = __float2bfloat16_rn(acc[t][0] * i0);
+                        og[(size_t)hc0 * D + d0 + 8] = __float2bfloat16_rn(acc[t][2] * i0);
+                    }
+                    if (hc1 < G) {
+                        og[(size_t)hc1 * D + d0] = __float2bfloat16_rn(acc[t][1] * i1);
+                        og[(size_t)hc1 * D + d0 + 8] = __float2bfloat16_rn(acc[t][3] * i1);
+                    }
+                }
+                if (a.want_score && g < G && tig == 0)
+                    a.stats[(size_t)s * a.h_q + h0 + g] = make_float2(m_run, l_run);
+            } else {
+                const int slot = 2 * blockIdx.x + ((prefix[s] <= u0) ? 0 : 1);
+                float *pa = a.part_acc + ((size_t)slot * a.h_q + h0) * D;
+#pragma unroll
+                for (int t = 0; t < KS; ++t) {
+                    const int d0 = 16 * t + g;
+                    if (hc0 < G) {
+                        pa[(size_t)hc0 * D + d0] = acc[t][0];
+                        pa[(size_t)hc0 * D + d0 + 8] = acc[t][2];
+                    }
+                    if (hc1 < G) {
+                        pa[(size_t)hc1 * D + d0] = acc[t][1];
+                        pa[(size_t)hc1 * D + d0 + 8] = acc[t][3];
+                    }
+                }
+                if (g < G && tig == 0) a.part_ml[(size_t)slot * a.h_q + h0 + g] = make_float2(m_run, l_run);
+                __threadfence();
+                named_bar_sync(1, ncw_threads);
+                if (tid == 0) {
+                    const int nseg = (int)(u + 1 - seg_begin);
+                    const int ntot = prefix[s + 1] - prefix[s];
+                    const int before = atomicAdd(&a.seq_count[s], nseg);
+                    *last_flag = (before + nseg == ntot) ? 1 : 0;
+                }
+                named_bar_sync(1, ncw_threads);
+                if (*last_flag) {
+                    __threadfence();
+                    const int c_lo = cta_of(prefix[s], U, Gd);
+                    const int c_hi = cta_of(prefix[s + 1] - 1, U, Gd);
+                    for (int e = tid; e < a.h_q * D; e += ncw_threads) {
+                        const int h = e / D;
+                        const int dd = e % D;
+                        float M = -INFINITY;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const long long cs = cta_start(c, U, Gd);
+                            if (cs == cta_start(c + 1, U, Gd)) continue;
+                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
+                            M = fmaxf(M, __ldcg(&a.part_ml[(size_t)sl * a.h_q + h].x));
+                        }
+                        float Ls = 0.f, A = 0.f;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const long long cs = cta_start(c, U, Gd);
+                            if (cs == cta_start(c + 1, U, Gd)) continue;
+                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
+                            const float2 ml = __ldcg(&a.part_ml[(size_t)sl * a.h_q + h]);
+                            const float f = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                            Ls += ml.y * f;
+                            A += __ldcg(&a.part_acc[((size_t)sl * a.h_q + h) * D + dd]) * f;
+                        }
+                        static_cast<__nv_bfloat16 *>(a.out)[((size_t)s * a.h_q + h) * D + dd] =
+                            __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
+                        if (a.want_score && dd == 0) a.stats[(size_t)s * a.h_q + h] = make_float2(M, Ls);
+                    }
+                }
+            }
+            if (u + 1 < u1) {
+                while (u + 1 >= prefix[s + 1]) ++s;
+                seg_begin = u + 1;
+                reset_state();
+                load_q(s);
+                window_step = compute_window(s);
+            }
+        }
+    }
+}
+
 struct Plan {
-    int T, wph, ncw, stages, smem, grid;
+    bool tc;  // tensor-core kernel (bf16) or CUDA-core kernel
+    int T, wph, ncw, threads, stages, smem, grid;
     size_t off_count, off_prefix, off_stats, off_pml, off_pacc, off_logits, total;
     long long logits_units;
 };
@@ -706,31 +1097,45 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     const int d = D->head_dim, b = D->block_size, h_kv = D->h_kv;
     const int G = D->h_q / D->h_kv;
     if (!(d == 64 || d == 128)) return fail(ZP_ERR_SHAPE, "decode: head_dim %d not in {64,128}", d);
-    if (!(G == 4 || G == 8)) return fail(ZP_ERR_SHAPE, "decode: group size %d not in {4,8}", G);
-    if (!(h_kv == 2 || h_kv == 4 || h_kv == 8 || h_kv == 16))
-        return fail(ZP_ERR_SHAPE, "decode: h_kv %d not in {2,4,8,16}", h_kv);
     if (b < 16 || (b & (b - 1))) return fail(ZP_ERR_SHAPE, "decode: block size %d", b);
     if (B > kMaxB) return fail(ZP_ERR_SHAPE, "decode: B %d > %d", B, kMaxB);
-    const int row = h_kv * d * es;
-    int T = b;
-    while (T > 8 && T * row > kStageBytesCap) T >>= 1;
-    if (T * row > kStageBytesCap) return fail(ZP_ERR_SHAPE, "decode: row of %d bytes too large", row);
-    int wph = T / 8;
-    if (wph > kMaxConsumerWarps / h_kv) wph = kMaxConsumerWarps / h_kv;
-    if (wph < 1) wph = 1;
-    p->T = T;
-    p->wph = wph;
-    p->ncw = h_kv * wph;
     p->grid = dev.sm_count;
-    const int stage_bytes = T * row;
-    int stages = 4;
-    while (stages > 2 &&
-           make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total > dev.smem_optin)
-        --stages;
-    p->stages = stages;
-    p->smem = make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total;
+    p->tc = D->dtype == ZP_BF16 && (h_kv == 1 || h_kv == 2 || h_kv == 4 || h_kv == 8) &&
+            (G == 1 || G == 2 || G == 4 || G == 8);
+    if (p->tc) {
+        p->T = kTcTokens;
+        p->wph = 1;
+        p->ncw = h_kv;
+        p->threads = (h_kv + 1) * 32;
+        int stages = 4;
+        while (stages > 2 && make_tc_layout(stages, h_kv, d / 64, B).total > dev.smem_optin) --stages;
+        p->stages = stages;
+        p->smem = make_tc_layout(stages, h_kv, d / 64, B).total;
+    } else {
+        if (!(G == 4 || G == 8)) return fail(ZP_ERR_SHAPE, "decode: group size %d not in {4,8}", G);
+        if (!(h_kv == 2 || h_kv == 4 || h_kv == 8 || h_kv == 16))
+            return fail(ZP_ERR_SHAPE, "decode: h_kv %d not in {2,4,8,16}", h_kv);
+        const int row = h_kv * d * es;
+        int T = b;
+        while (T > 8 && T * row > kStageBytesCap) T >>= 1;
+        if (T * row > kStageBytesCap) return fail(ZP_ERR_SHAPE, "decode: row of %d bytes too large", row);
+        int wph = T / 8;
+        if (wph > kMaxConsumerWarps / h_kv) wph = kMaxConsumerWarps / h_kv;
+        if (wph < 1) wph = 1;
+        p->T = T;
+        p->wph = wph;
+        p->ncw = h_kv * wph;
+        p->threads = p->ncw * 32;
+        const int stage_bytes = T * row;
+        int stages = 4;
+        while (stages > 2 &&
+               make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total > dev.smem_optin)
+            --stages;
+        p->stages = stages;
+        p->smem = make_layout(stages, stage_bytes, p->ncw, h_kv, G, d, B).total;
+    }
     if (p->smem > dev.smem_optin) return fail(ZP_ERR_SHAPE, "decode: needs %d B of shared memory", p->smem);
-    const long long units_cap = (long long)B * table_stride * (b / T);
+    const long long units_cap = (long long)B * table_stride * (b / p->T);
     p->logits_units = units_cap;
     size_t off = 0;
     p->off_count = off;
@@ -744,8 +1149,68 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     p->off_pacc = off;
     off = align_up(off + (size_t)2 * p->grid * D->h_q * d * 4, 256);
     p->off_logits = off;
-    off = align_up(off + (size_t)units_cap * T * D->h_q * 4, 256);
+    off = align_up(off + (size_t)units_cap * p->T * D->h_q * 4, 256);
     p->total = off;
+    return ZP_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map over one layer of a bf16 cache viewed as [N_total*b][h_kv][d]:
+// boxes of 16 tokens x 1 head x 64 dims, 128-byte swizzle.
+zp_status encode_cache_map(CUtensorMap *m, const void *base, const zp_cache_desc *D) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(ZP_ERR_CUDA, "decode: cuTensorMapEncodeTiled unavailable");
+    if (reinterpret_cast<uintptr_t>(base) % 16) return fail(ZP_ERR_INVALID_ARG, "decode: cache not 16-byte aligned");
+    const cuuint64_t dims[3] = {(cuuint64_t)D->head_dim, (cuuint64_t)D->h_kv,
+                                (cuuint64_t)D->n_total_blocks * (cuuint64_t)D->block_size};
+    const cuuint64_t strides[2] = {(cuuint64_t)D->head_dim * 2, (cuuint64_t)D->h_kv * D->head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcTokens};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ZP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ZP_OK;
+}
+
+template <int Dd, int G>
+zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cudaStream_t st,
+                    const zp_cache_desc *D) {
+    static int configured_smem[64] = {0};
+    auto kmain = decode_tc_kernel<Dd, G>;
+    const int dv = dev.device < 64 ? dev.device : 63;
+    if (configured_smem[dv] < p.smem) {
+        cudaError_t e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+        if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
+        configured_smem[dv] = p.smem;
+    }
+    CUtensorMap mk, mv;
+    zp_status rc = encode_cache_map(&mk, a.k, D);
+    if (rc != ZP_OK) return rc;
+    rc = encode_cache_map(&mv, a.v, D);
+    if (rc != ZP_OK) return rc;
+    kmain<<<p.grid, p.threads, p.smem, st>>>(mk, mv, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel launch");
+    if (a.want_score) {
+        decode_score_kernel<G><<<p.grid * 8, 128, (a.B + 1) * 4, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
+    }
     return ZP_OK;
 }
 
@@ -759,7 +1224,7 @@ zp_status launch_t(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cu
         if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
         configured_smem[dv] = p.smem;
     }
-    kmain<<<p.grid, p.ncw * 32, p.smem, st>>>(a);
+    kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: main kernel launch");
     if (a.want_score) {
@@ -843,6 +1308,16 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     if (e != cudaSuccess) return cuda_fail(e, "decode: memset of arrival counters");
     const int G = D->h_q / D->h_kv;
     const int d = D->head_dim;
+    if (p.tc) {
+        if (d == 128 && G == 4) return launch_tc<128, 4>(a, p, dev, st, D);
+        if (d == 128 && G == 8) return launch_tc<128, 8>(a, p, dev, st, D);
+        if (d == 128 && G == 2) return launch_tc<128, 2>(a, p, dev, st, D);
+        if (d == 128 && G == 1) return launch_tc<128, 1>(a, p, dev, st, D);
+        if (d == 64 && G == 4) return launch_tc<64, 4>(a, p, dev, st, D);
+        if (d == 64 && G == 8) return launch_tc<64, 8>(a, p, dev, st, D);
+        if (d == 64 && G == 2) return launch_tc<64, 2>(a, p, dev, st, D);
+        if (d == 64 && G == 1) return launch_tc<64, 1>(a, p, dev, st, D);
+    }
     if (D->dtype == ZP_BF16) {
         if (d == 128 && G == 4) return launch_t<__nv_bfloat16, 128, 4>(a, p, dev, st);
         if (d == 128 && G == 8) return launch_t<__nv_bfloat16, 128, 8>(a, p, dev, st);
