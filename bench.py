@@ -166,8 +166,11 @@ class Workload:
             self.c_ws = torch.empty(max(zp.zp_score_workspace_size(self.desc, n, self.c_Lmax), 1),
                                     dtype=torch.uint8, device=dev)
             self.params = zp.score_params(window=self.w)
-            self.c_targets = torch.tensor([self._plan(s)["targets"] for s in self.comp], dtype=torch.int32,
-                                          device=dev)
+            self.c_tables_np = c.block_table[idx].numpy().copy()
+            self.c_nblocks_np = (c.seq_lens[idx] // b).numpy().astype(np.int32)
+            plan = self.pool.plan_compaction_batch(self.c_tables_np, self.c_nblocks_np, N_max)
+            self.plan_out = plan
+            self.c_targets = torch.from_numpy(plan["targets"].copy()).to(dev)
         # pinned host copies for the end-to-end figure
         self.host_q = self.q.cpu().pin_memory()
         self.h_k_new = self.k_new.cpu().pin_memory()
@@ -215,8 +218,10 @@ class Workload:
         if not self.n_comp:
             return
         zp = self.zp
-        for s in self.comp:  # host planning (a11); identical plans each step
-            self._plan(s)
+        # host planning (a11), one C call for all triggered sequences; the batch
+        # is stationary, so the plans (and the uploaded targets) are the same
+        # every step
+        self.pool.plan_compaction_batch(self.c_tables_np, self.c_nblocks_np, self.N_max, out=self.plan_out)
         zp.zp_score_tokens(self.desc, self.params, self.K, self.c_table, self.c_lens, self.c_first, self.S,
                            self.F, self.c_scores, workspace=self.c_ws, stream=stream)
         zp.zp_select_topk(self.c_scores, self.c_lens, self.k, self.c_keep, stream=stream)

@@ -31,7 +31,7 @@ EXPORTS = [
     "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
-    "zp_pool_incref", "zp_pool_release", "zp_plan_compaction",
+    "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
 ]
 
 
@@ -93,6 +93,7 @@ def _load() -> ctypes.CDLL:
     lib.zp_pool_incref.argtypes = [P, I32, P]
     lib.zp_pool_release.argtypes = [P, I32, P]
     lib.zp_plan_compaction.argtypes = [P, P, I32, I32, P, P, P, P, P]
+    lib.zp_plan_compaction_batch.argtypes = [P, P, I32, P, I32, I32, P, P, P, P, P]
     return lib
 
 
@@ -269,6 +270,26 @@ class Pool:
                                       dropped, ctypes.byref(nd), ctypes.byref(nf)))
         return {"targets": list(targets)[: max_blocks - 1], "new_table": list(new_table)[:max_blocks],
                 "dropped": list(dropped)[: nd.value], "n_fresh": nf.value}
+
+    def plan_compaction_batch(self, tables, n_blocks, max_blocks: int, out=None):
+        """Plans of n sequences in one C call; tables int32 [n][stride] and
+        n_blocks int32 [n] as numpy arrays.  Returns numpy arrays (reused from
+        ``out`` when given): targets [n][max_blocks-1], new_tables
+        [n][max_blocks], dropped [n][stride], n_dropped [n], n_fresh [n]."""
+        import numpy as np
+        tables = np.ascontiguousarray(tables, dtype=np.int32)
+        n_blocks = np.ascontiguousarray(n_blocks, dtype=np.int32)
+        n, stride = tables.shape
+        if out is None:
+            out = {"targets": np.empty((n, max_blocks - 1), np.int32),
+                   "new_tables": np.empty((n, max_blocks), np.int32),
+                   "dropped": np.empty((n, stride), np.int32), "n_dropped": np.empty(n, np.int32),
+                   "n_fresh": np.empty(n, np.int32)}
+        P = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        _check(lib.zp_plan_compaction_batch(self._p, P(tables), stride, P(n_blocks), n, int(max_blocks),
+                                            P(out["targets"]), P(out["new_tables"]), P(out["dropped"]),
+                                            P(out["n_dropped"]), P(out["n_fresh"])))
+        return out
 
 
 __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "score_params",

@@ -7,7 +7,7 @@
 // target block r / b.
 //
 // One CTA per (kv head, sequence, layer).  Alg. 4 walks one slot at a time;
-// here a CTA moves a chunk of kChunk ranks at once: every thread first loads
+// here a CTA moves a chunk of up to 128 ranks at once: every thread first loads
 // its share of the chunk's source rows (16-byte vectors) into registers, the
 // CTA synchronises, then the rows are stored.  Rank r's source position is
 // >= r, so a chunk's stores (positions < chunk end) never overwrite a source
@@ -18,9 +18,9 @@
 namespace zp {
 namespace {
 
-constexpr int kChunk = 32;
+constexpr int kChunkMax = 128;       // ranks per load/store round (at most)
 constexpr int kThreads = 256;
-constexpr int kMaxVecPerThread = 8;  // kChunk * row_vec * 2 / kThreads
+constexpr int kMaxVecPerThread = 16;  // registers of 16 bytes per thread and round
 
 struct CompactArgs {
     uint4 *K;
@@ -36,6 +36,7 @@ struct CompactArgs {
     const int32_t *keep;
     int k, n, h_kv, b, n_total;
     int row_vec;  // vectors per (token, kv head) row = d * elem / 16
+    int chunk;    // ranks per round: min(kChunkMax, kThreads * kMaxVecPerThread / (2 * row_vec))
     unsigned *err;
 };
 
@@ -51,8 +52,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     uint4 *V = a.V + layer * a.layer_stride_vec;
     float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
     const int per_rank = 2 * a.row_vec;  // K then V vectors
-    for (int r0 = 0; r0 < kk; r0 += kChunk) {
-        const int nr = min(kChunk, kk - r0);
+    for (int r0 = 0; r0 < kk; r0 += a.chunk) {
+        const int nr = min(a.chunk, kk - r0);
         const int items = nr * per_rank;
         uint4 buf[kMaxVecPerThread];
         float fbuf = 0.f;
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
                 }
             }
         }
-        if (F && threadIdx.x < nr) {
+        if (F && threadIdx.x < nr) {  // nr <= kChunkMax <= kThreads
             const int pos = kp[r0 + threadIdx.x];
             if (pos >= 0 && pos < L) {
                 const int blk = a.src_table[(size_t)s * a.table_stride + pos / a.b];
@@ -139,8 +140,9 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     if ((layer_stride * es) % 16) return fail(ZP_ERR_INVALID_ARG, "compact: layer_stride not 16-byte aligned");
     if (((uintptr_t)k_base | (uintptr_t)v_base) % 16) return fail(ZP_ERR_INVALID_ARG, "compact: unaligned cache");
     const int row_vec = (int)(row_bytes / 16);
-    if (kChunk * 2 * row_vec > kThreads * kMaxVecPerThread)
-        return fail(ZP_ERR_SHAPE, "compact: head_dim %d too large", D->head_dim);
+    int chunk = kThreads * kMaxVecPerThread / (2 * row_vec);
+    if (chunk > kChunkMax) chunk = kChunkMax;
+    if (chunk < 1) return fail(ZP_ERR_SHAPE, "compact: head_dim %d too large", D->head_dim);
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
@@ -162,6 +164,7 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     a.b = D->block_size;
     a.n_total = D->n_total_blocks;
     a.row_vec = row_vec;
+    a.chunk = chunk;
     a.err = dev.error_word;
     dim3 grid(D->h_kv, n, layer_count);
     compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);

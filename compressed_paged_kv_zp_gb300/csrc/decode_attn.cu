@@ -66,8 +66,8 @@ struct DecodeArgs {
     float2 *stats;     // [B][h_q] final (max, sum), log2 units
     float *part_acc;   // [2*grid][h_q][D]
     float2 *part_ml;   // [2*grid][h_q]
-    int *seq_count;    // [B], zero on entry
     int *unit_prefix;  // [B+1]
+    int2 *unit_info;   // [units]: (sequence, first token) of every unit
     long long logits_units;  // capacity of `logits` in units
     unsigned *err;
 };
@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + a.stages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.ctl_off);
-    volatile int *last_flag = abort_flag + 1;
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
     int *lens = reinterpret_cast<int *>(smem + lay.lens_off);
 
@@ -304,6 +303,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
         int valid = lens[ps] - tok0;
         if (valid > TU) valid = TU;
         const int blk = __ldg(&a.table[(size_t)ps * a.table_stride + tok0 / a.b]);
+        if (a.want_score) a.unit_info[u] = make_int2(ps, tok0);
         unsigned char *ks = stage_base + (size_t)st * 2 * stage_bytes;
         unsigned char *vs = ks + stage_bytes;
         if (blk < 0 || blk >= a.n_total) {
@@ -591,47 +591,6 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
                             a.part_ml[(size_t)slot * a.h_q + h0 + j] = make_float2(m[j], l[j]);
                     }
                 }
-                __threadfence();
-                named_bar_sync(1, ncw_threads);
-                if (tid == 0) {
-                    const int nseg = (int)(u + 1 - seg_begin);
-                    const int ntot = prefix[s + 1] - prefix[s];
-                    const int before = atomicAdd(&a.seq_count[s], nseg);
-                    *last_flag = (before + nseg == ntot) ? 1 : 0;
-                }
-                named_bar_sync(1, ncw_threads);
-                if (*last_flag) {
-                    __threadfence();
-                    const int c_lo = cta_of(prefix[s], U, Gd);
-                    const int c_hi = cta_of(prefix[s + 1] - 1, U, Gd);
-                    // every consumer thread merges some (head, dim) elements
-                    for (int e = tid; e < a.h_q * D; e += ncw_threads) {
-                        const int h = e / D;
-                        const int dd = e % D;
-                        float M = -INFINITY;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const long long cs = cta_start(c, U, Gd);
-                            if (cs == cta_start(c + 1, U, Gd)) continue;  // empty range: no record
-                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
-                            M = fmaxf(M, __ldcg(&a.part_ml[(size_t)sl * a.h_q + h].x));
-                        }
-                        float Ls = 0.f, A = 0.f;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const long long cs = cta_start(c, U, Gd);
-                            if (cs == cta_start(c + 1, U, Gd)) continue;
-                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
-                            const float2 ml = __ldcg(&a.part_ml[(size_t)sl * a.h_q + h]);
-                            const float f = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                            Ls += ml.y * f;
-                            A += __ldcg(&a.part_acc[((size_t)sl * a.h_q + h) * D + dd]) * f;
-                        }
-                        const float o = Ls > 0.f ? A / Ls : 0.f;
-                        T *og = static_cast<T *>(a.out) + ((size_t)s * a.h_q + h) * D + dd;
-                        if constexpr (sizeof(T) == 2) *og = __float2bfloat16_rn(o);
-                        else *og = o;
-                        if (a.want_score && dd == 0) a.stats[(size_t)s * a.h_q + h] = make_float2(M, Ls);
-                    }
-                }
             }
             // next sequence (skipping empty ones)
             if (u + 1 < u1) {
@@ -645,54 +604,62 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
     }
 }
 
-// Window-score epilogue: one thread per (token, kv head) of window-step
-// sequences.  p_h(t) = 2^(logit - m_h) / l_h; S += (1/w) max_h p_h(t).
+// Window-score epilogue: one block per unit, one thread per (token, kv head)
+// of window-step sequences.  p_h(t) = 2^(logit - m_h) / l_h;
+// S += (1/w) max over the group of p_h(t) (written at the first window row
+// and for the newest token).  Each unit's sequence and first token come from
+// the main kernel, so a thread's chain of dependent loads is short and the
+// thousands of blocks keep the memory system busy.
 template <int G>
 __global__ void decode_score_kernel(const DecodeArgs a) {
-    extern __shared__ int pre[];  // unit prefix [B+1]
-    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) pre[i] = a.unit_prefix[i];
-    __syncthreads();
-    const int U = pre[a.B];
-    const int items = a.T * a.h_kv;
+    const int u = blockIdx.x;
+    const int U = __ldg(&a.unit_prefix[a.B]);
+    if (u >= U) return;
+    const int2 info = a.unit_info[u];
+    const int s = info.x;
+    int L = __ldg(&a.seq_lens[s]);
+    if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    const int P = L - 1;
+    if (P < 0) return;
+    const int r = P % a.b;
+    if (r < a.b - a.window) return;  // not a window step
+    const bool first_row = (r == a.b - a.window);
     const float inv_w = 1.f / (float)a.window;
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        int lo = 0, hi = a.B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= u) lo = mid;
-            else hi = mid - 1;
-        }
-        const int s = lo;
-        int L = a.seq_lens[s];
-        if (L > a.table_stride * a.b) L = a.table_stride * a.b;
-        const int P = L - 1;
-        if (P < 0) continue;
-        const int r = P % a.b;
-        if (r < a.b - a.window) continue;  // block-uniform
-        const bool first_row = (r == a.b - a.window);
-        for (int it = threadIdx.x; it < items; it += blockDim.x) {
-            const int tl = it / a.h_kv;
-            const int kvh = it % a.h_kv;
-            const int tok = (u - pre[s]) * a.T + tl;
-            if (tok >= L) continue;
-            const float *lg = a.logits + ((size_t)u * a.T + tl) * a.h_q + kvh * G;
-            const float2 *st = a.stats + (size_t)s * a.h_q + kvh * G;
-            float best = 0.f;
+    for (int it = threadIdx.x; it < a.T * a.h_kv; it += blockDim.x) {
+        const int tl = it / a.h_kv;
+        const int kvh = it % a.h_kv;
+        const int tok = info.y + tl;
+        if (tok >= L) continue;
+        const int blk = __ldg(&a.table[(size_t)s * a.table_stride + tok / a.b]);
+        const float *lg = a.logits + ((size_t)u * a.T + tl) * a.h_q + kvh * G;
+        const float2 *st = a.stats + (size_t)s * a.h_q + kvh * G;
+        float x[G];
+        float2 ml[G];
+        if constexpr (G % 4 == 0) {
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float2 ml = st[j];
-                const float p = exp2f(lg[j] - ml.x) / ml.y;
-                best = fmaxf(best, p);
+            for (int q4 = 0; q4 < G / 4; ++q4) {
+                const float4 v = reinterpret_cast<const float4 *>(lg)[q4];
+                x[4 * q4] = v.x;
+                x[4 * q4 + 1] = v.y;
+                x[4 * q4 + 2] = v.z;
+                x[4 * q4 + 3] = v.w;
             }
-            const float c = best * inv_w;
-            const int blk = a.table[(size_t)s * a.table_stride + tok / a.b];
-            if (blk < 0 || blk >= a.n_total) {
-                record_error(a.err, ZP_ERR_DEVICE, 5);
-                continue;
-            }
-            float *dst = a.score + ((size_t)blk * a.b + tok % a.b) * a.h_kv + kvh;
-            *dst = (first_row || tok == P) ? c : (*dst + c);
+        } else {
+#pragma unroll
+            for (int j = 0; j < G; ++j) x[j] = lg[j];
         }
+#pragma unroll
+        for (int j = 0; j < G; ++j) ml[j] = st[j];
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 5);
+            continue;
+        }
+        float best = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) best = fmaxf(best, exp2f(x[j] - ml[j].x) / ml[j].y);
+        const float c = best * inv_w;
+        float *dst = a.score + ((size_t)blk * a.b + tok % a.b) * a.h_kv + kvh;
+        *dst = (first_row || tok == P) ? c : (*dst + c);
     }
 }
 
@@ -758,7 +725,6 @@ __global__ void __launch_bounds__(9 * 32, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + a.stages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.ctl_off);
-    volatile int *last_flag = abort_flag + 1;
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
     int *lens = reinterpret_cast<int *>(smem + lay.lens_off);
     const int tid = threadIdx.x;
@@ -837,16 +803,28 @@ __global__ void __launch_bounds__(9 * 32, 1)
             prefetch_tmap(&tmv);
             const uint64_t pol = l2_evict_first_policy();
             const unsigned bytes = (unsigned)stage_bytes;
-            int s = s_first;
+            // the block id of the next unit is loaded one iteration ahead, so
+            // its latency overlaps the wait for a free stage
+            int ns = s_first;
+            while (u0 >= prefix[ns + 1]) ++ns;
+            int cur_s = ns;
+            int ntok0 = (int)(u0 - prefix[ns]) * kTcTokens;
+            int nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
             for (long long u = u0, i = 0; u < u1; ++u, ++i) {
-                while (u >= prefix[s + 1]) ++s;
+                const int tok0 = ntok0;
+                const int blk = nblk;
+                if (a.want_score) a.unit_info[u] = make_int2(cur_s, tok0);
+                if (u + 1 < u1) {
+                    while (u + 1 >= prefix[ns + 1]) ++ns;
+                    ntok0 = (int)(u + 1 - prefix[ns]) * kTcTokens;
+                    nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
+                }
+                cur_s = ns;  // sequence of unit u + 1
                 const int st = (int)(i % a.stages);
                 if (i >= a.stages &&
                     !mbar_wait_bounded(&empty[st], (unsigned)(((i / a.stages) - 1) & 1), a.err, abort_flag,
                                        30))
                     break;
-                const int tok0 = (int)(u - prefix[s]) * kTcTokens;
-                const int blk = __ldg(&a.table[(size_t)s * a.table_stride + tok0 / a.b]);
                 if (blk < 0 || blk >= a.n_total) {
                     record_error(a.err, ZP_ERR_DEVICE, 4);
                     mbar_arrive_expect_tx(&full[st], 0);
@@ -874,7 +852,6 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const int g = lane >> 2;    // fragment row group
     const int tig = lane & 3;   // thread in group
     const int h0 = kvh * G;
-    const int ncw_threads = h_kv * 32;
     // ldmatrix row/chunk of this lane: matrix m = lane/8 -> tokens (m/2)*8.., chunk +(m&1)
     const int lm = lane >> 3;
     const int lrow = (lm >> 1) * 8 + (lane & 7);
@@ -1034,44 +1011,6 @@ __global__ void __launch_bounds__(9 * 32, 1)
                     }
                 }
                 if (g < G && tig == 0) a.part_ml[(size_t)slot * a.h_q + h0 + g] = make_float2(m_run, l_run);
-                __threadfence();
-                named_bar_sync(1, ncw_threads);
-                if (tid == 0) {
-                    const int nseg = (int)(u + 1 - seg_begin);
-                    const int ntot = prefix[s + 1] - prefix[s];
-                    const int before = atomicAdd(&a.seq_count[s], nseg);
-                    *last_flag = (before + nseg == ntot) ? 1 : 0;
-                }
-                named_bar_sync(1, ncw_threads);
-                if (*last_flag) {
-                    __threadfence();
-                    const int c_lo = cta_of(prefix[s], U, Gd);
-                    const int c_hi = cta_of(prefix[s + 1] - 1, U, Gd);
-                    for (int e = tid; e < a.h_q * D; e += ncw_threads) {
-                        const int h = e / D;
-                        const int dd = e % D;
-                        float M = -INFINITY;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const long long cs = cta_start(c, U, Gd);
-                            if (cs == cta_start(c + 1, U, Gd)) continue;
-                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
-                            M = fmaxf(M, __ldcg(&a.part_ml[(size_t)sl * a.h_q + h].x));
-                        }
-                        float Ls = 0.f, A = 0.f;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const long long cs = cta_start(c, U, Gd);
-                            if (cs == cta_start(c + 1, U, Gd)) continue;
-                            const int sl = 2 * c + ((prefix[s] <= cs) ? 0 : 1);
-                            const float2 ml = __ldcg(&a.part_ml[(size_t)sl * a.h_q + h]);
-                            const float f = (M == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                            Ls += ml.y * f;
-                            A += __ldcg(&a.part_acc[((size_t)sl * a.h_q + h) * D + dd]) * f;
-                        }
-                        static_cast<__nv_bfloat16 *>(a.out)[((size_t)s * a.h_q + h) * D + dd] =
-                            __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
-                        if (a.want_score && dd == 0) a.stats[(size_t)s * a.h_q + h] = make_float2(M, Ls);
-                    }
-                }
             }
             if (u + 1 < u1) {
                 while (u + 1 >= prefix[s + 1]) ++s;
@@ -1084,10 +1023,124 @@ __global__ void __launch_bounds__(9 * 32, 1)
     }
 }
 
+// ===========================================================================
+// Merge of the sequences that the stream-K split cut between CTAs.
+//
+// Every CTA of the main kernel leaves, for a sequence it did not see whole, a
+// partial record: its running max m and sum l per q head (log2 units) and its
+// unnormalised accumulator.  Block c of this kernel merges the sequence whose
+// last unit lies in CTA c's range and which began in an earlier CTA, so every
+// cut sequence has exactly one merger and all merges run in parallel:
+//     M = max_j m_j,  w_j = 2^(m_j - M),  L = sum_j w_j l_j,
+//     out = sum_j w_j acc_j / L.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a, int grid_main) {
+    extern __shared__ float2 msm[];  // [grid_main][h_q] (m, l) then weights; then slots, L
+    const int c = blockIdx.x;
+    const int B = a.B;
+    const int *pre = a.unit_prefix;
+    const long long U = pre[B];
+    const long long cs = cta_start(c, U, grid_main), ce = cta_start(c + 1, U, grid_main);
+    if (cs >= ce) return;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= cs) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = lo;
+    if (!(pre[s] < cs && pre[s + 1] <= ce)) return;  // not cut, or not this block's
+    const int h_q = a.h_q;
+    const int c_lo = cta_of(pre[s], U, grid_main);
+    const int nc = c - c_lo + 1;
+    int *slot = reinterpret_cast<int *>(msm + (size_t)grid_main * h_q);
+    float *Lh = reinterpret_cast<float *>(slot + grid_main);
+    for (int j = threadIdx.x; j < nc; j += blockDim.x) {
+        const int cj = c_lo + j;
+        const long long sj = cta_start(cj, U, grid_main);
+        slot[j] = (sj == cta_start(cj + 1, U, grid_main)) ? -1 : 2 * cj + (pre[s] > sj ? 1 : 0);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < nc * h_q; e += blockDim.x) {
+        const int j = e / h_q, h = e % h_q;
+        msm[e] = slot[j] < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)slot[j] * h_q + h]);
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < h_q; h += blockDim.x) {
+        float M = -INFINITY;
+        for (int j = 0; j < nc; ++j) M = fmaxf(M, msm[j * h_q + h].x);
+        float L = 0.f;
+        for (int j = 0; j < nc; ++j) {
+            const float2 ml = msm[j * h_q + h];
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            L += w * ml.y;
+            msm[j * h_q + h].x = w;  // weight in place of the max
+        }
+        Lh[h] = L;
+        if (a.want_score) a.stats[(size_t)s * h_q + h] = make_float2(M, L);
+    }
+    __syncthreads();
+    constexpr int CH = 16;  // dims per item
+    for (int it = threadIdx.x; it < h_q * (D / CH); it += blockDim.x) {
+        const int h = it / (D / CH);
+        const int d0 = (it % (D / CH)) * CH;
+        float acc[CH];
+#pragma unroll
+        for (int i = 0; i < CH; ++i) acc[i] = 0.f;
+        for (int j = 0; j < nc; ++j) {
+            if (slot[j] < 0) continue;
+            const float w = msm[j * h_q + h].x;
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_acc + ((size_t)slot[j] * h_q + h) * D + d0);
+#pragma unroll
+            for (int q4 = 0; q4 < CH / 4; ++q4) {
+                const float4 v = __ldcg(src + q4);
+                acc[4 * q4] += w * v.x;
+                acc[4 * q4 + 1] += w * v.y;
+                acc[4 * q4 + 2] += w * v.z;
+                acc[4 * q4 + 3] += w * v.w;
+            }
+        }
+        const float inv = Lh[h] > 0.f ? 1.f / Lh[h] : 0.f;
+        T *og = static_cast<T *>(a.out) + ((size_t)s * h_q + h) * D + d0;
+        if constexpr (sizeof(T) == 2) {
+            uint32_t w4[CH / 2];
+#pragma unroll
+            for (int i = 0; i < CH / 2; ++i) w4[i] = f2_to_bf2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+            reinterpret_cast<uint4 *>(og)[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            reinterpret_cast<uint4 *>(og)[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+        } else {
+#pragma unroll
+            for (int q4 = 0; q4 < CH / 4; ++q4)
+                reinterpret_cast<float4 *>(og)[q4] =
+                    make_float4(acc[4 * q4] * inv, acc[4 * q4 + 1] * inv, acc[4 * q4 + 2] * inv, acc[4 * q4 + 3] * inv);
+        }
+    }
+}
+
+template <typename T, int D>
+zp_status launch_merge(const DecodeArgs &a, int grid, cudaStream_t st) {
+    const size_t smem = (size_t)grid * a.h_q * 8 + (size_t)grid * 4 + (size_t)a.h_q * 4;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e, "decode: merge attribute");
+    }
+    decode_merge_kernel<T, D><<<grid, 256, smem, st>>>(a, grid);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode: merge kernel launch");
+    return ZP_OK;
+}
+
+inline int score_threads(const DecodeArgs &a) {
+    int t = a.T * a.h_kv;
+    t = (t + 31) / 32 * 32;
+    return t > 1024 ? 1024 : t;
+}
+
 struct Plan {
     bool tc;  // tensor-core kernel (bf16) or CUDA-core kernel
     int T, wph, ncw, threads, stages, smem, grid;
-    size_t off_count, off_prefix, off_stats, off_pml, off_pacc, off_logits, total;
+    size_t off_count, off_prefix, off_stats, off_pml, off_pacc, off_info, off_logits, total;
     long long logits_units;
 };
 
@@ -1148,6 +1201,8 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     off = align_up(off + (size_t)2 * p->grid * D->h_q * 8, 256);
     p->off_pacc = off;
     off = align_up(off + (size_t)2 * p->grid * D->h_q * d * 4, 256);
+    p->off_info = off;
+    off = align_up(off + (size_t)units_cap * 8, 256);
     p->off_logits = off;
     off = align_up(off + (size_t)units_cap * p->T * D->h_q * 4, 256);
     p->total = off;
@@ -1206,8 +1261,10 @@ zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, c
     kmain<<<p.grid, p.threads, p.smem, st>>>(mk, mv, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel launch");
+    rc = launch_merge<__nv_bfloat16, Dd>(a, p.grid, st);
+    if (rc != ZP_OK) return rc;
     if (a.want_score) {
-        decode_score_kernel<G><<<p.grid * 8, 128, (a.B + 1) * 4, st>>>(a);
+        decode_score_kernel<G><<<(unsigned)p.logits_units, score_threads(a), 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
     }
@@ -1227,9 +1284,10 @@ zp_status launch_t(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cu
     kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: main kernel launch");
+    zp_status rc = launch_merge<T, Dd>(a, p.grid, st);
+    if (rc != ZP_OK) return rc;
     if (a.want_score) {
-        const int threads = 128;
-        decode_score_kernel<G><<<p.grid * 8, threads, (a.B + 1) * 4, st>>>(a);
+        decode_score_kernel<G><<<(unsigned)p.logits_units, score_threads(a), 0, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
     }
@@ -1299,13 +1357,11 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.stats = reinterpret_cast<float2 *>(ws + p.off_stats);
     a.part_acc = reinterpret_cast<float *>(ws + p.off_pacc);
     a.part_ml = reinterpret_cast<float2 *>(ws + p.off_pml);
-    a.seq_count = reinterpret_cast<int *>(ws + p.off_count);
     a.unit_prefix = reinterpret_cast<int *>(ws + p.off_prefix);
+    a.unit_info = reinterpret_cast<int2 *>(ws + p.off_info);
     a.logits_units = p.logits_units;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(a.seq_count, 0, (size_t)B * 4, st);
-    if (e != cudaSuccess) return cuda_fail(e, "decode: memset of arrival counters");
     const int G = D->h_q / D->h_kv;
     const int d = D->head_dim;
     if (p.tc) {
@@ -1384,8 +1440,8 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const 
                     "decode_noalloc: this call needs %zu bytes of scratch; the built-in buffer holds "
                     "%zu (reduce B or table_stride, or use zp_paged_decode_attn with a workspace)",
                     need, kNoAllocScratchBytes);
-    // The arrival counters, the only part that must start at zero, are
-    // cleared on the stream by zp_paged_decode_attn itself.
+    // Nothing in the scratch needs to start at zero: every part that is
+    // read is written earlier in the same call.
     return zp_paged_decode_attn(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out,
                                 score_accum, window, scratch, kNoAllocScratchBytes, stream);
 }

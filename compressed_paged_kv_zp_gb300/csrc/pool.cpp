@@ -125,3 +125,26 @@ extern "C" zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int
     *n_fresh = used;
     return ok();
 }
+
+extern "C" zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tables, int32_t table_stride,
+                                              const int32_t *n_blocks, int32_t n, int32_t max_blocks,
+                                              int32_t *targets, int32_t *new_tables, int32_t *dropped,
+                                              int32_t *n_dropped, int32_t *n_fresh) {
+    if (!pool || n < 0 || (n > 0 && (!tables || !n_blocks || !targets || !new_tables || !dropped ||
+                                     !n_dropped || !n_fresh)))
+        return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: NULL argument");
+    if (max_blocks < 2 || table_stride < max_blocks)
+        return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: table_stride %d < max_blocks %d", table_stride,
+                    max_blocks);
+    for (int32_t i = 0; i < n; ++i) {
+        if (n_blocks[i] > table_stride)
+            return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: sequence %d has %d > %d blocks", i,
+                        n_blocks[i], table_stride);
+        zp_status rc = zp_plan_compaction(pool, tables + (size_t)i * table_stride, n_blocks[i], max_blocks,
+                                          targets + (size_t)i * (max_blocks - 1),
+                                          new_tables + (size_t)i * max_blocks,
+                                          dropped + (size_t)i * table_stride, &n_dropped[i], &n_fresh[i]);
+        if (rc != ZP_OK) return rc;  // sequences before i stay planned
+    }
+    return ok();
+}

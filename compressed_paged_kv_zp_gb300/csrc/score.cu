@@ -190,6 +190,127 @@ __global__ void lightning_kernel(const ScoreArgs a) {
     }
 }
 
+// Tensor-core variant for bf16 keys and b = 16 (one 16 x 16 Gram per block and
+// kv head).  grid (ceil(Lmax / 16), n), one warp per kv head.  The block's
+// keys (all kv heads: one contiguous page) are copied with coalesced 16-byte
+// loads into shared memory, each head's 16 rows of 128 dims as two 16 x 128 B
+// tiles whose 16-byte chunks are XOR-swizzled by (row % 8), so that ldmatrix
+// reads conflict-free.  G = K K^T takes 16 mma.sync (8 k-steps x 2 n-tiles);
+// one ldmatrix.x4 per k-step feeds both operands.  Then, on the accumulator
+// fragments: cosine (zero-norm keys give 0), zero diagonal, per column the
+// newest row above p zeroed (a ballot over the column's lanes), row sums.
+template <int D>
+__global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
+    constexpr int HALVES = D / 64;
+    constexpr int KS = D / 16;
+    extern __shared__ __align__(128) unsigned char lsm[];
+    const int s = blockIdx.y;
+    const int bi = blockIdx.x;
+    const int L = clamp_len(a, s);
+    const int tb0 = bi * 16;
+    if (tb0 >= L) return;
+    const int nvalid = min(16, L - tb0);
+    const int blk = a.table[(size_t)s * a.table_stride + bi];
+    if (blk < 0 || blk >= a.n_total) {
+        if (threadIdx.x == 0) record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        return;
+    }
+    const int h_kv = a.h_kv;
+    // ---- page -> swizzled tiles [head][half][16 rows][8 chunks of 16 B]
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.k) +
+                                                       (size_t)blk * 16 * h_kv * D);
+    const int chunks_per_row = D / 8;  // 16-byte chunks in one (token, head) row
+    const int total = nvalid * h_kv * chunks_per_row;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int t = i / (h_kv * chunks_per_row);
+        const int rem = i % (h_kv * chunks_per_row);
+        const int h = rem / chunks_per_row;
+        const int c = rem % chunks_per_row;
+        const int hf = c >> 3, cc = c & 7;
+        reinterpret_cast<uint4 *>(lsm + ((h * HALVES + hf) * 16 + t) * 128)[cc ^ (t & 7)] = src[i];
+    }
+    // rows past the sequence end: zeros (excluded again below)
+    for (int i = threadIdx.x; i < (16 - nvalid) * h_kv * chunks_per_row; i += blockDim.x) {
+        const int t = nvalid + i / (h_kv * chunks_per_row);
+        const int rem = i % (h_kv * chunks_per_row);
+        const int h = rem / chunks_per_row;
+        const int c = rem % chunks_per_row;
+        reinterpret_cast<uint4 *>(lsm + ((h * HALVES + (c >> 3)) * 16 + t) * 128)[(c & 7) ^ (t & 7)] =
+            make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= h_kv) return;
+    const int kvh = warp;
+    const int g = lane >> 2, tig = lane & 3;
+    const int lm = lane >> 3;
+    const int lrow = (lm & 1) * 8 + (lane & 7);  // matrices: (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
+    const int lchunk = lm >> 1;
+    const uint32_t tile0 = smem_u32(lsm + (size_t)kvh * HALVES * 16 * 128);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+        const uint32_t tile = tile0 + (t >> 2) * 16 * 128;
+        const int chunk = (t & 3) * 2 + lchunk;
+        uint32_t r0, r1, r2, r3;  // (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
+        ldsm_x4(tile + lrow * 128 + ((chunk ^ (lrow & 7)) << 4), r0, r1, r2, r3);
+        // A = K rows (a0a1 row g / c, a2a3 row g+8 / c, a4a5 row g / c+1, a6a7 row g+8 / c+1)
+        // B = K^T: n-tile 0 = tokens 0-7 (b0 = chunk c, b1 = chunk c+1), n-tile 1 = tokens 8-15
+        mma_16816(c0, r0, r1, r2, r3, r0, r2);
+        mma_16816(c1, r0, r1, r2, r3, r1, r3);
+    }
+    // lane holds G[g][2tig+e] (c0[e]), G[g+8][2tig+e] (c0[2+e]), G[g][8+2tig+e] (c1[e]), G[g+8][8+2tig+e] (c1[2+e])
+    __shared__ float nrm[16][16];  // per warp: the 16 norms
+    float *myn = nrm[warp];
+    if (tig == (g >> 1)) myn[g] = c0[g & 1];               // G[g][g], g < 8
+    if (tig == (g >> 1)) myn[g + 8] = c1[2 + (g & 1)];     // G[g+8][g+8]
+    __syncwarp();
+    const int rows[2] = {g, g + 8};
+    const int cols[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+    float v[2][4];  // [row][col]
+    v[0][0] = c0[0]; v[0][1] = c0[1]; v[0][2] = c1[0]; v[0][3] = c1[1];
+    v[1][0] = c0[2]; v[1][1] = c0[3]; v[1][2] = c1[2]; v[1][3] = c1[3];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+        const float nr = sqrtf(fmaxf(myn[rows[ri]], 0.f));
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+            const float nc = sqrtf(fmaxf(myn[cols[ci]], 0.f));
+            const bool ok = rows[ri] < nvalid && cols[ci] < nvalid && rows[ri] != cols[ci] && nr > 0.f && nc > 0.f;
+            v[ri][ci] = ok ? v[ri][ci] / (nr * nc) : 0.f;
+        }
+    }
+    // per column: the newest row with cos > p loses its entry
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        const unsigned blo = __ballot_sync(0xFFFFFFFFu, v[0][ci] > a.p);
+        const unsigned bhi = __ballot_sync(0xFFFFFFFFu, v[1][ci] > a.p);
+        // bits of the lanes sharing this lane's column: lanes tig + 4 g', g' = 0..7
+        unsigned mlo = 0, mhi = 0;
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) {
+            mlo |= ((blo >> (tig + 4 * gg)) & 1u) << gg;
+            mhi |= ((bhi >> (tig + 4 * gg)) & 1u) << gg;
+        }
+        int rstar = -1;
+        if (mhi) rstar = 8 + (31 - __clz(mhi));
+        else if (mlo) rstar = 31 - __clz(mlo);
+        if (rstar == rows[0]) v[0][ci] = 0.f;
+        if (rstar == rows[1]) v[1][ci] = 0.f;
+    }
+    float rs0 = v[0][0] + v[0][1] + v[0][2] + v[0][3];
+    float rs1 = v[1][0] + v[1][1] + v[1][2] + v[1][3];
+    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 1);
+    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 2);
+    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 1);
+    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 2);
+    if (tig == 0) {
+        float *out = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax + tb0;
+        if (g < nvalid) out[g] = rs0;
+        if (g + 8 < nvalid) out[g + 8] = rs1;
+    }
+}
+
 // grid (h_kv, n), 1024 threads
 __global__ void finalize_kernel(const ScoreArgs a) {
     __shared__ float red[32];
@@ -327,7 +448,20 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
         dim3 g2((Lmax + a.b - 1) / a.b, n);
         const size_t smem = (size_t)a.h_kv * a.b * (a.d + 1) * 4;
         if (smem > (size_t)dev.smem_optin) return fail(ZP_ERR_SHAPE, "score: block of keys too large");
-        if (D->dtype == ZP_BF16) {
+        if (D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128)) {
+            const size_t smem_tc = (size_t)a.h_kv * (a.d / 64) * 16 * 128;
+            if (a.d == 128) {
+                if (smem_tc > 48 * 1024)
+                    cudaFuncSetAttribute(lightning_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_tc);
+                lightning_tc_kernel<128><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
+            } else {
+                if (smem_tc > 48 * 1024)
+                    cudaFuncSetAttribute(lightning_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_tc);
+                lightning_tc_kernel<64><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
+            }
+        } else if (D->dtype == ZP_BF16) {
             cudaFuncSetAttribute(lightning_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
             lightning_kernel<__nv_bfloat16><<<g2, a.h_kv * 32, smem, st>>>(a);

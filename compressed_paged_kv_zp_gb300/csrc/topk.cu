@@ -34,9 +34,15 @@ __device__ __forceinline__ int block_sum(int v, int *red) {
     return tot;
 }
 
+// Scores are staged in shared memory when the row fits (kSmemRow floats),
+// so the radix passes never go back to global memory.
+constexpr int kSmemRow = 32768;
+
+template <bool STAGED>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int h_kv, int Lmax,
                                                         const int32_t *seq_lens, int k, int32_t *keep,
                                                         int32_t *tie_count, unsigned *err) {
+    extern __shared__ float srow[];
     __shared__ int hist[256];
     __shared__ int red[32];
     __shared__ int scan[kThreads];
@@ -50,6 +56,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
     if (L > Lmax) L = Lmax;
     const float *sc = scores + ((size_t)s * h_kv + kvh) * Lmax;
     int32_t *out = keep + ((size_t)s * h_kv + kvh) * k;
+    if constexpr (STAGED) {
+        if (L > k) {
+            for (int t = tid; t < L; t += blockDim.x) srow[t] = sc[t];
+            __syncthreads();
+            sc = srow;
+        }
+    }
     if (L <= k) {
         for (int r = tid; r < k; r += blockDim.x) out[r] = r < L ? r : -1;
         if (tie_count && tid == 0) tie_count[(size_t)s * h_kv + kvh] = 0;
@@ -156,8 +169,20 @@ extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t L
     zp_status rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
     dim3 grid(h_kv, n);
-    topk_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        scores, h_kv, Lmax, seq_lens, k, keep_idx, tie_count, dev.error_word);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Lmax <= kSmemRow) {
+        const size_t smem = (size_t)Lmax * 4;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return cuda_fail(e, "topk: cudaFuncSetAttribute");
+        }
+        topk_kernel<true><<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, keep_idx, tie_count,
+                                                        dev.error_word);
+    } else {
+        topk_kernel<false><<<grid, kThreads, 0, st>>>(scores, h_kv, Lmax, seq_lens, k, keep_idx, tie_count,
+                                                      dev.error_word);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "topk: launch");
     return ok();

@@ -134,8 +134,8 @@ zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void
  * and does nothing.  No device memory is allocated by this call.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.
- * All calls share the array and it keeps the previous call's contents (the
- * part that must start at zero is cleared on the stream by each call), so
+ * All calls share the array and it keeps the previous call's contents (no
+ * part of it needs to start at zero: each call writes what it reads), so
  * calls that may overlap on the GPU -- on different streams, or from
  * different threads -- race and must be ordered by the caller. */
 zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q, const void *k_cache,
@@ -228,6 +228,16 @@ zp_status zp_pool_release(zp_pool *pool, int32_t n, const int32_t *ids);
 zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int32_t n_blocks,
                              int32_t max_blocks, int32_t *targets, int32_t *new_table,
                              int32_t *dropped, int32_t *n_dropped, int32_t *n_fresh);
+
+/* zp_plan_compaction for n sequences in one call.  tables [n][table_stride]
+ * (sequence i holds n_blocks[i] <= table_stride blocks); outputs per sequence:
+ * targets [n][max_blocks-1], new_tables [n][max_blocks], dropped
+ * [n][table_stride] (first n_dropped[i] valid), n_fresh [n].  Stops at the
+ * first sequence that fails (earlier ones stay planned) and returns its error. */
+zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tables, int32_t table_stride,
+                                   const int32_t *n_blocks, int32_t n, int32_t max_blocks,
+                                   int32_t *targets, int32_t *new_tables, int32_t *dropped,
+                                   int32_t *n_dropped, int32_t *n_fresh);
 
 #ifdef __cplusplus
 }

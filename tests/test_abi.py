@@ -111,3 +111,27 @@ def test_invalid_arguments_rejected_without_device(zp):
     rc = zp.lib.zp_compact_pages(ctypes.byref(desc), None, None, 0, 1, None, 0, None, 1, None, 1,
                                  None, None, 4, 1, None)
     assert rc == 3
+
+
+def test_batch_planner_matches_single_calls(zp):
+    import numpy as np
+    rng = np.random.default_rng(11)
+    pools = [zp.Pool(400), zp.Pool(400)]
+    n, stride, N_max = 6, 12, 5
+    tables = np.full((n, stride), -1, np.int32)
+    nb = rng.integers(N_max, stride + 1, size=n).astype(np.int32)
+    for pool in pools:  # identical histories: shared prefix of 3 blocks for all
+        prefix = pool.alloc(3)
+        for _ in range(n - 1):
+            pool.incref(prefix)
+        for i in range(n):
+            tables[i, :3] = prefix
+            tables[i, 3:nb[i]] = pool.alloc(int(nb[i]) - 3)
+    singles = [pools[0].plan_compaction(tables[i, :nb[i]].tolist(), N_max) for i in range(n)]
+    batch = pools[1].plan_compaction_batch(tables, nb, N_max)
+    for i, sp in enumerate(singles):
+        assert list(batch["targets"][i]) == sp["targets"]
+        assert list(batch["new_tables"][i]) == sp["new_table"]
+        assert list(batch["dropped"][i, :batch["n_dropped"][i]]) == sp["dropped"]
+        assert batch["n_fresh"][i] == sp["n_fresh"]
+    assert pools[0].num_free == pools[1].num_free
