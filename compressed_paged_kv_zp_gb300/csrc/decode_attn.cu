@@ -28,8 +28,6 @@
 //     scratch array; once every sequence's final max and sum are known, a
 //     second, fully parallel kernel turns them into probabilities, takes the
 //     max over the GQA group and adds 1/w of it to the paged score.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
@@ -674,15 +672,19 @@ __global__ void decode_score_kernel(const DecodeArgs a) {
 //   O^T += V^T P^T: A = V^T (ldmatrix.trans), B = P^T, which is exactly the
 //                  fragment the first product leaves in each lane, so P never
 //                  leaves the registers.
-// Operands come from shared memory filled by 3-D TMA tensor copies, one box
-// of 16 tokens x 64 dims per (kv head, half of d), swizzled by 128 bytes so
-// that the eight rows an ldmatrix reads sit on eight different bank groups
-// (a 1-D copy would leave the rows of one kv head 2 KB apart, all on the same
-// banks).  One consumer warp per kv head, one producer warp for the copies.
-// P is rounded to bf16 for the second product; the scores and the softmax
-// statistics stay in fp32.
-constexpr int kTcTokens = 16;     // tokens per unit (one TMA box)
-constexpr int kTcTile = 16 * 128; // bytes of one (head, half) tile: 16 rows x 128 B
+// Operands come from shared memory filled by a producer warp with 1-D bulk
+// copies (TMA engine), one per token row of a unit: the row of one token holds
+// all kv heads and is contiguous in HBM, so each unit is read in address
+// order -- the pattern that streams at the full copy rate (per-head tensor
+// boxes of 128-byte rows 2 KB apart measured ~20 % slower, 16-byte cp.async
+// copies slower still).  Row t lands at t * (row_bytes + 16): with that 16-byte
+// pad, the eight token rows an ldmatrix reads fall on eight different bank
+// groups.  One consumer warp per kv head.  P is rounded to bf16 for the
+// second product; the scores and the softmax statistics stay in fp32.
+constexpr int kTcTokens = 16;     // tokens per unit
+constexpr int kTcPad = 16;        // bytes of padding after each staged token row
+
+__host__ __device__ inline int tc_row_stride(int h_kv, int d) { return h_kv * d * 2 + kTcPad; }
 
 __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int halves, int B) {
     SmemLayout L;
@@ -691,9 +693,9 @@ __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int h
     off += 2 * stages * 8;
     L.ctl_off = off;
     off += 16;
-    off = (off + 1023) / 1024 * 1024;  // 128-byte swizzle atoms need 1024-byte alignment
+    off = (off + 1023) / 1024 * 1024;
     L.stage_off = off;
-    off += stages * 2 * h_kv * halves * kTcTile;
+    off += stages * 2 * kTcTokens * tc_row_stride(h_kv, halves * 64);
     L.warp_off = off;
     L.merge_off = off;
     L.prefix_off = off;
@@ -704,20 +706,12 @@ __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int h
     return L;
 }
 
-// Address of 16-byte chunk `chunk` (0..7) of row `row` (0..15) in a swizzled tile.
-__device__ __forceinline__ uint32_t sw128(uint32_t tile, int row, int chunk) {
-    return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
 template <int D, int G>
-__global__ void __launch_bounds__(9 * 32, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                     const DecodeArgs a) {
+__global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a) {
     constexpr int HALVES = D / 64;
     constexpr int KS = D / 16;  // k-steps of Q K^T = m-tiles of V^T P^T
     static_assert(G >= 1 && G <= 8, "group of at most 8 q heads");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // the swizzled tiles need 1024-byte aligned shared addresses
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int B = a.B;
     const int h_kv = a.h_kv;
@@ -730,7 +724,8 @@ __global__ void __launch_bounds__(9 * 32, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int stage_bytes = 2 * h_kv * HALVES * kTcTile;  // K then V
+    const int RS = tc_row_stride(h_kv, D);             // staged row stride
+    const int stage_bytes = 2 * kTcTokens * RS;        // K rows then V rows
 
     for (int s = tid; s < B; s += blockDim.x) {
         int L = a.seq_lens[s];
@@ -796,51 +791,47 @@ __global__ void __launch_bounds__(9 * 32, 1)
     unsigned char *stage_base = smem + lay.stage_off;
 
     // =====================================================================
-    // producer warp: TMA copies of K and V for every unit of the range
+    // producer warp: one bulk copy per token row (K rows by lanes 0..15, V rows
+    // by lanes 16..31), after lane 0 has announced the unit's bytes
     if (warp == h_kv) {
-        if (lane == 0) {
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
-            const uint64_t pol = l2_evict_first_policy();
-            const unsigned bytes = (unsigned)stage_bytes;
-            // the block id of the next unit is loaded one iteration ahead, so
-            // its latency overlaps the wait for a free stage
-            int ns = s_first;
-            while (u0 >= prefix[ns + 1]) ++ns;
-            int cur_s = ns;
-            int ntok0 = (int)(u0 - prefix[ns]) * kTcTokens;
-            int nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
-            for (long long u = u0, i = 0; u < u1; ++u, ++i) {
-                const int tok0 = ntok0;
-                const int blk = nblk;
-                if (a.want_score) a.unit_info[u] = make_int2(cur_s, tok0);
-                if (u + 1 < u1) {
-                    while (u + 1 >= prefix[ns + 1]) ++ns;
-                    ntok0 = (int)(u + 1 - prefix[ns]) * kTcTokens;
-                    nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
-                }
-                cur_s = ns;  // sequence of unit u + 1
-                const int st = (int)(i % a.stages);
-                if (i >= a.stages &&
-                    !mbar_wait_bounded(&empty[st], (unsigned)(((i / a.stages) - 1) & 1), a.err, abort_flag,
-                                       30))
-                    break;
-                if (blk < 0 || blk >= a.n_total) {
-                    record_error(a.err, ZP_ERR_DEVICE, 4);
-                    mbar_arrive_expect_tx(&full[st], 0);
-                    continue;
-                }
-                const int row = blk * a.b + (tok0 % a.b);
-                unsigned char *ks = stage_base + (size_t)st * stage_bytes;
-                unsigned char *vs = ks + stage_bytes / 2;
-                mbar_arrive_expect_tx(&full[st], bytes);
-                for (int h = 0; h < h_kv; ++h)
-#pragma unroll
-                    for (int hf = 0; hf < HALVES; ++hf) {
-                        const int t = h * HALVES + hf;
-                        tma_load_3d(ks + t * kTcTile, &tmk, hf * 64, h, row, &full[st], pol);
-                        tma_load_3d(vs + t * kTcTile, &tmv, hf * 64, h, row, &full[st], pol);
-                    }
+        const uint64_t pol = l2_evict_first_policy();
+        const unsigned row_bytes = (unsigned)(h_kv * D * 2);
+        const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.k);
+        const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.v);
+        // the next unit's block id is loaded one iteration ahead
+        int ns = s_first;
+        while (u0 >= prefix[ns + 1]) ++ns;
+        int cur_s = ns;
+        int ntok0 = (int)(u0 - prefix[ns]) * kTcTokens;
+        int nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
+        for (long long u = u0, i = 0; u < u1; ++u, ++i) {
+            const int tok0 = ntok0;
+            const int blk = nblk;
+            const int useq = cur_s;
+            if (a.want_score && lane == 0) a.unit_info[u] = make_int2(useq, tok0);
+            if (u + 1 < u1) {
+                while (u + 1 >= prefix[ns + 1]) ++ns;
+                ntok0 = (int)(u + 1 - prefix[ns]) * kTcTokens;
+                nblk = __ldg(&a.table[(size_t)ns * a.table_stride + ntok0 / a.b]);
+            }
+            cur_s = ns;
+            const int st = (int)(i % a.stages);
+            if (i >= a.stages &&
+                !mbar_wait_bounded(&empty[st], (unsigned)(((i / a.stages) - 1) & 1), a.err, abort_flag, 30))
+                break;
+            int valid = lens[useq] - tok0;
+            if (valid > kTcTokens) valid = kTcTokens;
+            const bool bad = blk < 0 || blk >= a.n_total;
+            if (lane == 0) {
+                if (bad) record_error(a.err, ZP_ERR_DEVICE, 4);
+                mbar_arrive_expect_tx(&full[st], bad ? 0u : 2u * valid * row_bytes);
+            }
+            __syncwarp();
+            const int t = lane & 15;
+            if (!bad && t < valid) {
+                const size_t off = ((size_t)blk * a.b + (tok0 % a.b) + t) * h_kv * D;
+                unsigned char *dst = stage_base + (size_t)st * stage_bytes + (lane >> 4) * kTcTokens * RS + t * RS;
+                bulk_g2s(dst, (lane < 16 ? kg : vg) + off, row_bytes, &full[st], pol);
             }
         }
         return;
@@ -894,17 +885,16 @@ __global__ void __launch_bounds__(9 * 32, 1)
         int valid = lens[s] - (int)(u - prefix[s]) * kTcTokens;
         if (valid > kTcTokens) valid = kTcTokens;
         if (!got) valid = 0;
-        unsigned char *ks = stage_base + (size_t)st * stage_bytes + kvh * HALVES * kTcTile;
-        unsigned char *vs = ks + stage_bytes / 2;
+        unsigned char *ks = stage_base + (size_t)st * stage_bytes + kvh * D * 2;  // this head's columns
+        unsigned char *vs = ks + kTcTokens * RS;
         if (valid > 0) {
             if (valid < kTcTokens) {
-                // rows past the sequence end hold whatever the block had: zero
-                // them in V so that 0 * garbage cannot produce a NaN
-                for (int c = lane; c < (kTcTokens - valid) * 8 * HALVES; c += 32) {
-                    const int hf = c / ((kTcTokens - valid) * 8);
-                    const int rem = c % ((kTcTokens - valid) * 8);
-                    const int row = valid + rem / 8;
-                    reinterpret_cast<uint4 *>(vs + hf * kTcTile + row * 128)[rem % 8] = make_uint4(0, 0, 0, 0);
+                // rows past the sequence end were not copied and hold stale
+                // data: zero this head's part of them in V so that
+                // 0 * garbage cannot produce a NaN
+                for (int c = lane; c < (kTcTokens - valid) * (D / 8); c += 32) {
+                    const int row = valid + c / (D / 8);
+                    reinterpret_cast<uint4 *>(vs + row * RS)[c % (D / 8)] = make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
             }
@@ -915,7 +905,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
 #pragma unroll
             for (int t = 0; t < KS; ++t) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(sw128(kt + (t >> 2) * kTcTile, lrow, (t & 3) * 2 + lchunk), b0, b1, b2, b3);
+                ldsm_x4(kt + lrow * RS + (2 * t + lchunk) * 16, b0, b1, b2, b3);
                 mma_16816(sc0, qa[t][0], 0u, qa[t][1], 0u, b0, b1);
                 mma_16816(sc1, qa[t][0], 0u, qa[t][1], 0u, b2, b3);
             }
@@ -963,7 +953,7 @@ __global__ void __launch_bounds__(9 * 32, 1)
                 acc[t][2] *= a_lo;
                 acc[t][3] *= a_hi;
                 uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(sw128(vt + (t >> 2) * kTcTile, lrow, (t & 3) * 2 + lchunk), v0, v1, v2, v3);
+                ldsm_x4_t(vt + lrow * RS + (2 * t + lchunk) * 16, v0, v1, v2, v3);
                 mma_16816(acc[t], v0, v1, v2, v3, pb0, pb1);
             }
         }
@@ -1209,39 +1199,6 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     return ZP_OK;
 }
 
-// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// Tensor map over one layer of a bf16 cache viewed as [N_total*b][h_kv][d]:
-// boxes of 16 tokens x 1 head x 64 dims, 128-byte swizzle.
-zp_status encode_cache_map(CUtensorMap *m, const void *base, const zp_cache_desc *D) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return fail(ZP_ERR_CUDA, "decode: cuTensorMapEncodeTiled unavailable");
-    if (reinterpret_cast<uintptr_t>(base) % 16) return fail(ZP_ERR_INVALID_ARG, "decode: cache not 16-byte aligned");
-    const cuuint64_t dims[3] = {(cuuint64_t)D->head_dim, (cuuint64_t)D->h_kv,
-                                (cuuint64_t)D->n_total_blocks * (cuuint64_t)D->block_size};
-    const cuuint64_t strides[2] = {(cuuint64_t)D->head_dim * 2, (cuuint64_t)D->h_kv * D->head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcTokens};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ZP_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return ZP_OK;
-}
-
 template <int Dd, int G>
 zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cudaStream_t st,
                     const zp_cache_desc *D) {
@@ -1253,15 +1210,12 @@ zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, c
         if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
         configured_smem[dv] = p.smem;
     }
-    CUtensorMap mk, mv;
-    zp_status rc = encode_cache_map(&mk, a.k, D);
-    if (rc != ZP_OK) return rc;
-    rc = encode_cache_map(&mv, a.v, D);
-    if (rc != ZP_OK) return rc;
-    kmain<<<p.grid, p.threads, p.smem, st>>>(mk, mv, a);
+    if ((reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) % 16)
+        return fail(ZP_ERR_INVALID_ARG, "decode: caches must be 16-byte aligned");
+    kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel launch");
-    rc = launch_merge<__nv_bfloat16, Dd>(a, p.grid, st);
+    zp_status rc = launch_merge<__nv_bfloat16, Dd>(a, p.grid, st);
     if (rc != ZP_OK) return rc;
     if (a.want_score) {
         decode_score_kernel<G><<<(unsigned)p.logits_units, score_threads(a), 0, st>>>(a);

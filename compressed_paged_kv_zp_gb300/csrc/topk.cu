@@ -89,17 +89,38 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
             if (pshift == 64 || (key >> pshift) == pre) atomicAdd(&hist[(key >> shift) & 255], 1);
         }
         __syncthreads();
-        if (tid == 0) {
-            int need = s_need, cum = 0, bin = 255;
-            for (; bin > 0; --bin) {
-                if (cum + hist[bin] >= need) break;
-                cum += hist[bin];
+        if (tid < 32) {
+            // warp 0: lane l owns bins 8l..8l+7; a suffix scan over the lanes
+            // finds the bin where the count from the top reaches `need`
+            const int need = s_need;
+            int h8[8], tot = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                h8[j] = hist[8 * tid + j];
+                tot += h8[j];
             }
-            need -= cum;
-            s_prefix = (pshift == 64 ? 0ull : (pre << 8)) | (unsigned long long)bin;
-            s_shift = shift;
-            s_need = need;
-            if (hist[bin] == need) s_done = 1;
+            int incl = tot;  // bins of lanes >= this one
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+                if (tid + o < 32) incl += y;
+            }
+            const int above = incl - tot;
+            if (above < need && need <= incl) {
+                int cum = above, bin = 8 * tid;
+                for (int j = 7; j >= 0; --j) {
+                    if (cum + h8[j] >= need) {
+                        bin = 8 * tid + j;
+                        break;
+                    }
+                    cum += h8[j];
+                }
+                const int rem = need - cum;
+                s_prefix = (pshift == 64 ? 0ull : (pre << 8)) | (unsigned long long)bin;
+                s_shift = shift;
+                s_need = rem;
+                if (hist[bin] == rem) s_done = 1;
+            }
         }
     }
     __syncthreads();
@@ -111,16 +132,31 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
     const int end = min(L, beg + chunk);
     int cnt = 0;
     for (int t = beg; t < end; ++t) cnt += (make_key(sc[t], t) >> tsh) >= thr;
-    scan[tid] = cnt;
-    __syncthreads();
-    for (int o = 1; o < (int)blockDim.x; o <<= 1) {
-        const int v = tid >= o ? scan[tid - o] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
+    // exclusive block scan of cnt: warp shuffles, then the 32 warp totals
+    const int lane = tid & 31, wid = tid >> 5;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
     }
-    int pos = scan[tid] - cnt;
-    const int total = scan[blockDim.x - 1];
+    if (lane == 31) scan[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        const int nw = blockDim.x >> 5;
+        int w = lane < nw ? scan[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < nw) scan[32 + lane] = wi - w;  // exclusive warp offsets
+        if (lane == nw - 1) scan[64] = wi;        // total
+    }
+    __syncthreads();
+    int pos = scan[32 + wid] + incl - cnt;
+    const int total = scan[64];
     if (total != k && tid == 0) record_error(err, ZP_ERR_DEVICE, 0x301);
     float kept_min = INFINITY;
     for (int t = beg; t < end; ++t) {

@@ -188,6 +188,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only, with an L2 policy):
+// the destination may be any 16-byte aligned shared address, so a copy can
+// read global memory in order and still land in a swizzled layout.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)),
+                 "l"(src), "l"(policy)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued before has landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
