@@ -65,7 +65,7 @@ struct DecodeArgs {
     float *part_acc;   // [2*grid][h_q][D]
     float2 *part_ml;   // [2*grid][h_q]
     int *unit_prefix;  // [B+1]
-    int2 *unit_info;   // [units]: (sequence, first token) of every unit
+    int4 *unit_info;   // [units]: (sequence, first token, length, window flags) of every unit
     long long logits_units;  // capacity of `logits` in units
     unsigned *err;
 };
@@ -153,6 +153,16 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
     while (c + 1 < G && cta_start(c + 1, U, G) <= u) ++c;
     while (c > 0 && cta_start(c, U, G) > u) --c;
     return c;
+}
+
+// Record of one unit for the score epilogue: sequence, first token, length
+// and flags (bit 0: the sequence is on a window step, bit 1: first window row).
+__device__ __forceinline__ int4 unit_record(const DecodeArgs &a, int s, int tok0, int L) {
+    const int P = L - 1;
+    const int r = P >= 0 ? P % a.b : -1;
+    const int win = (P >= 0 && r >= a.b - a.window) ? 1 : 0;
+    const int first = (win && r == a.b - a.window) ? 2 : 0;
+    return make_int4(s, tok0, L, win | first);
 }
 
 // Shared-memory layout (dynamic).
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
         int valid = lens[ps] - tok0;
         if (valid > TU) valid = TU;
         const int blk = __ldg(&a.table[(size_t)ps * a.table_stride + tok0 / a.b]);
-        if (a.want_score) a.unit_info[u] = make_int2(ps, tok0);
+        if (a.want_score) a.unit_info[u] = unit_record(a, ps, tok0, lens[ps]);
         unsigned char *ks = stage_base + (size_t)st * 2 * stage_bytes;
         unsigned char *vs = ks + stage_bytes;
         if (blk < 0 || blk >= a.n_total) {
@@ -604,24 +614,21 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
 
 // Window-score epilogue: one block per unit, one thread per (token, kv head)
 // of window-step sequences.  p_h(t) = 2^(logit - m_h) / l_h;
-// S += (1/w) max over the group of p_h(t) (written at the first window row
-// and for the newest token).  Each unit's sequence and first token come from
-// the main kernel, so a thread's chain of dependent loads is short and the
-// thousands of blocks keep the memory system busy.
+// S += (1/w) max over the group of p_h(t) (written instead of added at the
+// first window row and for the newest token).  (m_h, l_h) are the sequence's
+// final softmax statistics, written by the main kernel (sequences one CTA saw
+// whole) or by the merge kernel (cut sequences).  A thread's dependent loads
+// are: unit record -> block id and logits -> score slot.
 template <int G>
-__global__ void decode_score_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
     const int u = blockIdx.x;
     const int U = __ldg(&a.unit_prefix[a.B]);
-    if (u >= U) return;
-    const int2 info = a.unit_info[u];
+    const int4 info = a.unit_info[u];
+    if (u >= U || !(info.w & 1)) return;
     const int s = info.x;
-    int L = __ldg(&a.seq_lens[s]);
-    if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    const int L = info.z;
     const int P = L - 1;
-    if (P < 0) return;
-    const int r = P % a.b;
-    if (r < a.b - a.window) return;  // not a window step
-    const bool first_row = (r == a.b - a.window);
+    const bool first_row = (info.w & 2) != 0;
     const float inv_w = 1.f / (float)a.window;
     for (int it = threadIdx.x; it < a.T * a.h_kv; it += blockDim.x) {
         const int tl = it / a.h_kv;
@@ -808,7 +815,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             const int tok0 = ntok0;
             const int blk = nblk;
             const int useq = cur_s;
-            if (a.want_score && lane == 0) a.unit_info[u] = make_int2(useq, tok0);
+            if (a.want_score && lane == 0) a.unit_info[u] = unit_record(a, useq, tok0, lens[useq]);
             if (u + 1 < u1) {
                 while (u + 1 >= prefix[ns + 1]) ++ns;
                 ntok0 = (int)(u + 1 - prefix[ns]) * kTcTokens;
@@ -1107,8 +1114,10 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a, i
     }
 }
 
-template <typename T, int D>
-zp_status launch_merge(const DecodeArgs &a, int grid, cudaStream_t st) {
+// Merge kernel, then (window steps) the score epilogue.  (Programmatic
+// dependent launches of these two were measured slightly slower.)
+template <typename T, int D, int G>
+zp_status launch_finish(const DecodeArgs &a, int grid, long long units_cap, cudaStream_t st) {
     const size_t smem = (size_t)grid * a.h_q * 8 + (size_t)grid * 4 + (size_t)a.h_q * 4;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1118,13 +1127,12 @@ zp_status launch_merge(const DecodeArgs &a, int grid, cudaStream_t st) {
     decode_merge_kernel<T, D><<<grid, 256, smem, st>>>(a, grid);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: merge kernel launch");
+    if (a.want_score) {
+        decode_score_kernel<G><<<(unsigned)units_cap, 128, 0, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
+    }
     return ZP_OK;
-}
-
-inline int score_threads(const DecodeArgs &a) {
-    int t = a.T * a.h_kv;
-    t = (t + 31) / 32 * 32;
-    return t > 1024 ? 1024 : t;
 }
 
 struct Plan {
@@ -1192,7 +1200,7 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     p->off_pacc = off;
     off = align_up(off + (size_t)2 * p->grid * D->h_q * d * 4, 256);
     p->off_info = off;
-    off = align_up(off + (size_t)units_cap * 8, 256);
+    off = align_up(off + (size_t)units_cap * 16, 256);
     p->off_logits = off;
     off = align_up(off + (size_t)units_cap * p->T * D->h_q * 4, 256);
     p->total = off;
@@ -1215,14 +1223,7 @@ zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, c
     kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel launch");
-    zp_status rc = launch_merge<__nv_bfloat16, Dd>(a, p.grid, st);
-    if (rc != ZP_OK) return rc;
-    if (a.want_score) {
-        decode_score_kernel<G><<<(unsigned)p.logits_units, score_threads(a), 0, st>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
-    }
-    return ZP_OK;
+    return launch_finish<__nv_bfloat16, Dd, G>(a, p.grid, p.logits_units, st);
 }
 
 template <typename T, int Dd, int G>
@@ -1238,14 +1239,7 @@ zp_status launch_t(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cu
     kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: main kernel launch");
-    zp_status rc = launch_merge<T, Dd>(a, p.grid, st);
-    if (rc != ZP_OK) return rc;
-    if (a.want_score) {
-        decode_score_kernel<G><<<(unsigned)p.logits_units, score_threads(a), 0, st>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "decode: score kernel launch");
-    }
-    return ZP_OK;
+    return launch_finish<T, Dd, G>(a, p.grid, p.logits_units, st);
 }
 
 }  // namespace
@@ -1312,7 +1306,7 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.part_acc = reinterpret_cast<float *>(ws + p.off_pacc);
     a.part_ml = reinterpret_cast<float2 *>(ws + p.off_pml);
     a.unit_prefix = reinterpret_cast<int *>(ws + p.off_prefix);
-    a.unit_info = reinterpret_cast<int2 *>(ws + p.off_info);
+    a.unit_info = reinterpret_cast<int4 *>(ws + p.off_info);
     a.logits_units = p.logits_units;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
