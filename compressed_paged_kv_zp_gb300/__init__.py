@@ -29,6 +29,7 @@ STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTY
 EXPORTS = [
     "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
     "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
+    "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
@@ -80,7 +81,10 @@ def _load() -> ctypes.CDLL:
     lib.zp_needs_compression.argtypes = [I32, I32, I32]
     lib.zp_score_workspace_size.restype = SZ
     lib.zp_score_workspace_size.argtypes = [D, I32, I32]
-    lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P,
+    lib.zp_window_score_workspace_size.restype = SZ
+    lib.zp_window_score_workspace_size.argtypes = [D, I32, I32, I32]
+    lib.zp_window_score.argtypes = [D, P, I32, P, P, I32, P, I32, P, I32, P, SZ, P]
+    lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P, P,
                                     I32, P, SZ, P]
     lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
     lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, I32, P, I32, P, P, I32, I32, P]
@@ -179,8 +183,27 @@ def zp_score_workspace_size(desc: CacheDesc, n: int, Lmax: int) -> int:
     return int(lib.zp_score_workspace_size(ctypes.byref(desc), int(n), int(Lmax)))
 
 
+def zp_window_score_workspace_size(desc: CacheDesc, n: int, Lmax: int, window: int) -> int:
+    return int(lib.zp_window_score_workspace_size(ctypes.byref(desc), int(n), int(Lmax), int(window)))
+
+
+def zp_window_score(desc, q_window, k_cache, block_table, seq_lens, scores_out, workspace=None,
+                    stream=None) -> None:
+    n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    window = int(q_window.shape[1])
+    Lmax = int(scores_out.shape[-1])
+    if workspace is None:
+        workspace = torch.empty(max(zp_window_score_workspace_size(desc, n, Lmax, window), 1),
+                                dtype=torch.uint8, device=scores_out.device)
+    _check(lib.zp_window_score(ctypes.byref(desc), _dev(q_window, "q_window"), window,
+                               _dev(k_cache, "k_cache"), _dev(block_table, "block_table"), table_stride,
+                               _dev(seq_lens, "seq_lens"), n, _dev(scores_out, "scores_out"), Lmax,
+                               _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
 def zp_score_tokens(desc, params: ScoreParams, k_cache, block_table, seq_lens, first_compression,
-                    score_accum, global_F, scores_out, workspace=None, stream=None) -> None:
+                    score_accum, global_F, scores_out, workspace=None, stream=None,
+                    window_score=None) -> None:
     n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
     Lmax = int(scores_out.shape[-1])
     if workspace is None:
@@ -189,7 +212,8 @@ def zp_score_tokens(desc, params: ScoreParams, k_cache, block_table, seq_lens, f
     _check(lib.zp_score_tokens(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
                                _dev(block_table, "block_table"), table_stride,
                                _dev(seq_lens, "seq_lens"), _dev(first_compression, "first_compression"),
-                               n, _dev(score_accum, "score_accum"), _dev(global_F, "global_F"),
+                               n, _dev(score_accum, "score_accum"), _dev(window_score, "window_score"),
+                               _dev(global_F, "global_F"),
                                _dev(scores_out, "scores_out"), Lmax, _dev(workspace, "workspace"),
                                workspace.numel(), _stream(stream)))
 
@@ -295,5 +319,6 @@ class Pool:
 __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "score_params",
            "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn",
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
-           "zp_needs_compression", "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
+           "zp_needs_compression", "zp_window_score_workspace_size", "zp_window_score",
+           "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
            "zp_compact_pages", "zp_device_status", "Pool", "ZP_BF16", "ZP_F32"]

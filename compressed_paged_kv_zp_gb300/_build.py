@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzp.so")
 
-SOURCES = ["zp_api.cu", "decode_attn.cu", "append_kv.cu", "score.cu", "topk.cu", "compact.cu",
-           "pool.cpp"]
+SOURCES = ["zp_api.cu", "decode_attn.cu", "append_kv.cu", "window_score.cu", "score.cu", "topk.cu",
+           "compact.cu", "pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -30,7 +30,8 @@ struct ScoreArgs {
     const int32_t *seq_lens;
     const uint8_t *first;
     int n, h_kv, b, n_total, Lmax, d;
-    const float *S;   // paged [N_total][b][h_kv]
+    const float *S;   // paged [N_total][b][h_kv] (accumulated during decode), or NULL
+    const float *Sw;  // [n][h_kv][Lmax] (explicit window score), used when S is NULL
     float *F;         // paged, nullable
     float *X;         // [n][h_kv][Lmax]
     float *rho;       // [n][h_kv][Lmax]
@@ -75,7 +76,7 @@ __global__ void gather_global_kernel(const ScoreArgs a) {
                 record_error(a.err, ZP_ERR_DEVICE, 0x200);
             } else {
                 const size_t at = ((size_t)blk * a.b + t % a.b) * a.h_kv + kvh;
-                v = a.S[at];
+                v = a.S ? a.S[at] : a.Sw[((size_t)s * a.h_kv + kvh) * a.Lmax + t];
                 if (a.use_global) {
                     if (first) {
                         a.F[at] = v;
@@ -384,7 +385,8 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
                                      const void *k_cache, const int32_t *block_table,
                                      int32_t table_stride, const int32_t *seq_lens,
                                      const uint8_t *first_compression, int32_t n,
-                                     const float *score_accum, float *global_F, float *scores_out,
+                                     const float *score_accum, const float *window_score,
+                                     float *global_F, float *scores_out,
                                      int32_t Lmax, void *workspace, size_t workspace_bytes,
                                      void *stream) {
     zp_status rc = check_desc(D);
@@ -392,8 +394,10 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     if (!P) return fail(ZP_ERR_INVALID_ARG, "score: NULL params");
     if (n < 0 || Lmax < 0 || table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: bad sizes");
     if (n == 0 || Lmax == 0) return ok();
-    if (!block_table || !seq_lens || !score_accum || !scores_out || !workspace)
+    if (!block_table || !seq_lens || !scores_out || !workspace)
         return fail(ZP_ERR_INVALID_ARG, "score: NULL buffer");
+    if ((score_accum == nullptr) == (window_score == nullptr))
+        return fail(ZP_ERR_INVALID_ARG, "score: give exactly one of score_accum and window_score");
     if (P->use_global && !global_F) return fail(ZP_ERR_INVALID_ARG, "score: use_global needs global_F");
     if (P->use_similarity && !k_cache) return fail(ZP_ERR_INVALID_ARG, "score: similarity needs k_cache");
     if (P->window < 0) return fail(ZP_ERR_INVALID_ARG, "score: window %d", P->window);
@@ -423,6 +427,7 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     a.Lmax = Lmax;
     a.d = D->head_dim;
     a.S = score_accum;
+    a.Sw = window_score;
     a.F = global_F;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.X = reinterpret_cast<float *>(ws);

@@ -156,11 +156,29 @@ zp_status zp_append_kv(const zp_cache_desc *D, const void *k_new, const void *v_
 /* Compression trigger [Zipage §4.1]: 1 iff ceil(L/b) >= max_blocks and L%b == 0. */
 int32_t zp_needs_compression(int32_t seq_len, int32_t block_size, int32_t max_blocks);
 
+/* Explicit observation-window score [Zipage App. C.2, Alg. 1] of n sequences
+ * of one layer, for scoring without decode-time accumulation (a long prefill
+ * compressed at its first trigger).  q_window [n][window][h_q][d] (dtype)
+ * holds the queries of each sequence's `window` newest tokens, oldest first.
+ *   A[u,h,t] = q_{u,h} . k_t / sqrt(d), -inf where t > L - window + u (causal;
+ *              the mask printed in Alg. 1 is garbled, this is its reading)
+ *   S[kvh][t] = (1/window) * sum_u max_{h in group(kvh)} softmax_t(A[u,h,:])[t]
+ * scores_out: float [n][h_kv][Lmax], entries t >= L untouched.  Requires
+ * window <= L <= Lmax.  bf16 caches: h_kv <= 8, b a multiple of 16 and
+ * window * h_q/h_kv a multiple of 16 (ZP_ERR_SHAPE otherwise). */
+size_t zp_window_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax, int32_t window);
+zp_status zp_window_score(const zp_cache_desc *D, const void *q_window, int32_t window,
+                          const void *k_cache, const int32_t *block_table, int32_t table_stride,
+                          const int32_t *seq_lens, int32_t n, float *scores_out, int32_t Lmax,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
 
 /* Final per-token scores of n sequences of one layer, ready for the top-k
  * [Zipage App. C.2-C.8, §4.2], in the paper's order:
- *   S  <- score_accum gathered through the block table  (attention score)
+ *   S  <- score_accum gathered through the block table, or window_score
+ *         ([n][h_kv][Lmax], from zp_window_score): exactly one is non-NULL
+ *                                                        (attention score)
  *   S  <- Alg. 2 with global_F when use_global          (global score)
  *   Sp <- MaxPool1D(S) when pooling applies              (C.4, eq. 3)
  *   R  <- softmax_t(rho_t / (L*tau)) of the key redundancy (C.5 / C.7)
@@ -172,7 +190,8 @@ size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
 zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
                           const void *k_cache, const int32_t *block_table, int32_t table_stride,
                           const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
-                          const float *score_accum, float *global_F, float *scores_out,
+                          const float *score_accum, const float *window_score, float *global_F,
+                          float *scores_out,
                           int32_t Lmax, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Top-k keep set [Zipage §4.2, App. C.6]: for every (sequence, kv head) the k

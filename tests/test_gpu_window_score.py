@@ -1,0 +1,130 @@
+"""GPU parity of the explicit observation-window score (App. C.2, Alg. 1) and
+of the prefill-then-compress chain built on it.
+
+Cases: the tiny fp32 workload with w in {4, 8, 16}; Qwen3-8B-shaped bf16
+sequences long enough to span several CTA chunks of 64 pages, with a ragged
+last block; one long prefill (the 32k-token compression workload, sampled);
+and window score -> scores (global, first-compression pooling, lightning
+redundancy, eq. 4, window) -> top-k -> compaction against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zp_inputs
+from oracle import pipeline
+from tests.gpu_util import TOL_SCORE, DeviceCase, keep_sets_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def zp():
+    import compressed_paged_kv_zp_gb300 as m
+    return m
+
+
+def _desc(zp, c):
+    return zp.cache_desc(c.h_q, c.h_kv, c.d, c.b, c.n_total,
+                         torch.bfloat16 if c.dtype == "bf16" else torch.float32)
+
+
+def _window_case(seed, B, h_q, h_kv, d, b, lens, dtype, w):
+    c = zp_inputs.make_paged_case(seed, B, h_q, h_kv, d, b, lens=lens, dtype=dtype)
+    qw = zp_inputs.normal((B, w, h_q, d), seed + 1, dtype)
+    return c, qw
+
+
+@pytest.mark.parametrize("dtype,h_q,h_kv,d,w,lens", [
+    ("f32", 8, 2, 64, 4, [80, 150, 97, 121]),
+    ("f32", 8, 2, 64, 16, [80, 150, 97, 121]),
+    ("bf16", 32, 8, 128, 16, [16, 33, 1000, 1040, 2100]),
+    ("bf16", 32, 8, 128, 8, [500, 1500]),
+    ("bf16", 32, 8, 128, 4, [64, 1100]),
+])
+def test_window_score_matches_oracle(zp, dtype, h_q, h_kv, d, w, lens):
+    c, qw = _window_case(60 + w + len(lens), len(lens), h_q, h_kv, d, 16, lens, dtype, w)
+    dc = DeviceCase(c)
+    Lmax = max(lens) + 7
+    out = torch.full((c.B, h_kv, Lmax), -3.0, device="cuda")
+    zp.zp_window_score(_desc(zp, c), qw.cuda(), dc.K[0], dc.table, dc.lens, out)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    got = out.cpu().numpy()
+    K = dc.np_k()
+    for s, L in enumerate(lens):
+        ref = oracle.window_score(qw[s].float().numpy(), K, c.block_table[s].numpy(), L, w)
+        np.testing.assert_allclose(got[s, :, :L], ref, **TOL_SCORE[dtype])
+        assert np.all(got[s, :, L:] == -3.0)
+
+
+def test_window_score_long_prefill_sampled(zp):
+    """The 32k-token prefill of the compression workload (16 sequences at full
+    size in the benchmark); here 2 sequences, checked on sampled kv heads."""
+    lens = [32768, 20000]
+    c, qw = _window_case(77, 2, 32, 8, 128, 16, lens, "bf16", 16)
+    dc = DeviceCase(c)
+    out = torch.empty(2, 8, 32768, device="cuda")
+    zp.zp_window_score(_desc(zp, c), qw.cuda(), dc.K[0], dc.table, dc.lens, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    K = dc.np_k()
+    for s, L in enumerate(lens):
+        # the oracle over all heads of the sequence (about 2 G multiply-adds)
+        ref = oracle.window_score(qw[s].float().numpy(), K, c.block_table[s].numpy(), L, 16)
+        np.testing.assert_allclose(got[s, :, :L], ref, **TOL_SCORE["bf16"])
+        # each window row's softmax sums to one: sum_t S <= G and >= 1
+        tot = got[s, :, :L].sum(axis=1)
+        assert np.all(tot > 1.0 - 1e-3) and np.all(tot < 4.0 + 1e-3)
+
+
+@pytest.mark.parametrize("shape", ["tiny", "qwen"])
+def test_prefill_then_compress(zp, shape):
+    """First compression of long prefills: window score -> final scores ->
+    top-k -> compaction into the first N_max - 1 blocks, against the oracle."""
+    if shape == "tiny":
+        B, h_q, h_kv, d, N_max, dtype, lens = 3, 8, 2, 64, 4, "f32", [96, 144, 128]
+    else:
+        B, h_q, h_kv, d, N_max, dtype, lens = 3, 32, 8, 128, 8, "bf16", [1024, 2048, 1520]
+    b, w = 16, 16
+    c, qw = _window_case(88 + len(shape), B, h_q, h_kv, d, b, lens, dtype, w)
+    zp_inputs.plant_duplicates(c, 89)
+    dc = DeviceCase(c)
+    desc = _desc(zp, c)
+    Lmax = max(lens)
+    S = torch.empty(B, h_kv, Lmax, device="cuda")
+    zp.zp_window_score(desc, qw.cuda(), dc.K[0], dc.table, dc.lens, S)
+    F = torch.zeros(c.n_total, b, h_kv, device="cuda")
+    first = torch.ones(B, dtype=torch.uint8, device="cuda")
+    scores = torch.empty(B, h_kv, Lmax, device="cuda")
+    zp.zp_score_tokens(desc, zp.score_params(window=w), dc.K[0], dc.table, dc.lens, first, None, F, scores,
+                       window_score=S)
+    k = (N_max - 1) * b
+    keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
+    zp.zp_select_topk(scores, dc.lens, k, keep)
+    targets = c.block_table[:, : N_max - 1].contiguous().cuda()
+    zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    K0 = c.k_cache[0].float().numpy()
+    V0 = c.v_cache[0].float().numpy()
+    Kg = dc.K[0].float().cpu().numpy()
+    Vg = dc.V[0].float().cpu().numpy()
+    kept = keep.cpu().numpy()
+    prm = pipeline.ScoreParams(window=w)
+    swaps = 0
+    for s, L in enumerate(lens):
+        Sref = oracle.window_score(qw[s].float().numpy(), K0, c.block_table[s].numpy(), L, w)
+        Fref = np.zeros((c.n_total, b, h_kv))
+        sref = pipeline.final_scores(Sref, K0, Fref, c.block_table[s].numpy(), L, b, True, prm)
+        for h in range(h_kv):
+            kref = oracle.topk_keep(sref[h], k)[0]
+            swaps += keep_sets_match(kept[s, h], kref, sref[h], k, L)
+            for r in range(0, k, 5):
+                pos = kept[s, h, r]
+                sb, ss = c.block_table[s, pos // b], pos % b
+                db, ds = c.block_table[s, r // b], r % b
+                assert np.array_equal(Kg[db, ds, h], K0[sb, ss, h])
+                assert np.array_equal(Vg[db, ds, h], V0[sb, ss, h])
+    print("reported tie swaps:", swaps)
