@@ -14,7 +14,8 @@ __global__ void append_kv_kernel(const uint4 *k_new, const uint4 *v_new, uint4 *
                                  int b, int n_total, int row_vec, unsigned *err) {
     const int s = blockIdx.x;
     const int L = seq_lens[s];
-    if (L <= 0 || L > table_stride * b) {
+    if (L == 0) return;  // no token for this sequence in this step
+    if (L < 0 || L > table_stride * b) {
         if (threadIdx.x == 0) record_error(err, ZP_ERR_DEVICE, 0x100);
         return;
     }

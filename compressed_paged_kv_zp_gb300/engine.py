@@ -1,0 +1,176 @@
+"""Multi-step decode with Compressed PagedAttention on one GPU.
+
+The host side of the hot path around the libzp kernels:
+  * block allocation as sequences grow (Zipage paper §3);
+  * the compression trigger after every step: N >= N_max blocks and the last
+    block full (§4.1);
+  * target blocks from the reference-counted pool, one planner call for all
+    triggered sequences (§4.4);
+  * scoring, top-k and compaction on a side stream, ordered after the decode
+    that produced the window score by a CUDA event (§4.5); in asynchronous
+    mode the compressing sequences sit out decode until their event has
+    completed, then rejoin with their new block table, while everybody else
+    keeps decoding;
+  * the blocks a compressed sequence no longer holds go back to the pool only
+    after the compaction that reads them has completed.
+All device work is libzp calls; torch provides memory, streams and events.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compact_pages,
+               zp_decode_workspace_size, zp_paged_decode_attn, zp_score_tokens,
+               zp_score_workspace_size, zp_select_topk)
+
+
+class DecodeLoop:
+    """Batch of sequences decoding over `layers` paged layers of one pool."""
+
+    def __init__(self, h_q, h_kv, d, b, n_total, max_blocks, table_stride, layers=1, dtype=torch.bfloat16,
+                 window=None, params=None, async_compress=False, device="cuda"):
+        self.h_q, self.h_kv, self.d, self.b = h_q, h_kv, d, b
+        self.n_total, self.N_max, self.stride, self.layers = n_total, max_blocks, table_stride, layers
+        self.k = (max_blocks - 1) * b
+        self.window = window or b
+        self.dtype = dtype
+        self.dev = torch.device(device)
+        self.desc = cache_desc(h_q, h_kv, d, b, n_total, dtype)
+        self.params = params or score_params(window=self.window)
+        self.async_compress = async_compress
+        self.K = torch.zeros(layers, n_total, b, h_kv, d, dtype=dtype, device=self.dev)
+        self.V = torch.zeros_like(self.K)
+        self.S = torch.zeros(layers, n_total, b, h_kv, dtype=torch.float32, device=self.dev)
+        self.F = torch.zeros_like(self.S)
+        self.pool = Pool(n_total)
+        self.side = torch.cuda.Stream(device=self.dev)
+        self.B = 0
+        self.compressions = 0
+        self.pending = []  # (event, seqs, plan) of compressions in flight
+
+    # ------------------------------------------------------------------ setup
+    def add_sequences(self, lens, tables=None):
+        """Register B sequences with `lens` cached tokens.  Their blocks come
+        from the pool (lowest ids first) unless `tables` (np int32 [B][stride],
+        already holding the sequences' block ids) is given; the caller fills
+        the cache rows of those tokens directly (prefill is out of scope)."""
+        lens = np.asarray(lens, dtype=np.int32)
+        B = len(lens)
+        self.B = B
+        self.lens = lens.copy()
+        self.table = np.full((B, self.stride), -1, dtype=np.int32)
+        if tables is None:
+            for s in range(B):
+                nb = (int(lens[s]) + self.b - 1) // self.b
+                self.table[s, :nb] = self.pool.alloc(nb)
+        else:
+            self.table[:] = tables
+            used = sorted(set(int(x) for x in tables.flatten() if x >= 0))
+            self.pool.alloc(self.n_total)  # take every block, then give back the unused ones
+            self.pool.release([i for i in range(self.n_total) if i not in set(used)])
+            refs = {}
+            for x in tables.flatten():
+                if x >= 0:
+                    refs[int(x)] = refs.get(int(x), 0) + 1
+            for blk, r in refs.items():  # shared prefix blocks: one reference per holder
+                if r > 1:
+                    self.pool.incref([blk] * (r - 1))
+        self.first = np.ones(B, dtype=np.uint8)  # never compressed yet
+        self.active = np.ones(B, dtype=bool)
+        self.table_dev = torch.from_numpy(self.table).to(self.dev)
+        self.ws = torch.empty(zp_decode_workspace_size(self.desc, B, self.stride), dtype=torch.uint8,
+                              device=self.dev)
+        Lmax = self.stride * self.b
+        self.score_ws = torch.empty(max(zp_score_workspace_size(self.desc, B, Lmax), 1), dtype=torch.uint8,
+                                    device=self.dev)
+        self.scores = torch.empty(B, self.h_kv, Lmax, dtype=torch.float32, device=self.dev)
+        self.out = torch.zeros(self.layers, B, self.h_q, self.d, dtype=self.dtype, device=self.dev)
+
+    def layer_stride(self):
+        return self.n_total * self.b * self.h_kv * self.d
+
+    # ------------------------------------------------------------------ step
+    def step(self, q, k_new, v_new):
+        """One decode step: q [layers][B][h_q][d], k_new/v_new [layers][B][h_kv][d].
+        Returns the indices of the sequences that started a compression."""
+        self._retire(block=not self.async_compress)
+        act = self.active
+        # grow: a sequence whose next token opens a block takes one from the
+        # pool (a compressed sequence already holds its reserved block there)
+        for s in np.nonzero(act)[0]:
+            pos = int(self.lens[s])  # position of the new token
+            if pos % self.b == 0 and self.table[s, pos // self.b] < 0:
+                self.table[s, pos // self.b] = self.pool.alloc(1)[0]
+        self.lens[act] += 1
+        self.table_dev.copy_(torch.from_numpy(self.table), non_blocking=False)
+        step_lens = torch.from_numpy(np.where(act, self.lens, 0).astype(np.int32)).to(self.dev)
+        main = torch.cuda.current_stream(self.dev)
+        for l in range(self.layers):
+            zp_append_kv(self.desc, k_new[l], v_new[l], self.K[l], self.V[l], self.table_dev, step_lens)
+            zp_paged_decode_attn(self.desc, q[l], self.K[l], self.V[l], self.table_dev, step_lens, self.out[l],
+                                 score_accum=self.S[l], window=self.window, workspace=self.ws)
+        trig = [s for s in np.nonzero(act)[0]
+                if (self.lens[s] + self.b - 1) // self.b >= self.N_max and self.lens[s] % self.b == 0]
+        if trig:
+            self._compress(np.array(trig, dtype=np.int64), main)
+        return trig
+
+    def _compress(self, seqs, main):
+        n = len(seqs)
+        nb = (self.lens[seqs] // self.b).astype(np.int32)
+        sub_tables = np.ascontiguousarray(self.table[seqs])
+        plan = self.pool.plan_compaction_batch(sub_tables, nb, self.N_max)
+        tables_dev = torch.from_numpy(sub_tables).to(self.dev)
+        lens_dev = torch.from_numpy(self.lens[seqs].astype(np.int32)).to(self.dev)
+        first_dev = torch.from_numpy(self.first[seqs].copy()).to(self.dev)
+        targets_dev = torch.from_numpy(np.ascontiguousarray(plan["targets"])).to(self.dev)
+        ready = torch.cuda.Event()
+        ready.record(main)
+        with torch.cuda.stream(self.side):
+            self.side.wait_event(ready)
+            scores = self.scores[:n]
+            keep = torch.empty(self.layers, n, self.h_kv, self.k, dtype=torch.int32, device=self.dev)
+            for l in range(self.layers):
+                zp_score_tokens(self.desc, self.params, self.K[l], tables_dev, lens_dev, first_dev, self.S[l],
+                                self.F[l], scores, workspace=self.score_ws)
+                zp_select_topk(scores, lens_dev, self.k, keep[l])
+            zp_compact_pages(self.desc, self.K, self.V, self.layer_stride(), self.layers, self.F,
+                             self.n_total * self.b * self.h_kv, tables_dev, targets_dev, lens_dev, keep, self.k)
+            done = torch.cuda.Event()
+            done.record(self.side)
+        for t in (tables_dev, lens_dev, first_dev, targets_dev):
+            t.record_stream(self.side)
+        self.active[seqs] = False
+        self.last_keep = (seqs, keep)  # for inspection: [layers][n][h_kv][k]
+        self.pending.append((done, seqs, plan, keep))
+        self.compressions += n
+        if not self.async_compress:
+            main.wait_event(done)
+
+    def _retire(self, block=False):
+        """Apply the compressions that have finished: new tables, lengths and
+        the release of the blocks the sequences dropped."""
+        still = []
+        for done, seqs, plan, keep in self.pending:
+            if block:
+                torch.cuda.current_stream(self.dev).wait_event(done)
+            elif not done.query():
+                still.append((done, seqs, plan, keep))
+                continue
+            for i, s in enumerate(seqs):
+                self.table[s, :] = -1
+                self.table[s, : self.N_max] = plan["new_tables"][i]
+                self.lens[s] = self.k
+                self.first[s] = 0
+                self.active[s] = True
+                nd = int(plan["n_dropped"][i])
+                if nd:
+                    self.pool.release(plan["dropped"][i, :nd].tolist())
+        self.pending = still
+
+    def drain(self):
+        for done, _, _, _ in self.pending:
+            done.synchronize()
+        self._retire(block=True)
+

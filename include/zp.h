@@ -146,7 +146,9 @@ zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q, co
 /* Writes the new token's key and value of each sequence into its slot
  * [Zipage §3: the cache of a block is written into the block's slots]:
  * k_new, v_new [B][h_kv][d] go to slot (L-1) % b of block table[(L-1)/b],
- * where L = seq_lens[s] already counts the new token. */
+ * where L = seq_lens[s] already counts the new token.  L = 0 skips the
+ * sequence (no token this step); zp_paged_decode_attn likewise skips
+ * sequences with L = 0 and leaves their output rows untouched. */
 zp_status zp_append_kv(const zp_cache_desc *D, const void *k_new, const void *v_new,
                        void *k_cache, void *v_cache, const int32_t *block_table,
                        int32_t table_stride, const int32_t *seq_lens, int32_t B, void *stream);

@@ -1,0 +1,159 @@
+"""Multi-step decode with compression: the DecodeLoop driver against an oracle
+loop, step by step (the high-concurrency workload, scaled down).
+
+Every step both sides grow the block tables (lowest free block first), append
+the new token, run decode with the window-score accumulation and apply the
+§4.1 trigger; triggered sequences are scored, ranked and compacted into the
+§4.4 target blocks, their tables swapped, and the blocks they dropped
+released.  Checked every step: attention outputs (tolerance), block tables,
+lengths and the free pool (exact); at every compression: keep sets (exact up
+to reported near-ties, after which the oracle adopts the GPU's choice so both
+states stay identical), the moved K/V rows (bit-exact) and F.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zp_inputs
+from oracle import pipeline
+from tests.gpu_util import TOL_OUT, keep_sets_match
+
+pytestmark = pytest.mark.gpu
+
+
+class OracleLoop:
+    """The same loop on the oracle (fp64 arithmetic, float32 caches holding the
+    bf16 values, a Python mirror of the pool)."""
+
+    def __init__(self, cfg, K, V, table, lens):
+        self.c = cfg
+        self.K, self.V = K.copy(), V.copy()  # [layers][N_total][b][h_kv][d] float32
+        self.S = np.zeros(K.shape[:-1])      # [layers][N_total][b][h_kv] fp64
+        self.F = np.zeros(K.shape[:-1])
+        self.table = table.copy()
+        self.lens = lens.copy()
+        self.first = np.ones(len(lens), dtype=bool)
+        self.ref = np.zeros(cfg["n_total"], dtype=np.int32)
+        for x in table.flatten():
+            if x >= 0:
+                self.ref[x] += 1
+
+    def alloc(self):
+        free = np.nonzero(self.ref == 0)[0]
+        blk = int(free[0])
+        self.ref[blk] = 1
+        return blk
+
+    def step(self, q, kn, vn):
+        c = self.c
+        b = c["b"]
+        for s in range(len(self.lens)):
+            pos = int(self.lens[s])
+            if pos % b == 0 and self.table[s, pos // b] < 0:
+                self.table[s, pos // b] = self.alloc()
+        self.lens += 1
+        outs = []
+        for l in range(c["layers"]):
+            for s in range(len(self.lens)):
+                P = int(self.lens[s]) - 1
+                blk = self.table[s, P // b]
+                self.K[l, blk, P % b] = kn[l, s]
+                self.V[l, blk, P % b] = vn[l, s]
+            out, probs = oracle.decode_attention(q[l], self.K[l], self.V[l], self.table, self.lens, want_probs=True)
+            S = np.ascontiguousarray(self.S[l])
+            oracle.accumulate_window_score(probs, self.table, self.lens, c["h_kv"], b, c["w"], S)
+            self.S[l] = S
+            outs.append(out)
+        trig = [s for s in range(len(self.lens)) if oracle.needs_compression(int(self.lens[s]), b, c["N_max"])]
+        return np.stack(outs), trig
+
+    def compress(self, s, gpu_keep):
+        """Scores and keep sets of sequence s on every layer; returns the number
+        of reported near-tie swaps.  The moves use the GPU's keep sets."""
+        c = self.c
+        b, N_max = c["b"], c["N_max"]
+        L = int(self.lens[s])
+        k = (N_max - 1) * b
+        N = L // b
+        fresh = np.nonzero(self.ref == 0)[0].astype(np.int32)
+        plan = oracle.plan_targets(self.table[s, :N], N_max, self.ref, fresh)
+        for blk in plan["new_table"]:
+            if self.ref[blk] == 0:
+                self.ref[blk] = 1
+        swaps = 0
+        prm = pipeline.ScoreParams(window=c["w"])
+        for l in range(c["layers"]):
+            S_seq = pipeline.gather_slots(self.S[l], self.table[s], L, b)
+            F = np.ascontiguousarray(self.F[l])
+            sc = pipeline.final_scores(S_seq, self.K[l], F, self.table[s], L, b, bool(self.first[s]), prm)
+            self.F[l] = F
+            for h in range(c["h_kv"]):
+                ref_keep = oracle.topk_keep(sc[h], k)[0]
+                swaps += keep_sets_match(gpu_keep[l, h], ref_keep, sc[h], k, L)
+        pipeline.compact_sequence([self.K, self.V, self.F], [c["d"] * 4, c["d"] * 4, 8], b, c["h_kv"],
+                                  self.table[s], N, plan["targets"], gpu_keep, L)
+        for blk in list(plan["released"]) + list(plan["dropped_shared"]):
+            self.ref[blk] -= 1
+        self.table[s, :] = -1
+        self.table[s, :N_max] = plan["new_table"]
+        self.lens[s] = k
+        self.first[s] = False
+        return swaps
+
+
+@pytest.mark.parametrize("layers,async_compress", [(1, False), (2, False), (2, True)])
+def test_decode_loop_matches_oracle_loop(layers, async_compress):
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    cfg = dict(h_q=16, h_kv=4, d=64, b=16, N_max=4, w=16, layers=layers, n_total=160)
+    B, steps, stride = 6, 44, 12
+    torch.manual_seed(0)
+    g = torch.Generator().manual_seed(123 + layers)
+    lens0 = torch.randint(30, 70, (B,), generator=g).numpy().astype(np.int32)
+    loop = DecodeLoop(cfg["h_q"], cfg["h_kv"], cfg["d"], cfg["b"], cfg["n_total"], cfg["N_max"], stride,
+                      layers=layers, dtype=torch.bfloat16, window=cfg["w"], async_compress=async_compress)
+    loop.add_sequences(lens0)
+    # synthetic prefill: random rows in every block the sequences hold
+    loop.K.copy_(zp_inputs.normal(tuple(loop.K.shape), 7, "bf16").cuda())
+    loop.V.copy_(zp_inputs.normal(tuple(loop.V.shape), 8, "bf16").cuda())
+    ora = OracleLoop(cfg, loop.K.float().cpu().numpy(), loop.V.float().cpu().numpy(), loop.table, loop.lens)
+    total_swaps, compressions = 0, 0
+    for step in range(steps):
+        q = zp_inputs.normal((layers, B, cfg["h_q"], cfg["d"]), 1000 + step, "bf16")
+        kn = zp_inputs.normal((layers, B, cfg["h_kv"], cfg["d"]), 2000 + step, "bf16")
+        vn = zp_inputs.normal((layers, B, cfg["h_kv"], cfg["d"]), 3000 + step, "bf16")
+        if async_compress:
+            loop.drain()  # the oracle has no overlap: keep both sides in the same state
+        trig = loop.step(q.cuda(), kn.cuda(), vn.cuda())
+        torch.cuda.synchronize()
+        out_ref, trig_ref = ora.step(q.float().numpy(), kn.float().numpy(), vn.float().numpy())
+        assert sorted(int(x) for x in trig) == trig_ref
+        got = loop.out.float().cpu().numpy()
+        np.testing.assert_allclose(got, out_ref, **TOL_OUT["bf16"])
+        if trig:
+            seqs, keep = loop.last_keep
+            keep = keep.cpu().numpy()
+            for i, s in enumerate(seqs):
+                total_swaps += ora.compress(int(s), keep[:, i])
+                compressions += 1
+            loop.drain()
+            torch.cuda.synchronize()
+            # state after compression: tables, lengths, caches of the compressed rows
+            assert np.array_equal(loop.table, ora.table)
+            assert np.array_equal(loop.lens, ora.lens)
+            Kg = loop.K.float().cpu().numpy()
+            Vg = loop.V.float().cpu().numpy()
+            for s in seqs:
+                for blk in ora.table[s, : cfg["N_max"] - 1]:
+                    assert np.array_equal(Kg[:, blk], ora.K[:, blk])
+                    assert np.array_equal(Vg[:, blk], ora.V[:, blk])
+                    np.testing.assert_allclose(loop.F[:, blk].cpu().numpy(), ora.F[:, blk], rtol=1e-3, atol=1e-9)
+        assert loop.pool.num_free == int((ora.ref == 0).sum())
+    assert zp_device_clean()
+    assert compressions >= B  # every sequence compressed at least once
+    print("compressions", compressions, "reported tie swaps", total_swaps)
+
+
+def zp_device_clean():
+    import compressed_paged_kv_zp_gb300 as zp
+    return zp.zp_device_status() == (0, 0)
