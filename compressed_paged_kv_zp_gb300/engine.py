@@ -97,11 +97,16 @@ class DecodeLoop:
         self._retire(block=not self.async_compress)
         act = self.active
         # grow: a sequence whose next token opens a block takes one from the
-        # pool (a compressed sequence already holds its reserved block there)
-        for s in np.nonzero(act)[0]:
-            pos = int(self.lens[s])  # position of the new token
-            if pos % self.b == 0 and self.table[s, pos // self.b] < 0:
-                self.table[s, pos // self.b] = self.pool.alloc(1)[0]
+        # pool (a compressed sequence already holds its reserved block there);
+        # blocks go out in sequence order, lowest free id first
+        idx = np.nonzero(act)[0]
+        pos = self.lens[idx]
+        col = pos // self.b
+        need = idx[(pos % self.b == 0) & (self.table[idx, np.minimum(col, self.stride - 1)] < 0)]
+        if len(need):
+            if int(self.lens[need].max()) // self.b >= self.stride:
+                raise RuntimeError("a sequence outgrew table_stride blocks")
+            self.table[need, self.lens[need] // self.b] = self.pool.alloc(len(need))
         self.lens[act] += 1
         self.table_dev.copy_(torch.from_numpy(self.table), non_blocking=False)
         step_lens = torch.from_numpy(np.where(act, self.lens, 0).astype(np.int32)).to(self.dev)
@@ -110,11 +115,11 @@ class DecodeLoop:
             zp_append_kv(self.desc, k_new[l], v_new[l], self.K[l], self.V[l], self.table_dev, step_lens)
             zp_paged_decode_attn(self.desc, q[l], self.K[l], self.V[l], self.table_dev, step_lens, self.out[l],
                                  score_accum=self.S[l], window=self.window, workspace=self.ws)
-        trig = [s for s in np.nonzero(act)[0]
-                if (self.lens[s] + self.b - 1) // self.b >= self.N_max and self.lens[s] % self.b == 0]
-        if trig:
-            self._compress(np.array(trig, dtype=np.int64), main)
-        return trig
+        L = self.lens
+        trig = np.nonzero(act & ((L + self.b - 1) // self.b >= self.N_max) & (L % self.b == 0))[0]
+        if len(trig):
+            self._compress(trig.astype(np.int64), main)
+        return trig.tolist()
 
     def _compress(self, seqs, main):
         n = len(seqs)

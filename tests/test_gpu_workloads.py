@@ -1,0 +1,161 @@
+"""The larger decode-with-compression workloads at full size, on the
+DecodeLoop driver.
+
+* High concurrency: 32q/8kv/128 bf16, b = 16, 512 sequences starting at
+  contexts uniform in [1024, 4096], budget N_max = 128 blocks (2032 tokens
+  kept), 2048 decode steps with compression whenever the §4.1 trigger holds.
+  Checked: no device error; every sequence compressed; none holds more than
+  N_max blocks; the pool accounts for every block; sampled keep sets are
+  ascending and complete; the last step's attention output of sampled
+  sequences against the oracle on the cache as the kernels left it.
+* Prefix-shared, 36 layers: 32q/8kv/128 bf16, 32 sequences sharing a
+  1024-token prefix (64 blocks), private tails uniform in [0, 2048], budget
+  N_max = 64 blocks, compression asynchronous on the side stream while the
+  others decode.  A prefix cache holds one more reference to the prefix, so
+  every compaction must go to fresh target blocks (§4.4).  Checked: the
+  prefix blocks are never written; after all sequences compressed, only the
+  prefix cache holds them; the sequences' blocks are disjoint and at most
+  N_max each; the pool accounts for every block; decode outputs of sampled
+  sequences on the first and last layer against the oracle.
+The cache contents are drawn on the device from seeded generators; the oracle
+reads back the blocks it checks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.gpu_util import TOL_OUT
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_normal(shape, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(*shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+
+
+def _check_pool(loop, extra=()):
+    held = {}
+    for x in list(loop.table[loop.table >= 0].ravel()) + list(extra):
+        held[int(x)] = held.get(int(x), 0) + 1
+    for blk, r in held.items():
+        assert loop.pool.refcount(blk) == r, (blk, r)
+    assert loop.pool.num_free + len(held) == loop.n_total
+
+
+def _oracle_decode(loop, layer, q, seqs):
+    """Oracle attention of `seqs` on layer `layer`, reading back only the
+    blocks those sequences hold (renumbered)."""
+    tab = loop.table[seqs]
+    blocks = np.unique(tab[tab >= 0])
+    remap = np.full(loop.n_total, -1, dtype=np.int32)
+    remap[blocks] = np.arange(len(blocks), dtype=np.int32)
+    sub = np.where(tab >= 0, remap[np.maximum(tab, 0)], -1).astype(np.int32)
+    idx = torch.from_numpy(blocks.astype(np.int64)).to(loop.K.device)
+    K = loop.K[layer].index_select(0, idx).float().cpu().numpy()
+    V = loop.V[layer].index_select(0, idx).float().cpu().numpy()
+    return oracle.decode_attention(q.float().cpu().numpy(), K, V, sub, loop.lens[seqs])
+
+
+def test_high_concurrency_512_sequences_2048_steps():
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    B, h_q, h_kv, d, b, N_max, steps = 512, 32, 8, 128, 16, 128, 2048
+    g = torch.Generator().manual_seed(1003)
+    lens0 = torch.randint(1024, 4097, (B,), generator=g).numpy().astype(np.int32)
+    stride = 4096 // b + 2
+    n_total = int(np.maximum((lens0 + b - 1) // b + 1, N_max).sum()) + 64
+    loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=1, dtype=torch.bfloat16, window=b)
+    loop.add_sequences(lens0)
+    loop.K.copy_(_dev_normal(loop.K.shape, 11))
+    loop.V.copy_(_dev_normal(loop.V.shape, 12))
+    compressed = np.zeros(B, dtype=bool)
+    for step in range(steps):
+        q = _dev_normal((1, B, h_q, d), 100000 + step)
+        kn = _dev_normal((1, B, h_kv, d), 200000 + step)
+        vn = _dev_normal((1, B, h_kv, d), 300000 + step)
+        trig = loop.step(q, kn, vn)
+        if trig:
+            compressed[trig] = True
+            if step % 97 == 0:
+                seqs, keep = loop.last_keep
+                kp = keep[0].cpu().numpy()  # [n][h_kv][k]
+                assert np.all(np.diff(kp, axis=-1) > 0) and np.all(kp[..., 0] >= 0)
+    decoded = np.nonzero(loop.active)[0]  # decoded in the last step and not compacting now
+    torch.cuda.synchronize()
+    sample = decoded[[0, len(decoded) // 3, 2 * len(decoded) // 3, -1]]
+    ref = _oracle_decode(loop, 0, q[0][torch.from_numpy(sample).cuda()], sample)
+    np.testing.assert_allclose(loop.out[0][torch.from_numpy(sample).cuda()].float().cpu().numpy(), ref,
+                               **TOL_OUT["bf16"])
+    loop.drain()
+    torch.cuda.synchronize()
+    import compressed_paged_kv_zp_gb300 as zp
+    assert zp.zp_device_status() == (0, 0)
+    assert compressed.all()
+    assert (loop.table >= 0).sum(axis=1).max() <= N_max
+    _check_pool(loop)
+    print("compressions:", loop.compressions)
+
+
+def test_prefix_shared_36_layers_async():
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    B, h_q, h_kv, d, b, N_max, layers, steps = 32, 32, 8, 128, 16, 64, 36, 40
+    g = torch.Generator().manual_seed(1005)
+    lens0 = (1024 + torch.randint(0, 2049, (B,), generator=g).numpy()).astype(np.int32)
+    P = 1024 // b
+    stride = (1024 + 2048 + 64) // b + 2
+    own = (lens0 + b - 1) // b - P
+    n_total = P + int(own.sum()) + B * (N_max + 2) + 64
+    table = np.full((B, stride), -1, dtype=np.int32)
+    perm = torch.randperm(n_total, generator=g).numpy().astype(np.int32)
+    table[:, :P] = perm[:P]
+    cur = P
+    for s in range(B):
+        table[s, P:P + own[s]] = perm[cur:cur + own[s]]
+        cur += own[s]
+    loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=layers, dtype=torch.bfloat16, window=b,
+                      async_compress=True)
+    loop.add_sequences(lens0, tables=table)
+    prefix = table[0, :P].copy()
+    loop.pool.incref(prefix.tolist())  # the prefix cache's own reference
+    loop.K.copy_(_dev_normal(loop.K.shape, 21))
+    loop.V.copy_(_dev_normal(loop.V.shape, 22))
+    pidx = torch.from_numpy(prefix.astype(np.int64)).cuda()
+    K_prefix = loop.K.index_select(1, pidx).clone()
+    V_prefix = loop.V.index_select(1, pidx).clone()
+    assert all(loop.pool.refcount(int(x)) == B + 1 for x in prefix)
+    seen = np.zeros(B, dtype=bool)
+    checked = 0
+    for step in range(steps):
+        q = _dev_normal((layers, B, h_q, d), 400000 + step)
+        kn = _dev_normal((layers, B, h_kv, d), 500000 + step)
+        vn = _dev_normal((layers, B, h_kv, d), 600000 + step)
+        trig = loop.step(q, kn, vn)
+        seen[trig] = True
+        if trig:
+            plan = loop.pending[-1][2]
+            assert not set(plan["targets"].ravel().tolist()) & set(prefix.tolist())
+        if step % 7 == 3:
+            decoded = np.nonzero(loop.active)[0]
+            torch.cuda.synchronize()
+            s = decoded[step % len(decoded): step % len(decoded) + 1]
+            for l in (0, layers - 1):
+                ref = _oracle_decode(loop, l, q[l, s], s)
+                np.testing.assert_allclose(loop.out[l, s].float().cpu().numpy(), ref, **TOL_OUT["bf16"])
+                checked += 1
+    loop.drain()
+    torch.cuda.synchronize()
+    import compressed_paged_kv_zp_gb300 as zp
+    assert zp.zp_device_status() == (0, 0)
+    assert seen.all() and checked > 0
+    assert torch.equal(loop.K.index_select(1, pidx), K_prefix)
+    assert torch.equal(loop.V.index_select(1, pidx), V_prefix)
+    assert all(loop.pool.refcount(int(x)) == 1 for x in prefix)
+    assert not set(loop.table[loop.table >= 0].tolist()) & set(prefix.tolist())
+    held = [loop.table[s][loop.table[s] >= 0] for s in range(B)]
+    assert max(len(h) for h in held) <= N_max
+    allb = np.concatenate(held)
+    assert len(np.unique(allb)) == len(allb)
+    _check_pool(loop, extra=prefix.tolist())
+    print("compressions:", loop.compressions)
