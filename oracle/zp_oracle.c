@@ -279,24 +279,27 @@ int orc_max_pool(int L, int kernel, const double *x, double *y) {
 /* Redundancy score of the keys [Zipage App. C.5 (full, Fig. 11), C.7        */
 /* (lightning, Fig. 15), C.8 (temperature)].                                 */
 /*                                                                           */
-/* keys is one sequence's keys of one KV head, gathered, [L][d].            */
-/*   C[r][c] = cos(k_r, k_c)  for pairs in the domain, 0 elsewhere           */
-/*             domain = all pairs (full) or same-block pairs, i.e.           */
-/*             r / b == c / b (lightning)                                    */
+/* keys is one sequence's keys of one KV head, gathered, [L][d].  The pair  */
+/* domain splits the positions into groups: one group [0, L) for the full   */
+/* score, the blocks [j*b, min((j+1)*b, L)) for the lightning score (only    */
+/* same-block pairs are compared).  Within a group of m positions:           */
+/*   C[r][c] = cos(k_r, k_c)                                                 */
 /*   C[c][c] = 0                                                             */
 /*   for each column c: r* = largest r with C[r][c] > p; C[r*][c] = 0        */
 /*   rho[r] = sum_c C[r][c]                                                  */
+/* and over the whole sequence                                               */
 /*   R = softmax_t( rho[t] / (L * tau) )                                     */
 /* A key of zero norm has cosine 0 with every key.  The paper normalises by  */
 /* the sequence length for the full score and does not restate it for the    */
 /* lightning score; C.7 changes only the pair domain, so the same length     */
-/* normalisation is used for both.                                          */
+/* normalisation is used for both.  Memory is O(m^2) for the largest group.  */
 /* ------------------------------------------------------------------------- */
 int orc_redundancy(int L, int d, int b, const float *keys, double p, double tau,
                    int lightning, double *R) {
     if (L <= 0 || d <= 0 || b <= 0 || !(tau > 0.0)) return ORC_BAD_ARG;
+    const int group = lightning ? (b < L ? b : L) : L;
     double *norm = (double *)malloc(sizeof(double) * (size_t)L);
-    double *C = (double *)malloc(sizeof(double) * (size_t)L * (size_t)L);
+    double *C = (double *)malloc(sizeof(double) * (size_t)group * (size_t)group);
     double *rho = (double *)malloc(sizeof(double) * (size_t)L);
     if (!norm || !C || !rho) { free(norm); free(C); free(rho); return ORC_NO_MEMORY; }
     for (int t = 0; t < L; ++t) {
@@ -304,32 +307,36 @@ int orc_redundancy(int L, int d, int b, const float *keys, double p, double tau,
         for (int i = 0; i < d; ++i) ss += (double)keys[(size_t)t * d + i] * (double)keys[(size_t)t * d + i];
         norm[t] = sqrt(ss);
     }
-    for (int r = 0; r < L; ++r) {
-        for (int c = 0; c < L; ++c) {
-            double v = 0.0;
-            const int in_domain = lightning ? (r / b == c / b) : 1;
-            if (in_domain && norm[r] > 0.0 && norm[c] > 0.0) {
-                double dot = 0.0;
-                for (int i = 0; i < d; ++i)
-                    dot += (double)keys[(size_t)r * d + i] * (double)keys[(size_t)c * d + i];
-                v = dot / (norm[r] * norm[c]);
+    for (int g0 = 0; g0 < L; g0 += group) {
+        const int m = (L - g0 < group) ? L - g0 : group;
+        for (int r = 0; r < m; ++r) {
+            for (int c = 0; c < m; ++c) {
+                const int tr = g0 + r, tc = g0 + c;
+                double v = 0.0;
+                if (norm[tr] > 0.0 && norm[tc] > 0.0) {
+                    double dot = 0.0;
+                    for (int i = 0; i < d; ++i)
+                        dot += (double)keys[(size_t)tr * d + i] * (double)keys[(size_t)tc * d + i];
+                    v = dot / (norm[tr] * norm[tc]);
+                }
+                C[(size_t)r * m + c] = v;
             }
-            C[(size_t)r * L + c] = v;
         }
-    }
-    for (int c = 0; c < L; ++c) C[(size_t)c * L + c] = 0.0;
-    for (int c = 0; c < L; ++c) {
-        for (int r = L - 1; r >= 0; --r) {
-            if (C[(size_t)r * L + c] > p) { C[(size_t)r * L + c] = 0.0; break; }
+        for (int c = 0; c < m; ++c) C[(size_t)c * m + c] = 0.0;
+        for (int c = 0; c < m; ++c) {
+            for (int r = m - 1; r >= 0; --r) {
+                if (C[(size_t)r * m + c] > p) { C[(size_t)r * m + c] = 0.0; break; }
+            }
+        }
+        for (int r = 0; r < m; ++r) {
+            double acc = 0.0;
+            for (int c = 0; c < m; ++c) acc += C[(size_t)r * m + c];
+            rho[g0 + r] = acc / ((double)L * tau);
         }
     }
     double rmax = -INFINITY;
-    for (int r = 0; r < L; ++r) {
-        double acc = 0.0;
-        for (int c = 0; c < L; ++c) acc += C[(size_t)r * L + c];
-        rho[r] = acc / ((double)L * tau);
+    for (int r = 0; r < L; ++r)
         if (rho[r] > rmax) rmax = rho[r];
-    }
     double denom = 0.0;
     for (int r = 0; r < L; ++r) denom += exp(rho[r] - rmax);
     for (int r = 0; r < L; ++r) R[r] = exp(rho[r] - rmax) / denom;

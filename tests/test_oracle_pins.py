@@ -284,6 +284,34 @@ def test_redundancy_lightning_equals_full_when_blocks_orthogonal(orc):
     assert np.ptp(full) > 1e-3  # non-trivial: some pairs above the threshold
 
 
+@pytest.mark.parametrize("lightning", [0, 1])
+def test_redundancy_brute_force_with_duplicates(orc, lightning):
+    """Pure-Python brute force over the L x L pair matrix with the domain mask
+    (same block for lightning), keys with planted near-duplicates so the
+    threshold rule fires, a ragged last block."""
+    rng = np.random.default_rng(17 + lightning)
+    L, b, d, p, tau = 23, 8, 6, 0.5, 0.4
+    keys = rng.standard_normal((L, d)).astype(np.float32)
+    for t in (3, 5, 9, 12, 13, 20, 22):
+        keys[t] = keys[t - 1 - (t % 2)] + 0.05 * rng.standard_normal(d).astype(np.float32)
+    k = keys.astype(np.float64)
+    C = [[0.0] * L for _ in range(L)]
+    for r in range(L):
+        for c in range(L):
+            if r != c and (not lightning or r // b == c // b):
+                C[r][c] = sum(k[r, i] * k[c, i] for i in range(d)) / (
+                    np.sqrt(sum(x * x for x in k[r])) * np.sqrt(sum(x * x for x in k[c])))
+    fired = 0
+    for c in range(L):
+        above = [r for r in range(L) if C[r][c] > p]
+        if above:
+            C[max(above)][c] = 0.0
+            fired += 1
+    rho = [sum(C[r]) / (L * tau) for r in range(L)]
+    np.testing.assert_allclose(orc.redundancy(keys, b, p, tau, lightning), _softmax(rho), rtol=1e-12)
+    assert fired >= 6
+
+
 def test_redundancy_zero_norm_key_has_no_similarity(orc):
     keys = np.array([[0, 0], [1, 0], [0, 1]], dtype=np.float32)
     R = orc.redundancy(keys, 4, 0.5, 1.0, 0)
