@@ -139,8 +139,10 @@ class Workload:
         self.table = c.block_table.to(dev)
         self.lens = c.seq_lens.to(dev)
         self.out = torch.empty_like(self.q)
-        self.S = torch.zeros(c.n_total, b, h_kv, dtype=torch.float32, device=dev)
-        self.F = torch.zeros_like(self.S)
+        # attention score: one row per (sequence, kv head) over the table's capacity;
+        # global score F: paged like K
+        self.S = torch.zeros(B, h_kv, c.block_table.shape[1] * b, dtype=torch.float32, device=dev)
+        self.F = torch.zeros(c.n_total, b, h_kv, dtype=torch.float32, device=dev)
         g = torch.Generator().manual_seed(seed + seed_offset + 7)
         self.k_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
         self.v_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
@@ -158,6 +160,7 @@ class Workload:
         if n:
             idx = torch.tensor(self.comp, dtype=torch.long)
             self.c_table = c.block_table[idx].contiguous().to(dev)
+            self.c_rows = idx.to(torch.int32).to(dev)
             self.c_lens = c.seq_lens[idx].contiguous().to(dev)
             self.c_Lmax = int(c.seq_lens[idx].max())
             self.c_first = torch.ones(n, dtype=torch.uint8, device=dev)
@@ -205,7 +208,8 @@ class Workload:
         return tot
 
     def launches_per_step(self) -> int:
-        return 1 + 2 + (5 if self.n_comp else 0)  # append; decode main + score; score x3, top-k, compact
+        # append; decode main + merge + score epilogue; scores x3, top-k, compact
+        return 1 + 3 + (5 if self.n_comp else 0)
 
     # ---- the step
     def decode(self, stream=None):
@@ -223,10 +227,10 @@ class Workload:
         # every step
         self.pool.plan_compaction_batch(self.c_tables_np, self.c_nblocks_np, self.N_max, out=self.plan_out)
         zp.zp_score_tokens(self.desc, self.params, self.K, self.c_table, self.c_lens, self.c_first, self.S,
-                           self.F, self.c_scores, workspace=self.c_ws, stream=stream)
+                           self.F, self.c_scores, rows=self.c_rows, workspace=self.c_ws, stream=stream)
         zp.zp_select_topk(self.c_scores, self.c_lens, self.k, self.c_keep, stream=stream)
         zp.zp_compact_pages(self.desc, self.K, self.V, 0, 1, self.F, 0, self.c_table, self.c_targets,
-                            self.c_lens, self.c_keep, self.k, stream=stream)
+                            self.c_lens, self.c_keep, self.k, scores=self.S, rows=self.c_rows, stream=stream)
 
     def step(self):
         self.decode()

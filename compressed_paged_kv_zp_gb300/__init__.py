@@ -55,6 +55,24 @@ class ScoreParams(ctypes.Structure):
                 ("threshold", ctypes.c_float), ("lambda_", ctypes.c_float), ("tau", ctypes.c_float)]
 
 
+class ScoreRows(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+                ("rows", ctypes.c_void_p)]
+
+
+def _score_rows(attn, rows):
+    """attn: float32 [R][h_kv][stride] or [layers][R][h_kv][stride]; rows: int32 [n] or None."""
+    if attn is None:
+        return None
+    if attn.dtype != torch.float32 or attn.dim() not in (3, 4):
+        raise ValueError("score rows must be float32 [R][h_kv][stride] or [layers][R][h_kv][stride]")
+    if rows is not None and rows.dtype != torch.int32:
+        raise ValueError("rows must be int32")
+    layer_stride = attn.stride(0) if attn.dim() == 4 else 0
+    return ctypes.byref(ScoreRows(_dev(attn, "attn").value, int(attn.shape[-1]), int(layer_stride),
+                                  _dev(rows, "rows").value if rows is not None else None))
+
+
 def score_params(window=16, use_global=True, alpha=0.8, pool_kernel=7, pool_policy=1,
                  use_similarity=True, lightning=True, threshold=0.9, lam=0.2, tau=0.4) -> ScoreParams:
     return ScoreParams(int(window), int(bool(use_global)), float(alpha), int(pool_kernel),
@@ -84,10 +102,10 @@ def _load() -> ctypes.CDLL:
     lib.zp_window_score_workspace_size.restype = SZ
     lib.zp_window_score_workspace_size.argtypes = [D, I32, I32, I32]
     lib.zp_window_score.argtypes = [D, P, I32, P, P, I32, P, I32, P, I32, P, SZ, P]
-    lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P, P,
+    lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P,
                                     I32, P, SZ, P]
     lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
-    lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, I32, P, I32, P, P, I32, I32, P]
+    lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, P, I32, P, I32, P, P, I32, I32, P]
     lib.zp_pool_create.restype = P
     lib.zp_pool_create.argtypes = [I32]
     lib.zp_pool_destroy.argtypes = [P]
@@ -202,18 +220,21 @@ def zp_window_score(desc, q_window, k_cache, block_table, seq_lens, scores_out, 
 
 
 def zp_score_tokens(desc, params: ScoreParams, k_cache, block_table, seq_lens, first_compression,
-                    score_accum, global_F, scores_out, workspace=None, stream=None,
-                    window_score=None) -> None:
+                    attn, global_F, scores_out, rows=None, workspace=None, stream=None) -> None:
+    """attn: the attention-score rows, float32 [R][h_kv][stride] (the decode
+    score_accum, or the output of zp_window_score); sequence i reads row
+    rows[i] (rows None: row i).  On return the rows hold the global score."""
     n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
     Lmax = int(scores_out.shape[-1])
     if workspace is None:
         workspace = torch.empty(max(zp_score_workspace_size(desc, n, Lmax), 1), dtype=torch.uint8,
                                 device=scores_out.device)
+    if attn is None:
+        raise ValueError("attn (the attention-score rows) is required")
     _check(lib.zp_score_tokens(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
                                _dev(block_table, "block_table"), table_stride,
                                _dev(seq_lens, "seq_lens"), _dev(first_compression, "first_compression"),
-                               n, _dev(score_accum, "score_accum"), _dev(window_score, "window_score"),
-                               _dev(global_F, "global_F"),
+                               n, _score_rows(attn, rows), _dev(global_F, "global_F"),
                                _dev(scores_out, "scores_out"), Lmax, _dev(workspace, "workspace"),
                                workspace.numel(), _stream(stream)))
 
@@ -226,11 +247,15 @@ def zp_select_topk(scores, seq_lens, k, keep_idx, tie_count=None, stream=None) -
 
 
 def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, F_layer_stride,
-                     src_table, dst_targets, seq_lens, keep_idx, k, stream=None) -> None:
+                     src_table, dst_targets, seq_lens, keep_idx, k, scores=None, rows=None,
+                     stream=None) -> None:
+    """scores/rows: the score rows zp_score_tokens left (float32 [R][h_kv][stride],
+    or [layers][R][h_kv][stride] for several layers); needed when global_F is set."""
     n, table_stride = int(src_table.shape[0]), int(src_table.shape[1])
     _check(lib.zp_compact_pages(ctypes.byref(desc), _dev(k_base, "k_base"), _dev(v_base, "v_base"),
                                 int(layer_stride), int(layer_count), _dev(global_F, "global_F"),
-                                int(F_layer_stride), _dev(src_table, "src_table"), table_stride,
+                                int(F_layer_stride), _score_rows(scores, rows),
+                                _dev(src_table, "src_table"), table_stride,
                                 _dev(dst_targets, "dst_targets"), int(dst_targets.shape[1]),
                                 _dev(seq_lens, "seq_lens"), _dev(keep_idx, "keep_idx"), int(k), n,
                                 _stream(stream)))
@@ -316,7 +341,7 @@ class Pool:
         return out
 
 
-__all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "score_params",
+__all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "ScoreRows", "score_params",
            "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn",
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_window_score_workspace_size", "zp_window_score",

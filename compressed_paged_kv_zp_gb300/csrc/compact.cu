@@ -2,9 +2,11 @@
 //
 // Zipage paper App. C.6, Alg. 4: the kept entries of a sequence are packed, in
 // their original order, into the first N_max - 1 blocks (or the target blocks
-// of §4.4 when prefix blocks are shared); the global score cache F moves the
-// same way ("compress score").  Rank r of the keep list goes to slot r % b of
-// target block r / b.
+// of §4.4 when prefix blocks are shared).  Rank r of the keep list goes to
+// slot r % b of target block r / b.  The global score cache F of that slot
+// receives the kept token's global score ("compress score"), read from the
+// sequence's score row where zp_score_tokens left it: F is written only in
+// target blocks, never in a source block another sequence may share.
 //
 // One CTA per (kv head, sequence, layer).  Alg. 4 walks one slot at a time;
 // here a CTA moves a chunk of up to 128 ranks at once: every thread first loads
@@ -28,6 +30,9 @@ struct CompactArgs {
     long long layer_stride_vec;  // in 16-byte vectors
     float *F;
     long long F_layer_stride;
+    const float *S;  // score rows: S + layer*S_layer_stride + (row*h_kv + kvh)*S_stride + pos
+    long long S_stride, S_layer_stride;
+    const int32_t *S_rows;  // nullable
     const int32_t *src_table;
     int table_stride;
     const int32_t *dst;
@@ -46,11 +51,22 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     const int layer = blockIdx.z;
     int L = a.seq_lens[s];
     if (L > a.table_stride * a.b) L = a.table_stride * a.b;
-    const int kk = min(a.k, L);
     const int32_t *kp = a.keep + (((size_t)layer * a.n + s) * a.h_kv + kvh) * a.k;
     uint4 *K = a.K + layer * a.layer_stride_vec;
     uint4 *V = a.V + layer * a.layer_stride_vec;
     float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
+    const float *Srow = nullptr;
+    if (F) {
+        const int row = a.S_rows ? a.S_rows[s] : s;
+        if (row < 0) {
+            if (threadIdx.x == 0) record_error(a.err, ZP_ERR_DEVICE, 0x402);
+            F = nullptr;
+        } else {
+            Srow = a.S + layer * a.S_layer_stride + ((size_t)row * a.h_kv + kvh) * a.S_stride;
+        }
+    }
+    if (F && L > a.S_stride) L = (int)a.S_stride;
+    const int kk = min(a.k, L);
     const int per_rank = 2 * a.row_vec;  // K then V vectors
     for (int r0 = 0; r0 < kk; r0 += a.chunk) {
         const int nr = min(a.chunk, kk - r0);
@@ -79,10 +95,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
         }
         if (F && threadIdx.x < nr) {  // nr <= kChunkMax <= kThreads
             const int pos = kp[r0 + threadIdx.x];
-            if (pos >= 0 && pos < L) {
-                const int blk = a.src_table[(size_t)s * a.table_stride + pos / a.b];
-                if (blk >= 0 && blk < a.n_total) fbuf = F[((size_t)blk * a.b + pos % a.b) * a.h_kv + kvh];
-            }
+            if (pos >= 0 && pos < L) fbuf = Srow[pos];
         }
         __syncthreads();
         // ---- store phase
@@ -118,7 +131,8 @@ using namespace zp;
 
 extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
                                       int64_t layer_stride, int32_t layer_count, float *global_F,
-                                      int64_t F_layer_stride, const int32_t *src_table,
+                                      int64_t F_layer_stride, const zp_score_rows *scores,
+                                      const int32_t *src_table,
                                       int32_t table_stride, const int32_t *dst_targets,
                                       int32_t target_stride, const int32_t *seq_lens,
                                       const int32_t *keep_idx, int32_t k, int32_t n, void *stream) {
@@ -129,6 +143,8 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     if (n == 0 || k == 0 || layer_count == 0) return ok();
     if (!k_base || !v_base || !src_table || !dst_targets || !seq_lens || !keep_idx)
         return fail(ZP_ERR_INVALID_ARG, "compact: NULL buffer");
+    if (global_F && (!scores || !scores->data || scores->stride < 1))
+        return fail(ZP_ERR_INVALID_ARG, "compact: global_F needs the score rows");
     if ((long long)target_stride * D->block_size < k)
         return fail(ZP_ERR_CAPACITY, "compact: %d target blocks hold fewer than k=%d rows", target_stride, k);
     const int es = elem_bytes(D->dtype);
@@ -152,6 +168,10 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     a.layer_stride_vec = layer_stride * es / 16;
     a.F = global_F;
     a.F_layer_stride = F_layer_stride;
+    a.S = global_F ? scores->data : nullptr;
+    a.S_stride = global_F ? scores->stride : 1;
+    a.S_layer_stride = global_F ? scores->layer_stride : 0;
+    a.S_rows = global_F ? scores->rows : nullptr;
     a.src_table = src_table;
     a.table_stride = table_stride;
     a.dst = dst_targets;

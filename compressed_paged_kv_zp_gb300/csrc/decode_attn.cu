@@ -60,6 +60,7 @@ struct DecodeArgs {
     int want_score;
     int window;
     float *score;
+    long long score_stride;  // elements between kv-head rows of S: table_stride * b
     float *logits;     // [units * T][h_q]
     float2 *stats;     // [B][h_q] final (max, sum), log2 units
     float *part_acc;   // [2*grid][h_q][D]
@@ -612,13 +613,14 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
     }
 }
 
-// Window-score epilogue: one block per unit, one thread per (token, kv head)
+// Window-score epilogue: one block per unit, one thread per (kv head, token)
 // of window-step sequences.  p_h(t) = 2^(logit - m_h) / l_h;
 // S += (1/w) max over the group of p_h(t) (written instead of added at the
 // first window row and for the newest token).  (m_h, l_h) are the sequence's
 // final softmax statistics, written by the main kernel (sequences one CTA saw
-// whole) or by the merge kernel (cut sequences).  A thread's dependent loads
-// are: unit record -> block id and logits -> score slot.
+// whole) or by the merge kernel (cut sequences).  S is the sequence's own row
+// per kv head, indexed by token position: consecutive threads take
+// consecutive tokens of one row.
 template <int G>
 __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
     const int u = blockIdx.x;
@@ -631,11 +633,10 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
     const bool first_row = (info.w & 2) != 0;
     const float inv_w = 1.f / (float)a.window;
     for (int it = threadIdx.x; it < a.T * a.h_kv; it += blockDim.x) {
-        const int tl = it / a.h_kv;
-        const int kvh = it % a.h_kv;
+        const int tl = it % a.T;
+        const int kvh = it / a.T;
         const int tok = info.y + tl;
         if (tok >= L) continue;
-        const int blk = __ldg(&a.table[(size_t)s * a.table_stride + tok / a.b]);
         const float *lg = a.logits + ((size_t)u * a.T + tl) * a.h_q + kvh * G;
         const float2 *st = a.stats + (size_t)s * a.h_q + kvh * G;
         float x[G];
@@ -655,15 +656,11 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < G; ++j) ml[j] = st[j];
-        if (blk < 0 || blk >= a.n_total) {
-            record_error(a.err, ZP_ERR_DEVICE, 5);
-            continue;
-        }
         float best = 0.f;
 #pragma unroll
         for (int j = 0; j < G; ++j) best = fmaxf(best, exp2f(x[j] - ml[j].x) / ml[j].y);
         const float c = best * inv_w;
-        float *dst = a.score + ((size_t)blk * a.b + tok % a.b) * a.h_kv + kvh;
+        float *dst = a.score + ((size_t)s * a.h_kv + kvh) * a.score_stride + tok;
         *dst = (first_row || tok == P) ? c : (*dst + c);
     }
 }
@@ -1301,6 +1298,7 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.want_score = score_accum != nullptr;
     a.window = window;
     a.score = score_accum;
+    a.score_stride = (long long)table_stride * D->block_size;
     a.logits = reinterpret_cast<float *>(ws + p.off_logits);
     a.stats = reinterpret_cast<float2 *>(ws + p.off_stats);
     a.part_acc = reinterpret_cast<float *>(ws + p.off_pacc);

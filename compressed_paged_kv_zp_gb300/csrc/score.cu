@@ -3,10 +3,11 @@
 // Zipage paper App. C.2-C.8 and §4.2, in the order of the paper's per-op
 // timing figure (Figs. 13/14): attention score -> global score -> pooling ->
 // redundancy score -> window mask.  Three launches:
-//   1. gather_global: the accumulated window score S (paged, written by the
-//      decode kernel) is gathered per (sequence, kv head) and, if enabled, run
-//      through Alg. 2 against the paged global score cache F (updated in
-//      place).  Result X [n][h_kv][Lmax].
+//   1. gather_global: the attention score S of each (sequence, kv head) is
+//      read from its score row and, if enabled, run through Alg. 2 against
+//      the paged global score cache F (read only).  The global score goes
+//      back into the score row (the compaction stores it into F of the kept
+//      tokens) and to X [n][h_kv][Lmax].
 //   2. lightning: one CTA per (sequence, block): the block's keys of every kv
 //      head are staged in shared memory, each warp forms the b x b cosine
 //      matrix of one kv head, zeroes the diagonal and, per column, the newest
@@ -30,9 +31,10 @@ struct ScoreArgs {
     const int32_t *seq_lens;
     const uint8_t *first;
     int n, h_kv, b, n_total, Lmax, d;
-    const float *S;   // paged [N_total][b][h_kv] (accumulated during decode), or NULL
-    const float *Sw;  // [n][h_kv][Lmax] (explicit window score), used when S is NULL
-    float *F;         // paged, nullable
+    float *S;               // score rows: S + (row * h_kv + kvh) * S_stride + t
+    long long S_stride;
+    const int32_t *S_rows;  // nullable: row of sequence i
+    const float *F;         // paged [N_total][b][h_kv], nullable
     float *X;         // [n][h_kv][Lmax]
     float *rho;       // [n][h_kv][Lmax]
     float *out;       // [n][h_kv][Lmax]
@@ -51,10 +53,14 @@ __device__ __forceinline__ int clamp_len(const ScoreArgs &a, int s) {
     if (L < 0) L = 0;
     if (L > a.Lmax) L = a.Lmax;
     if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    if (L > a.S_stride) L = (int)a.S_stride;
     return L;
 }
 
-// grid (ceil(Lmax / kTile), n), 256 threads
+// grid (ceil(Lmax / kTile), n), 256 threads.  Phase 1 stages the tile's F
+// values (paged, (slot, kv head) fastest) in shared memory when Alg. 2 reads
+// them; phase 2 walks (kv head, token) so the score rows are read and written
+// along tokens.
 __global__ void gather_global_kernel(const ScoreArgs a) {
     __shared__ float tile[16][kTile + 1];  // h_kv <= 16
     const int s = blockIdx.y;
@@ -63,38 +69,42 @@ __global__ void gather_global_kernel(const ScoreArgs a) {
     if (t0 >= L) return;
     const int N = (L + a.b - 1) / a.b;
     const bool first = a.first ? a.first[s] != 0 : true;
+    const bool read_F = a.use_global && !first;
     const int items = kTile * a.h_kv;
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int tl = it / a.h_kv;
-        const int kvh = it % a.h_kv;
-        const int t = t0 + tl;
-        float v = 0.f;
-        if (t < L) {
-            const int bi = t / a.b;
-            const int blk = a.table[(size_t)s * a.table_stride + bi];
-            if (blk < 0 || blk >= a.n_total) {
-                record_error(a.err, ZP_ERR_DEVICE, 0x200);
-            } else {
-                const size_t at = ((size_t)blk * a.b + t % a.b) * a.h_kv + kvh;
-                v = a.S ? a.S[at] : a.Sw[((size_t)s * a.h_kv + kvh) * a.Lmax + t];
-                if (a.use_global) {
-                    if (first) {
-                        a.F[at] = v;
-                    } else {
-                        if (bi != N - 1) v = fmaxf(a.alpha * a.F[at], v);
-                        a.F[at] = v;
-                    }
-                }
-            }
-        }
-        tile[kvh][tl] = v;
+    const int row = a.S_rows ? a.S_rows[s] : s;
+    if (row < 0) {
+        if (threadIdx.x == 0) record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        return;
     }
-    __syncthreads();
+    if (read_F) {
+        for (int it = threadIdx.x; it < items; it += blockDim.x) {
+            const int tl = it / a.h_kv;
+            const int kvh = it % a.h_kv;
+            const int t = t0 + tl;
+            float f = 0.f;
+            if (t < L && t / a.b != N - 1) {
+                const int blk = a.table[(size_t)s * a.table_stride + t / a.b];
+                if (blk < 0 || blk >= a.n_total)
+                    record_error(a.err, ZP_ERR_DEVICE, 0x200);
+                else
+                    f = a.F[((size_t)blk * a.b + t % a.b) * a.h_kv + kvh];
+            }
+            tile[kvh][tl] = f;
+        }
+        __syncthreads();
+    }
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
         const int kvh = it / kTile;
         const int tl = it % kTile;
         const int t = t0 + tl;
-        if (t < L) a.X[((size_t)s * a.h_kv + kvh) * a.Lmax + t] = tile[kvh][tl];
+        if (t >= L) continue;
+        float *sp = a.S + ((size_t)row * a.h_kv + kvh) * a.S_stride + t;
+        float v = *sp;
+        if (read_F && t / a.b != N - 1) {
+            v = fmaxf(a.alpha * tile[kvh][tl], v);
+            *sp = v;
+        }
+        a.X[((size_t)s * a.h_kv + kvh) * a.Lmax + t] = v;
     }
 }
 
@@ -385,8 +395,8 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
                                      const void *k_cache, const int32_t *block_table,
                                      int32_t table_stride, const int32_t *seq_lens,
                                      const uint8_t *first_compression, int32_t n,
-                                     const float *score_accum, const float *window_score,
-                                     float *global_F, float *scores_out,
+                                     const zp_score_rows *attn, const float *global_F,
+                                     float *scores_out,
                                      int32_t Lmax, void *workspace, size_t workspace_bytes,
                                      void *stream) {
     zp_status rc = check_desc(D);
@@ -396,8 +406,8 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     if (n == 0 || Lmax == 0) return ok();
     if (!block_table || !seq_lens || !scores_out || !workspace)
         return fail(ZP_ERR_INVALID_ARG, "score: NULL buffer");
-    if ((score_accum == nullptr) == (window_score == nullptr))
-        return fail(ZP_ERR_INVALID_ARG, "score: give exactly one of score_accum and window_score");
+    if (!attn || !attn->data) return fail(ZP_ERR_INVALID_ARG, "score: NULL attention-score rows");
+    if (attn->stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: score row stride %lld", (long long)attn->stride);
     if (P->use_global && !global_F) return fail(ZP_ERR_INVALID_ARG, "score: use_global needs global_F");
     if (P->use_similarity && !k_cache) return fail(ZP_ERR_INVALID_ARG, "score: similarity needs k_cache");
     if (P->window < 0) return fail(ZP_ERR_INVALID_ARG, "score: window %d", P->window);
@@ -426,8 +436,9 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     a.n_total = D->n_total_blocks;
     a.Lmax = Lmax;
     a.d = D->head_dim;
-    a.S = score_accum;
-    a.Sw = window_score;
+    a.S = attn->data;
+    a.S_stride = attn->stride;
+    a.S_rows = attn->rows;
     a.F = global_F;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.X = reinterpret_cast<float *>(ws);

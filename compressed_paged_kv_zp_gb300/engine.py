@@ -41,8 +41,8 @@ class DecodeLoop:
         self.async_compress = async_compress
         self.K = torch.zeros(layers, n_total, b, h_kv, d, dtype=dtype, device=self.dev)
         self.V = torch.zeros_like(self.K)
-        self.S = torch.zeros(layers, n_total, b, h_kv, dtype=torch.float32, device=self.dev)
-        self.F = torch.zeros_like(self.S)
+        # global score cache F: paged like K (it moves with the kept tokens)
+        self.F = torch.zeros(layers, n_total, b, h_kv, dtype=torch.float32, device=self.dev)
         self.pool = Pool(n_total)
         self.side = torch.cuda.Stream(device=self.dev)
         self.B = 0
@@ -79,6 +79,10 @@ class DecodeLoop:
         self.first = np.ones(B, dtype=np.uint8)  # never compressed yet
         self.active = np.ones(B, dtype=bool)
         self.table_dev = torch.from_numpy(self.table).to(self.dev)
+        # attention score S: one row per (sequence, kv head), indexed by token
+        # position, so sequences sharing prefix blocks keep their own scores
+        self.S = torch.zeros(self.layers, B, self.h_kv, self.stride * self.b, dtype=torch.float32,
+                             device=self.dev)
         self.ws = torch.empty(zp_decode_workspace_size(self.desc, B, self.stride), dtype=torch.uint8,
                               device=self.dev)
         Lmax = self.stride * self.b
@@ -129,6 +133,7 @@ class DecodeLoop:
         tables_dev = torch.from_numpy(sub_tables).to(self.dev)
         lens_dev = torch.from_numpy(self.lens[seqs].astype(np.int32)).to(self.dev)
         first_dev = torch.from_numpy(self.first[seqs].copy()).to(self.dev)
+        rows_dev = torch.from_numpy(seqs.astype(np.int32)).to(self.dev)
         targets_dev = torch.from_numpy(np.ascontiguousarray(plan["targets"])).to(self.dev)
         ready = torch.cuda.Event()
         ready.record(main)
@@ -138,13 +143,14 @@ class DecodeLoop:
             keep = torch.empty(self.layers, n, self.h_kv, self.k, dtype=torch.int32, device=self.dev)
             for l in range(self.layers):
                 zp_score_tokens(self.desc, self.params, self.K[l], tables_dev, lens_dev, first_dev, self.S[l],
-                                self.F[l], scores, workspace=self.score_ws)
+                                self.F[l], scores, rows=rows_dev, workspace=self.score_ws)
                 zp_select_topk(scores, lens_dev, self.k, keep[l])
             zp_compact_pages(self.desc, self.K, self.V, self.layer_stride(), self.layers, self.F,
-                             self.n_total * self.b * self.h_kv, tables_dev, targets_dev, lens_dev, keep, self.k)
+                             self.n_total * self.b * self.h_kv, tables_dev, targets_dev, lens_dev, keep, self.k,
+                             scores=self.S, rows=rows_dev)
             done = torch.cuda.Event()
             done.record(self.side)
-        for t in (tables_dev, lens_dev, first_dev, targets_dev):
+        for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev):
             t.record_stream(self.side)
         self.active[seqs] = False
         self.last_keep = (seqs, keep)  # for inspection: [layers][n][h_kv][k]

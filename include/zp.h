@@ -103,13 +103,17 @@ size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table
  *     out[s][h] = sum_{t<L} softmax_t(q[s][h] . k_t / sqrt(d)) v_t
  * q, out: [B][h_q][d] (dtype); k_cache, v_cache: one layer, paged.
  *
- * score_accum (nullable, float [N_total][b][h_kv]): when set, sequences whose
- * query position P = L-1 lies in the observation window of its block
- * (P mod b >= b - window) add (1/window) * max over the q heads of each kv
- * head of the attention probability of every token t <= P; at the first
- * window row (P mod b == b - window) and for t == P the value is written
+ * score_accum (nullable, float [B][h_kv][table_stride*b]): the attention
+ * score S of each sequence, one row per kv head indexed by token position
+ * (row s belongs to batch entry s, as block-table row s does).  When set,
+ * sequences whose query position P = L-1 lies in the observation window of
+ * its block (P mod b >= b - window) add (1/window) * max over the q heads of
+ * each kv head of the attention probability of every token t <= P; at the
+ * first window row (P mod b == b - window) and for t == P the value is written
  * instead of added.  After the window steps that fill a block, S equals the
- * observation-window score of App. C.2 computed from those queries.
+ * observation-window score of App. C.2 computed from those queries.  The
+ * score lives with the sequence, not with the block: sequences that share
+ * prefix blocks [§4.4] each score those tokens with their own queries.
  *
  * Limits: B <= 4096, h_kv in {2,4,8,16}, h_q/h_kv in {4,8}, d in {64,128},
  * b a power of two >= 16.  Errors: ZP_ERR_INVALID_ARG (NULL buffer, B < 0,
@@ -176,24 +180,39 @@ zp_status zp_window_score(const zp_cache_desc *D, const void *q_window, int32_t 
 
 size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
 
+/* Per-sequence score rows: the attention score S written by
+ * zp_paged_decode_attn (stride = table_stride*b, rows = the decode batch) or
+ * by zp_window_score (stride = Lmax, rows = its n sequences).  Sequence i of a
+ * call uses row rows[i] (rows NULL: row i) at
+ *     data + l*layer_stride + (row*h_kv + kvh)*stride + t.
+ * layer_stride matters only to zp_compact_pages with several layers. */
+typedef struct zp_score_rows {
+    float *data;
+    int64_t stride;        /* >= L of every sequence */
+    int64_t layer_stride;  /* elements between layers */
+    const int32_t *rows;   /* nullable, int32 [n], device */
+} zp_score_rows;
+
 /* Final per-token scores of n sequences of one layer, ready for the top-k
  * [Zipage App. C.2-C.8, §4.2], in the paper's order:
- *   S  <- score_accum gathered through the block table, or window_score
- *         ([n][h_kv][Lmax], from zp_window_score): exactly one is non-NULL
- *                                                        (attention score)
- *   S  <- Alg. 2 with global_F when use_global          (global score)
+ *   S  <- the sequence's attention-score rows in attn (decode-accumulated or
+ *         explicit window score)                        (attention score)
+ *   S  <- Alg. 2 with global_F when use_global: S on the first compression,
+ *         else max(alpha*F, S) on blocks 0..N-2          (global score)
  *   Sp <- MaxPool1D(S) when pooling applies              (C.4, eq. 3)
  *   R  <- softmax_t(rho_t / (L*tau)) of the key redundancy (C.5 / C.7)
  *   out = Sp - lambda*R, then +inf on the last `window` tokens.
  * first_compression[n] (uint8) says whether each sequence was ever compressed
- * (Alg. 2 branch, pooling policy).  global_F (float [N_total][b][h_kv]) is
- * updated in place.  scores_out: float [n][h_kv][Lmax]; entries t >= L are
- * left untouched.  Requires L <= Lmax and L >= window for every sequence. */
+ * (Alg. 2 branch, pooling policy).  The global score replaces S in attn (t < L)
+ * so that zp_compact_pages can store it into F of the kept tokens' new slots;
+ * global_F (float [N_total][b][h_kv], paged like K) is only read, and only
+ * on compressions after the first, when every block of the sequence is its
+ * own [§4.4].  scores_out: float [n][h_kv][Lmax]; entries t >= L are left
+ * untouched.  Requires window <= L <= min(Lmax, attn->stride). */
 zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
                           const void *k_cache, const int32_t *block_table, int32_t table_stride,
                           const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
-                          const float *score_accum, const float *window_score, float *global_F,
-                          float *scores_out,
+                          const zp_score_rows *attn, const float *global_F, float *scores_out,
                           int32_t Lmax, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Top-k keep set [Zipage §4.2, App. C.6]: for every (sequence, kv head) the k
@@ -207,17 +226,21 @@ zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const 
                          void *stream);
 
 /* KV compaction [Zipage App. C.6, Alg. 4; §4.4 target blocks]: for layers
- * [0, layer_count) (K, V and global_F of layer l at base + l*layer_stride
- * elements), every sequence i and kv head h, rank r < min(k, L_i) moves the row
- * at position keep_idx[l][i][h][r] (block src_table[i][pos/b]) to slot r%b of
+ * [0, layer_count) (K and V of layer l at base + l*layer_stride elements),
+ * every sequence i and kv head h, rank r < min(k, L_i) moves the row at
+ * position keep_idx[l][i][h][r] (block src_table[i][pos/b]) to slot r%b of
  * block dst_targets[i][r/b].  The move is order preserving and safe when a
- * target block is the source block of the same index (in place).  global_F
- * (nullable) moves with the rows; src_table [n][table_stride],
- * dst_targets [n][target_stride] (at least ceil(k/b) entries), keep_idx
+ * target block is the source block of the same index (in place).
+ * global_F (nullable, layer l at global_F + l*F_layer_stride) receives at the
+ * same slot the global score of the kept token, read from the score rows
+ * `scores` left by zp_score_tokens ("compress score"); F is written only in
+ * the target blocks.  src_table [n][table_stride], dst_targets
+ * [n][target_stride] (at least ceil(k/b) entries), keep_idx
  * [layer_count][n][h_kv][k], seq_lens [n]. */
 zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
                            int64_t layer_stride, int32_t layer_count, float *global_F,
-                           int64_t F_layer_stride, const int32_t *src_table, int32_t table_stride,
+                           int64_t F_layer_stride, const zp_score_rows *scores,
+                           const int32_t *src_table, int32_t table_stride,
                            const int32_t *dst_targets, int32_t target_stride,
                            const int32_t *seq_lens, const int32_t *keep_idx, int32_t k,
                            int32_t n, void *stream);

@@ -108,9 +108,19 @@ def test_invalid_arguments_rejected_without_device(zp):
     desc = zp.cache_desc(8, 2, 64, 16, 10, 9)  # bad dtype
     rc = zp.lib.zp_select_topk(None, 2, 4, None, 1, 2, None, None, None)
     assert rc == 1
-    rc = zp.lib.zp_compact_pages(ctypes.byref(desc), None, None, 0, 1, None, 0, None, 1, None, 1,
+    rc = zp.lib.zp_compact_pages(ctypes.byref(desc), None, None, 0, 1, None, 0, None, None, 1, None, 1,
                                  None, None, 4, 1, None)
     assert rc == 3
+    # global_F without the score rows it is written from
+    desc = zp.cache_desc(8, 2, 64, 16, 10, 0)
+    one = ctypes.c_void_p(16)  # never dereferenced: the call fails its argument checks first
+    rc = zp.lib.zp_compact_pages(ctypes.byref(desc), one, one, 0, 1, one, 0, None, one, 1, one, 1,
+                                 one, one, 4, 1, None)
+    assert rc == 1
+    # score_tokens without attention-score rows
+    rc = zp.lib.zp_score_tokens(ctypes.byref(desc), ctypes.byref(zp.score_params()), one, one, 1, one, one, 1,
+                                None, one, one, 4, one, 1 << 30, None)
+    assert rc == 1
 
 
 def test_batch_planner_matches_single_calls(zp):

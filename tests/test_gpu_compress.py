@@ -65,29 +65,38 @@ def test_score_tokens_matches_oracle(zp, name, B, h_q, h_kv, d, b, lo, hi, dtype
                              use_similarity=P.use_similarity, lightning=P.lightning, threshold=P.p,
                              lam=P.lam, tau=P.tau)
     rng = np.random.default_rng(seed)
-    S = torch.from_numpy((rng.random((c.n_total, b, h_kv)) / 50).astype(np.float32)).cuda()
+    # attention-score rows in a larger table, reached through a row map
+    Lrow = int(c.seq_lens.max()) + 3
+    S0 = (rng.random((B + 2, h_kv, Lrow)) / 50).astype(np.float32)
+    rows = np.array([(B + 1 - s) for s in range(B)], dtype=np.int32)
+    S = torch.from_numpy(S0).cuda()
     F0 = (rng.random((c.n_total, b, h_kv)) / 40).astype(np.float32)
     F = torch.from_numpy(F0).cuda()
     Lmax = int(c.seq_lens.max()) + 5
     out = torch.full((B, h_kv, Lmax), -7.0, device="cuda")
     first_t = torch.full((B,), 1 if first else 0, dtype=torch.uint8, device="cuda")
-    zp.zp_score_tokens(_desc(zp, c), params, dc.K[0], dc.table, dc.lens, first_t, S, F, out)
+    zp.zp_score_tokens(_desc(zp, c), params, dc.K[0], dc.table, dc.lens, first_t, S, F, out,
+                       rows=torch.from_numpy(rows).cuda())
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     got = out.cpu().numpy()
-    Sg = S.cpu().numpy().astype(np.float64)
+    S_after = S.cpu().numpy().astype(np.float64)
     F_ref = F0.astype(np.float64)
     K = dc.np_k()
     for s in range(B):
         L = int(c.seq_lens[s])
-        S_seq = gather_slots(Sg, c.block_table[s].numpy(), L, b)
+        S_seq = S0[rows[s], :, :L].astype(np.float64)
         ref = pipeline.final_scores(S_seq, K, F_ref, c.block_table[s].numpy(), L, b, first, P)
         fin = np.isfinite(ref)
         assert np.array_equal(np.isinf(got[s, :, :L]), ~fin)
         np.testing.assert_allclose(got[s, :, :L][fin], ref[fin], **TOL_SCORE["f32"])
         assert np.all(got[s, :, L:] == -7.0)  # untouched beyond L
-    if P.use_global:
-        np.testing.assert_allclose(F.cpu().numpy(), F_ref, rtol=1e-6, atol=0)
+        # the row now holds the global score (what F of the kept tokens receives)
+        want = gather_slots(F_ref, c.block_table[s].numpy(), L, b) if P.use_global else S_seq
+        np.testing.assert_allclose(S_after[rows[s], :, :L], want, rtol=1e-6, atol=0)
+        assert np.array_equal(S_after[rows[s], :, L:], S0[rows[s], :, L:])
+    assert np.array_equal(S_after[0], S0[0])  # a row no sequence maps to
+    assert np.array_equal(F.cpu().numpy(), F0)  # F is only read
 
 
 TOPK_CASES = [(L, k) for L in (1, 47, 48, 49, 160, 1000, 4099) for k in (48, 112)] + [(32768, 2032)]
@@ -141,29 +150,45 @@ def _compaction_setup(zp, seed, layers, fresh_targets):
     else:
         tgt = c.block_table.numpy()[:, : N_max - 1].copy()
     F = torch.from_numpy(rng.random((layers, c.n_total, b, h_kv)).astype(np.float32)).cuda()
-    return c, dc, keep, tgt, F, k
+    # the global scores zp_score_tokens leaves in the score rows
+    S = torch.from_numpy(rng.random((layers, 3, h_kv, 8 * b + 5)).astype(np.float32)).cuda()
+    return c, dc, keep, tgt, F, S, k
 
 
 @pytest.mark.parametrize("layers,fresh", [(1, False), (3, False), (2, True)])
 def test_compaction_bit_exact_vs_alg4(zp, layers, fresh):
-    c, dc, keep, tgt, F, k = _compaction_setup(zp, 500 + layers, layers, fresh)
+    c, dc, keep, tgt, F, S, k = _compaction_setup(zp, 500 + layers, layers, fresh)
     Kraw = dc.K.view(torch.int16).cpu().numpy().copy()
     Vraw = dc.V.view(torch.int16).cpu().numpy().copy()
-    Fref = F.cpu().numpy().copy()
+    F0 = F.cpu().numpy().copy()
+    Srows = S.cpu().numpy()
     desc = _desc(zp, c)
     layer_stride = c.n_total * c.b * c.h_kv * c.d
     zp.zp_compact_pages(desc, dc.K, dc.V, layer_stride, layers, F, c.n_total * c.b * c.h_kv,
-                        dc.table, torch.from_numpy(tgt).cuda(), dc.lens, torch.from_numpy(keep).cuda(), k)
+                        dc.table, torch.from_numpy(tgt).cuda(), dc.lens, torch.from_numpy(keep).cuda(), k,
+                        scores=S)
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     row = c.d * 2
+    # Alg. 4 with F holding each sequence's global score at its own slots;
+    # the library writes F only in the target slots, the rest stays as it was
+    Fsrc = F0.copy()
+    for s, L in enumerate(c.seq_lens.tolist()):
+        t = np.arange(L)
+        for l in range(layers):
+            Fsrc[l, c.block_table[s].numpy()[t // c.b], t % c.b] = Srows[l, s, :, :L].T
+    Fmoved = Fsrc.copy()
     for s, L in enumerate(c.seq_lens.tolist()):
         N = (L + c.b - 1) // c.b
-        pipeline.compact_sequence([Kraw, Vraw, Fref], [row, row, 4], c.b, c.h_kv,
+        pipeline.compact_sequence([Kraw, Vraw, Fmoved], [row, row, 4], c.b, c.h_kv,
                                   c.block_table[s].numpy(), N, tgt[s], keep[:, s], L)
+    Fwant = F0.copy()
+    r = np.arange(k)
+    for s in range(3):
+        Fwant[:, tgt[s][r // c.b], r % c.b] = Fmoved[:, tgt[s][r // c.b], r % c.b]
     assert np.array_equal(dc.K.view(torch.int16).cpu().numpy(), Kraw)
     assert np.array_equal(dc.V.view(torch.int16).cpu().numpy(), Vraw)
-    assert np.array_equal(F.cpu().numpy(), Fref)
+    assert np.array_equal(F.cpu().numpy(), Fwant)
 
 
 @pytest.mark.parametrize("shape", ["tiny", "qwen"])
@@ -177,7 +202,7 @@ def test_end_to_end_compression(zp, shape):
     c = _block_aligned_case(900 + len(shape), B, h_q, h_kv, d, b, lo, hi, dtype, dup=True, spare=B * N_max)
     dc = DeviceCase(c)
     desc = _desc(zp, c)
-    S = torch.zeros(c.n_total, b, h_kv, device="cuda")
+    S = torch.zeros(B, h_kv, c.block_table.shape[1] * b, device="cuda")
     # the last w steps of each sequence, queries from the seeded generator
     final = c.seq_lens.tolist()
     qw = zp_inputs.normal((B, w, h_q, d), 901, dtype)
@@ -186,7 +211,7 @@ def test_end_to_end_compression(zp, shape):
         q = qw[:, u].contiguous().cuda()
         zp.zp_paged_decode_attn(desc, q, dc.K[0], dc.V[0], dc.table, lens_d, torch.empty_like(q),
                                 score_accum=S, window=w)
-    F = torch.zeros_like(S)
+    F = torch.zeros(c.n_total, b, h_kv, device="cuda")
     Lmax = max(final)
     scores = torch.empty(B, h_kv, Lmax, device="cuda")
     first = torch.ones(B, dtype=torch.uint8, device="cuda")
@@ -209,7 +234,7 @@ def test_end_to_end_compression(zp, shape):
         new_tables.append(plan["new_table"])
         pool.release(plan["dropped"])
     zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, torch.from_numpy(tg).cuda(), dc.lens,
-                        keep, k)
+                        keep, k, scores=S)
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     # ---- oracle, same steps
@@ -225,6 +250,7 @@ def test_end_to_end_compression(zp, shape):
         Sref = oracle.window_score(qw[s].float().numpy(), K0, c.block_table[s].numpy(), L, w)
         Fref = np.zeros((c.n_total, b, h_kv))
         sref = pipeline.final_scores(Sref, K0, Fref, c.block_table[s].numpy(), L, b, True, P)
+        Fg = F.cpu().numpy()
         for h in range(h_kv):
             kref = oracle.topk_keep(sref[h], k)[0]
             swaps += keep_sets_match(kept_all[s, h], kref, sref[h], k, L)
@@ -238,6 +264,8 @@ def test_end_to_end_compression(zp, shape):
                 db, ds = tg[s, r // b], r % b
                 assert np.array_equal(Kg[db, ds, h], K0[sb, ss, h])
                 assert np.array_equal(Vg[db, ds, h], V0[sb, ss, h])
+                # F of the new slot: the global score (first compression: S) of the kept token
+                np.testing.assert_allclose(Fg[db, ds, h], Fref[sb, ss, h], **TOL_SCORE[dtype])
         assert len(new_tables[s]) == N_max
     print("reported tie swaps:", swaps)
     assert pool.num_free == c.n_total - B * N_max

@@ -101,7 +101,7 @@ def test_decode_full_size_qwen_layer_sampled(zp):
     window score of the same sampled sequences."""
     c = zp_inputs.make_paged_case(1002, 64, 32, 8, 128, 16, len_range=(1024, 4096), dtype="bf16")
     dc = DeviceCase(c)
-    S = torch.zeros(c.n_total, 16, 8, dtype=torch.float32, device="cuda")
+    S = torch.zeros(64, 8, c.block_table.shape[1] * 16, dtype=torch.float32, device="cuda")
     got = _run_decode(zp, dc, score=S, window=16)
     seqs = [0, 9, 17, 33, 47, 63]
     K, V = dc.np_k(), dc.np_v()
@@ -114,8 +114,7 @@ def test_decode_full_size_qwen_layer_sampled(zp):
     Sg = S.cpu().numpy().astype(np.float64)
     for i, s in enumerate(seqs):
         L = int(c.seq_lens[s])
-        np.testing.assert_allclose(gather_slots(Sg, c.block_table[s].numpy(), L, 16),
-                                   gather_slots(S_ref, c.block_table[s].numpy(), L, 16),
+        np.testing.assert_allclose(Sg[s, :, :L], gather_slots(S_ref, c.block_table[s].numpy(), L, 16),
                                    **TOL_SCORE["bf16"])
 
 
@@ -132,8 +131,13 @@ def test_window_score_accumulates_over_decode_steps(zp, dtype, h_q, h_kv, d, w):
     c = zp_inputs.make_paged_case(40 + w, B, h_q, h_kv, d, b, lens=final, dtype=dtype)
     dc = DeviceCase(c)
     desc = _desc(zp, c)
-    S = torch.randn(c.n_total, b, h_kv, device="cuda").abs()
-    S_ref = S.cpu().numpy().astype(np.float64)
+    stride = c.block_table.shape[1]
+    S = torch.randn(B, h_kv, stride * b, device="cuda").abs()  # stale values: overwritten at the first row
+    S0 = S.cpu().numpy().astype(np.float64)
+    S_ref = np.zeros((c.n_total, b, h_kv))  # the oracle's paged copy of the same rows
+    for s, L in enumerate(final):
+        t = np.arange(L)
+        S_ref[c.block_table[s].numpy()[t // b], t % b] = S0[s, :, :L].T
     qw = zp_inputs.normal((B, w, h_q, d), 77, dtype)
     kw = zp_inputs.normal((B, w, h_kv, d), 78, dtype)
     vw = zp_inputs.normal((B, w, h_kv, d), 79, dtype)
@@ -155,7 +159,7 @@ def test_window_score_accumulates_over_decode_steps(zp, dtype, h_q, h_kv, d, w):
     Sg = S.cpu().numpy().astype(np.float64)
     K = dc.np_k()
     for s, L in enumerate(final):
-        got = gather_slots(Sg, c.block_table[s].numpy(), L, b)
+        got = Sg[s, :, :L]
         np.testing.assert_allclose(got, gather_slots(S_ref, c.block_table[s].numpy(), L, b),
                                    **TOL_SCORE[dtype])
         explicit = oracle.window_score(qw[s].float().numpy(), K, c.block_table[s].numpy(), L, w)

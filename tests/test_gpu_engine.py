@@ -14,92 +14,11 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import zp_inputs
-from oracle import pipeline
-from tests.gpu_util import TOL_OUT, keep_sets_match
+from tests.gpu_util import TOL_OUT
+from tests.oracle_loop import OracleLoop
 
 pytestmark = pytest.mark.gpu
-
-
-class OracleLoop:
-    """The same loop on the oracle (fp64 arithmetic, float32 caches holding the
-    bf16 values, a Python mirror of the pool)."""
-
-    def __init__(self, cfg, K, V, table, lens):
-        self.c = cfg
-        self.K, self.V = K.copy(), V.copy()  # [layers][N_total][b][h_kv][d] float32
-        self.S = np.zeros(K.shape[:-1])      # [layers][N_total][b][h_kv] fp64
-        self.F = np.zeros(K.shape[:-1])
-        self.table = table.copy()
-        self.lens = lens.copy()
-        self.first = np.ones(len(lens), dtype=bool)
-        self.ref = np.zeros(cfg["n_total"], dtype=np.int32)
-        for x in table.flatten():
-            if x >= 0:
-                self.ref[x] += 1
-
-    def alloc(self):
-        free = np.nonzero(self.ref == 0)[0]
-        blk = int(free[0])
-        self.ref[blk] = 1
-        return blk
-
-    def step(self, q, kn, vn):
-        c = self.c
-        b = c["b"]
-        for s in range(len(self.lens)):
-            pos = int(self.lens[s])
-            if pos % b == 0 and self.table[s, pos // b] < 0:
-                self.table[s, pos // b] = self.alloc()
-        self.lens += 1
-        outs = []
-        for l in range(c["layers"]):
-            for s in range(len(self.lens)):
-                P = int(self.lens[s]) - 1
-                blk = self.table[s, P // b]
-                self.K[l, blk, P % b] = kn[l, s]
-                self.V[l, blk, P % b] = vn[l, s]
-            out, probs = oracle.decode_attention(q[l], self.K[l], self.V[l], self.table, self.lens, want_probs=True)
-            S = np.ascontiguousarray(self.S[l])
-            oracle.accumulate_window_score(probs, self.table, self.lens, c["h_kv"], b, c["w"], S)
-            self.S[l] = S
-            outs.append(out)
-        trig = [s for s in range(len(self.lens)) if oracle.needs_compression(int(self.lens[s]), b, c["N_max"])]
-        return np.stack(outs), trig
-
-    def compress(self, s, gpu_keep):
-        """Scores and keep sets of sequence s on every layer; returns the number
-        of reported near-tie swaps.  The moves use the GPU's keep sets."""
-        c = self.c
-        b, N_max = c["b"], c["N_max"]
-        L = int(self.lens[s])
-        k = (N_max - 1) * b
-        N = L // b
-        fresh = np.nonzero(self.ref == 0)[0].astype(np.int32)
-        plan = oracle.plan_targets(self.table[s, :N], N_max, self.ref, fresh)
-        for blk in plan["new_table"]:
-            if self.ref[blk] == 0:
-                self.ref[blk] = 1
-        swaps = 0
-        prm = pipeline.ScoreParams(window=c["w"])
-        for l in range(c["layers"]):
-            S_seq = pipeline.gather_slots(self.S[l], self.table[s], L, b)
-            F = np.ascontiguousarray(self.F[l])
-            sc = pipeline.final_scores(S_seq, self.K[l], F, self.table[s], L, b, bool(self.first[s]), prm)
-            self.F[l] = F
-            for h in range(c["h_kv"]):
-                ref_keep = oracle.topk_keep(sc[h], k)[0]
-                swaps += keep_sets_match(gpu_keep[l, h], ref_keep, sc[h], k, L)
-        pipeline.compact_sequence([self.K, self.V, self.F], [c["d"] * 4, c["d"] * 4, 8], b, c["h_kv"],
-                                  self.table[s], N, plan["targets"], gpu_keep, L)
-        for blk in list(plan["released"]) + list(plan["dropped_shared"]):
-            self.ref[blk] -= 1
-        self.table[s, :] = -1
-        self.table[s, :N_max] = plan["new_table"]
-        self.lens[s] = k
-        self.first[s] = False
-        return swaps
 
 
 @pytest.mark.parametrize("layers,async_compress", [(1, False), (2, False), (2, True)])

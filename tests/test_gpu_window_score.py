@@ -98,13 +98,12 @@ def test_prefill_then_compress(zp, shape):
     F = torch.zeros(c.n_total, b, h_kv, device="cuda")
     first = torch.ones(B, dtype=torch.uint8, device="cuda")
     scores = torch.empty(B, h_kv, Lmax, device="cuda")
-    zp.zp_score_tokens(desc, zp.score_params(window=w), dc.K[0], dc.table, dc.lens, first, None, F, scores,
-                       window_score=S)
+    zp.zp_score_tokens(desc, zp.score_params(window=w), dc.K[0], dc.table, dc.lens, first, S, F, scores)
     k = (N_max - 1) * b
     keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
     zp.zp_select_topk(scores, dc.lens, k, keep)
     targets = c.block_table[:, : N_max - 1].contiguous().cuda()
-    zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k)
+    zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k, scores=S)
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     K0 = c.k_cache[0].float().numpy()

@@ -6,8 +6,10 @@ DecodeLoop driver.
   kept), 2048 decode steps with compression whenever the §4.1 trigger holds.
   Checked: no device error; every sequence compressed; none holds more than
   N_max blocks; the pool accounts for every block; sampled keep sets are
-  ascending and complete; the last step's attention output of sampled
-  sequences against the oracle on the cache as the kernels left it.
+  ascending and complete; two sequences (the longest, and the shortest that
+  starts above the budget) mirrored by the oracle loop for the first 256
+  steps: outputs every step (after a compression they read the moved rows),
+  triggers and keep sets.
 * Prefix-shared, 36 layers: 32q/8kv/128 bf16, 32 sequences sharing a
   1024-token prefix (64 blocks), private tails uniform in [0, 2048], budget
   N_max = 64 blocks, compression asynchronous on the side stream while the
@@ -15,17 +17,18 @@ DecodeLoop driver.
   every compaction must go to fresh target blocks (§4.4).  Checked: the
   prefix blocks are never written; after all sequences compressed, only the
   prefix cache holds them; the sequences' blocks are disjoint and at most
-  N_max each; the pool accounts for every block; decode outputs of sampled
-  sequences on the first and last layer against the oracle.
-The cache contents are drawn on the device from seeded generators; the oracle
-reads back the blocks it checks.
+  N_max each; the pool accounts for every block; two sequences mirrored by
+  the oracle loop on the first and last layer over all steps they decode.
+The cache contents and per-step inputs are drawn on the device from seeded
+generators; the oracle loops start from a copy of the mirrored sequences'
+blocks taken before any kernel ran and then keep their own state.
 """
 import numpy as np
 import pytest
 import torch
 
-import oracle
 from tests.gpu_util import TOL_OUT
+from tests.oracle_loop import OracleLoop
 
 pytestmark = pytest.mark.gpu
 
@@ -45,18 +48,36 @@ def _check_pool(loop, extra=()):
     assert loop.pool.num_free + len(held) == loop.n_total
 
 
-def _oracle_decode(loop, layer, q, seqs):
-    """Oracle attention of `seqs` on layer `layer`, reading back only the
-    blocks those sequences hold (renumbered)."""
-    tab = loop.table[seqs]
-    blocks = np.unique(tab[tab >= 0])
-    remap = np.full(loop.n_total, -1, dtype=np.int32)
-    remap[blocks] = np.arange(len(blocks), dtype=np.int32)
-    sub = np.where(tab >= 0, remap[np.maximum(tab, 0)], -1).astype(np.int32)
-    idx = torch.from_numpy(blocks.astype(np.int64)).to(loop.K.device)
-    K = loop.K[layer].index_select(0, idx).float().cpu().numpy()
-    V = loop.V[layer].index_select(0, idx).float().cpu().numpy()
-    return oracle.decode_attention(q.float().cpu().numpy(), K, V, sub, loop.lens[seqs])
+def _mirror(loop, seqs, layers, N_max, w):
+    """An oracle loop over `seqs` on `layers`, from the blocks they hold now."""
+    Kb, Vb = [], []
+    lidx = torch.tensor(layers, device=loop.K.device)
+    for s in seqs:
+        blk = torch.from_numpy(loop.table[s][loop.table[s] >= 0].astype(np.int64)).to(loop.K.device)
+        Kb.append(loop.K.index_select(0, lidx).index_select(1, blk).float().cpu().numpy())
+        Vb.append(loop.V.index_select(0, lidx).index_select(1, blk).float().cpu().numpy())
+    cfg = dict(h_q=loop.h_q, h_kv=loop.h_kv, d=loop.d, b=loop.b, N_max=N_max, w=w)
+    return OracleLoop.mirror(cfg, Kb, Vb, loop.lens[seqs], loop.stride, spare=loop.stride + 4)
+
+
+def _mirror_step(ora, loop, seqs, layers, q, kn, vn, trig):
+    """One step of the oracle loop; compares outputs, triggers and (at a
+    compression) keep sets with the device.  Returns reported near-ties."""
+    li = torch.tensor(layers, device=q.device)
+    si = torch.from_numpy(np.asarray(seqs, dtype=np.int64)).to(q.device)
+    pick = lambda x: x.index_select(0, li).index_select(1, si).float().cpu().numpy()
+    out_ref, trig_ref = ora.step(pick(q), pick(kn), pick(vn))
+    np.testing.assert_allclose(pick(loop.out), out_ref, **TOL_OUT["bf16"])
+    assert [seqs[i] for i in trig_ref] == [s for s in seqs if s in set(trig)]
+    swaps = 0
+    if trig_ref:
+        torch.cuda.synchronize()  # the keep sets are written on the side stream
+        gseqs, keep = loop.last_keep
+        keep = keep.index_select(0, li).cpu().numpy()
+        pos = {int(x): i for i, x in enumerate(gseqs)}
+        for i in trig_ref:
+            swaps += ora.compress(i, keep[:, pos[seqs[i]]])
+    return swaps
 
 
 def test_high_concurrency_512_sequences_2048_steps():
@@ -70,24 +91,25 @@ def test_high_concurrency_512_sequences_2048_steps():
     loop.add_sequences(lens0)
     loop.K.copy_(_dev_normal(loop.K.shape, 11))
     loop.V.copy_(_dev_normal(loop.V.shape, 12))
+    above = np.nonzero(lens0 > N_max * b)[0]
+    mseqs = [int(above[np.argmin(lens0[above])]), int(np.argmax(lens0))]
+    ora = _mirror(loop, mseqs, [0], N_max, b)
     compressed = np.zeros(B, dtype=bool)
+    swaps = 0
     for step in range(steps):
         q = _dev_normal((1, B, h_q, d), 100000 + step)
         kn = _dev_normal((1, B, h_kv, d), 200000 + step)
         vn = _dev_normal((1, B, h_kv, d), 300000 + step)
         trig = loop.step(q, kn, vn)
+        if step < 256:
+            swaps += _mirror_step(ora, loop, mseqs, [0], q, kn, vn, trig)
         if trig:
             compressed[trig] = True
             if step % 97 == 0:
                 seqs, keep = loop.last_keep
                 kp = keep[0].cpu().numpy()  # [n][h_kv][k]
                 assert np.all(np.diff(kp, axis=-1) > 0) and np.all(kp[..., 0] >= 0)
-    decoded = np.nonzero(loop.active)[0]  # decoded in the last step and not compacting now
-    torch.cuda.synchronize()
-    sample = decoded[[0, len(decoded) // 3, 2 * len(decoded) // 3, -1]]
-    ref = _oracle_decode(loop, 0, q[0][torch.from_numpy(sample).cuda()], sample)
-    np.testing.assert_allclose(loop.out[0][torch.from_numpy(sample).cuda()].float().cpu().numpy(), ref,
-                               **TOL_OUT["bf16"])
+    assert not ora.first.any()  # both mirrored sequences compressed
     loop.drain()
     torch.cuda.synchronize()
     import compressed_paged_kv_zp_gb300 as zp
@@ -95,7 +117,7 @@ def test_high_concurrency_512_sequences_2048_steps():
     assert compressed.all()
     assert (loop.table >= 0).sum(axis=1).max() <= N_max
     _check_pool(loop)
-    print("compressions:", loop.compressions)
+    print("compressions:", loop.compressions, "reported near-tie swaps:", swaps)
 
 
 def test_prefix_shared_36_layers_async():
@@ -125,8 +147,11 @@ def test_prefix_shared_36_layers_async():
     K_prefix = loop.K.index_select(1, pidx).clone()
     V_prefix = loop.V.index_select(1, pidx).clone()
     assert all(loop.pool.refcount(int(x)) == B + 1 for x in prefix)
+    mseqs = [int(np.argmax(lens0)), int(np.argmin(lens0))]
+    mlayers = [0, layers - 1]
+    oras = [_mirror(loop, [s], mlayers, N_max, b) for s in mseqs]
     seen = np.zeros(B, dtype=bool)
-    checked = 0
+    checked, swaps = 0, 0
     for step in range(steps):
         q = _dev_normal((layers, B, h_q, d), 400000 + step)
         kn = _dev_normal((layers, B, h_kv, d), 500000 + step)
@@ -136,19 +161,15 @@ def test_prefix_shared_36_layers_async():
         if trig:
             plan = loop.pending[-1][2]
             assert not set(plan["targets"].ravel().tolist()) & set(prefix.tolist())
-        if step % 7 == 3:
-            decoded = np.nonzero(loop.active)[0]
-            torch.cuda.synchronize()
-            s = decoded[step % len(decoded): step % len(decoded) + 1]
-            for l in (0, layers - 1):
-                ref = _oracle_decode(loop, l, q[l, s], s)
-                np.testing.assert_allclose(loop.out[l, s].float().cpu().numpy(), ref, **TOL_OUT["bf16"])
+        for s, ora in zip(mseqs, oras):
+            if loop.active[s] or s in trig:  # decoded in this step
+                swaps += _mirror_step(ora, loop, [s], mlayers, q, kn, vn, trig)
                 checked += 1
     loop.drain()
     torch.cuda.synchronize()
     import compressed_paged_kv_zp_gb300 as zp
     assert zp.zp_device_status() == (0, 0)
-    assert seen.all() and checked > 0
+    assert seen.all() and checked > 40
     assert torch.equal(loop.K.index_select(1, pidx), K_prefix)
     assert torch.equal(loop.V.index_select(1, pidx), V_prefix)
     assert all(loop.pool.refcount(int(x)) == 1 for x in prefix)
@@ -158,4 +179,5 @@ def test_prefix_shared_36_layers_async():
     allb = np.concatenate(held)
     assert len(np.unique(allb)) == len(allb)
     _check_pool(loop, extra=prefix.tolist())
-    print("compressions:", loop.compressions)
+    assert not any(o.first.any() for o in oras)
+    print("compressions:", loop.compressions, "mirrored steps:", checked, "reported near-tie swaps:", swaps)

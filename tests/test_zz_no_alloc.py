@@ -32,14 +32,14 @@ def test_noalloc_decode_matches_workspace_decode_twice():
     dev = torch.device("cuda")
     c = zp_inputs.make_paged_case(2024, 24, 32, 8, 128, 16, len_range=(1, 1500), dtype="bf16")
     desc, q, K, V, table, lens = _args(zp, c, dev)
-    S_ref = torch.zeros(c.n_total, 16, 8, device=dev)
+    S_ref = torch.zeros(c.B, 8, table.shape[1] * 16, device=dev)
     out_ref = torch.empty_like(q)
     zp.zp_paged_decode_attn(desc, q, K, V, table, lens, out_ref, score_accum=S_ref, window=16)
     torch.cuda.synchronize()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         out = torch.full_like(q, float("nan"))
-        S = torch.zeros(c.n_total, 16, 8, device=dev)
+        S = torch.zeros(c.B, 8, table.shape[1] * 16, device=dev)
         rc = zp.lib.zp_paged_decode_attn_noalloc(
             ctypes.byref(desc), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(K.data_ptr()),
             ctypes.c_void_p(V.data_ptr()), ctypes.c_void_p(table.data_ptr()), table.shape[1],
