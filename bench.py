@@ -28,6 +28,7 @@ than the 129 MB L2, so no flush is needed between steps.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -66,9 +67,10 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, kept for the samples whose
+    timestamps fall inside the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -76,44 +78,66 @@ class ClockSampler:
         self.idx = device_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
+        """Starts sampling and waits (up to 5 s) for the first sample."""
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        t_end = time.time() + 5.0
+        while time.time() < t_end and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, cmax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                if self.t0 is not None and not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(clk)
+                smax.append(cmax)
+                try:
+                    power.append(float(parts[4]))
+                except ValueError:
+                    pass
+                for n, v in zip(names, parts[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "power_w": statistics.median(power) if power else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
@@ -279,17 +303,17 @@ def _barrier(dist):
 
 
 class OracleSample:
-    """The CPU oracle on a bounded sample of one step of the workload: decode
-    (with the window-score accumulation) of n_seqs sequences and the
-    compression (scores, top-k, Alg. 4 moves) of n_comp triggered sequences --
-    about the workload's ratio of 7 compressions per 64 decodes."""
+    """The CPU oracle on the workload, one sequence-step at a time: step i
+    decodes sequence i mod B (attention with the window-score accumulation)
+    and, on every 9th step, compresses one triggered sequence (scores, top-k,
+    Alg. 4 moves) -- about the workload's 7 compressions per 64 decodes."""
 
-    def __init__(self, wl_name: str, n_seqs: int = 16, n_comp: int = 2, seed_offset: int = 0):
+    def __init__(self, wl_name: str, seed_offset: int = 0):
         import oracle
         from oracle import pipeline
         self.oracle, self.pipeline = oracle, pipeline
         B, h_q, h_kv, d, b, N_max, lr, dtype, seed = WORKLOADS[wl_name]
-        self.geom = (h_kv, d, b, N_max)
+        self.geom = (B, h_kv, d, b, N_max)
         c = zp_inputs.make_paged_case(seed + seed_offset, B, h_q, h_kv, d, b, len_range=lr, dtype=dtype)
         self.c = c
         self.K = c.k_cache[0].float().numpy()
@@ -299,30 +323,31 @@ class OracleSample:
         self.q = c.q.float().numpy()
         self.lens = c.seq_lens.numpy()
         self.table = c.block_table.numpy()
-        trig = [s for s in range(B) if oracle.needs_compression(int(self.lens[s]), b, N_max)][:n_comp]
-        rest = [s for s in range(B) if s not in trig]
-        self.trig = trig
-        self.seqs = trig + rest[: max(n_seqs - len(trig), 0)]
+        self.trig = [s for s in range(B) if oracle.needs_compression(int(self.lens[s]), b, N_max)]
+        self.S = np.zeros((c.n_total, b, h_kv))
+        self.F = np.zeros((c.n_total, b, h_kv))
+        self.prm = pipeline.ScoreParams(window=b)
 
-    def step(self) -> float:
+    def step(self, i: int) -> float:
         oracle, pipeline = self.oracle, self.pipeline
-        h_kv, d, b, N_max = self.geom
-        seqs, lens, table = self.seqs, self.lens, self.table
-        S = np.zeros((self.c.n_total, b, h_kv))
+        B, h_kv, d, b, N_max = self.geom
+        lens, table = self.lens, self.table
+        s = [i % B]
         t0 = time.perf_counter()
-        out, probs = oracle.decode_attention(self.q[seqs], self.K, self.V, table[seqs], lens[seqs],
-                                             want_probs=True)
-        oracle.accumulate_window_score(probs, table[seqs], lens[seqs], h_kv, b, b, S)
-        prm = pipeline.ScoreParams(window=b)
-        F = np.zeros((self.c.n_total, b, h_kv))
-        for s in self.trig:
-            L = int(lens[s])
-            sc = pipeline.final_scores(pipeline.gather_slots(S, table[s], L, b), self.K, F, table[s], L, b,
-                                       True, prm)
+        _, probs = oracle.decode_attention(self.q[s], self.K, self.V, table[s], lens[s], want_probs=True)
+        oracle.accumulate_window_score(probs, table[s], lens[s], h_kv, b, b, self.S)
+        if i % 9 == 8 and self.trig:
+            t = self.trig[(i // 9) % len(self.trig)]
+            L = int(lens[t])
+            sc = pipeline.final_scores(pipeline.gather_slots(self.S, table[t], L, b), self.K, self.F, table[t],
+                                       L, b, True, self.prm)
             keep = pipeline.keep_sets(sc, (N_max - 1) * b)
-            pipeline.compact_sequence([self.Kraw, self.Vraw], [d * 2, d * 2], b, h_kv, table[s], L // b,
-                                      table[s][:N_max - 1], keep[None], L)
+            pipeline.compact_sequence([self.Kraw, self.Vraw], [d * 2, d * 2], b, h_kv, table[t], L // b,
+                                      table[t][:N_max - 1], keep[None], L)
         return time.perf_counter() - t0
+
+    SAMPLE = ("one sequence-step per step: decode of one sequence of the workload with the window-score "
+              "accumulation, plus one compression of a triggered sequence every 9th step")
 
 
 def run_reference(args):
@@ -332,23 +357,20 @@ def run_reference(args):
         return 0
     wl = args.workload
     sample = OracleSample(wl)
-    n_sample = len(sample.seqs)
     times = []
     for i in range(args.warmup + args.steps):
-        dt = sample.step()
+        dt = sample.step(i)
         if i >= args.warmup:
             times.append(dt)
     tot = sum(times)
-    value = n_sample * len(times) / tot
+    value = len(times) / tot
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "seq-steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl, "sample": "%d of %d sequences per step" % (
-            n_sample, WORKLOADS[wl][0])},
+        "data": "synthetic", "config": {"workload": wl, "sample": OracleSample.SAMPLE},
         "cpu_baseline": {"value": value, "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
-                         "sample": "decode + window score of %d sequences and the compression of two "
-                                   "triggered sequences, per step" % n_sample},
+                         "sample": OracleSample.SAMPLE},
         "e2e": {"value": value, "unit": "seq-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -358,7 +380,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zp", choices=["zp", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -392,6 +414,7 @@ def main():
     clocks.start()
     _barrier(dist)
     torch.cuda.synchronize()
+    clocks.mark_start()
     start.record(stream)
     for i in range(args.steps):
         zp.zp_append_kv(wl.desc, wl.k_new, wl.v_new, wl.K, wl.V, wl.table, wl.lens)
@@ -402,6 +425,7 @@ def main():
         wl.compress()
     stop.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_stop()
     _barrier(dist)
     clk = clocks.stop()
     elapsed_ms = start.elapsed_time(stop)
@@ -457,12 +481,14 @@ def main():
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # a bounded sample: sequence-steps for about 10 s of CPU time (at least 18)
         sample = OracleSample(args.workload)
-        n = len(sample.seqs)
-        dt = sample.step()
-        line["cpu_baseline"] = {"value": n / dt, "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
-                                "sample": "decode + window score of %d of %d sequences and the "
-                                          "compression of two triggered sequences (one step)" % (n, wl.B)}
+        tot, n = 0.0, 0
+        while n < 18 or (tot < 10.0 and n < 10 * wl.B):
+            tot += sample.step(n)
+            n += 1
+        line["cpu_baseline"] = {"value": n / tot, "unit": "seq-steps/s", "cores": 1, "kind": "oracle",
+                                "sample": "%d steps of: %s" % (n, OracleSample.SAMPLE)}
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:

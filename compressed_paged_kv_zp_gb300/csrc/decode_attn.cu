@@ -68,6 +68,7 @@ struct DecodeArgs {
     int *unit_prefix;  // [B+1]
     int4 *unit_info;   // [units]: (sequence, first token, length, window flags) of every unit
     long long logits_units;  // capacity of `logits` in units
+    unsigned long long *ctl;  // [B] per-sequence control words of the in-kernel merge (tensor-core path)
     unsigned *err;
 };
 
@@ -611,6 +612,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
             }
         }
     }
+
 }
 
 // Window-score epilogue: one block per unit, one thread per (kv head, token)
@@ -686,11 +688,18 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
 // groups.  One consumer warp per kv head.  P is rounded to bf16 for the
 // second product; the scores and the softmax statistics stay in fp32.
 constexpr int kTcTokens = 16;     // tokens per unit
+// Epilogue region of shared memory: 8 ints, an mbarrier, (max, 1/sum) of up to
+// 64 q heads, up to kMaxSeg window segments {sequence, first token, end token,
+// byte offset}, the merged sequences' (max, 1/sum), then the first unit of
+// every CTA (grid + 1 long longs).
+constexpr int kEpiBar = 32, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
+constexpr int kEpiMl = kEpiSeg + kMaxSeg * 16;  // (M, 1/L) of the merged sequences: 2 x 64 float2
+constexpr int kEpiCst = kEpiMl + 2 * 64 * 8;
 constexpr int kTcPad = 16;        // bytes of padding after each staged token row
 
 __host__ __device__ inline int tc_row_stride(int h_kv, int d) { return h_kv * d * 2 + kTcPad; }
 
-__host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int halves, int B) {
+__host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int halves, int B, int grid) {
     SmemLayout L;
     int off = 0;
     L.bar_off = off;
@@ -701,13 +710,361 @@ __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int h
     L.stage_off = off;
     off += stages * 2 * kTcTokens * tc_row_stride(h_kv, halves * 64);
     L.warp_off = off;
-    L.merge_off = off;
+    L.merge_off = off;  // epilogue: see kEpi* offsets
+    off += kEpiCst + (grid + 1) * 8;
     L.prefix_off = off;
     off += (B + 1) * 4;
     L.lens_off = off;
     off += B * 4;
     L.total = (off + 127) / 128 * 128 + 1024;  // + slack to align the base at run time
     return L;
+}
+
+// ---------------------------------------------------------------------------
+// In-kernel epilogue of the tensor-core path (cooperative launch: every CTA is
+// resident).  After its main loop a CTA announces its parts of the sequences
+// cut between CTAs (at most its first and its last); the last CTA to announce
+// merges the sequence, then publishes it.  Every CTA then computes the window
+// score of its own units, waiting (bounded) only for the publication of its
+// cut sequences.  Merges never wait, so every publication happens.
+//
+// Per-sequence control word (64 bits): (kCtlTag << 16) | phase << 15 | count.
+// Phase 0 counts arrivals; the last arrival sets phase 1 ("published": every
+// part's record is written).
+// A word without the tag -- zero, or memory never written -- and a published
+// word left by an earlier call read as phase 0, count 0, so the workspace
+// needs no clearing between calls.
+constexpr unsigned long long kCtlTag = 0xC0DE5EC7A11Dull;  // 48 bits
+
+__device__ __forceinline__ unsigned long long ctl_word(int phase, int count) {
+    return (kCtlTag << 16) | ((unsigned long long)phase << 15) | (unsigned long long)count;
+}
+__device__ __forceinline__ bool ctl_valid(unsigned long long w) { return (w >> 16) == kCtlTag; }
+
+// CTA owning unit u, from the table cst[0..G] of first units (binary search).
+__device__ __forceinline__ int owner_of(long long u, const long long *cst, int G) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cst[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The CTAs that own units of [p0, p1): c_lo..c_hi, of which the returned
+// number own at least one.
+__device__ __forceinline__ int parts_of(long long p0, long long p1, const long long *cst, int G, int *c_lo,
+                                        int *c_hi) {
+    *c_lo = owner_of(p0, cst, G);
+    *c_hi = owner_of(p1 - 1, cst, G);
+    int n = 0;
+    for (int c = *c_lo; c <= *c_hi; ++c) n += cst[c + 1] > cst[c] ? 1 : 0;
+    return n;
+}
+
+// Announces one part; true for the last of n_parts, whose update publishes
+// the sequence (every part's record is then in place).  A word left
+// published by an earlier call counts as zero.
+__device__ bool ctl_arrive(unsigned long long *w, int n_parts, unsigned *err) {
+    unsigned long long cur = 0ull;  // a clean word is the common case: one round trip
+    for (int it = 0; it < 4096; ++it) {
+        const int have = (ctl_valid(cur) && ((cur >> 15) & 1) == 0) ? (int)(cur & 0x7FFF) : 0;
+        const bool last = have + 1 == n_parts;
+        const unsigned long long prev = atomicCAS(w, cur, last ? ctl_word(1, 0) : ctl_word(0, have + 1));
+        if (prev == cur) return last;
+        cur = prev;
+    }
+    record_error(err, ZP_ERR_DEVICE, 6);
+    return false;
+}
+
+// Waits (bounded) for the publication of the sequence's part records.  The word
+// stays published after the call: the next call's first arrival counts a
+// published word as zero.  False on timeout.
+__device__ bool ctl_wait_published(const unsigned long long *w, unsigned *err) {
+    const unsigned long long t0 = global_ns();
+    unsigned long long cur = *reinterpret_cast<const volatile unsigned long long *>(w);
+    while (!(ctl_valid(cur) && ((cur >> 15) & 1))) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            record_error(err, ZP_ERR_TIMEOUT, 50);
+            return false;
+        }
+        __nanosleep(32);
+        cur = *reinterpret_cast<const volatile unsigned long long *>(w);
+    }
+    return true;
+}
+
+// Merge of the partial records of the cut sequences this CTA finished last
+// (at most two, ms[0..1], -1 when absent), in two phases so that the final
+// statistics can be published before the outputs are combined:
+//     M = max_j m_j,  w_j = 2^(m_j - M),  L = sum_j w_j l_j,  out = sum_j w_j acc_j / L.
+// CTA c's record of s is slot 2c when s is the first sequence of c's range,
+// else 2c + 1.  Other CTAs wrote the records: read through L2 (ld.cg).
+
+// Part j of sequence s (p0 = its first unit): slot, or -1 for a CTA without units.
+__device__ __forceinline__ int part_slot(int c_lo, int j, long long p0, const long long *cst) {
+    const int c = c_lo + j;
+    return cst[c + 1] > cst[c] ? 2 * c + (p0 > cst[c] ? 1 : 0) : -1;
+}
+
+// Phase 1: (M, L) of every head of the merged sequences -> stats (global) and
+// sm_ml[i * h_q + h] = (M, 1/L) in shared memory.
+__device__ void merge_stats(const DecodeArgs &a, const int *ms, const int *prefix, const long long *cst, int Gd,
+                            float2 *sm_ml, int ctid, int nthr) {
+    const int h_q = a.h_q;
+    for (int it = ctid; it < 2 * h_q; it += nthr) {
+        const int i = it / h_q, h = it % h_q;
+        const int s = ms[i];
+        if (s < 0) continue;
+        const long long p0 = prefix[s];
+        int c_lo, c_hi;
+        parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
+        const int nc = c_hi - c_lo + 1;
+        float M = -INFINITY;
+        float2 v4[4];
+        for (int j0 = 0; j0 < nc; j0 += 4) {  // four loads in flight
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
+                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) M = fmaxf(M, v4[q].x);
+        }
+        float Lsum = 0.f;
+        for (int j0 = 0; j0 < nc; j0 += 4) {  // (L2 hits)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
+                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (v4[q].x != -INFINITY) Lsum += exp2f(v4[q].x - M) * v4[q].y;
+        }
+        if (a.want_score) a.stats[(size_t)s * h_q + h] = make_float2(M, Lsum);
+        sm_ml[it] = make_float2(M, Lsum > 0.f ? 1.f / Lsum : 0.f);
+    }
+}
+
+// Final (M, 1/L) of every head of cut sequence s from its part records, into
+// shared memory (one (head) item per thread; the records are published).
+__device__ void part_stats(const DecodeArgs &a, int s, const int *prefix, const long long *cst, int Gd,
+                           float2 *out, int ctid, int nthr) {
+    const int h_q = a.h_q;
+    for (int h = ctid; h < h_q; h += nthr) {
+        const long long p0 = prefix[s];
+        int c_lo, c_hi;
+        parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
+        const int nc = c_hi - c_lo + 1;
+        float M = -INFINITY, Lsum = 0.f;
+        for (int j0 = 0; j0 < nc; j0 += 4) {  // four loads in flight, online combination
+            float2 v4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
+                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (v4[q].x == -INFINITY) continue;
+                const float Mn = fmaxf(M, v4[q].x);
+                Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + v4[q].y * exp2f(v4[q].x - Mn);
+                M = Mn;
+            }
+        }
+        out[h] = make_float2(M, Lsum > 0.f ? 1.f / Lsum : 0.f);
+    }
+}
+
+// Phase 2: the outputs, one (sequence, head, 16 dims) item per thread.
+template <int D>
+__device__ void merge_outputs(const DecodeArgs &a, const int *ms, const int *prefix, const long long *cst, int Gd,
+                              const float2 *sm_ml, int ctid, int nthr) {
+    const int h_q = a.h_q;
+    constexpr int CH = 16;
+    for (int it = ctid; it < 2 * h_q * (D / CH); it += nthr) {
+        const int i = it / (h_q * (D / CH));
+        const int r = it % (h_q * (D / CH));
+        const int h = r / (D / CH);
+        const int d0 = (r % (D / CH)) * CH;
+        const int s = ms[i];
+        if (s < 0) continue;
+        const long long p0 = prefix[s];
+        int c_lo, c_hi;
+        parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
+        const int nc = c_hi - c_lo + 1;
+        const float2 Mi = sm_ml[i * h_q + h];
+        float acc[CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) acc[k] = 0.f;
+        for (int j0 = 0; j0 < nc; j0 += 2) {  // two parts' loads in flight
+            float w[2];
+            float4 x4[2][CH / 4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
+                w[q] = 0.f;
+                if (sl >= 0) {
+                    const float2 v = __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
+                    w[q] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - Mi.x);
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(a.part_acc + ((size_t)sl * h_q + h) * D + d0);
+#pragma unroll
+                    for (int q4 = 0; q4 < CH / 4; ++q4) x4[q][q4] = __ldcg(src + q4);
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < CH / 4; ++q4) x4[q][q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int q4 = 0; q4 < CH / 4; ++q4) {
+                    acc[4 * q4] += w[q] * x4[q][q4].x;
+                    acc[4 * q4 + 1] += w[q] * x4[q][q4].y;
+                    acc[4 * q4 + 2] += w[q] * x4[q][q4].z;
+                    acc[4 * q4 + 3] += w[q] * x4[q][q4].w;
+                }
+        }
+        const float inv = Mi.y;
+        uint32_t w4[CH / 2];
+#pragma unroll
+        for (int k = 0; k < CH / 2; ++k) w4[k] = f2_to_bf2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+        uint4 *og = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + ((size_t)s * h_q + h) * D + d0);
+        og[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        og[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+    }
+}
+
+// Window score of tokens [tb, te) of sequence s (tb a multiple of 16):
+//     S[kvh][t] (+)= (1/w) max_{h in group(kvh)} 2^(logit_h(t) - M_h) / L_h
+// written instead of added at the first window row and for t = P.  Chunks of
+// CT tokens: the logits rows (contiguous) and the h_kv score-row pieces come
+// into shared memory by bulk copies, are combined there, and the score pieces
+// go back by bulk copies.  buf: shared memory of buf_bytes (16-aligned);
+// sm_stats: the sequence's (M_h, 1/L_h), filled by the caller.
+template <int G, int HKV>
+__device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, int tb, int te, unsigned char *buf,
+                              int buf_bytes, uint64_t *bar, unsigned &bar_phase, volatile int *abort,
+                              float2 *sm_stats, int ctid, int nthr) {
+    constexpr int HQ = G * HKV;
+    const int P = L - 1;
+    const bool first_row = (P % a.b) == a.b - a.window;
+    const float inv_w = 1.f / (float)a.window;
+    // chunk capacity: CT tokens of logits (HQ floats each) + HKV score pieces of CT + 4 floats
+    int CT = (buf_bytes - HKV * 16) / (HQ * 4 + HKV * 4);
+    CT &= ~15;
+    const int RSF = CT + 4;  // score piece stride in floats (bank shift of 4 per kv head)
+    float *lg_s = reinterpret_cast<float *>(buf);
+    float *sc_s = lg_s + (size_t)CT * HQ;
+    float *srow0 = a.score + (size_t)s * HKV * a.score_stride;
+    const float *lg_g = a.logits + ((size_t)p0 * kTcTokens) * HQ;
+    fence_proxy_async_smem();  // earlier ordinary writes to buf precede the copies into it
+    named_bar_sync(1, nthr);
+    for (int c0 = tb; c0 < te; c0 += CT) {
+        const int n = min(CT, te - c0);
+        const int n16 = (n + 15) & ~15;  // whole units: in bounds of the logits and score rows
+        if (ctid == 0) {
+            mbar_arrive_expect_tx(bar, (unsigned)(n16 * HQ * 4 + HKV * n16 * 4));
+            bulk_g2s_plain(lg_s, lg_g + (size_t)c0 * HQ, (unsigned)(n16 * HQ * 4), bar);
+#pragma unroll
+            for (int kvh = 0; kvh < HKV; ++kvh)
+                bulk_g2s_plain(sc_s + kvh * RSF, srow0 + (size_t)kvh * a.score_stride + c0, (unsigned)(n16 * 4), bar);
+        }
+        const bool got = mbar_wait_bounded(bar, bar_phase, a.err, abort, 60);
+        bar_phase ^= 1u;
+        if (got) {
+            for (int it = ctid; it < n * HKV; it += nthr) {
+                const int t = it / HKV, kvh = it % HKV;
+                const int tok = c0 + t;
+                float x[G];
+                if constexpr (G % 4 == 0) {
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const float4 v = reinterpret_cast<const float4 *>(lg_s + (size_t)t * HQ + kvh * G)[q4];
+                        x[4 * q4] = v.x;
+                        x[4 * q4 + 1] = v.y;
+                        x[4 * q4 + 2] = v.z;
+                        x[4 * q4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) x[j] = lg_s[(size_t)t * HQ + kvh * G + j];
+                }
+                float best = 0.f;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float2 st = sm_stats[kvh * G + j];
+                    best = fmaxf(best, exp2f(x[j] - st.x) * st.y);
+                }
+                float &dst = sc_s[kvh * RSF + t];
+                dst = (first_row || tok == P) ? best * inv_w : dst + best * inv_w;
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, nthr);
+        if (ctid == 0) {
+            if (got) {
+#pragma unroll
+                for (int kvh = 0; kvh < HKV; ++kvh)
+                    bulk_s2g(srow0 + (size_t)kvh * a.score_stride + c0, sc_s + kvh * RSF, (unsigned)(n16 * 4));
+                bulk_commit();
+            }
+            bulk_wait_read_all();  // the pieces may be overwritten by the next chunk
+        }
+        named_bar_sync(1, nthr);
+    }
+}
+
+// Window score of a prefetched segment: tokens [tb, tb + n) of sequence s,
+// logits lg_s [n16][HQ] and the score pieces sc_s [HKV][n16 + 4] already in
+// shared memory; the pieces are updated there and written back by bulk
+// copies (committed, not waited for).  sm_stats holds (M_h, 1/L_h).
+template <int G, int HKV>
+__device__ void score_prefetched(const DecodeArgs &a, int s, int L, int tb, int n, int n16, const float *lg_s,
+                                 float *sc_s, const float2 *sm_stats, int ctid, int nthr) {
+    constexpr int HQ = G * HKV;
+    const int P = L - 1;
+    const bool first_row = (P % a.b) == a.b - a.window;
+    const float inv_w = 1.f / (float)a.window;
+    const int RSF = n16 + 4;
+    for (int it = ctid; it < n * HKV; it += nthr) {
+        const int t = it / HKV, kvh = it % HKV;
+        float x[G];
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < G / 4; ++q4) {
+                const float4 v = reinterpret_cast<const float4 *>(lg_s + (size_t)t * HQ + kvh * G)[q4];
+                x[4 * q4] = v.x;
+                x[4 * q4 + 1] = v.y;
+                x[4 * q4 + 2] = v.z;
+                x[4 * q4 + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < G; ++j) x[j] = lg_s[(size_t)t * HQ + kvh * G + j];
+        }
+        float best = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const float2 st = sm_stats[kvh * G + j];
+            best = fmaxf(best, exp2f(x[j] - st.x) * st.y);
+        }
+        float &dst = sc_s[kvh * RSF + t];
+        dst = (first_row || tb + t == P) ? best * inv_w : dst + best * inv_w;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, nthr);
+    if (ctid == 0) {
+        float *srow0 = a.score + (size_t)s * HKV * a.score_stride;
+#pragma unroll
+        for (int kvh = 0; kvh < HKV; ++kvh)
+            bulk_s2g(srow0 + (size_t)kvh * a.score_stride + tb, sc_s + kvh * RSF, (unsigned)(n16 * 4));
+        bulk_commit();
+    }
 }
 
 template <int D, int G>
@@ -719,12 +1076,20 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int B = a.B;
     const int h_kv = a.h_kv;
-    const SmemLayout lay = make_tc_layout(a.stages, h_kv, HALVES, B);
+    const SmemLayout lay = make_tc_layout(a.stages, h_kv, HALVES, B, gridDim.x);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bar_off);
     uint64_t *empty = full + a.stages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + lay.ctl_off);
     int *prefix = reinterpret_cast<int *>(smem + lay.prefix_off);
     int *lens = reinterpret_cast<int *>(smem + lay.lens_off);
+    // [0] -, [1..2] sequences to merge (-1: none), [3] broadcast, [4] cut parts, [5..6] their
+    // sequences, [7] window segments (negative: not prefetched)
+    int *mlist = reinterpret_cast<int *>(smem + lay.merge_off);
+    uint64_t *ebar = reinterpret_cast<uint64_t *>(smem + lay.merge_off + kEpiBar);  // epilogue copies
+    float2 *sm_stats = reinterpret_cast<float2 *>(smem + lay.merge_off + kEpiStats);
+    int4 *segs = reinterpret_cast<int4 *>(smem + lay.merge_off + kEpiSeg);
+    long long *cst = reinterpret_cast<long long *>(smem + lay.merge_off + kEpiCst);
+    float2 *sm_ml = reinterpret_cast<float2 *>(smem + lay.merge_off + kEpiMl);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -747,6 +1112,9 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     if (tid == 0) {
         abort_flag[0] = 0;
         abort_flag[1] = 0;
+        mlist[0] = 0;
+        mlist[4] = 0;
+        mbar_init(ebar, 1);
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], h_kv);
@@ -774,6 +1142,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const long long U = prefix[B];
     if (blockIdx.x == 0)
         for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
+    for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) cst[c] = cta_start(c, U, gridDim.x);
+    __syncthreads();
     if (a.want_score && U > a.logits_units) {
         if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 3);
         return;
@@ -812,7 +1182,6 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             const int tok0 = ntok0;
             const int blk = nblk;
             const int useq = cur_s;
-            if (a.want_score && lane == 0) a.unit_info[u] = unit_record(a, useq, tok0, lens[useq]);
             if (u + 1 < u1) {
                 while (u + 1 >= prefix[ns + 1]) ++ns;
                 ntok0 = (int)(u + 1 - prefix[ns]) * kTcTokens;
@@ -826,6 +1195,17 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             int valid = lens[useq] - tok0;
             if (valid > kTcTokens) valid = kTcTokens;
             const bool bad = blk < 0 || blk >= a.n_total;
+            if (a.want_score && (u == u0 || tok0 == 0) && lane < h_kv) {
+                // first unit of a segment on a window step: bring its score pieces into L2
+                const int L = lens[useq], P = L - 1;
+                if ((P % a.b) >= a.b - a.window) {
+                    const long long ue = prefix[useq + 1] < u1 ? prefix[useq + 1] : u1;
+                    int te = (int)(ue - prefix[useq]) * kTcTokens;
+                    if (te > L) te = L;
+                    const unsigned bytes = (unsigned)(((te - tok0) * 4 + 15) & ~15);
+                    bulk_prefetch_l2(a.score + ((size_t)useq * h_kv + lane) * a.score_stride + tok0, bytes);
+                }
+            }
             if (lane == 0) {
                 if (bad) record_error(a.err, ZP_ERR_DEVICE, 4);
                 mbar_arrive_expect_tx(&full[st], bad ? 0u : 2u * valid * row_bytes);
@@ -879,6 +1259,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
 
     int s = s_first;
     long long seg_begin = u0;
+    const uint64_t keep_pol = l2_evict_last_policy();
     reset_state();
     load_q(s);
     bool window_step = compute_window(s);
@@ -900,6 +1281,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                     const int row = valid + c / (D / 8);
                     reinterpret_cast<uint4 *>(vs + row * RS)[c % (D / 8)] = make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();  // ordered before later bulk copies into this stage
                 __syncwarp();
             }
             const uint32_t kt = smem_u32(ks);
@@ -923,11 +1305,11 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (g >= G || tk[e] >= valid) x[e] = -INFINITY;
-            if (window_step && g < G) {
+            if (window_step && g < G) {  // kept in L2 for the epilogue
                 float *lg = a.logits + ((size_t)u * kTcTokens) * a.h_q + h0 + g;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (tk[e] < valid) lg[(size_t)tk[e] * a.h_q] = x[e];
+                    if (tk[e] < valid) st_global_hint(lg + (size_t)tk[e] * a.h_q, x[e], keep_pol);
             }
             float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -1005,6 +1387,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                     }
                 }
                 if (g < G && tig == 0) a.part_ml[(size_t)slot * a.h_q + h0 + g] = make_float2(m_run, l_run);
+                if (tid == 0) mlist[5 + mlist[4]++] = s;  // announced after the loop
             }
             if (u + 1 < u1) {
                 while (u + 1 >= prefix[s + 1]) ++s;
@@ -1015,6 +1398,179 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             }
         }
     }
+
+    // =====================================================================
+    // epilogue (consumer warps; the producer has returned and every stage has
+    // been consumed, so the stage area is free scratch)
+    const int nthr = h_kv * 32;
+    unsigned char *scratch = stage_base;
+    const int scratch_bytes = a.stages * stage_bytes;
+    const int HQ = a.h_q;
+    // this thread's partial records and logits are visible to other CTAs and
+    // to the copy engine; the stage area may be overwritten by copies
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    fence_proxy_async_smem();
+    named_bar_sync(1, nthr);
+    int pre_bytes = 0;  // bytes of the stage area taken by prefetched segments (diagnostic)
+    if (warp == 0) {
+        if (lane == 0) {
+            // window segments of this CTA and, if they all fit, their prefetch
+            int nseg = 0, off = 0, tx = 0;
+            bool fits = a.want_score != 0;
+            if (a.want_score) {
+                for (int sq = s_first; sq <= s && nseg < kMaxSeg; ++sq) {
+                    if (!compute_window(sq)) continue;
+                    const long long pb = prefix[sq], pe = prefix[sq + 1];
+                    const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;
+                    const int tb = (int)(ub - pb) * kTcTokens;
+                    int te = (int)(ue - pb) * kTcTokens;
+                    if (te > lens[sq]) te = lens[sq];
+                    if (te <= tb) continue;
+                    const int n16 = (te - tb + 15) & ~15;
+                    segs[nseg++] = make_int4(sq, tb, te, off);
+                    off += n16 * HQ * 4 + h_kv * (n16 + 4) * 4;  // score pieces padded by 4 floats
+                    tx += n16 * HQ * 4 + h_kv * n16 * 4;         // bytes the copies deliver
+                }
+                bool all = true;  // every window sequence of the range got a segment entry
+                for (int sq = s_first, k2 = 0; sq <= s; ++sq)
+                    if (compute_window(sq) && lens[sq] > 0) {
+                        const long long pb = prefix[sq], pe = prefix[sq + 1];
+                        const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;
+                        if (ue > ub) all &= (k2++ < kMaxSeg);
+                    }
+                // room left for the merge's part list (at most one entry per CTA)
+                fits = all && off + 4 * (Gd + 16) <= scratch_bytes;
+            }
+            if (fits && nseg) {
+                mbar_arrive_expect_tx(ebar, (unsigned)tx);
+                for (int i = 0; i < nseg; ++i) {
+                    const int4 g = segs[i];
+                    const int n16 = (g.z - g.y + 15) & ~15;
+                    float *lg_s = reinterpret_cast<float *>(scratch + g.w);
+                    float *sc_s = lg_s + (size_t)n16 * HQ;
+                    bulk_g2s_plain(lg_s, a.logits + ((size_t)prefix[g.x] * kTcTokens + g.y) * HQ,
+                                   (unsigned)(n16 * HQ * 4), ebar);
+                    const float *srow0 = a.score + (size_t)g.x * h_kv * a.score_stride + g.y;
+                    for (int kvh = 0; kvh < h_kv; ++kvh)
+                        bulk_g2s_plain(sc_s + kvh * (n16 + 4), srow0 + (size_t)kvh * a.score_stride,
+                                       (unsigned)(n16 * 4), ebar);
+                }
+            }
+            mlist[7] = fits ? nseg : -1;
+            mlist[0] = fits ? off : 0;
+        }
+    }
+    // announce this CTA's parts of cut sequences (another warp than the
+    // prefetch when there is one); the last arriver merges.  The barrier
+    // above ordered every thread's partial records before this fence.
+    if (warp == (h_kv > 1 ? 1 : 0) && lane >= (h_kv > 1 ? 0 : 1) && lane < (h_kv > 1 ? 2 : 3)) {
+        const int i = lane - (h_kv > 1 ? 0 : 1);
+        mlist[1 + i] = -1;
+        if (i < mlist[4]) {
+            const int sc = mlist[5 + i];
+            int c_lo, c_hi;
+            const int n_parts = parts_of(prefix[sc], prefix[sc + 1], cst, Gd, &c_lo, &c_hi);
+            __threadfence();
+            if (ctl_arrive(a.ctl + sc, n_parts, a.err)) mlist[1 + i] = sc;
+            __threadfence();
+        }
+    }
+    named_bar_sync(1, nthr);
+    pre_bytes = mlist[0];
+    const int nseg = mlist[7];
+    const int *ms = mlist + 1;  // sequences this CTA merges (-1: none)
+    const bool merger = ms[0] >= 0 || ms[1] >= 0;
+    if (!a.want_score) {
+        if (merger) {
+            merge_stats(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
+            named_bar_sync(1, nthr);
+            merge_outputs<D>(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
+        }
+        return;
+    }
+    bool waited_copies = false;
+    unsigned ebar_phase = 0;
+    const int nsq = nseg >= 0 ? nseg : (s - s_first + 1);
+    // segments that need no other CTA first, then those waiting for a merge
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int k = 0; k < nsq; ++k) {
+            int sq, tb, te;
+            if (nseg >= 0) {
+                const int4 g = segs[k];
+                sq = g.x, tb = g.y, te = g.z;
+            } else {
+                sq = s_first + k;
+                if (!compute_window(sq)) continue;
+            }
+            const long long pb = prefix[sq], pe = prefix[sq + 1];
+            const bool whole = pb >= u0 && pe <= u1;
+            const bool merged = (ms[0] == sq) || (ms[1] == sq);
+            const bool need_wait = !whole && !merged;
+            if (need_wait != (pass == 1)) continue;
+            if (need_wait) {
+                if (tid == 0) {
+                    mlist[3] = ctl_wait_published(a.ctl + sq, a.err) ? 1 : 0;
+                    __threadfence();  // the part records are read after the publication
+                }
+                named_bar_sync(1, nthr);
+                const bool ok_flag = mlist[3] != 0;
+                named_bar_sync(1, nthr);
+                if (!ok_flag) continue;
+            }
+            const int L = lens[sq];
+            if (whole) {
+                for (int h = tid; h < HQ; h += nthr) {
+                    const float2 ml = __ldcg(&a.stats[(size_t)sq * HQ + h]);
+                    sm_stats[h] = make_float2(ml.x, ml.y > 0.f ? 1.f / ml.y : 0.f);
+                }
+            } else {
+                part_stats(a, sq, prefix, cst, Gd, sm_stats, tid, nthr);
+            }
+            if (nseg >= 0) {
+                if (!waited_copies) {
+                    waited_copies = true;
+                    mbar_wait_bounded(ebar, 0, a.err, abort_flag, 61);  // every thread observes the copies
+                }
+                named_bar_sync(1, nthr);
+                if (abort_flag[0]) break;  // set before the barrier by any thread that gave up: uniform
+                const int4 g = segs[k];
+                const int n = te - tb, n16 = (n + 15) & ~15;
+                float *lg_s = reinterpret_cast<float *>(scratch + g.w);
+                float *sc_s = lg_s + (size_t)n16 * HQ;
+                if (h_kv == 8) score_prefetched<G, 8>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
+                else if (h_kv == 4) score_prefetched<G, 4>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
+                else if (h_kv == 2) score_prefetched<G, 2>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
+                else score_prefetched<G, 1>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
+                named_bar_sync(1, nthr);  // sm_stats reused by the next segment
+            } else {
+                const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;  // this CTA's units of sq
+                tb = (int)(ub - pb) * kTcTokens;
+                te = (int)(ue - pb) * kTcTokens;
+                if (te > L) te = L;
+                if (h_kv == 8)
+                    score_segment<G, 8>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
+                                        abort_flag, sm_stats, tid, nthr);
+                else if (h_kv == 4)
+                    score_segment<G, 4>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
+                                        abort_flag, sm_stats, tid, nthr);
+                else if (h_kv == 2)
+                    score_segment<G, 2>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
+                                        abort_flag, sm_stats, tid, nthr);
+                else
+                    score_segment<G, 1>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
+                                        abort_flag, sm_stats, tid, nthr);
+            }
+        }
+        if (abort_flag[0]) break;
+    }
+    if (nseg > 0 && !waited_copies && tid == 0) mbar_wait_bounded(ebar, 0, a.err, abort_flag, 62);
+    if (merger) {  // the outputs of the merged sequences, off the other CTAs' path
+        named_bar_sync(1, nthr);
+        merge_stats(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
+        named_bar_sync(1, nthr);
+        merge_outputs<D>(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
+    }
+    if (tid == 0) bulk_wait_read_all();  // shared-memory sources read; the writes complete on their own
 }
 
 // ===========================================================================
@@ -1156,9 +1712,9 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
         p->ncw = h_kv;
         p->threads = (h_kv + 1) * 32;
         int stages = 4;
-        while (stages > 2 && make_tc_layout(stages, h_kv, d / 64, B).total > dev.smem_optin) --stages;
+        while (stages > 2 && make_tc_layout(stages, h_kv, d / 64, B, p->grid).total > dev.smem_optin) --stages;
         p->stages = stages;
-        p->smem = make_tc_layout(stages, h_kv, d / 64, B).total;
+        p->smem = make_tc_layout(stages, h_kv, d / 64, B, p->grid).total;
     } else {
         if (!(G == 4 || G == 8)) return fail(ZP_ERR_SHAPE, "decode: group size %d not in {4,8}", G);
         if (!(h_kv == 2 || h_kv == 4 || h_kv == 8 || h_kv == 16))
@@ -1186,8 +1742,8 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
     const long long units_cap = (long long)B * table_stride * (b / p->T);
     p->logits_units = units_cap;
     size_t off = 0;
-    p->off_count = off;
-    off = align_up(off + (size_t)B * 4, 256);
+    p->off_count = off;  // per-sequence arrival counters (tensor-core path)
+    off = align_up(off + (size_t)B * 8, 256);
     p->off_prefix = off;
     off = align_up(off + (size_t)(B + 1) * 4, 256);
     p->off_stats = off;
@@ -1217,10 +1773,13 @@ zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, c
     }
     if ((reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) % 16)
         return fail(ZP_ERR_INVALID_ARG, "decode: caches must be 16-byte aligned");
-    kmain<<<p.grid, p.threads, p.smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    // cooperative: CTAs wait (bounded) for the merges of other CTAs
+    DecodeArgs args = a;
+    void *params[] = {&args};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kmain), dim3(p.grid), dim3(p.threads), params,
+                                    (size_t)p.smem, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode: tensor-core kernel launch");
-    return launch_finish<__nv_bfloat16, Dd, G>(a, p.grid, p.logits_units, st);
+    return ok();  // merges and the window score run inside the kernel
 }
 
 template <typename T, int Dd, int G>
@@ -1267,6 +1826,8 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     if (table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "decode: table_stride < 1");
     if (score_accum && (window < 1 || window > D->block_size))
         return fail(ZP_ERR_INVALID_ARG, "decode: window %d outside [1, b=%d]", window, D->block_size);
+    if (reinterpret_cast<uintptr_t>(score_accum) % 16)
+        return fail(ZP_ERR_INVALID_ARG, "decode: score_accum must be 16-byte aligned");
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
@@ -1306,6 +1867,7 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.unit_prefix = reinterpret_cast<int *>(ws + p.off_prefix);
     a.unit_info = reinterpret_cast<int4 *>(ws + p.off_info);
     a.logits_units = p.logits_units;
+    a.ctl = reinterpret_cast<unsigned long long *>(ws + p.off_count);
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = D->h_q / D->h_kv;

@@ -145,6 +145,50 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, unsign
         : "memory");
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 4-byte global store with an L2 cache-policy hint.
+__device__ __forceinline__ void st_global_hint(float *p, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy) : "memory");
+}
+
+// Asynchronous prefetch of [src, src + bytes) into L2 (bytes and src multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Global -> shared 1-D bulk copy completing on `bar`, default L2 policy.
+__device__ __forceinline__ void bulk_g2s_plain(void *dst_smem, const void *src, unsigned bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared -> global 1-D bulk copy (bulk-group completion; bytes and both
+// addresses multiples of 16).  Before it, fence_proxy_async_smem() makes the
+// CTA's ordinary shared-memory writes visible to the copy engine.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of all committed groups have been read
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// all committed groups have completed (writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 3-D tiled TMA load (tensor map in param/const/global space) completing on
 // `bar`, with an L2 cache-policy hint.  c0 is the innermost coordinate.
 __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, int c0, int c1, int c2,

@@ -103,7 +103,7 @@ size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table
  *     out[s][h] = sum_{t<L} softmax_t(q[s][h] . k_t / sqrt(d)) v_t
  * q, out: [B][h_q][d] (dtype); k_cache, v_cache: one layer, paged.
  *
- * score_accum (nullable, float [B][h_kv][table_stride*b]): the attention
+ * score_accum (nullable, float [B][h_kv][table_stride*b], 16-byte aligned): the attention
  * score S of each sequence, one row per kv head indexed by token position
  * (row s belongs to batch entry s, as block-table row s does).  When set,
  * sequences whose query position P = L-1 lies in the observation window of
