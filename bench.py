@@ -11,9 +11,9 @@ One step = the whole hot path over that batch:
                            window-score accumulation (w = b = 16, so every
                            decode step is an observation-window step);
   3. compression of the sequences whose trigger holds at their length
-     (L % b == 0, L >= N_max * b): host planner, zp_score_tokens (global
-     score, first-compression pooling, lightning redundancy, eq. 4, window),
-     zp_select_topk, zp_compact_pages into the planned target blocks.
+     (L % b == 0, L >= N_max * b): host planner, then zp_compress_layer:
+     scores (global score, first-compression pooling, lightning redundancy,
+     eq. 4, window), keep sets and the move into the planned target blocks.
 The batch is stationary: lengths and tables are not advanced between steps,
 so every timed step does identical work (the compaction rewrites the same
 target slots each time).
@@ -190,7 +190,7 @@ class Workload:
             self.c_first = torch.ones(n, dtype=torch.uint8, device=dev)
             self.c_scores = torch.empty(n, h_kv, self.c_Lmax, dtype=torch.float32, device=dev)
             self.c_keep = torch.empty(n, h_kv, self.k, dtype=torch.int32, device=dev)
-            self.c_ws = torch.empty(max(zp.zp_score_workspace_size(self.desc, n, self.c_Lmax), 1),
+            self.c_ws = torch.empty(max(zp.zp_compress_workspace_size(self.desc, n, self.c_Lmax), 1),
                                     dtype=torch.uint8, device=dev)
             self.params = zp.score_params(window=self.w)
             self.c_tables_np = c.block_table[idx].numpy().copy()
@@ -232,8 +232,8 @@ class Workload:
         return tot
 
     def launches_per_step(self) -> int:
-        # append; decode (one cooperative kernel); scores x3, top-k, compact
-        return 1 + 1 + (5 if self.n_comp else 0)
+        # append; decode (one cooperative kernel); scores: global, redundancy, finish with selection and move
+        return 1 + 1 + (3 if self.n_comp else 0)
 
     # ---- the step
     def decode(self, stream=None):
@@ -256,15 +256,14 @@ class Workload:
         self.compress_device(stream)
 
     def compress_device(self, stream=None):
-        """The device part of the compression: scores, top-k, compaction."""
+        """The device part of the compression: scores, keep sets and moves of
+        the layer in one call."""
         if not self.n_comp:
             return
         zp = self.zp
-        zp.zp_score_tokens(self.desc, self.params, self.K, self.c_table, self.c_lens, self.c_first, self.S,
-                           self.F, self.c_scores, rows=self.c_rows, workspace=self.c_ws, stream=stream)
-        zp.zp_select_topk(self.c_scores, self.c_lens, self.k, self.c_keep, stream=stream)
-        zp.zp_compact_pages(self.desc, self.K, self.V, 0, 1, self.F, 0, self.c_table, self.c_targets,
-                            self.c_lens, self.c_keep, self.k, scores=self.S, rows=self.c_rows, stream=stream)
+        zp.zp_compress_layer(self.desc, self.params, self.K, self.V, self.c_table, self.c_lens, self.c_first,
+                             self.S, self.F, self.c_targets, self.k, self.c_keep, self.c_Lmax, rows=self.c_rows,
+                             workspace=self.c_ws, stream=stream)
 
     def step(self):
         self.decode()

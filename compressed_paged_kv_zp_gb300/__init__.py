@@ -31,6 +31,7 @@ EXPORTS = [
     "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
     "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
+    "zp_compress_workspace_size", "zp_compress_layer",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
 ]
@@ -106,6 +107,10 @@ def _load() -> ctypes.CDLL:
                                     I32, P, SZ, P]
     lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
     lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, P, I32, P, I32, P, P, I32, I32, P]
+    lib.zp_compress_workspace_size.restype = SZ
+    lib.zp_compress_workspace_size.argtypes = [D, I32, I32]
+    lib.zp_compress_layer.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, P, I32, P, P, I32, P, P, P, I32, I32,
+                                      P, P, P, I32, P, SZ, P]
     lib.zp_pool_create.restype = P
     lib.zp_pool_create.argtypes = [I32]
     lib.zp_pool_destroy.argtypes = [P]
@@ -261,6 +266,30 @@ def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, 
                                 _stream(stream)))
 
 
+def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int) -> int:
+    return int(lib.zp_compress_workspace_size(ctypes.byref(desc), int(n), int(Lmax)))
+
+
+def zp_compress_layer(desc, params: ScoreParams, k_cache, v_cache, block_table, seq_lens, first_compression,
+                      attn, global_F, dst_targets, k, keep_idx, Lmax, rows=None, tie_count=None, scores_out=None,
+                      workspace=None, stream=None) -> None:
+    """Scores, keep sets and moves of one layer (the three steps in one call).
+    attn: the attention-score rows (see zp_score_tokens); dst_targets int32
+    [n][target_stride]; keep_idx int32 [n][h_kv][k] (written)."""
+    n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    if workspace is None:
+        workspace = torch.empty(max(zp_compress_workspace_size(desc, n, Lmax), 1), dtype=torch.uint8,
+                                device=k_cache.device)
+    _check(lib.zp_compress_layer(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
+                                 _dev(v_cache, "v_cache"), _dev(block_table, "block_table"), table_stride,
+                                 _dev(seq_lens, "seq_lens"), _dev(first_compression, "first_compression"), n,
+                                 _score_rows(attn, rows), _dev(global_F, "global_F"),
+                                 _dev(dst_targets, "dst_targets"), int(dst_targets.shape[1]), int(k),
+                                 _dev(keep_idx, "keep_idx"), _dev(tie_count, "tie_count"),
+                                 _dev(scores_out, "scores_out"), int(Lmax), _dev(workspace, "workspace"),
+                                 workspace.numel(), _stream(stream)))
+
+
 def zp_device_status(clear: bool = True):
     code, detail = ctypes.c_int32(0), ctypes.c_int32(0)
     _check(lib.zp_device_status(ctypes.byref(code), ctypes.byref(detail), int(bool(clear))))
@@ -346,4 +375,5 @@ __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", 
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_window_score_workspace_size", "zp_window_score",
            "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
-           "zp_compact_pages", "zp_device_status", "Pool", "ZP_BF16", "ZP_F32"]
+           "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layer", "zp_device_status", "Pool",
+           "ZP_BF16", "ZP_F32"]

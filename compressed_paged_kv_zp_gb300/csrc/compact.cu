@@ -124,6 +124,121 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     }
 }
 
+// Main variant.  The CTA first resolves, in shared memory, every rank's keep
+// position, source block, F value and the target blocks (two rounds of
+// independent loads); then per chunk of up to kVChunk ranks every thread loads
+// its share of the chunk's row pieces (16-byte vectors, K then V of this kv
+// head) into registers, the CTA synchronises, and the pieces are stored to
+// the target slots.  A chunk reads positions >= its first rank and earlier
+// chunks write slots below it, and a slot shared by a source and a target has
+// the same index in both (the target rule): the move is correct in place.
+// (Many small bulk copies were measured slower: the copy engine keeps few
+// requests in flight per SM.)
+constexpr int kVChunk = 64;
+constexpr int kVThreads = 256;
+constexpr int kVPerThread = 8;  // 16-byte registers per thread and chunk (row pieces up to 256 B)
+
+// dynamic shared memory: pos[k], src block[k] (ints), F values[k], target blocks[ceil(k/b)]
+__host__ __device__ inline size_t compact_meta_smem(int k, int b) {
+    return (size_t)k * 12 + (size_t)((k + b - 1) / b) * 4 + 16;
+}
+
+__global__ void __launch_bounds__(kVThreads) compact_vec_kernel(const CompactArgs a) {
+    extern __shared__ __align__(16) unsigned char csm[];
+    __shared__ int s_L;
+    const int kvh = blockIdx.x;
+    const int s = blockIdx.y;
+    const int layer = blockIdx.z;
+    const int tid = threadIdx.x;
+    int *pos_s = reinterpret_cast<int *>(csm);
+    int *src_s = pos_s + a.k;
+    float *f_s = reinterpret_cast<float *>(src_s + a.k);
+    int *dst_s = reinterpret_cast<int *>(f_s + a.k);
+    const int32_t *kp = a.keep + (((size_t)layer * a.n + s) * a.h_kv + kvh) * a.k;
+    const uint4 *K = a.K + layer * a.layer_stride_vec;
+    const uint4 *V = a.V + layer * a.layer_stride_vec;
+    uint4 *Kw = a.K + layer * a.layer_stride_vec;
+    uint4 *Vw = a.V + layer * a.layer_stride_vec;
+    float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
+    const int nt = (a.k + a.b - 1) / a.b;
+    // ---- round 1: length, keep positions, target blocks (independent loads)
+    if (tid == 0) {
+        int L = a.seq_lens[s];
+        if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+        s_L = L;
+    }
+    for (int r = tid; r < a.k; r += blockDim.x) pos_s[r] = kp[r];
+    for (int t = tid; t < nt; t += blockDim.x) dst_s[t] = a.dst[(size_t)s * a.target_stride + t];
+    __syncthreads();
+    const float *Srow = nullptr;
+    int L = s_L;
+    if (F) {
+        const int row = a.S_rows ? a.S_rows[s] : s;
+        if (row < 0) {
+            if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x402);
+            F = nullptr;
+        } else {
+            Srow = a.S + layer * a.S_layer_stride + ((size_t)row * a.h_kv + kvh) * a.S_stride;
+            if (L > a.S_stride) L = (int)a.S_stride;
+        }
+    }
+    const int kk = min(a.k, L);
+    // ---- round 2: source blocks and F values of every rank
+    for (int r = tid; r < kk; r += blockDim.x) {
+        const int pos = pos_s[r];
+        int blk = -1;
+        if (pos >= 0 && pos < L) blk = a.src_table[(size_t)s * a.table_stride + pos / a.b];
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x400);
+            blk = -1;
+        }
+        src_s[r] = blk;
+        if (F) f_s[r] = (blk >= 0) ? Srow[pos] : 0.f;
+    }
+    __syncthreads();
+    const int per_rank = 2 * a.row_vec;  // K then V vectors
+    const int chunk = min(kVChunk, kVThreads * kVPerThread / per_rank);
+    for (int r0 = 0; r0 < kk; r0 += chunk) {
+        const int nr = min(chunk, kk - r0);
+        const int items = nr * per_rank;
+        uint4 buf[kVPerThread];
+#pragma unroll
+        for (int i = 0; i < kVPerThread; ++i) {
+            const int it = tid + i * kVThreads;
+            if (it < items) {
+                const int r = r0 + it / per_rank, v = it % per_rank;
+                const int blk = src_s[r];
+                if (blk >= 0) {
+                    const size_t row = ((size_t)blk * a.b + pos_s[r] % a.b) * a.h_kv + kvh;
+                    buf[i] = (v < a.row_vec ? K : V)[row * a.row_vec + (v % a.row_vec)];
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kVPerThread; ++i) {
+            const int it = tid + i * kVThreads;
+            if (it < items) {
+                const int r = r0 + it / per_rank, v = it % per_rank;
+                const int blk = dst_s[r / a.b];
+                if (blk < 0 || blk >= a.n_total) {
+                    record_error(a.err, ZP_ERR_DEVICE, 0x401);
+                } else if (src_s[r] >= 0) {
+                    const size_t row = ((size_t)blk * a.b + r % a.b) * a.h_kv + kvh;
+                    (v < a.row_vec ? Kw : Vw)[row * a.row_vec + (v % a.row_vec)] = buf[i];
+                }
+            }
+        }
+        if (F)
+            for (int i = tid; i < nr; i += blockDim.x) {
+                const int r = r0 + i;
+                const int blk = dst_s[r / a.b];
+                if (blk >= 0 && blk < a.n_total) F[((size_t)blk * a.b + r % a.b) * a.h_kv + kvh] = f_s[r];
+            }
+        __syncthreads();  // the next chunk's loads follow this chunk's stores
+    }
+}
+
 }  // namespace
 }  // namespace zp
 
@@ -187,7 +302,20 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     a.chunk = chunk;
     a.err = dev.error_word;
     dim3 grid(D->h_kv, n, layer_count);
-    compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    const int meta_smem = (int)compact_meta_smem(k, D->block_size);
+    if (2 * row_vec <= kVThreads * kVPerThread && meta_smem <= 96 * 1024) {
+        static int configured[64] = {0};
+        const int dv = dev.device < 64 ? dev.device : 63;
+        if (meta_smem > 48 * 1024 && configured[dv] < meta_smem) {
+            cudaError_t e = cudaFuncSetAttribute(compact_vec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 meta_smem);
+            if (e != cudaSuccess) return cuda_fail(e, "compact: cudaFuncSetAttribute");
+            configured[dv] = meta_smem;
+        }
+        compact_vec_kernel<<<grid, kVThreads, meta_smem, static_cast<cudaStream_t>(stream)>>>(a);
+    } else {
+        compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "compact: launch");
     return ok();

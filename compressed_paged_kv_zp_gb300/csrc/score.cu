@@ -18,7 +18,7 @@
 //      lambda * R (eq. 4), last w tokens -> +inf (§4.2, App. C.6).
 #include <math.h>
 
-#include "zp_common.cuh"
+#include "select.cuh"
 
 namespace zp {
 namespace {
@@ -322,6 +322,139 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
     }
 }
 
+// Redundancy and global score of one 16-token block in one CTA (bf16 keys,
+// b = 16, the path zp_compress_layer takes).  grid (ceil(Lmax / 16), n), one
+// warp per kv head.  The block's token rows (all kv heads, contiguous in HBM)
+// come by one bulk copy each into shared memory rows padded by 16 bytes, so
+// the eight rows an ldmatrix reads fall on eight bank groups; while they are
+// in flight, the CTA computes the block's global score (Alg. 2, as
+// gather_global_kernel) from the score rows and F.  Then G = K K^T per head
+// on the tensor cores (16 mma.sync), and on the accumulator fragments the
+// lightning rule as in lightning_tc_kernel.
+template <int D>
+__global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a) {
+    extern __shared__ __align__(128) unsigned char gsm[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_blk, s_abort;
+    __shared__ float nrm[16][16];
+    const int s = blockIdx.y;
+    const int bi = blockIdx.x;
+    const int L = clamp_len(a, s);
+    const int tb0 = bi * 16;
+    if (tb0 >= L) return;
+    const int nvalid = min(16, L - tb0);
+    const int h_kv = a.h_kv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned row_bytes = (unsigned)(h_kv * D * 2);
+    const int RS = (int)row_bytes + 16;
+    if (tid == 0) {
+        const int blk = a.table[(size_t)s * a.table_stride + bi];
+        s_blk = blk;
+        s_abort = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        } else {
+            mbar_arrive_expect_tx(&bar, row_bytes * (unsigned)nvalid);
+            const char *src = static_cast<const char *>(a.k) + (size_t)blk * 16 * row_bytes;
+            for (int t = 0; t < nvalid; ++t) bulk_g2s_plain(gsm + t * RS, src + (size_t)t * row_bytes, row_bytes, &bar);
+        }
+    }
+    __syncthreads();
+    const int blk = s_blk;
+    if (blk < 0 || blk >= a.n_total) return;
+    // ---- global score of the block's tokens (while the rows are in flight)
+    {
+        const int N = (L + a.b - 1) / a.b;
+        const bool first = a.first ? a.first[s] != 0 : true;
+        const bool read_F = a.use_global && !first && bi != N - 1;
+        const int row = a.S_rows ? a.S_rows[s] : s;
+        for (int it = tid; it < nvalid * h_kv; it += blockDim.x) {
+            const int kvh = it / nvalid, tl = it % nvalid;
+            const int t = tb0 + tl;
+            if (row < 0) {
+                record_error(a.err, ZP_ERR_DEVICE, 0x202);
+                continue;
+            }
+            float *sp = a.S + ((size_t)row * h_kv + kvh) * a.S_stride + t;
+            float v = *sp;
+            if (read_F) {
+                v = fmaxf(a.alpha * a.F[((size_t)blk * a.b + tl) * h_kv + kvh], v);
+                *sp = v;
+            }
+            a.X[((size_t)s * h_kv + kvh) * a.Lmax + t] = v;
+        }
+    }
+    mbar_wait_bounded(&bar, 0, a.err, &s_abort, 0x203);
+    __syncthreads();
+    if (s_abort || warp >= h_kv) return;
+    constexpr int KS = D / 16;
+    const int kvh = warp;
+    const int g = lane >> 2, tig = lane & 3;
+    const int lm = lane >> 3;
+    const int lrow = (lm & 1) * 8 + (lane & 7);  // matrices: (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
+    const int lchunk = lm >> 1;
+    const uint32_t base = smem_u32(gsm) + (uint32_t)(lrow * RS + kvh * D * 2);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(base + (uint32_t)((2 * t + lchunk) * 16), r0, r1, r2, r3);
+        mma_16816(c0, r0, r1, r2, r3, r0, r2);
+        mma_16816(c1, r0, r1, r2, r3, r1, r3);
+    }
+    // rows >= nvalid were not copied: every entry they touch is masked below
+    float *myn = nrm[warp];
+    if (tig == (g >> 1)) myn[g] = c0[g & 1];
+    if (tig == (g >> 1)) myn[g + 8] = c1[2 + (g & 1)];
+    __syncwarp();
+    const int rows[2] = {g, g + 8};
+    const int cols[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
+    float v[2][4];
+    v[0][0] = c0[0]; v[0][1] = c0[1]; v[0][2] = c1[0]; v[0][3] = c1[1];
+    v[1][0] = c0[2]; v[1][1] = c0[3]; v[1][2] = c1[2]; v[1][3] = c1[3];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+        const bool rv = rows[ri] < nvalid;
+        const float nr = rv ? sqrtf(fmaxf(myn[rows[ri]], 0.f)) : 0.f;
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+            const bool cv = cols[ci] < nvalid;
+            const float nc = cv ? sqrtf(fmaxf(myn[cols[ci]], 0.f)) : 0.f;
+            const bool ok = rv && cv && rows[ri] != cols[ci] && nr > 0.f && nc > 0.f;
+            v[ri][ci] = ok ? v[ri][ci] / (nr * nc) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        const unsigned blo = __ballot_sync(0xFFFFFFFFu, v[0][ci] > a.p);
+        const unsigned bhi = __ballot_sync(0xFFFFFFFFu, v[1][ci] > a.p);
+        unsigned mlo = 0, mhi = 0;
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg) {
+            mlo |= ((blo >> (tig + 4 * gg)) & 1u) << gg;
+            mhi |= ((bhi >> (tig + 4 * gg)) & 1u) << gg;
+        }
+        int rstar = -1;
+        if (mhi) rstar = 8 + (31 - __clz(mhi));
+        else if (mlo) rstar = 31 - __clz(mlo);
+        if (rstar == rows[0]) v[0][ci] = 0.f;
+        if (rstar == rows[1]) v[1][ci] = 0.f;
+    }
+    float rs0 = v[0][0] + v[0][1] + v[0][2] + v[0][3];
+    float rs1 = v[1][0] + v[1][1] + v[1][2] + v[1][3];
+    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 1);
+    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 2);
+    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 1);
+    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 2);
+    if (tig == 0) {
+        float *out = a.rho + ((size_t)s * h_kv + kvh) * a.Lmax + tb0;
+        if (g < nvalid) out[g] = rs0;
+        if (g + 8 < nvalid) out[g + 8] = rs1;
+    }
+}
+
 // grid (h_kv, n), 1024 threads
 __global__ void finalize_kernel(const ScoreArgs a) {
     __shared__ float red[32];
@@ -381,6 +514,176 @@ __global__ void finalize_kernel(const ScoreArgs a) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Fused finish of one layer's compression (zp_compress_layer): per (sequence,
+// kv head) one CTA takes the global score X and the row sums rho into shared
+// memory, finalises the scores there (as finalize_kernel), selects the keep
+// set (block_select_topk) and moves this kv head's kept rows of K and V into
+// the target blocks, F of each target slot receiving the kept token's global
+// score (as the compaction).  The keep set never leaves the CTA before the
+// move (it is also written out).
+struct MoveArgs {
+    uint4 *K, *V;
+    int row_vec;         // 16-byte vectors per (token, kv head) row
+    const int32_t *dst;  // [n][target_stride]
+    int target_stride;
+    int k;
+    int32_t *keep;       // [n][h_kv][k]
+    int32_t *tie;        // nullable [n][h_kv]
+    float *F;            // nullable, paged
+};
+
+constexpr int kFsThreads = 512;
+constexpr int kFsChunk = 128;      // ranks per move round
+constexpr int kFsVecPerThread = 8; // 16-byte registers per thread and round (row pieces up to 256 B)
+
+__host__ __device__ inline size_t fused_smem(int Lmax, int k, int b) {
+    return (size_t)Lmax * 8 + (size_t)k * 12 + (size_t)((k + b - 1) / b) * 4 + 64;
+}
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int o = 16; o; o >>= 1) {
+        const float y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = is_max ? fmaxf(v, y) : v + y;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = is_max ? -INFINITY : 0.f;
+    for (int w = 0; w < nw; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
+    return t;
+}
+
+__global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a, const MoveArgs m) {
+    extern __shared__ __align__(16) unsigned char fsm[];
+    __shared__ SelectShared sh;
+    __shared__ float red[32];
+    const int kvh = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
+    const int L = clamp_len(a, s);
+    float *xs = reinterpret_cast<float *>(fsm);
+    float *fs = xs + a.Lmax;
+    int *keep_s = reinterpret_cast<int *>(fs + a.Lmax);
+    int *src_s = keep_s + m.k;
+    float *fv_s = reinterpret_cast<float *>(src_s + m.k);
+    int *dst_s = reinterpret_cast<int *>(fv_s + m.k);
+    const int nt = (m.k + a.b - 1) / a.b;
+    for (int t = tid; t < nt; t += nthr) dst_s[t] = m.dst[(size_t)s * m.target_stride + t];
+    const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
+    for (int t = tid; t < L; t += nthr) {
+        xs[t] = a.X[row + t];
+        fs[t] = a.use_sim ? a.rho[row + t] : 0.f;
+    }
+    __syncthreads();
+    // ---- final scores (App. C.4-C.8, eq. 4, window), in place of rho
+    const bool first = a.first ? a.first[s] != 0 : true;
+    const bool pool = a.pool_kernel > 1 && (a.pool_policy == 2 || (a.pool_policy == 1 && first));
+    const int r = a.pool_kernel / 2;
+    const float inv = 1.f / ((float)L * a.tau);
+    float rmax = 0.f, rsum = 1.f;
+    if (a.use_sim && L > 0) {
+        float mx = -INFINITY;
+        for (int t = tid; t < L; t += nthr) mx = fmaxf(mx, fs[t] * inv);
+        rmax = block_reduce(mx, true, red);
+        float sm = 0.f;
+        for (int t = tid; t < L; t += nthr) sm += expf(fs[t] * inv - rmax);
+        rsum = block_reduce(sm, false, red);
+    }
+    for (int t = tid; t < L; t += nthr) {
+        float v;
+        if (pool) {
+            const int lo = max(0, t - r), hi = min(L - 1, t + r);
+            v = xs[lo];
+            for (int j = lo + 1; j <= hi; ++j) v = fmaxf(v, xs[j]);
+        } else {
+            v = xs[t];
+        }
+        if (a.use_sim) v -= a.lambda * (expf(fs[t] * inv - rmax) / rsum);
+        if (t >= L - a.window) v = INFINITY;
+        fs[t] = v;
+        if (a.out) a.out[row + t] = v;
+    }
+    __syncthreads();
+    // ---- keep set
+    int32_t *kout = m.keep + ((size_t)s * a.h_kv + kvh) * m.k;
+    if (L <= m.k) {
+        for (int i = tid; i < m.k; i += nthr) {
+            keep_s[i] = i < L ? i : -1;
+            kout[i] = i < L ? i : -1;
+        }
+        if (m.tie && tid == 0) m.tie[(size_t)s * a.h_kv + kvh] = 0;
+        __syncthreads();
+    } else {
+        block_select_topk(fs, L, m.k, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
+    }
+    // ---- move this kv head's kept rows (Alg. 4 with the target blocks)
+    const int kk = min(m.k, L);
+    const float *Srow = nullptr;
+    float *F = m.F;
+    if (F) {
+        const int rs = a.S_rows ? a.S_rows[s] : s;
+        if (rs < 0) {
+            if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x402);
+            F = nullptr;
+        } else {
+            Srow = a.S + ((size_t)rs * a.h_kv + kvh) * a.S_stride;
+        }
+    }
+    for (int i = tid; i < kk; i += nthr) {
+        const int pos = keep_s[i];
+        int blk = -1;
+        if (pos >= 0 && pos < L) blk = a.table[(size_t)s * a.table_stride + pos / a.b];
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x400);
+            blk = -1;
+        }
+        src_s[i] = blk;
+        if (F) fv_s[i] = blk >= 0 ? Srow[pos] : 0.f;
+    }
+    __syncthreads();
+    const int per_rank = 2 * m.row_vec;
+    const int chunk = min(kFsChunk, kFsThreads * kFsVecPerThread / per_rank);
+    for (int r0 = 0; r0 < kk; r0 += chunk) {
+        const int nr = min(chunk, kk - r0);
+        const int items = nr * per_rank;
+        uint4 buf[kFsVecPerThread];
+#pragma unroll
+        for (int i = 0; i < kFsVecPerThread; ++i) {
+            const int it = tid + i * kFsThreads;
+            if (it < items) {
+                const int rr = r0 + it / per_rank, v = it % per_rank;
+                const int blk = src_s[rr];
+                if (blk >= 0) {
+                    const size_t rw = ((size_t)blk * a.b + keep_s[rr] % a.b) * a.h_kv + kvh;
+                    buf[i] = (v < m.row_vec ? m.K : m.V)[rw * m.row_vec + (v % m.row_vec)];
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kFsVecPerThread; ++i) {
+            const int it = tid + i * kFsThreads;
+            if (it < items) {
+                const int rr = r0 + it / per_rank, v = it % per_rank;
+                const int blk = dst_s[rr / a.b];
+                if (blk < 0 || blk >= a.n_total) {
+                    record_error(a.err, ZP_ERR_DEVICE, 0x401);
+                } else if (src_s[rr] >= 0) {
+                    const size_t rw = ((size_t)blk * a.b + rr % a.b) * a.h_kv + kvh;
+                    (v < m.row_vec ? m.K : m.V)[rw * m.row_vec + (v % m.row_vec)] = buf[i];
+                }
+            }
+        }
+        if (F)
+            for (int i = tid; i < nr; i += nthr) {
+                const int rr = r0 + i;
+                const int blk = dst_s[rr / a.b];
+                if (blk >= 0 && blk < a.n_total) F[((size_t)blk * a.b + rr % a.b) * a.h_kv + kvh] = fv_s[rr];
+            }
+        __syncthreads();  // the next round's loads follow this round's stores
+    }
+}
 }  // namespace
 }  // namespace zp
 
@@ -391,20 +694,22 @@ extern "C" size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int
     return 2 * align_up((size_t)n * D->h_kv * Lmax * 4, 256);
 }
 
-extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
-                                     const void *k_cache, const int32_t *block_table,
-                                     int32_t table_stride, const int32_t *seq_lens,
-                                     const uint8_t *first_compression, int32_t n,
-                                     const zp_score_rows *attn, const float *global_F,
-                                     float *scores_out,
-                                     int32_t Lmax, void *workspace, size_t workspace_bytes,
-                                     void *stream) {
+// Validates the scoring arguments, fills `a` and launches the global-score and
+// redundancy kernels (X and rho in the workspace); the caller launches the
+// finish.  *launched = false when there is nothing to do (n or Lmax zero).
+static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P, const void *k_cache,
+                               const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
+                               const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
+                               const float *global_F, float *scores_out, int32_t Lmax, void *workspace,
+                               size_t workspace_bytes, cudaStream_t st, ScoreArgs &a, DeviceInfo &dev,
+                               bool *launched) {
+    *launched = false;
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (!P) return fail(ZP_ERR_INVALID_ARG, "score: NULL params");
     if (n < 0 || Lmax < 0 || table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: bad sizes");
     if (n == 0 || Lmax == 0) return ok();
-    if (!block_table || !seq_lens || !scores_out || !workspace)
+    if (!block_table || !seq_lens || !workspace)
         return fail(ZP_ERR_INVALID_ARG, "score: NULL buffer");
     if (!attn || !attn->data) return fail(ZP_ERR_INVALID_ARG, "score: NULL attention-score rows");
     if (attn->stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: score row stride %lld", (long long)attn->stride);
@@ -422,10 +727,8 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
         return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
     const size_t need = zp_score_workspace_size(D, n, Lmax);
     if (workspace_bytes < need) return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
-    DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
-    ScoreArgs a;
     a.table = block_table;
     a.table_stride = table_stride;
     a.seq_lens = seq_lens;
@@ -455,7 +758,27 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     a.tau = P->tau;
     a.window = P->window;
     a.err = dev.error_word;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (a.use_sim && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) && a.h_kv <= 16 &&
+        reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
+        // global score and redundancy of each block in one kernel
+        const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
+        dim3 g2((Lmax + 15) / 16, n);
+        if (a.d == 128) {
+            if (smem > 48 * 1024)
+                cudaFuncSetAttribute(global_lightning_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
+            global_lightning_kernel<128><<<g2, a.h_kv * 32, smem, st>>>(a);
+        } else {
+            if (smem > 48 * 1024)
+                cudaFuncSetAttribute(global_lightning_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem);
+            global_lightning_kernel<64><<<g2, a.h_kv * 32, smem, st>>>(a);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "score: global/lightning launch");
+        *launched = true;
+        return ok();
+    }
     dim3 g1((Lmax + kTile - 1) / kTile, n);
     gather_global_kernel<<<g1, 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
@@ -489,9 +812,102 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "score: lightning launch");
     }
+    *launched = true;
+    return ok();
+}
+
+extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
+                                     const void *k_cache, const int32_t *block_table,
+                                     int32_t table_stride, const int32_t *seq_lens,
+                                     const uint8_t *first_compression, int32_t n,
+                                     const zp_score_rows *attn, const float *global_F,
+                                     float *scores_out,
+                                     int32_t Lmax, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+    if (!scores_out && n > 0 && Lmax > 0) return fail(ZP_ERR_INVALID_ARG, "score: NULL scores_out");
+    ScoreArgs a;
+    DeviceInfo dev;
+    bool launched;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    zp_status rc = launch_scores(D, P, k_cache, block_table, table_stride, seq_lens, first_compression, n, attn,
+                                 global_F, scores_out, Lmax, workspace, workspace_bytes, st, a, dev, &launched);
+    if (rc != ZP_OK || !launched) return rc;
     dim3 g3(a.h_kv, n);
     finalize_kernel<<<g3, 1024, 0, st>>>(a);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score: finalize launch");
     return ok();
+}
+
+extern "C" size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax) {
+    return zp_score_workspace_size(D, n, Lmax);
+}
+
+extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base, int64_t layer_stride,
+                                      int32_t layer_count, float *global_F, int64_t F_layer_stride,
+                                      const zp_score_rows *scores, const int32_t *src_table,
+                                      int32_t table_stride, const int32_t *dst_targets, int32_t target_stride,
+                                      const int32_t *seq_lens, const int32_t *keep_idx, int32_t k, int32_t n,
+                                      void *stream);
+extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const int32_t *seq_lens,
+                                    int32_t n, int32_t k, int32_t *keep_idx, int32_t *tie_count, void *stream);
+
+extern "C" zp_status zp_compress_layer(const zp_cache_desc *D, const zp_score_params *P, void *k_cache,
+                                       void *v_cache, const int32_t *block_table, int32_t table_stride,
+                                       const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
+                                       const zp_score_rows *attn, float *global_F, const int32_t *dst_targets,
+                                       int32_t target_stride, int32_t k, int32_t *keep_idx, int32_t *tie_count,
+                                       float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    zp_status rc = check_desc(D);
+    if (rc != ZP_OK) return rc;
+    if (n < 0 || k < 0 || Lmax < 0 || target_stride < 1) return fail(ZP_ERR_INVALID_ARG, "compress: bad sizes");
+    if (n == 0 || k == 0) return ok();
+    if (!k_cache || !v_cache || !dst_targets || !keep_idx) return fail(ZP_ERR_INVALID_ARG, "compress: NULL buffer");
+    if ((long long)target_stride * D->block_size < k)
+        return fail(ZP_ERR_CAPACITY, "compress: %d target blocks hold fewer than k=%d rows", target_stride, k);
+    const int es = elem_bytes(D->dtype);
+    const size_t row_bytes = (size_t)D->head_dim * es;
+    if (row_bytes % 16) return fail(ZP_ERR_SHAPE, "compress: row of %zu bytes", row_bytes);
+    if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16) return fail(ZP_ERR_INVALID_ARG, "compress: unaligned cache");
+    ScoreArgs a;
+    DeviceInfo dev;
+    bool launched;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = launch_scores(D, P, k_cache, block_table, table_stride, seq_lens, first_compression, n, attn, global_F,
+                       scores_out, Lmax, workspace, workspace_bytes, st, a, dev, &launched);
+    if (rc != ZP_OK || !launched) return rc;
+    const int row_vec = (int)(row_bytes / 16);
+    const size_t smem = fused_smem(Lmax, k, D->block_size);
+    if (2 * row_vec <= kFsThreads * kFsVecPerThread && smem <= (size_t)dev.smem_optin) {
+        MoveArgs m;
+        m.K = static_cast<uint4 *>(k_cache);
+        m.V = static_cast<uint4 *>(v_cache);
+        m.row_vec = row_vec;
+        m.dst = dst_targets;
+        m.target_stride = target_stride;
+        m.k = k;
+        m.keep = keep_idx;
+        m.tie = tie_count;
+        m.F = global_F;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(finalize_select_move_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return cuda_fail(e, "compress: cudaFuncSetAttribute");
+        }
+        finalize_select_move_kernel<<<dim3(a.h_kv, n), kFsThreads, smem, st>>>(a, m);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "compress: launch");
+        return ok();
+    }
+    // rows too long for shared memory: the three separate steps (scores land in
+    // scores_out, else in place of the row sums)
+    if (!a.out) a.out = a.rho;
+    finalize_kernel<<<dim3(a.h_kv, n), 1024, 0, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "compress: finalize launch");
+    rc = zp_select_topk(a.out, a.h_kv, Lmax, seq_lens, n, k, keep_idx, tie_count, stream);
+    if (rc != ZP_OK) return rc;
+    return zp_compact_pages(D, k_cache, v_cache, 0, 1, global_F, 0, attn, block_table, table_stride, dst_targets,
+                            target_stride, seq_lens, keep_idx, k, n, stream);
 }

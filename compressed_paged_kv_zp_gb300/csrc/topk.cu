@@ -10,32 +10,14 @@
 // writes the kept positions in ascending order, the order Alg. 4 preserves.
 #include <math.h>
 
-#include "zp_common.cuh"
+#include "select.cuh"
 
 namespace zp {
 namespace {
 
 constexpr int kThreads = 1024;
-
-__device__ __forceinline__ unsigned long long make_key(float f, int t) {
-    unsigned u = __float_as_uint(f);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return ((unsigned long long)u << 32) | (unsigned)t;
-}
-
-__device__ __forceinline__ int block_sum(int v, int *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    int tot = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-    return tot;
-}
-
-// Scores are staged in shared memory when the row fits (kSmemRow floats),
-// so the radix passes never go back to global memory.
+// Scores are staged in shared memory when the row fits (kSmemRow floats), so
+// the radix passes never go back to global memory.
 constexpr int kSmemRow = 32768;
 
 template <bool STAGED>
@@ -43,11 +25,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
                                                         const int32_t *seq_lens, int k, int32_t *keep,
                                                         int32_t *tie_count, unsigned *err) {
     extern __shared__ float srow[];
-    __shared__ int hist[256];
-    __shared__ int red[32];
-    __shared__ int scan[kThreads];
-    __shared__ unsigned long long s_prefix;
-    __shared__ int s_shift, s_need, s_done;
+    __shared__ SelectShared sh;
     const int kvh = blockIdx.x;
     const int s = blockIdx.y;
     const int tid = threadIdx.x;
@@ -56,138 +34,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
     if (L > Lmax) L = Lmax;
     const float *sc = scores + ((size_t)s * h_kv + kvh) * Lmax;
     int32_t *out = keep + ((size_t)s * h_kv + kvh) * k;
-    if constexpr (STAGED) {
-        if (L > k) {
-            for (int t = tid; t < L; t += blockDim.x) srow[t] = sc[t];
-            __syncthreads();
-            sc = srow;
-        }
-    }
     if (L <= k) {
         for (int r = tid; r < k; r += blockDim.x) out[r] = r < L ? r : -1;
         if (tie_count && tid == 0) tie_count[(size_t)s * h_kv + kvh] = 0;
         return;
     }
-    if (tid == 0) {
-        s_prefix = 0;
-        s_shift = 64;
-        s_need = k;
-        s_done = 0;
-    }
-    for (int pass = 7; pass >= 0; --pass) {
+    if constexpr (STAGED) {
+        for (int t = tid; t < L; t += blockDim.x) srow[t] = sc[t];
         __syncthreads();
-        if (s_done) break;
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
-        const int shift = pass * 8;
-        const unsigned long long pre = s_prefix;
-        const int pshift = s_shift;
-        for (int t = tid; t < L; t += blockDim.x) {
-            const float f = sc[t];
-            if (f != f) record_error(err, ZP_ERR_DEVICE, 0x300);
-            const unsigned long long key = make_key(f, t);
-            if (pshift == 64 || (key >> pshift) == pre) atomicAdd(&hist[(key >> shift) & 255], 1);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // warp 0: lane l owns bins 8l..8l+7; a suffix scan over the lanes
-            // finds the bin where the count from the top reaches `need`
-            const int need = s_need;
-            int h8[8], tot = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                h8[j] = hist[8 * tid + j];
-                tot += h8[j];
-            }
-            int incl = tot;  // bins of lanes >= this one
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-                if (tid + o < 32) incl += y;
-            }
-            const int above = incl - tot;
-            if (above < need && need <= incl) {
-                int cum = above, bin = 8 * tid;
-                for (int j = 7; j >= 0; --j) {
-                    if (cum + h8[j] >= need) {
-                        bin = 8 * tid + j;
-                        break;
-                    }
-                    cum += h8[j];
-                }
-                const int rem = need - cum;
-                s_prefix = (pshift == 64 ? 0ull : (pre << 8)) | (unsigned long long)bin;
-                s_shift = shift;
-                s_need = rem;
-                if (hist[bin] == rem) s_done = 1;
-            }
-        }
+        sc = srow;
     }
-    __syncthreads();
-    const unsigned long long thr = s_prefix;
-    const int tsh = s_shift;
-    // keep iff key's top (64 - tsh) bits >= thr; write ascending positions
-    const int chunk = (L + blockDim.x - 1) / blockDim.x;
-    const int beg = tid * chunk;
-    const int end = min(L, beg + chunk);
-    int cnt = 0;
-    for (int t = beg; t < end; ++t) cnt += (make_key(sc[t], t) >> tsh) >= thr;
-    // exclusive block scan of cnt: warp shuffles, then the 32 warp totals
-    const int lane = tid & 31, wid = tid >> 5;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) scan[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-        const int nw = blockDim.x >> 5;
-        int w = lane < nw ? scan[lane] : 0;
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-            if (lane >= o) wi += y;
-        }
-        if (lane < nw) scan[32 + lane] = wi - w;  // exclusive warp offsets
-        if (lane == nw - 1) scan[64] = wi;        // total
-    }
-    __syncthreads();
-    int pos = scan[32 + wid] + incl - cnt;
-    const int total = scan[64];
-    if (total != k && tid == 0) record_error(err, ZP_ERR_DEVICE, 0x301);
-    float kept_min = INFINITY;
-    for (int t = beg; t < end; ++t) {
-        const float f = sc[t];
-        if ((make_key(f, t) >> tsh) >= thr) {
-            if (pos < k) out[pos] = t;
-            ++pos;
-            kept_min = fminf(kept_min, f);
-        }
-    }
-    if (tie_count) {
-        // score of the lowest kept token; ties split between kept and dropped?
-        for (int o = 16; o; o >>= 1) kept_min = fminf(kept_min, __shfl_xor_sync(0xFFFFFFFFu, kept_min, o));
-        __shared__ float s_min[32];
-        __syncthreads();
-        if ((tid & 31) == 0) s_min[tid >> 5] = kept_min;
-        __syncthreads();
-        float mk = INFINITY;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mk = fminf(mk, s_min[w]);
-        int eq_kept = 0, eq_drop = 0;
-        for (int t = tid; t < L; t += blockDim.x) {
-            const float f = sc[t];
-            if (f == mk) {
-                if ((make_key(f, t) >> tsh) >= thr) ++eq_kept;
-                else ++eq_drop;
-            }
-        }
-        const int a = block_sum(eq_kept, red);
-        const int b2 = block_sum(eq_drop, red);
-        if (tid == 0) tie_count[(size_t)s * h_kv + kvh] = b2 > 0 ? a + b2 : 0;
-    }
+    block_select_topk(sc, L, k, out, nullptr, tie_count ? tie_count + (size_t)s * h_kv + kvh : nullptr, err, sh);
 }
 
 }  // namespace

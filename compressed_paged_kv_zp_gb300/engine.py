@@ -20,9 +20,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compact_pages,
-               zp_decode_workspace_size, zp_paged_decode_attn, zp_score_tokens,
-               zp_score_workspace_size, zp_select_topk)
+from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layer, zp_compress_workspace_size,
+               zp_decode_workspace_size, zp_paged_decode_attn)
 
 
 class DecodeLoop:
@@ -86,9 +85,9 @@ class DecodeLoop:
         self.ws = torch.empty(zp_decode_workspace_size(self.desc, B, self.stride), dtype=torch.uint8,
                               device=self.dev)
         Lmax = self.stride * self.b
-        self.score_ws = torch.empty(max(zp_score_workspace_size(self.desc, B, Lmax), 1), dtype=torch.uint8,
+        self.Lmax = Lmax
+        self.score_ws = torch.empty(max(zp_compress_workspace_size(self.desc, B, Lmax), 1), dtype=torch.uint8,
                                     device=self.dev)
-        self.scores = torch.empty(B, self.h_kv, Lmax, dtype=torch.float32, device=self.dev)
         self.out = torch.zeros(self.layers, B, self.h_q, self.d, dtype=self.dtype, device=self.dev)
 
     def layer_stride(self):
@@ -139,15 +138,11 @@ class DecodeLoop:
         ready.record(main)
         with torch.cuda.stream(self.side):
             self.side.wait_event(ready)
-            scores = self.scores[:n]
             keep = torch.empty(self.layers, n, self.h_kv, self.k, dtype=torch.int32, device=self.dev)
-            for l in range(self.layers):
-                zp_score_tokens(self.desc, self.params, self.K[l], tables_dev, lens_dev, first_dev, self.S[l],
-                                self.F[l], scores, rows=rows_dev, workspace=self.score_ws)
-                zp_select_topk(scores, lens_dev, self.k, keep[l])
-            zp_compact_pages(self.desc, self.K, self.V, self.layer_stride(), self.layers, self.F,
-                             self.n_total * self.b * self.h_kv, tables_dev, targets_dev, lens_dev, keep, self.k,
-                             scores=self.S, rows=rows_dev)
+            for l in range(self.layers):  # scores, keep sets and moves of one layer per call
+                zp_compress_layer(self.desc, self.params, self.K[l], self.V[l], tables_dev, lens_dev, first_dev,
+                                  self.S[l], self.F[l], targets_dev, self.k, keep[l], self.Lmax, rows=rows_dev,
+                                  workspace=self.score_ws)
             done = torch.cuda.Event()
             done.record(self.side)
         for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev):

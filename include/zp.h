@@ -245,6 +245,23 @@ zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
                            const int32_t *seq_lens, const int32_t *keep_idx, int32_t k,
                            int32_t n, void *stream);
 
+/* One layer's compression of n sequences in one call [Zipage App. C.2-C.8,
+ * §4.2, App. C.6 Alg. 4, §4.4]: the final scores of zp_score_tokens, the keep
+ * sets of zp_select_topk (keep_idx [n][h_kv][k], tie_count nullable) and the
+ * moves of zp_compact_pages for this layer (K and V rows of k_cache/v_cache
+ * into dst_targets, F of each target slot <- the kept token's global score),
+ * with the same arguments, rules and results.  scores_out is nullable here.
+ * The finish of a (sequence, kv head) -- scores, selection and move -- runs in
+ * one CTA from shared memory while 8 * Lmax + 12 * k bytes fit in it; longer
+ * rows take the three separate steps.  Workspace: zp_compress_workspace_size. */
+size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
+zp_status zp_compress_layer(const zp_cache_desc *D, const zp_score_params *P, void *k_cache, void *v_cache,
+                            const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
+                            const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
+                            float *global_F, const int32_t *dst_targets, int32_t target_stride, int32_t k,
+                            int32_t *keep_idx, int32_t *tie_count, float *scores_out, int32_t Lmax,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---- host block pool and planner (no device work) ------------------------ */
 typedef struct zp_pool zp_pool;
 

@@ -269,3 +269,80 @@ def test_end_to_end_compression(zp, shape):
         assert len(new_tables[s]) == N_max
     print("reported tie swaps:", swaps)
     assert pool.num_free == c.n_total - B * N_max
+
+
+@pytest.mark.parametrize("shape", ["tiny", "qwen", "long_rows"])
+def test_compress_layer_matches_three_steps(zp, shape):
+    """zp_compress_layer (scores, selection and move fused per (sequence, kv
+    head), or the three steps for rows too long for shared memory) against the
+    three separate calls on copies of the same state: scores within 1e-6
+    relative, keep sets equal up to near-ties, every moved row bit-exact for
+    the keep set each path chose; and its keep sets against the oracle."""
+    if shape == "tiny":
+        B, h_q, h_kv, d, N_max, dtype, lo, hi = 4, 8, 2, 64, 4, "f32", 80, 150
+    elif shape == "qwen":
+        B, h_q, h_kv, d, N_max, dtype, lo, hi = 8, 32, 8, 128, 8, "bf16", 200, 900
+    else:
+        B, h_q, h_kv, d, N_max, dtype, lo, hi = 2, 32, 8, 128, 128, "bf16", 29000, 30000
+    b, w = 16, 16
+    c = _block_aligned_case(950 + len(shape), B, h_q, h_kv, d, b, lo, hi, dtype, dup=True, spare=B * N_max)
+    desc = _desc(zp, c)
+    lens = c.seq_lens.tolist()
+    Lmax = max(lens)
+    k = (N_max - 1) * b
+    rng = np.random.default_rng(951)
+    S0 = (rng.random((B, h_kv, Lmax + 16)) / 100).astype(np.float32)
+    F0 = (rng.random((c.n_total, b, h_kv)) / 80).astype(np.float32)
+    first = torch.tensor([1, 0] * (B // 2), dtype=torch.uint8, device="cuda")
+    free = c.free_blocks.numpy()
+    tg = np.stack([free[i * (N_max - 1):(i + 1) * (N_max - 1)] if i % 2 else c.block_table[i, : N_max - 1].numpy()
+                   for i in range(B)]).astype(np.int32)  # fresh targets for odd sequences, in place for even
+    targets = torch.from_numpy(tg).cuda()
+    params = zp.score_params(window=w)
+    out = {}
+    for path in ("three", "fused"):
+        dc = DeviceCase(c)
+        S = torch.from_numpy(S0.copy()).cuda()
+        F = torch.from_numpy(F0.copy()).cuda()
+        scores = torch.full((B, h_kv, Lmax), -5.0, device="cuda")
+        keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
+        if path == "three":
+            zp.zp_score_tokens(desc, params, dc.K[0], dc.table, dc.lens, first, S, F, scores)
+            zp.zp_select_topk(scores, dc.lens, k, keep)
+            zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k, scores=S)
+        else:
+            zp.zp_compress_layer(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, first, S, F, targets, k, keep,
+                                 Lmax, scores_out=scores)
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        out[path] = (scores.cpu().numpy(), keep.cpu().numpy(), dc.K[0].float().cpu().numpy(),
+                     dc.V[0].float().cpu().numpy(), F.cpu().numpy())
+    s3, k3, K3, V3, F3 = out["three"]
+    sf, kf, Kf, Vf, Ff = out["fused"]
+    fin = np.isfinite(s3)
+    assert np.array_equal(fin, np.isfinite(sf))
+    np.testing.assert_allclose(sf[fin], s3[fin], rtol=1e-6, atol=1e-9)  # reduction order differs
+    K0 = c.k_cache[0].float().numpy()
+    V0 = c.v_cache[0].float().numpy()
+    swaps = 0
+    prm = pipeline.ScoreParams(window=w)
+    for s in range(B):
+        L = lens[s]
+        for h in range(h_kv):
+            swaps += keep_sets_match(kf[s, h], k3[s, h], s3[s, h], k, L)
+            kept = kf[s, h]
+            for r in range(0, min(k, L), 3):  # moved rows of the fused path
+                pos = kept[r]
+                sb, ss = c.block_table[s, pos // b], pos % b
+                db, ds = tg[s, r // b], r % b
+                assert np.array_equal(Kf[db, ds, h], K0[sb, ss, h])
+                assert np.array_equal(Vf[db, ds, h], V0[sb, ss, h])
+        if shape != "long_rows" or s == 0:  # the oracle, sampled for the long rows
+            Fref = F0.astype(np.float64).copy()
+            sref = pipeline.final_scores(S0[s, :, :L].astype(np.float64), K0, Fref, c.block_table[s].numpy(), L, b,
+                                         bool(first[s]), prm)
+            np.testing.assert_allclose(sf[s, :, :L][np.isfinite(sref)], sref[np.isfinite(sref)],
+                                       **TOL_SCORE[dtype])
+            for h in range(h_kv):
+                swaps += keep_sets_match(kf[s, h], oracle.topk_keep(sref[h], k)[0], sref[h], k, L)
+    print("reported near-tie swaps:", swaps)
