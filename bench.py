@@ -57,6 +57,26 @@ WORKLOADS = {
 DEFAULT_WORKLOAD = "qwen3_8b_layer_64seq_ctx1k-4k"
 
 
+def _traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, while the
+    kernel's sources are the ones the counters were taken on (else None)."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    prof = os.path.join(here, "profiles", "decode_tc_qwen3_8b_layer_64seq.md")
+    try:
+        text = open(prof).read()
+        h = hashlib.sha1()
+        for f in ("decode_attn.cu", "zp_common.cuh"):
+            h.update(open(os.path.join(here, "compressed_paged_kv_zp_gb300", "csrc", f), "rb").read())
+        vals = dict(line.split(": ", 1) for line in text.splitlines()
+                    if line.startswith(("traffic_bytes_per_launch: ", "kernel_sources_sha1: ")))
+        if vals.get("kernel_sources_sha1", "").strip() != h.hexdigest():
+            return None
+        return int(vals["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -511,7 +531,8 @@ def main():
                    "peak_kind": peak_kind},
         "roofline": {"kernel": "zp_paged_decode_attn (decode_tc_kernel: attention, merges and window score)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "frac_of_8tbs": achieved / 8000.0, "traffic": None,
+                     "frac_of_8tbs": achieved / 8000.0,
+                     "traffic": _traffic() if wl.name == DEFAULT_WORKLOAD else None,
                      "algorithmic_bytes": dbytes, "avg_ms": dec_avg},
         "step_hbm_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
         "decode_ms_per_step": dec_avg,
