@@ -204,3 +204,34 @@ def test_workspace_too_small_is_rejected(zp):
         zp.zp_paged_decode_attn(_desc(zp, c), dc.q, dc.K[0], dc.V[0], dc.table, dc.lens,
                                 torch.empty_like(dc.q), workspace=ws)
     assert e.value.status == 4
+
+
+def test_wait_that_runs_out_is_reported(zp):
+    """Failure detection without a fault: the per-sequence control word of the
+    in-kernel merge (the first 8 bytes per sequence of the decode workspace)
+    is preset to a tagged arrival count that the CTAs' arrivals can never
+    complete, so nobody publishes the cut sequence and every CTA that waits
+    for it gives up after its 1 s limit.  The call returns, the device status
+    reads ZP_ERR_TIMEOUT, and a cleared workspace decodes correctly again."""
+    c = zp_inputs.make_paged_case(14, 1, 32, 8, 128, 16, lens=[8190], dtype="bf16")  # cut across all CTAs
+    dc = DeviceCase(c)
+    desc = _desc(zp, c)
+    ws = torch.zeros(zp.zp_decode_workspace_size(desc, 1, dc.table.shape[1]), dtype=torch.uint8, device="cuda")
+    tag = 0xC0DE5EC7A11D
+    word = (tag << 16) | 0x4000  # phase 0, 16384 arrivals already counted
+    ws[:8].view(torch.int64)[0] = word - (1 << 64) if word >= 1 << 63 else word  # same 64 bits
+    S = torch.zeros(1, 8, dc.table.shape[1] * 16, device="cuda")
+    zp.zp_device_status(clear=True)
+    out = torch.empty_like(dc.q)
+    zp.zp_paged_decode_attn(desc, dc.q, dc.K[0], dc.V[0], dc.table, dc.lens, out, score_accum=S, window=16,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    code, detail = zp.zp_device_status(clear=True)
+    assert code == 6 and detail == 50
+    ws.zero_()
+    out = torch.empty_like(dc.q)
+    zp.zp_paged_decode_attn(desc, dc.q, dc.K[0], dc.V[0], dc.table, dc.lens, out, score_accum=S, window=16,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    _check_out(out.float().cpu().numpy(), c, dc.np_k(), dc.np_v(), [0])
