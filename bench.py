@@ -11,7 +11,7 @@ One step = the whole hot path over that batch:
                            window-score accumulation (w = b = 16, so every
                            decode step is an observation-window step);
   3. compression of the sequences whose trigger holds at their length
-     (L % b == 0, L >= N_max * b): host planner, then zp_compress_layer:
+     (L % b == 0, L >= N_max * b): host planner, then zp_compress_layers:
      scores (global score, first-compression pooling, lightning redundancy,
      eq. 4, window), keep sets and the move into the planned target blocks.
 The batch is stationary: lengths and tables are not advanced between steps,
@@ -281,7 +281,7 @@ class Workload:
         if not self.n_comp:
             return
         zp = self.zp
-        zp.zp_compress_layer(self.desc, self.params, self.K, self.V, self.c_table, self.c_lens, self.c_first,
+        zp.zp_compress_layers(self.desc, self.params, self.K, self.V, self.c_table, self.c_lens, self.c_first,
                              self.S, self.F, self.c_targets, self.k, self.c_keep, self.c_Lmax, rows=self.c_rows,
                              workspace=self.c_ws, stream=stream)
 

@@ -31,9 +31,10 @@ EXPORTS = [
     "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
     "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
-    "zp_compress_workspace_size", "zp_compress_layer",
+    "zp_compress_workspace_size", "zp_compress_layers",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
+    "zp_plan_capacity",
 ]
 
 
@@ -108,9 +109,9 @@ def _load() -> ctypes.CDLL:
     lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
     lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, P, I32, P, I32, P, P, I32, I32, P]
     lib.zp_compress_workspace_size.restype = SZ
-    lib.zp_compress_workspace_size.argtypes = [D, I32, I32]
-    lib.zp_compress_layer.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, P, I32, P, P, I32, P, P, P, I32, I32,
-                                      P, P, P, I32, P, SZ, P]
+    lib.zp_compress_workspace_size.argtypes = [D, I32, I32, I32]
+    lib.zp_compress_layers.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P, P,
+                                       I64, P, I32, I32, P, P, P, I32, P, SZ, P]
     lib.zp_pool_create.restype = P
     lib.zp_pool_create.argtypes = [I32]
     lib.zp_pool_destroy.argtypes = [P]
@@ -121,6 +122,7 @@ def _load() -> ctypes.CDLL:
     lib.zp_pool_release.argtypes = [P, I32, P]
     lib.zp_plan_compaction.argtypes = [P, P, I32, I32, P, P, P, P, P]
     lib.zp_plan_compaction_batch.argtypes = [P, P, I32, P, I32, I32, P, P, P, P, P]
+    lib.zp_plan_capacity.argtypes = [I64, I64, I64, I32, I64, I64, P, P]
     return lib
 
 
@@ -266,28 +268,45 @@ def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, 
                                 _stream(stream)))
 
 
-def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int) -> int:
-    return int(lib.zp_compress_workspace_size(ctypes.byref(desc), int(n), int(Lmax)))
+def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int, layer_count: int = 1) -> int:
+    return int(lib.zp_compress_workspace_size(ctypes.byref(desc), int(n), int(Lmax), int(layer_count)))
 
 
-def zp_compress_layer(desc, params: ScoreParams, k_cache, v_cache, block_table, seq_lens, first_compression,
-                      attn, global_F, dst_targets, k, keep_idx, Lmax, rows=None, tie_count=None, scores_out=None,
-                      workspace=None, stream=None) -> None:
-    """Scores, keep sets and moves of one layer (the three steps in one call).
-    attn: the attention-score rows (see zp_score_tokens); dst_targets int32
-    [n][target_stride]; keep_idx int32 [n][h_kv][k] (written)."""
+def zp_compress_layers(desc, params: ScoreParams, k_cache, v_cache, block_table, seq_lens, first_compression,
+                       attn, global_F, dst_targets, k, keep_idx, Lmax, rows=None, tie_count=None, scores_out=None,
+                       workspace=None, stream=None) -> None:
+    """Scores, keep sets and moves of one or several layers in one call.
+    k_cache/v_cache: one layer [N_total][b][h_kv][d] or several
+    [layers][N_total][b][h_kv][d]; global_F and attn (score rows) alike;
+    keep_idx int32 [layers][n][h_kv][k] (or [n][h_kv][k] for one layer)."""
     n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    layers = int(k_cache.shape[0]) if k_cache.dim() == 5 else 1
+    layer_stride = int(k_cache.stride(0)) if layers > 1 else 0
+    F_layer = int(global_F.stride(0)) if (global_F is not None and global_F.dim() == 4) else 0
+    if layers > 1 and attn.dim() != 4:
+        raise ValueError("several layers need score rows [layers][R][h_kv][stride]")
     if workspace is None:
-        workspace = torch.empty(max(zp_compress_workspace_size(desc, n, Lmax), 1), dtype=torch.uint8,
+        workspace = torch.empty(max(zp_compress_workspace_size(desc, n, Lmax, layers), 1), dtype=torch.uint8,
                                 device=k_cache.device)
-    _check(lib.zp_compress_layer(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
-                                 _dev(v_cache, "v_cache"), _dev(block_table, "block_table"), table_stride,
-                                 _dev(seq_lens, "seq_lens"), _dev(first_compression, "first_compression"), n,
-                                 _score_rows(attn, rows), _dev(global_F, "global_F"),
-                                 _dev(dst_targets, "dst_targets"), int(dst_targets.shape[1]), int(k),
-                                 _dev(keep_idx, "keep_idx"), _dev(tie_count, "tie_count"),
-                                 _dev(scores_out, "scores_out"), int(Lmax), _dev(workspace, "workspace"),
-                                 workspace.numel(), _stream(stream)))
+    _check(lib.zp_compress_layers(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
+                                  _dev(v_cache, "v_cache"), layer_stride, layers, _dev(block_table, "block_table"),
+                                  table_stride, _dev(seq_lens, "seq_lens"),
+                                  _dev(first_compression, "first_compression"), n, _score_rows(attn, rows),
+                                  _dev(global_F, "global_F"), F_layer, _dev(dst_targets, "dst_targets"),
+                                  int(dst_targets.shape[1]), int(k), _dev(keep_idx, "keep_idx"),
+                                  _dev(tie_count, "tie_count"), _dev(scores_out, "scores_out"), int(Lmax),
+                                  _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def zp_plan_capacity(m_available: int, m_kv_block: int, m_q_request: int, max_blocks: int,
+                     extra=(0, 1)):
+    """(M, N_total) of eq. (1) / (2): the largest request concurrency and the
+    block count for a memory budget; extra = (num, den) per-block overhead of
+    the global score cache relative to K and V."""
+    M, N = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.zp_plan_capacity(int(m_available), int(m_kv_block), int(m_q_request), int(max_blocks),
+                                int(extra[0]), int(extra[1]), ctypes.byref(M), ctypes.byref(N)))
+    return M.value, N.value
 
 
 def zp_device_status(clear: bool = True):
@@ -375,5 +394,5 @@ __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", 
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_window_score_workspace_size", "zp_window_score",
            "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
-           "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layer", "zp_device_status", "Pool",
+           "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layers", "zp_plan_capacity", "zp_device_status", "Pool",
            "ZP_BF16", "ZP_F32"]

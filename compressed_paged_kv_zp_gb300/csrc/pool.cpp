@@ -148,3 +148,33 @@ extern "C" zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tabl
     }
     return ok();
 }
+
+// Capacity plan [Zipage §4.2 eq. (1), App. C.3 eq. (2)]: the largest request
+// concurrency M and the block count N_total that fit a memory budget,
+//     maximise M  s.t.  (1 + extra) m_kv N_total + M m_q <= m_available,
+//                       M <= N_total / N_max,  M > 0,  N_total > 0.
+// For a given M the least N_total is M N_max, so the optimum is
+//     M = floor(m_available / ((1 + extra) m_kv N_max + m_q)),
+// and the blocks of the linear program's optimum,
+//     N_total = floor(m_available / ((1 + extra) m_kv + m_q / N_max)),
+// satisfy both constraints with that M.  Integer arithmetic: extra is given
+// as the fraction extra_num / extra_den (the global score cache: 1/(2d) of a
+// block's K and V in the paper's element type; 0/1 without it).
+extern "C" zp_status zp_plan_capacity(int64_t m_available, int64_t m_kv_block, int64_t m_q_request,
+                                      int32_t max_blocks, int64_t extra_num, int64_t extra_den, int64_t *M,
+                                      int64_t *N_total) {
+    if (!M || !N_total) return fail(ZP_ERR_INVALID_ARG, "plan_capacity: NULL output");
+    if (m_available <= 0 || m_kv_block <= 0 || m_q_request < 0 || max_blocks < 1 || extra_num < 0 ||
+        extra_den <= 0)
+        return fail(ZP_ERR_INVALID_ARG, "plan_capacity: bad sizes");
+    // work in units of 1/extra_den byte: block cost (den + num) * m_kv
+    const __int128 den = extra_den, blk = (__int128)(extra_den + extra_num) * m_kv_block;
+    const __int128 avail = (__int128)m_available * den, q = (__int128)m_q_request * den;
+    const __int128 m = avail / (blk * max_blocks + q);
+    // N_total = floor(avail / (blk + q / N_max)) = floor(avail * N_max / (blk * N_max + q))
+    const __int128 nt = avail * max_blocks / (blk * max_blocks + q);
+    if (m <= 0) return fail(ZP_ERR_CAPACITY, "plan_capacity: the budget holds no request of %d blocks", max_blocks);
+    *M = (int64_t)m;
+    *N_total = (int64_t)nt;
+    return ok();
+}

@@ -46,7 +46,22 @@ struct ScoreArgs {
     float p, lambda, tau;
     int window;
     unsigned *err;
+    // layers of one call (blockIdx.z of the fused kernels): strides in bytes (K)
+    // and elements (S, F, X / rho / out)
+    long long k_layer_bytes, S_layer, F_layer, X_layer;
 };
+
+// The arguments of layer z: every per-layer pointer advanced by its stride.
+__device__ __forceinline__ ScoreArgs at_layer(const ScoreArgs &a0, int z) {
+    ScoreArgs a = a0;
+    a.k = static_cast<const char *>(a0.k) + z * a0.k_layer_bytes;
+    a.S = a0.S + z * a0.S_layer;
+    if (a0.F) a.F = a0.F + z * a0.F_layer;
+    a.X = a0.X + z * a0.X_layer;
+    a.rho = a0.rho + z * a0.X_layer;
+    if (a0.out) a.out = a0.out + z * a0.X_layer;
+    return a;
+}
 
 __device__ __forceinline__ int clamp_len(const ScoreArgs &a, int s) {
     int L = a.seq_lens[s];
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 }
 
 // Redundancy and global score of one 16-token block in one CTA (bf16 keys,
-// b = 16, the path zp_compress_layer takes).  grid (ceil(Lmax / 16), n), one
+// b = 16, the path zp_compress_layers takes).  grid (ceil(Lmax / 16), n), one
 // warp per kv head.  The block's token rows (all kv heads, contiguous in HBM)
 // come by one bulk copy each into shared memory rows padded by 16 bytes, so
 // the eight rows an ldmatrix reads fall on eight bank groups; while they are
@@ -332,7 +347,8 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // on the tensor cores (16 mma.sync), and on the accumulator fragments the
 // lightning rule as in lightning_tc_kernel.
 template <int D>
-__global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
+    const ScoreArgs a = at_layer(a0, blockIdx.z);
     extern __shared__ __align__(128) unsigned char gsm[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_blk, s_abort;
@@ -516,7 +532,7 @@ __global__ void finalize_kernel(const ScoreArgs a) {
 
 
 // ---------------------------------------------------------------------------
-// Fused finish of one layer's compression (zp_compress_layer): per (sequence,
+// Fused finish of one layer's compression (zp_compress_layers): per (sequence,
 // kv head) one CTA takes the global score X and the row sums rho into shared
 // memory, finalises the scores there (as finalize_kernel), selects the keep
 // set (block_select_topk) and moves this kv head's kept rows of K and V into
@@ -532,6 +548,8 @@ struct MoveArgs {
     int32_t *keep;       // [n][h_kv][k]
     int32_t *tie;        // nullable [n][h_kv]
     float *F;            // nullable, paged
+    long long kv_layer_vec;  // 16-byte vectors between layers of K (and V)
+    long long F_layer;       // elements between layers of F
 };
 
 constexpr int kFsThreads = 512;
@@ -556,7 +574,15 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) 
     return t;
 }
 
-__global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a, const MoveArgs m) {
+__global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a0, const MoveArgs m0) {
+    const int z = blockIdx.z;
+    const ScoreArgs a = at_layer(a0, z);
+    MoveArgs m = m0;
+    m.K = m0.K + z * m0.kv_layer_vec;
+    m.V = m0.V + z * m0.kv_layer_vec;
+    if (m0.F) m.F = m0.F + z * m0.F_layer;
+    m.keep = m0.keep + (size_t)z * a0.n * a0.h_kv * m0.k;
+    if (m0.tie) m.tie = m0.tie + (size_t)z * a0.n * a0.h_kv;
     extern __shared__ __align__(16) unsigned char fsm[];
     __shared__ SelectShared sh;
     __shared__ float red[32];
@@ -702,7 +728,8 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
                                const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
                                const float *global_F, float *scores_out, int32_t Lmax, void *workspace,
                                size_t workspace_bytes, cudaStream_t st, ScoreArgs &a, DeviceInfo &dev,
-                               bool *launched) {
+                               bool *launched, int layers = 1, long long k_layer_elems = 0,
+                               long long F_layer = 0) {
     *launched = false;
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
@@ -725,7 +752,7 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy score is not built; use lightning");
     if (P->use_similarity && D->block_size > 16)
         return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
-    const size_t need = zp_score_workspace_size(D, n, Lmax);
+    const size_t need = (size_t)layers * zp_score_workspace_size(D, n, Lmax);
     if (workspace_bytes < need) return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
@@ -744,8 +771,12 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     a.S_rows = attn->rows;
     a.F = global_F;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.X_layer = (long long)n * D->h_kv * Lmax;
     a.X = reinterpret_cast<float *>(ws);
-    a.rho = reinterpret_cast<float *>(ws + align_up((size_t)n * D->h_kv * Lmax * 4, 256));
+    a.rho = reinterpret_cast<float *>(ws + align_up((size_t)layers * a.X_layer * 4, 256));
+    a.k_layer_bytes = k_layer_elems * elem_bytes(D->dtype);
+    a.S_layer = attn->layer_stride;
+    a.F_layer = F_layer;
     a.out = scores_out;
     a.k = k_cache;
     a.use_global = P->use_global;
@@ -762,7 +793,7 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
         // global score and redundancy of each block in one kernel
         const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
-        dim3 g2((Lmax + 15) / 16, n);
+        dim3 g2((Lmax + 15) / 16, n, layers);
         if (a.d == 128) {
             if (smem > 48 * 1024)
                 cudaFuncSetAttribute(global_lightning_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -779,6 +810,7 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         *launched = true;
         return ok();
     }
+    if (layers != 1) return fail(ZP_ERR_SHAPE, "score: several layers per call need bf16 keys and b = 16");
     dim3 g1((Lmax + kTile - 1) / kTile, n);
     gather_global_kernel<<<g1, 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
@@ -839,8 +871,10 @@ extern "C" zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_para
     return ok();
 }
 
-extern "C" size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax) {
-    return zp_score_workspace_size(D, n, Lmax);
+extern "C" size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax,
+                                             int32_t layer_count) {
+    if (layer_count < 1) return 0;
+    return (size_t)layer_count * zp_score_workspace_size(D, n, Lmax);
 }
 
 extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base, int64_t layer_stride,
@@ -852,37 +886,53 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
 extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const int32_t *seq_lens,
                                     int32_t n, int32_t k, int32_t *keep_idx, int32_t *tie_count, void *stream);
 
-extern "C" zp_status zp_compress_layer(const zp_cache_desc *D, const zp_score_params *P, void *k_cache,
-                                       void *v_cache, const int32_t *block_table, int32_t table_stride,
-                                       const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
-                                       const zp_score_rows *attn, float *global_F, const int32_t *dst_targets,
-                                       int32_t target_stride, int32_t k, int32_t *keep_idx, int32_t *tie_count,
-                                       float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
-                                       void *stream) {
+extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
+                                        void *v_base, int64_t layer_stride, int32_t layer_count,
+                                        const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
+                                        const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
+                                        float *global_F, int64_t F_layer_stride, const int32_t *dst_targets,
+                                        int32_t target_stride, int32_t k, int32_t *keep_idx, int32_t *tie_count,
+                                        float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
+                                        void *stream) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
-    if (n < 0 || k < 0 || Lmax < 0 || target_stride < 1) return fail(ZP_ERR_INVALID_ARG, "compress: bad sizes");
-    if (n == 0 || k == 0) return ok();
-    if (!k_cache || !v_cache || !dst_targets || !keep_idx) return fail(ZP_ERR_INVALID_ARG, "compress: NULL buffer");
+    if (n < 0 || k < 0 || Lmax < 0 || target_stride < 1 || layer_count < 0)
+        return fail(ZP_ERR_INVALID_ARG, "compress: bad sizes");
+    if (n == 0 || k == 0 || layer_count == 0) return ok();
+    if (!k_base || !v_base || !dst_targets || !keep_idx || !attn)
+        return fail(ZP_ERR_INVALID_ARG, "compress: NULL buffer");
     if ((long long)target_stride * D->block_size < k)
         return fail(ZP_ERR_CAPACITY, "compress: %d target blocks hold fewer than k=%d rows", target_stride, k);
     const int es = elem_bytes(D->dtype);
     const size_t row_bytes = (size_t)D->head_dim * es;
     if (row_bytes % 16) return fail(ZP_ERR_SHAPE, "compress: row of %zu bytes", row_bytes);
-    if (((uintptr_t)k_cache | (uintptr_t)v_cache) % 16) return fail(ZP_ERR_INVALID_ARG, "compress: unaligned cache");
-    ScoreArgs a;
-    DeviceInfo dev;
-    bool launched;
+    const long long per_layer = (long long)D->n_total_blocks * D->block_size * D->h_kv * D->head_dim;
+    if (layer_count > 1 && (layer_stride < per_layer || (layer_stride * es) % 16))
+        return fail(ZP_ERR_INVALID_ARG, "compress: layer_stride %lld", (long long)layer_stride);
+    if (((uintptr_t)k_base | (uintptr_t)v_base) % 16) return fail(ZP_ERR_INVALID_ARG, "compress: unaligned cache");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    rc = launch_scores(D, P, k_cache, block_table, table_stride, seq_lens, first_compression, n, attn, global_F,
-                       scores_out, Lmax, workspace, workspace_bytes, st, a, dev, &launched);
-    if (rc != ZP_OK || !launched) return rc;
+    const size_t ws_layer = zp_score_workspace_size(D, n, Lmax);
+    const size_t out_layer = (size_t)n * D->h_kv * Lmax;
+    const size_t keep_layer = (size_t)n * D->h_kv * k;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != ZP_OK) return rc;
     const int row_vec = (int)(row_bytes / 16);
     const size_t smem = fused_smem(Lmax, k, D->block_size);
-    if (2 * row_vec <= kFsThreads * kFsVecPerThread && smem <= (size_t)dev.smem_optin) {
+    const bool fused_ok = D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
+                          D->h_kv <= 16 && P && P->use_similarity && P->lightning &&
+                          2 * row_vec <= kFsThreads * kFsVecPerThread && smem <= (size_t)dev.smem_optin;
+    if (fused_ok) {
+        // every layer in one launch of each kernel (blockIdx.z = layer)
+        ScoreArgs a;
+        bool launched;
+        rc = launch_scores(D, P, k_base, block_table, table_stride, seq_lens, first_compression, n, attn, global_F,
+                           scores_out, Lmax, workspace, workspace_bytes, st, a, dev, &launched, layer_count,
+                           layer_stride, F_layer_stride);
+        if (rc != ZP_OK || !launched) return rc;
         MoveArgs m;
-        m.K = static_cast<uint4 *>(k_cache);
-        m.V = static_cast<uint4 *>(v_cache);
+        m.K = static_cast<uint4 *>(k_base);
+        m.V = static_cast<uint4 *>(v_base);
         m.row_vec = row_vec;
         m.dst = dst_targets;
         m.target_stride = target_stride;
@@ -890,24 +940,47 @@ extern "C" zp_status zp_compress_layer(const zp_cache_desc *D, const zp_score_pa
         m.keep = keep_idx;
         m.tie = tie_count;
         m.F = global_F;
+        m.kv_layer_vec = layer_stride * es / 16;
+        m.F_layer = F_layer_stride;
         if (smem > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(finalize_select_move_kernel,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return cuda_fail(e, "compress: cudaFuncSetAttribute");
         }
-        finalize_select_move_kernel<<<dim3(a.h_kv, n), kFsThreads, smem, st>>>(a, m);
+        finalize_select_move_kernel<<<dim3(a.h_kv, n, layer_count), kFsThreads, smem, st>>>(a, m);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "compress: launch");
         return ok();
     }
-    // rows too long for shared memory: the three separate steps (scores land in
-    // scores_out, else in place of the row sums)
-    if (!a.out) a.out = a.rho;
-    finalize_kernel<<<dim3(a.h_kv, n), 1024, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "compress: finalize launch");
-    rc = zp_select_topk(a.out, a.h_kv, Lmax, seq_lens, n, k, keep_idx, tie_count, stream);
-    if (rc != ZP_OK) return rc;
-    return zp_compact_pages(D, k_cache, v_cache, 0, 1, global_F, 0, attn, block_table, table_stride, dst_targets,
-                            target_stride, seq_lens, keep_idx, k, n, stream);
+    // otherwise the three steps, one layer at a time (scores land in scores_out,
+    // else in place of the row sums)
+    if (workspace_bytes < (size_t)layer_count * ws_layer)
+        return fail(ZP_ERR_CAPACITY, "compress: workspace %zu < %zu", workspace_bytes, (size_t)layer_count * ws_layer);
+    for (int l = 0; l < layer_count; ++l) {
+        zp_score_rows at = *attn;
+        at.data = attn->data + (size_t)l * attn->layer_stride;
+        at.layer_stride = 0;
+        unsigned char *ws = static_cast<unsigned char *>(workspace) + (size_t)l * ws_layer;
+        char *kl = static_cast<char *>(k_base) + (size_t)l * layer_stride * es;
+        char *vl = static_cast<char *>(v_base) + (size_t)l * layer_stride * es;
+        float *Fl = global_F ? global_F + (size_t)l * F_layer_stride : nullptr;
+        ScoreArgs a;
+        bool launched;
+        rc = launch_scores(D, P, kl, block_table, table_stride, seq_lens, first_compression, n, &at, Fl,
+                           scores_out ? scores_out + l * out_layer : nullptr, Lmax, ws, ws_layer, st, a, dev,
+                           &launched);
+        if (rc != ZP_OK) return rc;
+        if (!launched) continue;
+        if (!a.out) a.out = a.rho;
+        finalize_kernel<<<dim3(a.h_kv, n), 1024, 0, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "compress: finalize launch");
+        rc = zp_select_topk(a.out, a.h_kv, Lmax, seq_lens, n, k, keep_idx + l * keep_layer,
+                            tie_count ? tie_count + (size_t)l * n * D->h_kv : nullptr, stream);
+        if (rc != ZP_OK) return rc;
+        rc = zp_compact_pages(D, kl, vl, 0, 1, Fl, 0, &at, block_table, table_stride, dst_targets, target_stride,
+                              seq_lens, keep_idx + l * keep_layer, k, n, stream);
+        if (rc != ZP_OK) return rc;
+    }
+    return ok();
 }

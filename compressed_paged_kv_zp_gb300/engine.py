@@ -20,7 +20,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layer, zp_compress_workspace_size,
+from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layers, zp_compress_workspace_size,
                zp_decode_workspace_size, zp_paged_decode_attn)
 
 
@@ -28,7 +28,7 @@ class DecodeLoop:
     """Batch of sequences decoding over `layers` paged layers of one pool."""
 
     def __init__(self, h_q, h_kv, d, b, n_total, max_blocks, table_stride, layers=1, dtype=torch.bfloat16,
-                 window=None, params=None, async_compress=False, device="cuda"):
+                 window=None, params=None, async_compress=False, layer_stride=None, device="cuda"):
         self.h_q, self.h_kv, self.d, self.b = h_q, h_kv, d, b
         self.n_total, self.N_max, self.stride, self.layers = n_total, max_blocks, table_stride, layers
         self.k = (max_blocks - 1) * b
@@ -38,6 +38,9 @@ class DecodeLoop:
         self.desc = cache_desc(h_q, h_kv, d, b, n_total, dtype)
         self.params = params or score_params(window=self.window)
         self.async_compress = async_compress
+        # layers compressed per call (App. C.1's layer stride): bounds the
+        # scoring scratch to layer_stride layers
+        self.layer_stride = max(1, min(layer_stride or layers, layers))
         self.K = torch.zeros(layers, n_total, b, h_kv, d, dtype=dtype, device=self.dev)
         self.V = torch.zeros_like(self.K)
         # global score cache F: paged like K (it moves with the kept tokens)
@@ -86,8 +89,8 @@ class DecodeLoop:
                               device=self.dev)
         Lmax = self.stride * self.b
         self.Lmax = Lmax
-        self.score_ws = torch.empty(max(zp_compress_workspace_size(self.desc, B, Lmax), 1), dtype=torch.uint8,
-                                    device=self.dev)
+        self.score_ws = torch.empty(max(zp_compress_workspace_size(self.desc, B, Lmax, self.layer_stride), 1),
+                                    dtype=torch.uint8, device=self.dev)
         self.out = torch.zeros(self.layers, B, self.h_q, self.d, dtype=self.dtype, device=self.dev)
 
     def layer_stride(self):
@@ -139,10 +142,11 @@ class DecodeLoop:
         with torch.cuda.stream(self.side):
             self.side.wait_event(ready)
             keep = torch.empty(self.layers, n, self.h_kv, self.k, dtype=torch.int32, device=self.dev)
-            for l in range(self.layers):  # scores, keep sets and moves of one layer per call
-                zp_compress_layer(self.desc, self.params, self.K[l], self.V[l], tables_dev, lens_dev, first_dev,
-                                  self.S[l], self.F[l], targets_dev, self.k, keep[l], self.Lmax, rows=rows_dev,
-                                  workspace=self.score_ws)
+            for l0 in range(0, self.layers, self.layer_stride):  # scores, keep sets, moves of a layer group
+                l1 = min(l0 + self.layer_stride, self.layers)
+                zp_compress_layers(self.desc, self.params, self.K[l0:l1], self.V[l0:l1], tables_dev, lens_dev,
+                                   first_dev, self.S[l0:l1], self.F[l0:l1], targets_dev, self.k, keep[l0:l1],
+                                   self.Lmax, rows=rows_dev, workspace=self.score_ws)
             done = torch.cuda.Event()
             done.record(self.side)
         for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev):

@@ -247,22 +247,30 @@ zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
                            const int32_t *seq_lens, const int32_t *keep_idx, int32_t k,
                            int32_t n, void *stream);
 
-/* One layer's compression of n sequences in one call [Zipage App. C.2-C.8,
- * §4.2, App. C.6 Alg. 4, §4.4]: the final scores of zp_score_tokens, the keep
- * sets of zp_select_topk (keep_idx [n][h_kv][k], tie_count nullable) and the
- * moves of zp_compact_pages for this layer (K and V rows of k_cache/v_cache
+/* Compression of n sequences over layer_count layers in one call [Zipage
+ * App. C.1 (cross-layer parallel compression, layer stride), C.2-C.8, §4.2,
+ * App. C.6 Alg. 4, §4.4]: per layer the final scores of zp_score_tokens, the
+ * keep sets of zp_select_topk and the moves of zp_compact_pages (K and V rows
  * into dst_targets, F of each target slot <- the kept token's global score),
- * with the same arguments, rules and results.  scores_out is nullable here.
- * The finish of a (sequence, kv head) -- scores, selection and move -- runs in
- * one CTA from shared memory while 8 * Lmax + 12 * k bytes fit in it; longer
- * rows take the three separate steps.  Workspace: zp_compress_workspace_size. */
-size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax);
-zp_status zp_compress_layer(const zp_cache_desc *D, const zp_score_params *P, void *k_cache, void *v_cache,
-                            const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
-                            const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
-                            float *global_F, const int32_t *dst_targets, int32_t target_stride, int32_t k,
-                            int32_t *keep_idx, int32_t *tie_count, float *scores_out, int32_t Lmax,
-                            void *workspace, size_t workspace_bytes, void *stream);
+ * with the same rules and results.  Layer l uses k_base/v_base + l*layer_stride
+ * elements, attn rows + l*attn->layer_stride, global_F + l*F_layer_stride,
+ * keep_idx [layer_count][n][h_kv][k], tie_count (nullable)
+ * [layer_count][n][h_kv] and scores_out (nullable) [layer_count][n][h_kv][Lmax].
+ * For bf16 caches with b = 16 and the lightning redundancy, every layer runs
+ * in one launch of each of two kernels: the global score and redundancy per
+ * (block, sequence, layer), then per (kv head, sequence, layer) one CTA that
+ * finishes the scores, selects the keep set and moves the rows from shared
+ * memory (while 8*Lmax + 12*k bytes fit in it); otherwise the three steps run
+ * layer by layer.  The workspace (zp_compress_workspace_size) grows with
+ * layer_count: the paper's layer stride is the number of layers per call. */
+size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax, int32_t layer_count);
+zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
+                             int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
+                             int32_t table_stride, const int32_t *seq_lens, const uint8_t *first_compression,
+                             int32_t n, const zp_score_rows *attn, float *global_F, int64_t F_layer_stride,
+                             const int32_t *dst_targets, int32_t target_stride, int32_t k, int32_t *keep_idx,
+                             int32_t *tie_count, float *scores_out, int32_t Lmax, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /* ---- host block pool and planner (no device work) ------------------------ */
 typedef struct zp_pool zp_pool;
@@ -301,6 +309,21 @@ zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tables, int32_t
                                    const int32_t *n_blocks, int32_t n, int32_t max_blocks,
                                    int32_t *targets, int32_t *new_tables, int32_t *dropped,
                                    int32_t *n_dropped, int32_t *n_fresh);
+
+/* Capacity plan [Zipage §4.2 eq. (1), App. C.3 eq. (2)] (host only): the
+ * largest request concurrency M and the block count N_total for a memory
+ * budget, maximising M subject to
+ *     (1 + extra) * m_kv_block * N_total + M * m_q_request <= m_available,
+ *     M <= N_total / max_blocks,  M > 0,  N_total > 0,
+ * with extra = extra_num / extra_den the per-block overhead of the global
+ * score cache relative to K and V (the paper's 1/(2d); 0/1 without it).
+ * Returns M = floor(m_available / ((1+extra) m_kv N_max + m_q)) and the
+ * linear program's N_total = floor(m_available / ((1+extra) m_kv + m_q/N_max)).
+ * m_kv_block: bytes of one block's K and V over all layers; m_q_request:
+ * per-request bytes that do not depend on N_total (the paper's query cache;
+ * here the attention-score rows).  ZP_ERR_CAPACITY when M would be 0. */
+zp_status zp_plan_capacity(int64_t m_available, int64_t m_kv_block, int64_t m_q_request, int32_t max_blocks,
+                           int64_t extra_num, int64_t extra_den, int64_t *M, int64_t *N_total);
 
 #ifdef __cplusplus
 }

@@ -145,3 +145,40 @@ def test_batch_planner_matches_single_calls(zp):
         assert list(batch["dropped"][i, :batch["n_dropped"][i]]) == sp["dropped"]
         assert batch["n_fresh"][i] == sp["n_fresh"]
     assert pools[0].num_free == pools[1].num_free
+
+
+def test_capacity_plan_brute_force(zp):
+    """eq. (1)/(2): M is the largest concurrency any block count allows; the
+    returned N_total is feasible with it and equals the linear program's
+    optimum (floored) -- checked against enumeration on small budgets."""
+    import random
+    from fractions import Fraction
+    rng = random.Random(5)
+    for _ in range(200):
+        A = rng.randint(50, 1200)
+        m = rng.randint(1, 40)
+        q = rng.randint(0, 60)
+        N = rng.randint(1, 9)
+        num, den = rng.choice([(0, 1), (1, 16), (1, 256), (3, 7)])
+        f = Fraction(num, den)
+        best = 0
+        for Nt in range(1, A // m + 2):
+            for M in range(1, Nt // N + 1):
+                if (1 + f) * m * Nt + M * q <= A:
+                    best = max(best, M)
+        if best == 0:
+            with pytest.raises(zp.ZPError):
+                zp.zp_plan_capacity(A, m, q, N, (num, den))
+            continue
+        M, Nt = zp.zp_plan_capacity(A, m, q, N, (num, den))
+        assert M == best
+        assert (1 + f) * m * Nt + M * q <= A and M <= Fraction(Nt, N)
+        assert Nt == int(Fraction(A) / ((1 + f) * m + Fraction(q, N)))
+
+
+def test_capacity_plan_closed_forms(zp):
+    # no per-request memory: every byte goes to blocks
+    assert zp.zp_plan_capacity(1000, 10, 0, 4) == (25, 100)
+    # the global score cache at the paper's ratio 1/(2d), d = 128: blocks cost 257/256
+    M, N = zp.zp_plan_capacity(257 * 1000, 256, 0, 8, (1, 256))
+    assert (M, N) == (125, 1000)

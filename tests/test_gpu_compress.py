@@ -273,7 +273,7 @@ def test_end_to_end_compression(zp, shape):
 
 @pytest.mark.parametrize("shape", ["tiny", "qwen", "long_rows"])
 def test_compress_layer_matches_three_steps(zp, shape):
-    """zp_compress_layer (scores, selection and move fused per (sequence, kv
+    """zp_compress_layers (scores, selection and move fused per (sequence, kv
     head), or the three steps for rows too long for shared memory) against the
     three separate calls on copies of the same state: scores within 1e-6
     relative, keep sets equal up to near-ties, every moved row bit-exact for
@@ -311,7 +311,7 @@ def test_compress_layer_matches_three_steps(zp, shape):
             zp.zp_select_topk(scores, dc.lens, k, keep)
             zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k, scores=S)
         else:
-            zp.zp_compress_layer(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, first, S, F, targets, k, keep,
+            zp.zp_compress_layers(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, first, S, F, targets, k, keep,
                                  Lmax, scores_out=scores)
         torch.cuda.synchronize()
         assert zp.zp_device_status() == (0, 0)
@@ -346,3 +346,42 @@ def test_compress_layer_matches_three_steps(zp, shape):
             for h in range(h_kv):
                 swaps += keep_sets_match(kf[s, h], oracle.topk_keep(sref[h], k)[0], sref[h], k, L)
     print("reported near-tie swaps:", swaps)
+
+
+def test_compress_layers_several_layers_in_one_call(zp):
+    """Three layers in one zp_compress_layers call (one launch per kernel,
+    App. C.1) equal three single-layer calls: scores, keep sets, K, V and F
+    bit-exact (the same arithmetic per layer)."""
+    B, h_q, h_kv, d, b, N_max, layers = 5, 32, 8, 128, 16, 8, 3
+    g = torch.Generator().manual_seed(960)
+    lens = (torch.randint(200, 900, (B,), generator=g) // b * b).tolist()
+    c = zp_inputs.make_paged_case(960, B, h_q, h_kv, d, b, lens=lens, dtype="bf16", layers=layers,
+                                  spare_blocks=B * N_max)
+    zp_inputs.plant_duplicates(c, 961)
+    desc = _desc(zp, c)
+    Lmax, k = max(lens), (N_max - 1) * b
+    rng = np.random.default_rng(962)
+    S0 = (rng.random((layers, B, h_kv, Lmax + 8)) / 100).astype(np.float32)
+    F0 = (rng.random((layers, c.n_total, b, h_kv)) / 80).astype(np.float32)
+    first = torch.tensor([0, 1, 0, 1, 0], dtype=torch.uint8, device="cuda")
+    targets = c.block_table[:, : N_max - 1].contiguous().cuda()
+    params = zp.score_params(window=16)
+    res = {}
+    for mode in ("one_call", "per_layer"):
+        dc = DeviceCase(c)
+        S = torch.from_numpy(S0.copy()).cuda()
+        F = torch.from_numpy(F0.copy()).cuda()
+        keep = torch.empty(layers, B, h_kv, k, dtype=torch.int32, device="cuda")
+        scores = torch.full((layers, B, h_kv, Lmax), -5.0, device="cuda")
+        if mode == "one_call":
+            zp.zp_compress_layers(desc, params, dc.K, dc.V, dc.table, dc.lens, first, S, F, targets, k, keep, Lmax,
+                                  scores_out=scores)
+        else:
+            for l in range(layers):
+                zp.zp_compress_layers(desc, params, dc.K[l], dc.V[l], dc.table, dc.lens, first, S[l], F[l],
+                                      targets, k, keep[l], Lmax, scores_out=scores[l])
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        res[mode] = [t.cpu() for t in (scores, keep, dc.K, dc.V, F, S)]
+    for x, y in zip(res["one_call"], res["per_layer"]):
+        assert torch.equal(x, y)

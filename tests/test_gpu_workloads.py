@@ -13,7 +13,7 @@ DecodeLoop driver.
 * Prefix-shared, 36 layers: 32q/8kv/128 bf16, 32 sequences sharing a
   1024-token prefix (64 blocks), private tails uniform in [0, 2048], budget
   N_max = 64 blocks, compression asynchronous on the side stream while the
-  others decode.  A prefix cache holds one more reference to the prefix, so
+  others decode, 8 layers per compression call (App. C.1's layer stride).  A prefix cache holds one more reference to the prefix, so
   every compaction must go to fresh target blocks (§4.4).  Checked: the
   prefix blocks are never written; after all sequences compressed, only the
   prefix cache holds them; the sequences' blocks are disjoint and at most
@@ -137,7 +137,7 @@ def test_prefix_shared_36_layers_async():
         table[s, P:P + own[s]] = perm[cur:cur + own[s]]
         cur += own[s]
     loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=layers, dtype=torch.bfloat16, window=b,
-                      async_compress=True)
+                      async_compress=True, layer_stride=8)  # 8 layers per compression call
     loop.add_sequences(lens0, tables=table)
     prefix = table[0, :P].copy()
     loop.pool.incref(prefix.tolist())  # the prefix cache's own reference
