@@ -471,6 +471,159 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     }
 }
 
+// All-pairs ("flash") redundancy [App. C.5, Fig. 11, Alg. 3] for bf16 keys,
+// in O(L) memory.  The definition zeroes, in every column c of the cosine
+// matrix, the entry of the newest row r*(c) above p; the matrix is symmetric,
+// so r*(c) is also the largest index j != c with cos(k_c, k_j) > p -- a
+// quantity of row c.  So one pass over the Gram matrix by row tiles suffices:
+// a CTA owns 128 rows of one (sequence, kv head) and sweeps all column tiles
+// of 64 tokens (double-buffered cp.async copies into padded shared rows,
+// products on the tensor cores, mma.sync m16n8k16), keeping per row the sum of
+// its cosines and its last (largest-index) entry above p.  Then
+//     rho[r]       += sum_{c != r} cos(k_r, k_c)
+//     rho[r*(c)]   -= cos(k_c, k_{r*(c)})         for every c with an r*(c),
+// both as atomic additions into rho (zeroed before).  grid (ceil(Lmax/128),
+// h_kv, n), 8 warps of 16 rows.
+constexpr int kFrRows = 128, kFrCols = 64, kFrThreads = 256;
+
+template <int D>
+__device__ __forceinline__ void fr_load_rows(unsigned char *dst, int RSB, const ScoreArgs &a, int s, int kvh,
+                                             int t0, int nrows, int L) {
+    constexpr int CH = D / 8;  // 16-byte chunks per row piece
+    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.k);
+    for (int i = threadIdx.x; i < nrows * CH; i += blockDim.x) {
+        const int r = i / CH, c = i % CH;
+        const int t = t0 + r;
+        unsigned char *d = dst + r * RSB + c * 16;
+        int blk = -1;
+        if (t < L) blk = a.table[(size_t)s * a.table_stride + t / a.b];
+        if (blk >= 0 && blk < a.n_total) {
+            cp_async16_plain(d, K + (((size_t)blk * a.b + t % a.b) * a.h_kv + kvh) * D + c * 8);
+        } else {
+            if (t < L) record_error(a.err, ZP_ERR_DEVICE, 0x204);
+            *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void fr_inv_norms(float *out, const unsigned char *rows, int RSB, int nrows) {
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+        const __nv_bfloat162 *k = reinterpret_cast<const __nv_bfloat162 *>(rows + r * RSB);
+        float ss = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < D / 2; ++i) {
+            const float2 v = __bfloat1622float2(k[i]);
+            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
+        }
+        out[r] = ss > 0.f ? rsqrtf(ss) : 0.f;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const ScoreArgs a) {
+    extern __shared__ __align__(128) unsigned char frs[];
+    constexpr int KS = D / 16;
+    constexpr int RSB = D * 2 + 16;  // padded row: the 8 rows of an ldmatrix on 8 bank groups
+    const int s = blockIdx.z, kvh = blockIdx.y, rt = blockIdx.x;
+    const int L = clamp_len(a, s);
+    const int r0 = rt * kFrRows;
+    if (r0 >= L) return;
+    unsigned char *rowsK = frs;
+    unsigned char *colK = rowsK + kFrRows * RSB;  // [2][kFrCols] rows
+    float *inv_r = reinterpret_cast<float *>(colK + 2 * kFrCols * RSB);
+    float *inv_c = inv_r + kFrRows;  // [2][kFrCols]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int lm = lane >> 3;
+    const int lrow = (lm & 1) * 8 + (lane & 7);
+    const int lchunk = lm >> 1;
+    const int ncol = (L + kFrCols - 1) / kFrCols;
+    fr_load_rows<D>(rowsK, RSB, a, s, kvh, r0, kFrRows, L);
+    fr_load_rows<D>(colK, RSB, a, s, kvh, 0, kFrCols, L);
+    cp_async_commit();
+    const int rA = r0 + warp * 16 + g, rB = rA + 8;
+    float sumA = 0.f, sumB = 0.f, valA = 0.f, valB = 0.f;
+    int maxA = -1, maxB = -1;
+    float irA = 0.f, irB = 0.f;
+    for (int cc = 0; cc < ncol; ++cc) {
+        const int buf = cc & 1;
+        if (cc + 1 < ncol)  // the other buffer was released by the barrier that ended step cc - 1
+            fr_load_rows<D>(colK + (buf ^ 1) * kFrCols * RSB, RSB, a, s, kvh, (cc + 1) * kFrCols, kFrCols, L);
+        cp_async_commit();
+        cp_async_wait<1>();  // everything but the prefetch just issued has landed
+        __syncthreads();
+        if (cc == 0) fr_inv_norms<D>(inv_r, rowsK, RSB, kFrRows);
+        fr_inv_norms<D>(inv_c + buf * kFrCols, colK + buf * kFrCols * RSB, RSB, kFrCols);
+        __syncthreads();
+        if (cc == 0) {
+            irA = inv_r[warp * 16 + g];
+            irB = inv_r[warp * 16 + g + 8];
+        }
+        float acc[kFrCols / 8][4];
+#pragma unroll
+        for (int j = 0; j < kFrCols / 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+        const uint32_t abase = smem_u32(rowsK) + (uint32_t)((warp * 16 + lrow) * RSB);
+        const uint32_t bbase = smem_u32(colK + buf * kFrCols * RSB) + (uint32_t)(lrow * RSB);
+#pragma unroll
+        for (int t = 0; t < KS; ++t) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(abase + (uint32_t)((2 * t + lchunk) * 16), a0, a1, a2, a3);
+#pragma unroll
+            for (int j2 = 0; j2 < kFrCols / 16; ++j2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(bbase + (uint32_t)(j2 * 16 * RSB + (2 * t + lchunk) * 16), b0, b1, b2, b3);
+                mma_16816(acc[2 * j2], a0, a1, a2, a3, b0, b2);
+                mma_16816(acc[2 * j2 + 1], a0, a1, a2, a3, b1, b3);
+            }
+        }
+        // lane holds rows rA (acc[j][0..1]) and rB (acc[j][2..3]), columns j*8 + 2tig + {0,1}
+        const float *ic = inv_c + buf * kFrCols;
+        const int c0 = cc * kFrCols;
+#pragma unroll
+        for (int j = 0; j < kFrCols / 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int col = c0 + j * 8 + 2 * tig + e;
+                const float icv = ic[j * 8 + 2 * tig + e];
+                const bool cv = col < L;
+                const float xa = acc[j][e] * irA * icv, xb = acc[j][2 + e] * irB * icv;
+                if (cv && col != rA) {
+                    sumA += xa;
+                    if (xa > a.p) maxA = col, valA = xa;
+                }
+                if (cv && col != rB) {
+                    sumB += xb;
+                    if (xb > a.p) maxB = col, valB = xb;
+                }
+            }
+        __syncthreads();  // buffer `buf` is refilled by the next step's prefetch
+    }
+    // the four lanes of a row: sums add, the largest index above p wins
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        sumA += __shfl_xor_sync(0xFFFFFFFFu, sumA, o);
+        sumB += __shfl_xor_sync(0xFFFFFFFFu, sumB, o);
+        const int mA = __shfl_xor_sync(0xFFFFFFFFu, maxA, o), mB = __shfl_xor_sync(0xFFFFFFFFu, maxB, o);
+        const float vA = __shfl_xor_sync(0xFFFFFFFFu, valA, o), vB = __shfl_xor_sync(0xFFFFFFFFu, valB, o);
+        if (mA > maxA) maxA = mA, valA = vA;
+        if (mB > maxB) maxB = mB, valB = vB;
+    }
+    if (tig == 0) {
+        float *rho = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax;
+        if (rA < L) {
+            atomicAdd(rho + rA, sumA);
+            if (maxA >= 0) atomicAdd(rho + maxA, -valA);
+        }
+        if (rB < L) {
+            atomicAdd(rho + rB, sumB);
+            if (maxB >= 0) atomicAdd(rho + maxB, -valB);
+        }
+    }
+}
+
 // grid (h_kv, n), 1024 threads
 __global__ void finalize_kernel(const ScoreArgs a) {
     __shared__ float red[32];
@@ -748,9 +901,10 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     if (P->pool_policy < 0 || P->pool_policy > 2) return fail(ZP_ERR_INVALID_ARG, "score: pool policy");
     if (P->use_similarity && !(P->tau > 0.f)) return fail(ZP_ERR_INVALID_ARG, "score: tau must be > 0");
     if (D->h_kv > 16) return fail(ZP_ERR_SHAPE, "score: h_kv %d > 16", D->h_kv);
-    if (P->use_similarity && !P->lightning)
-        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy score is not built; use lightning");
-    if (P->use_similarity && D->block_size > 16)
+    const bool all_pairs = P->use_similarity && !P->lightning;
+    if (all_pairs && !(D->dtype == ZP_BF16 && (D->head_dim == 64 || D->head_dim == 128)))
+        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy needs bf16 keys and head_dim 64 or 128");
+    if (P->use_similarity && P->lightning && D->block_size > 16)
         return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
     const size_t need = (size_t)layers * zp_score_workspace_size(D, n, Lmax);
     if (workspace_bytes < need) return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
@@ -789,8 +943,8 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     a.tau = P->tau;
     a.window = P->window;
     a.err = dev.error_word;
-    if (a.use_sim && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) && a.h_kv <= 16 &&
-        reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
+    if (a.use_sim && P->lightning && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) &&
+        a.h_kv <= 16 && reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
         // global score and redundancy of each block in one kernel
         const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
         dim3 g2((Lmax + 15) / 16, n, layers);
@@ -815,7 +969,22 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     gather_global_kernel<<<g1, 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score: gather launch");
-    if (a.use_sim) {
+    if (all_pairs) {
+        // rho accumulates atomically: start from zero
+        e = cudaMemsetAsync(a.rho, 0, (size_t)n * a.h_kv * Lmax * 4, st);
+        if (e != cudaSuccess) return cuda_fail(e, "score: clearing rho");
+        const size_t smem = (size_t)(kFrRows + 2 * kFrCols) * (a.d * 2 + 16) + (size_t)(kFrRows + 2 * kFrCols) * 4;
+        dim3 gf((Lmax + kFrRows - 1) / kFrRows, a.h_kv, n);
+        if (a.d == 128) {
+            cudaFuncSetAttribute(flash_redundancy_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            flash_redundancy_kernel<128><<<gf, kFrThreads, smem, st>>>(a);
+        } else {
+            cudaFuncSetAttribute(flash_redundancy_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            flash_redundancy_kernel<64><<<gf, kFrThreads, smem, st>>>(a);
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "score: all-pairs redundancy launch");
+    } else if (a.use_sim) {
         dim3 g2((Lmax + a.b - 1) / a.b, n);
         const size_t smem = (size_t)a.h_kv * a.b * (a.d + 1) * 4;
         if (smem > (size_t)dev.smem_optin) return fail(ZP_ERR_SHAPE, "score: block of keys too large");

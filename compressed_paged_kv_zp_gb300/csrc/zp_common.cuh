@@ -241,6 +241,18 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint
                  : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy, default policy; completion by
+// cp_async_commit / cp_async_wait.
+__device__ __forceinline__ void cp_async16_plain(void *dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most N of this thread's committed groups are still pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued before has landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");

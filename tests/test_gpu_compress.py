@@ -385,3 +385,71 @@ def test_compress_layers_several_layers_in_one_call(zp):
         res[mode] = [t.cpu() for t in (scores, keep, dc.K, dc.V, F, S)]
     for x, y in zip(res["one_call"], res["per_layer"]):
         assert torch.equal(x, y)
+
+
+def test_all_pairs_redundancy_matches_oracle(zp):
+    """The all-pairs ('flash') redundancy score [App. C.5, Alg. 3] on bf16 keys
+    against the oracle's definition over the full L x L cosine matrix, with
+    near-duplicates planted inside blocks and hundreds of tokens apart (so the
+    per-column zeroing acts across tiles), through zp_score_tokens and through
+    zp_compress_layers (keep sets and moved rows)."""
+    B, h_q, h_kv, d, b, N_max = 3, 32, 8, 128, 16, 8
+    lens = [304, 800, 1504]
+    c = zp_inputs.make_paged_case(970, B, h_q, h_kv, d, b, lens=lens, dtype="bf16", spare_blocks=B * N_max)
+    zp_inputs.plant_duplicates(c, 971)
+    rng = np.random.default_rng(972)
+    Kc = c.k_cache[0].float().numpy()
+    for s, L in enumerate(lens):  # far-apart near-copies, in the sequence's own order
+        t = np.arange(L)
+        phys = c.block_table[s].numpy()[t // b] * b + t % b
+        flat = Kc.reshape(-1, h_kv, d)
+        pool = np.arange(300, L)
+        for dst in rng.choice(pool, size=min(L // 20, len(pool)), replace=False):
+            src = dst - rng.integers(100, 300)
+            flat[phys[dst]] = flat[phys[src]] + 0.05 * rng.standard_normal((h_kv, d)).astype(np.float32)
+    c.k_cache[0] = torch.from_numpy(Kc).to(torch.bfloat16)
+    dc = DeviceCase(c)
+    desc = _desc(zp, c)
+    Lmax = max(lens)
+    S0 = (rng.random((B, h_kv, Lmax)) / 100).astype(np.float32)
+    params = zp.score_params(window=16, lightning=False)
+    prm = pipeline.ScoreParams(window=16, lightning=False)
+    S = torch.from_numpy(S0.copy()).cuda()
+    F = torch.zeros(c.n_total, b, h_kv, device="cuda")
+    first = torch.ones(B, dtype=torch.uint8, device="cuda")
+    scores = torch.full((B, h_kv, Lmax), -3.0, device="cuda")
+    zp.zp_score_tokens(desc, params, dc.K[0], dc.table, dc.lens, first, S, F, scores)
+    k = (N_max - 1) * b
+    keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
+    S2 = torch.from_numpy(S0.copy()).cuda()
+    targets = c.block_table[:, : N_max - 1].contiguous().cuda()
+    zp.zp_compress_layers(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, first, S2, F, targets, k, keep, Lmax)
+    torch.cuda.synchronize()
+    assert zp.zp_device_status() == (0, 0)
+    got = scores.cpu().numpy()
+    K0 = c.k_cache[0].float().numpy()
+    V0 = c.v_cache[0].float().numpy()
+    Kg, Vg = dc.K[0].float().cpu().numpy(), dc.V[0].float().cpu().numpy()
+    kept = keep.cpu().numpy()
+    swaps, fired = 0, 0
+    for s, L in enumerate(lens):
+        Fref = np.zeros((c.n_total, b, h_kv))
+        sref = pipeline.final_scores(S0[s, :, :L].astype(np.float64), K0, Fref, c.block_table[s].numpy(), L, b,
+                                     True, prm)
+        fin = np.isfinite(sref)
+        np.testing.assert_allclose(got[s, :, :L][fin], sref[fin], **TOL_SCORE["bf16"])
+        for h in range(h_kv):
+            swaps += keep_sets_match(kept[s, h], oracle.topk_keep(sref[h], k)[0], sref[h], k, L)
+            for r in range(0, k, 7):
+                pos = kept[s, h, r]
+                sb, ss = c.block_table[s, pos // b], pos % b
+                db, ds = c.block_table[s, r // b], r % b
+                assert np.array_equal(Kg[db, ds, h], K0[sb, ss, h])
+                assert np.array_equal(Vg[db, ds, h], V0[sb, ss, h])
+        keys = pipeline.gather_rows(K0, c.block_table[s].numpy(), L, b)[:, 0].astype(np.float64)
+        n = np.linalg.norm(keys, axis=1)
+        cosm = (keys @ keys.T) / np.outer(n, n)
+        np.fill_diagonal(cosm, 0)
+        fired += int((cosm > 0.9).any(axis=0).sum())
+    assert fired > 50  # the zeroing rule acted on many columns
+    print("reported near-tie swaps:", swaps, "columns with a zeroed entry (head 0):", fired)
