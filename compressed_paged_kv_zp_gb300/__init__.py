@@ -106,12 +106,12 @@ def _load() -> ctypes.CDLL:
     lib.zp_window_score.argtypes = [D, P, I32, P, P, I32, P, I32, P, I32, P, SZ, P]
     lib.zp_score_tokens.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I32, P, P, I32, P, P, P,
                                     I32, P, SZ, P]
-    lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P]
-    lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, P, I32, P, I32, P, P, I32, I32, P]
+    lib.zp_select_topk.argtypes = [P, I32, I32, P, I32, I32, P, P, P, P]
+    lib.zp_compact_pages.argtypes = [D, P, P, I64, I32, P, I64, P, P, I32, P, I32, P, P, I32, P, I32, P]
     lib.zp_compress_workspace_size.restype = SZ
     lib.zp_compress_workspace_size.argtypes = [D, I32, I32, I32]
     lib.zp_compress_layers.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P, P,
-                                       I64, P, I32, I32, P, P, P, I32, P, SZ, P]
+                                       I64, P, I32, I32, P, P, P, P, I32, P, SZ, P]
     lib.zp_pool_create.restype = P
     lib.zp_pool_create.argtypes = [I32]
     lib.zp_pool_destroy.argtypes = [P]
@@ -121,7 +121,7 @@ def _load() -> ctypes.CDLL:
     lib.zp_pool_incref.argtypes = [P, I32, P]
     lib.zp_pool_release.argtypes = [P, I32, P]
     lib.zp_plan_compaction.argtypes = [P, P, I32, I32, P, P, P, P, P]
-    lib.zp_plan_compaction_batch.argtypes = [P, P, I32, P, I32, I32, P, P, P, P, P]
+    lib.zp_plan_compaction_batch.argtypes = [P, P, I32, P, I32, I32, P, P, P, P, P, P]
     lib.zp_plan_capacity.argtypes = [I64, I64, I64, I32, I64, I64, P, P]
     return lib
 
@@ -246,16 +246,18 @@ def zp_score_tokens(desc, params: ScoreParams, k_cache, block_table, seq_lens, f
                                workspace.numel(), _stream(stream)))
 
 
-def zp_select_topk(scores, seq_lens, k, keep_idx, tie_count=None, stream=None) -> None:
+def zp_select_topk(scores, seq_lens, k, keep_idx, tie_count=None, k_seq=None, stream=None) -> None:
+    """k_seq: optional int32 [n] device array of per-request budgets k_i <= k;
+    keep_idx rows keep stride k and are padded with -1 after k_i."""
     n, h_kv, Lmax = (int(x) for x in scores.shape)
     _check(lib.zp_select_topk(_dev(scores, "scores"), h_kv, Lmax, _dev(seq_lens, "seq_lens"), n,
-                              int(k), _dev(keep_idx, "keep_idx"), _dev(tie_count, "tie_count"),
-                              _stream(stream)))
+                              int(k), _dev(k_seq, "k_seq"), _dev(keep_idx, "keep_idx"),
+                              _dev(tie_count, "tie_count"), _stream(stream)))
 
 
 def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, F_layer_stride,
                      src_table, dst_targets, seq_lens, keep_idx, k, scores=None, rows=None,
-                     stream=None) -> None:
+                     k_seq=None, stream=None) -> None:
     """scores/rows: the score rows zp_score_tokens left (float32 [R][h_kv][stride],
     or [layers][R][h_kv][stride] for several layers); needed when global_F is set."""
     n, table_stride = int(src_table.shape[0]), int(src_table.shape[1])
@@ -264,8 +266,8 @@ def zp_compact_pages(desc, k_base, v_base, layer_stride, layer_count, global_F, 
                                 int(F_layer_stride), _score_rows(scores, rows),
                                 _dev(src_table, "src_table"), table_stride,
                                 _dev(dst_targets, "dst_targets"), int(dst_targets.shape[1]),
-                                _dev(seq_lens, "seq_lens"), _dev(keep_idx, "keep_idx"), int(k), n,
-                                _stream(stream)))
+                                _dev(seq_lens, "seq_lens"), _dev(keep_idx, "keep_idx"), int(k),
+                                _dev(k_seq, "k_seq"), n, _stream(stream)))
 
 
 def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int, layer_count: int = 1) -> int:
@@ -274,11 +276,12 @@ def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int, layer_count: 
 
 def zp_compress_layers(desc, params: ScoreParams, k_cache, v_cache, block_table, seq_lens, first_compression,
                        attn, global_F, dst_targets, k, keep_idx, Lmax, rows=None, tie_count=None, scores_out=None,
-                       workspace=None, stream=None) -> None:
+                       workspace=None, k_seq=None, stream=None) -> None:
     """Scores, keep sets and moves of one or several layers in one call.
     k_cache/v_cache: one layer [N_total][b][h_kv][d] or several
     [layers][N_total][b][h_kv][d]; global_F and attn (score rows) alike;
-    keep_idx int32 [layers][n][h_kv][k] (or [n][h_kv][k] for one layer)."""
+    keep_idx int32 [layers][n][h_kv][k] (or [n][h_kv][k] for one layer);
+    k_seq: optional int32 [n] device array of per-request budgets k_i <= k."""
     n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
     layers = int(k_cache.shape[0]) if k_cache.dim() == 5 else 1
     layer_stride = int(k_cache.stride(0)) if layers > 1 else 0
@@ -293,7 +296,8 @@ def zp_compress_layers(desc, params: ScoreParams, k_cache, v_cache, block_table,
                                   table_stride, _dev(seq_lens, "seq_lens"),
                                   _dev(first_compression, "first_compression"), n, _score_rows(attn, rows),
                                   _dev(global_F, "global_F"), F_layer, _dev(dst_targets, "dst_targets"),
-                                  int(dst_targets.shape[1]), int(k), _dev(keep_idx, "keep_idx"),
+                                  int(dst_targets.shape[1]), int(k), _dev(k_seq, "k_seq"),
+                                  _dev(keep_idx, "keep_idx"),
                                   _dev(tie_count, "tie_count"), _dev(scores_out, "scores_out"), int(Lmax),
                                   _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
 
@@ -368,11 +372,13 @@ class Pool:
         return {"targets": list(targets)[: max_blocks - 1], "new_table": list(new_table)[:max_blocks],
                 "dropped": list(dropped)[: nd.value], "n_fresh": nf.value}
 
-    def plan_compaction_batch(self, tables, n_blocks, max_blocks: int, out=None):
+    def plan_compaction_batch(self, tables, n_blocks, max_blocks: int, out=None, max_blocks_seq=None):
         """Plans of n sequences in one C call; tables int32 [n][stride] and
-        n_blocks int32 [n] as numpy arrays.  Returns numpy arrays (reused from
-        ``out`` when given): targets [n][max_blocks-1], new_tables
-        [n][max_blocks], dropped [n][stride], n_dropped [n], n_fresh [n]."""
+        n_blocks int32 [n] as numpy arrays; max_blocks_seq: optional int32 [n]
+        per-request block budgets in [2, max_blocks] (rows padded with -1).
+        Returns numpy arrays (reused from ``out`` when given): targets
+        [n][max_blocks-1], new_tables [n][max_blocks], dropped [n][stride],
+        n_dropped [n], n_fresh [n]."""
         import numpy as np
         tables = np.ascontiguousarray(tables, dtype=np.int32)
         n_blocks = np.ascontiguousarray(n_blocks, dtype=np.int32)
@@ -383,8 +389,13 @@ class Pool:
                    "dropped": np.empty((n, stride), np.int32), "n_dropped": np.empty(n, np.int32),
                    "n_fresh": np.empty(n, np.int32)}
         P = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        mbs = None
+        if max_blocks_seq is not None:
+            mbs = np.ascontiguousarray(max_blocks_seq, dtype=np.int32)
+            if mbs.shape != (n,):
+                raise ValueError("max_blocks_seq must have one entry per sequence")
         _check(lib.zp_plan_compaction_batch(self._p, P(tables), stride, P(n_blocks), n, int(max_blocks),
-                                            P(out["targets"]), P(out["new_tables"]), P(out["dropped"]),
+                                            None if mbs is None else P(mbs), P(out["targets"]), P(out["new_tables"]), P(out["dropped"]),
                                             P(out["n_dropped"]), P(out["n_fresh"])))
         return out
 

@@ -39,6 +39,7 @@ struct CompactArgs {
     int target_stride;
     const int32_t *seq_lens;
     const int32_t *keep;
+    const int32_t *k_seq;  // nullable: per-request budgets
     int k, n, h_kv, b, n_total;
     int row_vec;  // vectors per (token, kv head) row = d * elem / 16
     int chunk;    // ranks per round: min(kChunkMax, kThreads * kMaxVecPerThread / (2 * row_vec))
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
         }
     }
     if (F && L > a.S_stride) L = (int)a.S_stride;
-    const int kk = min(a.k, L);
+    const int kk = min(a.k_seq ? min(a.k_seq[s], a.k) : a.k, L);
     const int per_rank = 2 * a.row_vec;  // K then V vectors
     for (int r0 = 0; r0 < kk; r0 += a.chunk) {
         const int nr = min(a.chunk, kk - r0);
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kVThreads) compact_vec_kernel(const CompactArg
             if (L > a.S_stride) L = (int)a.S_stride;
         }
     }
-    const int kk = min(a.k, L);
+    const int kk = min(a.k_seq ? min(a.k_seq[s], a.k) : a.k, L);
     // ---- round 2: source blocks and F values of every rank
     for (int r = tid; r < kk; r += blockDim.x) {
         const int pos = pos_s[r];
@@ -250,7 +251,8 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
                                       const int32_t *src_table,
                                       int32_t table_stride, const int32_t *dst_targets,
                                       int32_t target_stride, const int32_t *seq_lens,
-                                      const int32_t *keep_idx, int32_t k, int32_t n, void *stream) {
+                                      const int32_t *keep_idx, int32_t k, const int32_t *k_seq, int32_t n,
+                                      void *stream) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (n < 0 || k < 0 || layer_count < 0 || table_stride < 1 || target_stride < 1)
@@ -293,6 +295,7 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     a.target_stride = target_stride;
     a.seq_lens = seq_lens;
     a.keep = keep_idx;
+    a.k_seq = k_seq;
     a.k = k;
     a.n = n;
     a.h_kv = D->h_kv;

@@ -128,8 +128,9 @@ extern "C" zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int
 
 extern "C" zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tables, int32_t table_stride,
                                               const int32_t *n_blocks, int32_t n, int32_t max_blocks,
-                                              int32_t *targets, int32_t *new_tables, int32_t *dropped,
-                                              int32_t *n_dropped, int32_t *n_fresh) {
+                                              const int32_t *max_blocks_seq, int32_t *targets,
+                                              int32_t *new_tables, int32_t *dropped, int32_t *n_dropped,
+                                              int32_t *n_fresh) {
     if (!pool || n < 0 || (n > 0 && (!tables || !n_blocks || !targets || !new_tables || !dropped ||
                                      !n_dropped || !n_fresh)))
         return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: NULL argument");
@@ -140,11 +141,17 @@ extern "C" zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tabl
         if (n_blocks[i] > table_stride)
             return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: sequence %d has %d > %d blocks", i,
                         n_blocks[i], table_stride);
-        zp_status rc = zp_plan_compaction(pool, tables + (size_t)i * table_stride, n_blocks[i], max_blocks,
-                                          targets + (size_t)i * (max_blocks - 1),
-                                          new_tables + (size_t)i * max_blocks,
+        const int32_t mb = max_blocks_seq ? max_blocks_seq[i] : max_blocks;
+        if (mb < 2 || mb > max_blocks)
+            return fail(ZP_ERR_INVALID_ARG, "plan_compaction_batch: sequence %d budget %d outside [2, %d]", i, mb,
+                        max_blocks);
+        int32_t *tg = targets + (size_t)i * (max_blocks - 1);
+        int32_t *nt = new_tables + (size_t)i * max_blocks;
+        zp_status rc = zp_plan_compaction(pool, tables + (size_t)i * table_stride, n_blocks[i], mb, tg, nt,
                                           dropped + (size_t)i * table_stride, &n_dropped[i], &n_fresh[i]);
         if (rc != ZP_OK) return rc;  // sequences before i stay planned
+        for (int32_t t = mb - 1; t < max_blocks - 1; ++t) tg[t] = -1;
+        for (int32_t t = mb; t < max_blocks; ++t) nt[t] = -1;
     }
     return ok();
 }

@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const Scor
     const int rA = r0 + warp * 16 + g, rB = rA + 8;
     float sumA = 0.f, sumB = 0.f, valA = 0.f, valB = 0.f;
     int maxA = -1, maxB = -1;
-    float irA = 0.f, irB = 0.f;
+    float irA = 0.f, irB = 0.f, pA = 0.f, pB = 0.f;
     for (int cc = 0; cc < ncol; ++cc) {
         const int buf = cc & 1;
         if (cc + 1 < ncol)  // the other buffer was released by the barrier that ended step cc - 1
@@ -559,6 +559,8 @@ __global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const Scor
         if (cc == 0) {
             irA = inv_r[warp * 16 + g];
             irB = inv_r[warp * 16 + g + 8];
+            pA = irA > 0.f ? a.p / irA : (a.p < 0.f ? -INFINITY : INFINITY);
+            pB = irB > 0.f ? a.p / irB : (a.p < 0.f ? -INFINITY : INFINITY);
         }
         float acc[kFrCols / 8][4];
 #pragma unroll
@@ -579,26 +581,49 @@ __global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const Scor
                 mma_16816(acc[2 * j2 + 1], a0, a1, a2, a3, b1, b3);
             }
         }
-        // lane holds rows rA (acc[j][0..1]) and rB (acc[j][2..3]), columns j*8 + 2tig + {0,1}
+        // lane holds rows rA (acc[j][0..1]) and rB (acc[j][2..3]), columns j*8 + 2tig + {0,1}.
+        // x = acc * inv_norm(col) is the cosine divided by inv_norm(row): the row
+        // factor is applied once to the sum, and the threshold p to x compares as
+        // p / inv_norm(row) (a zero-norm row has cosine 0 with everything).
         const float *ic = inv_c + buf * kFrCols;
         const int c0 = cc * kFrCols;
+        const bool interior = c0 + kFrCols <= L && (c0 >= r0 + kFrRows || c0 + kFrCols <= r0);
+        if (interior) {
+            float2 sA2 = make_float2(0.f, 0.f), sB2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kFrCols / 8; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int col = c0 + j * 8 + 2 * tig + e;
-                const float icv = ic[j * 8 + 2 * tig + e];
-                const bool cv = col < L;
-                const float xa = acc[j][e] * irA * icv, xb = acc[j][2 + e] * irB * icv;
-                if (cv && col != rA) {
-                    sumA += xa;
-                    if (xa > a.p) maxA = col, valA = xa;
-                }
-                if (cv && col != rB) {
-                    sumB += xb;
-                    if (xb > a.p) maxB = col, valB = xb;
-                }
+            for (int j = 0; j < kFrCols / 8; ++j) {
+                const float2 icv = *reinterpret_cast<const float2 *>(ic + j * 8 + 2 * tig);
+                const float2 xa = fmul2(make_float2(acc[j][0], acc[j][1]), icv);
+                const float2 xb = fmul2(make_float2(acc[j][2], acc[j][3]), icv);
+                sA2 = ffma2(make_float2(1.f, 1.f), xa, sA2);
+                sB2 = ffma2(make_float2(1.f, 1.f), xb, sB2);
+                const int col = c0 + j * 8 + 2 * tig;
+                if (xa.x > pA) maxA = col, valA = xa.x;
+                if (xa.y > pA) maxA = col + 1, valA = xa.y;
+                if (xb.x > pB) maxB = col, valB = xb.x;
+                if (xb.y > pB) maxB = col + 1, valB = xb.y;
             }
+            sumA += sA2.x + sA2.y;
+            sumB += sB2.x + sB2.y;
+        } else {
+#pragma unroll
+            for (int j = 0; j < kFrCols / 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = c0 + j * 8 + 2 * tig + e;
+                    const float icv = ic[j * 8 + 2 * tig + e];
+                    const bool cv = col < L;
+                    const float xa = acc[j][e] * icv, xb = acc[j][2 + e] * icv;
+                    if (cv && col != rA) {
+                        sumA += xa;
+                        if (xa > pA) maxA = col, valA = xa;
+                    }
+                    if (cv && col != rB) {
+                        sumB += xb;
+                        if (xb > pB) maxB = col, valB = xb;
+                    }
+                }
+        }
         __syncthreads();  // buffer `buf` is refilled by the next step's prefetch
     }
     // the four lanes of a row: sums add, the largest index above p wins
@@ -611,15 +636,15 @@ __global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const Scor
         if (mA > maxA) maxA = mA, valA = vA;
         if (mB > maxB) maxB = mB, valB = vB;
     }
-    if (tig == 0) {
+    if (tig == 0) {  // back to cosines: times inv_norm(row)
         float *rho = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax;
         if (rA < L) {
-            atomicAdd(rho + rA, sumA);
-            if (maxA >= 0) atomicAdd(rho + maxA, -valA);
+            atomicAdd(rho + rA, sumA * irA);
+            if (maxA >= 0) atomicAdd(rho + maxA, -valA * irA);
         }
         if (rB < L) {
-            atomicAdd(rho + rB, sumB);
-            if (maxB >= 0) atomicAdd(rho + maxB, -valB);
+            atomicAdd(rho + rB, sumB * irB);
+            if (maxB >= 0) atomicAdd(rho + maxB, -valB * irB);
         }
     }
 }
@@ -697,7 +722,8 @@ struct MoveArgs {
     int row_vec;         // 16-byte vectors per (token, kv head) row
     const int32_t *dst;  // [n][target_stride]
     int target_stride;
-    int k;
+    int k;               // row stride of keep (the largest budget)
+    const int32_t *k_seq;  // nullable: per-request budgets k_i <= k
     int32_t *keep;       // [n][h_kv][k]
     int32_t *tie;        // nullable [n][h_kv]
     float *F;            // nullable, paged
@@ -784,20 +810,26 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
         if (a.out) a.out[row + t] = v;
     }
     __syncthreads();
-    // ---- keep set
+    // ---- keep set (this request's budget ki; the row is padded with -1)
     int32_t *kout = m.keep + ((size_t)s * a.h_kv + kvh) * m.k;
-    if (L <= m.k) {
-        for (int i = tid; i < m.k; i += nthr) {
+    int ki = m.k_seq ? m.k_seq[s] : m.k;
+    if (ki < 0 || ki > m.k) {
+        if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x302);
+        ki = ki < 0 ? 0 : m.k;
+    }
+    for (int i = ki + tid; i < m.k; i += nthr) kout[i] = -1;
+    if (L <= ki) {
+        for (int i = tid; i < ki; i += nthr) {
             keep_s[i] = i < L ? i : -1;
             kout[i] = i < L ? i : -1;
         }
         if (m.tie && tid == 0) m.tie[(size_t)s * a.h_kv + kvh] = 0;
         __syncthreads();
     } else {
-        block_select_topk(fs, L, m.k, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
+        block_select_topk(fs, L, ki, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
     }
     // ---- move this kv head's kept rows (Alg. 4 with the target blocks)
-    const int kk = min(m.k, L);
+    const int kk = min(ki, L);
     const float *Srow = nullptr;
     float *F = m.F;
     if (F) {
@@ -1046,21 +1078,14 @@ extern "C" size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, 
     return (size_t)layer_count * zp_score_workspace_size(D, n, Lmax);
 }
 
-extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base, int64_t layer_stride,
-                                      int32_t layer_count, float *global_F, int64_t F_layer_stride,
-                                      const zp_score_rows *scores, const int32_t *src_table,
-                                      int32_t table_stride, const int32_t *dst_targets, int32_t target_stride,
-                                      const int32_t *seq_lens, const int32_t *keep_idx, int32_t k, int32_t n,
-                                      void *stream);
-extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const int32_t *seq_lens,
-                                    int32_t n, int32_t k, int32_t *keep_idx, int32_t *tie_count, void *stream);
 
 extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
                                         void *v_base, int64_t layer_stride, int32_t layer_count,
                                         const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
                                         const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
                                         float *global_F, int64_t F_layer_stride, const int32_t *dst_targets,
-                                        int32_t target_stride, int32_t k, int32_t *keep_idx, int32_t *tie_count,
+                                        int32_t target_stride, int32_t k, const int32_t *k_seq,
+                                        int32_t *keep_idx, int32_t *tie_count,
                                         float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
                                         void *stream) {
     zp_status rc = check_desc(D);
@@ -1106,6 +1131,7 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         m.dst = dst_targets;
         m.target_stride = target_stride;
         m.k = k;
+        m.k_seq = k_seq;
         m.keep = keep_idx;
         m.tie = tie_count;
         m.F = global_F;
@@ -1144,11 +1170,11 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         finalize_kernel<<<dim3(a.h_kv, n), 1024, 0, st>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "compress: finalize launch");
-        rc = zp_select_topk(a.out, a.h_kv, Lmax, seq_lens, n, k, keep_idx + l * keep_layer,
+        rc = zp_select_topk(a.out, a.h_kv, Lmax, seq_lens, n, k, k_seq, keep_idx + l * keep_layer,
                             tie_count ? tie_count + (size_t)l * n * D->h_kv : nullptr, stream);
         if (rc != ZP_OK) return rc;
         rc = zp_compact_pages(D, kl, vl, 0, 1, Fl, 0, &at, block_table, table_stride, dst_targets, target_stride,
-                              seq_lens, keep_idx + l * keep_layer, k, n, stream);
+                              seq_lens, keep_idx + l * keep_layer, k, k_seq, n, stream);
         if (rc != ZP_OK) return rc;
     }
     return ok();

@@ -22,8 +22,8 @@ constexpr int kSmemRow = 32768;
 
 template <bool STAGED>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int h_kv, int Lmax,
-                                                        const int32_t *seq_lens, int k, int32_t *keep,
-                                                        int32_t *tie_count, unsigned *err) {
+                                                        const int32_t *seq_lens, int k, const int32_t *k_seq,
+                                                        int32_t *keep, int32_t *tie_count, unsigned *err) {
     extern __shared__ float srow[];
     __shared__ SelectShared sh;
     const int kvh = blockIdx.x;
@@ -33,9 +33,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
     if (L < 0) L = 0;
     if (L > Lmax) L = Lmax;
     const float *sc = scores + ((size_t)s * h_kv + kvh) * Lmax;
-    int32_t *out = keep + ((size_t)s * h_kv + kvh) * k;
-    if (L <= k) {
-        for (int r = tid; r < k; r += blockDim.x) out[r] = r < L ? r : -1;
+    int32_t *out = keep + ((size_t)s * h_kv + kvh) * k;  // row stride k
+    int ki = k_seq ? k_seq[s] : k;                       // this request's budget
+    if (ki < 0 || ki > k) {
+        if (tid == 0) record_error(err, ZP_ERR_DEVICE, 0x302);
+        ki = ki < 0 ? 0 : k;
+    }
+    for (int r = ki + tid; r < k; r += blockDim.x) out[r] = -1;
+    if (L <= ki) {
+        for (int r = tid; r < ki; r += blockDim.x) out[r] = r < L ? r : -1;
         if (tie_count && tid == 0) tie_count[(size_t)s * h_kv + kvh] = 0;
         return;
     }
@@ -44,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
         __syncthreads();
         sc = srow;
     }
-    block_select_topk(sc, L, k, out, nullptr, tie_count ? tie_count + (size_t)s * h_kv + kvh : nullptr, err, sh);
+    block_select_topk(sc, L, ki, out, nullptr, tie_count ? tie_count + (size_t)s * h_kv + kvh : nullptr, err, sh);
 }
 
 }  // namespace
@@ -53,8 +59,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
 using namespace zp;
 
 extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax,
-                                    const int32_t *seq_lens, int32_t n, int32_t k, int32_t *keep_idx,
-                                    int32_t *tie_count, void *stream) {
+                                    const int32_t *seq_lens, int32_t n, int32_t k, const int32_t *k_seq,
+                                    int32_t *keep_idx, int32_t *tie_count, void *stream) {
     if (n < 0 || h_kv <= 0 || Lmax < 0 || k < 0) return fail(ZP_ERR_INVALID_ARG, "topk: bad sizes");
     if (n == 0 || k == 0) return ok();
     if (!scores || !seq_lens || !keep_idx) return fail(ZP_ERR_INVALID_ARG, "topk: NULL buffer");
@@ -70,10 +76,10 @@ extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t L
                                                  (int)smem);
             if (e != cudaSuccess) return cuda_fail(e, "topk: cudaFuncSetAttribute");
         }
-        topk_kernel<true><<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, keep_idx, tie_count,
+        topk_kernel<true><<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count,
                                                         dev.error_word);
     } else {
-        topk_kernel<false><<<grid, kThreads, 0, st>>>(scores, h_kv, Lmax, seq_lens, k, keep_idx, tie_count,
+        topk_kernel<false><<<grid, kThreads, 0, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count,
                                                       dev.error_word);
     }
     cudaError_t e = cudaGetLastError();

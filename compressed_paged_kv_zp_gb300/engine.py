@@ -3,7 +3,8 @@
 The host side of the hot path around the libzp kernels:
   * block allocation as sequences grow (Zipage paper §3);
   * the compression trigger after every step: N >= N_max blocks and the last
-    block full (§4.1);
+    block full (§4.1), with N_max optionally set per request (a budget of its
+    own, at most the loop's N_max);
   * target blocks from the reference-counted pool, one planner call for all
     triggered sequences (§4.4);
   * scoring, top-k and compaction on a side stream, ordered after the decode
@@ -52,13 +53,22 @@ class DecodeLoop:
         self.pending = []  # (event, seqs, plan) of compressions in flight
 
     # ------------------------------------------------------------------ setup
-    def add_sequences(self, lens, tables=None):
+    def add_sequences(self, lens, tables=None, max_blocks=None):
         """Register B sequences with `lens` cached tokens.  Their blocks come
         from the pool (lowest ids first) unless `tables` (np int32 [B][stride],
         already holding the sequences' block ids) is given; the caller fills
-        the cache rows of those tokens directly (prefill is out of scope)."""
+        the cache rows of those tokens directly (prefill is out of scope).
+        max_blocks: optional per-request block budgets N_i in [2, N_max]; a
+        request then compresses at N_i blocks to (N_i - 1) b tokens."""
         lens = np.asarray(lens, dtype=np.int32)
         B = len(lens)
+        if max_blocks is None:
+            self.N_seq = np.full(B, self.N_max, dtype=np.int32)
+        else:
+            self.N_seq = np.asarray(max_blocks, dtype=np.int32).copy()
+            if self.N_seq.shape != (B,) or self.N_seq.min() < 2 or self.N_seq.max() > self.N_max:
+                raise ValueError("max_blocks: one budget in [2, N_max] per sequence")
+        self.uniform = bool((self.N_seq == self.N_max).all())
         self.B = B
         self.lens = lens.copy()
         self.table = np.full((B, self.stride), -1, dtype=np.int32)
@@ -122,7 +132,7 @@ class DecodeLoop:
             zp_paged_decode_attn(self.desc, q[l], self.K[l], self.V[l], self.table_dev, step_lens, self.out[l],
                                  score_accum=self.S[l], window=self.window, workspace=self.ws)
         L = self.lens
-        trig = np.nonzero(act & ((L + self.b - 1) // self.b >= self.N_max) & (L % self.b == 0))[0]
+        trig = np.nonzero(act & ((L + self.b - 1) // self.b >= self.N_seq) & (L % self.b == 0))[0]
         if len(trig):
             self._compress(trig.astype(np.int64), main)
         return trig.tolist()
@@ -131,7 +141,9 @@ class DecodeLoop:
         n = len(seqs)
         nb = (self.lens[seqs] // self.b).astype(np.int32)
         sub_tables = np.ascontiguousarray(self.table[seqs])
-        plan = self.pool.plan_compaction_batch(sub_tables, nb, self.N_max)
+        plan = self.pool.plan_compaction_batch(sub_tables, nb, self.N_max,
+                                               max_blocks_seq=None if self.uniform else self.N_seq[seqs])
+        k_seq = None if self.uniform else torch.from_numpy((self.N_seq[seqs] - 1) * self.b).to(self.dev)
         tables_dev = torch.from_numpy(sub_tables).to(self.dev)
         lens_dev = torch.from_numpy(self.lens[seqs].astype(np.int32)).to(self.dev)
         first_dev = torch.from_numpy(self.first[seqs].copy()).to(self.dev)
@@ -146,10 +158,10 @@ class DecodeLoop:
                 l1 = min(l0 + self.layer_stride, self.layers)
                 zp_compress_layers(self.desc, self.params, self.K[l0:l1], self.V[l0:l1], tables_dev, lens_dev,
                                    first_dev, self.S[l0:l1], self.F[l0:l1], targets_dev, self.k, keep[l0:l1],
-                                   self.Lmax, rows=rows_dev, workspace=self.score_ws)
+                                   self.Lmax, rows=rows_dev, workspace=self.score_ws, k_seq=k_seq)
             done = torch.cuda.Event()
             done.record(self.side)
-        for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev):
+        for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev) + ((k_seq,) if k_seq is not None else ()):
             t.record_stream(self.side)
         self.active[seqs] = False
         self.last_keep = (seqs, keep)  # for inspection: [layers][n][h_kv][k]
@@ -171,7 +183,7 @@ class DecodeLoop:
             for i, s in enumerate(seqs):
                 self.table[s, :] = -1
                 self.table[s, : self.N_max] = plan["new_tables"][i]
-                self.lens[s] = self.k
+                self.lens[s] = (int(self.N_seq[s]) - 1) * self.b
                 self.first[s] = 0
                 self.active[s] = True
                 nd = int(plan["n_dropped"][i])

@@ -222,9 +222,12 @@ zp_status zp_score_tokens(const zp_cache_desc *D, const zp_score_params *P,
  * kept positions are written ascending to keep_idx [n][h_kv][k].  If L <= k all
  * L positions are kept and keep_idx[L..k-1] = -1.  tie_count (nullable, int32
  * [n][h_kv]) receives how many tokens share the score of the k-th kept token
- * when that score was split between kept and dropped tokens, else 0. */
+ * when that score was split between kept and dropped tokens, else 0.
+ * Per-request budgets (Zipage, Limitations: N_max as an attribute of each request): k_seq
+ * (nullable, device int32 [n]) gives sequence i its own k_i <= k; keep_idx
+ * keeps the row stride k and rows are padded with -1 after k_i. */
 zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const int32_t *seq_lens,
-                         int32_t n, int32_t k, int32_t *keep_idx, int32_t *tie_count,
+                         int32_t n, int32_t k, const int32_t *k_seq, int32_t *keep_idx, int32_t *tie_count,
                          void *stream);
 
 /* KV compaction [Zipage App. C.6, Alg. 4; §4.4 target blocks]: for layers
@@ -238,13 +241,14 @@ zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t Lmax, const 
  * `scores` left by zp_score_tokens ("compress score"); F is written only in
  * the target blocks.  src_table [n][table_stride], dst_targets
  * [n][target_stride] (at least ceil(k/b) entries), keep_idx
- * [layer_count][n][h_kv][k], seq_lens [n]. */
+ * [layer_count][n][h_kv][k], seq_lens [n]; k_seq (nullable, device int32 [n])
+ * moves min(k_seq[i], L_i) ranks of sequence i (its own budget, <= k). */
 zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
                            int64_t layer_stride, int32_t layer_count, float *global_F,
                            int64_t F_layer_stride, const zp_score_rows *scores,
                            const int32_t *src_table, int32_t table_stride,
                            const int32_t *dst_targets, int32_t target_stride,
-                           const int32_t *seq_lens, const int32_t *keep_idx, int32_t k,
+                           const int32_t *seq_lens, const int32_t *keep_idx, int32_t k, const int32_t *k_seq,
                            int32_t n, void *stream);
 
 /* Compression of n sequences over layer_count layers in one call [Zipage
@@ -262,13 +266,16 @@ zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
  * finishes the scores, selects the keep set and moves the rows from shared
  * memory (while 8*Lmax + 12*k bytes fit in it); otherwise the three steps run
  * layer by layer.  The workspace (zp_compress_workspace_size) grows with
- * layer_count: the paper's layer stride is the number of layers per call. */
+ * layer_count: the paper's layer stride is the number of layers per call.
+ * k_seq (nullable, device int32 [n]): per-request budgets k_i <= k, as in
+ * zp_select_topk. */
 size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax, int32_t layer_count);
 zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
                              int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
                              int32_t table_stride, const int32_t *seq_lens, const uint8_t *first_compression,
                              int32_t n, const zp_score_rows *attn, float *global_F, int64_t F_layer_stride,
-                             const int32_t *dst_targets, int32_t target_stride, int32_t k, int32_t *keep_idx,
+                             const int32_t *dst_targets, int32_t target_stride, int32_t k,
+                             const int32_t *k_seq, int32_t *keep_idx,
                              int32_t *tie_count, float *scores_out, int32_t Lmax, void *workspace,
                              size_t workspace_bytes, void *stream);
 
@@ -303,12 +310,14 @@ zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int32_t n_bloc
 /* zp_plan_compaction for n sequences in one call.  tables [n][table_stride]
  * (sequence i holds n_blocks[i] <= table_stride blocks); outputs per sequence:
  * targets [n][max_blocks-1], new_tables [n][max_blocks], dropped
- * [n][table_stride] (first n_dropped[i] valid), n_fresh [n].  Stops at the
+ * [n][table_stride] (first n_dropped[i] valid), n_fresh [n].  max_blocks_seq
+ * (nullable, host int32 [n]): per-request budgets N_max,i <= max_blocks (rows
+ * padded with -1 after N_max,i - 1 targets and N_max,i blocks).  Stops at the
  * first sequence that fails (earlier ones stay planned) and returns its error. */
 zp_status zp_plan_compaction_batch(zp_pool *pool, const int32_t *tables, int32_t table_stride,
                                    const int32_t *n_blocks, int32_t n, int32_t max_blocks,
-                                   int32_t *targets, int32_t *new_tables, int32_t *dropped,
-                                   int32_t *n_dropped, int32_t *n_fresh);
+                                   const int32_t *max_blocks_seq, int32_t *targets, int32_t *new_tables,
+                                   int32_t *dropped, int32_t *n_dropped, int32_t *n_fresh);
 
 /* Capacity plan [Zipage §4.2 eq. (1), App. C.3 eq. (2)] (host only): the
  * largest request concurrency M and the block count N_total for a memory

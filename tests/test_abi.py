@@ -106,16 +106,16 @@ def test_invalid_arguments_rejected_without_device(zp):
     rc = zp.lib.zp_append_kv(ctypes.byref(desc), None, None, None, None, None, 1, None, 1, None)
     assert rc == 2
     desc = zp.cache_desc(8, 2, 64, 16, 10, 9)  # bad dtype
-    rc = zp.lib.zp_select_topk(None, 2, 4, None, 1, 2, None, None, None)
+    rc = zp.lib.zp_select_topk(None, 2, 4, None, 1, 2, None, None, None, None)
     assert rc == 1
     rc = zp.lib.zp_compact_pages(ctypes.byref(desc), None, None, 0, 1, None, 0, None, None, 1, None, 1,
-                                 None, None, 4, 1, None)
+                                 None, None, 4, None, 1, None)
     assert rc == 3
     # global_F without the score rows it is written from
     desc = zp.cache_desc(8, 2, 64, 16, 10, 0)
     one = ctypes.c_void_p(16)  # never dereferenced: the call fails its argument checks first
     rc = zp.lib.zp_compact_pages(ctypes.byref(desc), one, one, 0, 1, one, 0, None, one, 1, one, 1,
-                                 one, one, 4, 1, None)
+                                 one, one, 4, None, 1, None)
     assert rc == 1
     # score_tokens without attention-score rows
     rc = zp.lib.zp_score_tokens(ctypes.byref(desc), ctypes.byref(zp.score_params()), one, one, 1, one, one, 1,
@@ -145,6 +145,42 @@ def test_batch_planner_matches_single_calls(zp):
         assert list(batch["dropped"][i, :batch["n_dropped"][i]]) == sp["dropped"]
         assert batch["n_fresh"][i] == sp["n_fresh"]
     assert pools[0].num_free == pools[1].num_free
+
+
+def test_batch_planner_per_request_budgets(zp):
+    """Per-request block budgets: each row equals a single plan with that
+    sequence's own budget, padded with -1 up to the batch's largest budget;
+    a budget outside [2, max_blocks] is refused."""
+    import numpy as np
+    rng = np.random.default_rng(12)
+    pools = [zp.Pool(500), zp.Pool(500)]
+    n, stride, N_max = 7, 14, 8
+    mb = rng.integers(2, N_max + 1, size=n).astype(np.int32)
+    mb[0], mb[1] = 2, N_max
+    tables = np.full((n, stride), -1, np.int32)
+    nb = np.array([rng.integers(int(m), stride + 1) for m in mb], np.int32)
+    for pool in pools:
+        prefix = pool.alloc(2)
+        for _ in range(n - 1):
+            pool.incref(prefix)
+        for i in range(n):
+            tables[i, :2] = prefix
+            tables[i, 2:nb[i]] = pool.alloc(int(nb[i]) - 2)
+    singles = [pools[0].plan_compaction(tables[i, :nb[i]].tolist(), int(mb[i])) for i in range(n)]
+    batch = pools[1].plan_compaction_batch(tables, nb, N_max, max_blocks_seq=mb)
+    for i, sp in enumerate(singles):
+        m = int(mb[i])
+        assert list(batch["targets"][i, :m - 1]) == sp["targets"]
+        assert (batch["targets"][i, m - 1:] == -1).all()
+        assert list(batch["new_tables"][i, :m]) == sp["new_table"]
+        assert (batch["new_tables"][i, m:] == -1).all()
+        assert list(batch["dropped"][i, :batch["n_dropped"][i]]) == sp["dropped"]
+        assert batch["n_fresh"][i] == sp["n_fresh"]
+    assert pools[0].num_free == pools[1].num_free
+    with pytest.raises(zp.ZPError):
+        pools[1].plan_compaction_batch(tables[:1], nb[:1], N_max, max_blocks_seq=np.array([N_max + 1], np.int32))
+    with pytest.raises(zp.ZPError):
+        pools[1].plan_compaction_batch(tables[:1], nb[:1], N_max, max_blocks_seq=np.array([1], np.int32))
 
 
 def test_capacity_plan_brute_force(zp):

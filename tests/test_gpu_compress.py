@@ -348,6 +348,93 @@ def test_compress_layer_matches_three_steps(zp, shape):
     print("reported near-tie swaps:", swaps)
 
 
+@pytest.mark.parametrize("shape", ["qwen", "long_rows"])
+def test_per_request_budgets(zp, shape):
+    """Per-request budgets k_i = (N_i - 1) b given as a k_seq array, through
+    zp_compress_layers and through zp_select_topk + zp_compact_pages: each
+    keep row holds k_i positions then -1 up to the row stride k = max k_i;
+    the keep sets equal the oracle's top-k_i up to reported near-ties; both
+    paths agree; moved rows are bit-exact; no block outside the targets is
+    written (the short budgets' unused target slots stay -1)."""
+    b, w = 16, 16
+    if shape == "qwen":
+        B, h_q, h_kv, d, lo, hi = 6, 32, 8, 128, 200, 900
+        N_i = np.array([2, 8, 5, 3, 8, 6], np.int32)
+    else:  # rows too long for the fused kernel's shared memory: the three-step fallback
+        B, h_q, h_kv, d, lo, hi = 2, 32, 8, 128, 29000, 30000
+        N_i = np.array([128, 37], np.int32)
+    N_max = int(N_i.max())
+    c = _block_aligned_case(980 + len(shape), B, h_q, h_kv, d, b, lo, hi, "bf16", dup=True, spare=B * N_max)
+    desc = _desc(zp, c)
+    lens = c.seq_lens.tolist()
+    Lmax = max(lens)
+    k = (N_max - 1) * b
+    k_i = (N_i - 1) * b
+    rng = np.random.default_rng(981)
+    S0 = (rng.random((B, h_kv, Lmax + 16)) / 100).astype(np.float32)
+    F0 = (rng.random((c.n_total, b, h_kv)) / 80).astype(np.float32)
+    first = torch.tensor([1, 0] * (B // 2), dtype=torch.uint8, device="cuda")
+    free = c.free_blocks.numpy()
+    tg = np.full((B, N_max - 1), -1, np.int32)
+    for i in range(B):
+        m = int(N_i[i]) - 1
+        tg[i, :m] = free[i * (N_max - 1): i * (N_max - 1) + m] if i % 2 else c.block_table[i, :m].numpy()
+    targets = torch.from_numpy(tg).cuda()
+    k_seq = torch.from_numpy(k_i).cuda()
+    params = zp.score_params(window=w)
+    out = {}
+    for path in ("three", "fused"):
+        dc = DeviceCase(c)
+        S = torch.from_numpy(S0.copy()).cuda()
+        F = torch.from_numpy(F0.copy()).cuda()
+        scores = torch.full((B, h_kv, Lmax), -5.0, device="cuda")
+        keep = torch.full((B, h_kv, k), -7, dtype=torch.int32, device="cuda")
+        if path == "three":
+            zp.zp_score_tokens(desc, params, dc.K[0], dc.table, dc.lens, first, S, F, scores)
+            zp.zp_select_topk(scores, dc.lens, k, keep, k_seq=k_seq)
+            zp.zp_compact_pages(desc, dc.K, dc.V, 0, 1, F, 0, dc.table, targets, dc.lens, keep, k, scores=S,
+                                k_seq=k_seq)
+        else:
+            zp.zp_compress_layers(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, first, S, F, targets, k, keep,
+                                  Lmax, scores_out=scores, k_seq=k_seq)
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        out[path] = (scores.cpu().numpy(), keep.cpu().numpy(), dc.K[0].float().cpu().numpy(),
+                     dc.V[0].float().cpu().numpy())
+    s3, k3, K3, V3 = out["three"]
+    sf, kf, Kf, Vf = out["fused"]
+    K0 = c.k_cache[0].float().numpy()
+    V0 = c.v_cache[0].float().numpy()
+    written = set(tg[tg >= 0].tolist())
+    untouched = np.array([x for x in range(c.n_total) if x not in written])
+    prm = pipeline.ScoreParams(window=w)
+    swaps = 0
+    for s in range(B):
+        L, ki = lens[s], int(k_i[s])
+        for kp in (k3, kf):
+            assert (kp[s, :, ki:] == -1).all()
+            assert (kp[s, :, :min(ki, L)] >= 0).all()
+        for h in range(h_kv):
+            swaps += keep_sets_match(kf[s, h], k3[s, h], s3[s, h], ki, L)
+            for Kx, Vx, kp in ((Kf, Vf, kf), (K3, V3, k3)):
+                for r in range(0, min(ki, L), 5):
+                    pos = kp[s, h, r]
+                    sb, ss = c.block_table[s, pos // b], pos % b
+                    db, ds = tg[s, r // b], r % b
+                    assert np.array_equal(Kx[db, ds, h], K0[sb, ss, h])
+                    assert np.array_equal(Vx[db, ds, h], V0[sb, ss, h])
+        if shape != "long_rows" or s == 1:  # the oracle, sampled for the long rows
+            Fref = F0.astype(np.float64).copy()
+            sref = pipeline.final_scores(S0[s, :, :L].astype(np.float64), K0, Fref, c.block_table[s].numpy(), L, b,
+                                         bool(first[s]), prm)
+            for h in range(h_kv):
+                swaps += keep_sets_match(kf[s, h], oracle.topk_keep(sref[h], ki)[0], sref[h], ki, L)
+    for Kx, Vx in ((Kf, Vf), (K3, V3)):
+        assert np.array_equal(Kx[untouched], K0[untouched])
+        assert np.array_equal(Vx[untouched], V0[untouched])
+    print("reported near-tie swaps:", swaps)
+
+
 def test_compress_layers_several_layers_in_one_call(zp):
     """Three layers in one zp_compress_layers call (one launch per kernel,
     App. C.1) equal three single-layer calls: scores, keep sets, K, V and F

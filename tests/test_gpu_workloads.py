@@ -120,6 +120,60 @@ def test_high_concurrency_512_sequences_2048_steps():
     print("compressions:", loop.compressions, "reported near-tie swaps:", swaps)
 
 
+def test_per_request_budgets_in_the_loop():
+    """Per-request block budgets N_i uniform in [4, 128] (N_max = 128) on 48
+    sequences at contexts uniform in [1024, 4096], 600 steps, compression on
+    the side stream: every request compresses at its own N_i to (N_i - 1) b
+    tokens; two requests with different budgets mirrored by the oracle loop
+    at their own N_i over all steps (outputs, triggers, keep sets)."""
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    B, h_q, h_kv, d, b, N_max, steps = 48, 32, 8, 128, 16, 128, 600
+    g = torch.Generator().manual_seed(1007)
+    lens0 = torch.randint(1024, 4097, (B,), generator=g).numpy().astype(np.int32)
+    N_i = torch.randint(4, N_max + 1, (B,), generator=g).numpy().astype(np.int32)
+    N_i[0], N_i[1] = 4, 37
+    stride = 4096 // b + 2
+    n_total = int(np.maximum((lens0 + b - 1) // b + 1, N_i).sum()) + 64
+    loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=1, dtype=torch.bfloat16, window=b,
+                      async_compress=True)
+    loop.add_sequences(lens0, max_blocks=N_i)
+    loop.K.copy_(_dev_normal(loop.K.shape, 31))
+    loop.V.copy_(_dev_normal(loop.V.shape, 32))
+    mseqs = [0, 1]
+    oras = [_mirror(loop, [s], [0], int(N_i[s]), b) for s in mseqs]
+    count = np.zeros(B, dtype=np.int64)
+    swaps, checked = 0, 0
+    for step in range(steps):
+        q = _dev_normal((1, B, h_q, d), 700000 + step)
+        kn = _dev_normal((1, B, h_kv, d), 800000 + step)
+        vn = _dev_normal((1, B, h_kv, d), 900000 + step)
+        trig = loop.step(q, kn, vn)
+        if trig:
+            again = [x for x in trig if count[x] > 0]  # a compressed request grows back to N_i blocks
+            assert (loop.lens[again] == N_i[again] * b).all()
+            plan = loop.pending[-1][2]
+            for i, s in enumerate(trig):  # targets and new table padded past the request's own budget
+                assert (plan["targets"][i, N_i[s] - 1:] == -1).all() and (plan["targets"][i, :N_i[s] - 1] >= 0).all()
+                assert (plan["new_tables"][i, N_i[s]:] == -1).all()
+        count[trig] += 1
+        for s, ora in zip(mseqs, oras):
+            if loop.active[s] or s in trig:
+                swaps += _mirror_step(ora, loop, [s], [0], q, kn, vn, trig)
+                checked += 1
+    loop.drain()
+    torch.cuda.synchronize()
+    import compressed_paged_kv_zp_gb300 as zp
+    assert zp.zp_device_status() == (0, 0)
+    due = lens0 + steps >= N_i * b + b
+    assert (count[due] > 0).all()
+    assert count[0] >= 20  # N_0 = 4 blocks: a compression every 16 decoded steps
+    held = (loop.table >= 0).sum(axis=1)
+    assert (held <= N_i).all()
+    _check_pool(loop)
+    assert not any(o.first.any() for o in oras)
+    print("compressions:", loop.compressions, "mirrored steps:", checked, "reported near-tie swaps:", swaps)
+
+
 def test_prefix_shared_36_layers_async():
     from compressed_paged_kv_zp_gb300.engine import DecodeLoop
     B, h_q, h_kv, d, b, N_max, layers, steps = 32, 32, 8, 128, 16, 64, 36, 40
