@@ -25,7 +25,7 @@ _DTYPES = {torch.bfloat16: ZP_BF16, torch.float32: ZP_F32}
 STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTYPE",
           4: "ZP_ERR_CAPACITY", 5: "ZP_ERR_CUDA", 6: "ZP_ERR_TIMEOUT", 7: "ZP_ERR_DEVICE"}
 
-# every symbol include/zp.h declares
+# every symbol include/*.h declares
 EXPORTS = [
     "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
     "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
@@ -35,6 +35,9 @@ EXPORTS = [
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
     "zp_plan_capacity",
+    # include/zp_sched.h
+    "zp_sched_create", "zp_sched_destroy", "zp_sched_add_request", "zp_sched_schedule", "zp_sched_commit",
+    "zp_sched_take_compressions", "zp_sched_compression_done", "zp_sched_counts", "zp_sched_request_info",
 ]
 
 
@@ -95,8 +98,8 @@ def _load() -> ctypes.CDLL:
     lib.zp_device_status.argtypes = [P, P, I32]
     lib.zp_decode_workspace_size.restype = SZ
     lib.zp_decode_workspace_size.argtypes = [D, I32, I32]
-    lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, I32, P, SZ, P]
-    lib.zp_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, I32, P, I32, P, P, I32, P]
+    lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P, SZ, P]
+    lib.zp_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P]
     lib.zp_append_kv.argtypes = [D, P, P, P, P, P, I32, P, I32, P]
     lib.zp_needs_compression.argtypes = [I32, I32, I32]
     lib.zp_score_workspace_size.restype = SZ
@@ -167,27 +170,42 @@ def zp_decode_workspace_size(desc: CacheDesc, B: int, table_stride: int) -> int:
     return int(n)
 
 
+def _slot_map(score_accum, score_rows):
+    """(pointer, row count) of an optional int32 [B] slot map into score_accum [R][h_kv][stride]."""
+    if score_rows is None:
+        return None, 0
+    if score_rows.dtype != torch.int32:
+        raise ValueError("score_rows must be int32")
+    if score_accum is None:
+        raise ValueError("score_rows needs score_accum")
+    return _dev(score_rows, "score_rows"), int(score_accum.shape[0])
+
+
 def zp_paged_decode_attn(desc, q, k_cache, v_cache, block_table, seq_lens, out, score_accum=None,
-                         window=0, workspace=None, stream=None) -> None:
+                         window=0, workspace=None, stream=None, score_rows=None) -> None:
+    """score_rows: optional int32 [B] device map of batch entries to rows of
+    score_accum (query slots); -1 = no slot, the entry is not scored."""
     B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    rows_p, n_rows = _slot_map(score_accum, score_rows)
     if workspace is None:
         workspace = torch.empty(zp_decode_workspace_size(desc, B, table_stride), dtype=torch.uint8,
                                 device=q.device)
     _check(lib.zp_paged_decode_attn(ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"),
                                     _dev(v_cache, "v_cache"), _dev(block_table, "block_table"),
                                     table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
-                                    _dev(score_accum, "score_accum"), int(window),
+                                    _dev(score_accum, "score_accum"), rows_p, n_rows, int(window),
                                     _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def zp_paged_decode_attn_noalloc(desc, q, k_cache, v_cache, block_table, seq_lens, out,
-                                 score_accum=None, window=0, stream=None) -> None:
+                                 score_accum=None, window=0, stream=None, score_rows=None) -> None:
     """zp_paged_decode_attn with the library's built-in scratch (no workspace)."""
     B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
+    rows_p, n_rows = _slot_map(score_accum, score_rows)
     _check(lib.zp_paged_decode_attn_noalloc(ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"),
                                             _dev(v_cache, "v_cache"), _dev(block_table, "block_table"),
                                             table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
-                                            _dev(score_accum, "score_accum"), int(window),
+                                            _dev(score_accum, "score_accum"), rows_p, n_rows, int(window),
                                             _stream(stream)))
 
 

@@ -20,7 +20,7 @@ OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzp.so")
 
 SOURCES = ["zp_api.cu", "decode_attn.cu", "append_kv.cu", "window_score.cu", "score.cu", "topk.cu",
-           "compact.cu", "pool.cpp"]
+           "compact.cu", "pool.cpp", "sched.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -39,7 +39,7 @@ def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(OBJDIR, src + ".o")
     path = os.path.join(CSRC, src)
     headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
-    headers.append(os.path.join(INCLUDE, "zp.h"))
+    headers += [os.path.join(INCLUDE, h) for h in ("zp.h", "zp_sched.h")]
     newest = max(os.path.getmtime(p) for p in [path, __file__] + headers)
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest:
         return obj

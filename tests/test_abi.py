@@ -1,6 +1,6 @@
 """C ABI checks and host logic that need no GPU.
 
-* libzp.so loads and exports every function include/zp.h declares;
+* libzp.so loads and exports every function include/*.h declares;
 * the trigger and the host block pool / planner agree with the oracle's
   reading of [Zipage §4.1, §4.4] on random tables with shared prefixes;
 * calls with invalid arguments fail with the documented status before any
@@ -23,7 +23,8 @@ def zp():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "zp.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, h)).read() for h in sorted(os.listdir(inc)) if h.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(zp_[a-z_0-9]+)\s*\(", src)))
 
