@@ -61,6 +61,8 @@ struct DecodeArgs {
     int window;
     float *score;
     long long score_stride;  // elements between kv-head rows of S: table_stride * b
+    const int32_t *score_rows;  // nullable [B]: row of S (query slot) of each batch entry, -1 = none
+    int n_score_rows;           // rows of S when score_rows is set
     float *logits;     // [units * T][h_q]
     float2 *stats;     // [B][h_q] final (max, sum), log2 units
     float *part_acc;   // [2*grid][h_q][D]
@@ -157,12 +159,25 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int G) {
     return c;
 }
 
+// Row of S that batch entry s scores into: its query slot when a slot map is
+// given (-1: the entry holds no slot and is not scored), else s.  A slot
+// outside [0, n_score_rows) is recorded as an error and not scored.
+__device__ __forceinline__ int score_row_of(const DecodeArgs &a, int s) {
+    if (!a.score_rows) return s;
+    const int r = __ldg(&a.score_rows[s]);
+    if (r >= a.n_score_rows) {
+        record_error(a.err, ZP_ERR_DEVICE, 0x21);
+        return -1;
+    }
+    return r < 0 ? -1 : r;
+}
+
 // Record of one unit for the score epilogue: sequence, first token, length
 // and flags (bit 0: the sequence is on a window step, bit 1: first window row).
 __device__ __forceinline__ int4 unit_record(const DecodeArgs &a, int s, int tok0, int L) {
     const int P = L - 1;
     const int r = P >= 0 ? P % a.b : -1;
-    const int win = (P >= 0 && r >= a.b - a.window) ? 1 : 0;
+    const int win = (P >= 0 && r >= a.b - a.window && score_row_of(a, s) >= 0) ? 1 : 0;
     const int first = (win && r == a.b - a.window) ? 2 : 0;
     return make_int4(s, tok0, L, win | first);
 }
@@ -393,7 +408,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
     bool window_step = false;
     auto compute_window = [&](int seq) {
         const int P = lens[seq] - 1;
-        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window;
+        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window && score_row_of(a, seq) >= 0;
     };
     window_step = compute_window(s);
 
@@ -662,7 +677,7 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int j = 0; j < G; ++j) best = fmaxf(best, exp2f(x[j] - ml[j].x) / ml[j].y);
         const float c = best * inv_w;
-        float *dst = a.score + ((size_t)s * a.h_kv + kvh) * a.score_stride + tok;
+        float *dst = a.score + ((size_t)score_row_of(a, s) * a.h_kv + kvh) * a.score_stride + tok;
         *dst = (first_row || tok == P) ? c : (*dst + c);
     }
 }
@@ -960,7 +975,7 @@ __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, i
     const int RSF = CT + 4;  // score piece stride in floats (bank shift of 4 per kv head)
     float *lg_s = reinterpret_cast<float *>(buf);
     float *sc_s = lg_s + (size_t)CT * HQ;
-    float *srow0 = a.score + (size_t)s * HKV * a.score_stride;
+    float *srow0 = a.score + (size_t)score_row_of(a, s) * HKV * a.score_stride;
     const float *lg_g = a.logits + ((size_t)p0 * kTcTokens) * HQ;
     fence_proxy_async_smem();  // earlier ordinary writes to buf precede the copies into it
     named_bar_sync(1, nthr);
@@ -1059,7 +1074,7 @@ __device__ void score_prefetched(const DecodeArgs &a, int s, int L, int tb, int 
     fence_proxy_async_smem();
     named_bar_sync(1, nthr);
     if (ctid == 0) {
-        float *srow0 = a.score + (size_t)s * HKV * a.score_stride;
+        float *srow0 = a.score + (size_t)score_row_of(a, s) * HKV * a.score_stride;
 #pragma unroll
         for (int kvh = 0; kvh < HKV; ++kvh)
             bulk_s2g(srow0 + (size_t)kvh * a.score_stride + tb, sc_s + kvh * RSF, (unsigned)(n16 * 4));
@@ -1198,12 +1213,13 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             if (a.want_score && (u == u0 || tok0 == 0) && lane < h_kv) {
                 // first unit of a segment on a window step: bring its score pieces into L2
                 const int L = lens[useq], P = L - 1;
-                if ((P % a.b) >= a.b - a.window) {
+                const int row = score_row_of(a, useq);
+                if ((P % a.b) >= a.b - a.window && row >= 0) {
                     const long long ue = prefix[useq + 1] < u1 ? prefix[useq + 1] : u1;
                     int te = (int)(ue - prefix[useq]) * kTcTokens;
                     if (te > L) te = L;
                     const unsigned bytes = (unsigned)(((te - tok0) * 4 + 15) & ~15);
-                    bulk_prefetch_l2(a.score + ((size_t)useq * h_kv + lane) * a.score_stride + tok0, bytes);
+                    bulk_prefetch_l2(a.score + ((size_t)row * h_kv + lane) * a.score_stride + tok0, bytes);
                 }
             }
             if (lane == 0) {
@@ -1254,7 +1270,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     };
     auto compute_window = [&](int seq) {
         const int P = lens[seq] - 1;
-        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window;
+        return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window && score_row_of(a, seq) >= 0;
     };
 
     int s = s_first;
@@ -1450,7 +1466,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                     float *sc_s = lg_s + (size_t)n16 * HQ;
                     bulk_g2s_plain(lg_s, a.logits + ((size_t)prefix[g.x] * kTcTokens + g.y) * HQ,
                                    (unsigned)(n16 * HQ * 4), ebar);
-                    const float *srow0 = a.score + (size_t)g.x * h_kv * a.score_stride + g.y;
+                    const float *srow0 = a.score + (size_t)score_row_of(a, g.x) * h_kv * a.score_stride + g.y;
                     for (int kvh = 0; kvh < h_kv; ++kvh)
                         bulk_g2s_plain(sc_s + kvh * (n16 + 4), srow0 + (size_t)kvh * a.score_stride,
                                        (unsigned)(n16 * 4), ebar);
@@ -1815,8 +1831,9 @@ extern "C" size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, in
 extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
                                           const void *v_cache, const int32_t *block_table,
                                           int32_t table_stride, const int32_t *seq_lens, int32_t B,
-                                          void *out, float *score_accum, int32_t window,
-                                          void *workspace, size_t workspace_bytes, void *stream) {
+                                          void *out, float *score_accum, const int32_t *score_rows,
+                                          int32_t n_score_rows, int32_t window, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (B < 0 || table_stride < 0) return fail(ZP_ERR_INVALID_ARG, "decode: B or table_stride negative");
@@ -1828,6 +1845,8 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
         return fail(ZP_ERR_INVALID_ARG, "decode: window %d outside [1, b=%d]", window, D->block_size);
     if (reinterpret_cast<uintptr_t>(score_accum) % 16)
         return fail(ZP_ERR_INVALID_ARG, "decode: score_accum must be 16-byte aligned");
+    if (score_accum && score_rows && n_score_rows < 1)
+        return fail(ZP_ERR_INVALID_ARG, "decode: a slot map needs n_score_rows >= 1");
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
@@ -1860,6 +1879,8 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.window = window;
     a.score = score_accum;
     a.score_stride = (long long)table_stride * D->block_size;
+    a.score_rows = score_accum ? score_rows : nullptr;
+    a.n_score_rows = n_score_rows;
     a.logits = reinterpret_cast<float *>(ws + p.off_logits);
     a.stats = reinterpret_cast<float2 *>(ws + p.off_stats);
     a.part_acc = reinterpret_cast<float *>(ws + p.off_pacc);
@@ -1918,7 +1939,8 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const 
                                                   const void *k_cache, const void *v_cache,
                                                   const int32_t *block_table, int32_t table_stride,
                                                   const int32_t *seq_lens, int32_t B, void *out,
-                                                  float *score_accum, int32_t window, void *stream) {
+                                                  float *score_accum, const int32_t *score_rows,
+                                                  int32_t n_score_rows, int32_t window, void *stream) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (B < 0 || table_stride < 0) return fail(ZP_ERR_INVALID_ARG, "decode_noalloc: B or table_stride negative");
@@ -1951,5 +1973,6 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const 
     // Nothing in the scratch needs to start at zero: every part that is
     // read is written earlier in the same call.
     return zp_paged_decode_attn(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out,
-                                score_accum, window, scratch, kNoAllocScratchBytes, stream);
+                                score_accum, score_rows, n_score_rows, window, scratch, kNoAllocScratchBytes,
+                                stream);
 }

@@ -114,6 +114,11 @@ size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table
  * observation-window score of App. C.2 computed from those queries.  The
  * score lives with the sequence, not with the block: sequences that share
  * prefix blocks [§4.4] each score those tokens with their own queries.
+ * score_rows (nullable, device int32 [B]) maps batch entry s to the row of S
+ * it scores into -- the request's query slot [§4.2, §4.3] -- and then S holds
+ * n_score_rows rows; -1 marks an entry without a slot, which is decoded but
+ * not scored.  A slot >= n_score_rows is recorded as ZP_ERR_DEVICE (detail
+ * 0x21) and not scored.  Without the map row s belongs to batch entry s.
  *
  * The workspace needs no clearing between calls.  After a call that left
  * ZP_ERR_TIMEOUT in the device status, clear it (zeros) before reusing it.
@@ -124,8 +129,9 @@ size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table
 zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
                                const void *v_cache, const int32_t *block_table,
                                int32_t table_stride, const int32_t *seq_lens, int32_t B,
-                               void *out, float *score_accum, int32_t window,
-                               void *workspace, size_t workspace_bytes, void *stream);
+                               void *out, float *score_accum, const int32_t *score_rows,
+                               int32_t n_score_rows, int32_t window, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /* Same computation and arguments as zp_paged_decode_attn, without the
  * workspace: for callers that cannot allocate device memory when they decode
@@ -147,7 +153,8 @@ zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void
 zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q, const void *k_cache,
                                        const void *v_cache, const int32_t *block_table,
                                        int32_t table_stride, const int32_t *seq_lens, int32_t B,
-                                       void *out, float *score_accum, int32_t window, void *stream);
+                                       void *out, float *score_accum, const int32_t *score_rows,
+                                       int32_t n_score_rows, int32_t window, void *stream);
 
 /* Writes the new token's key and value of each sequence into its slot
  * [Zipage §3: the cache of a block is written into the block's slots]:

@@ -166,6 +166,66 @@ def test_window_score_accumulates_over_decode_steps(zp, dtype, h_q, h_kv, d, w):
         np.testing.assert_allclose(got, explicit, **TOL_SCORE[dtype])
 
 
+@pytest.mark.parametrize("dtype,h_q,h_kv,d", [("f32", 8, 2, 64), ("bf16", 32, 8, 128)])
+def test_slot_map_follows_the_request(zp, dtype, h_q, h_kv, d):
+    """Query slots [§4.2, §4.3]: with a slot map, batch entry i scores into
+    row score_rows[i] of S.  The batch order changes at every one of the w
+    window steps (as a scheduler's running batch does) while each request
+    keeps its slot; one request holds no slot (-1).  Each slot row must equal
+    the oracle's accumulation for its request, the slotless request and the
+    unused rows stay untouched, and the outputs match the oracle."""
+    b, w = 16, 16
+    final = [5 * b, 3 * b, 9 * b, 2 * b, 4 * b]
+    B = len(final)
+    slot = [3, 0, 5, 1, -1]  # the last request decodes without a query slot
+    R = 7
+    c = zp_inputs.make_paged_case(60, B, h_q, h_kv, d, b, lens=final, dtype=dtype)
+    dc = DeviceCase(c)
+    desc = _desc(zp, c)
+    stride = c.block_table.shape[1]
+    S = torch.randn(R, h_kv, stride * b, device="cuda").abs()
+    S0 = S.cpu().numpy().astype(np.float64)
+    S_ref = np.zeros((c.n_total, b, h_kv))
+    for s, L in enumerate(final):
+        if slot[s] >= 0:
+            t = np.arange(L)
+            S_ref[c.block_table[s].numpy()[t // b], t % b] = S0[slot[s], :, :L].T
+    qw = zp_inputs.normal((B, w, h_q, d), 87, dtype)
+    kw = zp_inputs.normal((B, w, h_kv, d), 88, dtype)
+    vw = zp_inputs.normal((B, w, h_kv, d), 89, dtype)
+    rng = np.random.default_rng(90)
+    for u in range(w):
+        order = rng.permutation(B)
+        lens = np.array([final[s] - w + u + 1 for s in range(B)], dtype=np.int32)
+        lens_d = torch.from_numpy(lens[order]).cuda()
+        table_d = dc.table[torch.from_numpy(order).cuda()].contiguous()
+        rows_d = torch.tensor([slot[s] for s in order], dtype=torch.int32, device="cuda")
+        zp.zp_append_kv(desc, kw[order, u].contiguous().cuda(), vw[order, u].contiguous().cuda(), dc.K[0],
+                        dc.V[0], table_d, lens_d)
+        q = qw[order, u].contiguous().cuda()
+        out = torch.empty_like(q)
+        zp.zp_paged_decode_attn(desc, q, dc.K[0], dc.V[0], table_d, lens_d, out, score_accum=S, window=w,
+                                score_rows=rows_d)
+        torch.cuda.synchronize()
+        K, V = dc.np_k(), dc.np_v()
+        ref, probs = oracle.decode_attention(qw[:, u].float().numpy(), K, V, c.block_table.numpy(), lens,
+                                             want_probs=True)
+        got = np.empty_like(ref)
+        got[order] = out.float().cpu().numpy()
+        np.testing.assert_allclose(got, ref, **TOL_OUT[dtype])
+        sl = [s for s in range(B) if slot[s] >= 0]
+        oracle.accumulate_window_score(probs[sl], c.block_table.numpy()[sl], lens[sl], h_kv, b, w,
+                                       S_ref)
+    assert zp.zp_device_status() == (0, 0)
+    Sg = S.cpu().numpy().astype(np.float64)
+    for s, L in enumerate(final):
+        if slot[s] >= 0:
+            np.testing.assert_allclose(Sg[slot[s], :, :L], gather_slots(S_ref, c.block_table[s].numpy(), L, b),
+                                       **TOL_SCORE[dtype])
+    for r in set(range(R)) - set(slot):
+        assert np.array_equal(Sg[r], S0[r])
+
+
 def test_append_writes_only_the_new_slot(zp):
     c = zp_inputs.make_paged_case(9, 5, 32, 8, 128, 16, len_range=(1, 100), dtype="bf16")
     dc = DeviceCase(c)

@@ -44,7 +44,7 @@ def test_noalloc_decode_matches_workspace_decode_twice():
             ctypes.byref(desc), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(K.data_ptr()),
             ctypes.c_void_p(V.data_ptr()), ctypes.c_void_p(table.data_ptr()), table.shape[1],
             ctypes.c_void_p(lens.data_ptr()), c.B, ctypes.c_void_p(out.data_ptr()),
-            ctypes.c_void_p(S.data_ptr()), 16, stream)
+            ctypes.c_void_p(S.data_ptr()), None, 0, 16, stream)
         assert rc == 0, zp.lib.zp_last_error().decode()
         torch.cuda.synchronize()
         assert zp.zp_device_status() == (0, 0)
