@@ -289,10 +289,15 @@ class Workload:
         self.decode()
         self.compress()
 
-    def capture(self):
-        """The device work of a step as three CUDA graphs (append, decode,
-        compression), so that per-launch host overhead stays off the GPU's
-        critical path; the host planner still runs every step."""
+    STEPS_PER_GRAPH = 10
+
+    def capture(self, n_steps: int):
+        """The device work of n_steps steps as CUDA graphs of up to
+        STEPS_PER_GRAPH whole steps each (append, decode, compression), so that
+        per-launch host overhead stays off the GPU's critical path.  Every
+        decode in them sits between its own pair of timing events (external
+        event-record nodes), so each decode of the timed region is timed.
+        Returns [(graph, steps in it)] and the event pairs in step order."""
         zp = self.zp
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -301,19 +306,26 @@ class Workload:
             self.compress_device()
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        graphs = []
-        for fn in (lambda: zp.zp_append_kv(self.desc, self.k_new, self.v_new, self.K, self.V, self.table,
-                                           self.lens),
-                   lambda: zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens,
-                                                   self.out, score_accum=self.S, window=self.w,
-                                                   workspace=self.ws),
-                   self.compress_device):
+        graphs, events = [], []
+        done = 0
+        while done < n_steps:
+            m = min(self.STEPS_PER_GRAPH, n_steps - done)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                fn()
-            graphs.append(g)
+                for _ in range(m):
+                    ev = (torch.cuda.Event(enable_timing=True, external=True),
+                          torch.cuda.Event(enable_timing=True, external=True))
+                    zp.zp_append_kv(self.desc, self.k_new, self.v_new, self.K, self.V, self.table, self.lens)
+                    ev[0].record()
+                    zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens, self.out,
+                                            score_accum=self.S, window=self.w, workspace=self.ws)
+                    ev[1].record()
+                    self.compress_device()
+                    events.append(ev)
+            graphs.append((g, m))
+            done += m
         torch.cuda.synchronize()
-        return graphs
+        return graphs, events
 
     def step_e2e(self):
         """Same step through the public calls with host buffers: H2D of q and
@@ -461,11 +473,10 @@ def main():
     if code:
         raise RuntimeError("device status %d after warm-up" % code)
 
-    # ---- timed region: K steps (device work replayed from CUDA graphs, the
-    # host planner every step), events around every decode
-    g_append, g_decode, g_compress = wl.capture()
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    # ---- timed region: K steps (device work replayed from CUDA graphs of ten
+    # whole steps, the host planner every step), timing events around every
+    # decode inside the graphs
+    graphs, ev_dec = wl.capture(args.steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
@@ -473,13 +484,10 @@ def main():
     torch.cuda.synchronize()
     clocks.mark_start()
     start.record(stream)
-    for i in range(args.steps):
-        g_append.replay()
-        ev_dec[i][0].record(stream)
-        g_decode.replay()
-        ev_dec[i][1].record(stream)
-        wl.plan()
-        g_compress.replay()
+    for g, m in graphs:
+        g.replay()
+        for _ in range(m):  # the host planner of each step, while the GPU runs
+            wl.plan()
     stop.record(stream)
     torch.cuda.synchronize()
     clocks.mark_stop()
@@ -525,8 +533,9 @@ def main():
         "config": {"workload": wl.name, "seqs": wl.B, "heads": "32q/8kv", "head_dim": wl.d,
                    "block": wl.b, "max_blocks_per_seq": wl.N_max, "kept_tokens": wl.k, "window": wl.w,
                    "ctx": "uniform 1024-4096", "compressed_per_step": wl.n_comp,
-                   "launch": "device work replayed from CUDA graphs (append, decode, compression); "
-                             "host planner every step; e2e through direct calls",
+                   "launch": "device work replayed from CUDA graphs of %d whole steps (append, decode, "
+                             "compression), a timing-event pair around each decode; host planner every step; "
+                             "e2e through direct calls" % wl.STEPS_PER_GRAPH,
                    "l2": "inputs larger than L2 (K+V %.0f MB)" % (2 * wl.K.numel() * wl.K.element_size() / 1e6),
                    "peak_kind": peak_kind},
         "roofline": {"kernel": "zp_paged_decode_attn (decode_tc_kernel: attention, merges and window score)", "bound": "hbm",

@@ -703,11 +703,12 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
 // groups.  One consumer warp per kv head.  P is rounded to bf16 for the
 // second product; the scores and the softmax statistics stay in fp32.
 constexpr int kTcTokens = 16;     // tokens per unit
-// Epilogue region of shared memory: 8 ints, an mbarrier, (max, 1/sum) of up to
+// Epilogue region of shared memory: 8 ints, an mbarrier, the CTA's last
+// sequence (for the announcement), (max, 1/sum) of up to
 // 64 q heads, up to kMaxSeg window segments {sequence, first token, end token,
 // byte offset}, the merged sequences' (max, 1/sum), then the first unit of
 // every CTA (grid + 1 long longs).
-constexpr int kEpiBar = 32, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
+constexpr int kEpiBar = 32, kEpiSLast = 40, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
 constexpr int kEpiMl = kEpiSeg + kMaxSeg * 16;  // (M, 1/L) of the merged sequences: 2 x 64 float2
 constexpr int kEpiCst = kEpiMl + 2 * 64 * 8;
 constexpr int kTcPad = 16;        // bytes of padding after each staged token row
@@ -756,6 +757,13 @@ __device__ __forceinline__ unsigned long long ctl_word(int phase, int count) {
 }
 __device__ __forceinline__ bool ctl_valid(unsigned long long w) { return (w >> 16) == kCtlTag; }
 
+// Release / acquire at GPU scope around the control words (the part records
+// written before a release are visible to a thread after its acquire).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
+    return *reinterpret_cast<const volatile unsigned long long *>(p);
+}
+
 // CTA owning unit u, from the table cst[0..G] of first units (binary search).
 __device__ __forceinline__ int owner_of(long long u, const long long *cst, int G) {
     int lo = 0, hi = G - 1;
@@ -780,9 +788,10 @@ __device__ __forceinline__ int parts_of(long long p0, long long p1, const long l
 
 // Announces one part; true for the last of n_parts, whose update publishes
 // the sequence (every part's record is then in place).  A word left
-// published by an earlier call counts as zero.
-__device__ bool ctl_arrive(unsigned long long *w, int n_parts, unsigned *err) {
-    unsigned long long cur = 0ull;  // a clean word is the common case: one round trip
+// published by an earlier call counts as zero.  `cur` is the caller's guess
+// of the word's value (read before the main loop): when no other part has
+// arrived since, the first compare-and-swap succeeds -- one round trip.
+__device__ bool ctl_arrive(unsigned long long *w, int n_parts, unsigned long long cur, unsigned *err) {
     for (int it = 0; it < 4096; ++it) {
         const int have = (ctl_valid(cur) && ((cur >> 15) & 1) == 0) ? (int)(cur & 0x7FFF) : 0;
         const bool last = have + 1 == n_parts;
@@ -824,48 +833,9 @@ __device__ __forceinline__ int part_slot(int c_lo, int j, long long p0, const lo
     return cst[c + 1] > cst[c] ? 2 * c + (p0 > cst[c] ? 1 : 0) : -1;
 }
 
-// Phase 1: (M, L) of every head of the merged sequences -> stats (global) and
-// sm_ml[i * h_q + h] = (M, 1/L) in shared memory.
-__device__ void merge_stats(const DecodeArgs &a, const int *ms, const int *prefix, const long long *cst, int Gd,
-                            float2 *sm_ml, int ctid, int nthr) {
-    const int h_q = a.h_q;
-    for (int it = ctid; it < 2 * h_q; it += nthr) {
-        const int i = it / h_q, h = it % h_q;
-        const int s = ms[i];
-        if (s < 0) continue;
-        const long long p0 = prefix[s];
-        int c_lo, c_hi;
-        parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
-        const int nc = c_hi - c_lo + 1;
-        float M = -INFINITY;
-        float2 v4[4];
-        for (int j0 = 0; j0 < nc; j0 += 4) {  // four loads in flight
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
-                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) M = fmaxf(M, v4[q].x);
-        }
-        float Lsum = 0.f;
-        for (int j0 = 0; j0 < nc; j0 += 4) {  // (L2 hits)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
-                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (v4[q].x != -INFINITY) Lsum += exp2f(v4[q].x - M) * v4[q].y;
-        }
-        if (a.want_score) a.stats[(size_t)s * h_q + h] = make_float2(M, Lsum);
-        sm_ml[it] = make_float2(M, Lsum > 0.f ? 1.f / Lsum : 0.f);
-    }
-}
-
 // Final (M, 1/L) of every head of cut sequence s from its part records, into
-// shared memory (one (head) item per thread; the records are published).
+// shared memory (one head per thread; the records are published).  Up to
+// eight records are loaded together, then combined.
 __device__ void part_stats(const DecodeArgs &a, int s, const int *prefix, const long long *cst, int Gd,
                            float2 *out, int ctid, int nthr) {
     const int h_q = a.h_q;
@@ -875,82 +845,169 @@ __device__ void part_stats(const DecodeArgs &a, int s, const int *prefix, const 
         parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
         const int nc = c_hi - c_lo + 1;
         float M = -INFINITY, Lsum = 0.f;
-        for (int j0 = 0; j0 < nc; j0 += 4) {  // four loads in flight, online combination
-            float2 v4[4];
+        for (int j0 = 0; j0 < nc; j0 += 8) {
+            float2 v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
-                v4[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
+                v[q] = sl < 0 ? make_float2(-INFINITY, 0.f) : __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
             }
+            float Mn = M;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (v4[q].x == -INFINITY) continue;
-                const float Mn = fmaxf(M, v4[q].x);
-                Lsum = (M == -INFINITY ? 0.f : Lsum * exp2f(M - Mn)) + v4[q].y * exp2f(v4[q].x - Mn);
-                M = Mn;
-            }
+            for (int q = 0; q < 8; ++q) Mn = fmaxf(Mn, v[q].x);
+            if (Mn == -INFINITY) continue;
+            Lsum = (M == -INFINITY) ? 0.f : Lsum * exp2f(M - Mn);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (v[q].x != -INFINITY) Lsum += v[q].y * exp2f(v[q].x - Mn);
+            M = Mn;
         }
         out[h] = make_float2(M, Lsum > 0.f ? 1.f / Lsum : 0.f);
     }
 }
 
-// Phase 2: the outputs, one (sequence, head, 16 dims) item per thread.
+// Output of cut sequence s from its part records, the share of this CTA:
+// the (head, 16 dims) items of the sequence are split evenly over the CTAs
+// that hold a part of it (in CTA order), so every part-holder combines a
+// slice once the sequence is published and no CTA combines the whole
+// sequence alone.  Each item derives its head's statistics from the records
+// it loads (online rescaling, four parts per round), so the merge needs no
+// shared statistics and runs beside part_stats: threads [t0, nthr) take the
+// items.  With all_items the CTA combines the whole output (used without the
+// window score, where only the last arrival merges and nobody waits).
+//     M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j acc_j / sum_j w_j l_j.
 template <int D>
-__device__ void merge_outputs(const DecodeArgs &a, const int *ms, const int *prefix, const long long *cst, int Gd,
-                              const float2 *sm_ml, int ctid, int nthr) {
+__device__ void merge_slice(const DecodeArgs &a, int s, const int *prefix, const long long *cst, int Gd,
+                            bool all_items, int ctid, int t0, int nthr) {
+    if (ctid < t0) return;
     const int h_q = a.h_q;
     constexpr int CH = 16;
-    for (int it = ctid; it < 2 * h_q * (D / CH); it += nthr) {
-        const int i = it / (h_q * (D / CH));
-        const int r = it % (h_q * (D / CH));
-        const int h = r / (D / CH);
-        const int d0 = (r % (D / CH)) * CH;
-        const int s = ms[i];
-        if (s < 0) continue;
-        const long long p0 = prefix[s];
-        int c_lo, c_hi;
-        parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
-        const int nc = c_hi - c_lo + 1;
-        const float2 Mi = sm_ml[i * h_q + h];
+    const long long p0 = prefix[s];
+    int c_lo, c_hi;
+    int np = parts_of(p0, prefix[s + 1], cst, Gd, &c_lo, &c_hi);
+    const int nc = c_hi - c_lo + 1;
+    int j = 0;  // this CTA's index among the parts that hold units
+    for (int c = c_lo; c < (int)blockIdx.x; ++c) j += cst[c + 1] > cst[c] ? 1 : 0;
+    if (all_items) j = 0, np = 1;
+    const int items = h_q * (D / CH);
+    const int it_b = (int)((long long)j * items / np), it_e = (int)((long long)(j + 1) * items / np);
+    for (int it = it_b + ctid - t0; it < it_e; it += nthr - t0) {
+        const int h = it / (D / CH);
+        const int d0 = (it % (D / CH)) * CH;
         float acc[CH];
 #pragma unroll
         for (int k = 0; k < CH; ++k) acc[k] = 0.f;
-        for (int j0 = 0; j0 < nc; j0 += 2) {  // two parts' loads in flight
-            float w[2];
-            float4 x4[2][CH / 4];
+        float M = -INFINITY, Lsum = 0.f;
+        for (int j0 = 0; j0 < nc; j0 += 4) {  // four parts' loads in flight
+            float2 ml[4];
+            float4 x4[4][CH / 4];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 const int sl = j0 + q < nc ? part_slot(c_lo, j0 + q, p0, cst) : -1;
-                w[q] = 0.f;
                 if (sl >= 0) {
-                    const float2 v = __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
-                    w[q] = (v.x == -INFINITY) ? 0.f : exp2f(v.x - Mi.x);
+                    ml[q] = __ldcg(&a.part_ml[(size_t)sl * h_q + h]);
                     const float4 *src =
                         reinterpret_cast<const float4 *>(a.part_acc + ((size_t)sl * h_q + h) * D + d0);
 #pragma unroll
                     for (int q4 = 0; q4 < CH / 4; ++q4) x4[q][q4] = __ldcg(src + q4);
                 } else {
+                    ml[q] = make_float2(-INFINITY, 0.f);
 #pragma unroll
                     for (int q4 = 0; q4 < CH / 4; ++q4) x4[q][q4] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            float Mn = M;
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+            for (int q = 0; q < 4; ++q) Mn = fmaxf(Mn, ml[q].x);
+            if (Mn == -INFINITY) continue;
+            const float r = (M == -INFINITY) ? 0.f : exp2f(M - Mn);  // rescale of what is summed so far
+            Lsum *= r;
+#pragma unroll
+            for (int k = 0; k < CH; ++k) acc[k] *= r;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - Mn);
+                Lsum += w * ml[q].y;
 #pragma unroll
                 for (int q4 = 0; q4 < CH / 4; ++q4) {
-                    acc[4 * q4] += w[q] * x4[q][q4].x;
-                    acc[4 * q4 + 1] += w[q] * x4[q][q4].y;
-                    acc[4 * q4 + 2] += w[q] * x4[q][q4].z;
-                    acc[4 * q4 + 3] += w[q] * x4[q][q4].w;
+                    acc[4 * q4] += w * x4[q][q4].x;
+                    acc[4 * q4 + 1] += w * x4[q][q4].y;
+                    acc[4 * q4 + 2] += w * x4[q][q4].z;
+                    acc[4 * q4 + 3] += w * x4[q][q4].w;
                 }
+            }
+            M = Mn;
         }
-        const float inv = Mi.y;
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         uint32_t w4[CH / 2];
 #pragma unroll
         for (int k = 0; k < CH / 2; ++k) w4[k] = f2_to_bf2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
         uint4 *og = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + ((size_t)s * h_q + h) * D + d0);
         og[0] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         og[1] = make_uint4(w4[4], w4[5], w4[6], w4[7]);
+    }
+}
+
+// Window score of n tokens whose logits (lg_s [n][HQ], log2 units) and
+// score pieces (sc_s [HKV][RSF], token t of kv head h at h * RSF + t) are in
+// shared memory; the pieces are updated in place:
+//     piece[t] (+)= (1/w) max_{h in group} 2^(logit_h(t) - M_h) / L_h,
+// written instead of added at the first window row and for the newest token
+// (tok0 + t == P).  nthr is a multiple of HKV, so each thread keeps one kv
+// head and its group's (M, 1/L) in registers; it takes UN tokens at a time so
+// that their shared-memory loads are in flight together.
+template <int G, int HKV>
+__device__ __forceinline__ void score_tokens_smem(const float *lg_s, float *sc_s, int RSF, int n, int tok0, int P,
+                                                  bool first_row, float inv_w, const float2 *sm_stats, int ctid,
+                                                  int nthr) {
+    constexpr int HQ = G * HKV;
+    constexpr int UN = 1;
+    const int kvh = ctid % HKV;
+    const int TS = nthr / HKV;
+    // 2^(x - M) / L = 2^(x - c) with c = M + log2 L, so the max over the group
+    // is taken on x - c and needs one exp2 per (token, kv head); 1/L = 0 gives
+    // c = +inf and a zero score.
+    float c[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        const float2 st = sm_stats[kvh * G + j];
+        c[j] = st.x - log2f(st.y);
+    }
+    float *row = sc_s + kvh * RSF;
+    for (int t0 = ctid / HKV; t0 < n; t0 += UN * TS) {
+        float x[UN][G], old[UN];
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int t = t0 + u * TS;
+            if (t < n) {
+                const float *lg = lg_s + (size_t)t * HQ + kvh * G;
+                if constexpr (G % 4 == 0) {
+#pragma unroll
+                    for (int q4 = 0; q4 < G / 4; ++q4) {
+                        const float4 v = reinterpret_cast<const float4 *>(lg)[q4];
+                        x[u][4 * q4] = v.x;
+                        x[u][4 * q4 + 1] = v.y;
+                        x[u][4 * q4 + 2] = v.z;
+                        x[u][4 * q4 + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) x[u][j] = lg[j];
+                }
+                old[u] = row[t];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int t = t0 + u * TS;
+            if (t < n) {
+                float e = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < G; ++j) e = fmaxf(e, x[u][j] - c[j]);
+                const float best = exp2f(e);
+                row[t] = (first_row || tok0 + t == P) ? best * inv_w : old[u] + best * inv_w;
+            }
+        }
     }
 }
 
@@ -991,34 +1048,7 @@ __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, i
         }
         const bool got = mbar_wait_bounded(bar, bar_phase, a.err, abort, 60);
         bar_phase ^= 1u;
-        if (got) {
-            for (int it = ctid; it < n * HKV; it += nthr) {
-                const int t = it / HKV, kvh = it % HKV;
-                const int tok = c0 + t;
-                float x[G];
-                if constexpr (G % 4 == 0) {
-#pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const float4 v = reinterpret_cast<const float4 *>(lg_s + (size_t)t * HQ + kvh * G)[q4];
-                        x[4 * q4] = v.x;
-                        x[4 * q4 + 1] = v.y;
-                        x[4 * q4 + 2] = v.z;
-                        x[4 * q4 + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) x[j] = lg_s[(size_t)t * HQ + kvh * G + j];
-                }
-                float best = 0.f;
-#pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    const float2 st = sm_stats[kvh * G + j];
-                    best = fmaxf(best, exp2f(x[j] - st.x) * st.y);
-                }
-                float &dst = sc_s[kvh * RSF + t];
-                dst = (first_row || tok == P) ? best * inv_w : dst + best * inv_w;
-            }
-        }
+        if (got) score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, c0, P, first_row, inv_w, sm_stats, ctid, nthr);
         fence_proxy_async_smem();
         named_bar_sync(1, nthr);
         if (ctid == 0) {
@@ -1041,36 +1071,11 @@ __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, i
 template <int G, int HKV>
 __device__ void score_prefetched(const DecodeArgs &a, int s, int L, int tb, int n, int n16, const float *lg_s,
                                  float *sc_s, const float2 *sm_stats, int ctid, int nthr) {
-    constexpr int HQ = G * HKV;
     const int P = L - 1;
     const bool first_row = (P % a.b) == a.b - a.window;
     const float inv_w = 1.f / (float)a.window;
     const int RSF = n16 + 4;
-    for (int it = ctid; it < n * HKV; it += nthr) {
-        const int t = it / HKV, kvh = it % HKV;
-        float x[G];
-        if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int q4 = 0; q4 < G / 4; ++q4) {
-                const float4 v = reinterpret_cast<const float4 *>(lg_s + (size_t)t * HQ + kvh * G)[q4];
-                x[4 * q4] = v.x;
-                x[4 * q4 + 1] = v.y;
-                x[4 * q4 + 2] = v.z;
-                x[4 * q4 + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < G; ++j) x[j] = lg_s[(size_t)t * HQ + kvh * G + j];
-        }
-        float best = 0.f;
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            const float2 st = sm_stats[kvh * G + j];
-            best = fmaxf(best, exp2f(x[j] - st.x) * st.y);
-        }
-        float &dst = sc_s[kvh * RSF + t];
-        dst = (first_row || tb + t == P) ? best * inv_w : dst + best * inv_w;
-    }
+    score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, tb, P, first_row, inv_w, sm_stats, ctid, nthr);
     fence_proxy_async_smem();
     named_bar_sync(1, nthr);
     if (ctid == 0) {
@@ -1104,7 +1109,6 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     float2 *sm_stats = reinterpret_cast<float2 *>(smem + lay.merge_off + kEpiStats);
     int4 *segs = reinterpret_cast<int4 *>(smem + lay.merge_off + kEpiSeg);
     long long *cst = reinterpret_cast<long long *>(smem + lay.merge_off + kEpiCst);
-    float2 *sm_ml = reinterpret_cast<float2 *>(smem + lay.merge_off + kEpiMl);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -1279,6 +1283,15 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     reset_state();
     load_q(s);
     bool window_step = compute_window(s);
+    // The control words of the CTA's first and last sequence are read now (into
+    // the epilogue's statistics area, unused until after the announcement), so
+    // that announcing a part after the loop is usually one compare-and-swap.
+    if (warp == 0 && lane < 2) {
+        int s_last = s_first;
+        while (u1 > prefix[s_last + 1]) ++s_last;
+        if (lane == 0) *reinterpret_cast<int *>(smem + lay.merge_off + kEpiSLast) = s_last;
+        reinterpret_cast<unsigned long long *>(sm_stats)[lane] = ld_volatile_u64(a.ctl + (lane ? s_last : s_first));
+    }
 
     for (long long u = u0, i = 0; u < u1; ++u, ++i) {
         const int st = (int)(i % a.stages);
@@ -1479,77 +1492,88 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     // announce this CTA's parts of cut sequences (another warp than the
     // prefetch when there is one); the last arriver merges.  The barrier
     // above ordered every thread's partial records before this fence.
-    if (warp == (h_kv > 1 ? 1 : 0) && lane >= (h_kv > 1 ? 0 : 1) && lane < (h_kv > 1 ? 2 : 3)) {
-        const int i = lane - (h_kv > 1 ? 0 : 1);
+    const int ann_lane0 = h_kv > 1 ? 0 : 1;  // warp 0 lane 0 issues the prefetch when h_kv == 1
+    if (warp == (h_kv > 1 ? 1 : 0) && lane >= ann_lane0 && lane < ann_lane0 + 2) {
+        const int i = lane - ann_lane0;
         mlist[1 + i] = -1;
         if (i < mlist[4]) {
             const int sc = mlist[5 + i];
             int c_lo, c_hi;
             const int n_parts = parts_of(prefix[sc], prefix[sc + 1], cst, Gd, &c_lo, &c_hi);
-            __threadfence();
-            if (ctl_arrive(a.ctl + sc, n_parts, a.err)) mlist[1 + i] = sc;
-            __threadfence();
+            const unsigned long long *guess_w = reinterpret_cast<const unsigned long long *>(sm_stats);
+            const unsigned long long guess =
+                sc == s_first ? guess_w[0]
+                              : (sc == *reinterpret_cast<const int *>(smem + lay.merge_off + kEpiSLast) ? guess_w[1] : 0ull);
+            fence_acq_rel_gpu();  // release: the CTA's part records (ordered by the barrier above)
+            if (ctl_arrive(a.ctl + sc, n_parts, guess, a.err)) {
+                fence_acq_rel_gpu();  // acquire: the other parts' records
+                mlist[1 + i] = sc;
+            }
         }
     }
     named_bar_sync(1, nthr);
     pre_bytes = mlist[0];
     const int nseg = mlist[7];
-    const int *ms = mlist + 1;  // sequences this CTA merges (-1: none)
-    const bool merger = ms[0] >= 0 || ms[1] >= 0;
-    if (!a.want_score) {
-        if (merger) {
-            merge_stats(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
-            named_bar_sync(1, nthr);
-            merge_outputs<D>(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
-        }
-        return;
-    }
+    const int n_cut = mlist[4];  // this CTA's parts of cut sequences: mlist[5..6]; mlist[1 + i]: published by us
     bool waited_copies = false;
     unsigned ebar_phase = 0;
-    const int nsq = nseg >= 0 ? nseg : (s - s_first + 1);
-    // segments that need no other CTA first, then those waiting for a merge
+    // Every sequence of the range, in two passes: first those that need no
+    // other CTA (whole sequences, and cut sequences this CTA published as the
+    // last arrival), then the cut sequences published by another CTA.  For a
+    // cut sequence this CTA computes the final statistics from the part
+    // records, scores its own tokens and combines its slice of the output.
     for (int pass = 0; pass < 2; ++pass) {
-        for (int k = 0; k < nsq; ++k) {
-            int sq, tb, te;
-            if (nseg >= 0) {
-                const int4 g = segs[k];
-                sq = g.x, tb = g.y, te = g.z;
-            } else {
-                sq = s_first + k;
-                if (!compute_window(sq)) continue;
-            }
+        int kseg = 0;  // index of the next window segment in segs
+        for (int sq = s_first; sq <= s; ++sq) {
+            if (abort_flag[0]) break;  // set before a barrier by a thread that gave up: uniform
             const long long pb = prefix[sq], pe = prefix[sq + 1];
+            const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;
+            if (ue <= ub) continue;
+            const int L = lens[sq];
+            const int tb = (int)(ub - pb) * kTcTokens;
+            int te = (int)(ue - pb) * kTcTokens;
+            if (te > L) te = L;
+            const bool has_seg = compute_window(sq) && te > tb;  // the same rule that built segs
+            const int kk = kseg;
+            if (has_seg) ++kseg;
             const bool whole = pb >= u0 && pe <= u1;
-            const bool merged = (ms[0] == sq) || (ms[1] == sq);
-            const bool need_wait = !whole && !merged;
+            const int ci = (n_cut > 0 && mlist[5] == sq) ? 0 : ((n_cut > 1 && mlist[6] == sq) ? 1 : -1);
+            if (!whole && ci < 0) continue;  // (cannot happen: every cut part was announced)
+            if (whole && !has_seg) continue;
+            const bool last = !whole && mlist[1 + ci] == sq;
+            if (!a.want_score && !last) continue;  // without the score only the last arrival works
+            const bool need_wait = !whole && !last;
             if (need_wait != (pass == 1)) continue;
             if (need_wait) {
                 if (tid == 0) {
                     mlist[3] = ctl_wait_published(a.ctl + sq, a.err) ? 1 : 0;
-                    __threadfence();  // the part records are read after the publication
+                    fence_acq_rel_gpu();  // the part records are read after the publication
                 }
                 named_bar_sync(1, nthr);
                 const bool ok_flag = mlist[3] != 0;
                 named_bar_sync(1, nthr);
                 if (!ok_flag) continue;
             }
-            const int L = lens[sq];
             if (whole) {
                 for (int h = tid; h < HQ; h += nthr) {
                     const float2 ml = __ldcg(&a.stats[(size_t)sq * HQ + h]);
                     sm_stats[h] = make_float2(ml.x, ml.y > 0.f ? 1.f / ml.y : 0.f);
                 }
             } else {
-                part_stats(a, sq, prefix, cst, Gd, sm_stats, tid, nthr);
+                // the statistics for the score (threads below HQ) and this CTA's
+                // slice of the output (the others), their loads in flight together
+                const int t0 = has_seg && nthr - HQ >= 64 ? HQ : 0;
+                if (has_seg) part_stats(a, sq, prefix, cst, Gd, sm_stats, tid, t0 ? t0 : nthr);
+                merge_slice<D>(a, sq, prefix, cst, Gd, !a.want_score, tid, t0, nthr);
             }
-            if (nseg >= 0) {
+            if (has_seg && nseg >= 0) {
                 if (!waited_copies) {
                     waited_copies = true;
                     mbar_wait_bounded(ebar, 0, a.err, abort_flag, 61);  // every thread observes the copies
                 }
                 named_bar_sync(1, nthr);
-                if (abort_flag[0]) break;  // set before the barrier by any thread that gave up: uniform
-                const int4 g = segs[k];
+                if (abort_flag[0]) break;
+                const int4 g = segs[kk];
                 const int n = te - tb, n16 = (n + 15) & ~15;
                 float *lg_s = reinterpret_cast<float *>(scratch + g.w);
                 float *sc_s = lg_s + (size_t)n16 * HQ;
@@ -1557,12 +1581,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 else if (h_kv == 4) score_prefetched<G, 4>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
                 else if (h_kv == 2) score_prefetched<G, 2>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
                 else score_prefetched<G, 1>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
-                named_bar_sync(1, nthr);  // sm_stats reused by the next segment
-            } else {
-                const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;  // this CTA's units of sq
-                tb = (int)(ub - pb) * kTcTokens;
-                te = (int)(ue - pb) * kTcTokens;
-                if (te > L) te = L;
+            } else if (has_seg) {
                 if (h_kv == 8)
                     score_segment<G, 8>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
                                         abort_flag, sm_stats, tid, nthr);
@@ -1575,17 +1594,13 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 else
                     score_segment<G, 1>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
                                         abort_flag, sm_stats, tid, nthr);
+            } else {
+                named_bar_sync(1, nthr);  // sm_stats complete
             }
+            named_bar_sync(1, nthr);  // sm_stats reused by the next sequence
         }
-        if (abort_flag[0]) break;
     }
     if (nseg > 0 && !waited_copies && tid == 0) mbar_wait_bounded(ebar, 0, a.err, abort_flag, 62);
-    if (merger) {  // the outputs of the merged sequences, off the other CTAs' path
-        named_bar_sync(1, nthr);
-        merge_stats(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
-        named_bar_sync(1, nthr);
-        merge_outputs<D>(a, ms, prefix, cst, Gd, sm_ml, tid, nthr);
-    }
     if (tid == 0) bulk_wait_read_all();  // shared-memory sources read; the writes complete on their own
 }
 
