@@ -1094,6 +1094,10 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     static_assert(G >= 1 && G <= 8, "group of at most 8 q heads");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    // A kernel launched after this one as its programmatic dependent (the
+    // compression's first kernel) may be scheduled on the SMs this grid
+    // leaves; it reads nothing this kernel writes before waiting for it.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int B = a.B;
     const int h_kv = a.h_kv;
     const SmemLayout lay = make_tc_layout(a.stages, h_kv, HALVES, B, gridDim.x);

@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // lightning rule as in lightning_tc_kernel.
 template <int D>
 __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
+    // the finish kernel may be scheduled once every CTA of this grid runs; it
+    // waits for this grid's completion before reading its output
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const ScoreArgs a = at_layer(a0, blockIdx.z);
     extern __shared__ __align__(128) unsigned char gsm[];
     __shared__ __align__(8) uint64_t bar;
@@ -377,6 +380,11 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
             for (int t = 0; t < nvalid; ++t) bulk_g2s_plain(gsm + t * RS, src + (size_t)t * row_bytes, row_bytes, &bar);
         }
     }
+    // Launched as a programmatic dependent of the preceding kernel (the decode
+    // call, when it precedes): the lengths, the block table and the keys read
+    // above are not written by it; the score rows and F below are read after
+    // its completion.  A no-op for a plain launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     const int blk = s_blk;
     if (blk < 0 || blk >= a.n_total) return;
@@ -731,26 +739,39 @@ struct MoveArgs {
     long long F_layer;       // elements between layers of F
 };
 
-constexpr int kFsThreads = 512;
+constexpr int kFsThreads = 1024;
 constexpr int kFsChunk = 128;      // ranks per move round
-constexpr int kFsVecPerThread = 8; // 16-byte registers per thread and round (row pieces up to 256 B)
+constexpr int kFsVecPerThread = 4; // 16-byte registers per thread and round (row pieces up to 256 B)
 
+// xs, fs [Lmax]; keep, source row, F value, target row [k]; target blocks
+// [ceil(k / b)]; the sequence's table row [ceil(Lmax / b)]
 __host__ __device__ inline size_t fused_smem(int Lmax, int k, int b) {
-    return (size_t)Lmax * 8 + (size_t)k * 12 + (size_t)((k + b - 1) / b) * 4 + 64;
+    return (size_t)Lmax * 8 + (size_t)k * 16 + (size_t)((k + b - 1) / b) * 4 + (size_t)((Lmax + b - 1) / b) * 4 + 64;
 }
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red) {
+// Block-wide combination of per-thread online-softmax pairs (max m, sum s of
+// 2^(y - m)): M = max m, S = sum s * 2^(m - M).  red: 64 floats.
+__device__ __forceinline__ float2 block_reduce_maxsum(float m, float s, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int o = 16; o; o >>= 1) {
-        const float y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        v = is_max ? fmaxf(v, y) : v + y;
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        const float M = fmaxf(m, m2);
+        s = (M == -INFINITY) ? 0.f : s * exp2f(m - M) + s2 * exp2f(m2 - M);
+        m = M;
     }
     __syncthreads();
-    if (lane == 0) red[warp] = v;
+    if (lane == 0) {
+        red[warp] = m;
+        red[32 + warp] = s;
+    }
     __syncthreads();
-    float t = is_max ? -INFINITY : 0.f;
-    for (int w = 0; w < nw; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
-    return t;
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, red[w]);
+    float S = 0.f;
+    if (M != -INFINITY)
+        for (int w = 0; w < nw; ++w) S += red[32 + w] * exp2f(red[w] - M);
+    return make_float2(M, S);
 }
 
 __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a0, const MoveArgs m0) {
@@ -764,17 +785,24 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
     if (m0.tie) m.tie = m0.tie + (size_t)z * a0.n * a0.h_kv;
     extern __shared__ __align__(16) unsigned char fsm[];
     __shared__ SelectShared sh;
-    __shared__ float red[32];
+    __shared__ float red[64];
     const int kvh = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
     const int L = clamp_len(a, s);
     float *xs = reinterpret_cast<float *>(fsm);
     float *fs = xs + a.Lmax;
     int *keep_s = reinterpret_cast<int *>(fs + a.Lmax);
-    int *src_s = keep_s + m.k;
-    float *fv_s = reinterpret_cast<float *>(src_s + m.k);
-    int *dst_s = reinterpret_cast<int *>(fv_s + m.k);
+    int *src_s = keep_s + m.k;                              // source row (token, kv head) of rank i, -1: none
+    float *fv_s = reinterpret_cast<float *>(src_s + m.k);  // global score of rank i
+    int *drow_s = reinterpret_cast<int *>(fv_s + m.k);     // target row of rank i, -1: bad target
+    int *dst_s = drow_s + m.k;
     const int nt = (m.k + a.b - 1) / a.b;
+    int *tbl_s = dst_s + nt;
+    const int nb = (L + a.b - 1) / a.b;
     for (int t = tid; t < nt; t += nthr) dst_s[t] = m.dst[(size_t)s * m.target_stride + t];
+    for (int t = tid; t < nb; t += nthr) tbl_s[t] = a.table[(size_t)s * a.table_stride + t];
+    // launched as a programmatic dependent of the scores kernel: X, rho and the
+    // score rows are read after its completion (a no-op for a plain launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
     for (int t = tid; t < L; t += nthr) {
         xs[t] = a.X[row + t];
@@ -785,26 +813,38 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
     const bool first = a.first ? a.first[s] != 0 : true;
     const bool pool = a.pool_kernel > 1 && (a.pool_policy == 2 || (a.pool_policy == 1 && first));
     const int r = a.pool_kernel / 2;
-    const float inv = 1.f / ((float)L * a.tau);
-    float rmax = 0.f, rsum = 1.f;
+    // R = softmax(rho / (L tau)) in base 2: one pass for the max and the sum
+    // (online), one block reduction of the (max, sum) pairs
+    const float inv2 = 1.4426950408889634f / ((float)L * a.tau);
+    float rmax = 0.f, rinv = 1.f;
     if (a.use_sim && L > 0) {
-        float mx = -INFINITY;
-        for (int t = tid; t < L; t += nthr) mx = fmaxf(mx, fs[t] * inv);
-        rmax = block_reduce(mx, true, red);
-        float sm = 0.f;
-        for (int t = tid; t < L; t += nthr) sm += expf(fs[t] * inv - rmax);
-        rsum = block_reduce(sm, false, red);
+        float mx = -INFINITY, sm = 0.f;
+        for (int t = tid; t < L; t += nthr) {
+            const float y = fs[t] * inv2;
+            if (y > mx) {
+                sm = sm * exp2f(mx - y) + 1.f;
+                mx = y;
+            } else {
+                sm += exp2f(y - mx);
+            }
+        }
+        const float2 ms = block_reduce_maxsum(mx, sm, red);
+        rmax = ms.x;
+        rinv = 1.f / ms.y;
     }
     for (int t = tid; t < L; t += nthr) {
-        float v;
-        if (pool) {
+        float v = xs[t];
+        if (pool && r <= 8) {
+            // the window's loads unrolled (clamped indices repeat an element,
+            // which leaves the max unchanged)
+#pragma unroll
+            for (int j = 1; j <= 8; ++j)
+                if (j <= r) v = fmaxf(v, fmaxf(xs[max(t - j, 0)], xs[min(t + j, L - 1)]));
+        } else if (pool) {
             const int lo = max(0, t - r), hi = min(L - 1, t + r);
-            v = xs[lo];
-            for (int j = lo + 1; j <= hi; ++j) v = fmaxf(v, xs[j]);
-        } else {
-            v = xs[t];
+            for (int j = lo; j <= hi; ++j) v = fmaxf(v, xs[j]);
         }
-        if (a.use_sim) v -= a.lambda * (expf(fs[t] * inv - rmax) / rsum);
+        if (a.use_sim) v -= a.lambda * (exp2f(fs[t] * inv2 - rmax) * rinv);
         if (t >= L - a.window) v = INFINITY;
         fs[t] = v;
         if (a.out) a.out[row + t] = v;
@@ -828,47 +868,50 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
     } else {
         block_select_topk(fs, L, ki, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
     }
-    // ---- move this kv head's kept rows (Alg. 4 with the target blocks)
+    // ---- move this kv head's kept rows (Alg. 4 with the target blocks).
+    // Rank i: source row (block of its token, from the table row in shared
+    // memory), target row (slot i of target block i / b) and its global score
+    // (X, the value the compaction stores into F).  b = 16 and the 16-byte
+    // vectors per row piece are a power of two on this path, so the item
+    // indices below are shifts.
     const int kk = min(ki, L);
-    const float *Srow = nullptr;
     float *F = m.F;
-    if (F) {
-        const int rs = a.S_rows ? a.S_rows[s] : s;
-        if (rs < 0) {
-            if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x402);
-            F = nullptr;
-        } else {
-            Srow = a.S + ((size_t)rs * a.h_kv + kvh) * a.S_stride;
-        }
+    if (F && a.S_rows && a.S_rows[s] < 0) {
+        if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x402);
+        F = nullptr;
     }
     for (int i = tid; i < kk; i += nthr) {
         const int pos = keep_s[i];
-        int blk = -1;
-        if (pos >= 0 && pos < L) blk = a.table[(size_t)s * a.table_stride + pos / a.b];
+        int blk = (pos >= 0 && pos < L) ? tbl_s[pos >> 4] : -1;
         if (blk < 0 || blk >= a.n_total) {
             record_error(a.err, ZP_ERR_DEVICE, 0x400);
             blk = -1;
         }
-        src_s[i] = blk;
-        if (F) fv_s[i] = blk >= 0 ? Srow[pos] : 0.f;
+        src_s[i] = blk >= 0 ? (blk * 16 + (pos & 15)) * a.h_kv + kvh : -1;
+        fv_s[i] = blk >= 0 ? xs[pos] : 0.f;
+        const int tblk = dst_s[i >> 4];
+        if (tblk < 0 || tblk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x401);
+            drow_s[i] = -1;
+        } else {
+            drow_s[i] = (tblk * 16 + (i & 15)) * a.h_kv + kvh;
+        }
     }
     __syncthreads();
-    const int per_rank = 2 * m.row_vec;
-    const int chunk = min(kFsChunk, kFsThreads * kFsVecPerThread / per_rank);
+    const int rv = m.row_vec, rv_sh = 31 - __clz(rv);
+    const int pr_sh = rv_sh + 1;  // 16-byte vectors per rank (K and V pieces)
+    const int chunk = min(kFsChunk, (kFsThreads * kFsVecPerThread) >> pr_sh);
     for (int r0 = 0; r0 < kk; r0 += chunk) {
         const int nr = min(chunk, kk - r0);
-        const int items = nr * per_rank;
+        const int items = nr << pr_sh;
         uint4 buf[kFsVecPerThread];
 #pragma unroll
         for (int i = 0; i < kFsVecPerThread; ++i) {
             const int it = tid + i * kFsThreads;
             if (it < items) {
-                const int rr = r0 + it / per_rank, v = it % per_rank;
-                const int blk = src_s[rr];
-                if (blk >= 0) {
-                    const size_t rw = ((size_t)blk * a.b + keep_s[rr] % a.b) * a.h_kv + kvh;
-                    buf[i] = (v < m.row_vec ? m.K : m.V)[rw * m.row_vec + (v % m.row_vec)];
-                }
+                const int rr = r0 + (it >> pr_sh), v = it & ((rv << 1) - 1);
+                const int sr = src_s[rr];
+                if (sr >= 0) buf[i] = (v < rv ? m.K : m.V)[(size_t)sr * rv + (v & (rv - 1))];
             }
         }
         __syncthreads();
@@ -876,21 +919,15 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
         for (int i = 0; i < kFsVecPerThread; ++i) {
             const int it = tid + i * kFsThreads;
             if (it < items) {
-                const int rr = r0 + it / per_rank, v = it % per_rank;
-                const int blk = dst_s[rr / a.b];
-                if (blk < 0 || blk >= a.n_total) {
-                    record_error(a.err, ZP_ERR_DEVICE, 0x401);
-                } else if (src_s[rr] >= 0) {
-                    const size_t rw = ((size_t)blk * a.b + rr % a.b) * a.h_kv + kvh;
-                    (v < m.row_vec ? m.K : m.V)[rw * m.row_vec + (v % m.row_vec)] = buf[i];
-                }
+                const int rr = r0 + (it >> pr_sh), v = it & ((rv << 1) - 1);
+                const int dr = drow_s[rr];
+                if (dr >= 0 && src_s[rr] >= 0) (v < rv ? m.K : m.V)[(size_t)dr * rv + (v & (rv - 1))] = buf[i];
             }
         }
         if (F)
             for (int i = tid; i < nr; i += nthr) {
-                const int rr = r0 + i;
-                const int blk = dst_s[rr / a.b];
-                if (blk >= 0 && blk < a.n_total) F[((size_t)blk * a.b + rr % a.b) * a.h_kv + kvh] = fv_s[rr];
+                const int dr = drow_s[r0 + i];
+                if (dr >= 0) F[dr] = fv_s[r0 + i];
             }
         __syncthreads();  // the next round's loads follow this round's stores
     }
@@ -980,18 +1017,21 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         // global score and redundancy of each block in one kernel
         const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
         dim3 g2((Lmax + 15) / 16, n, layers);
-        if (a.d == 128) {
-            if (smem > 48 * 1024)
-                cudaFuncSetAttribute(global_lightning_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
-            global_lightning_kernel<128><<<g2, a.h_kv * 32, smem, st>>>(a);
-        } else {
-            if (smem > 48 * 1024)
-                cudaFuncSetAttribute(global_lightning_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem);
-            global_lightning_kernel<64><<<g2, a.h_kv * 32, smem, st>>>(a);
-        }
-        cudaError_t e = cudaGetLastError();
+        auto kern = a.d == 128 ? global_lightning_kernel<128> : global_lightning_kernel<64>;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // programmatic dependent launch: the CTAs may start on SMs that the
+        // preceding kernel has left and fetch their keys while it drains
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = g2;
+        cfg.blockDim = dim3(a.h_kv * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
         if (e != cudaSuccess) return cuda_fail(e, "score: global/lightning launch");
         *launched = true;
         return ok();
@@ -1142,8 +1182,20 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return cuda_fail(e, "compress: cudaFuncSetAttribute");
         }
-        finalize_select_move_kernel<<<dim3(a.h_kv, n, layer_count), kFsThreads, smem, st>>>(a, m);
-        cudaError_t e = cudaGetLastError();
+        // programmatic dependent launch: the finish grid may start while the
+        // scores kernel drains; it reads that kernel's output only after
+        // griddepcontrol.wait
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.h_kv, n, layer_count);
+        cfg.blockDim = dim3(kFsThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, finalize_select_move_kernel, a, m);
         if (e != cudaSuccess) return cuda_fail(e, "compress: launch");
         return ok();
     }
