@@ -348,9 +348,6 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // lightning rule as in lightning_tc_kernel.
 template <int D>
 __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
-    // the finish kernel may be scheduled once every CTA of this grid runs; it
-    // waits for this grid's completion before reading its output
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const ScoreArgs a = at_layer(a0, blockIdx.z);
     extern __shared__ __align__(128) unsigned char gsm[];
     __shared__ __align__(8) uint64_t bar;
@@ -412,6 +409,11 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     }
     mbar_wait_bounded(&bar, 0, a.err, &s_abort, 0x203);
     __syncthreads();
+    // the finish kernel may be scheduled once every CTA of this grid is this
+    // far (late, so that its waiting CTAs do not take the SM slots of this
+    // grid's later CTAs); it waits for this grid's completion before reading
+    // its output
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (s_abort || warp >= h_kv) return;
     constexpr int KS = D / 16;
     const int kvh = warp;
@@ -766,12 +768,17 @@ __device__ __forceinline__ float2 block_reduce_maxsum(float m, float s, float *r
         red[32 + warp] = s;
     }
     __syncthreads();
-    float M = -INFINITY;
-    for (int w = 0; w < nw; ++w) M = fmaxf(M, red[w]);
-    float S = 0.f;
-    if (M != -INFINITY)
-        for (int w = 0; w < nw; ++w) S += red[32 + w] * exp2f(red[w] - M);
-    return make_float2(M, S);
+    // every warp combines the per-warp pairs by the same shuffle tree
+    m = lane < nw ? red[lane] : -INFINITY;
+    s = lane < nw ? red[32 + lane] : 0.f;
+    for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        const float M = fmaxf(m, m2);
+        s = (M == -INFINITY) ? 0.f : s * exp2f(m - M) + s2 * exp2f(m2 - M);
+        m = M;
+    }
+    return make_float2(m, s);
 }
 
 __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a0, const MoveArgs m0) {
@@ -804,9 +811,22 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
     // score rows are read after its completion (a no-op for a plain launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
-    for (int t = tid; t < L; t += nthr) {
-        xs[t] = a.X[row + t];
-        fs[t] = a.use_sim ? a.rho[row + t] : 0.f;
+    for (int t0 = tid; t0 < L; t0 += 4 * nthr) {  // four elements' loads in flight per thread
+        float xv[4], rv4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = t0 + i * nthr;
+            xv[i] = t < L ? a.X[row + t] : 0.f;
+            rv4[i] = (t < L && a.use_sim) ? a.rho[row + t] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = t0 + i * nthr;
+            if (t < L) {
+                xs[t] = xv[i];
+                fs[t] = rv4[i];
+            }
+        }
     }
     __syncthreads();
     // ---- final scores (App. C.4-C.8, eq. 4, window), in place of rho
