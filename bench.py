@@ -179,17 +179,29 @@ class Workload:
         self.desc = zp.cache_desc(h_q, h_kv, d, b, c.n_total, tdt)
         self.K = c.k_cache[0].contiguous().to(dev)
         self.V = c.v_cache[0].contiguous().to(dev)
-        self.q = c.q.to(dev)
+        # a step's inputs (q, the new keys and values) are views of one device
+        # buffer, its results (outputs, keep sets) of another, so that the
+        # end-to-end step moves each direction in one copy
+        n_q, n_kv = B * h_q * d, B * h_kv * d
+        self.in_dev = torch.empty(n_q + 2 * n_kv, dtype=tdt, device=dev)
+        self.q = self.in_dev[:n_q].view(B, h_q, d)
+        self.q.copy_(c.q.to(dev))
         self.table = c.block_table.to(dev)
         self.lens = c.seq_lens.to(dev)
-        self.out = torch.empty_like(self.q)
+        lens0 = c.seq_lens.tolist()
+        n_comp0 = sum(1 for L in lens0 if zp.zp_needs_compression(L, b, N_max))
+        out_bytes = n_q * self.q.element_size()
+        self.out_dev = torch.empty(out_bytes + n_comp0 * h_kv * self.k * 4, dtype=torch.uint8, device=dev)
+        self.out = self.out_dev[:out_bytes].view(tdt).view(B, h_q, d)
         # attention score: one row per (sequence, kv head) over the table's capacity;
         # global score F: paged like K
         self.S = torch.zeros(B, h_kv, c.block_table.shape[1] * b, dtype=torch.float32, device=dev)
         self.F = torch.zeros(c.n_total, b, h_kv, dtype=torch.float32, device=dev)
         g = torch.Generator().manual_seed(seed + seed_offset + 7)
-        self.k_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
-        self.v_new = torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev)
+        self.k_new = self.in_dev[n_q:n_q + n_kv].view(B, h_kv, d)
+        self.v_new = self.in_dev[n_q + n_kv:].view(B, h_kv, d)
+        self.k_new.copy_(torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev))
+        self.v_new.copy_(torch.randn(B, h_kv, d, generator=g).to(tdt).to(dev))
         self.ws = torch.empty(zp.zp_decode_workspace_size(self.desc, B, c.table_stride),
                               dtype=torch.uint8, device=dev)
         # compression set: sequences whose trigger holds at their length
@@ -209,7 +221,7 @@ class Workload:
             self.c_Lmax = int(c.seq_lens[idx].max())
             self.c_first = torch.ones(n, dtype=torch.uint8, device=dev)
             self.c_scores = torch.empty(n, h_kv, self.c_Lmax, dtype=torch.float32, device=dev)
-            self.c_keep = torch.empty(n, h_kv, self.k, dtype=torch.int32, device=dev)
+            self.c_keep = self.out_dev[out_bytes:].view(torch.int32).view(n, h_kv, self.k)
             self.c_ws = torch.empty(max(zp.zp_compress_workspace_size(self.desc, n, self.c_Lmax), 1),
                                     dtype=torch.uint8, device=dev)
             self.params = zp.score_params(window=self.w)
@@ -219,11 +231,8 @@ class Workload:
             self.plan_out = plan
             self.c_targets = torch.from_numpy(plan["targets"].copy()).to(dev)
         # pinned host copies for the end-to-end figure
-        self.host_q = self.q.cpu().pin_memory()
-        self.h_k_new = self.k_new.cpu().pin_memory()
-        self.h_v_new = self.v_new.cpu().pin_memory()
-        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.h_keep = (torch.empty(self.c_keep.shape, dtype=torch.int32).pin_memory() if n else None)
+        self.in_host = self.in_dev.cpu().pin_memory()
+        self.out_host = torch.empty(self.out_dev.shape, dtype=torch.uint8).pin_memory()
 
     def _plan(self, s):
         b, N_max = self.b, self.N_max
@@ -334,22 +343,16 @@ class Workload:
         return graphs, events
 
     def step_e2e(self):
-        """Same step through the public calls with host buffers: H2D of q and
-        the new k/v from pinned memory, D2H of the outputs and keep sets."""
-        self.q.copy_(self.host_q, non_blocking=True)
-        self.k_new.copy_(self.h_k_new, non_blocking=True)
-        self.v_new.copy_(self.h_v_new, non_blocking=True)
+        """Same step through the public calls with host buffers: one H2D copy
+        of q and the new k/v (packed) from pinned memory, one D2H copy of the
+        outputs and keep sets (packed)."""
+        self.in_dev.copy_(self.in_host, non_blocking=True)
         self.step()
-        self.h_out.copy_(self.out, non_blocking=True)
-        if self.n_comp:
-            self.h_keep.copy_(self.c_keep, non_blocking=True)
+        self.out_host.copy_(self.out_dev, non_blocking=True)
 
     def e2e_bytes(self):
-        bi = sum(t.numel() * t.element_size() for t in (self.host_q, self.h_k_new, self.h_v_new))
-        bo = self.h_out.numel() * self.h_out.element_size()
-        if self.n_comp:
-            bo += self.h_keep.numel() * 4
-        return bi, bo
+        return (self.in_host.numel() * self.in_host.element_size(),
+                self.out_host.numel() * self.out_host.element_size())
 
 
 def _dist():
