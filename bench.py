@@ -281,8 +281,9 @@ class Workload:
         return tot
 
     def launches_per_step(self) -> int:
-        # append; decode (one cooperative kernel); scores: global, redundancy, finish with selection and move
-        return 1 + 1 + (3 if self.n_comp else 0)
+        # append; decode (one cooperative kernel); compression: global score and
+        # redundancy, then the finish with selection and move
+        return 1 + 1 + (2 if self.n_comp else 0)
 
     # ---- the step
     def decode(self, stream=None):
