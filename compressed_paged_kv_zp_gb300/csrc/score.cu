@@ -346,77 +346,16 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // gather_global_kernel) from the score rows and F.  Then G = K K^T per head
 // on the tensor cores (16 mma.sync), and on the accumulator fragments the
 // lightning rule as in lightning_tc_kernel.
+// Lightning redundancy of one block for kv head `kvh` (one warp): the block's
+// token rows (all kv heads, row stride RS) are in shared memory; G = K K^T on
+// the tensor cores (16 mma.sync), then on the accumulator fragments: cosine
+// (zero-norm keys give 0), zero diagonal, per column the newest row above p
+// zeroed, row sums written to rho.  myn: 16 floats of this warp's shared memory.
 template <int D>
-__global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
-    const ScoreArgs a = at_layer(a0, blockIdx.z);
-    extern __shared__ __align__(128) unsigned char gsm[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int s_blk, s_abort;
-    __shared__ float nrm[16][16];
-    const int s = blockIdx.y;
-    const int bi = blockIdx.x;
-    const int L = clamp_len(a, s);
-    const int tb0 = bi * 16;
-    if (tb0 >= L) return;
-    const int nvalid = min(16, L - tb0);
+__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int RS, int nvalid,
+                                                int s, int tb0, float *myn, int kvh, int lane) {
     const int h_kv = a.h_kv;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const unsigned row_bytes = (unsigned)(h_kv * D * 2);
-    const int RS = (int)row_bytes + 16;
-    if (tid == 0) {
-        const int blk = a.table[(size_t)s * a.table_stride + bi];
-        s_blk = blk;
-        s_abort = 0;
-        mbar_init(&bar, 1);
-        fence_barrier_init();
-        if (blk < 0 || blk >= a.n_total) {
-            record_error(a.err, ZP_ERR_DEVICE, 0x202);
-        } else {
-            mbar_arrive_expect_tx(&bar, row_bytes * (unsigned)nvalid);
-            const char *src = static_cast<const char *>(a.k) + (size_t)blk * 16 * row_bytes;
-            for (int t = 0; t < nvalid; ++t) bulk_g2s_plain(gsm + t * RS, src + (size_t)t * row_bytes, row_bytes, &bar);
-        }
-    }
-    // Launched as a programmatic dependent of the preceding kernel (the decode
-    // call, when it precedes): the lengths, the block table and the keys read
-    // above are not written by it; the score rows and F below are read after
-    // its completion.  A no-op for a plain launch.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    __syncthreads();
-    const int blk = s_blk;
-    if (blk < 0 || blk >= a.n_total) return;
-    // ---- global score of the block's tokens (while the rows are in flight)
-    {
-        const int N = (L + a.b - 1) / a.b;
-        const bool first = a.first ? a.first[s] != 0 : true;
-        const bool read_F = a.use_global && !first && bi != N - 1;
-        const int row = a.S_rows ? a.S_rows[s] : s;
-        for (int it = tid; it < nvalid * h_kv; it += blockDim.x) {
-            const int kvh = it / nvalid, tl = it % nvalid;
-            const int t = tb0 + tl;
-            if (row < 0) {
-                record_error(a.err, ZP_ERR_DEVICE, 0x202);
-                continue;
-            }
-            float *sp = a.S + ((size_t)row * h_kv + kvh) * a.S_stride + t;
-            float v = *sp;
-            if (read_F) {
-                v = fmaxf(a.alpha * a.F[((size_t)blk * a.b + tl) * h_kv + kvh], v);
-                *sp = v;
-            }
-            a.X[((size_t)s * h_kv + kvh) * a.Lmax + t] = v;
-        }
-    }
-    mbar_wait_bounded(&bar, 0, a.err, &s_abort, 0x203);
-    __syncthreads();
-    // the finish kernel may be scheduled once every CTA of this grid is this
-    // far (late, so that its waiting CTAs do not take the SM slots of this
-    // grid's later CTAs); it waits for this grid's completion before reading
-    // its output
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (s_abort || warp >= h_kv) return;
     constexpr int KS = D / 16;
-    const int kvh = warp;
     const int g = lane >> 2, tig = lane & 3;
     const int lm = lane >> 3;
     const int lrow = (lm & 1) * 8 + (lane & 7);  // matrices: (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
@@ -431,7 +370,6 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
     // rows >= nvalid were not copied: every entry they touch is masked below
-    float *myn = nrm[warp];
     if (tig == (g >> 1)) myn[g] = c0[g & 1];
     if (tig == (g >> 1)) myn[g + 8] = c1[2 + (g & 1)];
     __syncwarp();
@@ -480,6 +418,79 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
         if (g + 8 < nvalid) out[g + 8] = rs1;
     }
 }
+
+template <int D>
+__global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
+    const ScoreArgs a = at_layer(a0, blockIdx.z);
+    extern __shared__ __align__(128) unsigned char gsm[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_blk, s_abort;
+    __shared__ float nrm[16][16];
+    const int s = blockIdx.y;
+    const int bi = blockIdx.x;
+    const int L = clamp_len(a, s);
+    const int tb0 = bi * 16;
+    if (tb0 >= L) return;
+    const int nvalid = min(16, L - tb0);
+    const int h_kv = a.h_kv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned row_bytes = (unsigned)(h_kv * D * 2);
+    const int RS = (int)row_bytes + 16;
+    if (tid == 0) {
+        const int blk = a.table[(size_t)s * a.table_stride + bi];
+        s_blk = blk;
+        s_abort = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (blk < 0 || blk >= a.n_total) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        } else {
+            mbar_arrive_expect_tx(&bar, row_bytes * (unsigned)nvalid);
+            const char *src = static_cast<const char *>(a.k) + (size_t)blk * 16 * row_bytes;
+            for (int t = 0; t < nvalid; ++t) bulk_g2s_plain(gsm + t * RS, src + (size_t)t * row_bytes, row_bytes, &bar);
+        }
+    }
+    __syncthreads();
+    const int blk = s_blk;
+    if (blk < 0 || blk >= a.n_total) return;
+    // This kernel is launched as a programmatic dependent of the preceding one
+    // (the decode call, when it precedes), which writes the score rows but not
+    // the lengths, the block table, the keys or F: everything but the score
+    // rows is read, and the redundancy computed, before griddepcontrol.wait.
+    // Global score (Alg. 2) of this thread's (kv head, token) of the block:
+    // F read now, the score row after the wait.
+    const int N = (L + a.b - 1) / a.b;
+    const bool first = a.first ? a.first[s] != 0 : true;
+    const bool read_F = a.use_global && !first && bi != N - 1;
+    const int row = a.S_rows ? a.S_rows[s] : s;
+    const int g_kvh = tid / nvalid, g_tl = tid % nvalid;  // one item per thread: 16 * h_kv <= blockDim
+    const bool g_on = tid < nvalid * h_kv;
+    const float fv = (g_on && read_F) ? a.F[((size_t)blk * a.b + g_tl) * h_kv + g_kvh] : 0.f;
+    mbar_wait_bounded(&bar, 0, a.err, &s_abort, 0x203);
+    __syncthreads();
+    // the finish kernel may be scheduled once every CTA of this grid is this
+    // far (late, so that its waiting CTAs do not take the SM slots of this
+    // grid's later CTAs); it waits for this grid's completion before reading
+    // its output
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (s_abort) return;
+    lightning_block<D>(a, gsm, RS, nvalid, s, tb0, nrm[warp], warp, lane);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (g_on) {
+        if (row < 0) {
+            record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        } else {
+            float *sp = a.S + ((size_t)row * h_kv + g_kvh) * a.S_stride + tb0 + g_tl;
+            float v = *sp;
+            if (read_F) {
+                v = fmaxf(a.alpha * fv, v);
+                *sp = v;
+            }
+            a.X[((size_t)s * h_kv + g_kvh) * a.Lmax + tb0 + g_tl] = v;
+        }
+    }
+}
+
 
 // All-pairs ("flash") redundancy [App. C.5, Fig. 11, Alg. 3] for bf16 keys,
 // in O(L) memory.  The definition zeroes, in every column c of the cosine
