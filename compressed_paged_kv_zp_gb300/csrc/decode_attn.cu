@@ -704,13 +704,12 @@ __global__ void __launch_bounds__(128) decode_score_kernel(const DecodeArgs a) {
 // second product; the scores and the softmax statistics stay in fp32.
 constexpr int kTcTokens = 16;     // tokens per unit
 // Epilogue region of shared memory: 8 ints, an mbarrier, the CTA's last
-// sequence (for the announcement), (max, 1/sum) of up to
-// 64 q heads, up to kMaxSeg window segments {sequence, first token, end token,
-// byte offset}, the merged sequences' (max, 1/sum), then the first unit of
-// every CTA (grid + 1 long longs).
+// sequence (for the announcement), (max, 1/sum) of up to 64 q heads (before
+// the announcement: the control words read ahead), up to kMaxSeg window
+// segments {sequence, first token, end token, byte offset}, then the first
+// unit of every CTA (grid + 1 long longs).
 constexpr int kEpiBar = 32, kEpiSLast = 40, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
-constexpr int kEpiMl = kEpiSeg + kMaxSeg * 16;  // (M, 1/L) of the merged sequences: 2 x 64 float2
-constexpr int kEpiCst = kEpiMl + 2 * 64 * 8;
+constexpr int kEpiCst = kEpiSeg + kMaxSeg * 16;
 constexpr int kTcPad = 16;        // bytes of padding after each staged token row
 
 __host__ __device__ inline int tc_row_stride(int h_kv, int d) { return h_kv * d * 2 + kTcPad; }
@@ -739,10 +738,12 @@ __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int h
 // ---------------------------------------------------------------------------
 // In-kernel epilogue of the tensor-core path (cooperative launch: every CTA is
 // resident).  After its main loop a CTA announces its parts of the sequences
-// cut between CTAs (at most its first and its last); the last CTA to announce
-// merges the sequence, then publishes it.  Every CTA then computes the window
-// score of its own units, waiting (bounded) only for the publication of its
-// cut sequences.  Merges never wait, so every publication happens.
+// cut between CTAs (at most its first and its last); the last arrival
+// publishes the sequence.  Every CTA then works through its sequences: the
+// final statistics of a cut sequence come from the part records once it is
+// published (a bounded wait unless this CTA published it), each part-holder
+// combines its slice of the output, and every CTA computes the window score
+// of its own units.  An arrival never waits, so every publication happens.
 //
 // Per-sequence control word (64 bits): (kCtlTag << 16) | phase << 15 | count.
 // Phase 0 counts arrivals; the last arrival sets phase 1 ("published": every
@@ -1444,7 +1445,6 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     asm volatile("fence.proxy.async.global;" ::: "memory");
     fence_proxy_async_smem();
     named_bar_sync(1, nthr);
-    int pre_bytes = 0;  // bytes of the stage area taken by prefetched segments (diagnostic)
     if (warp == 0) {
         if (lane == 0) {
             // window segments of this CTA and, if they all fit, their prefetch
@@ -1494,7 +1494,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         }
     }
     // announce this CTA's parts of cut sequences (another warp than the
-    // prefetch when there is one); the last arriver merges.  The barrier
+    // prefetch when there is one); the last arrival publishes.  The barrier
     // above ordered every thread's partial records before this fence.
     const int ann_lane0 = h_kv > 1 ? 0 : 1;  // warp 0 lane 0 issues the prefetch when h_kv == 1
     if (warp == (h_kv > 1 ? 1 : 0) && lane >= ann_lane0 && lane < ann_lane0 + 2) {
@@ -1516,7 +1516,6 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         }
     }
     named_bar_sync(1, nthr);
-    pre_bytes = mlist[0];
     const int nseg = mlist[7];
     const int n_cut = mlist[4];  // this CTA's parts of cut sequences: mlist[5..6]; mlist[1 + i]: published by us
     bool waited_copies = false;
