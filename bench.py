@@ -55,6 +55,11 @@ WORKLOADS = {
     "qwen3_8b_layer_16seq_ctx1k-4k": (16, 32, 8, 128, 16, 8, (1024, 4096), "bf16", 1012),
 }
 DEFAULT_WORKLOAD = "qwen3_8b_layer_64seq_ctx1k-4k"
+# the multi-step loop of the engine (growth, trigger, asynchronous compression
+# of the triggered sequences while the others decode, table swap, release):
+# 512 sequences starting at contexts uniform in [1024, 4096], N_max = 128
+# blocks (2048 tokens, 2032 kept), K decode steps
+ENGINE_WORKLOAD = "qwen3_8b_layer_512seq_ctx1k-4k_engine"
 
 
 def _traffic():
@@ -503,15 +508,86 @@ def run_reference(args):
     return 0
 
 
+def run_engine(args, dist, rank, world, dev):
+    """The engine's multi-step loop on the high-concurrency workload: every
+    step appends and decodes the active sequences (one launch each), checks
+    the trigger, and starts the compression of the triggered ones on the side
+    stream; those sit out decode until it has completed (asynchronous mode).
+    value = decoded sequence-steps / time of K steps (plus the drain of the
+    compressions still in flight); step_hbm_gbs = the decode calls'
+    algorithmic bytes / that time."""
+    from compressed_paged_kv_zp_gb300 import zp_device_status
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    B, h_q, h_kv, d, b, N_max = 512, 32, 8, 128, 16, 128
+    g = torch.Generator().manual_seed(1003 + rank)
+    lens0 = torch.randint(1024, 4097, (B,), generator=g).numpy().astype(np.int32)
+    stride = 4096 // b + 2
+    n_total = int(np.maximum((lens0 + b - 1) // b + 1, N_max).sum()) + 64
+    loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=1, dtype=torch.bfloat16, window=b,
+                      async_compress=not args.sync_compress, device=dev)
+    loop.add_sequences(lens0)
+    gd = torch.Generator(device=dev).manual_seed(1004 + rank)
+    loop.K.copy_(torch.randn(loop.K.shape, generator=gd, device=dev))
+    loop.V.copy_(torch.randn(loop.V.shape, generator=gd, device=dev))
+    q = torch.randn((1, B, h_q, d), generator=gd, device=dev).to(torch.bfloat16)
+    kn = torch.randn((1, B, h_kv, d), generator=gd, device=dev).to(torch.bfloat16)
+    vn = torch.randn((1, B, h_kv, d), generator=gd, device=dev).to(torch.bfloat16)
+    for _ in range(args.warmup):
+        loop.step(q, kn, vn)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    _barrier(dist)
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    decoded, dbytes, comps0 = 0, 0, loop.compressions
+    start.record(stream)
+    for _ in range(args.steps):
+        act = loop.active.copy()
+        L = loop.lens[act].astype(np.int64) + 1  # after this step's token
+        decoded += int(act.sum())
+        dbytes += int((2 * L * h_kv * d * 2 + 2 * h_q * d * 2 + 8 * L * h_kv).sum())
+        loop.step(q, kn, vn)
+    loop.drain()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    _barrier(dist)
+    clk = clocks.stop()
+    code, _ = zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d in the timed region" % code)
+    ms = _max_over_ranks(dist, start.elapsed_time(stop), dev)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": decoded * world / (ms / 1e3), "unit": "seq-steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": ENGINE_WORKLOAD, "seqs": B, "heads": "32q/8kv", "head_dim": d, "block": b,
+                       "max_blocks_per_seq": N_max, "kept_tokens": (N_max - 1) * b, "window": b,
+                       "ctx": "start uniform 1024-4096", "compressions": loop.compressions - comps0,
+                       "launch": "engine loop (DecodeLoop, %s compression), direct calls"
+                                 % ("synchronous" if args.sync_compress else "asynchronous"),
+                       "l2": "inputs larger than L2"},
+            "roofline": None, "step_hbm_gbs": dbytes / (ms / 1e3) / 1e9, "decoded_seq_steps": decoded,
+            "clocks": clk}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zp", choices=["zp", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + [ENGINE_WORKLOAD])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sync-compress", action="store_true",
+                    help="engine workload: decode waits for each compression instead of letting the "
+                         "compressing sequences sit out")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "zp":
         args.warmup = 3
@@ -522,6 +598,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.workload == ENGINE_WORKLOAD:
+        return run_engine(args, dist, rank, world, dev)
     wl = Workload(args.workload, seed_offset=rank, dev=dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):

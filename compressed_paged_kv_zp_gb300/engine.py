@@ -25,6 +25,13 @@ from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layers,
                zp_decode_workspace_size, zp_paged_decode_attn)
 
 
+def upload(arr: np.ndarray, dev) -> torch.Tensor:
+    """Host array -> new device tensor without blocking the host: the values
+    are staged in pinned memory (torch's caching host allocator keeps that
+    block until the copy has completed) and copied on the current stream."""
+    return torch.from_numpy(np.ascontiguousarray(arr)).pin_memory().to(dev, non_blocking=True)
+
+
 class DecodeLoop:
     """Batch of sequences decoding over `layers` paged layers of one pool."""
 
@@ -47,7 +54,10 @@ class DecodeLoop:
         # global score cache F: paged like K (it moves with the kept tokens)
         self.F = torch.zeros(layers, n_total, b, h_kv, dtype=torch.float32, device=self.dev)
         self.pool = Pool(n_total)
-        self.side = torch.cuda.Stream(device=self.dev)
+        # compression stream at high priority: its CTAs are scheduled as soon
+        # as SMs free up between decode launches, so a compressing sequence
+        # sits out as few steps as possible
+        self.side = torch.cuda.Stream(device=self.dev, priority=-1)
         self.B = 0
         self.compressions = 0
         self.pending = []  # (event, seqs, plan) of compressions in flight
@@ -124,8 +134,8 @@ class DecodeLoop:
                 raise RuntimeError("a sequence outgrew table_stride blocks")
             self.table[need, self.lens[need] // self.b] = self.pool.alloc(len(need))
         self.lens[act] += 1
-        self.table_dev.copy_(torch.from_numpy(self.table), non_blocking=False)
-        step_lens = torch.from_numpy(np.where(act, self.lens, 0).astype(np.int32)).to(self.dev)
+        self.table_dev.copy_(torch.from_numpy(self.table).pin_memory(), non_blocking=True)
+        step_lens = upload(np.where(act, self.lens, 0).astype(np.int32), self.dev)
         main = torch.cuda.current_stream(self.dev)
         for l in range(self.layers):
             zp_append_kv(self.desc, k_new[l], v_new[l], self.K[l], self.V[l], self.table_dev, step_lens)
@@ -143,12 +153,12 @@ class DecodeLoop:
         sub_tables = np.ascontiguousarray(self.table[seqs])
         plan = self.pool.plan_compaction_batch(sub_tables, nb, self.N_max,
                                                max_blocks_seq=None if self.uniform else self.N_seq[seqs])
-        k_seq = None if self.uniform else torch.from_numpy((self.N_seq[seqs] - 1) * self.b).to(self.dev)
-        tables_dev = torch.from_numpy(sub_tables).to(self.dev)
-        lens_dev = torch.from_numpy(self.lens[seqs].astype(np.int32)).to(self.dev)
-        first_dev = torch.from_numpy(self.first[seqs].copy()).to(self.dev)
-        rows_dev = torch.from_numpy(seqs.astype(np.int32)).to(self.dev)
-        targets_dev = torch.from_numpy(np.ascontiguousarray(plan["targets"])).to(self.dev)
+        k_seq = None if self.uniform else upload((self.N_seq[seqs] - 1) * self.b, self.dev)
+        tables_dev = upload(sub_tables, self.dev)
+        lens_dev = upload(self.lens[seqs].astype(np.int32), self.dev)
+        first_dev = upload(self.first[seqs], self.dev)
+        rows_dev = upload(seqs.astype(np.int32), self.dev)
+        targets_dev = upload(plan["targets"], self.dev)
         ready = torch.cuda.Event()
         ready.record(main)
         with torch.cuda.stream(self.side):

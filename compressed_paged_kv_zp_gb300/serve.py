@@ -27,6 +27,7 @@ import torch
 
 from . import (cache_desc, score_params, zp_append_kv, zp_compress_layers, zp_compress_workspace_size,
                zp_decode_workspace_size, zp_paged_decode_attn)
+from .engine import upload
 from .sched import CONSTRAINED, HYBRID, Scheduler
 
 
@@ -58,7 +59,7 @@ class ServeLoop:
             dtype=torch.uint8, device=self.dev)
         self.gen = torch.Generator(device=self.dev)
         self.gen.manual_seed(seed)
-        self.side = torch.cuda.Stream(device=self.dev)
+        self.side = torch.cuda.Stream(device=self.dev, priority=-1)  # compression kernels first when SMs free up
         self.inflight = []  # (done event, ids)
         self.budget = {}
         self.out = None
@@ -84,7 +85,7 @@ class ServeLoop:
             p = np.arange(int(st["start"][i]), int(st["lens"][i]))
             pos.append(p)
             blk.append(st["tables"][i][p // b] * b + p % b)
-        phys = torch.from_numpy(np.concatenate(blk).astype(np.int64)).to(self.dev)
+        phys = upload(np.concatenate(blk).astype(np.int64), self.dev)
         n = int(phys.numel())
         if n:
             kf = self.K.view(self.layers, -1, self.h_kv, self.d)
@@ -95,9 +96,9 @@ class ServeLoop:
 
     def _decode(self, st):
         B = len(st["ids"])
-        table = torch.from_numpy(st["tables"]).to(self.dev)
-        lens = torch.from_numpy(st["lens"]).to(self.dev)
-        rows = torch.from_numpy(st["slots"]).to(self.dev)
+        table = upload(st["tables"], self.dev)
+        lens = upload(st["lens"], self.dev)
+        rows = upload(st["slots"], self.dev)
         q = self._randn(self.layers, B, self.h_q, self.d)
         kn = self._randn(self.layers, B, self.h_kv, self.d)
         vn = self._randn(self.layers, B, self.h_kv, self.d)
@@ -114,13 +115,13 @@ class ServeLoop:
         if not n:
             return
         dev = self.dev
-        tables = torch.from_numpy(comp["tables"]).to(dev)
-        lens = torch.from_numpy(comp["lens"]).to(dev)
-        first = torch.from_numpy(comp["first"].astype(np.uint8)).to(dev)
-        rows = torch.from_numpy(comp["slots"]).to(dev)
-        targets = torch.from_numpy(comp["targets"]).to(dev)
+        tables = upload(comp["tables"], dev)
+        lens = upload(comp["lens"], dev)
+        first = upload(comp["first"].astype(np.uint8), dev)
+        rows = upload(comp["slots"], dev)
+        targets = upload(comp["targets"], dev)
         uniform = bool((comp["k"] == (self.N_max - 1) * self.b).all())
-        k_seq = None if uniform else torch.from_numpy(comp["k"]).to(dev)
+        k_seq = None if uniform else upload(comp["k"], dev)
         k = (self.N_max - 1) * self.b
         main = torch.cuda.current_stream(dev)
         ready = torch.cuda.Event()
