@@ -264,7 +264,8 @@ class Workload:
         L = int(self.case.seq_lens[s])
         return self.pool.plan_compaction(self.case.block_table[s, :L // b].tolist(), N_max)
 
-    # ---- algorithmic bytes (per the roofline definition in the design doc)
+    # ---- algorithmic bytes: what the method must move per call (K, V, q, out,
+    # score rows), not the implementation's scratch
     def decode_bytes(self) -> int:
         es = 2 if self.dtype == "bf16" else 4
         tot = 0

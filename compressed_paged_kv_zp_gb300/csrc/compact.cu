@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kVThreads) compact_vec_kernel(const CompactArg
     uint4 *Vw = a.V + layer * a.layer_stride_vec;
     float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
     const int nt = (a.k + a.b - 1) / a.b;
-    // ---- round 1: length, keep positions, target blocks (independent loads)
+    // ---- first loads: length, keep positions, target blocks (independent)
     if (tid == 0) {
         int L = a.seq_lens[s];
         if (L > a.table_stride * a.b) L = a.table_stride * a.b;
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kVThreads) compact_vec_kernel(const CompactArg
         }
     }
     const int kk = min(a.k_seq ? min(a.k_seq[s], a.k) : a.k, L);
-    // ---- round 2: source blocks and F values of every rank
+    // ---- second loads: source blocks and F values of every rank
     for (int r = tid; r < kk; r += blockDim.x) {
         const int pos = pos_s[r];
         int blk = -1;

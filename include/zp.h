@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     ZP_OK = 0,
     ZP_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad flag */
-    ZP_ERR_SHAPE = 2,       /* head / block geometry this build does not support */
+    ZP_ERR_SHAPE = 2,       /* head / block geometry the library does not support */
     ZP_ERR_DTYPE = 3,       /* unknown element type */
     ZP_ERR_CAPACITY = 4,    /* workspace too small, pool exhausted, budget < window */
     ZP_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
