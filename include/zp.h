@@ -271,11 +271,19 @@ zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
  * in one launch of each of two kernels: the global score and redundancy per
  * (block, sequence, layer), then per (kv head, sequence, layer) one CTA that
  * finishes the scores, selects the keep set and moves the rows from shared
- * memory (while 8*Lmax + 12*k bytes fit in it); otherwise the three steps run
- * layer by layer.  The workspace (zp_compress_workspace_size) grows with
- * layer_count: the paper's layer stride is the number of layers per call.
- * k_seq (nullable, device int32 [n]): per-request budgets k_i <= k, as in
- * zp_select_topk. */
+ * memory (while 8*Lmax + 16*k bytes and the table row fit in it); otherwise
+ * the three steps run layer by layer.  The workspace
+ * (zp_compress_workspace_size) grows with layer_count: the paper's layer
+ * stride is the number of layers per call.  k_seq (nullable, device int32
+ * [n]): per-request budgets k_i <= k, as in zp_select_topk.
+ * Ordering: both kernels of the fused path are launched as programmatic
+ * dependents of the kernel before them on the stream.  They read the score
+ * rows (and everything the decode may write) only after waiting for that
+ * kernel's completion, so results are those of a plain stream-ordered call;
+ * when zp_paged_decode_attn immediately precedes on the same stream, the
+ * first kernel starts on the SMs the decode's finished CTAs leave and
+ * computes the key redundancy while the decode drains.  Anything recorded
+ * between the two calls (an event, a copy) only removes that overlap. */
 size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax, int32_t layer_count);
 zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
                              int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
