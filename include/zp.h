@@ -122,6 +122,9 @@ size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, int32_t table
  *
  * The workspace needs no clearing between calls.  After a call that left
  * ZP_ERR_TIMEOUT in the device status, clear it (zeros) before reusing it.
+ * The kernel allows programmatic dependent launch of the next kernel on the
+ * stream (zp_compress_layers uses it); kernels launched without that
+ * attribute still start after it has completed.
  * Limits: B <= 4096, h_kv in {2,4,8,16}, h_q/h_kv in {4,8}, d in {64,128},
  * b a power of two >= 16.  Errors: ZP_ERR_INVALID_ARG (NULL buffer, B < 0,
  * window outside [1, b] with score_accum set), ZP_ERR_SHAPE, ZP_ERR_DTYPE,
