@@ -25,8 +25,12 @@
  *
  * Parity status of each function (pins live in tests/test_oracle_pins.py):
  *   orc_decode_attention          pinned (SDPA library, L=1, q=0, permutation)
- *   orc_accumulate_window_score   pinned (equals orc_window_score)
- *   orc_window_score              pinned (row sums, w=1 == decode probabilities)
+ *   orc_accumulate_window_score   pinned (equals orc_window_score; closed form
+ *                                 and masked brute force fixing the order of
+ *                                 the two reductions)
+ *   orc_window_score              pinned (row sums, w=1 == decode probabilities,
+ *                                 a closed form where max-then-mean and
+ *                                 mean-then-max differ, masked brute force)
  *   orc_global_score              pinned (hand-worked example, alpha=0, first)
  *   orc_max_pool                  pinned (torch max_pool1d, kernel 1)
  *   orc_redundancy                pinned (closed forms for identical and

@@ -137,6 +137,133 @@ def test_window_score_masks_future_tokens(orc):
     np.testing.assert_allclose(S[0, L - 1], probs[0, :, L - 1].max() / w, rtol=1e-13)
 
 
+def _crossed_focus_case(L, b, d, x):
+    """One kv head (g = 2, w = 2) over orthonormal keys k_t = e_t, and window
+    queries that put logit x on one token and 0 on every other: head 0 looks at
+    token A from the first window row and at token B from the second, head 1
+    the other way round.  Returns (q_window [2][2][d], k_cache, table_row, A, B)."""
+    assert d >= L and L % b == 0
+    nb = L // b
+    K = np.zeros((nb, b, 1, d), dtype=np.float32)
+    for t in range(L):
+        K[t // b, t % b, 0, t] = 1.0
+    A, B = 3, 7
+    beta = x * math.sqrt(d)  # q . e_t / sqrt(d) = x
+    qw = np.zeros((2, 2, d), dtype=np.float32)
+    qw[0, 0, A] = qw[1, 1, A] = beta
+    qw[0, 1, B] = qw[1, 0, B] = beta
+    return qw, K, np.arange(nb, dtype=np.int32), A, B
+
+
+def test_window_score_order_closed_form(orc):
+    """App. C.2 takes the max over the query heads of a kv head first and the
+    mean over the window rows second.  With one-hot-like attention the softmax
+    is a closed form: n visible tokens, logit x on the focused one, 0 elsewhere
+    give p_focus = e^x/(e^x + n - 1) and p_other = 1/(e^x + n - 1).  Row 0 sees
+    n0 = L-1 tokens, row 1 sees n1 = L.  Max then mean gives, for A and B,
+    (pf(n0) + pf(n1))/2; mean then max would give max of (pf(n0)+po(n1))/2 and
+    (po(n0)+pf(n1))/2, which is smaller by a wide margin."""
+    L, b, d, x = 12, 4, 16, 2.0
+    qw, K, row, A, B = _crossed_focus_case(L, b, d, x)
+    x = float(np.float32(x * math.sqrt(d))) / math.sqrt(d)  # the logit the float query gives
+    pf = lambda n: math.exp(x) / (math.exp(x) + n - 1)
+    po = lambda n: 1.0 / (math.exp(x) + n - 1)
+    n0, n1 = L - 1, L
+    S = orc.window_score(qw, K, row, L, 2)
+    want_AB = (pf(n0) + pf(n1)) / 2
+    swapped_AB = max((pf(n0) + po(n1)) / 2, (po(n0) + pf(n1)) / 2)
+    assert want_AB - swapped_AB > 0.1
+    for t in range(L):
+        if t in (A, B):
+            want = want_AB
+        elif t == L - 1:  # seen by the second row only
+            want = po(n1) / 2
+        else:
+            want = (po(n0) + po(n1)) / 2
+        assert abs(S[0, t] - want) <= 1e-14, (t, S[0, t], want)
+
+
+def test_accumulated_score_order_closed_form(orc):
+    """The per-decode-step accumulation over the same two window queries (the
+    two steps ending at a full block) gives the same closed form."""
+    L, b, d, x = 12, 4, 16, 2.0
+    w = 2
+    qw, K, row, A, B = _crossed_focus_case(L, b, d, x)
+    x = float(np.float32(x * math.sqrt(d))) / math.sqrt(d)
+    pf = lambda n: math.exp(x) / (math.exp(x) + n - 1)
+    po = lambda n: 1.0 / (math.exp(x) + n - 1)
+    S = np.full((L // b, b, 1), 5.0)  # stale values must be overwritten
+    table = row[None, :]
+    for u in range(w):
+        lens = np.array([L - w + u + 1], dtype=np.int32)
+        _, probs = orc.decode_attention(qw[u:u + 1], K, K, table, lens, want_probs=True)
+        orc.accumulate_window_score(probs, table, lens, 1, b, w, S)
+    got = pipeline.gather_slots(S, row, L, b)[0]
+    assert abs(got[A] - (pf(L - 1) + pf(L)) / 2) <= 1e-14
+    assert abs(got[B] - (pf(L - 1) + pf(L)) / 2) <= 1e-14
+    assert abs(got[0] - (po(L - 1) + po(L)) / 2) <= 1e-14
+    assert abs(got[L - 1] - po(L) / 2) <= 1e-14
+
+
+def _window_score_bruteforce(qw, Kseq, w, L, g, group_first=True):
+    """Masked logits in torch fp64, softmax per row over t < L, then the two
+    reductions in the order asked for.  qw [w][h_q][d], Kseq [L][h_kv][d]."""
+    q = torch.from_numpy(qw).double()
+    k = Kseq.double()
+    h_q, d = q.shape[1], q.shape[2]
+    h_kv = h_q // g
+    kh = k.permute(1, 0, 2).repeat_interleave(g, dim=0)  # [h_q][L][d]
+    logits = torch.einsum("uhi,hti->uht", q, kh) / math.sqrt(d)  # [w][h_q][L]
+    pos = torch.arange(L)
+    for u in range(w):
+        logits[u, :, pos > L - w + u] = -math.inf
+    P = torch.softmax(logits, dim=-1).reshape(w, h_kv, g, L)
+    if group_first:
+        return P.amax(dim=2).mean(dim=0)  # [h_kv][L]
+    return P.mean(dim=0).amax(dim=1)
+
+
+@pytest.mark.parametrize("w,g", [(4, 4), (8, 2), (16, 4)])
+def test_window_score_matches_masked_bruteforce_and_not_swapped_order(orc, w, g):
+    """Brute force over the explicit masked logits (max over the group, then
+    mean over the window) equals the oracle, and the swapped order (mean, then
+    max) is far from it, so a swap in the oracle would fail here."""
+    h_kv, d, b = 2, 16, 16
+    h_q = h_kv * g
+    L = 3 * b + 5
+    c = _case(40 + w + g, 1, h_q, h_kv, d, b, lens=[L])
+    qw = (zp_inputs.normal((w, h_q, d), 50 + w) * 2.0).numpy()
+    S = orc.window_score(qw, _np(c.k_cache[0]), c.block_table[0].numpy(), L, w)
+    Kseq = zp_inputs.gather_tokens(c.k_cache[0], c.block_table[0], L, b)
+    ref = _window_score_bruteforce(qw, Kseq, w, L, g).numpy()
+    np.testing.assert_allclose(S, ref, rtol=1e-12, atol=1e-15)
+    swapped = _window_score_bruteforce(qw, Kseq, w, L, g, group_first=False).numpy()
+    assert np.abs(S - swapped).max() > 1e-6
+
+
+@pytest.mark.parametrize("w", [4, 8])
+def test_accumulated_score_matches_masked_bruteforce(orc, w):
+    """The decode-time accumulation over the w steps ending at a full block
+    against the same brute force."""
+    h_q, h_kv, d, b = 8, 2, 16, 8
+    g = h_q // h_kv
+    L = 4 * b
+    c = _case(60 + w, 1, h_q, h_kv, d, b, lens=[L])
+    qw = (zp_inputs.normal((w, h_q, d), 70 + w) * 2.0).numpy()
+    S = np.zeros((c.n_total, b, h_kv))
+    for u in range(w):
+        lens = np.array([L - w + u + 1], dtype=np.int32)
+        _, probs = orc.decode_attention(np.ascontiguousarray(qw[u:u + 1]), _np(c.k_cache[0]),
+                                        _np(c.v_cache[0]), c.block_table.numpy(), lens, want_probs=True)
+        orc.accumulate_window_score(probs, c.block_table.numpy(), lens, h_kv, b, w, S)
+    got = pipeline.gather_slots(S, c.block_table[0].numpy(), L, b)
+    Kseq = zp_inputs.gather_tokens(c.k_cache[0], c.block_table[0], L, b)
+    ref = _window_score_bruteforce(qw, Kseq, w, L, g).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-15)
+    swapped = _window_score_bruteforce(qw, Kseq, w, L, g, group_first=False).numpy()
+    assert np.abs(got - swapped).max() > 1e-6
+
+
 @pytest.mark.parametrize("w,b", [(4, 4), (2, 8), (8, 8), (3, 4)])
 def test_accumulated_score_equals_explicit_window(orc, w, b):
     """Per-step accumulation over the w decode steps that end at a full block
