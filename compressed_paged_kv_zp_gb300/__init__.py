@@ -28,7 +28,9 @@ STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTY
 # every symbol include/*.h declares
 EXPORTS = [
     "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
-    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc", "zp_append_kv", "zp_needs_compression",
+    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc",
+    "zp_debug_noalloc_preset_ctl", "zp_append_kv", "zp_needs_compression",
+    "zp_needs_compression_batch",
     "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
     "zp_compress_workspace_size", "zp_compress_layers",
@@ -100,8 +102,10 @@ def _load() -> ctypes.CDLL:
     lib.zp_decode_workspace_size.argtypes = [D, I32, I32]
     lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P, SZ, P]
     lib.zp_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P]
+    lib.zp_debug_noalloc_preset_ctl.argtypes = [I32, ctypes.c_uint64]
     lib.zp_append_kv.argtypes = [D, P, P, P, P, P, I32, P, I32, P]
     lib.zp_needs_compression.argtypes = [I32, I32, I32]
+    lib.zp_needs_compression_batch.argtypes = [P, P, I32, I32, I32, P, P, P]
     lib.zp_score_workspace_size.restype = SZ
     lib.zp_score_workspace_size.argtypes = [D, I32, I32]
     lib.zp_window_score_workspace_size.restype = SZ
@@ -220,6 +224,24 @@ def zp_append_kv(desc, k_new, v_new, k_cache, v_cache, block_table, seq_lens, st
 # ----------------------------------------------------------------------------- compression
 def zp_needs_compression(seq_len: int, block_size: int, max_blocks: int) -> bool:
     return bool(lib.zp_needs_compression(int(seq_len), int(block_size), int(max_blocks)))
+
+
+def zp_needs_compression_batch(seq_lens, block_size: int, max_blocks: int, active=None,
+                               max_blocks_seq=None):
+    """Indices (int64 numpy array, ascending) of the sequences whose trigger
+    holds; host numpy arrays in, no device work."""
+    import numpy as np
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    n = int(lens.shape[0])
+    act = None if active is None else np.ascontiguousarray(active, dtype=np.uint8)
+    per = None if max_blocks_seq is None else np.ascontiguousarray(max_blocks_seq, dtype=np.int32)
+    out = np.empty(max(n, 1), dtype=np.int32)
+    cnt = ctypes.c_int32(0)
+    _check(lib.zp_needs_compression_batch(lens.ctypes.data, None if act is None else act.ctypes.data, n,
+                                          int(block_size), int(max_blocks),
+                                          None if per is None else per.ctypes.data, out.ctypes.data,
+                                          ctypes.byref(cnt)))
+    return out[:cnt.value].astype(np.int64)
 
 
 def zp_score_workspace_size(desc: CacheDesc, n: int, Lmax: int) -> int:
@@ -421,7 +443,7 @@ class Pool:
 __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "ScoreRows", "score_params",
            "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn",
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
-           "zp_needs_compression", "zp_window_score_workspace_size", "zp_window_score",
+           "zp_needs_compression", "zp_needs_compression_batch", "zp_window_score_workspace_size", "zp_window_score",
            "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
            "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layers", "zp_plan_capacity", "zp_device_status", "Pool",
            "ZP_BF16", "ZP_F32"]

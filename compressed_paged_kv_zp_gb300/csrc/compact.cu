@@ -307,14 +307,9 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     dim3 grid(D->h_kv, n, layer_count);
     const int meta_smem = (int)compact_meta_smem(k, D->block_size);
     if (2 * row_vec <= kVThreads * kVPerThread && meta_smem <= 96 * 1024) {
-        static int configured[64] = {0};
-        const int dv = dev.device < 64 ? dev.device : 63;
-        if (meta_smem > 48 * 1024 && configured[dv] < meta_smem) {
-            cudaError_t e = cudaFuncSetAttribute(compact_vec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 meta_smem);
-            if (e != cudaSuccess) return cuda_fail(e, "compact: cudaFuncSetAttribute");
-            configured[dv] = meta_smem;
-        }
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(compact_vec_kernel), meta_smem,
+                                            "compact: shared-memory attribute");
+        if (rs != ZP_OK) return rs;
         compact_vec_kernel<<<grid, kVThreads, meta_smem, static_cast<cudaStream_t>(stream)>>>(a);
     } else {
         compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);

@@ -1706,11 +1706,9 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeArgs a, i
 template <typename T, int D, int G>
 zp_status launch_finish(const DecodeArgs &a, int grid, long long units_cap, cudaStream_t st) {
     const size_t smem = (size_t)grid * a.h_q * 8 + (size_t)grid * 4 + (size_t)a.h_q * 4;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(decode_merge_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "decode: merge attribute");
-    }
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(decode_merge_kernel<T, D>), smem,
+                                        "decode: merge shared-memory attribute");
+    if (rs != ZP_OK) return rs;
     decode_merge_kernel<T, D><<<grid, 256, smem, st>>>(a, grid);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: merge kernel launch");
@@ -1797,14 +1795,10 @@ zp_status make_plan(const zp_cache_desc *D, int B, int table_stride, const Devic
 template <int Dd, int G>
 zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cudaStream_t st,
                     const zp_cache_desc *D) {
-    static int configured_smem[64] = {0};
     auto kmain = decode_tc_kernel<Dd, G>;
-    const int dv = dev.device < 64 ? dev.device : 63;
-    if (configured_smem[dv] < p.smem) {
-        cudaError_t e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
-        if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
-        configured_smem[dv] = p.smem;
-    }
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kmain), (size_t)p.smem,
+                                        "decode: shared-memory attribute");
+    if (rs != ZP_OK) return rs;
     if ((reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) % 16)
         return fail(ZP_ERR_INVALID_ARG, "decode: caches must be 16-byte aligned");
     // cooperative: CTAs wait (bounded) for the merges of other CTAs
@@ -1818,14 +1812,10 @@ zp_status launch_tc(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, c
 
 template <typename T, int Dd, int G>
 zp_status launch_t(const DecodeArgs &a, const Plan &p, const DeviceInfo &dev, cudaStream_t st) {
-    static int configured_smem[64] = {0};
     auto kmain = decode_main_kernel<T, Dd, G>;
-    const int dv = dev.device < 64 ? dev.device : 63;
-    if (configured_smem[dv] < p.smem) {
-        cudaError_t e = cudaFuncSetAttribute(kmain, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
-        if (e != cudaSuccess) return cuda_fail(e, "decode: cudaFuncSetAttribute");
-        configured_smem[dv] = p.smem;
-    }
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kmain), (size_t)p.smem,
+                                        "decode: shared-memory attribute");
+    if (rs != ZP_OK) return rs;
     kmain<<<p.grid, p.threads, p.smem, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "decode: main kernel launch");
@@ -1988,9 +1978,27 @@ extern "C" zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const 
                     "decode_noalloc: this call needs %zu bytes of scratch; the built-in buffer holds "
                     "%zu (reduce B or table_stride, or use zp_paged_decode_attn with a workspace)",
                     need, kNoAllocScratchBytes);
-    // Nothing in the scratch needs to start at zero: every part that is
-    // read is written earlier in the same call.
+    // The per-sequence control words of the in-kernel merge (the first B
+    // 64-bit words) persist from call to call.  A call that gave up on a
+    // bounded wait (ZP_ERR_TIMEOUT) can leave a word counting arrivals that
+    // never completed; a caller with a workspace clears it, but this array is
+    // out of a caller's reach, so every call zeroes those words on its own
+    // stream first (a zero word reads as "no arrival yet").  Every other part
+    // of the scratch is written before it is read within the call.
+    e = cudaMemsetAsync(scratch, 0, (size_t)B * 8, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode_noalloc: clearing the control words");
     return zp_paged_decode_attn(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out,
                                 score_accum, score_rows, n_score_rows, window, scratch, kNoAllocScratchBytes,
                                 stream);
+}
+
+// Test hook: writes one control word of the built-in array of the current
+// device, as a call that timed out could have left it.  Allocates nothing.
+extern "C" zp_status zp_debug_noalloc_preset_ctl(int32_t seq, uint64_t word) {
+    if (seq < 0 || (size_t)(seq + 1) * 8 > kNoAllocScratchBytes)
+        return fail(ZP_ERR_INVALID_ARG, "noalloc_preset_ctl: sequence %d outside the array", seq);
+    const unsigned long long w = word;
+    cudaError_t e = cudaMemcpyToSymbol(g_decode_noalloc_scratch, &w, 8, (size_t)seq * 8, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "noalloc_preset_ctl: cudaMemcpyToSymbol");
+    return ok();
 }

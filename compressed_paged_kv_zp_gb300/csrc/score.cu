@@ -1049,7 +1049,9 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
         dim3 g2((Lmax + 15) / 16, n, layers);
         auto kern = a.d == 128 ? global_lightning_kernel<128> : global_lightning_kernel<64>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem,
+                                            "score: global/lightning shared-memory attribute");
+        if (rs != ZP_OK) return rs;
         // programmatic dependent launch: the CTAs may start on SMs that the
         // preceding kernel has left and fetch their keys while it drains
         cudaLaunchConfig_t cfg = {};
@@ -1078,13 +1080,12 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         if (e != cudaSuccess) return cuda_fail(e, "score: clearing rho");
         const size_t smem = (size_t)(kFrRows + 2 * kFrCols) * (a.d * 2 + 16) + (size_t)(kFrRows + 2 * kFrCols) * 4;
         dim3 gf((Lmax + kFrRows - 1) / kFrRows, a.h_kv, n);
-        if (a.d == 128) {
-            cudaFuncSetAttribute(flash_redundancy_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            flash_redundancy_kernel<128><<<gf, kFrThreads, smem, st>>>(a);
-        } else {
-            cudaFuncSetAttribute(flash_redundancy_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            flash_redundancy_kernel<64><<<gf, kFrThreads, smem, st>>>(a);
-        }
+        const void *fk = a.d == 128 ? reinterpret_cast<const void *>(flash_redundancy_kernel<128>)
+                                    : reinterpret_cast<const void *>(flash_redundancy_kernel<64>);
+        zp_status rs = set_max_dynamic_smem(fk, smem, "score: all-pairs shared-memory attribute");
+        if (rs != ZP_OK) return rs;
+        if (a.d == 128) flash_redundancy_kernel<128><<<gf, kFrThreads, smem, st>>>(a);
+        else flash_redundancy_kernel<64><<<gf, kFrThreads, smem, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "score: all-pairs redundancy launch");
     } else if (a.use_sim) {
@@ -1093,24 +1094,21 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
         if (smem > (size_t)dev.smem_optin) return fail(ZP_ERR_SHAPE, "score: block of keys too large");
         if (D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128)) {
             const size_t smem_tc = (size_t)a.h_kv * (a.d / 64) * 16 * 128;
-            if (a.d == 128) {
-                if (smem_tc > 48 * 1024)
-                    cudaFuncSetAttribute(lightning_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_tc);
-                lightning_tc_kernel<128><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
-            } else {
-                if (smem_tc > 48 * 1024)
-                    cudaFuncSetAttribute(lightning_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_tc);
-                lightning_tc_kernel<64><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
-            }
+            const void *lk = a.d == 128 ? reinterpret_cast<const void *>(lightning_tc_kernel<128>)
+                                        : reinterpret_cast<const void *>(lightning_tc_kernel<64>);
+            zp_status rs = set_max_dynamic_smem(lk, smem_tc, "score: lightning shared-memory attribute");
+            if (rs != ZP_OK) return rs;
+            if (a.d == 128) lightning_tc_kernel<128><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
+            else lightning_tc_kernel<64><<<g2, a.h_kv * 32, smem_tc, st>>>(a);
         } else if (D->dtype == ZP_BF16) {
-            cudaFuncSetAttribute(lightning_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(lightning_kernel<__nv_bfloat16>), smem,
+                                                "score: lightning shared-memory attribute");
+            if (rs != ZP_OK) return rs;
             lightning_kernel<__nv_bfloat16><<<g2, a.h_kv * 32, smem, st>>>(a);
         } else {
-            cudaFuncSetAttribute(lightning_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(lightning_kernel<float>), smem,
+                                                "score: lightning shared-memory attribute");
+            if (rs != ZP_OK) return rs;
             lightning_kernel<float><<<g2, a.h_kv * 32, smem, st>>>(a);
         }
         e = cudaGetLastError();
@@ -1208,11 +1206,9 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         m.F = global_F;
         m.kv_layer_vec = layer_stride * es / 16;
         m.F_layer = F_layer_stride;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(finalize_select_move_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return cuda_fail(e, "compress: cudaFuncSetAttribute");
-        }
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(finalize_select_move_kernel), smem,
+                                            "compress: shared-memory attribute");
+        if (rs != ZP_OK) return rs;
         // programmatic dependent launch: the finish grid may start while the
         // scores kernel drains; it reads that kernel's output only after
         // griddepcontrol.wait

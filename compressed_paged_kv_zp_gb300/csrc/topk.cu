@@ -71,11 +71,9 @@ extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t L
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (Lmax <= kSmemRow) {
         const size_t smem = (size_t)Lmax * 4;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return cuda_fail(e, "topk: cudaFuncSetAttribute");
-        }
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(topk_kernel<true>), smem,
+                                            "topk: shared-memory attribute");
+        if (rs != ZP_OK) return rs;
         topk_kernel<true><<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count,
                                                         dev.error_word);
     } else {

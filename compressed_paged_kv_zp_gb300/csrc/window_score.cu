@@ -354,14 +354,11 @@ template <int D, int MT, int G>
 zp_status launch_ws_tc(const WsArgs &a, cudaStream_t st, const DeviceInfo &dev, size_t smem) {
     auto k1 = ws_tc_kernel<D, MT, G, false>;
     auto k2 = ws_tc_kernel<D, MT, G, true>;
-    static int configured[64] = {0};
-    const int dv = dev.device < 64 ? dev.device : 63;
-    if (configured[dv] < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "window score: cudaFuncSetAttribute");
-        configured[dv] = (int)smem;
-    }
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k1), smem,
+                                        "window score: shared-memory attribute");
+    if (rs == ZP_OK)
+        rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k2), smem, "window score: shared-memory attribute");
+    if (rs != ZP_OK) return rs;
     const dim3 grid(a.chunks, a.n);
     const int threads = (a.h_kv + 1) * 32;
     k1<<<grid, threads, smem, st>>>(a);

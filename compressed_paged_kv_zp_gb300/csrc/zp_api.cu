@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <map>
 #include <mutex>
 #include <string>
 
@@ -64,6 +65,25 @@ zp_status device_info(DeviceInfo *out) {
     return ZP_OK;
 }
 
+namespace {
+std::mutex g_smem_mutex;
+std::map<std::pair<const void *, int>, size_t> g_smem_set;  // (kernel, device) -> bytes
+}  // namespace
+
+zp_status set_max_dynamic_smem(const void *func, size_t bytes, const char *what) {
+    if (bytes <= 48 * 1024) return ZP_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    std::lock_guard<std::mutex> lock(g_smem_mutex);
+    size_t &have = g_smem_set[std::make_pair(func, dev)];
+    if (have >= bytes) return ZP_OK;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    have = bytes;
+    return ZP_OK;
+}
+
 zp_status check_desc(const zp_cache_desc *D) {
     if (!D) return fail(ZP_ERR_INVALID_ARG, "NULL cache descriptor");
     if (D->dtype != ZP_BF16 && D->dtype != ZP_F32) return fail(ZP_ERR_DTYPE, "unknown dtype %d", D->dtype);
@@ -119,4 +139,20 @@ extern "C" int32_t zp_needs_compression(int32_t seq_len, int32_t block_size, int
     if (seq_len <= 0 || block_size <= 0) return 0;
     const int32_t n = (seq_len + block_size - 1) / block_size;
     return (n >= max_blocks && seq_len % block_size == 0) ? 1 : 0;
+}
+
+extern "C" zp_status zp_needs_compression_batch(const int32_t *seq_lens, const uint8_t *active, int32_t n,
+                                                int32_t block_size, int32_t max_blocks,
+                                                const int32_t *max_blocks_seq, int32_t *triggered,
+                                                int32_t *n_triggered) {
+    if (n < 0 || block_size <= 0 || !n_triggered || (n > 0 && (!seq_lens || !triggered)))
+        return fail(ZP_ERR_INVALID_ARG, "needs_compression_batch: bad argument");
+    int32_t m = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (active && !active[i]) continue;
+        const int32_t nb = max_blocks_seq ? max_blocks_seq[i] : max_blocks;
+        if (zp_needs_compression(seq_lens[i], block_size, nb)) triggered[m++] = i;
+    }
+    *n_triggered = m;
+    return ok();
 }

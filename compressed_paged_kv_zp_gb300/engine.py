@@ -22,6 +22,7 @@ import numpy as np
 import torch
 
 from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layers, zp_compress_workspace_size,
+               zp_needs_compression_batch,
                zp_decode_workspace_size, zp_paged_decode_attn)
 
 
@@ -141,10 +142,9 @@ class DecodeLoop:
             zp_append_kv(self.desc, k_new[l], v_new[l], self.K[l], self.V[l], self.table_dev, step_lens)
             zp_paged_decode_attn(self.desc, q[l], self.K[l], self.V[l], self.table_dev, step_lens, self.out[l],
                                  score_accum=self.S[l], window=self.window, workspace=self.ws)
-        L = self.lens
-        trig = np.nonzero(act & ((L + self.b - 1) // self.b >= self.N_seq) & (L % self.b == 0))[0]
+        trig = zp_needs_compression_batch(self.lens, self.b, self.N_max, active=act, max_blocks_seq=self.N_seq)
         if len(trig):
-            self._compress(trig.astype(np.int64), main)
+            self._compress(trig, main)
         return trig.tolist()
 
     def _compress(self, seqs, main):

@@ -149,15 +149,28 @@ zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void
  * and does nothing.  No device memory is allocated by this call.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.
- * All calls share the array and it keeps the previous call's contents (no
- * part of it needs to start at zero: each call writes what it reads), so
- * calls that may overlap on the GPU -- on different streams, or from
- * different threads -- race and must be ordered by the caller. */
+ * All calls share the array and it keeps the previous call's contents.  The
+ * per-sequence control words of the in-kernel merge (its first B 64-bit
+ * words) are read before the kernel writes them; a call that gave up on a
+ * bounded wait (ZP_ERR_TIMEOUT) can leave them counting arrivals that never
+ * completed.  Every call therefore zeroes those B words on `stream` before
+ * its kernel, so a call after a timeout starts clean and the caller has
+ * nothing to recover; every other part of the array is written before it is
+ * read within a call.  Calls that may overlap on the GPU -- on different
+ * streams, or from different threads -- race and must be ordered by the
+ * caller. */
 zp_status zp_paged_decode_attn_noalloc(const zp_cache_desc *D, const void *q, const void *k_cache,
                                        const void *v_cache, const int32_t *block_table,
                                        int32_t table_stride, const int32_t *seq_lens, int32_t B,
                                        void *out, float *score_accum, const int32_t *score_rows,
                                        int32_t n_score_rows, int32_t window, void *stream);
+
+/* Test hook of zp_paged_decode_attn_noalloc (no counterpart in the paper):
+ * writes control word `seq` of the current device's built-in array, as a
+ * call that timed out could have left it, so that a test can check that the
+ * next call clears it.  Blocking copy; allocates nothing.  ZP_ERR_INVALID_ARG
+ * when the word lies outside the array. */
+zp_status zp_debug_noalloc_preset_ctl(int32_t seq, uint64_t word);
 
 /* Writes the new token's key and value of each sequence into its slot
  * [Zipage §3: the cache of a block is written into the block's slots]:
@@ -173,6 +186,15 @@ zp_status zp_append_kv(const zp_cache_desc *D, const void *k_new, const void *v_
 
 /* Compression trigger [Zipage §4.1]: 1 iff ceil(L/b) >= max_blocks and L%b == 0. */
 int32_t zp_needs_compression(int32_t seq_len, int32_t block_size, int32_t max_blocks);
+
+/* zp_needs_compression over n sequences (host arrays, no device work):
+ * triggered[0..*n_triggered) receives, ascending, every i with active[i] != 0
+ * (active nullable: all) whose trigger holds at seq_lens[i] with the budget
+ * max_blocks_seq[i] (nullable: max_blocks for all; per-request budgets,
+ * Zipage Limitations).  triggered holds up to n entries. */
+zp_status zp_needs_compression_batch(const int32_t *seq_lens, const uint8_t *active, int32_t n,
+                                     int32_t block_size, int32_t max_blocks, const int32_t *max_blocks_seq,
+                                     int32_t *triggered, int32_t *n_triggered);
 
 /* Explicit observation-window score [Zipage App. C.2, Alg. 1] of n sequences
  * of one layer, for scoring without decode-time accumulation (a long prefill

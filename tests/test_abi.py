@@ -52,6 +52,24 @@ def test_trigger_matches_oracle(zp, orc):
                 assert zp.zp_needs_compression(L, b, N_max) == orc.needs_compression(L, b, N_max)
 
 
+def test_batched_trigger_matches_oracle(zp, orc):
+    """The batched trigger returns exactly the active sequences whose
+    per-sequence trigger holds in the oracle, with uniform and per-request
+    budgets."""
+    rng = np.random.default_rng(5)
+    for b in (4, 16):
+        lens = rng.integers(0, 40 * b, size=300).astype(np.int32)
+        lens[::7] = (lens[::7] // b) * b  # many block-aligned lengths
+        active = rng.random(300) < 0.8
+        per = rng.integers(2, 33, size=300).astype(np.int32)
+        for N_max, budgets in ((8, None), (32, per)):
+            got = zp.zp_needs_compression_batch(lens, b, N_max, active=active, max_blocks_seq=budgets)
+            want = [i for i in range(300) if active[i] and orc.needs_compression(
+                int(lens[i]), b, int(budgets[i]) if budgets is not None else N_max)]
+            assert got.tolist() == want
+    assert zp.zp_needs_compression_batch(np.zeros(0, np.int32), 16, 8).tolist() == []
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_planner_matches_oracle(zp, orc, seed):
     rng = np.random.default_rng(seed)

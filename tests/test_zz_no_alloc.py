@@ -52,6 +52,32 @@ def test_noalloc_decode_matches_workspace_decode_twice():
         torch.testing.assert_close(S, S_ref, **TOL_SCORE["bf16"])
 
 
+def test_noalloc_starts_clean_after_a_stale_control_word():
+    """A call that gave up on its bounded wait can leave a control word of the
+    built-in array counting arrivals that never completed, and a caller of this
+    entry point cannot reach the array to clear it.  The test writes such a word
+    (phase 0, 16384 arrivals) for a sequence cut across every CTA; the next call
+    must clear it itself: no ZP_ERR_TIMEOUT, the same result as the workspace
+    decode, and again on the call after."""
+    import compressed_paged_kv_zp_gb300 as zp
+    dev = torch.device("cuda")
+    c = zp_inputs.make_paged_case(14, 1, 32, 8, 128, 16, lens=[8190], dtype="bf16")
+    desc, q, K, V, table, lens = _args(zp, c, dev)
+    out_ref = torch.empty_like(q)
+    zp.zp_paged_decode_attn(desc, q, K, V, table, lens, out_ref)
+    torch.cuda.synchronize()
+    stale = (0xC0DE5EC7A11D << 16) | 0x4000
+    zp.zp_device_status(clear=True)
+    for call in range(2):
+        rc = zp.lib.zp_debug_noalloc_preset_ctl(0, stale)
+        assert rc == 0, zp.lib.zp_last_error().decode()
+        out = torch.full_like(q, float("nan"))
+        zp.zp_paged_decode_attn_noalloc(desc, q, K, V, table, lens, out)
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        torch.testing.assert_close(out.float(), out_ref.float(), **TOL_OUT["bf16"])
+
+
 def test_noalloc_rejects_a_call_larger_than_its_buffer():
     import compressed_paged_kv_zp_gb300 as zp
     desc = zp.cache_desc(32, 8, 128, 16, 1000, torch.bfloat16)
