@@ -67,12 +67,15 @@ def make_paged_case(seed: int, B: int, h_q: int, h_kv: int, d: int, b: int,
                     lens: Optional[Sequence[int]] = None, len_range=(1, 64),
                     dtype: str = "f32", spare_blocks: int = 0,
                     table_stride: Optional[int] = None, layers: int = 1,
-                    shared_prefix_blocks: int = 0) -> PagedCase:
+                    shared_prefix_blocks: int = 0, device=None) -> PagedCase:
     """Random paged cache with ``B`` sequences.
 
     ``shared_prefix_blocks`` > 0 makes every sequence start with the same
     physical blocks (a shared prompt prefix, reference count B); each sequence
     then needs at least that many full blocks of its own length.
+    ``device``: draw K, V and q there (a torch generator of that device seeded
+    from ``seed``) instead of on the host -- for caches of several GB; lengths,
+    tables and the free list are drawn on the host as always.
     """
     g = _gen(seed)
     if lens is None:
@@ -104,10 +107,21 @@ def make_paged_case(seed: int, B: int, h_q: int, h_kv: int, d: int, b: int,
         cursor += m
         ref[table[s, :nb].long()] += 1
     free = perm[cursor:].clone()
+    dt = DTYPES[dtype]
+    if device is not None:
+        gd = torch.Generator(device=device).manual_seed(seed + 0x5EED)
+        k = torch.empty(layers, n_total, b, h_kv, d, dtype=dt, device=device)
+        v = torch.empty(layers, n_total, b, h_kv, d, dtype=dt, device=device)
+        for arr in (k, v):  # layer by layer: no fp32 copy of the whole cache
+            for layer in range(layers):
+                arr[layer].copy_(torch.randn(n_total, b, h_kv, d, generator=gd, device=device))
+        q = torch.randn(B, h_q, d, generator=gd, device=device)
+        return PagedCase(h_q=h_q, h_kv=h_kv, d=d, b=b, dtype=dtype, n_total=n_total,
+                         seq_lens=seq_lens.to(torch.int32), block_table=table,
+                         k_cache=k, v_cache=v, q=q.to(dt), free_blocks=free, ref=ref, layers=layers)
     k = torch.randn(layers, n_total, b, h_kv, d, generator=g, dtype=torch.float32)
     v = torch.randn(layers, n_total, b, h_kv, d, generator=g, dtype=torch.float32)
     q = torch.randn(B, h_q, d, generator=g, dtype=torch.float32)
-    dt = DTYPES[dtype]
     return PagedCase(h_q=h_q, h_kv=h_kv, d=d, b=b, dtype=dtype, n_total=n_total,
                      seq_lens=seq_lens.to(torch.int32), block_table=table,
                      k_cache=k.to(dt), v_cache=v.to(dt), q=q.to(dt), free_blocks=free,
