@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libzp.so")
 
-SOURCES = ["zp_api.cu", "decode_attn.cu", "append_kv.cu", "window_score.cu", "score.cu", "topk.cu",
+SOURCES = ["zp_api.cu", "decode_attn.cu", "append_kv.cu", "window_score.cu", "score.cu", "redundancy.cu", "topk.cu",
            "compact.cu", "pool.cpp", "sched.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

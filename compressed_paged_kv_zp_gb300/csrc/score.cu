@@ -492,184 +492,6 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
 }
 
 
-// All-pairs ("flash") redundancy [App. C.5, Fig. 11, Alg. 3] for bf16 keys,
-// in O(L) memory.  The definition zeroes, in every column c of the cosine
-// matrix, the entry of the newest row r*(c) above p; the matrix is symmetric,
-// so r*(c) is also the largest index j != c with cos(k_c, k_j) > p -- a
-// quantity of row c.  So one pass over the Gram matrix by row tiles suffices:
-// a CTA owns 128 rows of one (sequence, kv head) and sweeps all column tiles
-// of 64 tokens (double-buffered cp.async copies into padded shared rows,
-// products on the tensor cores, mma.sync m16n8k16), keeping per row the sum of
-// its cosines and its last (largest-index) entry above p.  Then
-//     rho[r]       += sum_{c != r} cos(k_r, k_c)
-//     rho[r*(c)]   -= cos(k_c, k_{r*(c)})         for every c with an r*(c),
-// both as atomic additions into rho (zeroed before).  grid (ceil(Lmax/128),
-// h_kv, n), 8 warps of 16 rows.
-constexpr int kFrRows = 128, kFrCols = 64, kFrThreads = 256;
-
-template <int D>
-__device__ __forceinline__ void fr_load_rows(unsigned char *dst, int RSB, const ScoreArgs &a, int s, int kvh,
-                                             int t0, int nrows, int L) {
-    constexpr int CH = D / 8;  // 16-byte chunks per row piece
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.k);
-    for (int i = threadIdx.x; i < nrows * CH; i += blockDim.x) {
-        const int r = i / CH, c = i % CH;
-        const int t = t0 + r;
-        unsigned char *d = dst + r * RSB + c * 16;
-        int blk = -1;
-        if (t < L) blk = a.table[(size_t)s * a.table_stride + t / a.b];
-        if (blk >= 0 && blk < a.n_total) {
-            cp_async16_plain(d, K + (((size_t)blk * a.b + t % a.b) * a.h_kv + kvh) * D + c * 8);
-        } else {
-            if (t < L) record_error(a.err, ZP_ERR_DEVICE, 0x204);
-            *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
-        }
-    }
-}
-
-template <int D>
-__device__ __forceinline__ void fr_inv_norms(float *out, const unsigned char *rows, int RSB, int nrows) {
-    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
-        const __nv_bfloat162 *k = reinterpret_cast<const __nv_bfloat162 *>(rows + r * RSB);
-        float ss = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < D / 2; ++i) {
-            const float2 v = __bfloat1622float2(k[i]);
-            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, ss));
-        }
-        out[r] = ss > 0.f ? rsqrtf(ss) : 0.f;
-    }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kFrThreads) flash_redundancy_kernel(const ScoreArgs a) {
-    extern __shared__ __align__(128) unsigned char frs[];
-    constexpr int KS = D / 16;
-    constexpr int RSB = D * 2 + 16;  // padded row: the 8 rows of an ldmatrix on 8 bank groups
-    const int s = blockIdx.z, kvh = blockIdx.y, rt = blockIdx.x;
-    const int L = clamp_len(a, s);
-    const int r0 = rt * kFrRows;
-    if (r0 >= L) return;
-    unsigned char *rowsK = frs;
-    unsigned char *colK = rowsK + kFrRows * RSB;  // [2][kFrCols] rows
-    float *inv_r = reinterpret_cast<float *>(colK + 2 * kFrCols * RSB);
-    float *inv_c = inv_r + kFrRows;  // [2][kFrCols]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
-    const int lm = lane >> 3;
-    const int lrow = (lm & 1) * 8 + (lane & 7);
-    const int lchunk = lm >> 1;
-    const int ncol = (L + kFrCols - 1) / kFrCols;
-    fr_load_rows<D>(rowsK, RSB, a, s, kvh, r0, kFrRows, L);
-    fr_load_rows<D>(colK, RSB, a, s, kvh, 0, kFrCols, L);
-    cp_async_commit();
-    const int rA = r0 + warp * 16 + g, rB = rA + 8;
-    float sumA = 0.f, sumB = 0.f, valA = 0.f, valB = 0.f;
-    int maxA = -1, maxB = -1;
-    float irA = 0.f, irB = 0.f, pA = 0.f, pB = 0.f;
-    for (int cc = 0; cc < ncol; ++cc) {
-        const int buf = cc & 1;
-        if (cc + 1 < ncol)  // the other buffer was released by the barrier that ended step cc - 1
-            fr_load_rows<D>(colK + (buf ^ 1) * kFrCols * RSB, RSB, a, s, kvh, (cc + 1) * kFrCols, kFrCols, L);
-        cp_async_commit();
-        cp_async_wait<1>();  // everything but the prefetch just issued has landed
-        __syncthreads();
-        if (cc == 0) fr_inv_norms<D>(inv_r, rowsK, RSB, kFrRows);
-        fr_inv_norms<D>(inv_c + buf * kFrCols, colK + buf * kFrCols * RSB, RSB, kFrCols);
-        __syncthreads();
-        if (cc == 0) {
-            irA = inv_r[warp * 16 + g];
-            irB = inv_r[warp * 16 + g + 8];
-            pA = irA > 0.f ? a.p / irA : (a.p < 0.f ? -INFINITY : INFINITY);
-            pB = irB > 0.f ? a.p / irB : (a.p < 0.f ? -INFINITY : INFINITY);
-        }
-        float acc[kFrCols / 8][4];
-#pragma unroll
-        for (int j = 0; j < kFrCols / 8; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-        const uint32_t abase = smem_u32(rowsK) + (uint32_t)((warp * 16 + lrow) * RSB);
-        const uint32_t bbase = smem_u32(colK + buf * kFrCols * RSB) + (uint32_t)(lrow * RSB);
-#pragma unroll
-        for (int t = 0; t < KS; ++t) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(abase + (uint32_t)((2 * t + lchunk) * 16), a0, a1, a2, a3);
-#pragma unroll
-            for (int j2 = 0; j2 < kFrCols / 16; ++j2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(bbase + (uint32_t)(j2 * 16 * RSB + (2 * t + lchunk) * 16), b0, b1, b2, b3);
-                mma_16816(acc[2 * j2], a0, a1, a2, a3, b0, b2);
-                mma_16816(acc[2 * j2 + 1], a0, a1, a2, a3, b1, b3);
-            }
-        }
-        // lane holds rows rA (acc[j][0..1]) and rB (acc[j][2..3]), columns j*8 + 2tig + {0,1}.
-        // x = acc * inv_norm(col) is the cosine divided by inv_norm(row): the row
-        // factor is applied once to the sum, and the threshold p to x compares as
-        // p / inv_norm(row) (a zero-norm row has cosine 0 with everything).
-        const float *ic = inv_c + buf * kFrCols;
-        const int c0 = cc * kFrCols;
-        const bool interior = c0 + kFrCols <= L && (c0 >= r0 + kFrRows || c0 + kFrCols <= r0);
-        if (interior) {
-            float2 sA2 = make_float2(0.f, 0.f), sB2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < kFrCols / 8; ++j) {
-                const float2 icv = *reinterpret_cast<const float2 *>(ic + j * 8 + 2 * tig);
-                const float2 xa = fmul2(make_float2(acc[j][0], acc[j][1]), icv);
-                const float2 xb = fmul2(make_float2(acc[j][2], acc[j][3]), icv);
-                sA2 = ffma2(make_float2(1.f, 1.f), xa, sA2);
-                sB2 = ffma2(make_float2(1.f, 1.f), xb, sB2);
-                const int col = c0 + j * 8 + 2 * tig;
-                if (xa.x > pA) maxA = col, valA = xa.x;
-                if (xa.y > pA) maxA = col + 1, valA = xa.y;
-                if (xb.x > pB) maxB = col, valB = xb.x;
-                if (xb.y > pB) maxB = col + 1, valB = xb.y;
-            }
-            sumA += sA2.x + sA2.y;
-            sumB += sB2.x + sB2.y;
-        } else {
-#pragma unroll
-            for (int j = 0; j < kFrCols / 8; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = c0 + j * 8 + 2 * tig + e;
-                    const float icv = ic[j * 8 + 2 * tig + e];
-                    const bool cv = col < L;
-                    const float xa = acc[j][e] * icv, xb = acc[j][2 + e] * icv;
-                    if (cv && col != rA) {
-                        sumA += xa;
-                        if (xa > pA) maxA = col, valA = xa;
-                    }
-                    if (cv && col != rB) {
-                        sumB += xb;
-                        if (xb > pB) maxB = col, valB = xb;
-                    }
-                }
-        }
-        __syncthreads();  // buffer `buf` is refilled by the next step's prefetch
-    }
-    // the four lanes of a row: sums add, the largest index above p wins
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        sumA += __shfl_xor_sync(0xFFFFFFFFu, sumA, o);
-        sumB += __shfl_xor_sync(0xFFFFFFFFu, sumB, o);
-        const int mA = __shfl_xor_sync(0xFFFFFFFFu, maxA, o), mB = __shfl_xor_sync(0xFFFFFFFFu, maxB, o);
-        const float vA = __shfl_xor_sync(0xFFFFFFFFu, valA, o), vB = __shfl_xor_sync(0xFFFFFFFFu, valB, o);
-        if (mA > maxA) maxA = mA, valA = vA;
-        if (mB > maxB) maxB = mB, valB = vB;
-    }
-    if (tig == 0) {  // back to cosines: times inv_norm(row)
-        float *rho = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax;
-        if (rA < L) {
-            atomicAdd(rho + rA, sumA * irA);
-            if (maxA >= 0) atomicAdd(rho + maxA, -valA * irA);
-        }
-        if (rB < L) {
-            atomicAdd(rho + rB, sumB * irB);
-            if (maxB >= 0) atomicAdd(rho + maxB, -valB * irB);
-        }
-    }
-}
-
 // grid (h_kv, n), 1024 threads
 __global__ void finalize_kernel(const ScoreArgs a) {
     __shared__ float red[32];
@@ -970,7 +792,8 @@ using namespace zp;
 
 extern "C" size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax) {
     if (!D || n < 0 || Lmax < 0) return 0;
-    return 2 * align_up((size_t)n * D->h_kv * Lmax * 4, 256);
+    // X and rho, then the all-pairs redundancy's scratch
+    return 2 * align_up((size_t)n * D->h_kv * Lmax * 4, 256) + all_pairs_workspace_size(n, D->h_kv, D->head_dim, Lmax);
 }
 
 // Validates the scoring arguments, fills `a` and launches the global-score and
@@ -1002,8 +825,10 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     if (P->use_similarity && !(P->tau > 0.f)) return fail(ZP_ERR_INVALID_ARG, "score: tau must be > 0");
     if (D->h_kv > 16) return fail(ZP_ERR_SHAPE, "score: h_kv %d > 16", D->h_kv);
     const bool all_pairs = P->use_similarity && !P->lightning;
-    if (all_pairs && !(D->dtype == ZP_BF16 && (D->head_dim == 64 || D->head_dim == 128)))
-        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy needs bf16 keys and head_dim 64 or 128");
+    if (all_pairs && !(D->head_dim == 64 || D->head_dim == 128))
+        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy needs head_dim 64 or 128");
+    if (all_pairs && D->dtype == ZP_BF16 && D->block_size % 16)
+        return fail(ZP_ERR_SHAPE, "score: the all-pairs redundancy of bf16 keys needs b a multiple of 16");
     if (P->use_similarity && P->lightning && D->block_size > 16)
         return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
     const size_t need = (size_t)layers * zp_score_workspace_size(D, n, Lmax);
@@ -1075,19 +900,27 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "score: gather launch");
     if (all_pairs) {
-        // rho accumulates atomically: start from zero
-        e = cudaMemsetAsync(a.rho, 0, (size_t)n * a.h_kv * Lmax * 4, st);
-        if (e != cudaSuccess) return cuda_fail(e, "score: clearing rho");
-        const size_t smem = (size_t)(kFrRows + 2 * kFrCols) * (a.d * 2 + 16) + (size_t)(kFrRows + 2 * kFrCols) * 4;
-        dim3 gf((Lmax + kFrRows - 1) / kFrRows, a.h_kv, n);
-        const void *fk = a.d == 128 ? reinterpret_cast<const void *>(flash_redundancy_kernel<128>)
-                                    : reinterpret_cast<const void *>(flash_redundancy_kernel<64>);
-        zp_status rs = set_max_dynamic_smem(fk, smem, "score: all-pairs shared-memory attribute");
+        AllPairsArgs ap;
+        ap.k = k_cache;
+        ap.dtype = D->dtype;
+        ap.table = block_table;
+        ap.table_stride = table_stride;
+        ap.seq_lens = seq_lens;
+        ap.n = n;
+        ap.h_kv = a.h_kv;
+        ap.d = a.d;
+        ap.b = a.b;
+        ap.n_total = a.n_total;
+        ap.Lmax = Lmax;
+        long long cap = Lmax;
+        if ((long long)table_stride * a.b < cap) cap = (long long)table_stride * a.b;
+        if (a.S_stride < cap) cap = a.S_stride;
+        ap.Lcap = (int)cap;
+        ap.p = a.p;
+        ap.rho = a.rho;
+        ap.workspace = reinterpret_cast<unsigned char *>(a.rho) + align_up((size_t)a.X_layer * 4, 256);
+        zp_status rs = launch_all_pairs(ap, st);
         if (rs != ZP_OK) return rs;
-        if (a.d == 128) flash_redundancy_kernel<128><<<gf, kFrThreads, smem, st>>>(a);
-        else flash_redundancy_kernel<64><<<gf, kFrThreads, smem, st>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "score: all-pairs redundancy launch");
     } else if (a.use_sim) {
         dim3 g2((Lmax + a.b - 1) / a.b, n);
         const size_t smem = (size_t)a.h_kv * a.b * (a.d + 1) * 4;

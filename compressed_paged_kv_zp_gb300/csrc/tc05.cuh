@@ -1,0 +1,117 @@
+// tc05.cuh -- inline PTX for the fifth-generation tensor cores of sm_100-family
+// GPUs (tcgen05: MMA from shared-memory descriptors into tensor memory),
+// tensor memory (TMEM) allocation and loads, and tiled TMA loads through a
+// tensor map.  Used by the kernels whose inner product is a dense contraction.
+//
+// Operand layout used throughout: K-major tiles with the 128-byte swizzle.  A
+// tile of R rows and 64 bf16 columns (128 bytes per row) sits at a 1024-byte
+// aligned address; 8-row groups are 1024 bytes apart, and inside a group the
+// 16-byte chunk c of row r is stored at chunk position c ^ (r % 8) -- exactly
+// what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes.  A head dimension of
+// 128 is two such tiles (the two 64-column halves) one after the other.
+#pragma once
+
+#include <cuda.h>
+
+#include "zp_common.cuh"
+
+namespace zp {
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor (64 bits): start address >> 4 in bits
+// [0,14), leading-dimension byte offset >> 4 in [16,30) (not used by swizzled
+// K-major layouts; 1 by convention), stride-dimension byte offset >> 4 in
+// [32,46) (1024 bytes between 8-row groups), descriptor version 1 in [46,48),
+// base offset 0 in [49,52) (1024-byte aligned atoms), layout type in [61,64)
+// (2 = 128-byte swizzle).  A K step of 16 bf16 elements inside the 128-byte
+// row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma .kind::f16: D fp32 (bits [4,6) = 1),
+// A and B bf16 (bits [7,10) and [10,13) = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits [17,23), M >> 4 in bits [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- tensor memory
+// Allocation and release are executed by one whole warp; the allocated base
+// address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Ordering of tcgen05 operations around thread synchronisation (mbarrier
+// waits, __syncthreads).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] = A * B^T (+ D when accumulate != 0): one thread issues it.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier receives one arrival once every tcgen05 operation issued so far
+// by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of the warp's 32 TMEM lanes (thread i: lane
+// base + i), waited for in the same statement so that no use of the registers
+// can be scheduled before the data is there.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+// 3-D tiled load through a tensor map (a __grid_constant__ kernel parameter)
+// completing on `bar`.  c0 is the innermost coordinate; it must be a multiple
+// of 16 bytes' worth of elements.  Coordinates outside the tensor read zeros.
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *tmap, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+}  // namespace zp

@@ -35,4 +35,21 @@ inline int elem_bytes(int dtype) { return dtype == ZP_BF16 ? 2 : (dtype == ZP_F3
 
 zp_status check_desc(const zp_cache_desc *D);
 
+// All-pairs key redundancy of one layer (redundancy.cu): rho [n][h_kv][Lmax]
+// receives the row sums of the thresholded cosine matrix of every sequence and
+// kv head (overwritten).  Lengths are clamped to Lcap.
+struct AllPairsArgs {
+    const void *k;  // paged keys of the layer
+    int dtype;      // ZP_BF16 or ZP_F32
+    const int32_t *table;
+    int table_stride;
+    const int32_t *seq_lens;
+    int n, h_kv, d, b, n_total, Lmax, Lcap;
+    float p;
+    float *rho;
+    void *workspace;  // all_pairs_workspace_size bytes
+};
+size_t all_pairs_workspace_size(int n, int h_kv, int d, int Lmax);
+zp_status launch_all_pairs(const AllPairsArgs &a, cudaStream_t st);
+
 }  // namespace zp

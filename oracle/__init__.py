@@ -56,6 +56,8 @@ def _load():
             lib.orc_global_score.argtypes = [_int, _int, _int, _int, _dbl, _i32p, _f64p, _f64p]
             lib.orc_max_pool.argtypes = [_int, _int, _f64p, _f64p]
             lib.orc_redundancy.argtypes = [_int, _int, _int, _f32p, _dbl, _dbl, _int, _f64p]
+            lib.orc_redundancy_rho.argtypes = [_int, _int, _int, _f32p, _dbl, _int, _f64p]
+            lib.orc_redundancy_rho_rows.argtypes = [_int, _int, _f32p, _dbl, _i32p, _int, _f64p]
             lib.orc_combine_and_window.argtypes = [_int, _int, _dbl, _f64p, _f64p]
             lib.orc_topk_keep.argtypes = [_int, _int, _f64p, _i32p, _u8p]
             lib.orc_compact_alg4.argtypes = [_u8p, ctypes.c_size_t, _int, _int, _int, _i32p, _int,
@@ -167,6 +169,30 @@ def redundancy(keys, b, p, tau, lightning):
     if rc:
         raise OracleError("orc_redundancy: %d" % rc)
     return R
+
+
+def redundancy_rho(keys, b, p, lightning):
+    """rho[L] (the row sums before normalisation) for one (sequence, KV head)."""
+    keys = _f32(keys)
+    L, d = keys.shape
+    rho = np.empty(L, dtype=np.float64)
+    rc = _load().orc_redundancy_rho(L, d, b, _p(keys, _f32p), float(p), int(bool(lightning)), _p(rho, _f64p))
+    if rc:
+        raise OracleError("orc_redundancy_rho: %d" % rc)
+    return rho
+
+
+def redundancy_rho_rows(keys, p, rows):
+    """All-pairs rho at the given rows only (O(L) memory)."""
+    keys = _f32(keys)
+    L, d = keys.shape
+    rows = _i32(rows)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    rc = _load().orc_redundancy_rho_rows(L, d, _p(keys, _f32p), float(p), _p(rows, _i32p), rows.shape[0],
+                                         _p(out, _f64p))
+    if rc:
+        raise OracleError("orc_redundancy_rho_rows: %d" % rc)
+    return out
 
 
 def combine_and_window(S, w, lam, R=None):

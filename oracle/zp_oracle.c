@@ -35,6 +35,11 @@
  *   orc_max_pool                  pinned (torch max_pool1d, kernel 1)
  *   orc_redundancy                pinned (closed forms for identical and
  *                                 orthogonal keys, lightning == full for L<=b)
+ *   orc_redundancy_rho            pinned (closed forms for identical and
+ *                                 orthogonal keys, pure-Python brute force,
+ *                                 softmax of it == orc_redundancy)
+ *   orc_redundancy_rho_rows       pinned (equals orc_redundancy_rho row by
+ *                                 row with planted near-duplicates; closed form)
  *   orc_combine_and_window        pinned (lambda=0, window = +inf)
  *   orc_topk_keep                 pinned (exhaustive subsets, Fig. 1 example)
  *   orc_compact_alg4              pinned (Fig. 1 layout, bitwise moves)
@@ -298,14 +303,14 @@ int orc_max_pool(int L, int kernel, const double *x, double *y) {
 /* lightning score; C.7 changes only the pair domain, so the same length     */
 /* normalisation is used for both.  Memory is O(m^2) for the largest group.  */
 /* ------------------------------------------------------------------------- */
-int orc_redundancy(int L, int d, int b, const float *keys, double p, double tau,
-                   int lightning, double *R) {
-    if (L <= 0 || d <= 0 || b <= 0 || !(tau > 0.0)) return ORC_BAD_ARG;
+/* The row sums rho[t] (before the normalisation and the softmax) of the     */
+/* groups above, for every position.                                        */
+int orc_redundancy_rho(int L, int d, int b, const float *keys, double p, int lightning, double *rho) {
+    if (L <= 0 || d <= 0 || b <= 0) return ORC_BAD_ARG;
     const int group = lightning ? (b < L ? b : L) : L;
     double *norm = (double *)malloc(sizeof(double) * (size_t)L);
     double *C = (double *)malloc(sizeof(double) * (size_t)group * (size_t)group);
-    double *rho = (double *)malloc(sizeof(double) * (size_t)L);
-    if (!norm || !C || !rho) { free(norm); free(C); free(rho); return ORC_NO_MEMORY; }
+    if (!norm || !C) { free(norm); free(C); return ORC_NO_MEMORY; }
     for (int t = 0; t < L; ++t) {
         double ss = 0.0;
         for (int i = 0; i < d; ++i) ss += (double)keys[(size_t)t * d + i] * (double)keys[(size_t)t * d + i];
@@ -335,16 +340,73 @@ int orc_redundancy(int L, int d, int b, const float *keys, double p, double tau,
         for (int r = 0; r < m; ++r) {
             double acc = 0.0;
             for (int c = 0; c < m; ++c) acc += C[(size_t)r * m + c];
-            rho[g0 + r] = acc / ((double)L * tau);
+            rho[g0 + r] = acc;
         }
     }
+    free(norm); free(C);
+    return ORC_OK;
+}
+
+int orc_redundancy(int L, int d, int b, const float *keys, double p, double tau,
+                   int lightning, double *R) {
+    if (L <= 0 || d <= 0 || b <= 0 || !(tau > 0.0)) return ORC_BAD_ARG;
+    double *rho = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!rho) return ORC_NO_MEMORY;
+    const int rc = orc_redundancy_rho(L, d, b, keys, p, lightning, rho);
+    if (rc != ORC_OK) { free(rho); return rc; }
+    for (int r = 0; r < L; ++r) rho[r] = rho[r] / ((double)L * tau);
     double rmax = -INFINITY;
     for (int r = 0; r < L; ++r)
         if (rho[r] > rmax) rmax = rho[r];
     double denom = 0.0;
     for (int r = 0; r < L; ++r) denom += exp(rho[r] - rmax);
     for (int r = 0; r < L; ++r) R[r] = exp(rho[r] - rmax) / denom;
-    free(norm); free(C); free(rho);
+    free(rho);
+    return ORC_OK;
+}
+
+/* The all-pairs row sums rho[r] of the definition above for the selected   */
+/* rows only, without the L x L matrix (O(L) memory): with C the cosine     */
+/* matrix (zero diagonal),                                                  */
+/*   rho[r] = sum_c C[r][c] - sum { C[r][c] : r is the largest j with        */
+/*                                  C[j][c] > p }                            */
+/* and only a column c with C[r][c] > p can have r as that largest index,    */
+/* so column c is scanned (newest row first) only for those.  Each cosine is */
+/* computed exactly as in orc_redundancy_rho.                               */
+static double cosine_at(const float *keys, const double *norm, int d, int tr, int tc) {
+    if (tr == tc || !(norm[tr] > 0.0 && norm[tc] > 0.0)) return 0.0;
+    double dot = 0.0;
+    for (int i = 0; i < d; ++i) dot += (double)keys[(size_t)tr * d + i] * (double)keys[(size_t)tc * d + i];
+    return dot / (norm[tr] * norm[tc]);
+}
+
+int orc_redundancy_rho_rows(int L, int d, const float *keys, double p, const int32_t *rows, int nrows,
+                            double *out) {
+    if (L <= 0 || d <= 0 || nrows < 0) return ORC_BAD_ARG;
+    double *norm = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!norm) return ORC_NO_MEMORY;
+    for (int t = 0; t < L; ++t) {
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += (double)keys[(size_t)t * d + i] * (double)keys[(size_t)t * d + i];
+        norm[t] = sqrt(ss);
+    }
+    for (int k = 0; k < nrows; ++k) {
+        const int r = rows[k];
+        if (r < 0 || r >= L) { free(norm); return ORC_BAD_ARG; }
+        double sum = 0.0;
+        for (int c = 0; c < L; ++c) sum += cosine_at(keys, norm, d, r, c);
+        for (int c = 0; c < L; ++c) {
+            if (c == r) continue;  /* zeroing the diagonal changes nothing */
+            const double v = cosine_at(keys, norm, d, r, c);
+            if (!(v > p)) continue;
+            int newest = r;
+            for (int j = L - 1; j > r; --j)
+                if (cosine_at(keys, norm, d, j, c) > p) { newest = j; break; }
+            if (newest == r) sum -= v;
+        }
+        out[k] = sum;
+    }
+    free(norm);
     return ORC_OK;
 }
 

@@ -439,6 +439,55 @@ def test_redundancy_brute_force_with_duplicates(orc, lightning):
     assert fired >= 6
 
 
+@pytest.mark.parametrize("m", [2, 5, 9])
+def test_redundancy_rho_identical_keys_closed_form(orc, m):
+    """All-pairs row sums of m identical keys: rho[m-1] = 0, rho[m-2] = m-2,
+    others m-1, from the full function and row by row."""
+    keys = np.tile(np.array([2, -1, 0.5, 3], dtype=np.float32), (m, 1))
+    want = np.full(m, m - 1.0)
+    want[m - 1] = 0.0
+    want[m - 2] = m - 2.0
+    np.testing.assert_allclose(orc.redundancy_rho(keys, m, 0.9, 0), want, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(orc.redundancy_rho_rows(keys, 0.9, np.arange(m)), want, rtol=1e-13, atol=1e-13)
+
+
+def test_redundancy_rho_orthogonal_keys_zero(orc):
+    keys = np.eye(10, dtype=np.float32)[:7] * 2.5
+    np.testing.assert_array_equal(orc.redundancy_rho(keys, 4, 0.9, 0), np.zeros(7))
+    np.testing.assert_array_equal(orc.redundancy_rho_rows(keys, 0.9, [0, 3, 6]), np.zeros(3))
+
+
+@pytest.mark.parametrize("p", [0.5, -0.3])
+def test_redundancy_rho_brute_force(orc, p):
+    """Pure-Python brute force of the all-pairs row sums (zero diagonal, the
+    newest row above p zeroed in every column, zero-norm key included), for the
+    full function and the selected-rows function; with p < 0 the zeroed
+    diagonal itself can be a column's newest entry above p."""
+    rng = np.random.default_rng(31)
+    L, d = 29, 5
+    keys = rng.standard_normal((L, d)).astype(np.float32)
+    for t in (4, 7, 11, 15, 16, 22, 27, 28):
+        keys[t] = keys[t - 3 - (t % 4)] + 0.05 * rng.standard_normal(d).astype(np.float32)
+    keys[9] = 0.0
+    k = keys.astype(np.float64)
+    nrm = [np.sqrt(sum(x * x for x in k[r])) for r in range(L)]
+    C = [[0.0] * L for _ in range(L)]
+    for r in range(L):
+        for c in range(L):
+            if r != c and nrm[r] > 0 and nrm[c] > 0:
+                C[r][c] = sum(k[r, i] * k[c, i] for i in range(d)) / (nrm[r] * nrm[c])
+    for c in range(L):
+        above = [r for r in range(L) if C[r][c] > p]
+        if above:
+            C[max(above)][c] = 0.0
+    want = np.array([sum(C[r]) for r in range(L)])
+    np.testing.assert_allclose(orc.redundancy_rho(keys, 4, p, 0), want, rtol=1e-12, atol=1e-12)
+    rows = np.array([0, 3, 9, 11, 16, 27, 28], dtype=np.int32)
+    np.testing.assert_allclose(orc.redundancy_rho_rows(keys, p, rows), want[rows], rtol=1e-12, atol=1e-12)
+    tau = 0.3
+    np.testing.assert_allclose(orc.redundancy(keys, 4, p, tau, 0), _softmax(want / (L * tau)), rtol=1e-12)
+
+
 def test_redundancy_zero_norm_key_has_no_similarity(orc):
     keys = np.array([[0, 0], [1, 0], [0, 1]], dtype=np.float32)
     R = orc.redundancy(keys, 4, 0.5, 1.0, 0)
