@@ -42,9 +42,11 @@ struct ApArgs {
     int Lpad;   // row stride of inv and cand (a multiple of 128, >= Lmax)
     float p;
     float *inv;   // [n][h_kv][Lpad]
+    float *cmax;  // [n][h_kv][Lpad / 32]: the largest 1/|k| of each 32-token chunk
     int *cand;    // [n][h_kv][Lpad]
     float *shat;  // [n][h_kv][d]
     float *rho;   // [n][h_kv][Lmax], zero on entry to the finish
+    int *counter; // work-item counter of the tensor-core kernel, zero on entry
     unsigned *err;
 };
 
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(128) ap_prep_kernel(const ApArgs a) {
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float chunk_max = 0.f;  // the warp's 32 tokens are one chunk
     for (int r = 0; r < 32; ++r) {
         const int t = t0 + warp * 32 + r;
         if (t >= a.Lpad) break;
@@ -139,7 +142,9 @@ __global__ void __launch_bounds__(128) ap_prep_kernel(const ApArgs a) {
             for (int e = 0; e < E; ++e) acc[e] = fmaf(x[e], inv, acc[e]);
         }
         if (lane == 0) a.inv[base + t] = inv;
+        chunk_max = fmaxf(chunk_max, inv);
     }
+    if (lane == 0) a.cmax[base / 32 + (t0 >> 5) + warp] = chunk_max;
 #pragma unroll
     for (int e = 0; e < E; ++e) part[warp][lane * E + e] = acc[e];
     __syncthreads();
@@ -260,21 +265,27 @@ __global__ void __launch_bounds__(128) ap_gram_f32_kernel(const ApArgs a) {
 // Persistent kernel, one CTA per SM (all 512 TMEM columns, ~193 KB of shared
 // memory).  A work item is (sequence, kv head, row super-tile of ROWS = RT*128
 // tokens, up to kItemCols columns starting at or after the super-tile's first
-// row): the rows' keys stay in shared memory (A) while the columns' keys
-// stream through a ring of kStages tiles of N = 256/RT keys (B).  For each
-// column tile one thread issues RT x (D/16) MMAs of M = 128, N, K = 16 into
-// one of two accumulator buffers (RT*N = 256 TMEM columns each); eight
-// epilogue warps read the other buffer, form y = acc * (1/|k_j|) - p*|k_i|
-// (the cosine test scaled by |k_i| > 0) two elements per packed FMA, and keep
-// only a running max: a warp whose 32 x 32 chunk has no y > 0 -- nearly every
-// chunk -- moves on.  Chunks with a hit, and chunks on the diagonal or past
-// L, take the exact path: per column the hit mask of the warp's 32 rows
-// (ballot) gives the column's largest row i < j (atomicMax into j's word),
-// and each row keeps its largest column j > i (one atomicMax per item).
+// row); items are taken from a grid-wide counter (one atomic per item by the
+// producer, handed to the other roles through a small ring in shared memory),
+// in (sequence, kv head)-major order so that the CTAs at work share the keys
+// of one head in L2, and the small items come last.  The rows' keys stay in
+// shared memory (A) while the columns' keys stream through a ring of
+// kStages tiles of N = 256/RT keys (B).  For each column tile one thread
+// issues RT x (D/16) MMAs of M = 128, N, K = 16 into one of two accumulator
+// buffers (RT*N = 256 TMEM columns each); eight epilogue warps read the other
+// buffer.  Row i hits column j when acc_ij * (1/|k_j|) > p*|k_i| (> 0 for
+// p > 0); since 1/|k_j| <= the chunk's largest, a 32-column chunk whose
+// largest acc times that bound stays at or below p*|k_i| has no hit -- nearly
+// every chunk -- so the common path is one three-way max per two elements.
+// Chunks that may hold a hit, chunks on the diagonal or past L, and rows with
+// p*|k_i| <= 0 take the exact path: per column the hit mask of the warp's 32
+// rows (ballot) gives the column's largest row i < j (atomicMax into j's
+// word), and each row keeps its largest column j > i (one atomicMax per item).
 constexpr int kApStages = 4;
 constexpr int kItemCols = 8192;
 constexpr int kEpiWarps = 8;
 constexpr int kApThreads = 32 * (2 + kEpiWarps);
+constexpr int kItemRing = 4;
 
 template <int D, int RT>
 struct GramCfg {
@@ -287,7 +298,9 @@ struct GramCfg {
     static constexpr int B_HALF = N * 128;
     static constexpr int STAGE = KH * B_HALF;
     static constexpr int BAR_OFF = A_BYTES + kApStages * STAGE;
-    static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers, words, alignment slack
+    static constexpr int BLK_OFF = BAR_OFF + 512;     // block rows of the current item
+    static constexpr int NBLK = ROWS / 16 + kItemCols / 16;
+    static constexpr int SMEM = BLK_OFF + NBLK * 4 + 1024;  // + alignment slack
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, N);
 };
 
@@ -315,10 +328,23 @@ __device__ __forceinline__ bool ap_item(const ApArgs &a, int g, int items_per_sh
     return c0 < L;
 }
 
-// Exact test of one 32-column chunk for the warp's rows (see the kernel).
-__device__ __forceinline__ void ap_chunk_exact(const uint32_t (&v)[32], const float (&ic)[32], int i, bool valid,
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(x), "f"(y), "f"(z));
+    return r;
+}
+
+// Exact test of one 32-column chunk (v: raw products, columns j0..j0+31) for
+// the warp's rows (see the kernel).
+__device__ __forceinline__ void ap_chunk_exact(const uint32_t *v, const float *inv_row, int i, bool valid,
                                                float nthr, int j0, int L, int rowbase, int *best, int *cand_row,
                                                int lane) {
+    float ic[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const float4 w = *reinterpret_cast<const float4 *>(inv_row + j0 + 4 * u);
+        ic[4 * u] = w.x, ic[4 * u + 1] = w.y, ic[4 * u + 2] = w.z, ic[4 * u + 3] = w.w;
+    }
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
         const int j = j0 + jj;
@@ -335,6 +361,7 @@ __global__ void __launch_bounds__(kApThreads, 1)
     ap_gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const ApArgs a, int items_per_sh, int n_items) {
     using C = GramCfg<D, RT>;
     constexpr int N = C::N;
+    static_assert(N % 32 == 0, "tiles are whole 32-column chunks");
     extern __shared__ unsigned char ap_smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(ap_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -344,11 +371,15 @@ __global__ void __launch_bounds__(kApThreads, 1)
     uint64_t *empty = full + kApStages;
     uint64_t *a_full = empty + kApStages;
     uint64_t *a_empty = a_full + 1;
-    uint64_t *acc_full = a_empty + 1;   // [2]
-    uint64_t *acc_empty = acc_full + 2; // [2]
-    uint64_t *drain = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *acc_full = a_empty + 1;    // [2]
+    uint64_t *acc_empty = acc_full + 2;  // [2]
+    uint64_t *item_full = acc_empty + 2; // [kItemRing]
+    uint64_t *item_empty = item_full + kItemRing;
+    uint64_t *drain = item_empty + kItemRing;
+    int *item_slot = reinterpret_cast<int *>(drain + 1);  // [kItemRing]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_slot + kItemRing);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *zrow = reinterpret_cast<int *>(smem + C::BLK_OFF);  // TMA row of each 16-token group, -16 = zeros
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -361,6 +392,10 @@ __global__ void __launch_bounds__(kApThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kItemRing; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -376,64 +411,89 @@ __global__ void __launch_bounds__(kApThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer: TMA loads of the row keys (A) and the column tiles (B)
-        if (lane == 0) {
-            prefetch_tensormap(&tmap);
-            uint32_t fill = 0, item = 0, item_armed = 0;
-            for (int g = blockIdx.x; g < n_items && !*abort_flag; g += gridDim.x) {
-                int s, h, r0, c0, c1, L;
-                if (!ap_item<C::ROWS>(a, g, items_per_sh, s, h, r0, c0, c1, L)) continue;
-                if (!mbar_wait_bounded(a_empty, (item & 1) ^ 1, a.err, abort_flag, 0x220)) break;
-                mbar_arrive_expect_tx(a_full, C::A_BYTES);
-                item_armed = item + 1;
-                for (int G = 0; G < RT * 8; ++G) {
-                    const int t = r0 + 16 * G;
-                    int z = -16;  // past the sequence: a box of zeros
-                    if (t < L) {
-                        const int blk = ap_block(a, s, t, 0x221);
-                        if (blk >= 0) z = blk * a.b + t % a.b;
-                    }
+        // ---------------- producer: takes the items, TMA loads of A and of the B tiles.
+        // The whole warp looks up the item's block ids (one table read per 16
+        // tokens) into shared memory first; lane 0 then issues the copies.
+        uint32_t fill = 0, item = 0, item_armed = 0;
+        if (lane == 0) prefetch_tensormap(&tmap);
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t slot = k % kItemRing;
+            int g = -1;
+            if (lane == 0) {
+                if (!*abort_flag &&
+                    mbar_wait_bounded(&item_empty[slot], ((k / kItemRing) & 1) ^ 1, a.err, abort_flag, 0x22B)) {
+                    g = atomicAdd(a.counter, 1);
+                    item_slot[slot] = g < n_items ? g : -1;
+                    mbar_arrive(&item_full[slot]);  // releases the slot's value to the other roles
+                    if (g >= n_items) g = -1;
+                } else {
+                    g = -2;  // aborted: nothing published
+                }
+            }
+            g = __shfl_sync(0xFFFFFFFFu, g, 0);
+            if (g < 0) break;
+            int s, h, r0, c0, c1, L;
+            if (!ap_item<C::ROWS>(a, g, items_per_sh, s, h, r0, c0, c1, L)) continue;
+            const int nrow = C::ROWS / 16, ncol = (c1 - c0 + 15) / 16;
+            __syncwarp();  // lane 0 is done with the previous item's rows
+            for (int G = lane; G < nrow + ncol; G += 32) {
+                const int t = G < nrow ? r0 + 16 * G : c0 + 16 * (G - nrow);
+                int z = -16;  // past the sequence: a box of zeros
+                if (t < L) {
+                    const int blk = ap_block(a, s, t, G < nrow ? 0x221 : 0x223);
+                    if (blk >= 0) z = blk * a.b + t % a.b;
+                }
+                zrow[G] = z;
+            }
+            __syncwarp();
+            if (lane != 0) continue;
+            // a wait that gives up sets the abort flag: lane 0 goes back to the
+            // top, where the other lanes learn it from the broadcast
+            if (!mbar_wait_bounded(a_empty, (item & 1) ^ 1, a.err, abort_flag, 0x220)) continue;
+            mbar_arrive_expect_tx(a_full, C::A_BYTES);
+            item_armed = item + 1;
+            for (int G = 0; G < nrow; ++G) {
+#pragma unroll
+                for (int kh = 0; kh < C::KH; ++kh)
+                    tma_load_3d(As + kh * C::A_HALF + G * 2048, &tmap, kh * 64, h, zrow[G], a_full);
+            }
+            const int ntiles = (c1 - c0 + N - 1) / N;
+            for (int j = 0; j < ntiles; ++j) {
+                const uint32_t st = fill % kApStages;
+                if (!mbar_wait_bounded(&empty[st], ((fill / kApStages) & 1) ^ 1, a.err, abort_flag, 0x222)) break;
+                mbar_arrive_expect_tx(&full[st], C::STAGE);
+                ++fill;
+                unsigned char *dst = Bs + st * C::STAGE;
+#pragma unroll
+                for (int G = 0; G < N / 16; ++G) {
+                    const int gi = nrow + j * (N / 16) + G;
+                    const int z = gi < nrow + ncol ? zrow[gi] : -16;
 #pragma unroll
                     for (int kh = 0; kh < C::KH; ++kh)
-                        tma_load_3d(As + kh * C::A_HALF + G * 2048, &tmap, kh * 64, h, z, a_full);
+                        tma_load_3d(dst + kh * C::B_HALF + G * 2048, &tmap, kh * 64, h, z, &full[st]);
                 }
-                const int ntiles = (c1 - c0 + N - 1) / N;
-                for (int j = 0; j < ntiles; ++j) {
-                    const uint32_t st = fill % kApStages;
-                    if (!mbar_wait_bounded(&empty[st], ((fill / kApStages) & 1) ^ 1, a.err, abort_flag, 0x222))
-                        break;
-                    mbar_arrive_expect_tx(&full[st], C::STAGE);
-                    ++fill;
-                    unsigned char *dst = Bs + st * C::STAGE;
-                    for (int G = 0; G < N / 16; ++G) {
-                        const int t = c0 + j * N + 16 * G;
-                        int z = -16;
-                        if (t < L) {
-                            const int blk = ap_block(a, s, t, 0x223);
-                            if (blk >= 0) z = blk * a.b + t % a.b;
-                        }
-#pragma unroll
-                        for (int kh = 0; kh < C::KH; ++kh)
-                            tma_load_3d(dst + kh * C::B_HALF + G * 2048, &tmap, kh * 64, h, z, &full[st]);
-                    }
-                }
-                ++item;
             }
-            if (*abort_flag) {
-                // let the loads already armed land before the CTA releases its
-                // shared memory: the newest armed phase of each stage and of A
-                volatile int never = 0;
-                for (uint32_t f = fill > kApStages ? fill - kApStages : 0; f < fill; ++f)
-                    mbar_wait_bounded(&full[f % kApStages], (f / kApStages) & 1, a.err, &never, 0x229);
-                if (item_armed > item) mbar_wait_bounded(a_full, item & 1, a.err, &never, 0x22A);
-            }
+            ++item;
+        }
+        if (lane == 0 && *abort_flag) {
+            // let the loads already armed land before the CTA releases its
+            // shared memory: the newest armed phase of each stage and of A
+            volatile int never = 0;
+            for (uint32_t f = fill > kApStages ? fill - kApStages : 0; f < fill; ++f)
+                mbar_wait_bounded(&full[f % kApStages], (f / kApStages) & 1, a.err, &never, 0x229);
+            if (item_armed > item) mbar_wait_bounded(a_full, item & 1, a.err, &never, 0x22A);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
             uint32_t fill = 0, tile = 0, item = 0;
             const uint32_t a_addr = smem_u32(As), b_addr = smem_u32(Bs);
-            for (int g = blockIdx.x; g < n_items && !*abort_flag; g += gridDim.x) {
+            for (uint32_t k = 0; !*abort_flag; ++k) {
+                const uint32_t slot = k % kItemRing;
+                if (!mbar_wait_bounded(&item_full[slot], (k / kItemRing) & 1, a.err, abort_flag, 0x22C)) break;
+                const int g = item_slot[slot];
+                mbar_arrive(&item_empty[slot]);
+                if (g < 0) break;
                 int s, h, r0, c0, c1, L;
                 if (!ap_item<C::ROWS>(a, g, items_per_sh, s, h, r0, c0, c1, L)) continue;
                 if (!mbar_wait_bounded(a_full, item & 1, a.err, abort_flag, 0x224)) break;
@@ -473,65 +533,72 @@ __global__ void __launch_bounds__(kApThreads, 1)
         const int q = warp & 3;      // TMEM lanes 32q..32q+31 (fixed by the warp's position)
         const int half = e >> 2;     // row tiles half, half + 2, ...
         uint32_t tile = 0;
-        for (int g = blockIdx.x; g < n_items && !*abort_flag; g += gridDim.x) {
+        for (uint32_t k = 0; !*abort_flag; ++k) {
+            const uint32_t slot = k % kItemRing;
+            if (!mbar_wait_bounded(&item_full[slot], (k / kItemRing) & 1, a.err, abort_flag, 0x22D)) break;
+            const int g = item_slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (g < 0) break;
             int s, h, r0, c0, c1, L;
             if (!ap_item<C::ROWS>(a, g, items_per_sh, s, h, r0, c0, c1, L)) continue;
             const size_t base = ((size_t)s * a.h_kv + h) * a.Lpad;
             const float *inv_row = a.inv + base;
+            const float *cmax_row = a.cmax + base / 32;
             int *cand_row = a.cand + base;
             constexpr int M = RT / 2;  // rows per thread
             int rowi[M], best[M];
             bool valid[M];
-            float nthr[M];
+            float thr[M];
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 rowi[m] = r0 + (half + 2 * m) * 128 + 32 * q + lane;
                 valid[m] = rowi[m] < L;
                 const float iv = valid[m] ? inv_row[rowi[m]] : 0.f;
-                const float thr = iv > 0.f ? a.p / iv : (a.p < 0.f ? -INFINITY : INFINITY);
-                nthr[m] = -thr;
+                thr[m] = iv > 0.f ? a.p / iv : (a.p < 0.f ? -INFINITY : INFINITY);
                 best[m] = -1;
             }
             const int ntiles = (c1 - c0 + N - 1) / N;
             bool ok_item = true;
             for (int j = 0; j < ntiles; ++j, ++tile) {
                 const uint32_t ab = tile & 1;
+                const int cb = c0 + j * N;
+                float cm[N / 32];  // chunk bounds of 1/|k_j|, fetched before the wait
+#pragma unroll
+                for (int ch = 0; ch < N / 32; ++ch) cm[ch] = cmax_row[(cb >> 5) + ch];
                 if (!mbar_wait_bounded(&acc_full[ab], (tile >> 1) & 1, a.err, abort_flag, 0x227)) {
                     ok_item = false;
                     break;
                 }
                 tc_fence_after();
-                const int cb = c0 + j * N;
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const int rt = half + 2 * m;
                     const int rowbase = r0 + rt * 128 + 32 * q;
-#pragma unroll 1
-                    for (int ch = 0; ch < N / 32; ++ch) {
-                        const int j0 = cb + ch * 32;
-                        uint32_t v[32];
-                        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + ab * 256 + rt * N + ch * 32, v);
-                        float ic[32];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const float4 w = *reinterpret_cast<const float4 *>(inv_row + j0 + 4 * u);
-                            ic[4 * u] = w.x, ic[4 * u + 1] = w.y, ic[4 * u + 2] = w.z, ic[4 * u + 3] = w.w;
-                        }
-                        const bool interior = j0 > rowbase + 31 && j0 + 31 < L && rowbase + 31 < L;
-                        bool exact = !interior;
-                        if (interior) {
-                            const float2 nt2 = make_float2(nthr[m], nthr[m]);
-                            float mx = -INFINITY;
+                    for (int c2 = 0; c2 < N / 64; ++c2) {
+                        uint32_t v[64];
+                        tmem_ld64(tmem + ((uint32_t)(32 * q) << 16) + ab * 256 + rt * N + c2 * 64, v);
 #pragma unroll
-                            for (int jj = 0; jj < 32; jj += 2) {
-                                const float2 y = ffma2(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
-                                                       make_float2(ic[jj], ic[jj + 1]), nt2);
-                                mx = fmaxf(mx, fmaxf(y.x, y.y));
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int ch = c2 * 2 + hh;
+                            const int j0 = cb + ch * 32;
+                            const uint32_t *vc = v + hh * 32;
+                            bool exact = !(j0 > rowbase + 31 && j0 + 31 < L && rowbase + 31 < L);
+                            if (!exact) {
+                                float mx = __uint_as_float(vc[0]);
+#pragma unroll
+                                for (int jj = 1; jj < 31; jj += 2)
+                                    mx = max3f(mx, __uint_as_float(vc[jj]), __uint_as_float(vc[jj + 1]));
+                                mx = fmaxf(mx, __uint_as_float(vc[31]));
+                                // no hit possible iff thr > 0 and mx * bound <= thr
+                                const bool maybe = !(thr[m] > 0.f) || fmaf(mx, cm[ch], -thr[m]) > 0.f;
+                                exact = __any_sync(0xFFFFFFFFu, maybe);
                             }
-                            exact = __any_sync(0xFFFFFFFFu, mx > 0.f);
+                            if (exact)
+                                ap_chunk_exact(vc, inv_row, rowi[m], valid[m], -thr[m], j0, L, rowbase, &best[m],
+                                               cand_row, lane);
                         }
-                        if (exact)
-                            ap_chunk_exact(v, ic, rowi[m], valid[m], nthr[m], j0, L, rowbase, &best[m], cand_row, lane);
                     }
                 }
                 tc_fence_before();
@@ -545,8 +612,8 @@ __global__ void __launch_bounds__(kApThreads, 1)
         }
     }
 
-    // ---------------- teardown: after a timeout, let the copies and products in
-    // flight land before the shared memory and the tensor memory are released
+    // ---------------- teardown: after a timeout, let the products in flight
+    // land before the tensor memory is released
     __syncthreads();
     if (*abort_flag && threadIdx.x == 32) {
         volatile int never = 0;
@@ -611,6 +678,7 @@ zp_status launch_gram_tc(const ApArgs &a, const DeviceInfo &dev, cudaStream_t st
 template <typename T, int D>
 zp_status launch_typed(const ApArgs &a, const DeviceInfo &dev, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(a.shat, 0, (size_t)a.n * a.h_kv * D * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.counter, 0, 4, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(a.rho, 0, (size_t)a.n * a.h_kv * a.Lmax * 4, st);
     if (e != cudaSuccess) return cuda_fail(e, "all-pairs redundancy: clearing the sums");
     ap_prep_kernel<T, D><<<dim3(a.Lpad / 128, a.h_kv, a.n), 128, 0, st>>>(a);
@@ -618,7 +686,7 @@ zp_status launch_typed(const ApArgs &a, const DeviceInfo &dev, cudaStream_t st) 
     if (e != cudaSuccess) return cuda_fail(e, "all-pairs redundancy: prep launch");
     zp_status rc = ZP_OK;
     if constexpr (sizeof(T) == 2) {
-        rc = launch_gram_tc<D, 4>(a, dev, st);
+        rc = launch_gram_tc<D, 2>(a, dev, st);  // two 128-row tiles, N = 128 (measured best)
     } else {
         ap_gram_f32_kernel<D><<<dim3((a.Lmax + 127) / 128, a.h_kv, a.n), 128, 0, st>>>(a);
         e = cudaGetLastError();
@@ -635,7 +703,8 @@ zp_status launch_typed(const ApArgs &a, const DeviceInfo &dev, cudaStream_t st) 
 
 size_t all_pairs_workspace_size(int n, int h_kv, int d, int Lmax) {
     const size_t Lpad = align_up((size_t)(Lmax > 0 ? Lmax : 1), 128);
-    return 2 * align_up((size_t)n * h_kv * Lpad * 4, 256) + align_up((size_t)n * h_kv * d * 4, 256);
+    return 2 * align_up((size_t)n * h_kv * Lpad * 4, 256) + align_up((size_t)n * h_kv * d * 4, 256) +
+           align_up((size_t)n * h_kv * (Lpad / 32) * 4, 256) + 256;
 }
 
 zp_status launch_all_pairs(const AllPairsArgs &in, cudaStream_t st) {
@@ -665,6 +734,9 @@ zp_status launch_all_pairs(const AllPairsArgs &in, cudaStream_t st) {
     a.inv = reinterpret_cast<float *>(ws);
     a.cand = reinterpret_cast<int *>(ws + arr);
     a.shat = reinterpret_cast<float *>(ws + 2 * arr);
+    const size_t sh_bytes = align_up((size_t)in.n * in.h_kv * in.d * 4, 256);
+    a.cmax = reinterpret_cast<float *>(ws + 2 * arr + sh_bytes);
+    a.counter = reinterpret_cast<int *>(ws + 2 * arr + sh_bytes + align_up((size_t)in.n * in.h_kv * (a.Lpad / 32) * 4, 256));
     a.rho = in.rho;
     a.err = dev.error_word;
     if (in.n == 0 || in.Lmax == 0) return ZP_OK;
