@@ -709,6 +709,49 @@ def long_prefill_measure(dev, peak, reps=10, all_pairs_reps=2):
     return out
 
 
+ALL_PAIRS = "all_pairs_redundancy_4x32k"
+
+
+def run_all_pairs(args, dev):
+    """The all-pairs redundancy alone (zp_score_tokens with lightning = 0) on
+    4 sequences of 32768 tokens (32q/8kv/128, bf16, b = 16, keys drawn on the
+    device): W untimed calls, then K calls between one event pair.  Prints one
+    JSON line (a profiling entry point, not the headline workload)."""
+    import compressed_paged_kv_zp_gb300 as zp
+    B, h_kv, d, b, L = 4, 8, 128, 16, 32768
+    c = zp_inputs.make_paged_case(1140, B, 32, h_kv, d, b, lens=[L] * B, dtype="bf16", device=dev)
+    desc = zp.cache_desc(32, h_kv, d, b, c.n_total, torch.bfloat16)
+    K = c.k_cache[0]
+    lens, tab = c.seq_lens.to(dev), c.block_table.to(dev)
+    S = torch.full((B, h_kv, L), 0.01, device=dev)
+    F = torch.zeros(c.n_total, b, h_kv, device=dev)
+    first = torch.ones(B, dtype=torch.uint8, device=dev)
+    scores = torch.empty(B, h_kv, L, device=dev)
+    ws = torch.empty(zp.zp_score_workspace_size(desc, B, L), dtype=torch.uint8, device=dev)
+    prm = zp.score_params(window=16, lightning=False)
+
+    def call():
+        zp.zp_score_tokens(desc, prm, K, tab, lens, first, S, F, scores, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    code, _ = zp.zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d" % code)
+    ms = e0.elapsed_time(e1) / args.steps
+    gram = 2.0 * B * h_kv * d * L * (L - 1) / 2
+    print(json.dumps({"workload": ALL_PAIRS, "ms_per_call": ms, "gram_tflops_distinct_pairs": gram / ms / 1e9,
+                      "steps": args.steps, "warmup": args.warmup}))
+    return 0
+
+
 def tie_check(wl):
     """One more compression of the triggered sequences against the oracle fed
     the same score rows and keys (snapshot before the call): keep sets must be
@@ -785,7 +828,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zp", choices=["zp", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + [ENGINE_WORKLOAD])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(WORKLOADS) + [ENGINE_WORKLOAD, ALL_PAIRS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sub", action="store_true",
@@ -808,6 +852,8 @@ def main():
     torch.cuda.set_device(dev)
     if args.workload == ENGINE_WORKLOAD:
         return run_engine(args, dist, rank, world, dev)
+    if args.workload == ALL_PAIRS:
+        return run_all_pairs(args, dev)
     wl = Workload(args.workload, seed_offset=rank, dev=dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):

@@ -89,16 +89,14 @@ class DecodeLoop:
                 self.table[s, :nb] = self.pool.alloc(nb)
         else:
             self.table[:] = tables
-            used = sorted(set(int(x) for x in tables.flatten() if x >= 0))
+            held = np.asarray(tables, dtype=np.int64).ravel()
+            held = held[held >= 0]
+            refs = np.bincount(held, minlength=self.n_total)
             self.pool.alloc(self.n_total)  # take every block, then give back the unused ones
-            self.pool.release([i for i in range(self.n_total) if i not in set(used)])
-            refs = {}
-            for x in tables.flatten():
-                if x >= 0:
-                    refs[int(x)] = refs.get(int(x), 0) + 1
-            for blk, r in refs.items():  # shared prefix blocks: one reference per holder
-                if r > 1:
-                    self.pool.incref([blk] * (r - 1))
+            self.pool.release(np.nonzero(refs == 0)[0].tolist())
+            extra = np.repeat(np.arange(self.n_total), np.maximum(refs - 1, 0))
+            if len(extra):  # shared prefix blocks: one reference per holder
+                self.pool.incref(extra.tolist())
         self.first = np.ones(B, dtype=np.uint8)  # never compressed yet
         self.active = np.ones(B, dtype=bool)
         self.table_dev = torch.from_numpy(self.table).to(self.dev)

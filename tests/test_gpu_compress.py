@@ -540,3 +540,63 @@ def test_all_pairs_redundancy_matches_oracle(zp):
         fired += int((cosm > 0.9).any(axis=0).sum())
     assert fired > 50  # the zeroing rule acted on many columns
     print("reported near-tie swaps:", swaps, "columns with a zeroed entry (head 0):", fired)
+
+
+@pytest.mark.parametrize("w", [4, 8, 16])
+def test_tiny_every_flag_combination(zp, w):
+    """The tiny workload (4 sequences, 8q/2kv/64, fp32, b 16, N_max 4, 80-150
+    tokens, near-duplicate keys) through zp_compress_layers under every
+    combination of the scoring switches -- global score on/off, pooling
+    never / first / every, redundancy off / lightning / all pairs, first or
+    later compression -- at window w: final scores against the oracle at the
+    fp32 tolerance, keep sets equal up to reported near-ties, and the moved
+    key rows bitwise."""
+    import itertools
+    B, h_q, h_kv, d, b, N_max = 4, 8, 2, 64, 16, 4
+    c = _block_aligned_case(1200 + w, B, h_q, h_kv, d, b, 80, 150, "f32", dup=True, spare=B * N_max)
+    desc = _desc(zp, c)
+    lens = c.seq_lens.tolist()
+    Lmax = max(lens)
+    k = (N_max - 1) * b
+    rng = np.random.default_rng(1210 + w)
+    S0 = (rng.random((B, h_kv, Lmax)) / 100).astype(np.float32)
+    F0 = (rng.random((c.n_total, b, h_kv)) / 80).astype(np.float32)
+    free = c.free_blocks.numpy()
+    targets = torch.from_numpy(np.stack([free[i * (N_max - 1):(i + 1) * (N_max - 1)]
+                                         for i in range(B)]).astype(np.int32)).cuda()
+    K0 = c.k_cache[0].float().numpy()
+    swaps = combos = 0
+    for use_global, pool_policy, redundancy, first in itertools.product((True, False), (0, 1, 2),
+                                                                        ("off", "lightning", "all"), (1, 0)):
+        kw = dict(window=w, use_global=use_global, pool_policy=pool_policy,
+                  use_similarity=redundancy != "off", lightning=redundancy != "all")
+        params = zp.score_params(**kw)
+        prm = pipeline.ScoreParams(window=w, use_global=use_global, pool_policy=pool_policy,
+                                   use_similarity=redundancy != "off", lightning=redundancy != "all")
+        dc = DeviceCase(c)
+        S = torch.from_numpy(S0.copy()).cuda()
+        F = torch.from_numpy(F0.copy()).cuda()
+        fc = torch.full((B,), first, dtype=torch.uint8, device="cuda")
+        scores = torch.full((B, h_kv, Lmax), -5.0, device="cuda")
+        keep = torch.empty(B, h_kv, k, dtype=torch.int32, device="cuda")
+        zp.zp_compress_layers(desc, params, dc.K[0], dc.V[0], dc.table, dc.lens, fc, S, F, targets, k, keep, Lmax,
+                              scores_out=scores)
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        got, kept, Kg = scores.cpu().numpy(), keep.cpu().numpy(), dc.K[0].cpu().numpy()
+        Fref = F0.astype(np.float64).copy()
+        for s, L in enumerate(lens):
+            want = pipeline.final_scores(S0[s, :, :L].astype(np.float64), K0, Fref, c.block_table[s].numpy(), L, b,
+                                         bool(first), prm)
+            fin = np.isfinite(want)
+            assert np.array_equal(fin, np.isfinite(got[s, :, :L])), kw
+            np.testing.assert_allclose(got[s, :, :L][fin], want[fin], **TOL_SCORE["f32"], err_msg=str(kw))
+            for h in range(h_kv):
+                swaps += keep_sets_match(kept[s, h], oracle.topk_keep(want[h], k)[0], want[h], k, L)
+                tg = targets[s].cpu().numpy()
+                for r, pos in enumerate(kept[s, h][:min(k, L)]):
+                    src = K0[c.block_table[s, pos // b], pos % b, h]
+                    assert np.array_equal(Kg[tg[r // b], r % b, h], src)
+        combos += 1
+    assert combos == 36
+    print("w=%d combinations: %d, reported near-tie swaps: %d" % (w, combos, swaps))
