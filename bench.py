@@ -752,6 +752,48 @@ def run_all_pairs(args, dev):
     return 0
 
 
+WINDOW_SCORE = "window_score_16x32k"
+
+
+def run_window_score(args, dev):
+    """The explicit window score alone (zp_window_score: Alg. 1 with 16 window
+    queries) on the long-prefill shape, 16 sequences of 32768 tokens
+    (32q/8kv/128, bf16, b = 16, keys drawn on the device): W untimed calls,
+    then K calls between one event pair.  Prints one JSON line (a profiling
+    entry point, not the headline workload)."""
+    import compressed_paged_kv_zp_gb300 as zp
+    B, h_q, h_kv, d, b, L, w = 16, 32, 8, 128, 16, 32768, 16
+    c = zp_inputs.make_paged_case(1004, B, h_q, h_kv, d, b, lens=[L] * B, dtype="bf16", device=dev)
+    desc = zp.cache_desc(h_q, h_kv, d, b, c.n_total, torch.bfloat16)
+    K = c.k_cache[0]
+    lens, tab = c.seq_lens.to(dev), c.block_table.to(dev)
+    gd = torch.Generator(device=dev).manual_seed(1005)
+    qw = torch.randn(B, w, h_q, d, generator=gd, device=dev).to(torch.bfloat16)
+    W = torch.empty(B, h_kv, L, device=dev)
+    ws = torch.empty(zp.zp_window_score_workspace_size(desc, B, L, w), dtype=torch.uint8, device=dev)
+
+    def call():
+        zp.zp_window_score(desc, qw, K, tab, lens, W, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    code, _ = zp.zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d" % code)
+    ms = e0.elapsed_time(e1) / args.steps
+    by = B * L * h_kv * d * 2 + B * w * h_q * d * 2 + 4 * B * L * h_kv
+    print(json.dumps({"workload": WINDOW_SCORE, "ms_per_call": ms, "algorithmic_GBs": by / ms / 1e6,
+                      "steps": args.steps, "warmup": args.warmup}))
+    return 0
+
+
 def tie_check(wl):
     """One more compression of the triggered sequences against the oracle fed
     the same score rows and keys (snapshot before the call): keep sets must be
@@ -829,7 +871,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zp", choices=["zp", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(WORKLOADS) + [ENGINE_WORKLOAD, ALL_PAIRS])
+                    choices=sorted(WORKLOADS) + [ENGINE_WORKLOAD, ALL_PAIRS, WINDOW_SCORE])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sub", action="store_true",
@@ -854,6 +896,8 @@ def main():
         return run_engine(args, dist, rank, world, dev)
     if args.workload == ALL_PAIRS:
         return run_all_pairs(args, dev)
+    if args.workload == WINDOW_SCORE:
+        return run_window_score(args, dev)
     wl = Workload(args.workload, seed_offset=rank, dev=dev)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):

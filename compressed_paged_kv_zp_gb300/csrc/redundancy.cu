@@ -23,9 +23,6 @@
 // token than any word < L.
 #include <math.h>
 
-#include <cudaTypedefs.h>
-#include <mutex>
-
 #include "tc05.cuh"
 
 namespace zp {
@@ -627,29 +624,13 @@ __global__ void __launch_bounds__(kApThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-cudaError_t g_encode_err = cudaSuccess;
-
+// The layer's keys as a 3-D tensor (element of the head, kv head, token row);
+// a box is 64 elements of one kv head for 16 tokens.
 zp_status encode_key_map(CUtensorMap *map, const void *k, int d, int h_kv, int b, int n_total) {
-    std::call_once(g_encode_once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!g_encode) return fail(ZP_ERR_CUDA, "all-pairs redundancy: cuTensorMapEncodeTiled unavailable");
-    // the layer's keys as a 3-D tensor: (element of the head, kv head, token row)
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)h_kv, (cuuint64_t)n_total * (cuuint64_t)b};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)h_kv * d * 2};
-    const cuuint32_t box[3] = {64, 1, 16};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(ZP_ERR_CUDA, "all-pairs redundancy: cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return ZP_OK;
+    const uint64_t dims[3] = {(uint64_t)d, (uint64_t)h_kv, (uint64_t)n_total * (uint64_t)b};
+    const uint64_t strides[2] = {(uint64_t)d * 2, (uint64_t)h_kv * d * 2};
+    const uint32_t box[3] = {64, 1, 16};
+    return encode_tmap_bf16_3d(map, k, dims, strides, box, "all-pairs redundancy");
 }
 
 template <int D, int RT>

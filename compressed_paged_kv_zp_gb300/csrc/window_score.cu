@@ -11,25 +11,18 @@
 // queries exist but no decode step has accumulated the score.
 //
 // The R = w*g query rows of a kv head against the sequence's keys form a
-// dense contraction (64 x 128 x L for the Qwen3-8B shape), run on the tensor
-// cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) in two passes over K:
-//   pass 1: per CTA and row, the max and sum of exp over its chunk of pages;
-//   merge:  the chunks' statistics -> per row (M, L);
-//   pass 2: logits again, P from (M, L), max over the group, sum over u.
-// One CTA per (sequence, chunk of pages); a producer warp copies each token
-// row of a page (all kv heads, contiguous in HBM) with one bulk copy into a
-// padded staging row; one consumer warp per kv head.  fp32 caches take a
-// plain CUDA-core kernel (the small parity workload).
+// dense contraction (64 x 128 x L for the Qwen3-8B shape), run on the
+// fifth-generation tensor cores in two passes over K (see the bf16 path
+// below: tcgen05.mma with the tokens as the M = 128 operand, accumulators in
+// tensor memory, TMA loads of the keys and of the window queries).  fp32
+// caches take a plain CUDA-core kernel (the small parity workload, 1e-4).
 #include <math.h>
 
-#include "zp_common.cuh"
+#include "tc05.cuh"
 
 namespace zp {
 namespace {
 
-constexpr int kPages = 64;   // pages (16-token units) per CTA chunk
-constexpr int kWsStages = 2;
-constexpr int kRowPad = 16;
 
 struct WsArgs {
     const void *q;       // [n][w][h_q][d]
@@ -39,10 +32,8 @@ struct WsArgs {
     const int32_t *seq_lens;
     int n, h_q, h_kv, d, b, n_total, w, Lmax;
     float qscale;        // log2(e) / sqrt(d)
-    float2 *part;        // [n][chunks][h_kv * R] partial (max, sum)
-    float2 *stats;       // [n][h_kv * R] final (max, sum)
+    float2 *stats;       // [n][h_kv][w * G] final (max, sum)
     float *out;          // [n][h_kv][Lmax]
-    int chunks;          // chunk capacity per sequence
     unsigned *err;
 };
 
@@ -54,214 +45,451 @@ __device__ __forceinline__ int seq_len(const WsArgs &a, int s) {
 }
 
 // ------------------------------------------------------------------ bf16 path
-// smem: bars | Q tiles [h_kv][R rows][D*2 + pad] | stages [kWsStages][16 rows][h_kv*D*2 + pad]
-template <int D, int MT, int G, bool PASS2>
-__global__ void __launch_bounds__(9 * 32, 1) ws_tc_kernel(const WsArgs a) {
-    constexpr int R = MT * 16;
-    constexpr int KS = D / 16;
-    extern __shared__ __align__(128) unsigned char sm[];
-    const int s = blockIdx.y;
-    const int chunk = blockIdx.x;
-    const int L = seq_len(a, s);
-    const int npages = (L + 15) / 16;
-    const int p0 = chunk * kPages;
-    if (p0 >= npages || L < a.w) return;
-    const int p1 = min(npages, p0 + kPages);
-    const int h_kv = a.h_kv;
-    const int QRS = D * 2 + kRowPad;               // Q row stride
-    const int KRS = h_kv * D * 2 + kRowPad;        // staged K row stride
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm);
-    uint64_t *empty = full + kWsStages;
-    unsigned char *qs = sm + 128;
-    unsigned char *ks0 = qs + (size_t)h_kv * R * QRS;
-    ks0 += (128 - (reinterpret_cast<uintptr_t>(ks0) & 127)) & 127;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int stage_bytes = 16 * KRS;
+// Per (sequence, kv head) the contraction is D[t][c] = k_t . q_c for the
+// R = w*g query rows c = u*g + j of the head (window row u, q head j of the
+// group) against every token t: 128 tokens are the M = 128 operand of one
+// tcgen05.mma (A: the head's keys, by TMA from the paged cache with the
+// 128-byte swizzle), the R query rows the N operand (B: one TMA box of the
+// window queries, rows landing in (u, j) order); the accumulator, R fp32
+// columns per token, sits in tensor memory, double-buffered.  A persistent
+// kernel per pass takes work items (sequence, kv head, 2048 tokens) from a
+// grid-wide counter; a producer warp (TMA), an MMA thread and eight epilogue
+// warps (two per TMEM lane quarter, each half of the columns).  An epilogue
+// thread owns one token:
+//   pass 1: per column an online (max, sum of exp) over the thread's tokens
+//           -- one exp2 per element: e = 2^-|x - m| either rescales the sum
+//           or is added to it -- reduced over the warp and the four lane
+//           quarters at the end of the item into a partial per (item, column);
+//   merge:  the partials of a (sequence, kv head) -> c = max + log2(sum) per column;
+//   pass 2: per window row u the max over the group of x - c (the softmax is
+//           monotonic in it), one exp2 per (token, u), summed over u and
+//           divided by w; the two column halves meet in shared memory.
+// x is the logit in log2 units; the causal mask hides token t from window row
+// u when t > L - w + u.
+constexpr int kWsTile = 128;     // tokens per MMA tile
+constexpr int kWsItem = 2048;    // tokens per work item
+constexpr int kWsTcStages = 4;
+constexpr int kWsEpi = 8;
+constexpr int kWsThreads = 32 * (2 + kWsEpi);
 
-    if (tid == 0) {
-        for (int i = 0; i < kWsStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], h_kv);
-        }
-        fence_barrier_init();
-    }
-    // Q rows (u, j) of every kv head: row r = u*G + j, q head kvh*G + j
-    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(a.q) + (size_t)s * a.w * a.h_q * D;
-    for (int c = tid; c < h_kv * R * (D / 8); c += blockDim.x) {
-        const int kvh = c / (R * (D / 8));
-        const int rem = c % (R * (D / 8));
-        const int r = rem / (D / 8);
-        const int c16 = rem % (D / 8);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        const int u = r / G, j = r % G;
-        if (u < a.w)
-            v = reinterpret_cast<const uint4 *>(qg + ((size_t)u * a.h_q + kvh * G + j) * D)[c16];
-        reinterpret_cast<uint4 *>(qs + ((size_t)kvh * R + r) * QRS)[c16] = v;
-    }
-    __syncthreads();
-    volatile int abort_flag = 0;
+template <int D, int R>
+struct WsCfg {
+    static constexpr int KH = D / 64;
+    static constexpr int KS = D / 16;
+    static constexpr int HALVES = R >= 32 ? 2 : 1;   // column halves of the epilogue
+    static constexpr int RH = R / HALVES;            // columns per epilogue warp
+    static constexpr int B_HALF = R * 128;           // query rows, one 64-element half
+    static constexpr int B_BYTES = KH * B_HALF;
+    static constexpr int A_HALF = kWsTile * 128;
+    static constexpr int STAGE = KH * A_HALF;
+    static constexpr int A_OFF = (B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int BAR_OFF = A_OFF + kWsTcStages * STAGE;
+    static constexpr int ZROW_OFF = BAR_OFF + 384;
+    static constexpr int RED_OFF = ZROW_OFF + (kWsItem / 16) * 4;
+    static constexpr int XCH_OFF = RED_OFF + 2 * 4 * R * 8;
+    static constexpr int SMEM = XCH_OFF + 2 * 4 * 32 * 4 + 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * R <= 32 ? 32 : (2 * R <= 64 ? 64 : (2 * R <= 128 ? 128 : 256));
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, R);
+};
 
-    if (warp == h_kv) {  // producer
-        const uint64_t pol = l2_evict_first_policy();
-        const unsigned row_bytes = (unsigned)(h_kv * D * 2);
-        const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.k);
-        for (int p = p0, i = 0; p < p1; ++p, ++i) {
-            const int st = i % kWsStages;
-            if (i >= kWsStages &&
-                !mbar_wait_bounded(&empty[st], (unsigned)(((i / kWsStages) - 1) & 1), a.err, &abort_flag, 50))
-                break;
-            const int blk = __ldg(&a.table[(size_t)s * a.table_stride + (p * 16) / a.b]);
-            const bool bad = blk < 0 || blk >= a.n_total;
-            int valid = L - p * 16;
-            if (valid > 16) valid = 16;
-            if (lane == 0) {
-                if (bad) record_error(a.err, ZP_ERR_DEVICE, 0x500);
-                mbar_arrive_expect_tx(&full[st], bad ? 0u : valid * row_bytes);
-            }
-            __syncwarp();
-            if (!bad && lane < valid) {
-                const size_t off = ((size_t)blk * a.b + (p * 16) % a.b + lane) * h_kv * D;
-                bulk_g2s(ks0 + (size_t)st * stage_bytes + lane * KRS, kg + off, row_bytes, &full[st], pol);
-            }
-        }
-        return;
-    }
+struct WsTcArgs {
+    const int32_t *table;
+    int table_stride;
+    const int32_t *seq_lens;
+    int n, h_kv, b, n_total, w, Lmax;
+    int items_per_sh, n_items;
+    float qscale;   // log2(e) / sqrt(d)
+    float2 *part;   // [n][h_kv][items_per_sh][R] (max, sum) per item (pass 1)
+    float *cst;     // [n][h_kv][R] max + log2(sum) per column (pass 2)
+    float *out;     // [n][h_kv][Lmax]
+    int *counter;   // work items taken (zero on entry)
+    unsigned *err;
+};
 
-    // consumer warp = kv head
-    const int kvh = warp;
-    const int g = lane >> 2, tig = lane & 3;
-    const int lm = lane >> 3;
-    // K (B operand) matrices: (t0-7,c) (t0-7,c+1) (t8-15,c) (t8-15,c+1)
-    const int krow = (lm >> 1) * 8 + (lane & 7), kch = lm & 1;
-    // Q (A operand) matrices: (r0-7,c) (r8-15,c) (r0-7,c+1) (r8-15,c+1)
-    const int qrow = (lm & 1) * 8 + (lane & 7), qch = lm >> 1;
-    const uint32_t qt = smem_u32(qs + (size_t)kvh * R * QRS);
-    // rows of this lane: (mt, g) and (mt, g+8); row r = 16*mt + g (+8)
-    float m_run[MT][2], l_run[MT][2];
-    float2 fin[MT][2];  // pass 2: final (max, 1/sum)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            m_run[mt][hh] = -INFINITY;
-            l_run[mt][hh] = 0.f;
-            if constexpr (PASS2) {
-                const float2 st2 = a.stats[(size_t)s * h_kv * R + kvh * R + 16 * mt + g + 8 * hh];
-                fin[mt][hh] = make_float2(st2.x, st2.y > 0.f ? 1.f / st2.y : 0.f);
-            }
-        }
-    const float inv_w = 1.f / (float)a.w;
-    for (int p = p0, i = 0; p < p1; ++p, ++i) {
-        const int st = i % kWsStages;
-        const bool got = mbar_wait_bounded(&full[st], (unsigned)((i / kWsStages) & 1), a.err, &abort_flag, 60);
-        int valid = L - p * 16;
-        if (valid > 16) valid = 16;
-        if (got) {
-            const uint32_t kt = smem_u32(ks0 + (size_t)st * stage_bytes) + kvh * D * 2;
-            uint32_t kb[KS][4];
-#pragma unroll
-            for (int t = 0; t < KS; ++t)
-                ldsm_x4(kt + krow * KRS + (2 * t + kch) * 16, kb[t][0], kb[t][1], kb[t][2], kb[t][3]);
-            float colsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // pass 2: [n-tile][e] sum over u of max over h
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int t = 0; t < KS; ++t) {
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(qt + (16 * mt + qrow) * QRS + (2 * t + qch) * 16, a0, a1, a2, a3);
-                    mma_16816(c0, a0, a1, a2, a3, kb[t][0], kb[t][1]);
-                    mma_16816(c1, a0, a1, a2, a3, kb[t][2], kb[t][3]);
-                }
-                // c0: rows (g, g+8) x tokens (2tig, 2tig+1); c1: tokens (8+2tig, 9+2tig)
-                float x[2][4];  // [row half][token]
-                x[0][0] = c0[0]; x[0][1] = c0[1]; x[0][2] = c1[0]; x[0][3] = c1[1];
-                x[1][0] = c0[2]; x[1][1] = c0[3]; x[1][2] = c1[2]; x[1][3] = c1[3];
-                const int tk[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * mt + g + 8 * hh;
-                    const int u = r / G;
-                    const int last = L - a.w + u;  // last key this query sees
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int t = p * 16 + tk[e];
-                        x[hh][e] = (u < a.w && tk[e] < valid && t <= last) ? x[hh][e] * a.qscale : -INFINITY;
-                    }
-                }
-                if constexpr (!PASS2) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float mx = fmaxf(fmaxf(x[hh][0], x[hh][1]), fmaxf(x[hh][2], x[hh][3]));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-                        const float mn = fmaxf(m_run[mt][hh], mx);
-                        float sum = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sum += (x[hh][e] == -INFINITY) ? 0.f : exp2f(x[hh][e] - mn);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-                        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-                        l_run[mt][hh] = (mn == -INFINITY) ? 0.f : l_run[mt][hh] * exp2f(m_run[mt][hh] - mn) + sum;
-                        m_run[mt][hh] = mn;
-                    }
-                } else {
-                    // P, then the max over the G rows of a window query: rows
-                    // r = u*G + j with j in the low bits of g
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float pv = (x[hh][e] == -INFINITY) ? 0.f : exp2f(x[hh][e] - fin[mt][hh].x) * fin[mt][hh].y;
-#pragma unroll
-                            for (int o = 4; o < 4 * G && o < 32; o <<= 1)
-                                pv = fmaxf(pv, __shfl_xor_sync(0xFFFFFFFFu, pv, o));
-                            // one lane per (u) group adds it: rows with j == 0
-                            if ((g % G) == 0) colsum[e >> 1][e & 1] += pv;
-                        }
-                }
-            }
-            if constexpr (PASS2) {
-                // sum over the u's held by different g (lanes with j == 0) and
-                // both row halves: add across the g bits above the group bits
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float v = ((g % G) == 0) ? colsum[nt][e] : 0.f;
-                        v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-                        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-                        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-                        const int t = nt * 8 + 2 * tig + e;
-                        if (g == 0 && t < valid)
-                            a.out[((size_t)s * h_kv + kvh) * a.Lmax + p * 16 + t] = v * inv_w;
-                    }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    if constexpr (!PASS2) {
-        if (tig == 0) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-                    a.part[((size_t)s * a.chunks + chunk) * h_kv * R + kvh * R + 16 * mt + g + 8 * hh] =
-                        make_float2(m_run[mt][hh], l_run[mt][hh]);
-        }
-    }
+__device__ __forceinline__ int ws_len(const WsTcArgs &a, int s) {
+    int L = a.seq_lens[s];
+    if (L < 0) L = 0;
+    if (L > a.Lmax) L = a.Lmax;
+    if (L > a.table_stride * a.b) L = a.table_stride * a.b;
+    return L;
 }
 
-// merge of the chunks' (max, sum) per (sequence, row); one thread per row
-__global__ void ws_merge_kernel(const WsArgs a, int rows) {
-    const int s = blockIdx.y;
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= rows) return;
-    const int L = seq_len(a, s);
-    const int nchunk = ((L + 15) / 16 + kPages - 1) / kPages;
+// 2^x by the PTX ISA's approximate base-2 exponential (ex2.approx.ftz.f32,
+// relative error ~2^-22; inputs below -126 give 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Work item g: (sequence, chunk, kv head) with the kv head fastest, so that
+// the CTAs at work read the kv heads' pieces of the same token rows (a row
+// holds every kv head) at about the same time.
+__device__ __forceinline__ void ws_item(const WsTcArgs &a, int g, int &s, int &h, int &t0, int &t1, int &L) {
+    const int per_seq = a.items_per_sh * a.h_kv;
+    s = g / per_seq;
+    const int r = g - s * per_seq;
+    const int chunk = r / a.h_kv;
+    h = r - chunk * a.h_kv;
+    L = ws_len(a, s);
+    t0 = chunk * kWsItem;
+    t1 = min(L, t0 + kWsItem);
+}
+
+template <int D, int R, int G, bool PASS2>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    ws_tc05_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                   const WsTcArgs a) {
+    using C = WsCfg<D, R>;
+    constexpr int RH = C::RH;
+    static_assert(R % 16 == 0 && R <= 128 && RH % 16 == 0 && RH % G == 0, "query rows");
+    extern __shared__ unsigned char ws_smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(ws_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char *Bs = smem;
+    unsigned char *As = smem + C::A_OFF;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + kWsTcStages;
+    uint64_t *b_full = empty + kWsTcStages;
+    uint64_t *b_empty = b_full + 1;
+    uint64_t *acc_full = b_empty + 1;    // [2]
+    uint64_t *acc_empty = acc_full + 2;  // [2]
+    uint64_t *item_full = acc_empty + 2; // [4]
+    uint64_t *item_empty = item_full + 4;
+    uint64_t *drain = item_empty + 4;
+    uint64_t *xch_full = drain + 1;      // [2] pass 2: the second column half's sums are in xch
+    uint64_t *red_full = xch_full + 2;   // [2] pass 1: every warp's statistics are in red
+    int *item_slot = reinterpret_cast<int *>(red_full + 2);  // [4]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_slot + 4);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *zrow = reinterpret_cast<int *>(smem + C::ZROW_OFF);
+    float2 *red = reinterpret_cast<float2 *>(smem + C::RED_OFF);  // [2][4 quarters][R]
+    float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);    // [2][4 quarters][32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWsTcStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kWsEpi);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 1 + kWsEpi);
+        }
+        mbar_init(drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xch_full[i], 4);      // one warp per lane quarter
+            mbar_init(&red_full[i], kWsEpi);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer: items, the head's query rows (B), token tiles (A)
+        uint32_t fill = 0, item = 0, b_armed = 0;
+        if (lane == 0) {
+            prefetch_tensormap(&kmap);
+            prefetch_tensormap(&qmap);
+        }
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t slot = k & 3;
+            int g = -1;
+            if (lane == 0) {
+                if (!*abort_flag &&
+                    mbar_wait_bounded(&item_empty[slot], ((k >> 2) & 1) ^ 1, a.err, abort_flag, 0x510)) {
+                    g = atomicAdd(a.counter, 1);
+                    item_slot[slot] = g < a.n_items ? g : -1;
+                    mbar_arrive(&item_full[slot]);
+                    if (g >= a.n_items) g = -1;
+                } else {
+                    g = -2;
+                }
+            }
+            g = __shfl_sync(0xFFFFFFFFu, g, 0);
+            if (g < 0) break;
+            int s, h, t0, t1, L;
+            ws_item(a, g, s, h, t0, t1, L);
+            if (t0 >= t1 || L < a.w) continue;
+            const int ngrp = (t1 - t0 + 15) / 16;
+            for (int q = lane; q < ngrp; q += 32) {
+                const int t = t0 + 16 * q;
+                int z = -16;
+                const int blk = a.table[(size_t)s * a.table_stride + t / a.b];
+                if (blk >= 0 && blk < a.n_total) z = blk * a.b + t % a.b;
+                else record_error(a.err, ZP_ERR_DEVICE, 0x511);
+                zrow[q] = z;
+            }
+            __syncwarp();
+            if (lane != 0) continue;
+            if (!mbar_wait_bounded(b_empty, (item & 1) ^ 1, a.err, abort_flag, 0x512)) continue;
+            mbar_arrive_expect_tx(b_full, C::B_BYTES);
+            b_armed = item + 1;
+#pragma unroll
+            for (int kh = 0; kh < C::KH; ++kh)
+                tma_load_3d(Bs + kh * C::B_HALF, &qmap, kh * 64, h * G, s * a.w, b_full);
+            const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
+            for (int j = 0; j < ntiles; ++j) {
+                const uint32_t st = fill % kWsTcStages;
+                if (!mbar_wait_bounded(&empty[st], ((fill / kWsTcStages) & 1) ^ 1, a.err, abort_flag, 0x513)) break;
+                mbar_arrive_expect_tx(&full[st], C::STAGE);
+                ++fill;
+                unsigned char *dst = As + st * C::STAGE;
+#pragma unroll
+                for (int q = 0; q < kWsTile / 16; ++q) {
+                    const int gi = j * (kWsTile / 16) + q;
+                    const int z = gi < ngrp ? zrow[gi] : -16;
+#pragma unroll
+                    for (int kh = 0; kh < C::KH; ++kh)
+                        tma_load_3d(dst + kh * C::A_HALF + q * 2048, &kmap, kh * 64, h, z, &full[st]);
+                }
+            }
+            ++item;
+        }
+        if (lane == 0 && *abort_flag) {
+            volatile int never = 0;
+            for (uint32_t f = fill > kWsTcStages ? fill - kWsTcStages : 0; f < fill; ++f)
+                mbar_wait_bounded(&full[f % kWsTcStages], (f / kWsTcStages) & 1, a.err, &never, 0x514);
+            if (b_armed > item) mbar_wait_bounded(b_full, item & 1, a.err, &never, 0x515);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t fill = 0, tile = 0, item = 0;
+            const uint32_t a_addr = smem_u32(As), b_addr = smem_u32(Bs);
+            for (uint32_t k = 0; !*abort_flag; ++k) {
+                const uint32_t slot = k & 3;
+                if (!mbar_wait_bounded(&item_full[slot], (k >> 2) & 1, a.err, abort_flag, 0x516)) break;
+                const int g = item_slot[slot];
+                mbar_arrive(&item_empty[slot]);
+                if (g < 0) break;
+                int s, h, t0, t1, L;
+                ws_item(a, g, s, h, t0, t1, L);
+                if (t0 >= t1 || L < a.w) continue;
+                if (!mbar_wait_bounded(b_full, item & 1, a.err, abort_flag, 0x517)) break;
+                tc_fence_after();
+                const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
+                bool ok_item = true;
+                for (int j = 0; j < ntiles; ++j, ++fill, ++tile) {
+                    const uint32_t st = fill % kWsTcStages, ab = tile & 1;
+                    if (!mbar_wait_bounded(&full[st], (fill / kWsTcStages) & 1, a.err, abort_flag, 0x518) ||
+                        !mbar_wait_bounded(&acc_empty[ab], ((tile >> 1) & 1) ^ 1, a.err, abort_flag, 0x519)) {
+                        ok_item = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < C::KS; ++ks) {
+                        const uint32_t ao = st * C::STAGE + (ks >> 2) * C::A_HALF + (ks & 3) * 32;
+                        const uint32_t bo = (ks >> 2) * C::B_HALF + (ks & 3) * 32;
+                        tc_mma_bf16(tmem + ab * R, sdesc_k_sw128(a_addr + ao), sdesc_k_sw128(b_addr + bo), C::IDESC,
+                                    ks > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&empty[st]);
+                    tc_commit(&acc_full[ab]);
+                }
+                if (!ok_item) break;
+                tc_commit(b_empty);
+                ++item;
+            }
+        }
+    } else {
+        // ---------------- epilogue: thread = token (lane quarter q), columns [half*RH, half*RH + RH)
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const int half = e >> 2;
+        const bool works = half < C::HALVES;
+        const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
+        uint32_t tile = 0, eitem = 0;
+        // every synchronisation here is an mbarrier with a bounded wait, so a
+        // warp that stops after a timeout cannot leave another one waiting
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t slot = k & 3;
+            if (!mbar_wait_bounded(&item_full[slot], (k >> 2) & 1, a.err, abort_flag, 0x51A)) break;
+            const int g = item_slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (g < 0) break;
+            int s, h, t0, t1, L;
+            ws_item(a, g, s, h, t0, t1, L);
+            if (t0 >= t1 || L < a.w) continue;
+            const int last0 = L - a.w;  // window row u sees tokens t <= last0 + u
+            const size_t sh = (size_t)s * a.h_kv + h;
+            float m[RH], l[RH], cst[RH];
+#pragma unroll
+            for (int c = 0; c < RH; ++c) {
+                m[c] = -1e30f;  // pass 1: reference of the sum (finite: x - m is never NaN)
+                l[c] = 0.f;
+                cst[c] = 0.f;
+            }
+            if constexpr (PASS2) {
+                if (works) {
+#pragma unroll
+                    for (int c = 0; c < RH; ++c) cst[c] = a.cst[sh * R + half * RH + c];
+                }
+            }
+            const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
+            bool ok_item = true;
+            for (int j = 0; j < ntiles; ++j, ++tile) {
+                const uint32_t ab = tile & 1;
+                if (!mbar_wait_bounded(&acc_full[ab], (tile >> 1) & 1, a.err, abort_flag, 0x51B)) {
+                    ok_item = false;
+                    break;
+                }
+                tc_fence_after();
+                const int t = t0 + j * kWsTile + 32 * q + lane;  // this thread's token
+                const int tbase = t0 + j * kWsTile;
+                // every token of the tile valid and seen by every window row
+                const bool full_tile = tbase + kWsTile - 1 <= last0 && tbase + kWsTile <= L;
+                float wsum = 0.f;  // pass 2: sum over this half's window rows
+                if (works) {
+#pragma unroll
+                    for (int ch = 0; ch < RH / 16; ++ch) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ab * R + half * RH + ch * 16, v);
+                        if constexpr (!PASS2) {
+                            // l is the sum of 2^(x - ref): rescaled only when x exceeds
+                            // the reference by more than 64 (the first token of an
+                            // item, or a jump of 2^64) -- tested once per 16 columns
+                            float y[16];
+                            float ymax = -INFINITY;
+#pragma unroll
+                            for (int c2 = 0; c2 < 16; ++c2) {
+                                const int c = ch * 16 + c2;
+                                const int u = (half * RH + c) / G;
+                                const bool vis = full_tile || (t < L && t <= last0 + u);
+                                y[c2] = vis ? fmaf(__uint_as_float(v[c2]), a.qscale, -m[c]) : -INFINITY;
+                                ymax = fmaxf(ymax, y[c2]);
+                            }
+                            if (ymax > 64.f) {
+#pragma unroll
+                                for (int c2 = 0; c2 < 16; ++c2) {
+                                    const int c = ch * 16 + c2;
+                                    if (y[c2] > 64.f) {
+                                        const float x = __uint_as_float(v[c2]) * a.qscale;
+                                        l[c] *= ex2_approx(m[c] - x);
+                                        m[c] = x;
+                                        y[c2] = 0.f;
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int c2 = 0; c2 < 16; ++c2) l[ch * 16 + c2] += ex2_approx(y[c2]);
+                        } else {
+#pragma unroll
+                            for (int u2 = 0; u2 < 16 / G; ++u2) {
+                                const int u = (half * RH + ch * 16) / G + u2;
+                                float y = -INFINITY;
+#pragma unroll
+                                for (int jj = 0; jj < G; ++jj) {
+                                    const int c = ch * 16 + u2 * G + jj;
+                                    y = fmaxf(y, fmaf(__uint_as_float(v[u2 * G + jj]), a.qscale, -cst[c]));
+                                }
+                                if (full_tile || (t < L && t <= last0 + u)) wsum += ex2_approx(y);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                if constexpr (PASS2) {
+                    // the two column halves of a lane quarter meet in xch; the
+                    // first half reads before releasing the accumulator, so the
+                    // buffer is free again when the second half reaches it
+                    float *xb = xch + ((tile & 1) * 4 + q) * 32;
+                    if (C::HALVES == 2) {
+                        if (half == 1) {
+                            xb[lane] = wsum;
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xch_full[tile & 1]);
+                        } else if (mbar_wait_bounded(&xch_full[tile & 1], (tile >> 1) & 1, a.err, abort_flag,
+                                                     0x51D)) {
+                            wsum += xb[lane];
+                        }
+                    }
+                    if (half == 0 && t < L) a.out[sh * a.Lmax + t] = wsum / (float)a.w;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            }
+            if constexpr (!PASS2) {
+                // (max, sum) per column: over the warp's 32 tokens, then the 4
+                // lane quarters (red is double-buffered by item; every warp
+                // waits for the buffer's completion, so a buffer is rewritten
+                // only after every reader of its previous use has moved on)
+                float2 *rb = red + (eitem & 1) * 4 * R;
+                if (works) {
+#pragma unroll
+                    for (int c = 0; c < RH; ++c) {
+                        // (reference, sum) pairs combine like (max, sum) pairs;
+                        // a lane that saw nothing has sum 0 and reference -1e30
+                        float M = m[c];
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+                        float Ls = l[c] * exp2f(m[c] - M);
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xFFFFFFFFu, Ls, o);
+                        if (lane == 0) rb[q * R + half * RH + c] = make_float2(M, Ls);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&red_full[eitem & 1]);
+                if (mbar_wait_bounded(&red_full[eitem & 1], (eitem >> 1) & 1, a.err, abort_flag, 0x51E) && et < R) {
+                    float M = -INFINITY, Ls = 0.f;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float2 p = rb[qq * R + et];
+                        if (!(p.y > 0.f)) continue;
+                        if (p.x > M) {
+                            Ls = Ls * exp2f(M - p.x) + p.y;
+                            M = p.x;
+                        } else {
+                            Ls += p.y * exp2f(p.x - M);
+                        }
+                    }
+                    a.part[(sh * a.items_per_sh + (size_t)(t0 / kWsItem)) * R + et] = make_float2(M, Ls);
+                }
+            }
+            ++eitem;
+            if (!ok_item) break;
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 32) {
+        volatile int never = 0;
+        tc_commit(drain);
+        mbar_wait_bounded(drain, 0, a.err, &never, 0x51C);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// merge of the items' (max, sum) per (sequence, kv head, column) -> max + log2(sum)
+__global__ void ws_tc_merge_kernel(const WsTcArgs a, int R) {
+    const int sh = blockIdx.y;
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= R) return;
+    const int L = ws_len(a, sh / a.h_kv);
+    const int nitem = (L + kWsItem - 1) / kWsItem;
     float M = -INFINITY, S = 0.f;
-    for (int c = 0; c < nchunk; ++c) {
-        const float2 ml = a.part[((size_t)s * a.chunks + c) * rows + r];
+    for (int it = 0; it < nitem; ++it) {
+        const float2 ml = a.part[((size_t)sh * a.items_per_sh + it) * R + c];
         if (ml.x == -INFINITY) continue;
         if (ml.x > M) {
             S = S * exp2f(M - ml.x) + ml.y;
@@ -270,7 +498,7 @@ __global__ void ws_merge_kernel(const WsArgs a, int rows) {
             S += ml.y * exp2f(ml.x - M);
         }
     }
-    a.stats[(size_t)s * rows + r] = make_float2(M, S);
+    a.cst[(size_t)sh * R + c] = S > 0.f ? M + log2f(S) : INFINITY;
 }
 
 // ------------------------------------------------------------------ fp32 path
@@ -350,22 +578,43 @@ __global__ void ws_f32_score_kernel(const WsArgs a) {
     a.out[((size_t)s * a.h_kv + kvh) * a.Lmax + t] = acc / (float)a.w;
 }
 
-template <int D, int MT, int G>
-zp_status launch_ws_tc(const WsArgs &a, cudaStream_t st, const DeviceInfo &dev, size_t smem) {
-    auto k1 = ws_tc_kernel<D, MT, G, false>;
-    auto k2 = ws_tc_kernel<D, MT, G, true>;
-    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k1), smem,
-                                        "window score: shared-memory attribute");
+template <int D, int R, int G>
+zp_status launch_ws_tc05(WsTcArgs a, const void *k, const void *q, int h_q, const DeviceInfo &dev, cudaStream_t st) {
+    using Cfg = WsCfg<D, R>;
+    if ((size_t)Cfg::SMEM > (size_t)dev.smem_optin)
+        return fail(ZP_ERR_SHAPE, "window score: needs %d B of shared memory", Cfg::SMEM);
+    CUtensorMap kmap, qmap;
+    {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)a.h_kv, (uint64_t)a.n_total * (uint64_t)a.b};
+        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)a.h_kv * D * 2};
+        const uint32_t box[3] = {64, 1, 16};
+        zp_status rc = encode_tmap_bf16_3d(&kmap, k, dims, strides, box, "window score (keys)");
+        if (rc != ZP_OK) return rc;
+    }
+    {
+        // the window queries [n][w][h_q][d]: a box is 64 elements of the G q
+        // heads of one kv head for the w window rows -> rows in (u, j) order
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)h_q, (uint64_t)a.n * (uint64_t)a.w};
+        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)h_q * D * 2};
+        const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)a.w};
+        zp_status rc = encode_tmap_bf16_3d(&qmap, q, dims, strides, box, "window score (queries)");
+        if (rc != ZP_OK) return rc;
+    }
+    auto k1 = ws_tc05_kernel<D, R, G, false>;
+    auto k2 = ws_tc05_kernel<D, R, G, true>;
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k1), Cfg::SMEM, "window score: shared memory");
     if (rs == ZP_OK)
-        rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k2), smem, "window score: shared-memory attribute");
+        rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k2), Cfg::SMEM, "window score: shared memory");
     if (rs != ZP_OK) return rs;
-    const dim3 grid(a.chunks, a.n);
-    const int threads = (a.h_kv + 1) * 32;
-    k1<<<grid, threads, smem, st>>>(a);
-    const int rows = a.h_kv * MT * 16;
-    ws_merge_kernel<<<dim3((rows + 127) / 128, a.n), 128, 0, st>>>(a, rows);
-    k2<<<grid, threads, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaMemsetAsync(a.counter, 0, 8, st);
+    if (e != cudaSuccess) return cuda_fail(e, "window score: clearing the item counters");
+    const int grid = a.n_items < dev.sm_count ? a.n_items : dev.sm_count;
+    k1<<<grid, kWsThreads, Cfg::SMEM, st>>>(kmap, qmap, a);
+    ws_tc_merge_kernel<<<dim3((R + 127) / 128, a.n * a.h_kv), 128, 0, st>>>(a, R);
+    WsTcArgs a2 = a;
+    a2.counter = a.counter + 1;
+    k2<<<grid, kWsThreads, Cfg::SMEM, st>>>(kmap, qmap, a2);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "window score: launch");
     return ZP_OK;
 }
@@ -379,9 +628,15 @@ extern "C" size_t zp_window_score_workspace_size(const zp_cache_desc *D, int32_t
                                                  int32_t window) {
     if (!D || n < 0 || Lmax < 0 || window <= 0 || D->h_kv <= 0) return 0;
     const int G = D->h_q / D->h_kv;
-    const size_t rows = (size_t)D->h_kv * ((window * G + 15) / 16) * 16;
-    const size_t chunks = ((size_t)(Lmax + 15) / 16 + kPages - 1) / kPages;
-    return align_up((size_t)n * chunks * rows * 8, 256) + align_up((size_t)n * rows * 8, 256) + 256;
+    // fp32 path: final (max, sum) per (sequence, kv head, query row)
+    const size_t f32 = align_up((size_t)n * D->h_kv * window * G * 8, 256);
+    // bf16 path: (max, sum) per (work item, query row), max + log2(sum) per
+    // query row, two item counters
+    const size_t R = (size_t)window * G;
+    const size_t items = ((size_t)Lmax + kWsItem - 1) / kWsItem;
+    const size_t tc = align_up((size_t)n * D->h_kv * items * R * 8, 256) + align_up((size_t)n * D->h_kv * R * 4, 256) +
+                      256;
+    return f32 > tc ? f32 : tc;
 }
 
 extern "C" zp_status zp_window_score(const zp_cache_desc *D, const void *q_window, int32_t window,
@@ -418,11 +673,8 @@ extern "C" zp_status zp_window_score(const zp_cache_desc *D, const void *q_windo
     a.w = window;
     a.Lmax = Lmax;
     a.qscale = (float)(1.4426950408889634 / sqrt((double)d));
-    a.chunks = (int)(((size_t)(Lmax + 15) / 16 + kPages - 1) / kPages);
-    const size_t rows = (size_t)D->h_kv * ((window * G + 15) / 16) * 16;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    a.part = reinterpret_cast<float2 *>(ws);
-    a.stats = reinterpret_cast<float2 *>(ws + align_up((size_t)n * a.chunks * rows * 8, 256));
+    a.stats = reinterpret_cast<float2 *>(ws);  // fp32 path
     a.out = scores_out;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -434,29 +686,52 @@ extern "C" zp_status zp_window_score(const zp_cache_desc *D, const void *q_windo
         if (e != cudaSuccess) return cuda_fail(e, "window score: launch");
         return ok();
     }
-    // bf16: tensor-core passes
-    if (D->h_kv > 8) return fail(ZP_ERR_SHAPE, "window score: h_kv %d > 8", D->h_kv);
+    // bf16: two passes on the tensor cores (tcgen05)
     if (D->block_size % 16) return fail(ZP_ERR_SHAPE, "window score: block size %d not a multiple of 16", D->block_size);
-    if ((window * G) % 16) return fail(ZP_ERR_SHAPE, "window score: window*group %d not a multiple of 16", window * G);
-    const int MT = window * G / 16;
+    const int R = window * G;
+    if (!(R == 16 || R == 32 || R == 64 || R == 128) || !(G == 1 || G == 2 || G == 4 || G == 8) || window > 256)
+        return fail(ZP_ERR_SHAPE, "window score: window*group = %d (bf16 needs 16, 32, 64 or 128)", R);
     if (((uintptr_t)k_cache | (uintptr_t)q_window) % 16)
         return fail(ZP_ERR_INVALID_ARG, "window score: buffers must be 16-byte aligned");
-    const size_t smem = 128 + (size_t)D->h_kv * MT * 16 * (d * 2 + kRowPad) + 128 +
-                        (size_t)kWsStages * 16 * (D->h_kv * d * 2 + kRowPad);
-    if (smem > (size_t)dev.smem_optin) return fail(ZP_ERR_SHAPE, "window score: needs %zu B of shared memory", smem);
-#define ZP_WS(DD, MM, GG)                                               \
-    if (d == DD && MT == MM && G == GG) {                               \
-        rc = launch_ws_tc<DD, MM, GG>(a, st, dev, smem);                \
-        return rc == ZP_OK ? ok() : rc;                                 \
+    WsTcArgs t;
+    t.table = block_table;
+    t.table_stride = table_stride;
+    t.seq_lens = seq_lens;
+    t.n = n;
+    t.h_kv = D->h_kv;
+    t.b = D->block_size;
+    t.n_total = D->n_total_blocks;
+    t.w = window;
+    t.Lmax = Lmax;
+    t.items_per_sh = (Lmax + kWsItem - 1) / kWsItem;
+    const long long n_items = (long long)n * D->h_kv * t.items_per_sh;
+    if (n_items > 0x7FFFFFFF) return fail(ZP_ERR_SHAPE, "window score: too many work items");
+    t.n_items = (int)n_items;
+    t.qscale = a.qscale;
+    t.part = reinterpret_cast<float2 *>(ws);
+    const size_t part_bytes = align_up((size_t)n * D->h_kv * t.items_per_sh * R * 8, 256);
+    t.cst = reinterpret_cast<float *>(ws + part_bytes);
+    t.counter = reinterpret_cast<int *>(ws + part_bytes + align_up((size_t)n * D->h_kv * R * 4, 256));
+    t.out = scores_out;
+    t.err = dev.error_word;
+#define ZP_WS(DD, RR, GG)                                                                        \
+    if (d == DD && R == RR && G == GG) {                                                         \
+        rc = launch_ws_tc05<DD, RR, GG>(t, k_cache, q_window, D->h_q, dev, st);                  \
+        return rc == ZP_OK ? ok() : rc;                                                          \
     }
-    ZP_WS(128, 4, 4)
-    ZP_WS(128, 2, 4)
-    ZP_WS(128, 1, 4)
-    ZP_WS(128, 8, 8)
-    ZP_WS(128, 4, 8)
-    ZP_WS(64, 4, 4)
-    ZP_WS(64, 2, 4)
-    ZP_WS(64, 1, 4)
+    ZP_WS(128, 64, 4)
+    ZP_WS(128, 32, 4)
+    ZP_WS(128, 16, 4)
+    ZP_WS(128, 128, 8)
+    ZP_WS(128, 64, 8)
+    ZP_WS(128, 32, 8)
+    ZP_WS(128, 16, 8)
+    ZP_WS(128, 128, 4)
+    ZP_WS(64, 64, 4)
+    ZP_WS(64, 32, 4)
+    ZP_WS(64, 16, 4)
+    ZP_WS(64, 128, 8)
+    ZP_WS(64, 64, 8)
 #undef ZP_WS
-    return fail(ZP_ERR_SHAPE, "window score: no kernel for d=%d, window*group/16=%d, group=%d", d, MT, G);
+    return fail(ZP_ERR_SHAPE, "window score: no kernel for d=%d, window*group=%d, group=%d", d, R, G);
 }

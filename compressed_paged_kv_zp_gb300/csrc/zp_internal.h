@@ -35,6 +35,13 @@ inline int elem_bytes(int dtype) { return dtype == ZP_BF16 ? 2 : (dtype == ZP_F3
 
 zp_status check_desc(const zp_cache_desc *D);
 
+// Host: a 3-D tiled tensor map of bf16 elements with the 128-byte swizzle
+// (tensor maps for the TMA loads of tcgen05 operands).  dims innermost first;
+// strides (bytes) of dims 1 and 2; box innermost first (box[0] * 2 <= 128).
+// Encoded through the driver entry point (no link against libcuda).
+zp_status encode_tmap_bf16_3d(void *map /* CUtensorMap */, const void *base, const uint64_t dims[3],
+                              const uint64_t strides[2], const uint32_t box[3], const char *what);
+
 // All-pairs key redundancy of one layer (redundancy.cu): rho [n][h_kv][Lmax]
 // receives the row sums of the thresholded cosine matrix of every sequence and
 // kv head (overwritten).  Lengths are clamped to Lcap.

@@ -42,6 +42,8 @@ def _window_case(seed, B, h_q, h_kv, d, b, lens, dtype, w):
     ("bf16", 32, 8, 128, 16, [16, 33, 1000, 1040, 2100]),
     ("bf16", 32, 8, 128, 8, [500, 1500]),
     ("bf16", 32, 8, 128, 4, [64, 1100]),
+    ("bf16", 64, 8, 128, 16, [100, 4200]),   # group of 8: 128 query rows per kv head
+    ("bf16", 16, 4, 64, 8, [3000, 17]),      # head_dim 64
 ])
 def test_window_score_matches_oracle(zp, dtype, h_q, h_kv, d, w, lens):
     c, qw = _window_case(60 + w + len(lens), len(lens), h_q, h_kv, d, 16, lens, dtype, w)
