@@ -31,9 +31,10 @@ near-tie swaps of the keep sets against the oracle, the oracle's CPU
 throughput on a bounded sample (every core, and one core), an end-to-end
 figure measured with pinned host buffers and the host<->device copies inside
 the timed region, and two sub-results: the engine's multi-step loop on the
-high-concurrency workload (512 sequences x 2048 steps) and the long-prefill
+high-concurrency workload (512 sequences x 2048 steps), the long-prefill
 compression (16 x 32k tokens: window score, scores, top-k, compaction, and
-the all-pairs redundancy).  Inputs (~0.8 GB of K/V per layer) are larger than
+the all-pairs redundancy) and the prefix-shared 36-layer workload (256
+sequences, asynchronous compression).  Inputs (~0.8 GB of K/V per layer) are larger than
 the 129 MB L2, so no flush is needed between steps.
 """
 from __future__ import annotations
@@ -709,6 +710,76 @@ def long_prefill_measure(dev, peak, reps=10, all_pairs_reps=2):
     return out
 
 
+PREFIX_SHARED = "prefix_shared_36layer_256seq"
+
+
+def prefix_shared_measure(dev, steps=32, warmup=3):
+    """The prefix-shared workload at its stated size: 256 sequences sharing a
+    1024-token prefix (64 blocks, plus the prefix cache's reference) with
+    private tails uniform in [0, 8192], 36 layers of 32q/8kv/128 bf16, b 16,
+    N_max 64 (1008 kept), asynchronous compression on the side stream, 8
+    layers per compression call, compaction into fresh target blocks.  K and
+    V: ~194 GB drawn on the device layer by layer.  Returns the decoded
+    sequence-steps (all 36 layers) per second and the decode calls'
+    algorithmic GB/s over the timed steps."""
+    from compressed_paged_kv_zp_gb300.engine import DecodeLoop
+    B, h_q, h_kv, d, b, N_max, layers = 256, 32, 8, 128, 16, 64, 36
+    g = torch.Generator().manual_seed(1005)
+    lens0 = (1024 + torch.randint(0, 8193, (B,), generator=g).numpy()).astype(np.int32)
+    P = 1024 // b
+    stride = (int(lens0.max()) + steps + warmup + b - 1) // b + 2
+    own = (lens0 + b - 1) // b - P
+    n_total = P + int(own.sum()) + B * (N_max + 2) + 64
+    table = np.full((B, stride), -1, dtype=np.int32)
+    perm = torch.randperm(n_total, generator=g).numpy().astype(np.int32)
+    table[:, :P] = perm[:P]
+    cur = P
+    for s in range(B):
+        table[s, P:P + own[s]] = perm[cur:cur + own[s]]
+        cur += own[s]
+    loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=layers, dtype=torch.bfloat16, window=b,
+                      async_compress=True, layer_stride=8, device=dev)
+    loop.add_sequences(lens0, tables=table)
+    loop.pool.incref(table[0, :P].tolist())  # the prefix cache's own reference
+    gd = torch.Generator(device=dev).manual_seed(1006)
+    for l in range(layers):
+        loop.K[l].copy_(torch.randn(loop.K[l].shape, generator=gd, device=dev))
+        loop.V[l].copy_(torch.randn(loop.V[l].shape, generator=gd, device=dev))
+    q = torch.randn((layers, B, h_q, d), generator=gd, device=dev).to(torch.bfloat16)
+    kn = torch.randn((layers, B, h_kv, d), generator=gd, device=dev).to(torch.bfloat16)
+    vn = torch.randn((layers, B, h_kv, d), generator=gd, device=dev).to(torch.bfloat16)
+    for _ in range(warmup):
+        loop.step(q, kn, vn)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    decoded, dbytes, comps0 = 0, 0, loop.compressions
+    start.record()
+    for _ in range(steps):
+        act = loop.active.copy()
+        L = loop.lens[act].astype(np.int64) + 1
+        decoded += int(act.sum())
+        dbytes += layers * int((2 * L * h_kv * d * 2 + 2 * h_q * d * 2 + 8 * L * h_kv).sum())
+        loop.step(q, kn, vn)
+    loop.drain()
+    stop.record()
+    torch.cuda.synchronize()
+    from compressed_paged_kv_zp_gb300 import zp_device_status
+    code, _ = zp_device_status(clear=True)
+    if code:
+        raise RuntimeError("device status %d in the prefix-shared workload" % code)
+    ms = start.elapsed_time(stop)
+    res = {"workload": PREFIX_SHARED, "seqs": B, "layers": layers, "heads": "32q/8kv", "head_dim": d, "block": b,
+           "max_blocks_per_seq": N_max, "kept_tokens": (N_max - 1) * b, "prefix_tokens": 1024,
+           "private_tokens": "uniform 0-8192", "steps": steps, "compressions": loop.compressions - comps0,
+           "seq_steps_per_s": decoded / (ms / 1e3), "layer_seq_steps_per_s": layers * decoded / (ms / 1e3),
+           "ms_per_step": ms / steps, "decode_algorithmic_GBs": dbytes / (ms / 1e3) / 1e9,
+           "launch": "engine loop (36 layers, append + decode per layer), asynchronous compression of 8 layers "
+                     "per call, direct calls"}
+    del loop, q, kn, vn
+    torch.cuda.empty_cache()
+    return res
+
+
 ALL_PAIRS = "all_pairs_redundancy_4x32k"
 
 
@@ -1025,6 +1096,12 @@ def main():
                                      decode_frac=edbytes / (ems / 1e3) / 1e9 / peak,
                                      launch="engine loop, asynchronous compression, direct calls")}
         sub[LONG_PREFILL] = long_prefill_measure(dev, peak)
+        torch.cuda.empty_cache()
+        if torch.cuda.mem_get_info(dev)[0] > 230e9:  # K and V of the 256 sequences take ~194 GB
+            sub[PREFIX_SHARED] = prefix_shared_measure(dev)
+            sub[PREFIX_SHARED]["decode_frac"] = sub[PREFIX_SHARED]["decode_algorithmic_GBs"] / peak
+        else:
+            sub[PREFIX_SHARED] = {"skipped": "less than 230 GB of free device memory"}
         line["sub_results"] = sub
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # bounded samples: sequence-steps for about 10 s of CPU time each, on
