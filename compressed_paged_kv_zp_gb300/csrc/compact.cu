@@ -135,16 +135,17 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
 // the same index in both (the target rule): the move is correct in place.
 // (Many small bulk copies were measured slower: the copy engine keeps few
 // requests in flight per SM.)
-constexpr int kVChunk = 64;
-constexpr int kVThreads = 256;
-constexpr int kVPerThread = 8;  // 16-byte registers per thread and chunk (row pieces up to 256 B)
+constexpr int kVChunk = 256;
+constexpr int kVThreads = 1024;  // rounds of 256 ranks for 256-byte row pieces (64 ranks with 256 threads
+                                 // took 4x the load-then-store round trips, each one a memory latency)
+constexpr int kVPerThread = 8;   // 16-byte registers per thread and chunk (row pieces up to 256 B)
 
 // dynamic shared memory: pos[k], src block[k] (ints), F values[k], target blocks[ceil(k/b)]
 __host__ __device__ inline size_t compact_meta_smem(int k, int b) {
     return (size_t)k * 12 + (size_t)((k + b - 1) / b) * 4 + 16;
 }
 
-__global__ void __launch_bounds__(kVThreads) compact_vec_kernel(const CompactArgs a) {
+__global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const CompactArgs a) {
     extern __shared__ __align__(16) unsigned char csm[];
     __shared__ int s_L;
     const int kvh = blockIdx.x;
