@@ -102,7 +102,8 @@ std::map<std::pair<const void *, int>, size_t> g_smem_set;  // (kernel, device) 
 }  // namespace
 
 zp_status set_max_dynamic_smem(const void *func, size_t bytes, const char *what) {
-    if (bytes <= 48 * 1024) return ZP_OK;
+    // (set even below 48 KB: that default limit covers a kernel's static and
+    // dynamic shared memory together)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, what);

@@ -24,8 +24,8 @@ struct DeviceInfo {
 zp_status device_info(DeviceInfo *out);
 
 // Host: raise the dynamic shared-memory limit of kernel `func` on the current
-// device to at least `bytes` (no call below the 48 KB default, one call per
-// kernel, device and larger size; safe from several host threads).  A failure
+// device to at least `bytes` (one call per kernel, device and larger size;
+// safe from several host threads).  A failure
 // returns ZP_ERR_CUDA with `what` in the message.
 zp_status set_max_dynamic_smem(const void *func, size_t bytes, const char *what);
 
