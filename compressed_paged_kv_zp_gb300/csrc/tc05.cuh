@@ -142,6 +142,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *t
         : "memory");
 }
 
+// The same load with an L2 cache-policy hint (createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst_smem, const CUtensorMap *tmap, int c0, int c1, int c2,
+                                                 uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

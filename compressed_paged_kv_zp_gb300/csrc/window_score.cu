@@ -45,25 +45,30 @@ __device__ __forceinline__ int seq_len(const WsArgs &a, int s) {
 }
 
 // ------------------------------------------------------------------ bf16 path
-// Per (sequence, kv head) the contraction is D[t][c] = k_t . q_c for the
-// R = w*g query rows c = u*g + j of the head (window row u, q head j of the
-// group) against every token t: 128 tokens are the M = 128 operand of one
+// Per (sequence, kv head) -- a "pair" -- the contraction is D[t][c] = k_t . q_c
+// for the R = w*g query rows c = u*g + j of the head (window row u, q head j of
+// the group) against every token t: 128 tokens are the M = 128 operand of one
 // tcgen05.mma (A: the head's keys, by TMA from the paged cache with the
 // 128-byte swizzle), the R query rows the N operand (B: one TMA box of the
 // window queries, rows landing in (u, j) order); the accumulator, R fp32
-// columns per token, sits in tensor memory, double-buffered.  A persistent
-// kernel per pass takes work items (sequence, kv head, 2048 tokens) from a
-// grid-wide counter; a producer warp (TMA), an MMA thread and eight epilogue
-// warps (two per TMEM lane quarter, each half of the columns).  An epilogue
-// thread owns one token:
-//   pass 1: per column an online (max, sum of exp) over the thread's tokens
-//           -- one exp2 per element: e = 2^-|x - m| either rescales the sum
-//           or is added to it -- reduced over the warp and the four lane
-//           quarters at the end of the item into a partial per (item, column);
-//   merge:  the partials of a (sequence, kv head) -> c = max + log2(sum) per column;
-//   pass 2: per window row u the max over the group of x - c (the softmax is
-//           monotonic in it), one exp2 per (token, u), summed over u and
-//           divided by w; the two column halves meet in shared memory.
+// columns per token, sits in tensor memory, double-buffered.  One persistent
+// kernel runs both passes.  Work items (kind, pair, 2048-token chunk) come
+// from a grid-wide counter in an order where a pair's pass-2 items follow its
+// pass-1 items by `lag` pairs: by then the pass-1 items are done and the
+// pair's keys (8.4 MB for the Qwen3-8B shape at 32k tokens) are still in L2
+// for the second read.  A producer warp (TMA), an MMA thread and eight
+// epilogue warps (two per TMEM lane quarter, each half of the columns); an
+// epilogue thread owns one token:
+//   pass 1: per column a sum of 2^(x - ref) over the thread's tokens (one
+//           exponential per element, the reference raised only when x exceeds
+//           it by more than 64), reduced over the warp and the four lane
+//           quarters into a partial (max, sum) per (item, column); the last
+//           item of a pair to finish a column merges that column's partials
+//           into c = max + log2(sum) and counts it ready;
+//   pass 2: once all R columns of the pair are ready (bounded wait), per
+//           window row u the max over the group of x - c (the probability is
+//           monotonic in it), one exponential per (token, u), summed over u
+//           and divided by w; the two column halves meet in shared memory.
 // x is the logit in log2 units; the causal mask hides token t from window row
 // u when t > L - w + u.
 constexpr int kWsTile = 128;     // tokens per MMA tile
@@ -97,12 +102,15 @@ struct WsTcArgs {
     int table_stride;
     const int32_t *seq_lens;
     int n, h_kv, b, n_total, w, Lmax;
-    int items_per_sh, n_items;
-    float qscale;   // log2(e) / sqrt(d)
-    float2 *part;   // [n][h_kv][items_per_sh][R] (max, sum) per item (pass 1)
-    float *cst;     // [n][h_kv][R] max + log2(sum) per column (pass 2)
-    float *out;     // [n][h_kv][Lmax]
-    int *counter;   // work items taken (zero on entry)
+    int items_per_sh;  // chunks per pair (for Lmax)
+    int pairs, lag, n_items;
+    float qscale;      // log2(e) / sqrt(d)
+    float2 *part;      // [pairs][items_per_sh][R] (max, sum) per item (pass 1)
+    float *cst;        // [pairs][R] max + log2(sum) per column (pass 2)
+    int *done_col;     // [pairs][R] pass-1 items finished per column (zero on entry)
+    int *ready;        // [pairs] columns merged (zero on entry)
+    float *out;        // [n][h_kv][Lmax]
+    int *counter;      // work items taken (zero on entry)
     unsigned *err;
 };
 
@@ -122,21 +130,58 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Work item g: (sequence, chunk, kv head) with the kv head fastest, so that
-// the CTAs at work read the kv heads' pieces of the same token rows (a row
-// holds every kv head) at about the same time.
-__device__ __forceinline__ void ws_item(const WsTcArgs &a, int g, int &s, int &h, int &t0, int &t1, int &L) {
-    const int per_seq = a.items_per_sh * a.h_kv;
-    s = g / per_seq;
-    const int r = g - s * per_seq;
-    const int chunk = r / a.h_kv;
-    h = r - chunk * a.h_kv;
-    L = ws_len(a, s);
-    t0 = chunk * kWsItem;
-    t1 = min(L, t0 + kWsItem);
+// Work item g -> (pass2, pair, chunk): the first lag*C items are pass 1 of
+// pairs 0..lag-1; then per pair j >= lag its C pass-1 items followed by the C
+// pass-2 items of pair j - lag; the last lag*C items are pass 2 of the last
+// lag pairs (C = chunks per pair).
+struct WsItem {
+    int pass2, pair, s, h, t0, t1, L;
+};
+
+__device__ __forceinline__ WsItem ws_item(const WsTcArgs &a, int g) {
+    const int C = a.items_per_sh, P = a.pairs, lag = a.lag;
+    WsItem it;
+    int chunk;
+    if (g < lag * C) {
+        it.pass2 = 0;
+        it.pair = g / C;
+        chunk = g - it.pair * C;
+    } else {
+        const int g1 = g - lag * C;
+        if (g1 < (P - lag) * 2 * C) {
+            const int j = lag + g1 / (2 * C);
+            const int r = g1 - (j - lag) * 2 * C;
+            it.pass2 = r >= C;
+            it.pair = it.pass2 ? j - lag : j;
+            chunk = it.pass2 ? r - C : r;
+        } else {
+            const int g2 = g1 - (P - lag) * 2 * C;
+            it.pass2 = 1;
+            it.pair = P - lag + g2 / C;
+            chunk = g2 - (g2 / C) * C;
+        }
+    }
+    it.s = it.pair / a.h_kv;
+    it.h = it.pair - it.s * a.h_kv;
+    it.L = ws_len(a, it.s);
+    it.t0 = chunk * kWsItem;
+    it.t1 = min(it.L, it.t0 + kWsItem);
+    return it;
 }
 
-template <int D, int R, int G, bool PASS2>
+__device__ __forceinline__ bool ws_item_empty(const WsTcArgs &a, const WsItem &it) {
+    return it.t0 >= it.t1 || it.L < a.w;
+}
+
+// The RH columns of one epilogue warp in one TMEM load (RH = 16, 32 or 64).
+template <int RH>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[RH]) {
+    if constexpr (RH == 16) tmem_ld16(taddr, v);
+    else if constexpr (RH == 32) tmem_ld32(taddr, v);
+    else tmem_ld64(taddr, v);
+}
+
+template <int D, int R, int G>
 __global__ void __launch_bounds__(kWsThreads, 1)
     ws_tc05_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                    const WsTcArgs a) {
@@ -200,8 +245,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer: items, the head's query rows (B), token tiles (A)
+        // ---------------- producer: items, the head's query rows (B), token tiles (A);
+        // pass-1 keys are kept in L2 for the pass-2 read, pass-2 keys are not needed after
         uint32_t fill = 0, item = 0, b_armed = 0;
+        const uint64_t keep_pol = l2_evict_last_policy(), drop_pol = l2_evict_first_policy();
         if (lane == 0) {
             prefetch_tensormap(&kmap);
             prefetch_tensormap(&qmap);
@@ -222,14 +269,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
             g = __shfl_sync(0xFFFFFFFFu, g, 0);
             if (g < 0) break;
-            int s, h, t0, t1, L;
-            ws_item(a, g, s, h, t0, t1, L);
-            if (t0 >= t1 || L < a.w) continue;
-            const int ngrp = (t1 - t0 + 15) / 16;
+            const WsItem it = ws_item(a, g);
+            if (ws_item_empty(a, it)) continue;
+            const int ngrp = (it.t1 - it.t0 + 15) / 16;
             for (int q = lane; q < ngrp; q += 32) {
-                const int t = t0 + 16 * q;
+                const int t = it.t0 + 16 * q;
                 int z = -16;
-                const int blk = a.table[(size_t)s * a.table_stride + t / a.b];
+                const int blk = a.table[(size_t)it.s * a.table_stride + t / a.b];
                 if (blk >= 0 && blk < a.n_total) z = blk * a.b + t % a.b;
                 else record_error(a.err, ZP_ERR_DEVICE, 0x511);
                 zrow[q] = z;
@@ -241,8 +287,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             b_armed = item + 1;
 #pragma unroll
             for (int kh = 0; kh < C::KH; ++kh)
-                tma_load_3d(Bs + kh * C::B_HALF, &qmap, kh * 64, h * G, s * a.w, b_full);
-            const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
+                tma_load_3d(Bs + kh * C::B_HALF, &qmap, kh * 64, it.h * G, it.s * a.w, b_full);
+            const uint64_t pol = it.pass2 ? drop_pol : keep_pol;
+            const int ntiles = (it.t1 - it.t0 + kWsTile - 1) / kWsTile;
             for (int j = 0; j < ntiles; ++j) {
                 const uint32_t st = fill % kWsTcStages;
                 if (!mbar_wait_bounded(&empty[st], ((fill / kWsTcStages) & 1) ^ 1, a.err, abort_flag, 0x513)) break;
@@ -255,7 +302,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const int z = gi < ngrp ? zrow[gi] : -16;
 #pragma unroll
                     for (int kh = 0; kh < C::KH; ++kh)
-                        tma_load_3d(dst + kh * C::A_HALF + q * 2048, &kmap, kh * 64, h, z, &full[st]);
+                        tma_load_3d_hint(dst + kh * C::A_HALF + q * 2048, &kmap, kh * 64, it.h, z, &full[st], pol);
                 }
             }
             ++item;
@@ -277,12 +324,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const int g = item_slot[slot];
                 mbar_arrive(&item_empty[slot]);
                 if (g < 0) break;
-                int s, h, t0, t1, L;
-                ws_item(a, g, s, h, t0, t1, L);
-                if (t0 >= t1 || L < a.w) continue;
+                const WsItem it = ws_item(a, g);
+                if (ws_item_empty(a, it)) continue;
                 if (!mbar_wait_bounded(b_full, item & 1, a.err, abort_flag, 0x517)) break;
                 tc_fence_after();
-                const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
+                const int ntiles = (it.t1 - it.t0 + kWsTile - 1) / kWsTile;
                 bool ok_item = true;
                 for (int j = 0; j < ntiles; ++j, ++fill, ++tile) {
                     const uint32_t st = fill % kWsTcStages, ab = tile & 1;
@@ -314,9 +360,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int half = e >> 2;
         const bool works = half < C::HALVES;
         const int et = threadIdx.x - 64;  // 0..255 over the epilogue warps
-        uint32_t tile = 0, eitem = 0;
-        // every synchronisation here is an mbarrier with a bounded wait, so a
-        // warp that stops after a timeout cannot leave another one waiting
+        uint32_t tile = 0, eitem = 0, xtile = 0;  // all tiles, pass-1 items, pass-2 tiles
+        // every synchronisation here is an mbarrier or a flag with a bounded
+        // wait, so a warp that stops after a timeout cannot leave another
+        // waiting for ever
         for (uint32_t k = 0;; ++k) {
             const uint32_t slot = k & 3;
             if (!mbar_wait_bounded(&item_full[slot], (k >> 2) & 1, a.err, abort_flag, 0x51A)) break;
@@ -324,22 +371,39 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             if (g < 0) break;
-            int s, h, t0, t1, L;
-            ws_item(a, g, s, h, t0, t1, L);
-            if (t0 >= t1 || L < a.w) continue;
+            const WsItem it = ws_item(a, g);
+            if (ws_item_empty(a, it)) continue;
+            const int t0 = it.t0, t1 = it.t1, L = it.L;
             const int last0 = L - a.w;  // window row u sees tokens t <= last0 + u
-            const size_t sh = (size_t)s * a.h_kv + h;
-            float m[RH], l[RH], cst[RH];
+            const size_t pr = (size_t)it.pair;
+            // pass 1: m = reference and l = sum per column; pass 2: m = the column's c
+            float m[RH], l[RH];
 #pragma unroll
             for (int c = 0; c < RH; ++c) {
-                m[c] = -1e30f;  // pass 1: reference of the sum (finite: x - m is never NaN)
+                m[c] = -1e30f;  // finite: x - m is never NaN
                 l[c] = 0.f;
-                cst[c] = 0.f;
             }
-            if constexpr (PASS2) {
+            if (it.pass2) {
+                // the pair's R columns merged by the last pass-1 items (bounded wait)
+                if (lane == 0) {
+                    const volatile int *rd = a.ready + pr;
+                    if (*rd < R) {
+                        const unsigned long long t_0 = global_ns();
+                        while (*rd < R) {
+                            if (global_ns() - t_0 > kWaitLimitNs) {
+                                record_error(a.err, ZP_ERR_TIMEOUT, 0x51F);
+                                *abort_flag = 1;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    __threadfence();
+                }
+                __syncwarp();
                 if (works) {
 #pragma unroll
-                    for (int c = 0; c < RH; ++c) cst[c] = a.cst[sh * R + half * RH + c];
+                    for (int c = 0; c < RH; ++c) m[c] = __ldcg(a.cst + pr * R + half * RH + c);
                 }
             }
             const int ntiles = (t1 - t0 + kWsTile - 1) / kWsTile;
@@ -357,11 +421,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const bool full_tile = tbase + kWsTile - 1 <= last0 && tbase + kWsTile <= L;
                 float wsum = 0.f;  // pass 2: sum over this half's window rows
                 if (works) {
+                    uint32_t vall[RH];  // the warp's columns, one load
+                    tmem_ld_cols<RH>(tmem + ((uint32_t)(32 * q) << 16) + ab * R + half * RH, vall);
 #pragma unroll
                     for (int ch = 0; ch < RH / 16; ++ch) {
-                        uint32_t v[16];
-                        tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + ab * R + half * RH + ch * 16, v);
-                        if constexpr (!PASS2) {
+                        const uint32_t *v = vall + ch * 16;
+                        if (!it.pass2) {
                             // l is the sum of 2^(x - ref): rescaled only when x exceeds
                             // the reference by more than 64 (the first token of an
                             // item, or a jump of 2^64) -- tested once per 16 columns
@@ -393,43 +458,45 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
                             for (int u2 = 0; u2 < 16 / G; ++u2) {
                                 const int u = (half * RH + ch * 16) / G + u2;
-                                float y = -INFINITY;
+                                float yy = -INFINITY;
 #pragma unroll
                                 for (int jj = 0; jj < G; ++jj) {
                                     const int c = ch * 16 + u2 * G + jj;
-                                    y = fmaxf(y, fmaf(__uint_as_float(v[u2 * G + jj]), a.qscale, -cst[c]));
+                                    yy = fmaxf(yy, fmaf(__uint_as_float(v[u2 * G + jj]), a.qscale, -m[c]));
                                 }
-                                if (full_tile || (t < L && t <= last0 + u)) wsum += ex2_approx(y);
+                                if (full_tile || (t < L && t <= last0 + u)) wsum += ex2_approx(yy);
                             }
                         }
                     }
                 }
                 tc_fence_before();
-                if constexpr (PASS2) {
+                if (it.pass2) {
                     // the two column halves of a lane quarter meet in xch; the
                     // first half reads before releasing the accumulator, so the
                     // buffer is free again when the second half reaches it
-                    float *xb = xch + ((tile & 1) * 4 + q) * 32;
+                    float *xb = xch + ((xtile & 1) * 4 + q) * 32;
                     if (C::HALVES == 2) {
                         if (half == 1) {
                             xb[lane] = wsum;
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&xch_full[tile & 1]);
-                        } else if (mbar_wait_bounded(&xch_full[tile & 1], (tile >> 1) & 1, a.err, abort_flag,
+                            if (lane == 0) mbar_arrive(&xch_full[xtile & 1]);
+                        } else if (mbar_wait_bounded(&xch_full[xtile & 1], (xtile >> 1) & 1, a.err, abort_flag,
                                                      0x51D)) {
                             wsum += xb[lane];
                         }
                     }
-                    if (half == 0 && t < L) a.out[sh * a.Lmax + t] = wsum / (float)a.w;
+                    if (half == 0 && t < L) a.out[((size_t)it.s * a.h_kv + it.h) * a.Lmax + t] = wsum / (float)a.w;
+                    ++xtile;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
             }
-            if constexpr (!PASS2) {
+            if (!it.pass2) {
                 // (max, sum) per column: over the warp's 32 tokens, then the 4
-                // lane quarters (red is double-buffered by item; every warp
-                // waits for the buffer's completion, so a buffer is rewritten
-                // only after every reader of its previous use has moved on)
+                // lane quarters (red is double-buffered by pass-1 item; every
+                // warp waits for the buffer's completion, so a buffer is
+                // rewritten only after every reader of its previous use has
+                // moved on)
                 float2 *rb = red + (eitem & 1) * 4 * R;
                 if (works) {
 #pragma unroll
@@ -460,10 +527,32 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                             Ls += p.y * exp2f(p.x - M);
                         }
                     }
-                    a.part[(sh * a.items_per_sh + (size_t)(t0 / kWsItem)) * R + et] = make_float2(M, Ls);
+                    a.part[(pr * a.items_per_sh + (size_t)(t0 / kWsItem)) * R + et] = make_float2(M, Ls);
+                    // the last item of the pair to finish this column merges it
+                    // (fence, then count: the partials written before each count
+                    // are visible to the thread that sees the last count)
+                    __threadfence();
+                    const int nitem = (L + kWsItem - 1) / kWsItem;
+                    if (atomicAdd(a.done_col + pr * R + et, 1) == nitem - 1) {
+                        __threadfence();
+                        float MM = -INFINITY, SS = 0.f;
+                        for (int i2 = 0; i2 < nitem; ++i2) {
+                            const float2 ml = __ldcg(a.part + (pr * a.items_per_sh + i2) * R + et);
+                            if (!(ml.y > 0.f)) continue;
+                            if (ml.x > MM) {
+                                SS = SS * exp2f(MM - ml.x) + ml.y;
+                                MM = ml.x;
+                            } else {
+                                SS += ml.y * exp2f(ml.x - MM);
+                            }
+                        }
+                        a.cst[pr * R + et] = SS > 0.f ? MM + log2f(SS) : INFINITY;
+                        __threadfence();
+                        atomicAdd(a.ready + pr, 1);
+                    }
                 }
+                ++eitem;
             }
-            ++eitem;
             if (!ok_item) break;
         }
     }
@@ -478,27 +567,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
-}
-
-// merge of the items' (max, sum) per (sequence, kv head, column) -> max + log2(sum)
-__global__ void ws_tc_merge_kernel(const WsTcArgs a, int R) {
-    const int sh = blockIdx.y;
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= R) return;
-    const int L = ws_len(a, sh / a.h_kv);
-    const int nitem = (L + kWsItem - 1) / kWsItem;
-    float M = -INFINITY, S = 0.f;
-    for (int it = 0; it < nitem; ++it) {
-        const float2 ml = a.part[((size_t)sh * a.items_per_sh + it) * R + c];
-        if (ml.x == -INFINITY) continue;
-        if (ml.x > M) {
-            S = S * exp2f(M - ml.x) + ml.y;
-            M = ml.x;
-        } else {
-            S += ml.y * exp2f(ml.x - M);
-        }
-    }
-    a.cst[(size_t)sh * R + c] = S > 0.f ? M + log2f(S) : INFINITY;
 }
 
 // ------------------------------------------------------------------ fp32 path
@@ -600,20 +668,21 @@ zp_status launch_ws_tc05(WsTcArgs a, const void *k, const void *q, int h_q, cons
         zp_status rc = encode_tmap_bf16_3d(&qmap, q, dims, strides, box, "window score (queries)");
         if (rc != ZP_OK) return rc;
     }
-    auto k1 = ws_tc05_kernel<D, R, G, false>;
-    auto k2 = ws_tc05_kernel<D, R, G, true>;
-    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k1), Cfg::SMEM, "window score: shared memory");
-    if (rs == ZP_OK)
-        rs = set_max_dynamic_smem(reinterpret_cast<const void *>(k2), Cfg::SMEM, "window score: shared memory");
+    auto kern = ws_tc05_kernel<D, R, G>;
+    zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), Cfg::SMEM, "window score: shared memory");
     if (rs != ZP_OK) return rs;
-    cudaError_t e = cudaMemsetAsync(a.counter, 0, 8, st);
-    if (e != cudaSuccess) return cuda_fail(e, "window score: clearing the item counters");
     const int grid = a.n_items < dev.sm_count ? a.n_items : dev.sm_count;
-    k1<<<grid, kWsThreads, Cfg::SMEM, st>>>(kmap, qmap, a);
-    ws_tc_merge_kernel<<<dim3((R + 127) / 128, a.n * a.h_kv), 128, 0, st>>>(a, R);
-    WsTcArgs a2 = a;
-    a2.counter = a.counter + 1;
-    k2<<<grid, kWsThreads, Cfg::SMEM, st>>>(kmap, qmap, a2);
+    // pass 2 of a pair follows its pass 1 by about the items in flight (one
+    // or two per CTA, 2 * items_per_sh per pair) plus two pairs: late enough
+    // that the pass-1 items are mostly done, early enough that the keys of the
+    // pairs in between (lag * 8.4 MB at 32k tokens) stay in L2
+    int lag = (grid + 2 * a.items_per_sh - 1) / (2 * a.items_per_sh) + 2;
+    if (lag < 1) lag = 1;
+    if (lag > a.pairs) lag = a.pairs;
+    a.lag = lag;
+    cudaError_t e = cudaMemsetAsync(a.done_col, 0, ((size_t)a.pairs * (R + 1) + 1) * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "window score: clearing the counters");
+    kern<<<grid, kWsThreads, Cfg::SMEM, st>>>(kmap, qmap, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "window score: launch");
     return ZP_OK;
@@ -630,12 +699,13 @@ extern "C" size_t zp_window_score_workspace_size(const zp_cache_desc *D, int32_t
     const int G = D->h_q / D->h_kv;
     // fp32 path: final (max, sum) per (sequence, kv head, query row)
     const size_t f32 = align_up((size_t)n * D->h_kv * window * G * 8, 256);
-    // bf16 path: (max, sum) per (work item, query row), max + log2(sum) per
-    // query row, two item counters
+    // bf16 path: (max, sum) per (pass-1 item, query row), max + log2(sum) per
+    // query row, per-column and per-pair counters, the item counter
     const size_t R = (size_t)window * G;
     const size_t items = ((size_t)Lmax + kWsItem - 1) / kWsItem;
-    const size_t tc = align_up((size_t)n * D->h_kv * items * R * 8, 256) + align_up((size_t)n * D->h_kv * R * 4, 256) +
-                      256;
+    const size_t pairs = (size_t)n * D->h_kv;
+    const size_t tc = align_up(pairs * items * R * 8, 256) + align_up(pairs * R * 4, 256) +
+                      align_up((pairs * (R + 1) + 1) * 4, 256);
     return f32 > tc ? f32 : tc;
 }
 
@@ -704,14 +774,19 @@ extern "C" zp_status zp_window_score(const zp_cache_desc *D, const void *q_windo
     t.w = window;
     t.Lmax = Lmax;
     t.items_per_sh = (Lmax + kWsItem - 1) / kWsItem;
-    const long long n_items = (long long)n * D->h_kv * t.items_per_sh;
+    t.pairs = n * D->h_kv;
+    const long long n_items = 2LL * t.pairs * t.items_per_sh;  // pass 1 and pass 2
     if (n_items > 0x7FFFFFFF) return fail(ZP_ERR_SHAPE, "window score: too many work items");
     t.n_items = (int)n_items;
+    t.lag = 1;  // set by the launcher
     t.qscale = a.qscale;
     t.part = reinterpret_cast<float2 *>(ws);
-    const size_t part_bytes = align_up((size_t)n * D->h_kv * t.items_per_sh * R * 8, 256);
+    const size_t part_bytes = align_up((size_t)t.pairs * t.items_per_sh * R * 8, 256);
     t.cst = reinterpret_cast<float *>(ws + part_bytes);
-    t.counter = reinterpret_cast<int *>(ws + part_bytes + align_up((size_t)n * D->h_kv * R * 4, 256));
+    // counters, one run that the launcher zeroes: done_col [pairs][R], ready [pairs], the item counter
+    t.done_col = reinterpret_cast<int *>(ws + part_bytes + align_up((size_t)t.pairs * R * 4, 256));
+    t.ready = t.done_col + (size_t)t.pairs * R;
+    t.counter = t.ready + t.pairs;
     t.out = scores_out;
     t.err = dev.error_word;
 #define ZP_WS(DD, RR, GG)                                                                        \
