@@ -10,10 +10,16 @@ One step = the whole hot path over that batch:
   2. zp_paged_decode_attn  decode attention of all 64 sequences fused with the
                            window-score accumulation (w = b = 16, so every
                            decode step is an observation-window step);
+     The decode also forms the lightning redundancy row sums of the
+     sequences about to be compressed (zp_paged_decode_attn_rho) from the key
+     tiles it already holds;
   3. compression of the sequences whose trigger holds at their length
-     (L % b == 0, L >= N_max * b): host planner, then zp_compress_layers:
-     scores (global score, first-compression pooling, lightning redundancy,
-     eq. 4, window), keep sets and the move into the planned target blocks.
+     (L % b == 0, L >= N_max * b): host planner, then zp_compress_layers_rho:
+     scores (global score, first-compression pooling, the decode's
+     redundancy row sums, eq. 4, window), keep sets and the move into the
+     planned target blocks, in one kernel.  --no-rho runs the plain calls
+     (the compression then reads the keys again and forms the row sums in a
+     kernel of its own).
 The batch is stationary: lengths and tables are not advanced between steps,
 so every timed step does identical work (the compaction rewrites the same
 target slots each time).
@@ -181,7 +187,7 @@ class ClockSampler:
 class Workload:
     """Device buffers and the step of the decode + compression hot path."""
 
-    def __init__(self, name: str, seed_offset: int, dev: torch.device):
+    def __init__(self, name: str, seed_offset: int, dev: torch.device, use_rho: bool = True):
         import compressed_paged_kv_zp_gb300 as zp
         self.zp = zp
         B, h_q, h_kv, d, b, N_max, lr, dtype, seed = WORKLOADS[name]
@@ -247,6 +253,14 @@ class Workload:
             plan = self.pool.plan_compaction_batch(self.c_tables_np, self.c_nblocks_np, N_max)
             self.plan_out = plan
             self.c_targets = torch.from_numpy(plan["targets"].copy()).to(dev)
+        # the lightning row sums of the triggered sequences, formed by the
+        # decode: row i belongs to compressed sequence i
+        self.use_rho = bool(use_rho and n)
+        if self.use_rho:
+            self.rho = torch.empty(n, h_kv, self.c_Lmax, dtype=torch.float32, device=dev)
+            slot = torch.full((B,), -1, dtype=torch.int32)
+            slot[torch.tensor(self.comp, dtype=torch.long)] = torch.arange(n, dtype=torch.int32)
+            self.rho_rows = slot.to(dev)
         # pinned host copies for the end-to-end figure, and a second set of
         # step buffers: the end-to-end loop alternates between the two so that
         # a step's copies overlap the neighbouring steps' kernels
@@ -286,6 +300,8 @@ class Workload:
             r = (L - 1) % self.b
             if r >= self.b - self.w:
                 tot += (4 if r == self.b - self.w else 8) * L * self.h_kv
+        if self.use_rho:  # the row sums written
+            tot += sum(4 * int(self.case.seq_lens[s]) * self.h_kv for s in self.comp)
         return tot
 
     def compress_bytes(self) -> int:
@@ -293,22 +309,28 @@ class Workload:
         tot = 0
         for s in self.comp:
             L = int(self.case.seq_lens[s])
-            tot += 4 * L * self.h_kv + 8 * L * self.h_kv + L * self.h_kv * self.d * es  # S, F r/w, K
+            tot += 4 * L * self.h_kv + 8 * L * self.h_kv  # S, F r/w
+            tot += 4 * L * self.h_kv if self.use_rho else L * self.h_kv * self.d * es  # row sums read, or K
             tot += 4 * L * self.h_kv + 4 * self.k * self.h_kv                        # top-k
             tot += 2 * 2 * self.k * self.h_kv * self.d * es + 8 * self.k * self.h_kv  # move K, V, F
         return tot
 
     def launches_per_step(self) -> int:
-        # append; decode (one cooperative kernel); compression: global score and
-        # redundancy, then the finish with selection and move
-        return 1 + 1 + (2 if self.n_comp else 0)
+        # append; decode (one cooperative kernel); compression: one kernel with
+        # the decode's row sums, else global score and redundancy, then the
+        # finish with selection and move
+        return 1 + 1 + ((1 if self.use_rho else 2) if self.n_comp else 0)
 
     # ---- the step
     def decode(self, stream=None):
         zp = self.zp
         zp.zp_append_kv(self.desc, self.k_new, self.v_new, self.K, self.V, self.table, self.lens, stream)
-        zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens, self.out,
-                                score_accum=self.S, window=self.w, workspace=self.ws, stream=stream)
+        self.decode_call(stream)
+
+    def decode_call(self, stream=None):
+        rho = dict(rho=self.rho, rho_rows=self.rho_rows, rho_threshold=self.params.threshold) if self.use_rho else {}
+        self.zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens, self.out,
+                                     score_accum=self.S, window=self.w, workspace=self.ws, stream=stream, **rho)
 
     def plan(self):
         """Host planning (a11), one C call for all triggered sequences; the
@@ -329,9 +351,10 @@ class Workload:
         if not self.n_comp:
             return
         zp = self.zp
+        extra = dict(rho=self.rho) if self.use_rho else dict(workspace=self.c_ws)
         zp.zp_compress_layers(self.desc, self.params, self.K, self.V, self.c_table, self.c_lens, self.c_first,
-                             self.S, self.F, self.c_targets, self.k, self.c_keep, self.c_Lmax, rows=self.c_rows,
-                             workspace=self.c_ws, stream=stream)
+                              self.S, self.F, self.c_targets, self.k, self.c_keep, self.c_Lmax, rows=self.c_rows,
+                              stream=stream, **extra)
 
     def step(self):
         self.decode()
@@ -372,8 +395,7 @@ class Workload:
                     zp.zp_append_kv(self.desc, self.k_new, self.v_new, self.K, self.V, self.table, self.lens)
                     if timed:
                         ev[0].record()
-                    zp.zp_paged_decode_attn(self.desc, self.q, self.K, self.V, self.table, self.lens, self.out,
-                                            score_accum=self.S, window=self.w, workspace=self.ws)
+                    self.decode_call()
                     if timed:
                         ev[1].record()
                     self.compress_device()
@@ -874,6 +896,7 @@ def tie_check(wl):
     from oracle import pipeline
     if not wl.n_comp:
         return None
+    wl.decode()  # the row sums the compression may take are those of the keys snapshotted below
     torch.cuda.synchronize()
     b, h_kv, k = wl.b, wl.h_kv, wl.k
     idx = torch.tensor(wl.comp, dtype=torch.long, device=wl.S.device)
@@ -950,6 +973,9 @@ def main():
     ap.add_argument("--min-timed-s", type=float, default=0.6,
                     help="repeat the K timed steps until this much device time is covered")
     ap.add_argument("--engine-steps", type=int, default=2048)
+    ap.add_argument("--no-rho", action="store_true",
+                    help="the compression forms the lightning row sums itself (a second read of the keys) "
+                         "instead of taking those the decode formed")
     ap.add_argument("--sync-compress", action="store_true",
                     help="engine workload: decode waits for each compression instead of letting the "
                          "compressing sequences sit out")
@@ -969,7 +995,7 @@ def main():
         return run_all_pairs(args, dev)
     if args.workload == WINDOW_SCORE:
         return run_window_score(args, dev)
-    wl = Workload(args.workload, seed_offset=rank, dev=dev)
+    wl = Workload(args.workload, seed_offset=rank, dev=dev, use_rho=not args.no_rho)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wl.step()
@@ -1058,11 +1084,14 @@ def main():
                              "compression), event pairs around the decode and the compression of the first "
                              "step of each; host planner every step; e2e through direct calls"
                              % wl.STEPS_PER_GRAPH,
+                   "redundancy": "lightning row sums formed by the decode" if wl.use_rho else
+                                 "lightning row sums formed by the compression",
                    "l2": "inputs larger than L2 (K+V %.0f MB)" % (2 * wl.K.numel() * wl.K.element_size() / 1e6),
                    "peak_kind": peak_kind},
         "repeats": len(rep_ms), "ms_per_step_median": ms_per_step, "ms_per_step_min": min(rep_ms) / args.steps,
         "timed_s": timed_total / 1e3,
-        "roofline": {"kernel": "zp_paged_decode_attn (decode_tc_kernel: attention, merges and window score)",
+        "roofline": {"kernel": "zp_paged_decode_attn%s (decode_tc_kernel: attention, merges, window score%s)"
+                               % (("_rho", ", lightning row sums") if wl.use_rho else ("", "")),
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "frac_of_8tbs": achieved / 8000.0,
                      "traffic": _traffic() if wl.name == DEFAULT_WORKLOAD else None,
@@ -1077,7 +1106,8 @@ def main():
     if comp_ms:
         c_avg = sum(comp_ms) / len(comp_ms)
         line["roofline_compress"] = {
-            "kernel": "zp_compress_layers (global_lightning_kernel + finalize_select_move_kernel), %d sequences"
+            "kernel": ("zp_compress_layers_rho (finalize_select_move_kernel), %d sequences" if wl.use_rho else
+                       "zp_compress_layers (global_lightning_kernel + finalize_select_move_kernel), %d sequences")
                       % wl.n_comp,
             "bound": "hbm", "achieved": cbytes / (c_avg / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
             "frac": cbytes / (c_avg / 1e3) / 1e9 / peak, "traffic": None, "algorithmic_bytes": cbytes,

@@ -28,12 +28,12 @@ STATUS = {0: "ZP_OK", 1: "ZP_ERR_INVALID_ARG", 2: "ZP_ERR_SHAPE", 3: "ZP_ERR_DTY
 # every symbol include/*.h declares
 EXPORTS = [
     "zp_last_error", "zp_status_string", "zp_version", "zp_device_status",
-    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_noalloc",
+    "zp_decode_workspace_size", "zp_paged_decode_attn", "zp_paged_decode_attn_rho", "zp_paged_decode_attn_noalloc",
     "zp_debug_noalloc_preset_ctl", "zp_append_kv", "zp_needs_compression",
     "zp_needs_compression_batch",
     "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
-    "zp_compress_workspace_size", "zp_compress_layers",
+    "zp_compress_workspace_size", "zp_compress_layers", "zp_compress_layers_rho",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
     "zp_plan_capacity",
@@ -65,6 +65,23 @@ class ScoreParams(ctypes.Structure):
 class ScoreRows(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
                 ("rows", ctypes.c_void_p)]
+
+
+class RhoRows(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+                ("rows", ctypes.c_void_p), ("n_rows", ctypes.c_int32), ("threshold", ctypes.c_float)]
+
+
+def _rho_rows(rho, rows, threshold=0.0):
+    """rho: float32 [R][h_kv][stride] or [layers][R][h_kv][stride]; rows: int32 device or None."""
+    if rho.dtype != torch.float32 or rho.dim() not in (3, 4):
+        raise ValueError("redundancy rows must be float32 [R][h_kv][stride] or [layers][R][h_kv][stride]")
+    if rows is not None and rows.dtype != torch.int32:
+        raise ValueError("rho_rows must be int32")
+    layer_stride = rho.stride(0) if rho.dim() == 4 else 0
+    return ctypes.byref(RhoRows(_dev(rho, "rho").value, int(rho.shape[-1]), int(layer_stride),
+                                _dev(rows, "rho_rows").value if rows is not None else None,
+                                int(rho.shape[-3]), float(threshold)))
 
 
 def _score_rows(attn, rows):
@@ -101,6 +118,7 @@ def _load() -> ctypes.CDLL:
     lib.zp_decode_workspace_size.restype = SZ
     lib.zp_decode_workspace_size.argtypes = [D, I32, I32]
     lib.zp_paged_decode_attn.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P, SZ, P]
+    lib.zp_paged_decode_attn_rho.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P, P, SZ, P]
     lib.zp_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, I32, P, I32, P, P, P, I32, I32, P]
     lib.zp_debug_noalloc_preset_ctl.argtypes = [I32, ctypes.c_uint64]
     lib.zp_append_kv.argtypes = [D, P, P, P, P, P, I32, P, I32, P]
@@ -119,6 +137,8 @@ def _load() -> ctypes.CDLL:
     lib.zp_compress_workspace_size.argtypes = [D, I32, I32, I32]
     lib.zp_compress_layers.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P, P,
                                        I64, P, I32, I32, P, P, P, P, I32, P, SZ, P]
+    lib.zp_compress_layers_rho.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P,
+                                           P, I64, P, I32, I32, P, P, P, P, I32, P, P]
     lib.zp_pool_create.restype = P
     lib.zp_pool_create.argtypes = [I32]
     lib.zp_pool_destroy.argtypes = [P]
@@ -186,19 +206,28 @@ def _slot_map(score_accum, score_rows):
 
 
 def zp_paged_decode_attn(desc, q, k_cache, v_cache, block_table, seq_lens, out, score_accum=None,
-                         window=0, workspace=None, stream=None, score_rows=None) -> None:
+                         window=0, workspace=None, stream=None, score_rows=None, rho=None, rho_rows=None,
+                         rho_threshold=0.9) -> None:
     """score_rows: optional int32 [B] device map of batch entries to rows of
-    score_accum (query slots); -1 = no slot, the entry is not scored."""
+    score_accum (query slots); -1 = no slot, the entry is not scored.
+    rho (optional float32 [R][h_kv][stride]) with rho_rows (int32 [B] device,
+    -1 = none): the lightning redundancy row sums of the entries that have a
+    row, at threshold rho_threshold (zp_paged_decode_attn_rho)."""
     B, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
     rows_p, n_rows = _slot_map(score_accum, score_rows)
     if workspace is None:
         workspace = torch.empty(zp_decode_workspace_size(desc, B, table_stride), dtype=torch.uint8,
                                 device=q.device)
-    _check(lib.zp_paged_decode_attn(ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"),
-                                    _dev(v_cache, "v_cache"), _dev(block_table, "block_table"),
-                                    table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
-                                    _dev(score_accum, "score_accum"), rows_p, n_rows, int(window),
-                                    _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    args = (ctypes.byref(desc), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_table, "block_table"), table_stride, _dev(seq_lens, "seq_lens"), B, _dev(out, "out"),
+            _dev(score_accum, "score_accum"), rows_p, n_rows, int(window))
+    tail = (_dev(workspace, "workspace"), workspace.numel(), _stream(stream))
+    if rho is None:
+        _check(lib.zp_paged_decode_attn(*args, *tail))
+    else:
+        if rho_rows is None or rho_rows.numel() != B:
+            raise ValueError("rho needs rho_rows: one int32 entry per batch entry")
+        _check(lib.zp_paged_decode_attn_rho(*args, _rho_rows(rho, rho_rows, rho_threshold), *tail))
 
 
 def zp_paged_decode_attn_noalloc(desc, q, k_cache, v_cache, block_table, seq_lens, out,
@@ -316,18 +345,34 @@ def zp_compress_workspace_size(desc: CacheDesc, n: int, Lmax: int, layer_count: 
 
 def zp_compress_layers(desc, params: ScoreParams, k_cache, v_cache, block_table, seq_lens, first_compression,
                        attn, global_F, dst_targets, k, keep_idx, Lmax, rows=None, tie_count=None, scores_out=None,
-                       workspace=None, k_seq=None, stream=None) -> None:
+                       workspace=None, k_seq=None, stream=None, rho=None, rho_rows=None) -> None:
     """Scores, keep sets and moves of one or several layers in one call.
     k_cache/v_cache: one layer [N_total][b][h_kv][d] or several
     [layers][N_total][b][h_kv][d]; global_F and attn (score rows) alike;
     keep_idx int32 [layers][n][h_kv][k] (or [n][h_kv][k] for one layer);
-    k_seq: optional int32 [n] device array of per-request budgets k_i <= k."""
+    k_seq: optional int32 [n] device array of per-request budgets k_i <= k.
+    rho (optional float32 [R][h_kv][stride], or [layers][R][h_kv][stride]) with
+    rho_rows (int32 [n] device or None: row i): lightning row sums written by
+    the decode; the call then runs zp_compress_layers_rho (no workspace)."""
     n, table_stride = int(block_table.shape[0]), int(block_table.shape[1])
     layers = int(k_cache.shape[0]) if k_cache.dim() == 5 else 1
     layer_stride = int(k_cache.stride(0)) if layers > 1 else 0
     F_layer = int(global_F.stride(0)) if (global_F is not None and global_F.dim() == 4) else 0
     if layers > 1 and attn.dim() != 4:
         raise ValueError("several layers need score rows [layers][R][h_kv][stride]")
+    if rho is not None:
+        if layers > 1 and rho.dim() != 4:
+            raise ValueError("several layers need redundancy rows [layers][R][h_kv][stride]")
+        _check(lib.zp_compress_layers_rho(ctypes.byref(desc), ctypes.byref(params), _dev(k_cache, "k_cache"),
+                                          _dev(v_cache, "v_cache"), layer_stride, layers,
+                                          _dev(block_table, "block_table"), table_stride, _dev(seq_lens, "seq_lens"),
+                                          _dev(first_compression, "first_compression"), n, _score_rows(attn, rows),
+                                          _dev(global_F, "global_F"), F_layer, _dev(dst_targets, "dst_targets"),
+                                          int(dst_targets.shape[1]), int(k), _dev(k_seq, "k_seq"),
+                                          _dev(keep_idx, "keep_idx"), _dev(tie_count, "tie_count"),
+                                          _dev(scores_out, "scores_out"), int(Lmax), _rho_rows(rho, rho_rows),
+                                          _stream(stream)))
+        return
     if workspace is None:
         workspace = torch.empty(max(zp_compress_workspace_size(desc, n, Lmax, layers), 1), dtype=torch.uint8,
                                 device=k_cache.device)
@@ -440,7 +485,7 @@ class Pool:
         return out
 
 
-__all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "ScoreRows", "score_params",
+__all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", "ScoreRows", "RhoRows", "score_params",
            "cache_desc", "zp_decode_workspace_size", "zp_paged_decode_attn",
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_needs_compression_batch", "zp_window_score_workspace_size", "zp_window_score",

@@ -32,6 +32,7 @@
 
 #include <mutex>
 
+#include "lightning.cuh"
 #include "zp_common.cuh"
 
 namespace zp {
@@ -40,6 +41,10 @@ namespace {
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kStageBytesCap = 32768;  // per tensor and stage
 constexpr int kMaxB = 4096;
+// A unit whose block also gets its lightning row sums costs the consumer warps
+// about this much more than a plain one (eighths); the stream-K split weighs
+// such units accordingly so that the CTAs holding them do not finish last.
+constexpr int kRhoUnitWeight8 = 10;
 
 struct DecodeArgs {
     const void *q;
@@ -71,6 +76,14 @@ struct DecodeArgs {
     int4 *unit_info;   // [units]: (sequence, first token, length, window flags) of every unit
     long long logits_units;  // capacity of `logits` in units
     unsigned long long *ctl;  // [B] per-sequence control words of the in-kernel merge (tensor-core path)
+    // lightning redundancy of the sequences about to be compressed (tensor-core
+    // path, b = 16): row sums of each block's cosine matrix per kv head
+    float *rho;               // nullable: rho + (row * h_kv + kvh) * rho_stride + t
+    long long rho_stride;
+    const int32_t *rho_rows;  // [B]: row of each batch entry, -1 = none
+    int n_rho_rows;
+    float rho_p;              // similarity threshold p
+    int rho_weight8;          // stream-K weight of a unit with row sums, in eighths of a plain unit
     unsigned *err;
 };
 
@@ -1166,15 +1179,58 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const long long U = prefix[B];
     if (blockIdx.x == 0)
         for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
-    for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) cst[c] = cta_start(c, U, gridDim.x);
+    if (a.rho && a.rho_weight8 != 8) {
+        // Stream-K over weighted units: a unit of a sequence with row sums
+        // weighs rho_weight8, a plain one 8.  The weighted prefix sits in the
+        // stage area, which no copy has written yet.
+        int *wpre = reinterpret_cast<int *>(smem + lay.stage_off);
+        auto weight = [&](int sq) { return a.rho_rows[sq] >= 0 ? a.rho_weight8 : 8; };
+        if (warp == 0) {
+            int carry = 0;
+            for (int base = 0; base < B; base += 32) {
+                const int sq = base + lane;
+                const int n = sq < B ? (prefix[sq + 1] - prefix[sq]) * weight(sq) : 0;
+                int x = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (sq < B) wpre[sq] = carry + x - n;
+                carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+            }
+            if (lane == 0) wpre[B] = carry;
+        }
+        __syncthreads();
+        const long long W = wpre[B];
+        for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) {
+            const long long target = (long long)c * W / gridDim.x;
+            int lo = 0, hi = B;  // the last sequence whose weighted start is <= target
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (wpre[mid] <= target) lo = mid;
+                else hi = mid - 1;
+            }
+            long long v = U;
+            if (lo < B) {
+                const int wgt = weight(lo);
+                v = prefix[lo] + (target - wpre[lo] + wgt - 1) / wgt;
+                if (v > prefix[lo + 1]) v = prefix[lo + 1];
+            }
+            cst[c] = v;
+        }
+        fence_proxy_async_smem();  // these reads of the stage area precede the copies into it
+    } else {
+        for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) cst[c] = cta_start(c, U, gridDim.x);
+    }
     __syncthreads();
     if (a.want_score && U > a.logits_units) {
         if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 3);
         return;
     }
     const int Gd = gridDim.x;
-    const long long u0 = cta_start(blockIdx.x, U, Gd);
-    const long long u1 = cta_start(blockIdx.x + 1, U, Gd);
+    const long long u0 = cst[blockIdx.x];
+    const long long u1 = cst[blockIdx.x + 1];
     if (u0 >= u1) return;
     int s_first = 0;
     {
@@ -1281,6 +1337,16 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         const int P = lens[seq] - 1;
         return a.want_score && P >= 0 && (P % a.b) >= a.b - a.window && score_row_of(a, seq) >= 0;
     };
+    // this sequence's row of lightning row sums, -1: none
+    auto rho_row_of = [&](int seq) {
+        if (!a.rho) return -1;
+        const int r = a.rho_rows[seq];
+        if (r >= a.n_rho_rows || (r >= 0 && lens[seq] > a.rho_stride)) {
+            if (lane == 0) record_error(a.err, ZP_ERR_DEVICE, 0x22);
+            return -1;
+        }
+        return r;
+    };
 
     int s = s_first;
     long long seg_begin = u0;
@@ -1288,6 +1354,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     reset_state();
     load_q(s);
     bool window_step = compute_window(s);
+    int rho_row = rho_row_of(s);
     // The control words of the CTA's first and last sequence are read now (into
     // the epilogue's statistics area, unused until after the announcement), so
     // that announcing a part after the loop is usually one compare-and-swap.
@@ -1376,6 +1443,30 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 ldsm_x4_t(vt + lrow * RS + (2 * t + lchunk) * 16, v0, v1, v2, v3);
                 mma_16816(acc[t], v0, v1, v2, v3, pb0, pb1);
             }
+            if (rho_row >= 0) {
+                // A sequence about to be compressed: the unit is one block
+                // (b = 16), and the key fragments of Q K^T, loaded again, are
+                // both operands of its Gram K K^T (A = {b0, b2, b1, b3}; B of
+                // the n-tile of tokens 0-7 = {b0, b1}, of tokens 8-15 = {b2,
+                // b3}), in the k-step order of the compression's own Gram, so
+                // the lightning row sums carry the same bits.  K rows >= valid
+                // hold stale data: lightning_rowsums masks every entry they
+                // touch.
+                float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int t = 0; t < KS; ++t) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kt + lrow * RS + (2 * t + lchunk) * 16, b0, b1, b2, b3);
+                    mma_16816(g0, b0, b2, b1, b3, b0, b1);
+                    mma_16816(g1, b0, b2, b1, b3, b2, b3);
+                }
+                const float2 rsum = lightning_rowsums(g0, g1, valid, a.rho_p, lane);
+                if (tig == 0) {
+                    float *ro = a.rho + ((size_t)rho_row * h_kv + kvh) * a.rho_stride + (u - prefix[s]) * kTcTokens;
+                    if (g < valid) ro[g] = rsum.x;
+                    if (g + 8 < valid) ro[g + 8] = rsum.y;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
@@ -1429,6 +1520,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 reset_state();
                 load_q(s);
                 window_step = compute_window(s);
+                rho_row = rho_row_of(s);
             }
         }
     }
@@ -1836,12 +1928,11 @@ extern "C" size_t zp_decode_workspace_size(const zp_cache_desc *D, int32_t B, in
     return p.total;
 }
 
-extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
-                                          const void *v_cache, const int32_t *block_table,
-                                          int32_t table_stride, const int32_t *seq_lens, int32_t B,
-                                          void *out, float *score_accum, const int32_t *score_rows,
-                                          int32_t n_score_rows, int32_t window, void *workspace,
-                                          size_t workspace_bytes, void *stream) {
+static zp_status decode_impl(const zp_cache_desc *D, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                             void *out, float *score_accum, const int32_t *score_rows, int32_t n_score_rows,
+                             int32_t window, void *workspace, size_t workspace_bytes, void *stream,
+                             const zp_rho_rows *rho) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (B < 0 || table_stride < 0) return fail(ZP_ERR_INVALID_ARG, "decode: B or table_stride negative");
@@ -1863,6 +1954,14 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     if (rc != ZP_OK) return rc;
     if (workspace_bytes < p.total)
         return fail(ZP_ERR_CAPACITY, "decode: workspace %zu < %zu bytes", workspace_bytes, p.total);
+    if (rho) {
+        if (!rho->data || !rho->rows) return fail(ZP_ERR_INVALID_ARG, "decode: redundancy rows need data and rows");
+        if (rho->stride < 1 || rho->n_rows < 1)
+            return fail(ZP_ERR_INVALID_ARG, "decode: redundancy rows: stride %lld, %d rows", (long long)rho->stride,
+                        rho->n_rows);
+        if (!p.tc || D->block_size != 16)
+            return fail(ZP_ERR_SHAPE, "decode: the lightning redundancy needs the bf16 tensor-core path and b = 16");
+    }
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     DecodeArgs a;
     a.q = q;
@@ -1897,6 +1996,14 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
     a.unit_info = reinterpret_cast<int4 *>(ws + p.off_info);
     a.logits_units = p.logits_units;
     a.ctl = reinterpret_cast<unsigned long long *>(ws + p.off_count);
+    a.rho = rho ? rho->data : nullptr;
+    a.rho_stride = rho ? rho->stride : 0;
+    a.rho_rows = rho ? rho->rows : nullptr;
+    a.n_rho_rows = rho ? rho->n_rows : 0;
+    a.rho_p = rho ? rho->threshold : 0.f;
+    // weighted split only while the weighted unit count fits in 32 bits
+    const double max_units = (double)B * table_stride * D->block_size / 16.0;
+    a.rho_weight8 = (rho && max_units * kRhoUnitWeight8 < 2.0e9) ? kRhoUnitWeight8 : 8;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = D->h_q / D->h_kv;
@@ -1923,6 +2030,26 @@ extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q,
         if (d == 64 && G == 8) return launch_t<float, 64, 8>(a, p, dev, st);
     }
     return fail(ZP_ERR_SHAPE, "decode: no kernel for d=%d, group=%d", d, G);
+}
+
+extern "C" zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_table,
+                                          int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                                          void *out, float *score_accum, const int32_t *score_rows,
+                                          int32_t n_score_rows, int32_t window, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    return decode_impl(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out, score_accum, score_rows,
+                       n_score_rows, window, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" zp_status zp_paged_decode_attn_rho(const zp_cache_desc *D, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_table,
+                                              int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                                              void *out, float *score_accum, const int32_t *score_rows,
+                                              int32_t n_score_rows, int32_t window, const zp_rho_rows *rho,
+                                              void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(D, q, k_cache, v_cache, block_table, table_stride, seq_lens, B, out, score_accum, score_rows,
+                       n_score_rows, window, workspace, workspace_bytes, stream, rho);
 }
 
 // ---------------------------------------------------------------------------

@@ -18,6 +18,7 @@
 //      lambda * R (eq. 4), last w tokens -> +inf (§4.2, App. C.6).
 #include <math.h>
 
+#include "lightning.cuh"
 #include "select.cuh"
 
 namespace zp {
@@ -49,6 +50,11 @@ struct ScoreArgs {
     // layers of one call (blockIdx.z of the fused kernels): strides in bytes (K)
     // and elements (S, F, X / rho / out)
     long long k_layer_bytes, S_layer, F_layer, X_layer;
+    // lightning row sums given by the caller (zp_compress_layers_rho), else null
+    const float *rho_in;     // rho_in + (row * h_kv + kvh) * rho_stride + t
+    long long rho_stride, rho_layer;
+    const int32_t *rho_rows;  // nullable [n]
+    int n_rho_rows;
 };
 
 // The arguments of layer z: every per-layer pointer advanced by its stride.
@@ -60,6 +66,7 @@ __device__ __forceinline__ ScoreArgs at_layer(const ScoreArgs &a0, int z) {
     a.X = a0.X + z * a0.X_layer;
     a.rho = a0.rho + z * a0.X_layer;
     if (a0.out) a.out = a0.out + z * a0.X_layer;
+    if (a0.rho_in) a.rho_in = a0.rho_in + z * a0.rho_layer;
     return a;
 }
 
@@ -190,9 +197,11 @@ __global__ void lightning_kernel(const ScoreArgs a) {
                     }
                 }
             }
-            // cosine, diagonal, threshold: for column c the newest row r* with
-            // cos > p is zeroed.  Rows of this column live in lanes with the
-            // same chalf across the 16-row groups; with b <= 16 one group.
+            // cosine, diagonal, threshold: for column c the newest row r* < nvalid
+            // with cos > p is zeroed (rows past the block's end take no part,
+            // also when p < 0 makes their zero entries exceed it).  Rows of this
+            // column live in lanes with the same chalf across the 16-row groups;
+            // with b <= 16 one group.
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int c = c0 + j;
@@ -203,7 +212,7 @@ __global__ void lightning_kernel(const ScoreArgs a) {
                     const float nc = sqrtf(nc2);
                     if (nr > 0.f && nc > 0.f) cosv = dot[j] / (nr * nc);
                 }
-                const unsigned above = __ballot_sync(0xFFFFFFFFu, cosv > a.p);
+                const unsigned above = __ballot_sync(0xFFFFFFFFu, r < nvalid && cosv > a.p);
                 const unsigned mine = (above >> (chalf * 16)) & 0xFFFFu;
                 const int rstar = mine ? (31 - __clz(mine)) : -1;
                 if ((lane & 15) == rstar) cosv = 0.f;
@@ -285,51 +294,9 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
         mma_16816(c0, r0, r1, r2, r3, r0, r2);
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
-    // lane holds G[g][2tig+e] (c0[e]), G[g+8][2tig+e] (c0[2+e]), G[g][8+2tig+e] (c1[e]), G[g+8][8+2tig+e] (c1[2+e])
-    __shared__ float nrm[16][16];  // per warp: the 16 norms
-    float *myn = nrm[warp];
-    if (tig == (g >> 1)) myn[g] = c0[g & 1];               // G[g][g], g < 8
-    if (tig == (g >> 1)) myn[g + 8] = c1[2 + (g & 1)];     // G[g+8][g+8]
-    __syncwarp();
-    const int rows[2] = {g, g + 8};
-    const int cols[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
-    float v[2][4];  // [row][col]
-    v[0][0] = c0[0]; v[0][1] = c0[1]; v[0][2] = c1[0]; v[0][3] = c1[1];
-    v[1][0] = c0[2]; v[1][1] = c0[3]; v[1][2] = c1[2]; v[1][3] = c1[3];
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-        const float nr = sqrtf(fmaxf(myn[rows[ri]], 0.f));
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-            const float nc = sqrtf(fmaxf(myn[cols[ci]], 0.f));
-            const bool ok = rows[ri] < nvalid && cols[ci] < nvalid && rows[ri] != cols[ci] && nr > 0.f && nc > 0.f;
-            v[ri][ci] = ok ? v[ri][ci] / (nr * nc) : 0.f;
-        }
-    }
-    // per column: the newest row with cos > p loses its entry
-#pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
-        const unsigned blo = __ballot_sync(0xFFFFFFFFu, v[0][ci] > a.p);
-        const unsigned bhi = __ballot_sync(0xFFFFFFFFu, v[1][ci] > a.p);
-        // bits of the lanes sharing this lane's column: lanes tig + 4 g', g' = 0..7
-        unsigned mlo = 0, mhi = 0;
-#pragma unroll
-        for (int gg = 0; gg < 8; ++gg) {
-            mlo |= ((blo >> (tig + 4 * gg)) & 1u) << gg;
-            mhi |= ((bhi >> (tig + 4 * gg)) & 1u) << gg;
-        }
-        int rstar = -1;
-        if (mhi) rstar = 8 + (31 - __clz(mhi));
-        else if (mlo) rstar = 31 - __clz(mlo);
-        if (rstar == rows[0]) v[0][ci] = 0.f;
-        if (rstar == rows[1]) v[1][ci] = 0.f;
-    }
-    float rs0 = v[0][0] + v[0][1] + v[0][2] + v[0][3];
-    float rs1 = v[1][0] + v[1][1] + v[1][2] + v[1][3];
-    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 1);
-    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 2);
-    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 1);
-    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 2);
+    // rows >= nvalid hold zeros: every entry they touch is masked
+    const float2 rs = lightning_rowsums(c0, c1, nvalid, a.p, lane);
+    const float rs0 = rs.x, rs1 = rs.y;
     if (tig == 0) {
         float *out = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax + tb0;
         if (g < nvalid) out[g] = rs0;
@@ -350,10 +317,10 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // token rows (all kv heads, row stride RS) are in shared memory; G = K K^T on
 // the tensor cores (16 mma.sync), then on the accumulator fragments: cosine
 // (zero-norm keys give 0), zero diagonal, per column the newest row above p
-// zeroed, row sums written to rho.  myn: 16 floats of this warp's shared memory.
+// zeroed, row sums written to rho (lightning_rowsums).
 template <int D>
 __device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int RS, int nvalid,
-                                                int s, int tb0, float *myn, int kvh, int lane) {
+                                                int s, int tb0, int kvh, int lane) {
     const int h_kv = a.h_kv;
     constexpr int KS = D / 16;
     const int g = lane >> 2, tig = lane & 3;
@@ -369,49 +336,9 @@ __device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsign
         mma_16816(c0, r0, r1, r2, r3, r0, r2);
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
-    // rows >= nvalid were not copied: every entry they touch is masked below
-    if (tig == (g >> 1)) myn[g] = c0[g & 1];
-    if (tig == (g >> 1)) myn[g + 8] = c1[2 + (g & 1)];
-    __syncwarp();
-    const int rows[2] = {g, g + 8};
-    const int cols[4] = {2 * tig, 2 * tig + 1, 8 + 2 * tig, 9 + 2 * tig};
-    float v[2][4];
-    v[0][0] = c0[0]; v[0][1] = c0[1]; v[0][2] = c1[0]; v[0][3] = c1[1];
-    v[1][0] = c0[2]; v[1][1] = c0[3]; v[1][2] = c1[2]; v[1][3] = c1[3];
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-        const bool rv = rows[ri] < nvalid;
-        const float nr = rv ? sqrtf(fmaxf(myn[rows[ri]], 0.f)) : 0.f;
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-            const bool cv = cols[ci] < nvalid;
-            const float nc = cv ? sqrtf(fmaxf(myn[cols[ci]], 0.f)) : 0.f;
-            const bool ok = rv && cv && rows[ri] != cols[ci] && nr > 0.f && nc > 0.f;
-            v[ri][ci] = ok ? v[ri][ci] / (nr * nc) : 0.f;
-        }
-    }
-#pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
-        const unsigned blo = __ballot_sync(0xFFFFFFFFu, v[0][ci] > a.p);
-        const unsigned bhi = __ballot_sync(0xFFFFFFFFu, v[1][ci] > a.p);
-        unsigned mlo = 0, mhi = 0;
-#pragma unroll
-        for (int gg = 0; gg < 8; ++gg) {
-            mlo |= ((blo >> (tig + 4 * gg)) & 1u) << gg;
-            mhi |= ((bhi >> (tig + 4 * gg)) & 1u) << gg;
-        }
-        int rstar = -1;
-        if (mhi) rstar = 8 + (31 - __clz(mhi));
-        else if (mlo) rstar = 31 - __clz(mlo);
-        if (rstar == rows[0]) v[0][ci] = 0.f;
-        if (rstar == rows[1]) v[1][ci] = 0.f;
-    }
-    float rs0 = v[0][0] + v[0][1] + v[0][2] + v[0][3];
-    float rs1 = v[1][0] + v[1][1] + v[1][2] + v[1][3];
-    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 1);
-    rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 2);
-    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 1);
-    rs1 += __shfl_xor_sync(0xFFFFFFFFu, rs1, 2);
+    // rows >= nvalid were not copied: every entry they touch is masked
+    const float2 rs = lightning_rowsums(c0, c1, nvalid, a.p, lane);
+    const float rs0 = rs.x, rs1 = rs.y;
     if (tig == 0) {
         float *out = a.rho + ((size_t)s * h_kv + kvh) * a.Lmax + tb0;
         if (g < nvalid) out[g] = rs0;
@@ -425,7 +352,6 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     extern __shared__ __align__(128) unsigned char gsm[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_blk, s_abort;
-    __shared__ float nrm[16][16];
     const int s = blockIdx.y;
     const int bi = blockIdx.x;
     const int L = clamp_len(a, s);
@@ -474,7 +400,7 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     // its output
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (s_abort) return;
-    lightning_block<D>(a, gsm, RS, nvalid, s, tb0, nrm[warp], warp, lane);
+    lightning_block<D>(a, gsm, RS, nvalid, s, tb0, warp, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (g_on) {
         if (row < 0) {
@@ -614,6 +540,10 @@ __device__ __forceinline__ float2 block_reduce_maxsum(float m, float s, float *r
     return make_float2(m, s);
 }
 
+// OWN_X: the global score (Alg. 2, as global_lightning_kernel) is formed here
+// from the score row and F, and rho comes from the caller's rows (a.rho_in);
+// otherwise both are read from X and rho of the preceding scores kernel.
+template <bool OWN_X>
 __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const ScoreArgs a0, const MoveArgs m0) {
     const int z = blockIdx.z;
     const ScoreArgs a = at_layer(a0, z);
@@ -640,10 +570,65 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
     const int nb = (L + a.b - 1) / a.b;
     for (int t = tid; t < nt; t += nthr) dst_s[t] = m.dst[(size_t)s * m.target_stride + t];
     for (int t = tid; t < nb; t += nthr) tbl_s[t] = a.table[(size_t)s * a.table_stride + t];
+    const bool first = a.first ? a.first[s] != 0 : true;
+    const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
+    if constexpr (OWN_X) {
+        // Global score (Alg. 2): max(alpha * F, S) on blocks 0..N-2 after the
+        // first compression, else S.  alpha * F first (F is not written by the
+        // kernel this one may follow), the score row after the wait.
+        const bool read_F = a.use_global && !first;
+        if (read_F) {
+            __syncthreads();
+            for (int t = tid; t < L; t += nthr) {
+                if ((t >> 4) == nb - 1) continue;
+                const int blk = tbl_s[t >> 4];
+                float f = 0.f;
+                if (blk < 0 || blk >= a.n_total) record_error(a.err, ZP_ERR_DEVICE, 0x202);
+                else f = a.F[((size_t)blk * 16 + (t & 15)) * a.h_kv + kvh];
+                xs[t] = a.alpha * f;
+            }
+        }
+        // launched as a programmatic dependent of the decode: the score rows
+        // and rho are read after its completion (a no-op for a plain launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const int srow = a.S_rows ? a.S_rows[s] : s;
+        int rrow = a.rho_rows ? a.rho_rows[s] : s;
+        if (a.use_sim && (rrow < 0 || rrow >= a.n_rho_rows || L > a.rho_stride)) {
+            if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x203);
+            rrow = -1;
+        }
+        if (srow < 0) {
+            if (tid == 0) record_error(a.err, ZP_ERR_DEVICE, 0x202);
+        } else {
+            float *sp = a.S + ((size_t)srow * a.h_kv + kvh) * a.S_stride;
+            const float *rp = rrow >= 0 ? a.rho_in + ((size_t)rrow * a.h_kv + kvh) * a.rho_stride : nullptr;
+            for (int t0 = tid; t0 < L; t0 += 4 * nthr) {  // four elements' loads in flight per thread
+                float sv[4], rv4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = t0 + i * nthr;
+                    sv[i] = t < L ? sp[t] : 0.f;
+                    rv4[i] = (t < L && rp) ? rp[t] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = t0 + i * nthr;
+                    if (t < L) {
+                        float v = sv[i];
+                        if (read_F && (t >> 4) != nb - 1) {
+                            v = fmaxf(xs[t], v);
+                            sp[t] = v;
+                        }
+                        xs[t] = v;
+                        fs[t] = rv4[i];
+                    }
+                }
+            }
+        }
+    } else {
     // launched as a programmatic dependent of the scores kernel: X, rho and the
     // score rows are read after its completion (a no-op for a plain launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const size_t row = ((size_t)s * a.h_kv + kvh) * a.Lmax;
     for (int t0 = tid; t0 < L; t0 += 4 * nthr) {  // four elements' loads in flight per thread
         float xv[4], rv4[4];
 #pragma unroll
@@ -661,9 +646,9 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
             }
         }
     }
+    }
     __syncthreads();
     // ---- final scores (App. C.4-C.8, eq. 4, window), in place of rho
-    const bool first = a.first ? a.first[s] != 0 : true;
     const bool pool = a.pool_kernel > 1 && (a.pool_policy == 2 || (a.pool_policy == 1 && first));
     const int r = a.pool_kernel / 2;
     // R = softmax(rho / (L tau)) in base 2: one pass for the max and the sum
@@ -799,20 +784,22 @@ extern "C" size_t zp_score_workspace_size(const zp_cache_desc *D, int32_t n, int
 // Validates the scoring arguments, fills `a` and launches the global-score and
 // redundancy kernels (X and rho in the workspace); the caller launches the
 // finish.  *launched = false when there is nothing to do (n or Lmax zero).
+// With rho_in (lightning row sums given by the caller) nothing is launched and
+// the workspace is not needed: the finish kernel forms X itself.
 static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P, const void *k_cache,
                                const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
                                const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
                                const float *global_F, float *scores_out, int32_t Lmax, void *workspace,
                                size_t workspace_bytes, cudaStream_t st, ScoreArgs &a, DeviceInfo &dev,
                                bool *launched, int layers = 1, long long k_layer_elems = 0,
-                               long long F_layer = 0) {
+                               long long F_layer = 0, const zp_rho_rows *rho_in = nullptr) {
     *launched = false;
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (!P) return fail(ZP_ERR_INVALID_ARG, "score: NULL params");
     if (n < 0 || Lmax < 0 || table_stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: bad sizes");
     if (n == 0 || Lmax == 0) return ok();
-    if (!block_table || !seq_lens || !workspace)
+    if (!block_table || !seq_lens || (!workspace && !rho_in))
         return fail(ZP_ERR_INVALID_ARG, "score: NULL buffer");
     if (!attn || !attn->data) return fail(ZP_ERR_INVALID_ARG, "score: NULL attention-score rows");
     if (attn->stride < 1) return fail(ZP_ERR_INVALID_ARG, "score: score row stride %lld", (long long)attn->stride);
@@ -832,7 +819,15 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     if (P->use_similarity && P->lightning && D->block_size > 16)
         return fail(ZP_ERR_SHAPE, "score: lightning kernel supports b <= 16 (b=%d)", D->block_size);
     const size_t need = (size_t)layers * zp_score_workspace_size(D, n, Lmax);
-    if (workspace_bytes < need) return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
+    if (!rho_in && workspace_bytes < need)
+        return fail(ZP_ERR_CAPACITY, "score: workspace %zu < %zu", workspace_bytes, need);
+    if (rho_in) {
+        if (!(P->use_similarity && P->lightning && D->dtype == ZP_BF16 && D->block_size == 16))
+            return fail(ZP_ERR_SHAPE, "score: given row sums need bf16 keys, b = 16 and the lightning redundancy");
+        if (!rho_in->data || rho_in->stride < 1 || rho_in->n_rows < 1 ||
+            (layers > 1 && rho_in->layer_stride < (long long)rho_in->n_rows * D->h_kv * rho_in->stride))
+            return fail(ZP_ERR_INVALID_ARG, "score: bad redundancy rows");
+    }
     rc = device_info(&dev);
     if (rc != ZP_OK) return rc;
     a.table = block_table;
@@ -853,6 +848,11 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     a.X_layer = (long long)n * D->h_kv * Lmax;
     a.X = reinterpret_cast<float *>(ws);
     a.rho = reinterpret_cast<float *>(ws + align_up((size_t)layers * a.X_layer * 4, 256));
+    a.rho_in = rho_in ? rho_in->data : nullptr;
+    a.rho_stride = rho_in ? rho_in->stride : 0;
+    a.rho_layer = rho_in ? rho_in->layer_stride : 0;
+    a.rho_rows = rho_in ? rho_in->rows : nullptr;
+    a.n_rho_rows = rho_in ? rho_in->n_rows : 0;
     a.k_layer_bytes = k_layer_elems * elem_bytes(D->dtype);
     a.S_layer = attn->layer_stride;
     a.F_layer = F_layer;
@@ -868,6 +868,10 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     a.tau = P->tau;
     a.window = P->window;
     a.err = dev.error_word;
+    if (rho_in) {
+        *launched = true;
+        return ok();
+    }
     if (a.use_sim && P->lightning && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) &&
         a.h_kv <= 16 && reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
         // global score and redundancy of each block in one kernel
@@ -981,15 +985,13 @@ extern "C" size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, 
 }
 
 
-extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
-                                        void *v_base, int64_t layer_stride, int32_t layer_count,
-                                        const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
-                                        const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
-                                        float *global_F, int64_t F_layer_stride, const int32_t *dst_targets,
-                                        int32_t target_stride, int32_t k, const int32_t *k_seq,
-                                        int32_t *keep_idx, int32_t *tie_count,
-                                        float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
-                                        void *stream) {
+static zp_status compress_impl(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
+                               int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
+                               int32_t table_stride, const int32_t *seq_lens, const uint8_t *first_compression,
+                               int32_t n, const zp_score_rows *attn, float *global_F, int64_t F_layer_stride,
+                               const int32_t *dst_targets, int32_t target_stride, int32_t k, const int32_t *k_seq,
+                               int32_t *keep_idx, int32_t *tie_count, float *scores_out, int32_t Lmax,
+                               void *workspace, size_t workspace_bytes, void *stream, const zp_rho_rows *rho) {
     zp_status rc = check_desc(D);
     if (rc != ZP_OK) return rc;
     if (n < 0 || k < 0 || Lmax < 0 || target_stride < 1 || layer_count < 0)
@@ -1018,13 +1020,16 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
     const bool fused_ok = D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
                           D->h_kv <= 16 && P && P->use_similarity && P->lightning &&
                           2 * row_vec <= kFsThreads * kFsVecPerThread && smem <= (size_t)dev.smem_optin;
+    if (rho && !fused_ok)
+        return fail(ZP_ERR_SHAPE, "compress: given row sums need the one-kernel path (bf16, b = 16, lightning, "
+                                  "%zu bytes of shared memory per row)", smem);
     if (fused_ok) {
         // every layer in one launch of each kernel (blockIdx.z = layer)
         ScoreArgs a;
         bool launched;
         rc = launch_scores(D, P, k_base, block_table, table_stride, seq_lens, first_compression, n, attn, global_F,
                            scores_out, Lmax, workspace, workspace_bytes, st, a, dev, &launched, layer_count,
-                           layer_stride, F_layer_stride);
+                           layer_stride, F_layer_stride, rho);
         if (rc != ZP_OK || !launched) return rc;
         MoveArgs m;
         m.K = static_cast<uint4 *>(k_base);
@@ -1039,11 +1044,13 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         m.F = global_F;
         m.kv_layer_vec = layer_stride * es / 16;
         m.F_layer = F_layer_stride;
-        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(finalize_select_move_kernel), smem,
+        auto kfin = rho ? finalize_select_move_kernel<true> : finalize_select_move_kernel<false>;
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kfin), smem,
                                             "compress: shared-memory attribute");
         if (rs != ZP_OK) return rs;
         // programmatic dependent launch: the finish grid may start while the
-        // scores kernel drains; it reads that kernel's output only after
+        // kernel before it (the scores kernel, or with given row sums the
+        // decode) drains; it reads that kernel's output only after
         // griddepcontrol.wait
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(a.h_kv, n, layer_count);
@@ -1055,7 +1062,7 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, finalize_select_move_kernel, a, m);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kfin, a, m);
         if (e != cudaSuccess) return cuda_fail(e, "compress: launch");
         return ok();
     }
@@ -1090,4 +1097,32 @@ extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_p
         if (rc != ZP_OK) return rc;
     }
     return ok();
+}
+
+extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
+                                        void *v_base, int64_t layer_stride, int32_t layer_count,
+                                        const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,
+                                        const uint8_t *first_compression, int32_t n, const zp_score_rows *attn,
+                                        float *global_F, int64_t F_layer_stride, const int32_t *dst_targets,
+                                        int32_t target_stride, int32_t k, const int32_t *k_seq,
+                                        int32_t *keep_idx, int32_t *tie_count,
+                                        float *scores_out, int32_t Lmax, void *workspace, size_t workspace_bytes,
+                                        void *stream) {
+    return compress_impl(D, P, k_base, v_base, layer_stride, layer_count, block_table, table_stride, seq_lens,
+                         first_compression, n, attn, global_F, F_layer_stride, dst_targets, target_stride, k, k_seq,
+                         keep_idx, tie_count, scores_out, Lmax, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" zp_status zp_compress_layers_rho(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
+                                            void *v_base, int64_t layer_stride, int32_t layer_count,
+                                            const int32_t *block_table, int32_t table_stride,
+                                            const int32_t *seq_lens, const uint8_t *first_compression, int32_t n,
+                                            const zp_score_rows *attn, float *global_F, int64_t F_layer_stride,
+                                            const int32_t *dst_targets, int32_t target_stride, int32_t k,
+                                            const int32_t *k_seq, int32_t *keep_idx, int32_t *tie_count,
+                                            float *scores_out, int32_t Lmax, const zp_rho_rows *rho, void *stream) {
+    if (!rho) return fail(ZP_ERR_INVALID_ARG, "compress: NULL redundancy rows");
+    return compress_impl(D, P, k_base, v_base, layer_stride, layer_count, block_table, table_stride, seq_lens,
+                         first_compression, n, attn, global_F, F_layer_stride, dst_targets, target_stride, k, k_seq,
+                         keep_idx, tie_count, scores_out, Lmax, nullptr, 0, stream, rho);
 }

@@ -79,6 +79,27 @@ typedef struct {
     float tau;              /* softmax temperature of the redundancy score (C.8) */
 } zp_score_params;
 
+/* Rows of lightning redundancy row sums [Zipage App. C.5 (definition), C.7
+ * (same-block pairs)]: for each block of b = 16 tokens and each kv head, the
+ * cosine matrix of the block's keys with a zero diagonal and, per column, the
+ * newest row above the threshold p zeroed; rho[t] is the sum of row t.  Row r
+ * of kv head h holds rho[t] at data + l*layer_stride + (r*h_kv + h)*stride + t
+ * (t < L of the sequence the row belongs to).
+ *   zp_paged_decode_attn_rho writes them: rows[s] (device int32 [B]) is the
+ *     row of batch entry s, -1 = none; threshold is p.
+ *   zp_compress_layers_rho reads them: rows (nullable, device int32 [n]) is the
+ *     row of compressed sequence i (NULL: row i); threshold is not read (the
+ *     row sums already hold it).
+ * n_rows bounds the rows (a row >= n_rows is recorded as ZP_ERR_DEVICE). */
+typedef struct zp_rho_rows {
+    float *data;
+    int64_t stride;        /* >= L of every sequence with a row */
+    int64_t layer_stride;  /* elements between layers (zp_compress_layers_rho) */
+    const int32_t *rows;
+    int32_t n_rows;
+    float threshold;       /* p */
+} zp_rho_rows;
+
 /* ---- status ------------------------------------------------------------- */
 const char *zp_last_error(void);
 const char *zp_status_string(zp_status s);
@@ -135,6 +156,25 @@ zp_status zp_paged_decode_attn(const zp_cache_desc *D, const void *q, const void
                                void *out, float *score_accum, const int32_t *score_rows,
                                int32_t n_score_rows, int32_t window, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/* zp_paged_decode_attn that also computes, for the batch entries with a row
+ * in rho (the sequences about to be compressed after this step), the lightning
+ * redundancy row sums of every block of their keys [Zipage App. C.5, C.7]
+ * from the key tiles the decode already holds on chip (no second read of the
+ * keys).  The row sums equal, bit for bit, those zp_score_tokens and
+ * zp_compress_layers compute for the same keys and threshold; a compression
+ * that runs after this call with the same cache can take them through
+ * zp_compress_layers_rho.  Outputs and scores of the decode are unchanged.
+ * Requires the bf16 cache and b = 16 (ZP_ERR_SHAPE otherwise); a sequence
+ * longer than rho->stride is not given row sums and is recorded as
+ * ZP_ERR_DEVICE (detail 0x22).  Other arguments and errors: as
+ * zp_paged_decode_attn. */
+zp_status zp_paged_decode_attn_rho(const zp_cache_desc *D, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_table,
+                                   int32_t table_stride, const int32_t *seq_lens, int32_t B,
+                                   void *out, float *score_accum, const int32_t *score_rows,
+                                   int32_t n_score_rows, int32_t window, const zp_rho_rows *rho,
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Same computation and arguments as zp_paged_decode_attn, without the
  * workspace: for callers that cannot allocate device memory when they decode
@@ -318,6 +358,25 @@ zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, v
                              const int32_t *k_seq, int32_t *keep_idx,
                              int32_t *tie_count, float *scores_out, int32_t Lmax, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/* zp_compress_layers with the lightning redundancy row sums given (rho, as
+ * written by zp_paged_decode_attn_rho for the same keys) instead of computed:
+ * the same scores, keep sets, moves, F and score-row updates, in ONE kernel per
+ * call -- per (kv head, sequence, layer) the global score (Alg. 2) of the score
+ * row, then the rest as zp_compress_layers; the second read of the keys and
+ * the global/lightning kernel drop out.  Requires what the fused path of
+ * zp_compress_layers requires (bf16, b = 16, use_similarity and lightning set,
+ * the row in shared memory; ZP_ERR_SHAPE otherwise).  Layer l reads rho->data
+ * + l*rho->layer_stride.  The workspace is not used (it may be NULL).  The
+ * kernel is launched as a programmatic dependent of the kernel before it and
+ * reads the score rows and rho only after that kernel has completed. */
+zp_status zp_compress_layers_rho(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
+                                 int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
+                                 int32_t table_stride, const int32_t *seq_lens, const uint8_t *first_compression,
+                                 int32_t n, const zp_score_rows *attn, float *global_F, int64_t F_layer_stride,
+                                 const int32_t *dst_targets, int32_t target_stride, int32_t k,
+                                 const int32_t *k_seq, int32_t *keep_idx, int32_t *tie_count, float *scores_out,
+                                 int32_t Lmax, const zp_rho_rows *rho, void *stream);
 
 /* ---- host block pool and planner (no device work) ------------------------ */
 typedef struct zp_pool zp_pool;
