@@ -559,7 +559,7 @@ def run_reference(args):
     return 0
 
 
-def engine_measure(dev, rank, steps, warmup, sync_compress, dist=None, clocks=None):
+def engine_measure(dev, rank, steps, warmup, sync_compress, dist=None, clocks=None, decode_rho=True):
     """The engine's multi-step loop on the high-concurrency workload: every
     step appends and decodes the active sequences (one launch each), checks
     the trigger, and starts the compression of the triggered ones on the side
@@ -574,7 +574,7 @@ def engine_measure(dev, rank, steps, warmup, sync_compress, dist=None, clocks=No
     stride = 4096 // b + 2
     n_total = int(np.maximum((lens0 + b - 1) // b + 1, N_max).sum()) + 64
     loop = DecodeLoop(h_q, h_kv, d, b, n_total, N_max, stride, layers=1, dtype=torch.bfloat16, window=b,
-                      async_compress=not sync_compress, device=dev)
+                      async_compress=not sync_compress, device=dev, decode_rho=decode_rho)
     loop.add_sequences(lens0)
     gd = torch.Generator(device=dev).manual_seed(1004 + rank)
     loop.K.copy_(torch.randn(loop.K.shape, generator=gd, device=dev))
@@ -610,7 +610,9 @@ def engine_measure(dev, rank, steps, warmup, sync_compress, dist=None, clocks=No
         raise RuntimeError("device status %d in the timed region" % code)
     ms = _max_over_ranks(dist, start.elapsed_time(stop), dev)
     geom = {"seqs": B, "heads": "32q/8kv", "head_dim": d, "block": b, "max_blocks_per_seq": N_max,
-            "kept_tokens": (N_max - 1) * b, "window": b, "ctx": "start uniform 1024-4096"}
+            "kept_tokens": (N_max - 1) * b, "window": b, "ctx": "start uniform 1024-4096",
+            "redundancy": "lightning row sums formed by the decode" if loop.use_rho else
+                          "lightning row sums formed by the compression"}
     comps = loop.compressions - comps0
     del loop
     torch.cuda.empty_cache()
@@ -624,7 +626,7 @@ def run_engine(args, dist, rank, world, dev):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     ms, decoded, dbytes, comps, geom = engine_measure(dev, rank, args.steps, args.warmup, args.sync_compress,
-                                                      dist, clocks)
+                                                      dist, clocks, decode_rho=not args.no_rho)
     clk = clocks.stop()
     if rank == 0:
         cfg = dict(workload=ENGINE_WORKLOAD, **geom)

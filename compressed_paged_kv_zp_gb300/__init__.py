@@ -33,7 +33,7 @@ EXPORTS = [
     "zp_needs_compression_batch",
     "zp_window_score_workspace_size", "zp_window_score",
     "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk", "zp_compact_pages",
-    "zp_compress_workspace_size", "zp_compress_layers", "zp_compress_layers_rho",
+    "zp_compress_workspace_size", "zp_compress_layers", "zp_compress_layers_rho", "zp_compress_rho_supported",
     "zp_pool_create", "zp_pool_destroy", "zp_pool_num_free", "zp_pool_refcount", "zp_pool_alloc",
     "zp_pool_incref", "zp_pool_release", "zp_plan_compaction", "zp_plan_compaction_batch",
     "zp_plan_capacity",
@@ -137,6 +137,8 @@ def _load() -> ctypes.CDLL:
     lib.zp_compress_workspace_size.argtypes = [D, I32, I32, I32]
     lib.zp_compress_layers.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P, P,
                                        I64, P, I32, I32, P, P, P, P, I32, P, SZ, P]
+    lib.zp_compress_rho_supported.restype = I32
+    lib.zp_compress_rho_supported.argtypes = [D, ctypes.POINTER(ScoreParams), I32, I32]
     lib.zp_compress_layers_rho.argtypes = [D, ctypes.POINTER(ScoreParams), P, P, I64, I32, P, I32, P, P, I32, P,
                                            P, I64, P, I32, I32, P, P, P, P, I32, P, P]
     lib.zp_pool_create.restype = P
@@ -387,6 +389,12 @@ def zp_compress_layers(desc, params: ScoreParams, k_cache, v_cache, block_table,
                                   _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
 
 
+def zp_compress_rho_supported(desc, params: ScoreParams, Lmax: int, k: int) -> bool:
+    """Whether zp_compress_layers_rho (the decode's row sums, one kernel) covers
+    this cache, these switches, Lmax and k on the current device."""
+    return bool(lib.zp_compress_rho_supported(ctypes.byref(desc), ctypes.byref(params), int(Lmax), int(k)))
+
+
 def zp_plan_capacity(m_available: int, m_kv_block: int, m_q_request: int, max_blocks: int,
                      extra=(0, 1)):
     """(M, N_total) of eq. (1) / (2): the largest request concurrency and the
@@ -473,7 +481,7 @@ class Pool:
                    "new_tables": np.empty((n, max_blocks), np.int32),
                    "dropped": np.empty((n, stride), np.int32), "n_dropped": np.empty(n, np.int32),
                    "n_fresh": np.empty(n, np.int32)}
-        P = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        P = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
         mbs = None
         if max_blocks_seq is not None:
             mbs = np.ascontiguousarray(max_blocks_seq, dtype=np.int32)
@@ -490,5 +498,5 @@ __all__ = ["lib", "LIB_PATH", "EXPORTS", "ZPError", "CacheDesc", "ScoreParams", 
            "zp_paged_decode_attn_noalloc", "zp_append_kv",
            "zp_needs_compression", "zp_needs_compression_batch", "zp_window_score_workspace_size", "zp_window_score",
            "zp_score_workspace_size", "zp_score_tokens", "zp_select_topk",
-           "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layers", "zp_plan_capacity", "zp_device_status", "Pool",
+           "zp_compact_pages", "zp_compress_workspace_size", "zp_compress_layers", "zp_compress_rho_supported", "zp_plan_capacity", "zp_device_status", "Pool",
            "ZP_BF16", "ZP_F32"]

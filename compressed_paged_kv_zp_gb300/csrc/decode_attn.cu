@@ -1132,6 +1132,12 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const int lane = tid & 31;
     const int RS = tc_row_stride(h_kv, D);             // staged row stride
     const int stage_bytes = 2 * kTcTokens * RS;        // K rows then V rows
+    // Weighted stream-K split (row sums requested): the weighted prefix
+    // wpre[0..B] and the per-sequence unit weights wgt[0..B) sit in the stage
+    // area, which no copy writes before the split is done.
+    const bool weighted = a.rho && a.rho_weight8 != 8;
+    int *wpre = reinterpret_cast<int *>(smem + lay.stage_off);
+    int *wgt = wpre + (B + 1);
 
     for (int s = tid; s < B; s += blockDim.x) {
         int L = a.seq_lens[s];
@@ -1145,6 +1151,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             L = maxL;
         }
         lens[s] = L;
+        if (weighted) wgt[s] = a.rho_rows[s] >= 0 ? a.rho_weight8 : 8;
     }
     if (tid == 0) {
         abort_flag[0] = 0;
@@ -1160,48 +1167,41 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     }
     __syncthreads();
     if (warp == 0) {
-        int carry = 0;
+        // unit prefix, and with a weighted split the weighted prefix, in one pass
+        int carry = 0, wcarry = 0;
         for (int base = 0; base < B; base += 32) {
             const int s = base + lane;
             const int n = s < B ? (lens[s] + kTcTokens - 1) / kTcTokens : 0;
-            int x = n;
+            const int nw = (weighted && s < B) ? n * wgt[s] : 0;
+            int x = n, xw = nw;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o) x += y;
+                const int yw = __shfl_up_sync(0xFFFFFFFFu, xw, o);
+                if (lane >= o) {
+                    x += y;
+                    xw += yw;
+                }
             }
-            if (s < B) prefix[s] = carry + x - n;
+            if (s < B) {
+                prefix[s] = carry + x - n;
+                if (weighted) wpre[s] = wcarry + xw - nw;
+            }
             carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+            wcarry += __shfl_sync(0xFFFFFFFFu, xw, 31);
         }
-        if (lane == 0) prefix[B] = carry;
+        if (lane == 0) {
+            prefix[B] = carry;
+            if (weighted) wpre[B] = wcarry;
+        }
     }
     __syncthreads();
     const long long U = prefix[B];
     if (blockIdx.x == 0)
         for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
-    if (a.rho && a.rho_weight8 != 8) {
+    if (weighted) {
         // Stream-K over weighted units: a unit of a sequence with row sums
-        // weighs rho_weight8, a plain one 8.  The weighted prefix sits in the
-        // stage area, which no copy has written yet.
-        int *wpre = reinterpret_cast<int *>(smem + lay.stage_off);
-        auto weight = [&](int sq) { return a.rho_rows[sq] >= 0 ? a.rho_weight8 : 8; };
-        if (warp == 0) {
-            int carry = 0;
-            for (int base = 0; base < B; base += 32) {
-                const int sq = base + lane;
-                const int n = sq < B ? (prefix[sq + 1] - prefix[sq]) * weight(sq) : 0;
-                int x = n;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                    if (lane >= o) x += y;
-                }
-                if (sq < B) wpre[sq] = carry + x - n;
-                carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-            }
-            if (lane == 0) wpre[B] = carry;
-        }
-        __syncthreads();
+        // weighs rho_weight8, a plain one 8.
         const long long W = wpre[B];
         for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) {
             const long long target = (long long)c * W / gridDim.x;
@@ -1213,8 +1213,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             }
             long long v = U;
             if (lo < B) {
-                const int wgt = weight(lo);
-                v = prefix[lo] + (target - wpre[lo] + wgt - 1) / wgt;
+                const int w = wgt[lo];
+                v = prefix[lo] + (target - wpre[lo] + w - 1) / w;
                 if (v > prefix[lo + 1]) v = prefix[lo + 1];
             }
             cst[c] = v;
@@ -2001,9 +2001,12 @@ static zp_status decode_impl(const zp_cache_desc *D, const void *q, const void *
     a.rho_rows = rho ? rho->rows : nullptr;
     a.n_rho_rows = rho ? rho->n_rows : 0;
     a.rho_p = rho ? rho->threshold : 0.f;
-    // weighted split only while the weighted unit count fits in 32 bits
+    // weighted split only while the weighted unit count fits in 32 bits and
+    // its two arrays (2B + 1 ints) fit in the stage area
     const double max_units = (double)B * table_stride * D->block_size / 16.0;
-    a.rho_weight8 = (rho && max_units * kRhoUnitWeight8 < 2.0e9) ? kRhoUnitWeight8 : 8;
+    const long long stage_area = (long long)p.stages * 2 * kTcTokens * tc_row_stride(D->h_kv, D->head_dim);
+    a.rho_weight8 = (rho && p.tc && max_units * kRhoUnitWeight8 < 2.0e9 && (2LL * B + 1) * 4 <= stage_area)
+                        ? kRhoUnitWeight8 : 8;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = D->h_q / D->h_kv;

@@ -4,6 +4,7 @@
 // the kept entries occupy the first N_max - 1 blocks, the N_max-th block is
 // reserved, the rest are released) and §4.4 (reference-counted prefix blocks;
 // compression writes into target blocks so shared blocks survive).
+#include <algorithm>
 #include <set>
 #include <vector>
 
@@ -115,12 +116,13 @@ extern "C" zp_status zp_plan_compaction(zp_pool *pool, const int32_t *table, int
         new_table[t] = id;
         if (t < max_blocks - 1) targets[t] = id;
     }
+    // dropped: the table's blocks that the new table does not hold, in table
+    // order (a sorted copy of the new table answers each lookup)
+    std::vector<int32_t> held(new_table, new_table + max_blocks);
+    std::sort(held.begin(), held.end());
     int32_t nd = 0;
-    for (int32_t i = 0; i < n_blocks; ++i) {
-        bool kept = false;
-        for (int32_t t = 0; t < max_blocks; ++t) kept |= new_table[t] == table[i];
-        if (!kept) dropped[nd++] = table[i];
-    }
+    for (int32_t i = 0; i < n_blocks; ++i)
+        if (!std::binary_search(held.begin(), held.end(), table[i])) dropped[nd++] = table[i];
     *n_dropped = nd;
     *n_fresh = used;
     return ok();

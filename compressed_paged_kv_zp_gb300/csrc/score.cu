@@ -1099,6 +1099,17 @@ static zp_status compress_impl(const zp_cache_desc *D, const zp_score_params *P,
     return ok();
 }
 
+extern "C" int32_t zp_compress_rho_supported(const zp_cache_desc *D, const zp_score_params *P, int32_t Lmax,
+                                             int32_t k) {
+    if (check_desc(D) != ZP_OK || !P || Lmax < 0 || k < 0) return 0;
+    DeviceInfo dev;
+    if (device_info(&dev) != ZP_OK) return 0;
+    const int row_vec = D->head_dim * elem_bytes(D->dtype) / 16;
+    return D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
+           D->h_kv <= 16 && P->use_similarity && P->lightning && 2 * row_vec <= kFsThreads * kFsVecPerThread &&
+           fused_smem(Lmax, k, D->block_size) <= (size_t)dev.smem_optin;
+}
+
 extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
                                         void *v_base, int64_t layer_stride, int32_t layer_count,
                                         const int32_t *block_table, int32_t table_stride, const int32_t *seq_lens,

@@ -7,6 +7,10 @@ The host side of the hot path around the libzp kernels:
     own, at most the loop's N_max);
   * target blocks from the reference-counted pool, one planner call for all
     triggered sequences (§4.4);
+  * the decode of the step in which a sequence triggers also forms the
+    lightning redundancy row sums of its blocks from the keys it reads (no
+    second read of the keys for the compression), when the library's
+    one-kernel compression covers the cache and switches;
   * scoring, top-k and compaction on a side stream, ordered after the decode
     that produced the window score by a CUDA event (§4.5); in asynchronous
     mode the compressing sequences sit out decode until their event has
@@ -21,9 +25,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layers, zp_compress_workspace_size,
-               zp_needs_compression_batch,
-               zp_decode_workspace_size, zp_paged_decode_attn)
+from . import (Pool, cache_desc, score_params, zp_append_kv, zp_compress_layers, zp_compress_rho_supported,
+               zp_compress_workspace_size, zp_needs_compression_batch, zp_decode_workspace_size,
+               zp_paged_decode_attn)
 
 
 def upload(arr: np.ndarray, dev) -> torch.Tensor:
@@ -33,11 +37,31 @@ def upload(arr: np.ndarray, dev) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(arr)).pin_memory().to(dev, non_blocking=True)
 
 
+def upload_packed(arrays, dev):
+    """Several small host arrays -> device tensors of the same dtypes and
+    shapes, through ONE pinned staging buffer and one copy (each array starts
+    on a 16-byte boundary)."""
+    offs, total = [], 0
+    for a in arrays:
+        offs.append(total)
+        total += (a.nbytes + 15) // 16 * 16
+    host = np.empty(max(total, 16), dtype=np.uint8)
+    for a, o in zip(arrays, offs):
+        host[o:o + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+    buf = torch.from_numpy(host).pin_memory().to(dev, non_blocking=True)
+    out = []
+    for a, o in zip(arrays, offs):
+        dt = {np.dtype(np.int32): torch.int32, np.dtype(np.uint8): torch.uint8}[a.dtype]
+        out.append(buf[o:o + a.nbytes].view(dt).view(a.shape))
+    return out
+
+
 class DecodeLoop:
     """Batch of sequences decoding over `layers` paged layers of one pool."""
 
     def __init__(self, h_q, h_kv, d, b, n_total, max_blocks, table_stride, layers=1, dtype=torch.bfloat16,
-                 window=None, params=None, async_compress=False, layer_stride=None, device="cuda"):
+                 window=None, params=None, async_compress=False, layer_stride=None, device="cuda",
+                 decode_rho=True):
         self.h_q, self.h_kv, self.d, self.b = h_q, h_kv, d, b
         self.n_total, self.N_max, self.stride, self.layers = n_total, max_blocks, table_stride, layers
         self.k = (max_blocks - 1) * b
@@ -47,6 +71,7 @@ class DecodeLoop:
         self.desc = cache_desc(h_q, h_kv, d, b, n_total, dtype)
         self.params = params or score_params(window=self.window)
         self.async_compress = async_compress
+        self.decode_rho = decode_rho
         # layers compressed per call (App. C.1's layer stride): bounds the
         # scoring scratch to layer_stride layers
         self.layer_stride = max(1, min(layer_stride or layers, layers))
@@ -62,6 +87,10 @@ class DecodeLoop:
         self.B = 0
         self.compressions = 0
         self.pending = []  # (event, seqs, plan) of compressions in flight
+        # buffers of the decode's row sums: reused once the compression that
+        # read them has completed, so that no step allocates device or pinned
+        # memory while the host runs ahead of the GPU
+        self._rho_ring = []
 
     # ------------------------------------------------------------------ setup
     def add_sequences(self, lens, tables=None, max_blocks=None):
@@ -81,6 +110,7 @@ class DecodeLoop:
                 raise ValueError("max_blocks: one budget in [2, N_max] per sequence")
         self.uniform = bool((self.N_seq == self.N_max).all())
         self.B = B
+        self._rho_ring = []  # slot maps are [B]
         self.lens = lens.copy()
         self.table = np.full((B, self.stride), -1, dtype=np.int32)
         if tables is None:
@@ -108,8 +138,10 @@ class DecodeLoop:
                               device=self.dev)
         Lmax = self.stride * self.b
         self.Lmax = Lmax
-        self.score_ws = torch.empty(max(zp_compress_workspace_size(self.desc, B, Lmax, self.layer_stride), 1),
-                                    dtype=torch.uint8, device=self.dev)
+        self.use_rho = bool(self.decode_rho and zp_compress_rho_supported(self.desc, self.params, Lmax, self.k))
+        self.score_ws = None if self.use_rho else torch.empty(
+            max(zp_compress_workspace_size(self.desc, B, Lmax, self.layer_stride), 1), dtype=torch.uint8,
+            device=self.dev)
         self.out = torch.zeros(self.layers, B, self.h_q, self.d, dtype=self.dtype, device=self.dev)
 
     def layer_stride(self):
@@ -136,27 +168,56 @@ class DecodeLoop:
         self.table_dev.copy_(torch.from_numpy(self.table).pin_memory(), non_blocking=True)
         step_lens = upload(np.where(act, self.lens, 0).astype(np.int32), self.dev)
         main = torch.cuda.current_stream(self.dev)
+        # the sequences that compress after this step: their decode also forms
+        # the lightning row sums (row i of rho for the i-th of them)
+        trig = zp_needs_compression_batch(self.lens, self.b, self.N_max, active=act, max_blocks_seq=self.N_seq)
+        rho, buf, extra = None, None, {}
+        if len(trig) and self.use_rho:
+            n, Lr = len(trig), int(self.lens[trig].max())
+            buf = self._rho_buffer(self.layers * n * self.h_kv * Lr)
+            slot = buf["host"].numpy()
+            slot[:] = -1
+            slot[trig] = np.arange(n, dtype=np.int32)
+            buf["rows"].copy_(buf["host"], non_blocking=True)
+            rho = buf["rho"][: self.layers * n * self.h_kv * Lr].view(self.layers, n, self.h_kv, Lr)
+            extra = dict(rho_rows=buf["rows"], rho_threshold=self.params.threshold)
         for l in range(self.layers):
             zp_append_kv(self.desc, k_new[l], v_new[l], self.K[l], self.V[l], self.table_dev, step_lens)
             zp_paged_decode_attn(self.desc, q[l], self.K[l], self.V[l], self.table_dev, step_lens, self.out[l],
-                                 score_accum=self.S[l], window=self.window, workspace=self.ws)
-        trig = zp_needs_compression_batch(self.lens, self.b, self.N_max, active=act, max_blocks_seq=self.N_seq)
+                                 score_accum=self.S[l], window=self.window, workspace=self.ws,
+                                 rho=None if rho is None else rho[l], **extra)
         if len(trig):
-            self._compress(trig, main)
+            done = self._compress(trig, main, rho)
+            if buf is not None:
+                buf["busy"] = done
         return trig.tolist()
 
-    def _compress(self, seqs, main):
+    def _rho_buffer(self, elems):
+        """A free buffer of at least `elems` floats, with its slot-map arrays
+        (device and pinned host int32 [B])."""
+        for e in self._rho_ring:
+            if e["rho"].numel() >= elems and (e["busy"] is None or e["busy"].query()):
+                e["busy"] = None
+                return e
+        e = dict(rho=torch.empty(elems + elems // 4, dtype=torch.float32, device=self.dev),
+                 rows=torch.empty(self.B, dtype=torch.int32, device=self.dev),
+                 host=torch.empty(self.B, dtype=torch.int32).pin_memory(), busy=None)
+        self._rho_ring.append(e)
+        return e
+
+    def _compress(self, seqs, main, rho=None):
         n = len(seqs)
         nb = (self.lens[seqs] // self.b).astype(np.int32)
         sub_tables = np.ascontiguousarray(self.table[seqs])
         plan = self.pool.plan_compaction_batch(sub_tables, nb, self.N_max,
                                                max_blocks_seq=None if self.uniform else self.N_seq[seqs])
-        k_seq = None if self.uniform else upload((self.N_seq[seqs] - 1) * self.b, self.dev)
-        tables_dev = upload(sub_tables, self.dev)
-        lens_dev = upload(self.lens[seqs].astype(np.int32), self.dev)
-        first_dev = upload(self.first[seqs], self.dev)
-        rows_dev = upload(seqs.astype(np.int32), self.dev)
-        targets_dev = upload(plan["targets"], self.dev)
+        parts = [sub_tables, self.lens[seqs].astype(np.int32), seqs.astype(np.int32), plan["targets"],
+                 self.first[seqs].astype(np.uint8)]
+        if not self.uniform:
+            parts.append(((self.N_seq[seqs] - 1) * self.b).astype(np.int32))
+        dev_parts = upload_packed(parts, self.dev)
+        tables_dev, lens_dev, rows_dev, targets_dev, first_dev = dev_parts[:5]
+        k_seq = None if self.uniform else dev_parts[5]
         ready = torch.cuda.Event()
         ready.record(main)
         with torch.cuda.stream(self.side):
@@ -166,17 +227,18 @@ class DecodeLoop:
                 l1 = min(l0 + self.layer_stride, self.layers)
                 zp_compress_layers(self.desc, self.params, self.K[l0:l1], self.V[l0:l1], tables_dev, lens_dev,
                                    first_dev, self.S[l0:l1], self.F[l0:l1], targets_dev, self.k, keep[l0:l1],
-                                   self.Lmax, rows=rows_dev, workspace=self.score_ws, k_seq=k_seq)
+                                   self.Lmax, rows=rows_dev, workspace=self.score_ws, k_seq=k_seq,
+                                   rho=None if rho is None else rho[l0:l1])
             done = torch.cuda.Event()
             done.record(self.side)
-        for t in (tables_dev, lens_dev, first_dev, targets_dev, rows_dev) + ((k_seq,) if k_seq is not None else ()):
-            t.record_stream(self.side)
+        tables_dev.record_stream(self.side)  # every part is a view of one device buffer
         self.active[seqs] = False
         self.last_keep = (seqs, keep)  # for inspection: [layers][n][h_kv][k]
         self.pending.append((done, seqs, plan, keep))
         self.compressions += n
         if not self.async_compress:
             main.wait_event(done)
+        return done
 
     def _retire(self, block=False):
         """Apply the compressions that have finished: new tables, lengths and

@@ -370,6 +370,11 @@ zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, v
  * + l*rho->layer_stride.  The workspace is not used (it may be NULL).  The
  * kernel is launched as a programmatic dependent of the kernel before it and
  * reads the score rows and rho only after that kernel has completed. */
+/* 1 when zp_compress_layers_rho accepts this cache, these switches, Lmax and k
+ * on the current device (the one-kernel path: bf16, b = 16, d 64 or 128,
+ * h_kv <= 16, similarity with the lightning redundancy, a row of Lmax scores
+ * and k ranks in shared memory), else 0.  No device work. */
+int32_t zp_compress_rho_supported(const zp_cache_desc *D, const zp_score_params *P, int32_t Lmax, int32_t k);
 zp_status zp_compress_layers_rho(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
                                  int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
                                  int32_t table_stride, const int32_t *seq_lens, const uint8_t *first_compression,

@@ -8,7 +8,9 @@ the new token, run decode with the window-score accumulation and apply the
 released.  Checked every step: attention outputs (tolerance), block tables,
 lengths and the free pool (exact); at every compression: keep sets (exact up
 to reported near-ties, after which the oracle adopts the GPU's choice so both
-states stay identical), the moved K/V rows (bit-exact) and F.
+states stay identical), the moved K/V rows (bit-exact) and F.  The loop runs
+with the lightning row sums formed by the decode (the default) and, in one
+case, formed by the compression itself.
 """
 import numpy as np
 import pytest
@@ -21,8 +23,9 @@ from tests.oracle_loop import OracleLoop
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("layers,async_compress", [(1, False), (2, False), (2, True)])
-def test_decode_loop_matches_oracle_loop(layers, async_compress):
+@pytest.mark.parametrize("layers,async_compress,decode_rho", [(1, False, True), (2, False, True), (2, True, True),
+                                                               (2, True, False)])
+def test_decode_loop_matches_oracle_loop(layers, async_compress, decode_rho):
     from compressed_paged_kv_zp_gb300.engine import DecodeLoop
     cfg = dict(h_q=16, h_kv=4, d=64, b=16, N_max=4, w=16, layers=layers, n_total=160)
     B, steps, stride = 6, 44, 12
@@ -30,8 +33,10 @@ def test_decode_loop_matches_oracle_loop(layers, async_compress):
     g = torch.Generator().manual_seed(123 + layers)
     lens0 = torch.randint(30, 70, (B,), generator=g).numpy().astype(np.int32)
     loop = DecodeLoop(cfg["h_q"], cfg["h_kv"], cfg["d"], cfg["b"], cfg["n_total"], cfg["N_max"], stride,
-                      layers=layers, dtype=torch.bfloat16, window=cfg["w"], async_compress=async_compress)
+                      layers=layers, dtype=torch.bfloat16, window=cfg["w"], async_compress=async_compress,
+                      decode_rho=decode_rho)
     loop.add_sequences(lens0)
+    assert loop.use_rho == decode_rho
     # synthetic prefill: random rows in every block the sequences hold
     loop.K.copy_(zp_inputs.normal(tuple(loop.K.shape), 7, "bf16").cuda())
     loop.V.copy_(zp_inputs.normal(tuple(loop.V.shape), 8, "bf16").cuda())
