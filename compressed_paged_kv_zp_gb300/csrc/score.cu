@@ -510,6 +510,17 @@ __host__ __device__ inline size_t fused_smem(int Lmax, int k, int b) {
     return (size_t)Lmax * 8 + (size_t)k * 16 + (size_t)((k + b - 1) / b) * 4 + (size_t)((Lmax + b - 1) / b) * 4 + 64;
 }
 
+// Whether the one-kernel finish (scores, selection, move per (kv head,
+// sequence, layer)) covers this cache, these switches, Lmax and k: its dynamic
+// shared memory and its static part (the select's state, the reductions) fit.
+inline bool fused_finish_fits(const zp_cache_desc *D, const zp_score_params *P, int Lmax, int k, size_t optin) {
+    const int row_vec = D->head_dim * elem_bytes(D->dtype) / 16;
+    const size_t static_bytes = sizeof(SelectShared) + 64 * sizeof(float) + 256;
+    return D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
+           D->h_kv <= 16 && P && P->use_similarity && P->lightning && 2 * row_vec <= kFsThreads * kFsVecPerThread &&
+           fused_smem(Lmax, k, D->block_size) + static_bytes <= optin;
+}
+
 // Block-wide combination of per-thread online-softmax pairs (max m, sum s of
 // 2^(y - m)): M = max m, S = sum s * 2^(m - M).  red: 64 floats.
 __device__ __forceinline__ float2 block_reduce_maxsum(float m, float s, float *red) {
@@ -1017,9 +1028,7 @@ static zp_status compress_impl(const zp_cache_desc *D, const zp_score_params *P,
     if (rc != ZP_OK) return rc;
     const int row_vec = (int)(row_bytes / 16);
     const size_t smem = fused_smem(Lmax, k, D->block_size);
-    const bool fused_ok = D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
-                          D->h_kv <= 16 && P && P->use_similarity && P->lightning &&
-                          2 * row_vec <= kFsThreads * kFsVecPerThread && smem <= (size_t)dev.smem_optin;
+    const bool fused_ok = fused_finish_fits(D, P, Lmax, k, (size_t)dev.smem_optin);
     if (rho && !fused_ok)
         return fail(ZP_ERR_SHAPE, "compress: given row sums need the one-kernel path (bf16, b = 16, lightning, "
                                   "%zu bytes of shared memory per row)", smem);
@@ -1104,10 +1113,7 @@ extern "C" int32_t zp_compress_rho_supported(const zp_cache_desc *D, const zp_sc
     if (check_desc(D) != ZP_OK || !P || Lmax < 0 || k < 0) return 0;
     DeviceInfo dev;
     if (device_info(&dev) != ZP_OK) return 0;
-    const int row_vec = D->head_dim * elem_bytes(D->dtype) / 16;
-    return D->dtype == ZP_BF16 && D->block_size == 16 && (D->head_dim == 64 || D->head_dim == 128) &&
-           D->h_kv <= 16 && P->use_similarity && P->lightning && 2 * row_vec <= kFsThreads * kFsVecPerThread &&
-           fused_smem(Lmax, k, D->block_size) <= (size_t)dev.smem_optin;
+    return fused_finish_fits(D, P, Lmax, k, (size_t)dev.smem_optin);
 }
 
 extern "C" zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base,
