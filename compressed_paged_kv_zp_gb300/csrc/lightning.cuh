@@ -11,13 +11,23 @@
 
 namespace zp {
 
-// One column `col` of a lane's fragment: its entries of rows g (va) and g + 8
-// (vb), the reciprocal norm of the column and of the two rows (0 for a
-// missing row or column, or a zero key).  Forms both cosines, then zeroes the
-// entry of the newest existing row whose cosine exceeds p; colmask selects the
-// eight lanes that hold this column (lanes tig + 4 g'), and the highest set
-// bit of a ballot over them, shifted right by two, is that row's index within
-// its half.
+// Token order of the fragments.  Natural: fragment row (and column) r is
+// token r.  Paired (PAIRED = true): the block's tokens were staged two rows
+// per copy and each 8-token operand tile holds every other token, so
+// fragment row r < 8 is token 2r and row r >= 8 is token 2 (r - 8) + 1.
+template <bool PAIRED>
+__device__ __forceinline__ int lightning_token(int r) {
+    return PAIRED ? (r < 8 ? 2 * r : 2 * (r - 8) + 1) : r;
+}
+
+// One column `col` (fragment index) of a lane's fragment: its entries of
+// fragment rows g (va) and g + 8 (vb), the reciprocal norm of the column and
+// of the two rows (0 for a missing row or column, or a zero key).  Forms both
+// cosines, then zeroes the entry of the newest existing token whose cosine
+// exceeds p; colmask selects the eight lanes that hold this column (lanes
+// tig + 4 g'), and the highest set bit of a ballot over them, shifted right
+// by two, is the fragment row g' within its half.
+template <bool PAIRED>
 __device__ __forceinline__ void lightning_column(float &va, float &vb, int col, float inv_c, float inv_a,
                                                  float inv_b, bool rva, bool rvb, int g, unsigned colmask, float p) {
     // a zero reciprocal norm masks the entry (stale rows past the block's
@@ -28,7 +38,13 @@ __device__ __forceinline__ void lightning_column(float &va, float &vb, int col, 
     // zero entries exceed it
     const unsigned blo = __ballot_sync(0xFFFFFFFFu, rva && va > p) & colmask;
     const unsigned bhi = __ballot_sync(0xFFFFFFFFu, rvb && vb > p) & colmask;
-    const int rstar = bhi ? 8 + ((31 - __clz(bhi)) >> 2) : (blo ? (31 - __clz(blo)) >> 2 : -1);
+    const int glo = blo ? (31 - __clz(blo)) >> 2 : -1;  // newest hit among fragment rows 0..7
+    const int ghi = bhi ? (31 - __clz(bhi)) >> 2 : -1;  // among rows 8..15
+    // natural order: rows 8..15 are the newer tokens; paired: row 8 + g' is
+    // token 2 g' + 1, newer than row g'' (token 2 g'') iff g' >= g''
+    int rstar;
+    if (PAIRED) rstar = (ghi >= 0 && ghi >= glo) ? 8 + ghi : glo;
+    else rstar = ghi >= 0 ? 8 + ghi : glo;
     if (rstar == g) va = 0.f;
     if (rstar == g + 8) vb = 0.f;
 }
@@ -39,18 +55,19 @@ __device__ __forceinline__ float lightning_inv_norm(float n_sq, bool exists) {
 }
 
 // Fragment layout (m16n8k16 accumulators, lane = 4 g + tig): c0[e] = G[g][2tig+e],
-// c0[2+e] = G[g+8][2tig+e], c1[e] = G[g][8+2tig+e], c1[2+e] = G[g+8][8+2tig+e].
+// c0[2+e] = G[g+8][2tig+e], c1[e] = G[g][8+2tig+e], c1[2+e] = G[g+8][8+2tig+e]
+// (fragment indices; lightning_token gives the tokens).
 //
-// The rule, on the rows and columns r, c < nvalid (the block's tokens that
-// exist):
+// The rule, on the tokens r, c < nvalid (the block's tokens that exist):
 //     C[r][c] = G[r][c] / (|k_r| |k_c|), 0 when either norm is 0
 //     C[c][c] = 0
-//     per column c: the largest r with C[r][c] > p loses its entry
+//     per column c: the largest (newest) r with C[r][c] > p loses its entry
 //     rho[r] = sum_c C[r][c]
 // The squared norms are the diagonal of G; C[r][c] is formed as
 // G[r][c] * (1/|k_r|) * (1/|k_c|) with the reciprocal square root.  Returns
-// (rho[g], rho[g + 8]), complete in every lane of the warp (whole warp must
-// call).
+// (rho of fragment row g, rho of fragment row g + 8), complete in every lane
+// of the warp (whole warp must call).
+template <bool PAIRED>
 __device__ __forceinline__ float2 lightning_rowsums(const float (&c0)[4], const float (&c1)[4], int nvalid, float p,
                                                     int lane) {
     const int g = lane >> 2, tig = lane & 3;
@@ -58,8 +75,9 @@ __device__ __forceinline__ float2 lightning_rowsums(const float (&c0)[4], const 
     // c1[2 + (r & 1)] for r >= 8.  Each lane turns its own diagonal candidate
     // into a reciprocal norm first, so the shuffles move finished values.
     const int c_lo = 2 * tig, c_hi = 8 + 2 * tig;
-    const float i0 = lightning_inv_norm((g & 1) ? c0[1] : c0[0], g < nvalid);
-    const float i1 = lightning_inv_norm((g & 1) ? c1[3] : c1[2], g + 8 < nvalid);
+    const bool rva = lightning_token<PAIRED>(g) < nvalid, rvb = lightning_token<PAIRED>(g + 8) < nvalid;
+    const float i0 = lightning_inv_norm((g & 1) ? c0[1] : c0[0], rva);
+    const float i1 = lightning_inv_norm((g & 1) ? c1[3] : c1[2], rvb);
     const int src_row = 4 * g + (g >> 1);
     const float inv_a = __shfl_sync(0xFFFFFFFFu, i0, src_row);  // row g
     const float inv_b = __shfl_sync(0xFFFFFFFFu, i1, src_row);  // row g + 8
@@ -67,14 +85,13 @@ __device__ __forceinline__ float2 lightning_rowsums(const float (&c0)[4], const 
     const float inv1 = __shfl_sync(0xFFFFFFFFu, i0, 9 * tig + 4);
     const float inv2 = __shfl_sync(0xFFFFFFFFu, i1, 9 * tig);  // column 8 + 2 tig
     const float inv3 = __shfl_sync(0xFFFFFFFFu, i1, 9 * tig + 4);
-    const bool rva = g < nvalid, rvb = g + 8 < nvalid;
     const unsigned colmask = 0x11111111u << tig;
     float a0 = c0[0], a1 = c0[1], a2 = c1[0], a3 = c1[1];  // row g
     float b0 = c0[2], b1 = c0[3], b2 = c1[2], b3 = c1[3];  // row g + 8
-    lightning_column(a0, b0, c_lo, inv0, inv_a, inv_b, rva, rvb, g, colmask, p);
-    lightning_column(a1, b1, c_lo + 1, inv1, inv_a, inv_b, rva, rvb, g, colmask, p);
-    lightning_column(a2, b2, c_hi, inv2, inv_a, inv_b, rva, rvb, g, colmask, p);
-    lightning_column(a3, b3, c_hi + 1, inv3, inv_a, inv_b, rva, rvb, g, colmask, p);
+    lightning_column<PAIRED>(a0, b0, c_lo, inv0, inv_a, inv_b, rva, rvb, g, colmask, p);
+    lightning_column<PAIRED>(a1, b1, c_lo + 1, inv1, inv_a, inv_b, rva, rvb, g, colmask, p);
+    lightning_column<PAIRED>(a2, b2, c_hi, inv2, inv_a, inv_b, rva, rvb, g, colmask, p);
+    lightning_column<PAIRED>(a3, b3, c_hi + 1, inv3, inv_a, inv_b, rva, rvb, g, colmask, p);
     float rs0 = a0 + a1 + a2 + a3;
     float rs1 = b0 + b1 + b2 + b3;
     rs0 += __shfl_xor_sync(0xFFFFFFFFu, rs0, 1);

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
     // rows >= nvalid hold zeros: every entry they touch is masked
-    const float2 rs = lightning_rowsums(c0, c1, nvalid, a.p, lane);
+    const float2 rs = lightning_rowsums<false>(c0, c1, nvalid, a.p, lane);
     const float rs0 = rs.x, rs1 = rs.y;
     if (tig == 0) {
         float *out = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax + tb0;
@@ -304,48 +304,47 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
     }
 }
 
-// Redundancy and global score of one 16-token block in one CTA (bf16 keys,
-// b = 16, the path zp_compress_layers takes).  grid (ceil(Lmax / 16), n), one
-// warp per kv head.  The block's token rows (all kv heads, contiguous in HBM)
-// come by one bulk copy each into shared memory rows padded by 16 bytes, so
-// the eight rows an ldmatrix reads fall on eight bank groups; while they are
-// in flight, the CTA computes the block's global score (Alg. 2, as
-// gather_global_kernel) from the score rows and F.  Then G = K K^T per head
-// on the tensor cores (16 mma.sync), and on the accumulator fragments the
-// lightning rule as in lightning_tc_kernel.
-// Lightning redundancy of one block for kv head `kvh` (one warp): the block's
-// token rows (all kv heads, row stride RS) are in shared memory; G = K K^T on
-// the tensor cores (16 mma.sync), then on the accumulator fragments: cosine
-// (zero-norm keys give 0), zero diagonal, per column the newest row above p
-// zeroed, row sums written to rho (lightning_rowsums).
+// Lightning redundancy of one block for kv head `kvh` (one warp).  The
+// block's token rows (all kv heads) are in shared memory as pairs: tokens 2j,
+// 2j + 1 at j * PS and j * PS + RB (RB = bytes of a row, PS = 2 RB + 16), the
+// layout the decode stages its units in.  G = K K^T on the tensor cores (16
+// mma.sync) with the same fragments as the decode's Gram -- the even tokens
+// as the first 8-row / 8-column tile, the odd tokens as the second -- then
+// the rule on the accumulator fragments (lightning_rowsums), row sums to rho.
 template <int D>
-__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int RS, int nvalid,
+__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int PS, int nvalid,
                                                 int s, int tb0, int kvh, int lane) {
     const int h_kv = a.h_kv;
     constexpr int KS = D / 16;
     const int g = lane >> 2, tig = lane & 3;
     const int lm = lane >> 3;
-    const int lrow = (lm & 1) * 8 + (lane & 7);  // matrices: (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
-    const int lchunk = lm >> 1;
-    const uint32_t base = smem_u32(gsm) + (uint32_t)(lrow * RS + kvh * D * 2);
+    const int RB = h_kv * D * 2;
+    // matrices: (even tokens, chunk c) (odd tokens, c) (even, c + 1) (odd, c + 1)
+    const uint32_t base = smem_u32(gsm) + (uint32_t)((lane & 7) * PS + (lm & 1) * RB + (lm >> 1) * 16 + kvh * D * 2);
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < KS; ++t) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4(base + (uint32_t)((2 * t + lchunk) * 16), r0, r1, r2, r3);
+        ldsm_x4(base + (uint32_t)(32 * t), r0, r1, r2, r3);
         mma_16816(c0, r0, r1, r2, r3, r0, r2);
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
     // rows >= nvalid were not copied: every entry they touch is masked
-    const float2 rs = lightning_rowsums(c0, c1, nvalid, a.p, lane);
-    const float rs0 = rs.x, rs1 = rs.y;
-    if (tig == 0) {
+    const float2 rs = lightning_rowsums<true>(c0, c1, nvalid, a.p, lane);
+    if (tig == 0) {  // fragment rows g, g + 8 are tokens 2g, 2g + 1
         float *out = a.rho + ((size_t)s * h_kv + kvh) * a.Lmax + tb0;
-        if (g < nvalid) out[g] = rs0;
-        if (g + 8 < nvalid) out[g + 8] = rs1;
+        if (2 * g < nvalid) out[2 * g] = rs.x;
+        if (2 * g + 1 < nvalid) out[2 * g + 1] = rs.y;
     }
 }
 
+// Redundancy and global score of one 16-token block in one CTA (bf16 keys,
+// b = 16, the path zp_compress_layers takes).  grid (ceil(Lmax / 16), n), one
+// warp per kv head.  The block's token rows (all kv heads, contiguous in HBM)
+// come by one bulk copy per pair of rows into shared memory pairs padded by 16
+// bytes; while they are in flight, the CTA computes the block's global score
+// (Alg. 2, as gather_global_kernel) from the score rows and F.  Then the
+// lightning rule per head (lightning_block).
 template <int D>
 __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a0) {
     const ScoreArgs a = at_layer(a0, blockIdx.z);
@@ -361,7 +360,7 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     const int h_kv = a.h_kv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned row_bytes = (unsigned)(h_kv * D * 2);
-    const int RS = (int)row_bytes + 16;
+    const int PS = 2 * (int)row_bytes + 16;  // staged pair of rows
     if (tid == 0) {
         const int blk = a.table[(size_t)s * a.table_stride + bi];
         s_blk = blk;
@@ -373,7 +372,9 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
         } else {
             mbar_arrive_expect_tx(&bar, row_bytes * (unsigned)nvalid);
             const char *src = static_cast<const char *>(a.k) + (size_t)blk * 16 * row_bytes;
-            for (int t = 0; t < nvalid; ++t) bulk_g2s_plain(gsm + t * RS, src + (size_t)t * row_bytes, row_bytes, &bar);
+            for (int j = 0; 2 * j < nvalid; ++j)
+                bulk_g2s_plain(gsm + j * PS, src + (size_t)2 * j * row_bytes, (unsigned)min(2, nvalid - 2 * j) * row_bytes,
+                               &bar);
         }
     }
     __syncthreads();
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     // its output
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (s_abort) return;
-    lightning_block<D>(a, gsm, RS, nvalid, s, tb0, warp, lane);
+    lightning_block<D>(a, gsm, PS, nvalid, s, tb0, warp, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (g_on) {
         if (row < 0) {
@@ -886,7 +887,7 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     if (a.use_sim && P->lightning && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) &&
         a.h_kv <= 16 && reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
         // global score and redundancy of each block in one kernel
-        const size_t smem = (size_t)16 * (a.h_kv * a.d * 2 + 16);
+        const size_t smem = (size_t)8 * (2 * a.h_kv * a.d * 2 + 16);  // 8 pairs of token rows
         dim3 g2((Lmax + 15) / 16, n, layers);
         auto kern = a.d == 128 ? global_lightning_kernel<128> : global_lightning_kernel<64>;
         zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem,
