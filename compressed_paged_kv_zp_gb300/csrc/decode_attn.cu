@@ -726,12 +726,14 @@ constexpr int kTcTokens = 16;     // tokens per unit
 // unit of every CTA (grid + 1 long longs).
 constexpr int kEpiBar = 32, kEpiSLast = 40, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
 constexpr int kEpiCst = kEpiSeg + kMaxSeg * 16;
-constexpr int kTcPad = 16;        // bytes of padding after each staged pair of token rows
+constexpr int kTcPad = 16;        // bytes of padding after each staged group of token rows
 
-// Staged unit: K then V, each as kTcTokens / 2 pairs of token rows; a pair is
-// one bulk copy (two consecutive rows of the block) followed by 16 bytes of
-// pad.  Token t sits at (t / 2) * pair_stride + (t % 2) * row_bytes.
-__host__ __device__ inline int tc_pair_stride(int h_kv, int d) { return 2 * h_kv * d * 2 + kTcPad; }
+// Staged unit: K then V, each as kTcTokens / kStageRows groups of kStageRows
+// consecutive token rows of the block (one bulk copy each) followed by 16
+// bytes of pad.  Token t sits at (t / kStageRows) * group_stride +
+// (t % kStageRows) * row_bytes.
+__host__ __device__ inline int tc_group_stride(int h_kv, int d) { return kStageRows * h_kv * d * 2 + kTcPad; }
+constexpr int kTcGroups = kTcTokens / kStageRows;
 
 __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int halves, int B, int grid) {
     SmemLayout L;
@@ -742,7 +744,7 @@ __host__ __device__ inline SmemLayout make_tc_layout(int stages, int h_kv, int h
     off += 16;
     off = (off + 1023) / 1024 * 1024;
     L.stage_off = off;
-    off += stages * 2 * (kTcTokens / 2) * tc_pair_stride(h_kv, halves * 64);
+    off += stages * 2 * kTcGroups * tc_group_stride(h_kv, halves * 64);
     L.warp_off = off;
     L.merge_off = off;  // epilogue: see kEpi* offsets
     off += kEpiCst + (grid + 1) * 8;
@@ -1137,8 +1139,8 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int RB = h_kv * D * 2;                       // bytes of one token row (every kv head)
-    const int PS = tc_pair_stride(h_kv, D);            // staged pair stride
-    const int stage_bytes = 2 * (kTcTokens / 2) * PS;  // K pairs then V pairs
+    const int GS = tc_group_stride(h_kv, D);           // staged group stride
+    const int stage_bytes = 2 * kTcGroups * GS;        // K groups then V groups
     // Weighted stream-K split (row sums requested): the weighted prefix
     // wpre[0..B] and the per-sequence unit weights wgt[0..B) sit in the stage
     // area, which no copy writes before the split is done.
@@ -1299,14 +1301,14 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 mbar_arrive_expect_tx(&full[st], bad ? 0u : 2u * valid * row_bytes);
             }
             __syncwarp();
-            // lanes 0..7: K pairs, 8..15: V pairs; a pair is tokens 2j, 2j + 1
-            // (one row when the unit ends after 2j)
-            const int j = lane & 7;
-            const int nrows = min(2, valid - 2 * j);
-            if (!bad && lane < 16 && nrows > 0) {
-                const size_t off = ((size_t)blk * a.b + (tok0 % a.b) + 2 * j) * h_kv * D;
-                unsigned char *dst = stage_base + (size_t)st * stage_bytes + (lane >> 3) * (kTcTokens / 2) * PS + j * PS;
-                bulk_g2s(dst, (lane < 8 ? kg : vg) + off, (unsigned)nrows * row_bytes, &full[st], pol);
+            // lanes [0, kTcGroups): K groups, then V groups; group j holds
+            // tokens [j R, j R + R) (fewer when the unit ends inside it)
+            const int j = lane % kTcGroups;
+            const int nrows = min(kStageRows, valid - kStageRows * j);
+            if (!bad && lane < 2 * kTcGroups && nrows > 0) {
+                const size_t off = ((size_t)blk * a.b + (tok0 % a.b) + kStageRows * j) * h_kv * D;
+                unsigned char *dst = stage_base + (size_t)st * stage_bytes + (lane / kTcGroups) * kTcGroups * GS + j * GS;
+                bulk_g2s(dst, (lane < kTcGroups ? kg : vg) + off, (unsigned)nrows * row_bytes, &full[st], pol);
             }
         }
         return;
@@ -1318,12 +1320,12 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const int g = lane >> 2;    // fragment row group
     const int tig = lane & 3;   // thread in group
     const int h0 = kvh * G;
-    // ldmatrix address of this lane: matrix m = lane / 8 holds the even
-    // tokens (m < 2: 0, 2, .., 14) or the odd ones (m >= 2), 16-byte chunk
-    // +(m & 1); its row i = lane % 8 is token 2i (+1).  With the pair stride
-    // the eight rows fall on eight different bank groups.
+    // ldmatrix address of this lane: matrix m = lane / 8 is operand tile
+    // m / 2 (staged_token) at 16-byte chunk +(m & 1); its row i = lane % 8.
     const int lm = lane >> 3;
-    const uint32_t loff = (uint32_t)((lane & 7) * PS + (lm >> 1) * RB + (lm & 1) * 16);
+    const int li = lane & 7;
+    const uint32_t loff = (uint32_t)((li / (kStageRows / 2)) * GS +
+                                     (li % (kStageRows / 2) + (lm >> 1) * (kStageRows / 2)) * RB + (lm & 1) * 16);
 
     uint32_t qa[KS][2];
     float acc[KS][4];
@@ -1384,7 +1386,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         if (valid > kTcTokens) valid = kTcTokens;
         if (!got) valid = 0;
         unsigned char *ks = stage_base + (size_t)st * stage_bytes + kvh * D * 2;  // this head's columns
-        unsigned char *vs = ks + (kTcTokens / 2) * PS;
+        unsigned char *vs = ks + kTcGroups * GS;
         if (valid > 0) {
             if (valid < kTcTokens) {
                 // rows past the sequence end were not copied and hold stale
@@ -1392,7 +1394,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 // 0 * garbage cannot produce a NaN
                 for (int c = lane; c < (kTcTokens - valid) * (D / 8); c += 32) {
                     const int row = valid + c / (D / 8);
-                    reinterpret_cast<uint4 *>(vs + (row >> 1) * PS + (row & 1) * RB)[c % (D / 8)] =
+                    reinterpret_cast<uint4 *>(vs + (row / kStageRows) * GS + (row % kStageRows) * RB)[c % (D / 8)] =
                         make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();  // ordered before later bulk copies into this stage
@@ -1409,16 +1411,17 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                 mma_16816(sc0, qa[t][0], 0u, qa[t][1], 0u, b0, b1);
                 mma_16816(sc1, qa[t][0], 0u, qa[t][1], 0u, b2, b3);
             }
-            // the n-tiles hold the even and the odd tokens: lane holds
-            // S[head g][tokens 4tig, 4tig+2] (sc0) and [4tig+1, 4tig+3] (sc1).
-            // The k order of V^T P^T below is the same (even tokens, then
-            // odd), so P goes to it in these registers unchanged.
+            // the n-tiles are the two operand tiles: lane holds S[head g] of
+            // tile 0 rows 2tig, 2tig+1 (sc0) and tile 1 rows 2tig, 2tig+1
+            // (sc1).  The k order of V^T P^T below is the same (tile 0, then
+            // tile 1), so P goes to it in these registers unchanged.
             float x[4];
             x[0] = sc0[0] * a.qscale;
             x[1] = sc0[1] * a.qscale;
             x[2] = sc1[0] * a.qscale;
             x[3] = sc1[1] * a.qscale;
-            const int tk[4] = {4 * tig, 4 * tig + 2, 4 * tig + 1, 4 * tig + 3};
+            const int tk[4] = {staged_token(0, 2 * tig), staged_token(0, 2 * tig + 1), staged_token(1, 2 * tig),
+                               staged_token(1, 2 * tig + 1)};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (g >= G || tk[e] >= valid) x[e] = -INFINITY;
@@ -1462,9 +1465,9 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             if (rho_row >= 0) {
                 // A sequence about to be compressed: the unit is one block
                 // (b = 16), and the key fragments of Q K^T, loaded again, are
-                // both operands of its Gram K K^T (A = {b0, b2, b1, b3}: the
-                // even tokens, then the odd ones; B of the n-tile of even
-                // tokens = {b0, b1}, of odd tokens = {b2, b3}), in the
+                // both operands of its Gram K K^T (A = {b0, b2, b1, b3}: tile
+                // 0, then tile 1; B of tile 0 = {b0, b1}, of tile 1 = {b2,
+                // b3}), in the
                 // fragment order and k-step order of the compression's own
                 // Gram, so the lightning row sums carry the same bits.  K rows
                 // >= valid hold stale data: lightning_rowsums masks every
@@ -1478,10 +1481,11 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
                     mma_16816(g1, b0, b2, b1, b3, b2, b3);
                 }
                 const float2 rsum = lightning_rowsums<true>(g0, g1, valid, a.rho_p, lane);
-                if (tig == 0) {  // fragment rows g, g + 8 are tokens 2g, 2g + 1
+                if (tig == 0) {  // fragment rows g, g + 8: row g of tiles 0 and 1
                     float *ro = a.rho + ((size_t)rho_row * h_kv + kvh) * a.rho_stride + (u - prefix[s]) * kTcTokens;
-                    if (2 * g < valid) ro[2 * g] = rsum.x;
-                    if (2 * g + 1 < valid) ro[2 * g + 1] = rsum.y;
+                    const int t0 = staged_token(0, g), t1 = staged_token(1, g);
+                    if (t0 < valid) ro[t0] = rsum.x;
+                    if (t1 < valid) ro[t1] = rsum.y;
                 }
             }
         }
@@ -2021,7 +2025,7 @@ static zp_status decode_impl(const zp_cache_desc *D, const void *q, const void *
     // weighted split only while the weighted unit count fits in 32 bits and
     // its two arrays (2B + 1 ints) fit in the stage area
     const double max_units = (double)B * table_stride * D->block_size / 16.0;
-    const long long stage_area = (long long)p.stages * 2 * (kTcTokens / 2) * tc_pair_stride(D->h_kv, D->head_dim);
+    const long long stage_area = (long long)p.stages * 2 * kTcGroups * tc_group_stride(D->h_kv, D->head_dim);
     a.rho_weight8 = (rho && p.tc && max_units * kRhoUnitWeight8 < 2.0e9 && (2LL * B + 1) * 4 <= stage_area)
                         ? kRhoUnitWeight8 : 8;
     a.err = dev.error_word;

@@ -305,22 +305,25 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 }
 
 // Lightning redundancy of one block for kv head `kvh` (one warp).  The
-// block's token rows (all kv heads) are in shared memory as pairs: tokens 2j,
-// 2j + 1 at j * PS and j * PS + RB (RB = bytes of a row, PS = 2 RB + 16), the
-// layout the decode stages its units in.  G = K K^T on the tensor cores (16
-// mma.sync) with the same fragments as the decode's Gram -- the even tokens
-// as the first 8-row / 8-column tile, the odd tokens as the second -- then
-// the rule on the accumulator fragments (lightning_rowsums), row sums to rho.
+// block's token rows (all kv heads) are in shared memory in the decode's
+// staged layout (lightning.cuh: groups of kStageRows rows, group stride GS =
+// kStageRows RB + 16, RB = bytes of a row).  G = K K^T on the tensor cores
+// (16 mma.sync) with the same fragments as the decode's Gram -- operand tile
+// 0 as the first 8 rows / columns, tile 1 as the second -- then the rule on
+// the accumulator fragments (lightning_rowsums), row sums to rho.
 template <int D>
-__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int PS, int nvalid,
+__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int GS, int nvalid,
                                                 int s, int tb0, int kvh, int lane) {
     const int h_kv = a.h_kv;
     constexpr int KS = D / 16;
     const int g = lane >> 2, tig = lane & 3;
     const int lm = lane >> 3;
+    const int li = lane & 7;
     const int RB = h_kv * D * 2;
-    // matrices: (even tokens, chunk c) (odd tokens, c) (even, c + 1) (odd, c + 1)
-    const uint32_t base = smem_u32(gsm) + (uint32_t)((lane & 7) * PS + (lm & 1) * RB + (lm >> 1) * 16 + kvh * D * 2);
+    // matrices: (tile 0, chunk c) (tile 1, c) (tile 0, c + 1) (tile 1, c + 1)
+    const uint32_t base =
+        smem_u32(gsm) + (uint32_t)((li / (kStageRows / 2)) * GS + (li % (kStageRows / 2) + (lm & 1) * (kStageRows / 2)) * RB +
+                                   (lm >> 1) * 16 + kvh * D * 2);
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int t = 0; t < KS; ++t) {
@@ -331,10 +334,11 @@ __device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsign
     }
     // rows >= nvalid were not copied: every entry they touch is masked
     const float2 rs = lightning_rowsums<true>(c0, c1, nvalid, a.p, lane);
-    if (tig == 0) {  // fragment rows g, g + 8 are tokens 2g, 2g + 1
+    if (tig == 0) {  // fragment rows g, g + 8: row g of tiles 0 and 1
         float *out = a.rho + ((size_t)s * h_kv + kvh) * a.Lmax + tb0;
-        if (2 * g < nvalid) out[2 * g] = rs.x;
-        if (2 * g + 1 < nvalid) out[2 * g + 1] = rs.y;
+        const int t0 = staged_token(0, g), t1 = staged_token(1, g);
+        if (t0 < nvalid) out[t0] = rs.x;
+        if (t1 < nvalid) out[t1] = rs.y;
     }
 }
 
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     const int h_kv = a.h_kv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned row_bytes = (unsigned)(h_kv * D * 2);
-    const int PS = 2 * (int)row_bytes + 16;  // staged pair of rows
+    const int GS = kStageRows * (int)row_bytes + 16;  // staged group of rows
     if (tid == 0) {
         const int blk = a.table[(size_t)s * a.table_stride + bi];
         s_blk = blk;
@@ -372,9 +376,9 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
         } else {
             mbar_arrive_expect_tx(&bar, row_bytes * (unsigned)nvalid);
             const char *src = static_cast<const char *>(a.k) + (size_t)blk * 16 * row_bytes;
-            for (int j = 0; 2 * j < nvalid; ++j)
-                bulk_g2s_plain(gsm + j * PS, src + (size_t)2 * j * row_bytes, (unsigned)min(2, nvalid - 2 * j) * row_bytes,
-                               &bar);
+            for (int j = 0; kStageRows * j < nvalid; ++j)
+                bulk_g2s_plain(gsm + j * GS, src + (size_t)kStageRows * j * row_bytes,
+                               (unsigned)min(kStageRows, nvalid - kStageRows * j) * row_bytes, &bar);
         }
     }
     __syncthreads();
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     // its output
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (s_abort) return;
-    lightning_block<D>(a, gsm, PS, nvalid, s, tb0, warp, lane);
+    lightning_block<D>(a, gsm, GS, nvalid, s, tb0, warp, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (g_on) {
         if (row < 0) {
@@ -887,7 +891,7 @@ static zp_status launch_scores(const zp_cache_desc *D, const zp_score_params *P,
     if (a.use_sim && P->lightning && D->dtype == ZP_BF16 && a.b == 16 && (a.d == 64 || a.d == 128) &&
         a.h_kv <= 16 && reinterpret_cast<uintptr_t>(k_cache) % 16 == 0) {
         // global score and redundancy of each block in one kernel
-        const size_t smem = (size_t)8 * (2 * a.h_kv * a.d * 2 + 16);  // 8 pairs of token rows
+        const size_t smem = (size_t)(16 / kStageRows) * (kStageRows * a.h_kv * a.d * 2 + 16);  // staged groups
         dim3 g2((Lmax + 15) / 16, n, layers);
         auto kern = a.d == 128 ? global_lightning_kernel<128> : global_lightning_kernel<64>;
         zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem,
