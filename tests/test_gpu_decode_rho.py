@@ -219,3 +219,51 @@ def test_rho_paths_refuse_what_they_do_not_cover(zp):
         zp.zp_compress_layers(descb, zp.score_params(window=16, lightning=False), dcb.K[0], dcb.V[0], dcb.table,
                               dcb.lens, first, S, F, tg, 16, keep, 48, rho=torch.zeros(B, 8, 64, device="cuda"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("B,h_q,h_kv,d,lo,hi,every", [
+    (300, 32, 8, 128, 17, 300, 1),   # every sequence forms row sums: several 32-wide scan rounds
+    (2500, 4, 1, 64, 3, 40, 3),      # the split's arrays do not fit the stage area: unweighted split
+])
+def test_decode_rho_many_sequences(zp, B, h_q, h_kv, d, lo, hi, every):
+    """Row sums for many sequences at once: the decode's outputs stay those of
+    the plain decode (rounding) and every row equals the compression's own
+    kernel; sampled rows against the oracle."""
+    b, w = 16, 16
+    g = torch.Generator().manual_seed(4500 + B)
+    lens = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    c = zp_inputs.make_paged_case(4500 + B, B, h_q, h_kv, d, b, lens=lens, dtype="bf16")
+    zp_inputs.plant_duplicates(c, 4501)
+    desc = _desc(zp, c)
+    table_stride = int(c.block_table.shape[1])
+    chosen = list(range(0, B, every))
+    slot = np.full(B, -1, np.int32)
+    slot[chosen] = np.arange(len(chosen), dtype=np.int32)
+    rows = torch.from_numpy(slot).cuda()
+    stride = max(lens)
+    res = {}
+    for mode in ("plain", "rho"):
+        dc = DeviceCase(c)
+        out = torch.empty(B, h_q, d, dtype=torch.bfloat16, device="cuda")
+        S = torch.zeros(B, h_kv, table_stride * b, device="cuda")
+        rho = torch.full((len(chosen), h_kv, stride), -9.0, device="cuda")
+        extra = dict(rho=rho, rho_rows=rows, rho_threshold=0.5) if mode == "rho" else {}
+        zp.zp_paged_decode_attn(desc, dc.q, dc.K[0], dc.V[0], dc.table, dc.lens, out, S, w, **extra)
+        torch.cuda.synchronize()
+        assert zp.zp_device_status() == (0, 0)
+        res[mode] = (out.cpu(), S.cpu(), rho.cpu().numpy())
+    torch.testing.assert_close(res["rho"][0].float(), res["plain"][0].float(), atol=1e-2, rtol=1e-2)
+    torch.testing.assert_close(res["rho"][1], res["plain"][1], atol=1e-9, rtol=1e-5)
+    rho = res["rho"][2]
+    sub = torch.tensor(chosen, dtype=torch.long, device="cuda")
+    dc = DeviceCase(c)
+    ref_gpu = _score_tokens_rho(zp, desc, dc.K[0], dc.table[sub].contiguous(), dc.lens[sub].contiguous(), 0.5)
+    K0 = c.k_cache[0].float().numpy()
+    for j, s in enumerate(chosen):
+        L = lens[s]
+        assert np.array_equal(rho[j, :, :L], ref_gpu[j, :, :L]), s
+    for j in range(0, len(chosen), max(1, len(chosen) // 12)):
+        s, L = chosen[j], lens[chosen[j]]
+        for h in range(h_kv):
+            want = oracle.redundancy_rho(_keys(K0, c.block_table[s].numpy(), L, h), b, 0.5, True)
+            np.testing.assert_allclose(rho[j, h, :L], want, **RHO_TOL)
