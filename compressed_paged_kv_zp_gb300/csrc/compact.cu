@@ -125,18 +125,20 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
     }
 }
 
-// Main variant.  The CTA first resolves, in shared memory, every rank's keep
+// Main variant, one CTA per (tensor, kv head, sequence, layer): K and V are
+// independent, so each moves in a CTA of its own (twice the CTAs, half the
+// bytes each).  The CTA first resolves, in shared memory, every rank's keep
 // position, source block, F value and the target blocks (two rounds of
 // independent loads); then per chunk of up to kVChunk ranks every thread loads
-// its share of the chunk's row pieces (16-byte vectors, K then V of this kv
-// head) into registers, the CTA synchronises, and the pieces are stored to
-// the target slots.  A chunk reads positions >= its first rank and earlier
+// its share of the chunk's row pieces (16-byte vectors of this kv head's row
+// in its tensor) into registers, the CTA synchronises, and the pieces are
+// stored to the target slots; the K CTA also writes F.  A chunk reads positions >= its first rank and earlier
 // chunks write slots below it, and a slot shared by a source and a target has
 // the same index in both (the target rule): the move is correct in place.
 // (Many small bulk copies were measured slower: the copy engine keeps few
 // requests in flight per SM.)
-constexpr int kVChunk = 256;
-constexpr int kVThreads = 1024;  // rounds of 256 ranks for 256-byte row pieces (64 ranks with 256 threads
+constexpr int kVChunk = 512;
+constexpr int kVThreads = 1024;  // rounds of 512 ranks for 256-byte row pieces (64 ranks with 256 threads
                                  // took 4x the load-then-store round trips, each one a memory latency)
 constexpr int kVPerThread = 8;   // 16-byte registers per thread and chunk (row pieces up to 256 B)
 
@@ -148,7 +150,8 @@ __host__ __device__ inline size_t compact_meta_smem(int k, int b) {
 __global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const CompactArgs a) {
     extern __shared__ __align__(16) unsigned char csm[];
     __shared__ int s_L;
-    const int kvh = blockIdx.x;
+    const int kvh = blockIdx.x >> 1;
+    const int tensor = blockIdx.x & 1;  // 0: K (and F), 1: V
     const int s = blockIdx.y;
     const int layer = blockIdx.z;
     const int tid = threadIdx.x;
@@ -157,11 +160,8 @@ __global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const Compact
     float *f_s = reinterpret_cast<float *>(src_s + a.k);
     int *dst_s = reinterpret_cast<int *>(f_s + a.k);
     const int32_t *kp = a.keep + (((size_t)layer * a.n + s) * a.h_kv + kvh) * a.k;
-    const uint4 *K = a.K + layer * a.layer_stride_vec;
-    const uint4 *V = a.V + layer * a.layer_stride_vec;
-    uint4 *Kw = a.K + layer * a.layer_stride_vec;
-    uint4 *Vw = a.V + layer * a.layer_stride_vec;
-    float *F = a.F ? a.F + layer * a.F_layer_stride : nullptr;
+    uint4 *X = (tensor ? a.V : a.K) + layer * a.layer_stride_vec;  // this CTA's tensor
+    float *F = (a.F && tensor == 0) ? a.F + layer * a.F_layer_stride : nullptr;
     const int nt = (a.k + a.b - 1) / a.b;
     // ---- first loads: length, keep positions, target blocks (independent)
     if (tid == 0) {
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const Compact
         if (F) f_s[r] = (blk >= 0) ? Srow[pos] : 0.f;
     }
     __syncthreads();
-    const int per_rank = 2 * a.row_vec;  // K then V vectors
+    const int per_rank = a.row_vec;  // vectors of this kv head's row piece in the tensor
     const int chunk = min(kVChunk, kVThreads * kVPerThread / per_rank);
     for (int r0 = 0; r0 < kk; r0 += chunk) {
         const int nr = min(chunk, kk - r0);
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const Compact
                 const int blk = src_s[r];
                 if (blk >= 0) {
                     const size_t row = ((size_t)blk * a.b + pos_s[r] % a.b) * a.h_kv + kvh;
-                    buf[i] = (v < a.row_vec ? K : V)[row * a.row_vec + (v % a.row_vec)];
+                    buf[i] = X[row * a.row_vec + v];
                 }
             }
         }
@@ -224,10 +224,10 @@ __global__ void __launch_bounds__(kVThreads, 1) compact_vec_kernel(const Compact
                 const int r = r0 + it / per_rank, v = it % per_rank;
                 const int blk = dst_s[r / a.b];
                 if (blk < 0 || blk >= a.n_total) {
-                    record_error(a.err, ZP_ERR_DEVICE, 0x401);
+                    if (tensor == 0) record_error(a.err, ZP_ERR_DEVICE, 0x401);
                 } else if (src_s[r] >= 0) {
                     const size_t row = ((size_t)blk * a.b + r % a.b) * a.h_kv + kvh;
-                    (v < a.row_vec ? Kw : Vw)[row * a.row_vec + (v % a.row_vec)] = buf[i];
+                    X[row * a.row_vec + v] = buf[i];
                 }
             }
         }
@@ -305,14 +305,15 @@ extern "C" zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void
     a.row_vec = row_vec;
     a.chunk = chunk;
     a.err = dev.error_word;
-    dim3 grid(D->h_kv, n, layer_count);
     const int meta_smem = (int)compact_meta_smem(k, D->block_size);
-    if (2 * row_vec <= kVThreads * kVPerThread && meta_smem <= 96 * 1024) {
+    if (row_vec <= kVThreads * kVPerThread && meta_smem <= 96 * 1024) {
         zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(compact_vec_kernel), meta_smem,
                                             "compact: shared-memory attribute");
         if (rs != ZP_OK) return rs;
+        dim3 grid(2 * D->h_kv, n, layer_count);  // (tensor, kv head) fastest
         compact_vec_kernel<<<grid, kVThreads, meta_smem, static_cast<cudaStream_t>(stream)>>>(a);
     } else {
+        dim3 grid(D->h_kv, n, layer_count);
         compact_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     }
     cudaError_t e = cudaGetLastError();
