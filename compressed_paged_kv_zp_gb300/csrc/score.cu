@@ -310,13 +310,13 @@ __global__ void __launch_bounds__(512) lightning_tc_kernel(const ScoreArgs a) {
 // kStageRows RB + 16, RB = bytes of a row).  G = K K^T on the tensor cores
 // (16 mma.sync) with the same fragments as the decode's Gram -- operand tile
 // 0 as the first 8 rows / columns, tile 1 as the second -- then the rule on
-// the accumulator fragments (lightning_rowsums), row sums to rho.
+// the accumulator fragments (lightning_rowsums).  Returns the row sums of
+// fragment rows g and g + 8 (store_block_rho writes them).
 template <int D>
-__device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsigned char *gsm, int GS, int nvalid,
-                                                int s, int tb0, int kvh, int lane) {
+__device__ __forceinline__ float2 lightning_block(const ScoreArgs &a, const unsigned char *gsm, int GS, int nvalid,
+                                                  int kvh, int lane) {
     const int h_kv = a.h_kv;
     constexpr int KS = D / 16;
-    const int g = lane >> 2, tig = lane & 3;
     const int lm = lane >> 3;
     const int li = lane & 7;
     const int RB = h_kv * D * 2;
@@ -333,9 +333,16 @@ __device__ __forceinline__ void lightning_block(const ScoreArgs &a, const unsign
         mma_16816(c1, r0, r1, r2, r3, r1, r3);
     }
     // rows >= nvalid were not copied: every entry they touch is masked
-    const float2 rs = lightning_rowsums<true>(c0, c1, nvalid, a.p, lane);
-    if (tig == 0) {  // fragment rows g, g + 8: row g of tiles 0 and 1
-        float *out = a.rho + ((size_t)s * h_kv + kvh) * a.Lmax + tb0;
+    return lightning_rowsums<true>(c0, c1, nvalid, a.p, lane);
+}
+
+// Row sums of lightning_block to rho: fragment rows g, g + 8 are row g of
+// operand tiles 0 and 1.
+__device__ __forceinline__ void store_block_rho(const ScoreArgs &a, float2 rs, int nvalid, int s, int tb0, int kvh,
+                                                int lane) {
+    const int g = lane >> 2, tig = lane & 3;
+    if (tig == 0) {
+        float *out = a.rho + ((size_t)s * a.h_kv + kvh) * a.Lmax + tb0;
         const int t0 = staged_token(0, g), t1 = staged_token(1, g);
         if (t0 < nvalid) out[t0] = rs.x;
         if (t1 < nvalid) out[t1] = rs.y;
@@ -388,6 +395,10 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     // (the decode call, when it precedes), which writes the score rows but not
     // the lengths, the block table, the keys or F: everything but the score
     // rows is read, and the redundancy computed, before griddepcontrol.wait.
+    // Nothing is stored to global memory before the wait: the caller may have
+    // given this call memory that the preceding kernel still uses (a scratch
+    // buffer freed after that call was queued and handed out again, which
+    // stream order alone makes safe).
     // Global score (Alg. 2) of this thread's (kv head, token) of the block:
     // F read now, the score row after the wait.
     const int N = (L + a.b - 1) / a.b;
@@ -405,8 +416,9 @@ __global__ void __launch_bounds__(512) global_lightning_kernel(const ScoreArgs a
     // its output
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (s_abort) return;
-    lightning_block<D>(a, gsm, GS, nvalid, s, tb0, warp, lane);
+    const float2 rs = lightning_block<D>(a, gsm, GS, nvalid, warp, lane);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    store_block_rho(a, rs, nvalid, s, tb0, warp, lane);
     if (g_on) {
         if (row < 0) {
             record_error(a.err, ZP_ERR_DEVICE, 0x202);

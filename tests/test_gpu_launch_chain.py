@@ -32,7 +32,7 @@ def _setup():
     return c, comp
 
 
-def _run(zp, c, comp, K0, V0, F0, chained):
+def _run(zp, c, comp, K0, V0, F0, chained, shared_ws=False):
     dev = torch.device("cuda")
     k = (N_MAX - 1) * BS
     desc = zp.cache_desc(H_Q, H_KV, D, BS, c.n_total, torch.bfloat16)
@@ -51,12 +51,21 @@ def _run(zp, c, comp, K0, V0, F0, chained):
     keep = torch.empty(len(comp), H_KV, k, dtype=torch.int32, device=dev)
     Lmax = int(c_lens.max())
     params = zp.score_params(window=W)
-    zp.zp_paged_decode_attn(desc, q, K, V, table, lens, out, score_accum=S, window=W)
+    ws_dec = ws_comp = None
+    if shared_ws:
+        # one scratch buffer for both calls, which stream order makes legal:
+        # the compression may start while the decode drains and must not
+        # store into it before the decode has completed
+        n_ws = max(zp.zp_decode_workspace_size(desc, B, table.shape[1]),
+                   zp.zp_compress_workspace_size(desc, len(comp), Lmax, 1))
+        ws_dec = ws_comp = torch.zeros(n_ws, dtype=torch.uint8, device=dev)
+    zp.zp_paged_decode_attn(desc, q, K, V, table, lens, out, score_accum=S, window=W, workspace=ws_dec)
     S_after_decode = None
     if not chained:
         torch.cuda.synchronize()
         S_after_decode = S.clone()
-    zp.zp_compress_layers(desc, params, K, V, c_table, c_lens, first, S, F, targets, k, keep, Lmax, rows=rows)
+    zp.zp_compress_layers(desc, params, K, V, c_table, c_lens, first, S, F, targets, k, keep, Lmax, rows=rows,
+                          workspace=ws_comp)
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     return dict(out=out, S=S, K=K, V=V, F=F, keep=keep), S_after_decode, first
@@ -89,3 +98,19 @@ def test_decode_then_compression_without_sync_is_bit_exact():
         for h in range(H_KV):
             swaps += keep_sets_match(kp[h], oracle.topk_keep(sref[h], k)[0], sref[h], k, L)
     print("reported near-tie swaps:", swaps)
+
+
+def test_compression_sharing_the_decode_scratch_is_bit_exact():
+    """The compression handed the decode's own scratch buffer (reuse that stream
+    order allows) and chained without a synchronisation leaves the state of the
+    synchronised pair, bit for bit."""
+    import compressed_paged_kv_zp_gb300 as zp
+    c, comp = _setup()
+    K0 = c.k_cache[0].contiguous().cuda()
+    V0 = c.v_cache[0].contiguous().cuda()
+    F0 = (torch.rand(c.n_total, BS, H_KV, generator=torch.Generator().manual_seed(8)) * 1e-3).cuda()
+    ref, _, _ = _run(zp, c, comp, K0, V0, F0, chained=False)
+    for _ in range(8):
+        got, _, _ = _run(zp, c, comp, K0, V0, F0, chained=True, shared_ws=True)
+        for name in ref:
+            assert torch.equal(got[name], ref[name]), name
