@@ -42,9 +42,10 @@ constexpr int kMaxConsumerWarps = 16;
 constexpr int kStageBytesCap = 32768;  // per tensor and stage
 constexpr int kMaxB = 4096;
 // A unit whose block also gets its lightning row sums costs the consumer warps
-// about this much more than a plain one (eighths); the stream-K split weighs
-// such units accordingly so that the CTAs holding them do not finish last.
-constexpr int kRhoUnitWeight8 = 10;
+// about this much more than a plain one (sixteenths; per-CTA loop times of
+// the 64-sequence Qwen3-8B layer fit 1.15-1.18); the stream-K split weighs
+// such units accordingly so that the CTAs holding them finish with the rest.
+constexpr int kRhoUnitWeight16 = 19;
 
 struct DecodeArgs {
     const void *q;
@@ -83,7 +84,7 @@ struct DecodeArgs {
     const int32_t *rho_rows;  // [B]: row of each batch entry, -1 = none
     int n_rho_rows;
     float rho_p;              // similarity threshold p
-    int rho_weight8;          // stream-K weight of a unit with row sums, in eighths of a plain unit
+    int rho_weight16;         // stream-K weight of a unit with row sums, in sixteenths of a plain unit
     unsigned *err;
 };
 
@@ -1144,7 +1145,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     // Weighted stream-K split (row sums requested): the weighted prefix
     // wpre[0..B] and the per-sequence unit weights wgt[0..B) sit in the stage
     // area, which no copy writes before the split is done.
-    const bool weighted = a.rho && a.rho_weight8 != 8;
+    const bool weighted = a.rho && a.rho_weight16 != 16;
     int *wpre = reinterpret_cast<int *>(smem + lay.stage_off);
     int *wgt = wpre + (B + 1);
 
@@ -1160,7 +1161,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             L = maxL;
         }
         lens[s] = L;
-        if (weighted) wgt[s] = a.rho_rows[s] >= 0 ? a.rho_weight8 : 8;
+        if (weighted) wgt[s] = a.rho_rows[s] >= 0 ? a.rho_weight16 : 16;
     }
     if (tid == 0) {
         abort_flag[0] = 0;
@@ -1210,7 +1211,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         for (int s = tid; s <= B; s += blockDim.x) a.unit_prefix[s] = prefix[s];
     if (weighted) {
         // Stream-K over weighted units: a unit of a sequence with row sums
-        // weighs rho_weight8, a plain one 8.
+        // weighs rho_weight16, a plain one 16.
         const long long W = wpre[B];
         for (int c = tid; c <= (int)gridDim.x; c += blockDim.x) {
             const long long target = (long long)c * W / gridDim.x;
@@ -2026,8 +2027,8 @@ static zp_status decode_impl(const zp_cache_desc *D, const void *q, const void *
     // its two arrays (2B + 1 ints) fit in the stage area
     const double max_units = (double)B * table_stride * D->block_size / 16.0;
     const long long stage_area = (long long)p.stages * 2 * kTcGroups * tc_group_stride(D->h_kv, D->head_dim);
-    a.rho_weight8 = (rho && p.tc && max_units * kRhoUnitWeight8 < 2.0e9 && (2LL * B + 1) * 4 <= stage_area)
-                        ? kRhoUnitWeight8 : 8;
+    a.rho_weight16 = (rho && p.tc && max_units * kRhoUnitWeight16 < 2.0e9 && (2LL * B + 1) * 4 <= stage_area)
+                         ? kRhoUnitWeight16 : 16;
     a.err = dev.error_word;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = D->h_q / D->h_kv;
