@@ -725,7 +725,8 @@ constexpr int kTcTokens = 16;     // tokens per unit
 // the announcement: the control words read ahead), up to kMaxSeg window
 // segments {sequence, first token, end token, byte offset}, then the first
 // unit of every CTA (grid + 1 long longs).
-constexpr int kEpiBar = 32, kEpiSLast = 40, kEpiStats = 48, kEpiSeg = 48 + 64 * 8, kMaxSeg = 32;
+constexpr int kEpiStatsHeads = 64;  // q heads of one statistics slot; two slots (the two cut sequences)
+constexpr int kEpiBar = 32, kEpiSLast = 40, kEpiStats = 48, kEpiSeg = 48 + 2 * kEpiStatsHeads * 8, kMaxSeg = 32;
 constexpr int kEpiCst = kEpiSeg + kMaxSeg * 16;
 constexpr int kTcPad = 16;        // bytes of padding after each staged group of token rows
 
@@ -826,21 +827,27 @@ __device__ bool ctl_arrive(unsigned long long *w, int n_parts, unsigned long lon
     return false;
 }
 
-// Waits (bounded) for the publication of the sequence's part records.  The word
+// Waits (bounded) for the publication of the part records of up to two
+// sequences (w0, w1; nullptr: none), polling both words together.  A word
 // stays published after the call: the next call's first arrival counts a
-// published word as zero.  False on timeout.
-__device__ bool ctl_wait_published(const unsigned long long *w, unsigned *err) {
+// published word as zero.  Returns bit i set when word i is published (or
+// absent); a timeout records an error.
+__device__ unsigned ctl_wait_published2(const unsigned long long *w0, const unsigned long long *w1, unsigned *err) {
     const unsigned long long t0 = global_ns();
-    unsigned long long cur = *reinterpret_cast<const volatile unsigned long long *>(w);
-    while (!(ctl_valid(cur) && ((cur >> 15) & 1))) {
+    bool p0 = w0 == nullptr, p1 = w1 == nullptr;
+    while (true) {
+        const unsigned long long v0 = p0 ? 0ull : ld_volatile_u64(w0);
+        const unsigned long long v1 = p1 ? 0ull : ld_volatile_u64(w1);
+        p0 = p0 || (ctl_valid(v0) && ((v0 >> 15) & 1));
+        p1 = p1 || (ctl_valid(v1) && ((v1 >> 15) & 1));
+        if (p0 && p1) break;
         if (global_ns() - t0 > kWaitLimitNs) {
             record_error(err, ZP_ERR_TIMEOUT, 50);
-            return false;
+            break;
         }
         __nanosleep(32);
-        cur = *reinterpret_cast<const volatile unsigned long long *>(w);
     }
-    return true;
+    return (p0 ? 1u : 0u) | (p1 ? 2u : 0u);
 }
 
 // Merge of the partial records of the cut sequences this CTA finished last
@@ -1109,6 +1116,15 @@ __device__ void score_prefetched(const DecodeArgs &a, int s, int L, int tb, int 
         bulk_commit();
     }
 }
+
+// A sequence cut between CTAs, as one CTA of its parts sees it in the epilogue:
+// its tokens [tb, te) in this CTA, window segment kk, whether another CTA
+// publishes it (wait) and whether this CTA scores tokens of it (seg).
+struct CutSeq {
+    int sq, L, tb, te, kk;
+    long long pb;
+    bool seg, wait;
+};
 
 template <int D, int G>
 __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a) {
@@ -1634,12 +1650,49 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const int n_cut = mlist[4];  // this CTA's parts of cut sequences: mlist[5..6]; mlist[1 + i]: published by us
     bool waited_copies = false;
     unsigned ebar_phase = 0;
-    // Every sequence of the range, in two passes: first those that need no
-    // other CTA (whole sequences, and cut sequences this CTA published as the
-    // last arrival), then the cut sequences published by another CTA.  For a
-    // cut sequence this CTA computes the final statistics from the part
-    // records, scores its own tokens and combines its slice of the output.
-    for (int pass = 0; pass < 2; ++pass) {
+    float2 *sm_stats1 = sm_stats + kEpiStatsHeads;  // statistics of the second cut sequence
+    // The window score of this CTA's tokens [tb, te) of sequence sq (window
+    // segment kk when prefetched) with the statistics st; false on abort.
+    auto score_own = [&](int sq, int L, long long pb, int tb, int te, int kk, float2 *st) -> bool {
+        if (nseg >= 0) {
+            if (!waited_copies) {
+                waited_copies = true;
+                mbar_wait_bounded(ebar, 0, a.err, abort_flag, 61);  // every thread observes the copies
+            }
+            named_bar_sync(1, nthr);
+            if (abort_flag[0]) return false;
+            const int4 g = segs[kk];
+            const int n = te - tb, n16 = (n + 15) & ~15;
+            float *lg_s = reinterpret_cast<float *>(scratch + g.w);
+            float *sc_s = lg_s + (size_t)n16 * HQ;
+            if (h_kv == 8) score_prefetched<G, 8>(a, sq, L, tb, n, n16, lg_s, sc_s, st, tid, nthr);
+            else if (h_kv == 4) score_prefetched<G, 4>(a, sq, L, tb, n, n16, lg_s, sc_s, st, tid, nthr);
+            else if (h_kv == 2) score_prefetched<G, 2>(a, sq, L, tb, n, n16, lg_s, sc_s, st, tid, nthr);
+            else score_prefetched<G, 1>(a, sq, L, tb, n, n16, lg_s, sc_s, st, tid, nthr);
+        } else {
+            if (h_kv == 8)
+                score_segment<G, 8>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase, abort_flag, st,
+                                    tid, nthr);
+            else if (h_kv == 4)
+                score_segment<G, 4>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase, abort_flag, st,
+                                    tid, nthr);
+            else if (h_kv == 2)
+                score_segment<G, 2>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase, abort_flag, st,
+                                    tid, nthr);
+            else
+                score_segment<G, 1>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase, abort_flag, st,
+                                    tid, nthr);
+        }
+        return true;
+    };
+    // Whole sequences first (their statistics are this CTA's own), one at a
+    // time; then the cut sequences -- at most two, the first and the last of
+    // the range -- together: one bounded wait for the publication of those
+    // another CTA publishes, the final statistics from the part records and
+    // this CTA's slice of each output with the loads of both in flight (two
+    // halves of the threads), then the scores of this CTA's tokens of each.
+    int cut_kk0 = 0, cut_kk1 = 0;  // window segment index of the cut sequences
+    {
         int kseg = 0;  // index of the next window segment in segs
         for (int sq = s_first; sq <= s; ++sq) {
             if (abort_flag[0]) break;  // set before a barrier by a thread that gave up: uniform
@@ -1654,67 +1707,82 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             const int kk = kseg;
             if (has_seg) ++kseg;
             const bool whole = pb >= u0 && pe <= u1;
-            const int ci = (n_cut > 0 && mlist[5] == sq) ? 0 : ((n_cut > 1 && mlist[6] == sq) ? 1 : -1);
-            if (!whole && ci < 0) continue;  // (cannot happen: every cut part was announced)
-            if (whole && !has_seg) continue;
-            const bool last = !whole && mlist[1 + ci] == sq;
-            if (!a.want_score && !last) continue;  // without the score only the last arrival works
-            const bool need_wait = !whole && !last;
-            if (need_wait != (pass == 1)) continue;
-            if (need_wait) {
-                if (tid == 0) {
-                    mlist[3] = ctl_wait_published(a.ctl + sq, a.err) ? 1 : 0;
-                    fence_acq_rel_gpu();  // the part records are read after the publication
-                }
-                named_bar_sync(1, nthr);
-                const bool ok_flag = mlist[3] != 0;
-                named_bar_sync(1, nthr);
-                if (!ok_flag) continue;
+            if (!whole) {
+                if (n_cut > 0 && mlist[5] == sq) cut_kk0 = kk;
+                if (n_cut > 1 && mlist[6] == sq) cut_kk1 = kk;
+                continue;
             }
-            if (whole) {
-                for (int h = tid; h < HQ; h += nthr) {
-                    const float2 ml = __ldcg(&a.stats[(size_t)sq * HQ + h]);
-                    sm_stats[h] = make_float2(ml.x, ml.y > 0.f ? 1.f / ml.y : 0.f);
-                }
-            } else {
-                // the statistics for the score (threads below HQ) and this CTA's
-                // slice of the output (the others), their loads in flight together
-                const int t0 = has_seg && nthr - HQ >= 64 ? HQ : 0;
-                if (has_seg) part_stats(a, sq, prefix, cst, Gd, sm_stats, tid, t0 ? t0 : nthr);
-                merge_slice<D>(a, sq, prefix, cst, Gd, !a.want_score, tid, t0, nthr);
+            if (!has_seg) continue;
+            for (int h = tid; h < HQ; h += nthr) {
+                const float2 ml = __ldcg(&a.stats[(size_t)sq * HQ + h]);
+                sm_stats[h] = make_float2(ml.x, ml.y > 0.f ? 1.f / ml.y : 0.f);
             }
-            if (has_seg && nseg >= 0) {
-                if (!waited_copies) {
-                    waited_copies = true;
-                    mbar_wait_bounded(ebar, 0, a.err, abort_flag, 61);  // every thread observes the copies
-                }
-                named_bar_sync(1, nthr);
-                if (abort_flag[0]) break;
-                const int4 g = segs[kk];
-                const int n = te - tb, n16 = (n + 15) & ~15;
-                float *lg_s = reinterpret_cast<float *>(scratch + g.w);
-                float *sc_s = lg_s + (size_t)n16 * HQ;
-                if (h_kv == 8) score_prefetched<G, 8>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
-                else if (h_kv == 4) score_prefetched<G, 4>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
-                else if (h_kv == 2) score_prefetched<G, 2>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
-                else score_prefetched<G, 1>(a, sq, L, tb, n, n16, lg_s, sc_s, sm_stats, tid, nthr);
-            } else if (has_seg) {
-                if (h_kv == 8)
-                    score_segment<G, 8>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
-                                        abort_flag, sm_stats, tid, nthr);
-                else if (h_kv == 4)
-                    score_segment<G, 4>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
-                                        abort_flag, sm_stats, tid, nthr);
-                else if (h_kv == 2)
-                    score_segment<G, 2>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
-                                        abort_flag, sm_stats, tid, nthr);
-                else
-                    score_segment<G, 1>(a, sq, L, pb, tb, te, scratch, scratch_bytes, ebar, ebar_phase,
-                                        abort_flag, sm_stats, tid, nthr);
-            } else {
-                named_bar_sync(1, nthr);  // sm_stats complete
-            }
+            if (!score_own(sq, L, pb, tb, te, kk, sm_stats)) break;
             named_bar_sync(1, nthr);  // sm_stats reused by the next sequence
+        }
+    }
+    if (!abort_flag[0] && n_cut > 0) {
+        // cut sequence i of the range (mlist[5 + i]); wait: published by another CTA
+        auto cut_seq = [&](int i) -> CutSeq {
+            CutSeq c;
+            c.sq = mlist[5 + i];
+            const long long pb = prefix[c.sq], pe = prefix[c.sq + 1];
+            const long long ub = pb > u0 ? pb : u0, ue = pe < u1 ? pe : u1;
+            c.L = lens[c.sq];
+            c.pb = pb;
+            c.tb = (int)(ub - pb) * kTcTokens;
+            c.te = (int)(ue - pb) * kTcTokens;
+            if (c.te > c.L) c.te = c.L;
+            c.seg = compute_window(c.sq) && c.te > c.tb;
+            c.wait = mlist[1 + i] != c.sq;
+            c.kk = i ? cut_kk1 : cut_kk0;
+            return c;
+        };
+        CutSeq cs0 = cut_seq(0);
+        CutSeq cs1 = n_cut > 1 ? cut_seq(1) : cs0;
+        // without the score only the last arrival works
+        bool use0 = a.want_score || !cs0.wait;
+        bool use1 = n_cut > 1 && (a.want_score || !cs1.wait);
+        if (!use0) {
+            cs0 = cs1;
+            use0 = use1;
+            use1 = false;
+        }
+        const int nc = (use0 ? 1 : 0) + (use1 ? 1 : 0);
+        named_bar_sync(1, nthr);  // mlist[1..2] read by every thread before tid 0 reuses them
+        if (tid == 0) {
+            const bool w0 = nc > 0 && cs0.wait, w1 = nc > 1 && cs1.wait;
+            unsigned okm = 3u;
+            if (w0 || w1) {
+                okm = ctl_wait_published2(w0 ? a.ctl + cs0.sq : nullptr, w1 ? a.ctl + cs1.sq : nullptr, a.err);
+                fence_acq_rel_gpu();  // the part records are read after the publication
+            }
+            mlist[1] = okm & 1u;
+            mlist[2] = (okm >> 1) & 1u;
+        }
+        named_bar_sync(1, nthr);
+        const bool cok0 = mlist[1] != 0, cok1 = mlist[2] != 0;
+        // the statistics for the score (the first HQ threads of a group) and this
+        // CTA's slice of the output (the others); with two sequences and at
+        // least 128 threads each half of the threads takes one
+        const bool split = nc == 2 && nthr >= 128;
+        const int gsz = split ? nthr / 2 : nthr;
+        for (int r = 0; r < (split ? 1 : nc); ++r) {
+            const int j = split ? tid / gsz : r;
+            const int gt = split ? tid - j * gsz : tid;
+            const CutSeq c = j ? cs1 : cs0;
+            if (j ? cok1 : cok0) {
+                const int t0 = c.seg && gsz - HQ >= 64 ? HQ : 0;
+                if (c.seg) part_stats(a, c.sq, prefix, cst, Gd, j ? sm_stats1 : sm_stats, gt, t0 ? t0 : gsz);
+                merge_slice<D>(a, c.sq, prefix, cst, Gd, !a.want_score, gt, t0, gsz);
+            }
+        }
+        for (int j = 0; j < nc; ++j) {
+            if (abort_flag[0]) break;
+            const CutSeq c = j ? cs1 : cs0;
+            if (!(j ? cok1 : cok0) || !c.seg) continue;
+            if (!score_own(c.sq, c.L, c.pb, c.tb, c.te, c.kk, j ? sm_stats1 : sm_stats)) break;
+            named_bar_sync(1, nthr);
         }
     }
     if (nseg > 0 && !waited_copies && tid == 0) mbar_wait_bounded(ebar, 0, a.err, abort_flag, 62);
