@@ -863,11 +863,12 @@ __device__ __forceinline__ int part_slot(int c_lo, int j, long long p0, const lo
     return cst[c + 1] > cst[c] ? 2 * c + (p0 > cst[c] ? 1 : 0) : -1;
 }
 
-// Final (M, 1/L) of every head of cut sequence s from its part records, into
-// shared memory (one head per thread; the records are published).  Up to
-// eight records are loaded together, then combined.
+// Final statistics of every head of cut sequence s from its part records, as
+// c = M + log2 L into shared memory (one head per thread; the records are
+// published; +inf for an empty sum).  Up to eight records are loaded
+// together, then combined.
 __device__ void part_stats(const DecodeArgs &a, int s, const int *prefix, const long long *cst, int Gd,
-                           float2 *out, int ctid, int nthr) {
+                           float *out, int ctid, int nthr) {
     const int h_q = a.h_q;
     for (int h = ctid; h < h_q; h += nthr) {
         const long long p0 = prefix[s];
@@ -892,7 +893,7 @@ __device__ void part_stats(const DecodeArgs &a, int s, const int *prefix, const 
                 if (v[q].x != -INFINITY) Lsum += v[q].y * exp2f(v[q].x - Mn);
             M = Mn;
         }
-        out[h] = make_float2(M, Lsum > 0.f ? 1.f / Lsum : 0.f);
+        out[h] = Lsum > 0.f ? M + log2f(Lsum) : INFINITY;
     }
 }
 
@@ -978,66 +979,63 @@ __device__ void merge_slice(const DecodeArgs &a, int s, const int *prefix, const
     }
 }
 
-// Window score of n tokens whose logits (lg_s [n][HQ], log2 units) and
-// score pieces (sc_s [HKV][RSF], token t of kv head h at h * RSF + t) are in
+// Window score of n tokens whose logits (lg_s [n16][HQ], log2 units, n16 the
+// token count rounded up to 16) and score pieces (sc_s [HKV][RSF], token t of
+// kv head h at h * RSF + t; RSF a multiple of 4, sc_s 16-byte aligned) are in
 // shared memory; the pieces are updated in place:
 //     piece[t] (+)= (1/w) max_{h in group} 2^(logit_h(t) - M_h) / L_h,
 // written instead of added at the first window row and for the newest token
-// (tok0 + t == P).  nthr is a multiple of HKV, so each thread keeps one kv
-// head and its group's (M, 1/L) in registers; it takes UN tokens at a time so
-// that their shared-memory loads are in flight together.
+// (tok0 + t == P).  2^(x - M) / L = 2^(x - c) with c = M + log2 L (sm_c, one
+// per q head; +inf gives a zero score), so the max over the group is taken on
+// x - c and each (token, kv head) needs one exponential (the ISA's
+// approximate one).  nthr is a multiple of HKV, so each thread keeps one kv
+// head and its group's c in registers; it takes four consecutive tokens at a
+// time (their logits rows exist up to n16), so that the four rows' loads and
+// the pieces' one 16-byte load are in flight together.
 template <int G, int HKV>
 __device__ __forceinline__ void score_tokens_smem(const float *lg_s, float *sc_s, int RSF, int n, int tok0, int P,
-                                                  bool first_row, float inv_w, const float2 *sm_stats, int ctid,
+                                                  bool first_row, float inv_w, const float *sm_c, int ctid,
                                                   int nthr) {
     constexpr int HQ = G * HKV;
-    constexpr int UN = 1;
     const int kvh = ctid % HKV;
     const int TS = nthr / HKV;
-    // 2^(x - M) / L = 2^(x - c) with c = M + log2 L, so the max over the group
-    // is taken on x - c and needs one exp2 per (token, kv head); 1/L = 0 gives
-    // c = +inf and a zero score.
     float c[G];
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-        const float2 st = sm_stats[kvh * G + j];
-        c[j] = st.x - log2f(st.y);
-    }
+    for (int j = 0; j < G; ++j) c[j] = sm_c[kvh * G + j];
+    const float keep_old = first_row ? 0.f : 1.f;  // 0: the piece is written, not added to
     float *row = sc_s + kvh * RSF;
-    for (int t0 = ctid / HKV; t0 < n; t0 += UN * TS) {
-        float x[UN][G], old[UN];
+    for (int t4 = (ctid / HKV) * 4; t4 < n; t4 += 4 * TS) {
+        float x[4][G];
 #pragma unroll
-        for (int u = 0; u < UN; ++u) {
-            const int t = t0 + u * TS;
-            if (t < n) {
-                const float *lg = lg_s + (size_t)t * HQ + kvh * G;
-                if constexpr (G % 4 == 0) {
+        for (int u = 0; u < 4; ++u) {
+            const float *lg = lg_s + (size_t)(t4 + u) * HQ + kvh * G;
+            if constexpr (G % 4 == 0) {
 #pragma unroll
-                    for (int q4 = 0; q4 < G / 4; ++q4) {
-                        const float4 v = reinterpret_cast<const float4 *>(lg)[q4];
-                        x[u][4 * q4] = v.x;
-                        x[u][4 * q4 + 1] = v.y;
-                        x[u][4 * q4 + 2] = v.z;
-                        x[u][4 * q4 + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) x[u][j] = lg[j];
+                for (int q4 = 0; q4 < G / 4; ++q4) {
+                    const float4 v = reinterpret_cast<const float4 *>(lg)[q4];
+                    x[u][4 * q4] = v.x;
+                    x[u][4 * q4 + 1] = v.y;
+                    x[u][4 * q4 + 2] = v.z;
+                    x[u][4 * q4 + 3] = v.w;
                 }
-                old[u] = row[t];
+            } else {
+#pragma unroll
+                for (int j = 0; j < G; ++j) x[u][j] = lg[j];
             }
         }
+        const float4 old4 = *reinterpret_cast<const float4 *>(row + t4);
+        float o[4] = {old4.x, old4.y, old4.z, old4.w};
 #pragma unroll
-        for (int u = 0; u < UN; ++u) {
-            const int t = t0 + u * TS;
-            if (t < n) {
-                float e = -INFINITY;
+        for (int u = 0; u < 4; ++u) {
+            float e = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < G; ++j) e = fmaxf(e, x[u][j] - c[j]);
-                const float best = exp2f(e);
-                row[t] = (first_row || tok0 + t == P) ? best * inv_w : old[u] + best * inv_w;
-            }
+            for (int j = 0; j < G; ++j) e = fmaxf(e, x[u][j] - c[j]);
+            const int t = t4 + u;
+            const float k = tok0 + t == P ? 0.f : keep_old;
+            const float v = fmaf(ex2_approx(e), inv_w, o[u] * k);
+            o[u] = t < n ? v : o[u];
         }
+        *reinterpret_cast<float4 *>(row + t4) = make_float4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -1047,11 +1045,11 @@ __device__ __forceinline__ void score_tokens_smem(const float *lg_s, float *sc_s
 // CT tokens: the logits rows (contiguous) and the h_kv score-row pieces come
 // into shared memory by bulk copies, are combined there, and the score pieces
 // go back by bulk copies.  buf: shared memory of buf_bytes (16-aligned);
-// sm_stats: the sequence's (M_h, 1/L_h), filled by the caller.
+// sm_c: the sequence's c_h = M_h + log2 L_h, filled by the caller.
 template <int G, int HKV>
 __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, int tb, int te, unsigned char *buf,
                               int buf_bytes, uint64_t *bar, unsigned &bar_phase, volatile int *abort,
-                              float2 *sm_stats, int ctid, int nthr) {
+                              const float *sm_c, int ctid, int nthr) {
     constexpr int HQ = G * HKV;
     const int P = L - 1;
     const bool first_row = (P % a.b) == a.b - a.window;
@@ -1078,7 +1076,7 @@ __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, i
         }
         const bool got = mbar_wait_bounded(bar, bar_phase, a.err, abort, 60);
         bar_phase ^= 1u;
-        if (got) score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, c0, P, first_row, inv_w, sm_stats, ctid, nthr);
+        if (got) score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, c0, P, first_row, inv_w, sm_c, ctid, nthr);
         fence_proxy_async_smem();
         named_bar_sync(1, nthr);
         if (ctid == 0) {
@@ -1097,17 +1095,19 @@ __device__ void score_segment(const DecodeArgs &a, int s, int L, long long p0, i
 // Window score of a prefetched segment: tokens [tb, tb + n) of sequence s,
 // logits lg_s [n16][HQ] and the score pieces sc_s [HKV][n16 + 4] already in
 // shared memory; the pieces are updated there and written back by bulk
-// copies (committed, not waited for).  sm_stats holds (M_h, 1/L_h).
-template <int G, int HKV>
+// copies (committed, not waited for) by thread ctid 0.  sm_c holds
+// c_h = M_h + log2 L_h.  nthr threads (a multiple of HKV) take part; BAR is
+// the named barrier they share.
+template <int G, int HKV, int BAR = 1>
 __device__ void score_prefetched(const DecodeArgs &a, int s, int L, int tb, int n, int n16, const float *lg_s,
-                                 float *sc_s, const float2 *sm_stats, int ctid, int nthr) {
+                                 float *sc_s, const float *sm_c, int ctid, int nthr) {
     const int P = L - 1;
     const bool first_row = (P % a.b) == a.b - a.window;
     const float inv_w = 1.f / (float)a.window;
     const int RSF = n16 + 4;
-    score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, tb, P, first_row, inv_w, sm_stats, ctid, nthr);
+    score_tokens_smem<G, HKV>(lg_s, sc_s, RSF, n, tb, P, first_row, inv_w, sm_c, ctid, nthr);
     fence_proxy_async_smem();
-    named_bar_sync(1, nthr);
+    named_bar_sync_id<BAR>(nthr);
     if (ctid == 0) {
         float *srow0 = a.score + (size_t)score_row_of(a, s) * HKV * a.score_stride;
 #pragma unroll
@@ -1149,7 +1149,10 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     // sequences, [7] window segments (negative: not prefetched)
     int *mlist = reinterpret_cast<int *>(smem + lay.merge_off);
     uint64_t *ebar = reinterpret_cast<uint64_t *>(smem + lay.merge_off + kEpiBar);  // epilogue copies
-    float2 *sm_stats = reinterpret_cast<float2 *>(smem + lay.merge_off + kEpiStats);
+    // per q head c = M + log2 L of the sequence being scored (two slots); before
+    // the epilogue the same bytes hold the guessed control words
+    float *sm_c = reinterpret_cast<float *>(smem + lay.merge_off + kEpiStats);
+    unsigned long long *guess_words = reinterpret_cast<unsigned long long *>(smem + lay.merge_off + kEpiStats);
     int4 *segs = reinterpret_cast<int4 *>(smem + lay.merge_off + kEpiSeg);
     long long *cst = reinterpret_cast<long long *>(smem + lay.merge_off + kEpiCst);
     const int tid = threadIdx.x;
@@ -1393,7 +1396,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
         int s_last = s_first;
         while (u1 > prefix[s_last + 1]) ++s_last;
         if (lane == 0) *reinterpret_cast<int *>(smem + lay.merge_off + kEpiSLast) = s_last;
-        reinterpret_cast<unsigned long long *>(sm_stats)[lane] = ld_volatile_u64(a.ctl + (lane ? s_last : s_first));
+        guess_words[lane] = ld_volatile_u64(a.ctl + (lane ? s_last : s_first));
     }
 
     for (long long u = u0, i = 0; u < u1; ++u, ++i) {
@@ -1634,7 +1637,7 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             const int sc = mlist[5 + i];
             int c_lo, c_hi;
             const int n_parts = parts_of(prefix[sc], prefix[sc + 1], cst, Gd, &c_lo, &c_hi);
-            const unsigned long long *guess_w = reinterpret_cast<const unsigned long long *>(sm_stats);
+            const unsigned long long *guess_w = guess_words;
             const unsigned long long guess =
                 sc == s_first ? guess_w[0]
                               : (sc == *reinterpret_cast<const int *>(smem + lay.merge_off + kEpiSLast) ? guess_w[1] : 0ull);
@@ -1650,10 +1653,10 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
     const int n_cut = mlist[4];  // this CTA's parts of cut sequences: mlist[5..6]; mlist[1 + i]: published by us
     bool waited_copies = false;
     unsigned ebar_phase = 0;
-    float2 *sm_stats1 = sm_stats + kEpiStatsHeads;  // statistics of the second cut sequence
+    float *sm_c1 = sm_c + kEpiStatsHeads;  // statistics of the second cut sequence
     // The window score of this CTA's tokens [tb, te) of sequence sq (window
     // segment kk when prefetched) with the statistics st; false on abort.
-    auto score_own = [&](int sq, int L, long long pb, int tb, int te, int kk, float2 *st) -> bool {
+    auto score_own = [&](int sq, int L, long long pb, int tb, int te, int kk, const float *st) -> bool {
         if (nseg >= 0) {
             if (!waited_copies) {
                 waited_copies = true;
@@ -1715,10 +1718,10 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             if (!has_seg) continue;
             for (int h = tid; h < HQ; h += nthr) {
                 const float2 ml = __ldcg(&a.stats[(size_t)sq * HQ + h]);
-                sm_stats[h] = make_float2(ml.x, ml.y > 0.f ? 1.f / ml.y : 0.f);
+                sm_c[h] = ml.y > 0.f ? ml.x + log2f(ml.y) : INFINITY;
             }
-            if (!score_own(sq, L, pb, tb, te, kk, sm_stats)) break;
-            named_bar_sync(1, nthr);  // sm_stats reused by the next sequence
+            if (!score_own(sq, L, pb, tb, te, kk, sm_c)) break;
+            named_bar_sync(1, nthr);  // sm_c reused by the next sequence
         }
     }
     if (!abort_flag[0] && n_cut > 0) {
@@ -1773,20 +1776,49 @@ __global__ void __launch_bounds__(9 * 32, 1) decode_tc_kernel(const DecodeArgs a
             const CutSeq c = j ? cs1 : cs0;
             if (j ? cok1 : cok0) {
                 const int t0 = c.seg && gsz - HQ >= 64 ? HQ : 0;
-                if (c.seg) part_stats(a, c.sq, prefix, cst, Gd, j ? sm_stats1 : sm_stats, gt, t0 ? t0 : gsz);
+                if (c.seg) part_stats(a, c.sq, prefix, cst, Gd, j ? sm_c1 : sm_c, gt, t0 ? t0 : gsz);
                 merge_slice<D>(a, c.sq, prefix, cst, Gd, !a.want_score, gt, t0, gsz);
             }
         }
-        for (int j = 0; j < nc; ++j) {
-            if (abort_flag[0]) break;
-            const CutSeq c = j ? cs1 : cs0;
-            if (!(j ? cok1 : cok0) || !c.seg) continue;
-            if (!score_own(c.sq, c.L, c.pb, c.tb, c.te, c.kk, j ? sm_stats1 : sm_stats)) break;
-            named_bar_sync(1, nthr);
+        if (split && nseg >= 0 && cok0 && cok1 && cs0.seg && cs1.seg) {
+            // both segments prefetched: each half of the threads scores its own
+            // sequence's tokens (named barrier 2 + half)
+            if (!waited_copies) {
+                waited_copies = true;
+                mbar_wait_bounded(ebar, 0, a.err, abort_flag, 61);  // every thread observes the copies
+            }
+            named_bar_sync(1, nthr);  // both halves' statistics are in place
+            if (!abort_flag[0]) {
+                const int j = tid / gsz;
+                const CutSeq c = j ? cs1 : cs0;
+                const int4 g = segs[c.kk];
+                const int n = c.te - c.tb, n16 = (n + 15) & ~15;
+                const float *lg_s = reinterpret_cast<const float *>(scratch + g.w);
+                float *sc_s = reinterpret_cast<float *>(scratch + g.w) + (size_t)n16 * HQ;
+                const float *st = j ? sm_c1 : sm_c;
+                const int gt = tid - j * gsz;
+                if (h_kv == 8) {
+                    if (j) score_prefetched<G, 8, 3>(a, c.sq, c.L, c.tb, n, n16, lg_s, sc_s, st, gt, gsz);
+                    else score_prefetched<G, 8, 2>(a, c.sq, c.L, c.tb, n, n16, lg_s, sc_s, st, gt, gsz);
+                } else {
+                    if (j) score_prefetched<G, 4, 3>(a, c.sq, c.L, c.tb, n, n16, lg_s, sc_s, st, gt, gsz);
+                    else score_prefetched<G, 4, 2>(a, c.sq, c.L, c.tb, n, n16, lg_s, sc_s, st, gt, gsz);
+                }
+            }
+        } else {
+            for (int j = 0; j < nc; ++j) {
+                if (abort_flag[0]) break;
+                const CutSeq c = j ? cs1 : cs0;
+                if (!(j ? cok1 : cok0) || !c.seg) continue;
+                if (!score_own(c.sq, c.L, c.pb, c.tb, c.te, c.kk, j ? sm_c1 : sm_c)) break;
+                named_bar_sync(1, nthr);
+            }
         }
     }
     if (nseg > 0 && !waited_copies && tid == 0) mbar_wait_bounded(ebar, 0, a.err, abort_flag, 62);
-    if (tid == 0) bulk_wait_read_all();  // shared-memory sources read; the writes complete on their own
+    // shared-memory sources read (the score pieces' copies are issued by
+    // threads 0 and nthr / 2); the writes complete on their own
+    if (tid == 0 || tid == nthr / 2) bulk_wait_read_all();
 }
 
 // ===========================================================================

@@ -122,13 +122,6 @@ __device__ __forceinline__ int ws_len(const WsTcArgs &a, int s) {
     return L;
 }
 
-// 2^x by the PTX ISA's approximate base-2 exponential (ex2.approx.ftz.f32,
-// relative error ~2^-22; inputs below -126 give 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // Work item g -> (pass2, pair, chunk): the first lag*C items are pass 1 of
 // pairs 0..lag-1; then per pair j >= lag its C pass-1 items followed by the C

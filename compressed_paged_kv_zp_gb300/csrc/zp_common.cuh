@@ -61,6 +61,14 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     return *reinterpret_cast<float2 *>(&Dv);
 }
 
+// 2^x by the PTX ISA's approximate base-2 exponential (ex2.approx.ftz.f32,
+// relative error ~2^-22; inputs below -126 give 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -245,6 +253,11 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// the same with the barrier id a constant (so that only the ids used count)
+template <int ID>
+__device__ __forceinline__ void named_bar_sync_id(int threads) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(threads) : "memory");
 }
 
 // ---------------------------------------------------------------- misc
