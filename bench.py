@@ -89,7 +89,7 @@ def _traffic():
     try:
         text = open(prof).read()
         h = hashlib.sha1()
-        for f in ("decode_attn.cu", "zp_common.cuh"):
+        for f in ("decode_attn.cu", "zp_common.cuh", "lightning.cuh"):
             h.update(open(os.path.join(here, "compressed_paged_kv_zp_gb300", "csrc", f), "rb").read())
         vals = dict(line.split(": ", 1) for line in text.splitlines()
                     if line.startswith(("traffic_bytes_per_launch: ", "kernel_sources_sha1: ")))
