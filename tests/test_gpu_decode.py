@@ -295,3 +295,66 @@ def test_wait_that_runs_out_is_reported(zp):
     torch.cuda.synchronize()
     assert zp.zp_device_status() == (0, 0)
     _check_out(out.float().cpu().numpy(), c, dc.np_k(), dc.np_v(), [0])
+
+
+def _stale_scores(c, b, seed):
+    """A stale score row per sequence (device) and the oracle's paged copy."""
+    B, h_kv = c.seq_lens.shape[0], c.h_kv
+    stride = c.block_table.shape[1]
+    S0 = torch.rand(B, h_kv, stride * b, generator=torch.Generator().manual_seed(seed)) + 0.5
+    S_ref = np.zeros((c.n_total, b, h_kv))
+    for s in range(B):
+        L = int(c.seq_lens[s])
+        t = np.arange(L)
+        S_ref[c.block_table[s].numpy()[t // b], t % b] = S0[s, :, :L].numpy().astype(np.float64).T
+    return S0.cuda(), S_ref
+
+
+@pytest.mark.parametrize("h_q,h_kv,d", [(32, 8, 128), (16, 4, 128), (8, 2, 64), (4, 1, 64)])
+def test_window_score_step_with_two_cut_sequences_per_cta(zp, h_q, h_kv, d):
+    """One decode step with the window score on the tensor-core path, with
+    enough sequences that most CTAs hold the end of one sequence and the start
+    of the next (two cut sequences per CTA: their merges and scores run side by
+    side for h_kv >= 4, one after the other below) and one long sequence cut
+    across about fifteen CTAs.  S starts stale: each token's piece is added to
+    it, or written where the step is the first window row (App. C.2)."""
+    b, w = 16, 16
+    rng = np.random.default_rng(1234 + h_kv)
+    lens = [int(x) for x in rng.integers(60, 400, size=119)] + [3001]
+    lens[0], lens[7], lens[50] = 17, 161, 33  # L = 16 j + 1: the first window row (written)
+    c = zp_inputs.make_paged_case(90 + h_kv, len(lens), h_q, h_kv, d, b, lens=lens, dtype="bf16")
+    dc = DeviceCase(c)
+    S, S_ref = _stale_scores(c, b, 11 + h_kv)
+    got = _run_decode(zp, dc, score=S, window=w)
+    K, V = dc.np_k(), dc.np_v()
+    ref, probs = oracle.decode_attention(c.q.float().numpy(), K, V, c.block_table.numpy(), c.seq_lens.numpy(),
+                                         want_probs=True)
+    np.testing.assert_allclose(got, ref, **TOL_OUT["bf16"])
+    oracle.accumulate_window_score(probs, c.block_table.numpy(), c.seq_lens.numpy(), h_kv, b, w, S_ref)
+    Sg = S.cpu().numpy().astype(np.float64)
+    for s, L in enumerate(lens):
+        np.testing.assert_allclose(Sg[s, :, :L], gather_slots(S_ref, c.block_table[s].numpy(), L, b),
+                                   **TOL_SCORE["bf16"])
+
+
+def test_window_score_step_segments_beyond_the_prefetch_area(zp):
+    """A layer of ~9k-token sequences (about 1,400 scored tokens per CTA): a
+    CTA's logits rows no longer fit the stage area at once, so the window score
+    takes them in chunks (score_segment); outputs of every sequence, scores of
+    sampled ones against the oracle, S stale as above."""
+    b, w = 16, 16
+    c = zp_inputs.make_paged_case(1077, 24, 32, 8, 128, b, len_range=(8000, 10000), dtype="bf16")
+    dc = DeviceCase(c)
+    S, S_ref = _stale_scores(c, b, 17)
+    got = _run_decode(zp, dc, score=S, window=w)
+    seqs = [0, 5, 11, 16, 23]
+    K, V = dc.np_k(), dc.np_v()
+    _check_out(got, c, K, V, seqs)
+    _, probs = oracle.decode_attention(c.q.float().numpy()[seqs], K, V, c.block_table.numpy()[seqs],
+                                       c.seq_lens.numpy()[seqs], want_probs=True)
+    oracle.accumulate_window_score(probs, c.block_table.numpy()[seqs], c.seq_lens.numpy()[seqs], 8, b, w, S_ref)
+    Sg = S.cpu().numpy().astype(np.float64)
+    for s in seqs:
+        L = int(c.seq_lens[s])
+        np.testing.assert_allclose(Sg[s, :, :L], gather_slots(S_ref, c.block_table[s].numpy(), L, b),
+                                   **TOL_SCORE["bf16"])
