@@ -732,7 +732,7 @@ __global__ void __launch_bounds__(kFsThreads) finalize_select_move_kernel(const 
         if (m.tie && tid == 0) m.tie[(size_t)s * a.h_kv + kvh] = 0;
         __syncthreads();
     } else {
-        block_select_topk(fs, L, ki, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
+        block_select_topk<false>(fs, L, ki, kout, keep_s, m.tie ? m.tie + (size_t)s * a.h_kv + kvh : nullptr, a.err, sh);
     }
     // ---- move this kv head's kept rows (Alg. 4 with the target blocks).
     // Rank i: source row (block of its token, from the table row in shared

@@ -20,7 +20,7 @@ constexpr int kThreads = 1024;
 // the radix passes never go back to global memory.
 constexpr int kSmemRow = 32768;
 
-template <bool STAGED>
+template <bool STAGED, bool WARP_SCAN>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int h_kv, int Lmax,
                                                         const int32_t *seq_lens, int k, const int32_t *k_seq,
                                                         int32_t *keep, int32_t *tie_count, unsigned *err) {
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float *scores, int
         __syncthreads();
         sc = srow;
     }
-    block_select_topk(sc, L, ki, out, nullptr, tie_count ? tie_count + (size_t)s * h_kv + kvh : nullptr, err, sh);
+    block_select_topk<WARP_SCAN>(sc, L, ki, out, nullptr, tie_count ? tie_count + (size_t)s * h_kv + kvh : nullptr, err, sh);
 }
 
 }  // namespace
@@ -69,16 +69,17 @@ extern "C" zp_status zp_select_topk(const float *scores, int32_t h_kv, int32_t L
     if (rc != ZP_OK) return rc;
     dim3 grid(h_kv, n);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the final scan per warp once a thread would scan more than four keys
+    const bool warp_scan = (Lmax + kThreads - 1) / kThreads > 4;
     if (Lmax <= kSmemRow) {
         const size_t smem = (size_t)Lmax * 4;
-        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(topk_kernel<true>), smem,
-                                            "topk: shared-memory attribute");
+        auto kern = warp_scan ? topk_kernel<true, true> : topk_kernel<true, false>;
+        zp_status rs = set_max_dynamic_smem(reinterpret_cast<const void *>(kern), smem, "topk: shared-memory attribute");
         if (rs != ZP_OK) return rs;
-        topk_kernel<true><<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count,
-                                                        dev.error_word);
+        kern<<<grid, kThreads, smem, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count, dev.error_word);
     } else {
-        topk_kernel<false><<<grid, kThreads, 0, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx, tie_count,
-                                                      dev.error_word);
+        topk_kernel<false, true><<<grid, kThreads, 0, st>>>(scores, h_kv, Lmax, seq_lens, k, k_seq, keep_idx,
+                                                            tie_count, dev.error_word);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "topk: launch");
