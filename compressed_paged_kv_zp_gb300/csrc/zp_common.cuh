@@ -191,8 +191,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// all committed groups have completed (writes performed)
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -225,31 +223,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 16-byte asynchronous global -> shared copy (L2 only, with an L2 policy):
-// the destination may be any 16-byte aligned shared address, so a copy can
-// read global memory in order and still land in a swizzled layout.
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)),
-                 "l"(src), "l"(policy)
-                 : "memory");
-}
 
-// 16-byte asynchronous global -> shared copy, default policy; completion by
-// cp_async_commit / cp_async_wait.
-__device__ __forceinline__ void cp_async16_plain(void *dst_smem, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// waits until at most N of this thread's committed groups are still pending
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Arrive on `bar` once every cp.async this thread issued before has landed.
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -264,7 +238,5 @@ __device__ __forceinline__ void named_bar_sync_id(int threads) {
 __device__ __forceinline__ float warp_max_xor(float v, int mask) {
     return fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, mask));
 }
-
-__device__ __forceinline__ float ld_cg(const float *p) { return __ldcg(p); }
 
 }  // namespace zp
