@@ -488,6 +488,32 @@ def test_redundancy_rho_brute_force(orc, p):
     np.testing.assert_allclose(orc.redundancy(keys, 4, p, tau, 0), _softmax(want / (L * tau)), rtol=1e-12)
 
 
+@pytest.mark.parametrize("p", [-2.0, -1.5])
+def test_redundancy_rho_lightning_below_minus_one_closed_form(orc, p):
+    """Lightning row sums (App. C.5, same-block pairs of C.7) with p < -1:
+    every cosine, and every column's zeroed diagonal, exceeds p, so in each
+    column the newest row of the block loses its entry.  Per block -- the last
+    one partial -- the block's last row sums to 0 and every other row to its
+    cosines with the block's other tokens; a zero key adds nothing.  Taking
+    the diagonal out of the newest-row search, letting rows of another block
+    (or past the sequence's end) take part, or keeping the zeroed entry would
+    each change some row."""
+    rng = np.random.default_rng(44)
+    L, b, d = 27, 8, 5  # blocks of 8, 8, 8 and one of 3
+    keys = rng.standard_normal((L, d)).astype(np.float32)
+    keys[10] = 0.0
+    k = keys.astype(np.float64)
+    nrm = [float(np.sqrt(sum(x * x for x in k[r]))) for r in range(L)]
+    want = np.zeros(L)
+    for b0 in range(0, L, b):
+        blk = list(range(b0, min(L, b0 + b)))
+        for r in blk[:-1]:
+            for c in blk:
+                if c != r and nrm[r] > 0 and nrm[c] > 0:
+                    want[r] += sum(k[r, i] * k[c, i] for i in range(d)) / (nrm[r] * nrm[c])
+    np.testing.assert_allclose(orc.redundancy_rho(keys, b, p, 1), want, rtol=1e-12, atol=1e-12)
+
+
 def test_redundancy_zero_norm_key_has_no_similarity(orc):
     keys = np.array([[0, 0], [1, 0], [0, 1]], dtype=np.float32)
     R = orc.redundancy(keys, 4, 0.5, 1.0, 0)
