@@ -555,6 +555,16 @@ def test_combine_lambda_zero_and_window(orc):
     np.testing.assert_allclose(out2, S - 0.5 * R, rtol=1e-15)
 
 
+def test_combine_hand_worked_example(orc):
+    """Eq. (4) with the window of App. C.6, worked by hand: S - lambda R on the
+    first L - w tokens, +inf on the last w (binary fractions, so exact)."""
+    S = np.array([0.5, 0.25, 0.875, 0.125, 0.75])
+    R = np.array([0.25, 0.5, 0.125, 0.0625, 0.0625])
+    out = orc.combine_and_window(S, 2, 2.0, R)
+    np.testing.assert_array_equal(out[:3], [0.0, -0.75, 0.625])
+    assert np.all(np.isposinf(out[3:]))
+
+
 # --------------------------------------------------------------------------- top-k
 def _dominates(s, a, c):
     return s[a] > s[c] or (s[a] == s[c] and a > c)
