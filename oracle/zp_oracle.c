@@ -37,10 +37,14 @@
  *                                 orthogonal keys, lightning == full for L<=b)
  *   orc_redundancy_rho            pinned (closed forms for identical and
  *                                 orthogonal keys, pure-Python brute force,
- *                                 softmax of it == orc_redundancy)
+ *                                 softmax of it == orc_redundancy; lightning
+ *                                 row sums with p < -1 in closed form)
  *   orc_redundancy_rho_rows       pinned (equals orc_redundancy_rho row by
  *                                 row with planted near-duplicates; closed form)
- *   orc_combine_and_window        pinned (lambda=0, window = +inf)
+ *   orc_combine_and_window        pinned (lambda=0, window = +inf, a
+ *                                 hand-worked example with lambda=2; the
+ *                                 order global score, pooling, combination
+ *                                 worked by hand through the step pipeline)
  *   orc_topk_keep                 pinned (exhaustive subsets, Fig. 1 example)
  *   orc_compact_alg4              pinned (Fig. 1 layout, bitwise moves)
  *   orc_plan_targets              pinned (both cases of [Zipage §4.4], Fig. 1)

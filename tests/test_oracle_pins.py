@@ -722,6 +722,27 @@ def test_plan_shared_prefix_below_budget(orc):
     assert kept_own | set(plan["released"]) | set(plan["dropped_shared"]) == set(table.tolist())
 
 
+def test_final_scores_step_order_hand_worked(orc):
+    """One sequence, one kv head, b = 2, L = 6, a later compression that pools
+    (kernel 3, every compression), alpha 0.5, lambda 0.6, window 1 and
+    orthogonal keys (rho = 0, so R = 1/6 for every token).  In the pages'
+    order -- the global score (Alg. 2: max(alpha F, S) before the last block),
+    max pooling of it (eq. 3), S - lambda R (eq. 4), the window (C.6) -- the
+    scores are [0.3, 0.3, 0.2, 0.2, 0.5, +inf], worked by hand; pooling before
+    the global score would give 0.2 at token 1."""
+    b, L = 2, 6
+    S = np.array([[0.1, 0.2, 0.3, 0.1, 0.05, 0.6]])
+    F = np.zeros((3, b, 1))
+    F[0, 0, 0] = 0.8
+    keys = np.zeros((3, b, 1, 8), dtype=np.float32)  # [N_total][b][h_kv][d], one-hot
+    for t in range(L):
+        keys[t // b, t % b, 0, t] = 1.0
+    prm = pipeline.ScoreParams(window=1, alpha=0.5, lam=0.6, pool_kernel=3, pool_policy=2)
+    out = pipeline.final_scores(S, keys, F, np.arange(3), L, b, False, prm)
+    np.testing.assert_allclose(out[0, :5], [0.3, 0.3, 0.2, 0.2, 0.5], rtol=1e-12)
+    assert np.isposinf(out[0, 5])
+
+
 def test_pipeline_under_budget_keeps_everything(orc):
     """A sequence at or below the budget k evicts nothing (invariant)."""
     prm = pipeline.ScoreParams(window=2, pool_kernel=3)
