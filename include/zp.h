@@ -348,7 +348,10 @@ zp_status zp_compact_pages(const zp_cache_desc *D, void *k_base, void *v_base,
  * when zp_paged_decode_attn immediately precedes on the same stream, the
  * first kernel starts on the SMs the decode's finished CTAs leave and
  * computes the key redundancy while the decode drains.  Anything recorded
- * between the two calls (an event, a copy) only removes that overlap. */
+ * between the two calls (an event, a copy) only removes that overlap.  No
+ * kernel of the call stores to memory before that wait, so its workspace and
+ * outputs may be memory the preceding call has just released (the reuse a
+ * stream-ordered allocator makes). */
 size_t zp_compress_workspace_size(const zp_cache_desc *D, int32_t n, int32_t Lmax, int32_t layer_count);
 zp_status zp_compress_layers(const zp_cache_desc *D, const zp_score_params *P, void *k_base, void *v_base,
                              int64_t layer_stride, int32_t layer_count, const int32_t *block_table,
