@@ -6,28 +6,32 @@
 // and, on observation-window steps, the per-token window score of App. C.2
 // accumulated one decode step at a time (see zp_paged_decode_attn in zp.h).
 //
-// Design (HBM bound: ~4 flop per byte of K/V at a group of 4):
+// Design (HBM bound: ~4 flop per byte of K/V at a group of 4), common to both
+// paths:
 //   * Work unit = up to T tokens of one block of one sequence, all kv heads:
 //     in the [N_total][b][h_kv][d] layout these are T*h_kv*d contiguous
-//     elements, fetched with ONE 1-D bulk copy (TMA engine) per tensor into a
-//     shared-memory ring of S stages guarded by mbarriers.  K/V loads carry
-//     an L2 evict-first hint so the small scratch arrays stay resident.
+//     elements, fetched by 1-D bulk copies (TMA engine) into a shared-memory
+//     ring of S stages guarded by mbarriers.  K/V loads carry an L2
+//     evict-first hint so the small scratch arrays stay resident.
 //   * Stream-K split: the units of all sequences are concatenated and every
 //     CTA (one per SM, persistent) takes an equal contiguous range, so ragged
 //     lengths cannot unbalance the grid.  A sequence cut between CTAs leaves
-//     per-CTA partial (max, sum, accumulator) records; the CTA that finishes
-//     the sequence's last partial merges them (atomic arrival count, no wait).
-//   * Warp specialisation: one producer warp issues the copies; consumer warp
-//     w handles kv head w / WPH, so the GQA group of a kv head shares each
-//     K/V row read from shared memory.  In a warp, a half-warp covers one
-//     token row (16 lanes x d/16 dims, one 16-byte smem load for bf16 d=128)
-//     and the two halves take different tokens.  Dot products use the packed
-//     fp32x2 FMA; the 16-lane reduction is a butterfly reduce-scatter so each
-//     lane ends with one (token, head) logit.  Online softmax in base 2.
+//     per-CTA partial (max, sum, accumulator) records that are merged later.
+//   * Warp specialisation: one producer warp issues the copies, consumer
+//     warps do the products with an online softmax in base 2.
 //   * Score: on window steps the logits (already in log2 units) go to a
-//     scratch array; once every sequence's final max and sum are known, a
-//     second, fully parallel kernel turns them into probabilities, takes the
-//     max over the GQA group and adds 1/w of it to the paged score.
+//     scratch array; once a sequence's final max and sum are known they become
+//     probabilities, the max over the GQA group is taken and 1/w of it is
+//     added to (or at the first window row written into) the score row.
+// bf16 caches (decode_tc_kernel): 16-token units copied a pair of token rows
+// at a time, S = Q K^T and O^T += V^T P^T on the tensor cores (mma.sync), one
+// cooperative launch whose epilogue merges the cut sequences and forms the
+// window score (see the epilogue notes below), optionally with the lightning
+// row sums of the sequences about to be compressed.
+// fp32 caches (decode_main_kernel, small parity workloads): a half-warp per
+// token row, packed fp32x2 FMAs and a butterfly reduce-scatter, then two more
+// launches: decode_merge_kernel (one merger per cut sequence) and
+// decode_score_kernel (the window score).
 #include <math.h>
 
 #include <mutex>
